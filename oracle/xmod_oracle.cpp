@@ -1,0 +1,373 @@
+// CPU oracle for the X-MoD / MoD sparse-depth layer forward pass.
+//
+// TEST INFRASTRUCTURE ONLY. Only tests/, __graft_entry__.smoke() and the
+// cpu_baseline / reference legs of bench.py may load this library. The CUDA
+// library never includes, links or calls anything in this directory, and this
+// file includes nothing from the CUDA library.
+//
+// Everything is computed in double precision with plain loops, in the order the
+// method states its steps. Loops over independent rows or (sequence, head)
+// pairs are spread over OpenMP threads; that changes no arithmetic.
+//
+// Sources (page: "X-MoD: Practical Scaling Laws for Sparse-Depth Routing Beyond
+// Mixture-of-Depths", reading notes; page: "Mixture-of-Depths explained"):
+//   router            X-MoD notes, Eq. 8 (router logit plus token-choice bias, sigmoid gate);
+//                     MoD blog, "MoDLayer" listing (router = Linear(d, 1) + sigmoid)
+//   top-(T/K)         X-MoD notes, "MoD structural limit" section and Eq. 1 (top-1/K tokens);
+//                     MoD blog listing (topk over int(seq_len * capacity))
+//   gather            MoD blog listing (boolean-mask gather keeps position order)
+//   block             X-MoD notes, "backbone configuration" (GQA attention, standard FFN,
+//                     Table 4); textbook chapter on dense Transformers (SwiGLU: three d x d_ff
+//                     matrices, no bias); pre-norm RMSNorm before attention and before FFN
+//   gated residual    X-MoD notes, Eq. 6 (MoD) and Eq. 7 (X-MoD); skip path y = x
+//
+// Readings where the pages are silent (each also listed in the design notes):
+//   * the bias is passed already signed and is ADDED to the logit (Eq. 8 writes s - tau*b);
+//   * the gate r includes the bias, as Eq. 8 defines r;
+//   * selection ranks the logit s, not r = sigmoid(s) (same order in exact arithmetic);
+//     ties go to the lower position; -0.0 equals +0.0; a non-finite logit is an error;
+//   * n = floor(T / K) tokens are selected per sequence;
+//   * no positional encoding, natural-exp softmax with scale 1/sqrt(head_dim);
+//   * FFN input is h = x_sel + a (the ungated in-block residual);
+//   * dense layers: y = x + a + f for every token.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <numeric>
+#include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+extern "C" {
+
+typedef struct {
+  int B, T, d, hq, hkv, hd, F;
+  double eps;
+} oracle_dims;
+
+// Matrices are [out, in] row-major (the nn.Linear layout):
+//   wq [hq*hd, d], wk [hkv*hd, d], wv [hkv*hd, d], wo [d, hq*hd],
+//   wg [F, d], wu [F, d], wd [d, F]; w_r, g1, g2 are [d].
+typedef struct {
+  const double *w_r, *g1, *wq, *wk, *wv, *wo, *g2, *wg, *wu, *wd;
+  double varsigma;
+} oracle_layer_w;
+
+enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_NONFINITE = -5 };
+enum { ORACLE_GATE_XMOD = 0, ORACLE_GATE_MOD = 1 };
+enum { ORACLE_DENSE = 0, ORACLE_SPARSE = 1 };
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+// Round to the nearest bfloat16 value (8 significant bits), ties to even.
+// Used only to mirror a bf16 residual stream between layers.
+double oracle_round_bf16(double v) {
+  if (v == 0.0 || !std::isfinite(v)) return v;
+  int e;
+  std::frexp(v, &e);                      // v = m * 2^e, 0.5 <= |m| < 1
+  double ulp = std::ldexp(1.0, e - 8);    // 8 significant bits
+  return std::nearbyint(v / ulp) * ulp;   // default rounding mode: nearest-even
+}
+
+// Eq. 8: s_i = w_r . x_i + b_i, r_i = sigmoid(s_i).
+void oracle_router(int64_t rows, int d, const double* x, const double* w_r,
+                   const double* bias, double* s, double* r) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < rows; ++i) {
+    double acc = 0.0;
+    for (int j = 0; j < d; ++j) acc += w_r[j] * x[i * d + j];
+    if (bias) acc += bias[i];
+    s[i] = acc;
+    if (r) r[i] = 1.0 / (1.0 + std::exp(-acc));
+  }
+}
+
+// Per-sequence top-k: the k largest logits, ties to the lower position, returned
+// as ascending positions. Brute force: order all positions by (-s, position).
+int oracle_topk(int B, int T, int k, const double* s, int32_t* idx) {
+  if (B < 0 || T <= 0 || k <= 0 || k > T) return ORACLE_BAD_ARG;
+  for (int64_t i = 0; i < (int64_t)B * T; ++i)
+    if (!std::isfinite(s[i])) return ORACLE_NONFINITE;
+  for (int b = 0; b < B; ++b) {
+    const double* sb = s + (int64_t)b * T;
+    std::vector<int32_t> order(T);
+    std::iota(order.begin(), order.end(), 0);
+    std::sort(order.begin(), order.end(), [sb](int32_t p, int32_t q) {
+      if (sb[p] != sb[q]) return sb[p] > sb[q];
+      return p < q;
+    });
+    std::sort(order.begin(), order.begin() + k);
+    for (int j = 0; j < k; ++j) idx[(int64_t)b * k + j] = order[j];
+  }
+  return ORACLE_OK;
+}
+
+// RMSNorm: out = x / sqrt(mean(x^2) + eps) * gamma.
+void oracle_rmsnorm(int64_t rows, int d, const double* x, const double* gamma,
+                    double eps, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < rows; ++i) {
+    double ss = 0.0;
+    for (int j = 0; j < d; ++j) ss += x[i * d + j] * x[i * d + j];
+    double inv = 1.0 / std::sqrt(ss / d + eps);
+    for (int j = 0; j < d; ++j) out[i * d + j] = x[i * d + j] * inv * gamma[j];
+  }
+}
+
+// y[rows, out] = x[rows, in] . W[out, in]^T
+void oracle_linear(int64_t rows, int in, int out, const double* x, const double* W,
+                   double* y) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < rows; ++i) {
+    for (int o = 0; o < out; ++o) {
+      double acc = 0.0;
+      for (int j = 0; j < in; ++j) acc += x[i * in + j] * W[(int64_t)o * in + j];
+      y[i * out + o] = acc;
+    }
+  }
+}
+
+// Causal grouped-query attention over one sequence of n tokens.
+// q [n, hq*hd], k and v [n, hkv*hd]; query head h reads KV head h / (hq/hkv).
+// o[i, h] = sum_{j<=i} softmax_j(q_i.k_j / sqrt(hd)) v_j.
+// Only the rows listed in `rows` (nrows of them) are computed; rows == NULL means all.
+void oracle_attention_rows(int n, int hq, int hkv, int hd, const double* q,
+                           const double* k, const double* v, double* o,
+                           const int32_t* rows, int nrows) {
+  const int G = hq / hkv;
+  const double scale = 1.0 / std::sqrt((double)hd);
+  const int nr = rows ? nrows : n;
+  const int qs = hq * hd, ks = hkv * hd;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+  for (int ri = 0; ri < nr; ++ri) {
+    for (int h = 0; h < hq; ++h) {
+      const int i = rows ? rows[ri] : ri;
+      const int g = h / G;
+      std::vector<double> sc(i + 1);
+      double m = -INFINITY;
+      for (int j = 0; j <= i; ++j) {
+        double acc = 0.0;
+        for (int c = 0; c < hd; ++c)
+          acc += q[(int64_t)i * qs + h * hd + c] * k[(int64_t)j * ks + g * hd + c];
+        sc[j] = acc * scale;
+        m = std::max(m, sc[j]);
+      }
+      double denom = 0.0;
+      for (int j = 0; j <= i; ++j) {
+        sc[j] = std::exp(sc[j] - m);
+        denom += sc[j];
+      }
+      for (int c = 0; c < hd; ++c) {
+        double acc = 0.0;
+        for (int j = 0; j <= i; ++j) acc += sc[j] * v[(int64_t)j * ks + g * hd + c];
+        o[(int64_t)ri * qs + h * hd + c] = acc / denom;
+      }
+    }
+  }
+}
+
+static inline double silu(double z) { return z / (1.0 + std::exp(-z)); }
+
+// The transformer block on ONE sequence's compact buffer xs [n, d] (rows in
+// position order). Produces the attention residual a and the FFN residual f
+// for the requested compact rows (rows == NULL: all n rows), written densely
+// in request order: a_out, f_out are [nrows, d].
+//   u = RMSNorm(xs) * g1;  q,k,v = u Wq^T, u Wk^T, u Wv^T
+//   o = causal GQA attention;  a = o Wo^T;  h = xs + a
+//   v2 = RMSNorm(h) * g2;  f = (silu(v2 Wg^T) * (v2 Wu^T)) Wd^T
+void oracle_block_rows(const oracle_dims* dm, int n, const double* xs,
+                       const oracle_layer_w* w, const int32_t* rows, int nrows,
+                       double* a_out, double* f_out) {
+  const int d = dm->d, hq = dm->hq, hkv = dm->hkv, hd = dm->hd, F = dm->F;
+  const int nr = rows ? nrows : n;
+  if (nr <= 0) return;
+  // Keys and values are needed for every compact row up to the last requested one.
+  int last = n - 1;
+  if (rows) {
+    last = 0;
+    for (int i = 0; i < nr; ++i) last = std::max(last, rows[i]);
+  }
+  const int nkv = last + 1;
+  std::vector<double> u((int64_t)nkv * d);
+  oracle_rmsnorm(nkv, d, xs, w->g1, dm->eps, u.data());
+  std::vector<double> kk((int64_t)nkv * hkv * hd), vv((int64_t)nkv * hkv * hd);
+  oracle_linear(nkv, d, hkv * hd, u.data(), w->wk, kk.data());
+  oracle_linear(nkv, d, hkv * hd, u.data(), w->wv, vv.data());
+  // Queries for the requested rows only.
+  std::vector<double> ur((int64_t)nr * d), xr((int64_t)nr * d);
+  for (int i = 0; i < nr; ++i) {
+    const int src = rows ? rows[i] : i;
+    std::memcpy(&ur[(int64_t)i * d], &u[(int64_t)src * d], sizeof(double) * d);
+    std::memcpy(&xr[(int64_t)i * d], &xs[(int64_t)src * d], sizeof(double) * d);
+  }
+  std::vector<double> qfull((int64_t)nkv * hq * hd, 0.0);
+  {
+    std::vector<double> qr((int64_t)nr * hq * hd);
+    oracle_linear(nr, d, hq * hd, ur.data(), w->wq, qr.data());
+    for (int i = 0; i < nr; ++i) {
+      const int dst = rows ? rows[i] : i;
+      std::memcpy(&qfull[(int64_t)dst * hq * hd], &qr[(int64_t)i * hq * hd],
+                  sizeof(double) * hq * hd);
+    }
+  }
+  std::vector<double> o((int64_t)nr * hq * hd);
+  std::vector<int32_t> all;
+  const int32_t* rr = rows;
+  if (!rows) {
+    all.resize(n);
+    std::iota(all.begin(), all.end(), 0);
+    rr = all.data();
+  }
+  oracle_attention_rows(nkv, hq, hkv, hd, qfull.data(), kk.data(), vv.data(), o.data(),
+                        rr, nr);
+  oracle_linear(nr, hq * hd, d, o.data(), w->wo, a_out);
+  std::vector<double> h((int64_t)nr * d), v2((int64_t)nr * d);
+  for (int64_t i = 0; i < (int64_t)nr * d; ++i) h[i] = xr[i] + a_out[i];
+  oracle_rmsnorm(nr, d, h.data(), w->g2, dm->eps, v2.data());
+  std::vector<double> g((int64_t)nr * F), up((int64_t)nr * F), hid((int64_t)nr * F);
+  oracle_linear(nr, d, F, v2.data(), w->wg, g.data());
+  oracle_linear(nr, d, F, v2.data(), w->wu, up.data());
+  for (int64_t i = 0; i < (int64_t)nr * F; ++i) hid[i] = silu(g[i]) * up[i];
+  oracle_linear(nr, F, d, hid.data(), w->wd, f_out);
+}
+
+// One layer of the stack on x_in [B, T, d] -> y [B, T, d].
+//   sparse: router (Eq. 8) -> top-(T/K) -> gather -> block -> gated residual
+//           (Eq. 7 if gate == XMOD, Eq. 6 if gate == MOD); unselected rows y = x.
+//   dense:  block on all T tokens, y = x + a + f.
+// Optional arguments:
+//   bias      [B, T]  signed per-token router bias, added to the logit;
+//   s_out     [B, T]  router logits; r_out [B, T] gates;
+//   idx_out   [B, n]  selected positions (ascending); rsel_out [B, n] their gates;
+//   idx_force [B, n]  use these positions instead of the oracle's own top-k (used to
+//                     decouple block parity from near-tie routing decisions; must
+//                     be ascending and in range);
+//   row_mask  [B, T]  nonzero marks output rows that are wanted; other rows are
+//                     copied from x_in (NULL: all rows computed).
+// Returns ORACLE_OK, ORACLE_BAD_ARG or ORACLE_NONFINITE.
+int oracle_layer_fwd(const oracle_dims* dm, int kind, int K, int gate,
+                     const oracle_layer_w* w, const double* x_in, const double* bias,
+                     double* y, double* s_out, double* r_out, int32_t* idx_out,
+                     double* rsel_out, const int32_t* idx_force, const int32_t* row_mask) {
+  const int B = dm->B, T = dm->T, d = dm->d;
+  if (B <= 0 || T <= 0 || d <= 0 || dm->hq % dm->hkv != 0) return ORACLE_BAD_ARG;
+  const int64_t BT = (int64_t)B * T;
+  std::memcpy(y, x_in, sizeof(double) * BT * d);
+  if (kind == ORACLE_DENSE) {
+    for (int b = 0; b < B; ++b) {
+      std::vector<int32_t> rows;
+      for (int t = 0; t < T; ++t)
+        if (!row_mask || row_mask[(int64_t)b * T + t]) rows.push_back(t);
+      if (rows.empty()) continue;
+      const double* xb = x_in + (int64_t)b * T * d;
+      std::vector<double> a(rows.size() * (size_t)d), f(rows.size() * (size_t)d);
+      oracle_block_rows(dm, T, xb, w, rows.data(), (int)rows.size(), a.data(), f.data());
+      for (size_t i = 0; i < rows.size(); ++i)
+        for (int c = 0; c < d; ++c) {
+          const int64_t o = ((int64_t)b * T + rows[i]) * d + c;
+          y[o] = x_in[o] + a[i * d + c] + f[i * d + c];
+        }
+    }
+    return ORACLE_OK;
+  }
+  if (kind != ORACLE_SPARSE || K <= 0) return ORACLE_BAD_ARG;
+  const int n = T / K;
+  if (n <= 0) return ORACLE_BAD_ARG;
+  std::vector<double> s(BT), r(BT);
+  oracle_router(BT, d, x_in, w->w_r, bias, s.data(), r.data());
+  if (s_out) std::memcpy(s_out, s.data(), sizeof(double) * BT);
+  if (r_out) std::memcpy(r_out, r.data(), sizeof(double) * BT);
+  std::vector<int32_t> idx((int64_t)B * n);
+  if (idx_force) {
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < n; ++j) {
+        const int32_t p = idx_force[(int64_t)b * n + j];
+        if (p < 0 || p >= T || (j > 0 && p <= idx_force[(int64_t)b * n + j - 1]))
+          return ORACLE_BAD_ARG;
+        idx[(int64_t)b * n + j] = p;
+      }
+  } else {
+    int st = oracle_topk(B, T, n, s.data(), idx.data());
+    if (st != ORACLE_OK) return st;
+  }
+  if (idx_out) std::memcpy(idx_out, idx.data(), sizeof(int32_t) * B * n);
+  if (rsel_out)
+    for (int b = 0; b < B; ++b)
+      for (int j = 0; j < n; ++j)
+        rsel_out[(int64_t)b * n + j] = r[(int64_t)b * T + idx[(int64_t)b * n + j]];
+  for (int b = 0; b < B; ++b) {
+    // gather in position order
+    std::vector<double> xs((int64_t)n * d);
+    for (int j = 0; j < n; ++j)
+      std::memcpy(&xs[(int64_t)j * d], x_in + ((int64_t)b * T + idx[(int64_t)b * n + j]) * d,
+                  sizeof(double) * d);
+    std::vector<int32_t> rows;
+    for (int j = 0; j < n; ++j)
+      if (!row_mask || row_mask[(int64_t)b * T + idx[(int64_t)b * n + j]]) rows.push_back(j);
+    if (rows.empty()) continue;
+    std::vector<double> a(rows.size() * (size_t)d), f(rows.size() * (size_t)d);
+    oracle_block_rows(dm, n, xs.data(), w, rows.data(), (int)rows.size(), a.data(), f.data());
+    for (size_t i = 0; i < rows.size(); ++i) {
+      const int j = rows[i];
+      const int t = idx[(int64_t)b * n + j];
+      const double rt = r[(int64_t)b * T + t];
+      for (int c = 0; c < d; ++c) {
+        const int64_t o = ((int64_t)b * T + t) * d + c;
+        const double ai = a[i * d + c], fi = f[i * d + c];
+        if (gate == ORACLE_GATE_XMOD)
+          y[o] = x_in[o] + w->varsigma * rt * (ai + fi);   // Eq. 7
+        else
+          y[o] = x_in[o] + ai + rt * fi;                   // Eq. 6
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+// Whole stack: layers applied in the given order (kinds[l] = DENSE or SPARSE).
+// The same bias is used by every sparse layer. With mirror_bf16 != 0 the
+// residual stream is rounded to bf16 after every layer, as a bf16 stream stores it.
+// seq_mask [B] (nullable): only sequences with a nonzero entry are computed;
+// the others keep their input values. x is updated in place.
+int oracle_stack_fwd(const oracle_dims* dm, int K, int gate, int n_layers, const int* kinds,
+                     const oracle_layer_w* layers, double* x, const double* bias,
+                     int mirror_bf16, const int32_t* seq_mask) {
+  const int64_t BT = (int64_t)dm->B * dm->T;
+  const int64_t N = BT * dm->d;
+  std::vector<int32_t> row_mask;
+  if (seq_mask) {
+    row_mask.resize(BT);
+    for (int b = 0; b < dm->B; ++b)
+      for (int t = 0; t < dm->T; ++t) row_mask[(int64_t)b * dm->T + t] = seq_mask[b] ? 1 : 0;
+  }
+  std::vector<double> y(N);
+  for (int l = 0; l < n_layers; ++l) {
+    int st = oracle_layer_fwd(dm, kinds[l], K, gate, &layers[l], x, bias, y.data(), nullptr,
+                              nullptr, nullptr, nullptr, nullptr,
+                              seq_mask ? row_mask.data() : nullptr);
+    if (st != ORACLE_OK) return st;
+    if (mirror_bf16)
+      for (int64_t i = 0; i < N; ++i) y[i] = oracle_round_bf16(y[i]);
+    std::memcpy(x, y.data(), sizeof(double) * N);
+  }
+  return ORACLE_OK;
+}
+
+}  // extern "C"

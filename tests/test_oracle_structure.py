@@ -1,0 +1,107 @@
+"""Pins of the oracle's layer-structure arithmetic against the X-MoD notes' printed values.
+
+Every expected value here is printed on the page (tests/golden/paper_counts.json
+cites the equation or table of each); none is computed by the code under test.
+"""
+import json
+import os
+from fractions import Fraction
+
+import pytest
+
+from oracle import structure as S
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "paper_counts.json")))
+
+
+def _stack(entry):
+    return S.schedule_segments(entry["N0"], entry["segments"])
+
+
+def test_eq2_mod_ratio_printed():
+    g = GOLD["eq2_mod_ratio"]
+    K = g["K"]
+    assert S.eq2_mod_ratio(K) == Fraction(*g["printed_fraction"])
+    # The MoD stack of Eq. 1 with any N has exactly that total/active ratio.
+    for N in (1, 4, 24):
+        kinds = S.schedule(0, N, Fraction(1, K), K)
+        assert S.total_over_active(kinds, K) == Fraction(*g["printed_fraction"])
+    assert round(float(S.eq2_mod_ratio(K)), 2) == g["printed_decimal"]
+    # Eq. 2 stays below 2 for every K.
+    assert all(S.eq2_mod_ratio(k) < 2 for k in range(1, 200))
+
+
+@pytest.mark.parametrize("entry", GOLD["stacks"], ids=lambda e: e["name"])
+def test_stack_depths_printed(entry):
+    kinds = _stack(entry)
+    assert S.physical_layers(kinds) == entry["physical"]
+    assert S.active_layers(kinds, entry["K"]) == entry["active"]
+
+
+@pytest.mark.parametrize("N0,N1,A,K", [(4, 6, 3, 16), (4, 24, 1, 8), (2, 2, 3, 16), (0, 1, 4, 8),
+                                       (1, 1, 1, 4), (0, 4, Fraction(1, 8), 8)])
+def test_eq4_eq5_match_schedule(N0, N1, A, K):
+    """Eq. 4 / Eq. 5 closed forms equal the counts of the Eq. 3 schedule (N_layer = 1)."""
+    kinds = S.schedule(N0, N1, A, K)
+    assert S.eq4_total(1, N0, N1, A, K) == S.physical_layers(kinds)
+    assert S.eq5_active(1, N0, N1, A) == S.active_layers(kinds, K)
+    # Eq. 3 order: the dense prefix, then blocks that end in a dense anchor.
+    assert kinds[:N0] == [S.DENSE] * N0
+    if N1:
+        assert kinds[-1] == S.DENSE
+
+
+def test_schedule_rejects_fractional_ak():
+    with pytest.raises(ValueError):
+        S.schedule(0, 1, Fraction(1, 3), 8)
+
+
+def _backbone(name):
+    d, hd, hq, hkv, F = GOLD["backbones"][name]
+    return d, hq, hkv, hd, F
+
+
+def _kinds_for(stack):
+    byname = {e["name"]: e for e in GOLD["stacks"]}
+    if stack == "Dense":
+        return [S.DENSE] * 28
+    if stack == "Deep Dense":
+        return [S.DENSE] * 52
+    return _stack(byname[stack])
+
+
+@pytest.mark.parametrize("row", GOLD["param_totals"], ids=lambda r: f"{r['backbone']}-{r['stack']}")
+def test_param_totals_printed(row):
+    """The block's weight set (GQA q/k/v/o, three-matrix SwiGLU, two gains) plus untied
+    embeddings reproduces the printed totals; printed values the formula cannot reach
+    are recorded as the page's own mismatches."""
+    d, hq, hkv, hd, F = _backbone(row["backbone"])
+    n = S.model_params(_kinds_for(row["stack"]), d, hq, hkv, hd, F, vocab=GOLD["backbones"]["vocab"])
+    printed = row["printed_B"]
+    digits = len(str(printed).split(".")[1])
+    agrees = round(n / 1e9, digits) == printed
+    if row.get("mismatch"):
+        assert not agrees, "a recorded mismatch now agrees; update the golden file"
+        assert abs(n / 1e9 - printed) / printed < 0.05
+    else:
+        assert agrees, (n / 1e9, printed)
+
+
+def test_total_over_active_936M():
+    g = GOLD["total_over_active_936M"]
+    d, hq, hkv, hd, F = _backbone("936M")
+    V = GOLD["backbones"]["vocab"]
+    # The notes divide the totals, as printed in billions to two decimals, by the
+    # nominal 936M active size.
+    for stack in ("A4K8", "A3K16", "MoD"):
+        n = S.model_params(_kinds_for(stack), d, hq, hkv, hd, F, vocab=V)
+        digits = len(str(g[stack]).split(".")[1])
+        assert round(round(n / 1e9, 2) / 0.936, digits) == g[stack]
+
+
+def test_router_params_negligible():
+    d, hq, hkv, hd, F = _backbone("936M")
+    kinds = _kinds_for("A3K16")
+    a = S.model_params(kinds, d, hq, hkv, hd, F, vocab=50257)
+    b = S.model_params(kinds, d, hq, hkv, hd, F, vocab=50257, router=True)
+    assert 0 < (b - a) / a < 1e-3
