@@ -1,0 +1,440 @@
+"""Benchmark of the sparse-depth layer forward on GB300.
+
+One step = one pass of the whole X-MoD A4K8 block (32 Sparse(K=8) layers with
+Eq. 7 gating + 1 Dense anchor; d=1536, 12 q / 4 kv heads, head_dim 128, SwiGLU
+d_ff=4096, B=8 sequences of T=4096 tokens, per-token router bias) through the
+library's stack entry point. Metric: selected tokens processed by sparse layers
+per second (B * T/K * 32 per step), whole job over all ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl xmod|reference]
+
+Under torchrun every rank runs its own B sequences (sequences are independent;
+no data-path collective), the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_depth_token_gb300 import inputs as I  # noqa: E402
+
+METRIC = "selected tokens/s per X-MoD sparse-layer fwd (bf16, 1xGB300); % HBM / tensor roofline"
+UNIT = "selected tokens/s"
+WORKLOAD = "a4k8_bf16"
+ABI_NAMES = {"w_r": "w_router", "g1": "rms1", "wq": "wq", "wk": "wk", "wv": "wv", "wo": "wo",
+             "g2": "rms2", "wg": "w_gate", "wu": "w_up", "wd": "w_down"}
+
+
+def schedule(w: I.Workload):
+    """Layer kinds of the Eq. 3 stack (1 = sparse) for counting work."""
+    ak = int(round(w.A * w.K))
+    return [0] * w.N0 + ([1] * ak + [0]) * w.N1
+
+
+def workload_config(w: I.Workload) -> dict:
+    kinds = schedule(w)
+    return {
+        "workload": f"{w.name}: X-MoD stack {sum(kinds)} Sparse(K={w.K}) + {len(kinds) - sum(kinds)} "
+                    f"Dense (Eq. 3, N0={w.N0}, N1={w.N1}, A={w.A}), Eq. "
+                    f"{'7' if w.gate == 0 else '6'} gating, d={w.d}, {w.hq}/{w.hkv} heads, "
+                    f"head_dim {w.hd}, SwiGLU d_ff={w.F}",
+        "B_per_gpu": w.B, "T": w.T, "K": w.K,
+        "selected_tokens_per_step_per_gpu": sum(kinds) * w.B * (w.T // w.K),
+        "l2": "no flush: one step streams 1.7 GB of distinct layer weights and a 100 MB "
+              "stream, both larger than the 129 MB L2",
+        "inputs": "seeded synthetic: x~N(0,1), matrices~N(0,0.02^2), w_r~N(0,1/d), "
+                  "bias~N(0,0.1^2), varsigma~U(0.5,1.5), RMSNorm gains 1",
+    }
+
+
+def algorithmic_work(w: I.Workload) -> dict:
+    """Algorithmic FLOPs (tensor kinds) or bytes (memory kinds) per step, per kernel kind.
+    Sparse layers count only the selected tokens; attention is causal (half the square)."""
+    es = 2 if w.dtype == "bf16" else 4
+    out = {}
+
+    def add(kind, v):
+        out[kind] = out.get(kind, 0.0) + float(v)
+
+    for sparse in schedule(w):
+        n = w.T // w.K if sparse else w.T
+        M = w.B * n
+        if sparse:
+            add("router", w.B * w.T * w.d * es + 4 * w.B * w.T)
+            add("topk", 4 * w.B * w.T + 8 * M)
+        add("gather_rmsnorm", 2 * M * w.d * es)
+        add("gemm_q", 2 * M * w.d * w.hq * w.hd)
+        add("gemm_k", 2 * M * w.d * w.hkv * w.hd)
+        add("gemm_v", 2 * M * w.d * w.hkv * w.hd)
+        add("attention", 2 * w.B * n * n * w.hd * w.hq)
+        add("gemm_o_residual", 2 * M * w.hq * w.hd * w.d)
+        add("rmsnorm2", 2 * M * w.d * es)
+        add("gemm_gate_up_swiglu", 4 * M * w.d * w.F)
+        add("gemm_down_scatter", 2 * M * w.F * w.d)
+    return out
+
+
+TENSOR_KINDS = {"gemm_q", "gemm_k", "gemm_v", "attention", "gemm_o_residual",
+                "gemm_gate_up_swiglu", "gemm_down_scatter"}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------- CPU oracle baseline
+
+def oracle_sample(w: I.Workload, budget_s: float = 15.0, max_reps: int = 50):
+    """The CPU oracle on a bounded sample of the workload: one sparse layer of the stack
+    (layer 0 weights) on sequence 0 of the batch, repeated until `budget_s` elapses.
+    Returns (selected tokens/s, threads, description)."""
+    import oracle as O
+    lw = I.layer_weights(w, 0)
+    L = O.Layer({k: I.to_f64(v, w.dtype) for k, v in lw.items() if k in ABI_NAMES},
+                lw["varsigma"])
+    w1 = w.replace(B=1)
+    x = I.to_f64(I.residual_stream(w1), w.dtype)
+    bias = I.router_bias(w1)
+    dm = O.dims(1, w.T, w.d, w.hq, w.hkv, w.hd, w.F, w.eps)
+    n = w.T // w.K
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        O.layer_fwd(dm, O.SPARSE, w.K, w.gate, L, x, bias=bias)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            break
+    return reps * n / el, O.num_threads(), (
+        f"one Sparse(K={w.K}) layer on 1 of the {w.B} sequences (T={w.T}, n={n} selected), "
+        f"{reps} repetition(s) in {el:.1f} s")
+
+
+def run_reference(args):
+    """--impl reference: the oracle as it stands, timed on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = I.WORKLOADS[args.workload]
+    import oracle as O
+    lw = I.layer_weights(w, 0)
+    L = O.Layer({k: I.to_f64(v, w.dtype) for k, v in lw.items() if k in ABI_NAMES},
+                lw["varsigma"])
+    w1 = w.replace(B=1)
+    x = I.to_f64(I.residual_stream(w1), w.dtype)
+    bias = I.router_bias(w1)
+    dm = O.dims(1, w.T, w.d, w.hq, w.hkv, w.hd, w.F, w.eps)
+    n = w.T // w.K
+
+    def step():
+        O.layer_fwd(dm, O.SPARSE, w.K, w.gate, L, x, bias=bias)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = args.steps * n / el
+    sample = (f"each step: one Sparse(K={w.K}) layer of the workload on 1 of its {w.B} "
+              f"sequences (n={n} selected tokens)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------- GPU arm
+
+def run_xmod(args):
+    import torch
+    from sparse_depth_token_gb300 import xmod as X
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    X.load()
+
+    w = I.WORKLOADS[args.workload]
+    kinds = schedule(w)
+    n_sparse = sum(kinds)
+    sel_per_step = n_sparse * w.B * (w.T // w.K)
+    # per-rank data: the same weights, different sequences
+    wr = w.replace(seed=w.seed + 1000 * rank) if rank else w
+    layers = I.all_layer_weights(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def to_dev(a):
+        if w.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    dev_layers = [{ABI_NAMES[k]: to_dev(v) for k, v in l.items() if k in ABI_NAMES} for l in layers]
+    abi = [X.layer_weights(d, l["varsigma"]) for d, l in zip(dev_layers, layers)]
+    x_host = I.residual_stream(wr)
+    bias_host = I.router_bias(wr)
+    x0 = to_dev(x_host)
+    x = torch.empty_like(x0)
+    bias = torch.from_numpy(bias_host).to(dev) if bias_host is not None else None
+    dm = X.dims(w.B, w.T, w.d, w.hq, w.hkv, w.hd, w.F, X.BF16 if w.dtype == "bf16" else X.FP32,
+                w.eps)
+    ws = torch.zeros(X.workspace_bytes(dm, w.K), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        x.copy_(x0, non_blocking=True)
+        X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, x, bias, ws, stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    X.reset_status(ws)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    st = X.sync_status(ws)
+    if st != X.OK:
+        raise RuntimeError(f"device status after warm-up: {X.status_string(st)}")
+
+    # ---- timed region
+    clocks = ClockSampler(local if world > 1 else 0)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = X.launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = (X.launch_count() - launches0) // args.steps
+    clock_info = clocks.stop()
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = world * sel_per_step / (ms_max / 1e3)
+
+    # ---- profiled pass: per-kernel CUDA-event times on the launching stream
+    X.profile_read()
+    X.profile_enable(True)
+    prof_steps = max(1, min(args.steps, 3))
+    for _ in range(prof_steps):
+        step()
+    torch.cuda.synchronize()
+    X.profile_enable(False)
+    prof = X.profile_read()
+    work = algorithmic_work(w)
+    peaks = measured_peaks()
+    total_ms = sum(v[1] for v in prof.values())
+    kernels = {}
+    for kind, (cnt, kms) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+        per_step_ms = kms / prof_steps
+        wk = work.get(kind)
+        entry = {"launches_per_step": cnt // prof_steps, "ms_per_step": per_step_ms,
+                 "share": kms / total_ms if total_ms else None}
+        if wk is not None and kms > 0:
+            if kind in TENSOR_KINDS:
+                entry["tflops"] = wk / (per_step_ms / 1e3) / 1e12
+            else:
+                entry["gbs"] = wk / (per_step_ms / 1e3) / 1e9
+        kernels[kind] = entry
+    top = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
+    roofline = None
+    if top is not None and top in work:
+        cnt, kms = prof[top]
+        if top in TENSOR_KINDS:
+            ach = work[top] / (kms / prof_steps / 1e3) / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            roofline = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": peak,
+                        "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                        "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside "
+                                       f"a long step)",
+                        "algorithmic_per_launch": work[top] / (cnt / prof_steps)}
+        else:
+            ach = work[top] / (kms / prof_steps / 1e3) / 1e9
+            peak = peaks["hbm_gbs"]
+            roofline = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": peak,
+                        "unit": "GB/s", "frac": ach / peak, "traffic": None,
+                        "peak_source": f"{peaks['source']} HBM copy",
+                        "algorithmic_per_launch": work[top] / (cnt / prof_steps)}
+    step_flops = sum(v for k, v in work.items() if k in TENSOR_KINDS)
+
+    # ---- end to end through the C ABI call with host buffers (pinned), copies timed
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(np.ascontiguousarray(x_host).view(np.int16)).view(torch.bfloat16) \
+            if w.dtype == "bf16" else torch.from_numpy(x_host)
+        xh = xh.pin_memory()
+        out_h = torch.empty_like(xh).pin_memory()
+        bh = torch.from_numpy(bias_host).pin_memory() if bias_host is not None else None
+
+        def e2e_step():
+            x.copy_(xh, non_blocking=True)
+            if bh is not None:
+                bias.copy_(bh, non_blocking=True)
+            X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, x, bias, ws, stream)
+            out_h.copy_(x, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1) / args.steps
+        if dist is not None:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * sel_per_step / (ems / 1e3), "unit": UNIT,
+               "ms_per_step": ems,
+               "h2d_bytes_per_step": int(xh.numel() * xh.element_size() +
+                                         (bh.numel() * 4 if bh is not None else 0)),
+               "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size())}
+    st = X.sync_status(ws)
+    if st != X.OK:
+        raise RuntimeError(f"device status after the run: {X.status_string(st)}")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = oracle_sample(w, budget_s=args.cpu_budget)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        cfg = workload_config(w)
+        cfg["parallelism"] = f"replicas x{world} (sequences sharded, no collective)"
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.dtype == "bf16" else "fp32",
+                "data": "synthetic (seeded; random-init weights)", "config": cfg,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": int(launches) * args.steps,
+                "gpu_launches_per_step": int(launches),
+                "clocks": clock_info,
+                "step_tflops": step_flops / (ms_max / 1e3) / 1e12,
+                "kernels": kernels}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["xmod", "reference"], default="xmod")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_xmod(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,190 @@
+/*
+ * xmod.h -- C ABI of the X-MoD / MoD sparse-depth layer forward pass on one GPU.
+ *
+ * The method (page "X-MoD: Practical Scaling Laws for Sparse-Depth Routing Beyond
+ * Mixture-of-Depths", reading notes): every sparse layer scores each token with a
+ * router (Eq. 8), keeps the top 1/K tokens of every sequence (section "MoD
+ * structural limit", Eq. 1), runs the transformer block on those tokens only --
+ * attention among the selected tokens (section "mechanism controls") -- and writes
+ * them back with the gated residual of Eq. 7 (X-MoD) or Eq. 6 (MoD). Unselected
+ * tokens pass through unchanged. Layers follow Eq. 3:
+ * [Dense] x N0 + ([Sparse(K)] x AK + [Dense]) x N1.
+ * The page "Mixture-of-Depths explained" (its MoDLayer listing) fixes the
+ * position-ordered gather and the floor(T / K) selection count.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers, owned by the caller. The library
+ *     never allocates, frees or synchronises (except xmod_sync_status).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream).
+ *   - Residual-stream tensors and weights are in dims->dtype (bf16 or fp32),
+ *     row-major. Router logits, gates and biases are always fp32; indices int32.
+ *   - Matrices use the [out, in] row-major layout: wq [hq*hd, d], wk and wv
+ *     [hkv*hd, d], wo [d, hq*hd], w_gate and w_up [F, d], w_down [d, F];
+ *     w_router, rms1, rms2 are [d].
+ *   - Host-detected errors return a negative xmod_status before anything is
+ *     launched. Errors found on the device (a non-finite router logit, a bounded
+ *     wait that ran out) are recorded in the workspace status word and returned
+ *     by xmod_sync_status; kernels never trap.
+ *   - Pointers must be 16-byte aligned; d, hq*hd, hkv*hd and F must be
+ *     multiples of 8.
+ *   - Entry points are stateless and may run concurrently on different streams
+ *     with different workspaces.
+ */
+#ifndef XMOD_H
+#define XMOD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define XMOD_API __attribute__((visibility("default")))
+#else
+#define XMOD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  XMOD_OK = 0,
+  XMOD_ERR_INVALID_ARG = -1,   /* bad pointer, size or combination; nothing launched */
+  XMOD_ERR_UNSUPPORTED = -2,   /* valid but not implemented (e.g. T beyond the top-k limit) */
+  XMOD_ERR_CUDA = -3,          /* a CUDA runtime call failed */
+  XMOD_ERR_TIMEOUT = -4,       /* a bounded device-side wait ran out (device status) */
+  XMOD_ERR_DEVICE_CHECK = -5,  /* non-finite router logit or bad index seen on device */
+  XMOD_ERR_WORKSPACE = -6      /* workspace missing or smaller than xmod_workspace_bytes */
+} xmod_status;
+
+typedef enum { XMOD_BF16 = 0, XMOD_FP32 = 1 } xmod_dtype;
+
+/* Residual gate: Eq. 7 (X-MoD) x + varsigma * r * (a + f); Eq. 6 (MoD) x + a + r * f. */
+typedef enum { XMOD_GATE_XMOD = 0, XMOD_GATE_MOD = 1 } xmod_gate;
+
+typedef enum { XMOD_LAYER_DENSE = 0, XMOD_LAYER_SPARSE = 1 } xmod_layer_kind;
+
+/* Problem sizes in the pages' notation: B sequences of T tokens, model width d,
+ * n_heads query heads and n_kv_heads key/value heads of head_dim (GQA), SwiGLU
+ * hidden width d_ff. rms_eps is the RMSNorm epsilon. */
+typedef struct {
+  int B, T, d, n_heads, n_kv_heads, head_dim, d_ff;
+  xmod_dtype dtype;
+  float rms_eps;
+} xmod_dims;
+
+/* One layer's weights (device pointers, dims->dtype). w_router is used by sparse
+ * layers only; varsigma is the per-layer scalar of Eq. 7. */
+typedef struct {
+  const void *w_router, *rms1, *wq, *wk, *wv, *wo, *rms2, *w_gate, *w_up, *w_down;
+  float varsigma;
+} xmod_layer_weights;
+
+/* Library version string. */
+XMOD_API const char* xmod_version(void);
+
+/* Human-readable name of an xmod_status value. */
+XMOD_API const char* xmod_status_string(int status);
+
+/* Bytes of device workspace the calls below need for these sizes and sparsity K
+ * (K = 1 sizes a dense layer; the stack needs the size for its own K, which
+ * covers its dense layers). Returns 0 for invalid dims. The workspace is
+ * caller-owned scratch; its first 256 bytes hold the device status word. */
+XMOD_API size_t xmod_workspace_bytes(const xmod_dims* dims, int K);
+
+/* Clear the device status word of a workspace (asynchronous). */
+XMOD_API int xmod_reset_status(void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream` and return the device status word of the workspace
+ * (XMOD_OK or the first device-side error recorded since the last reset), or
+ * XMOD_ERR_CUDA if synchronisation itself failed. */
+XMOD_API int xmod_sync_status(void* ws, void* stream);
+
+/* Router and per-sequence top-(T/K) selection (X-MoD notes Eq. 8; MoD blog listing).
+ *   x        [B, T, d]   residual stream (dtype)
+ *   w_r      [d]         router vector (dtype)
+ *   bias     [B, T] fp32 signed per-token bias added to the logit, or NULL
+ *   logits   [B, T] fp32 out: s = w_r . x + bias (NULL: kept in the workspace)
+ *   r        [B, T] fp32 out: sigmoid(s) (NULL: not written)
+ *   idx      [B, n] int32 out: the n = floor(T/K) positions with the largest s,
+ *                    ties to the lower position, ascending
+ *   r_sel    [B, n] fp32 out: sigmoid(s) at idx (NULL: not written)
+ * A non-finite logit records XMOD_ERR_DEVICE_CHECK in the status word. */
+XMOD_API int xmod_router_topk(const xmod_dims* dims, int K, const void* x, const void* w_r,
+                     const float* bias, float* logits, float* r, int32_t* idx, float* r_sel,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* Top-(T/K) selection on given fp32 logits [B, T] (same rule and outputs as
+ * xmod_router_topk; r_sel may be NULL). */
+XMOD_API int xmod_topk(const xmod_dims* dims, int K, const float* logits, int32_t* idx, float* r_sel,
+              void* ws, size_t ws_bytes, void* stream);
+
+/* Position-ordered gather: xs[b*n + j, :] = x[b, idx[b, j], :], n = floor(T/K). */
+XMOD_API int xmod_gather(const xmod_dims* dims, int K, const void* x, const int32_t* idx, void* xs,
+                void* stream);
+
+/* The transformer block on n_per_seq tokens of every sequence (X-MoD notes,
+ * backbone configuration: GQA attention, SwiGLU FFN; pre-norm RMSNorm):
+ *   u = RMSNorm(xs) * rms1; q, k, v = u Wq^T, u Wk^T, u Wv^T
+ *   o = causal GQA softmax attention among the n_per_seq tokens of a sequence,
+ *       scale 1/sqrt(head_dim), query head h reads KV head h / (n_heads/n_kv_heads)
+ *   a = o Wo^T; h = xs + a; f = (silu(v2 Wg^T) * (v2 Wu^T)) Wd^T, v2 = RMSNorm(h) * rms2
+ * With idx == NULL, `xs` is the compact buffer [B * n_per_seq, d]; otherwise `xs`
+ * is the full stream x [B, T, d] and row j of sequence b is x[b, idx[b, j]].
+ * a_out, f_out: [B * n_per_seq, d] (dtype). Workspace: xmod_workspace_bytes with
+ * K = T / n_per_seq rounded down. */
+XMOD_API int xmod_block_fwd(const xmod_dims* dims, int n_per_seq, const void* xs, const int32_t* idx,
+                   const xmod_layer_weights* w, void* a_out, void* f_out, void* ws,
+                   size_t ws_bytes, void* stream);
+
+/* Gated scatter back into the stream, in place (X-MoD notes Eq. 6 / Eq. 7):
+ *   gate XMOD: x[b, idx[b,j]] += varsigma * r_sel[b,j] * (a + f)
+ *   gate MOD:  x[b, idx[b,j]] += a + r_sel[b,j] * f
+ * a, f: [B * n, d] (dtype). f may be NULL under XMOD, in which case `a` holds a + f.
+ * Rows not in idx are not touched. */
+XMOD_API int xmod_gated_scatter(const xmod_dims* dims, int K, void* x_inout, const int32_t* idx,
+                       const float* r_sel, const void* a, const void* f, float varsigma,
+                       xmod_gate gate, void* stream);
+
+/* One layer in place on x [B, T, d]. Sparse: router + top-(T/K) + block on the
+ * selected tokens + gated residual; unselected rows untouched. Dense: the block on
+ * all tokens and x += a + f. bias: [B, T] fp32 or NULL. idx_out ([B, n] int32) and
+ * r_sel_out ([B, n] fp32) optionally receive the sparse layer's selection. */
+XMOD_API int xmod_layer_fwd(const xmod_dims* dims, xmod_layer_kind kind, int K, xmod_gate gate,
+                   const xmod_layer_weights* w, void* x_inout, const float* bias,
+                   int32_t* idx_out, float* r_sel_out, void* ws, size_t ws_bytes, void* stream);
+
+/* The Eq. 3 stack in place: [Dense] x N0 + ([Sparse(K)] x AK + [Dense]) x N1 with
+ * AK = round(A * K) (must equal A * K and be >= 1). `layers` holds n_layers =
+ * N0 + N1 * (AK + 1) weight sets in execution order. Every sparse layer uses the
+ * same bias (NULL: none). MoD's Eq. 1 stack is N0 = 0, A = 1/K. */
+XMOD_API int xmod_stack_fwd(const xmod_dims* dims, int K, double A, int N0, int N1, xmod_gate gate,
+                   const xmod_layer_weights* layers, int n_layers, void* x_inout,
+                   const float* bias, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- measurement
+ * Not part of the method: support for benchmarking the calls above. */
+
+/* Per-kernel-kind timing record filled by xmod_profile_read. */
+typedef struct {
+  char name[32];     /* kernel kind, e.g. "gemm_gate_up" */
+  int launches;      /* launches recorded since the last read */
+  double total_ms;   /* summed CUDA-event time of those launches */
+} xmod_kernel_time;
+
+/* Host-side count of kernel launches this library has issued so far. */
+XMOD_API uint64_t xmod_launch_count(void);
+
+/* Turn per-launch CUDA-event recording on (1) or off (0). While on, every
+ * launch is bracketed by two events on its own stream. Process-wide. */
+XMOD_API int xmod_profile_enable(int enable);
+
+/* Wait for the recorded events, aggregate them per kernel kind into out[0..max),
+ * set *n_kinds, and clear the records. Returns XMOD_ERR_CUDA if an event failed. */
+XMOD_API int xmod_profile_read(xmod_kernel_time* out, int max_kinds, int* n_kinds);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XMOD_H */

@@ -56,6 +56,9 @@ def lib():
         L.oracle_layer_fwd.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.POINTER(LayerW), _DP, _DP, _DP,
                                        _DP, _DP, _IP, _DP, _IP, _IP]
+        L.oracle_gated_scatter.argtypes = [ctypes.c_int64, ctypes.c_int, _DP,
+                                           ctypes.POINTER(ctypes.c_int64), _DP, _DP, _DP,
+                                           ctypes.c_double, ctypes.c_int]
         L.oracle_stack_fwd.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                        ctypes.POINTER(LayerW), _DP, _DP, ctypes.c_int, _IP]
@@ -148,6 +151,19 @@ def attention(q, k, v, hq, hkv, hd, rows=None):
     o = np.empty((nr, hq * hd))
     lib().oracle_attention_rows(n, hq, hkv, hd, qp, kp, vp, o.ctypes.data_as(_DP), rp, nr)
     return o
+
+
+def gated_scatter(x, rows, a, f, r, varsigma, gate):
+    """Eq. 7 / Eq. 6 residual written into rows of x [R, d] (returns a new array)."""
+    x = np.array(x, dtype=np.float64, copy=True, order="C")
+    rows_a = np.ascontiguousarray(rows, dtype=np.int64)
+    a, ap = _d(a)
+    f_a, fp = _d(f)
+    r, rp = _d(r)
+    lib().oracle_gated_scatter(len(rows_a), x.shape[-1], x.ctypes.data_as(_DP),
+                               rows_a.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), ap, fp, rp,
+                               float(varsigma), int(gate))
+    return x
 
 
 class Layer:

@@ -185,6 +185,27 @@ void oracle_attention_rows(int n, int hq, int hkv, int hd, const double* q,
 
 static inline double silu(double z) { return z / (1.0 + std::exp(-z)); }
 
+// Gated residual of one selected row (Eq. 7 for gate == XMOD, Eq. 6 for gate == MOD):
+//   Eq. 7: y = x + varsigma * r * (a + f);   Eq. 6: y = x + a + r * f.
+static inline double gated(double x, double a, double f, double r, double varsigma, int gate) {
+  if (gate == ORACLE_GATE_XMOD) return x + varsigma * r * (a + f);
+  return x + a + r * f;
+}
+
+// The scatter step on its own: rows[m] of x [rows_total, d] receives the gated
+// residual of a[m], f[m] with gate value r[m]; other rows are left as they are.
+// f == NULL means `a` already holds a + f (Eq. 7 only).
+void oracle_gated_scatter(int64_t M, int d, double* x, const int64_t* rows, const double* a,
+                          const double* f, const double* r, double varsigma, int gate) {
+  for (int64_t m = 0; m < M; ++m)
+    for (int c = 0; c < d; ++c) {
+      double* px = x + rows[m] * d + c;
+      const double am = a[m * d + c];
+      *px = f ? gated(*px, am, f[m * d + c], r[m], varsigma, gate)
+              : gated(*px, am, 0.0, r[m], varsigma, ORACLE_GATE_XMOD);
+    }
+}
+
 // The transformer block on ONE sequence's compact buffer xs [n, d] (rows in
 // position order). Produces the attention residual a and the FFN residual f
 // for the requested compact rows (rows == NULL: all n rows), written densely
@@ -330,11 +351,7 @@ int oracle_layer_fwd(const oracle_dims* dm, int kind, int K, int gate,
       const double rt = r[(int64_t)b * T + t];
       for (int c = 0; c < d; ++c) {
         const int64_t o = ((int64_t)b * T + t) * d + c;
-        const double ai = a[i * d + c], fi = f[i * d + c];
-        if (gate == ORACLE_GATE_XMOD)
-          y[o] = x_in[o] + w->varsigma * rt * (ai + fi);   // Eq. 7
-        else
-          y[o] = x_in[o] + ai + rt * fi;                   // Eq. 6
+        y[o] = gated(x_in[o], a[i * d + c], f[i * d + c], rt, w->varsigma, gate);
       }
     }
   }

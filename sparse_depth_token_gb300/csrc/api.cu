@@ -1,0 +1,362 @@
+// C ABI of the sparse-depth layer library: argument checks, workspace layout,
+// and the layer / stack schedules built from the kernels.
+//
+// Layer semantics follow "X-MoD: Practical Scaling Laws for Sparse-Depth Routing
+// Beyond Mixture-of-Depths" (reading notes): Eq. 8 router, top-1/K selection,
+// attention within the selected subset, Eq. 6 / Eq. 7 gated residuals, Eq. 3
+// stack layout; and "Mixture-of-Depths explained" (MoDLayer listing) for the
+// floor(T * ratio) count and position-ordered gather.
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "internal.h"
+#include "xmod.h"
+
+namespace xmod {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+inline size_t esize(xmod_dtype dt) { return dt == XMOD_BF16 ? 2 : 4; }
+inline bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+inline bool aligned16_or_null(const void* p) { return !p || ((uintptr_t)p & 15u) == 0; }
+
+bool dims_ok(const xmod_dims* dm) {
+  if (!dm) return false;
+  if (dm->dtype != XMOD_BF16 && dm->dtype != XMOD_FP32) return false;
+  if (dm->B <= 0 || dm->T <= 0 || dm->d <= 0 || dm->n_heads <= 0 || dm->n_kv_heads <= 0 ||
+      dm->head_dim <= 0 || dm->d_ff <= 0)
+    return false;
+  if (dm->n_heads % dm->n_kv_heads) return false;
+  if (dm->d % 8 || dm->d_ff % 8 || (dm->n_heads * dm->head_dim) % 8 ||
+      (dm->n_kv_heads * dm->head_dim) % 8)
+    return false;
+  if (!(dm->rms_eps >= 0.0f) || !isfinite(dm->rms_eps)) return false;
+  return true;
+}
+
+bool head_dim_supported(int hd) { return hd == 32 || hd == 64 || hd == 128; }
+
+// Workspace carve-up. M rows of block scratch cover a dense layer (M = B*T).
+struct Layout {
+  size_t status, s, idx, r_sel, u, qkv, o, a, h, hidden, total;
+};
+
+Layout layout(const xmod_dims* dm, int K) {
+  Layout L{};
+  const size_t es = esize(dm->dtype);
+  const size_t BT = (size_t)dm->B * dm->T;
+  const size_t n = (size_t)(dm->T / (K > 0 ? K : 1));
+  const size_t Bn = (size_t)dm->B * (n > 0 ? n : 1);
+  const size_t M = BT;
+  const size_t qkv_w = (size_t)(dm->n_heads + 2 * dm->n_kv_heads) * dm->head_dim;
+  size_t off = 0;
+  L.status = off; off += kAlign;
+  L.s = off;      off = align_up(off + 4 * BT);
+  L.idx = off;    off = align_up(off + 4 * Bn);
+  L.r_sel = off;  off = align_up(off + 4 * Bn);
+  L.u = off;      off = align_up(off + es * M * dm->d);
+  L.qkv = off;    off = align_up(off + es * M * qkv_w);
+  L.o = off;      off = align_up(off + es * M * dm->n_heads * dm->head_dim);
+  L.a = off;      off = align_up(off + es * M * dm->d);
+  L.h = off;      off = align_up(off + es * M * dm->d);
+  L.hidden = off; off = align_up(off + es * M * dm->d_ff);
+  L.total = off;
+  return L;
+}
+
+inline char* at(void* ws, size_t off) { return (char*)ws + off; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? XMOD_OK : XMOD_ERR_CUDA; }
+
+// One kernel launch: counted, optionally timed, and checked.
+#define XMOD_RUN(kind, expr)                         \
+  do {                                               \
+    cudaError_t _e;                                  \
+    {                                                \
+      ProfScope _p(kind, c.stream);                  \
+      _e = (expr);                                   \
+    }                                                \
+    count_launch();                                  \
+    if (_e != cudaSuccess) return XMOD_ERR_CUDA;     \
+  } while (0)
+
+bool weights_ok(const xmod_layer_weights* w, bool need_router) {
+  if (!w) return false;
+  if (need_router && !aligned16(w->w_router)) return false;
+  const void* ps[] = {w->rms1, w->wq, w->wk, w->wv, w->wo, w->rms2, w->w_gate, w->w_up, w->w_down};
+  for (const void* p : ps)
+    if (!aligned16(p)) return false;
+  return isfinite(w->varsigma);
+}
+
+// The block on B*n compact rows (rows of x selected by idx, or identity when
+// idx == NULL and n == T). Writes a to a_out (or the workspace) and either
+// scatters the gated residual into x (scatter == true) or stores f to f_out.
+int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int n,
+              const void* x_src, const int32_t* idx, const xmod_layer_weights* w, void* a_out,
+              void* f_out, bool scatter, void* x_inout, const float* r_sel, int gate) {
+  const xmod_dtype dt = dm->dtype;
+  const int B = dm->B, T = dm->T, d = dm->d, hq = dm->n_heads, hkv = dm->n_kv_heads,
+            hd = dm->head_dim, F = dm->d_ff;
+  const int M = B * n;
+  const int qw = hq * hd, kw = hkv * hd, qkv_w = qw + 2 * kw;
+  const size_t es = esize(dt);
+  char* u = at(ws, L.u);
+  char* qkv = at(ws, L.qkv);
+  char* o = at(ws, L.o);
+  char* a = a_out ? (char*)a_out : at(ws, L.a);
+  char* h = at(ws, L.h);
+  char* hidden = at(ws, L.hidden);
+  // 1. gather + RMSNorm1
+  XMOD_RUN("gather_rmsnorm", launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms1, dm->rms_eps, u));
+  // 2. q, k, v projections into one [M, qkv_w] buffer
+  Epilogue e;
+  e.kind = EPI_STORE;
+  e.ldo = qkv_w;
+  e.out = qkv;
+  XMOD_RUN("gemm_q", launch_gemm_simt(c, dt, M, qw, d, u, d, w->wq, d, nullptr, e));
+  e.out = qkv + es * qw;
+  XMOD_RUN("gemm_k", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wk, d, nullptr, e));
+  e.out = qkv + es * (qw + kw);
+  XMOD_RUN("gemm_v", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wv, d, nullptr, e));
+  // 3. causal GQA attention among the n rows of each sequence
+  XMOD_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w, qkv + es * qw,
+                                 qkv + es * (qw + kw), qkv_w, o));
+  // 4. a = o Wo^T, h = x_sel + a
+  Epilogue eo;
+  eo.kind = EPI_OPROJ;
+  eo.out = a;
+  eo.ldo = d;
+  eo.out2 = h;
+  eo.ldo2 = d;
+  eo.x = (void*)x_src;
+  eo.idx = idx;
+  eo.T = T;
+  eo.n_per_seq = n;
+  eo.d = d;
+  XMOD_RUN("gemm_o_residual", launch_gemm_simt(c, dt, M, d, qw, o, qw, w->wo, qw, nullptr, eo));
+  // 5. v2 = RMSNorm(h) * rms2 (in place)
+  XMOD_RUN("rmsnorm2", launch_gather_rmsnorm(c, dt, 1, M, M, d, h, nullptr, w->rms2, dm->rms_eps, h));
+  // 6. hidden = silu(v2 Wg^T) * (v2 Wu^T)
+  Epilogue eg;
+  eg.kind = EPI_SWIGLU;
+  eg.out = hidden;
+  eg.ldo = F;
+  XMOD_RUN("gemm_gate_up_swiglu", launch_gemm_simt(c, dt, M, F, d, h, d, w->w_gate, d, w->w_up, eg));
+  // 7. f = hidden Wd^T, then the gated residual (or f stored)
+  Epilogue ed;
+  if (scatter) {
+    ed.kind = EPI_DOWN_SCATTER;
+    ed.x = x_inout;
+    ed.idx = idx;
+    ed.T = T;
+    ed.n_per_seq = n;
+    ed.d = d;
+    ed.a = a;
+    ed.r_sel = r_sel;
+    ed.varsigma = w->varsigma;
+    ed.gate = gate;
+  } else {
+    ed.kind = EPI_STORE;
+    ed.out = f_out;
+    ed.ldo = d;
+  }
+  XMOD_RUN(scatter ? "gemm_down_scatter" : "gemm_down", launch_gemm_simt(c, dt, M, d, F, hidden, F, w->w_down, F, nullptr, ed));
+  return XMOD_OK;
+}
+
+int check_ws(const xmod_dims* dm, int K, void* ws, size_t ws_bytes) {
+  if (!aligned16(ws)) return XMOD_ERR_WORKSPACE;
+  if (ws_bytes < layout(dm, K).total) return XMOD_ERR_WORKSPACE;
+  return XMOD_OK;
+}
+
+int layer_impl(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
+               const xmod_layer_weights* w, void* x, const float* bias, int32_t* idx_out,
+               float* r_sel_out, void* ws, const Layout& L, cudaStream_t stream) {
+  Ctx c{stream, (int*)at(ws, L.status)};
+  if (kind == XMOD_LAYER_DENSE)
+    return run_block(c, dm, L, ws, dm->T, x, nullptr, w, nullptr, nullptr, true, x, nullptr, -1);
+  const int n = dm->T / K;
+  float* s = (float*)at(ws, L.s);
+  int32_t* idx = idx_out ? idx_out : (int32_t*)at(ws, L.idx);
+  float* r_sel = r_sel_out ? r_sel_out : (float*)at(ws, L.r_sel);
+  XMOD_RUN("router", launch_router(c, dm->dtype, (int64_t)dm->B * dm->T, dm->d, x, w->w_router, bias, s,
+                         nullptr));
+  XMOD_RUN("topk", launch_topk(c, dm->B, dm->T, n, s, idx, r_sel));
+  return run_block(c, dm, L, ws, n, x, idx, w, nullptr, nullptr, true, x, r_sel, (int)gate);
+}
+
+}  // namespace
+}  // namespace xmod
+
+using namespace xmod;
+
+extern "C" {
+
+const char* xmod_version(void) { return "xmod-gb300 0.1 (sm_103a)"; }
+
+const char* xmod_status_string(int st) {
+  switch (st) {
+    case XMOD_OK: return "ok";
+    case XMOD_ERR_INVALID_ARG: return "invalid argument";
+    case XMOD_ERR_UNSUPPORTED: return "unsupported combination";
+    case XMOD_ERR_CUDA: return "CUDA runtime error";
+    case XMOD_ERR_TIMEOUT: return "device-side wait timed out";
+    case XMOD_ERR_DEVICE_CHECK: return "device-side check failed (non-finite logit or bad index)";
+    case XMOD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+size_t xmod_workspace_bytes(const xmod_dims* dm, int K) {
+  if (!dims_ok(dm) || K <= 0 || K > dm->T) return 0;
+  return layout(dm, K).total;
+}
+
+int xmod_reset_status(void* ws, size_t ws_bytes, void* stream) {
+  if (!aligned16(ws) || ws_bytes < kAlign) return XMOD_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, sizeof(int), (cudaStream_t)stream));
+}
+
+int xmod_sync_status(void* ws, void* stream) {
+  if (!aligned16(ws)) return XMOD_ERR_WORKSPACE;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return XMOD_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return XMOD_ERR_CUDA;
+  return h;
+}
+
+int xmod_router_topk(const xmod_dims* dm, int K, const void* x, const void* w_r,
+                     const float* bias, float* logits, float* r, int32_t* idx, float* r_sel,
+                     void* ws, size_t ws_bytes, void* stream) {
+  if (!dims_ok(dm) || K <= 0 || K > dm->T) return XMOD_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_r) || !aligned16(idx) || !aligned16_or_null(bias) ||
+      !aligned16_or_null(logits) || !aligned16_or_null(r) || !aligned16_or_null(r_sel))
+    return XMOD_ERR_INVALID_ARG;
+  if (dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
+  int st = check_ws(dm, K, ws, ws_bytes);
+  if (st) return st;
+  const Layout L = layout(dm, K);
+  Ctx c{(cudaStream_t)stream, (int*)at(ws, L.status)};
+  float* s = logits ? logits : (float*)at(ws, L.s);
+  XMOD_RUN("router", launch_router(c, dm->dtype, (int64_t)dm->B * dm->T, dm->d, x, w_r, bias, s, r));
+  XMOD_RUN("topk", launch_topk(c, dm->B, dm->T, dm->T / K, s, idx, r_sel));
+  return XMOD_OK;
+}
+
+int xmod_topk(const xmod_dims* dm, int K, const float* logits, int32_t* idx, float* r_sel,
+              void* ws, size_t ws_bytes, void* stream) {
+  if (!dims_ok(dm) || K <= 0 || K > dm->T) return XMOD_ERR_INVALID_ARG;
+  if (!aligned16(logits) || !aligned16(idx) || !aligned16_or_null(r_sel))
+    return XMOD_ERR_INVALID_ARG;
+  if (dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
+  int st = check_ws(dm, K, ws, ws_bytes);
+  if (st) return st;
+  const Layout L = layout(dm, K);
+  Ctx c{(cudaStream_t)stream, (int*)at(ws, L.status)};
+  XMOD_RUN("topk", launch_topk(c, dm->B, dm->T, dm->T / K, logits, idx, r_sel));
+  return XMOD_OK;
+}
+
+int xmod_gather(const xmod_dims* dm, int K, const void* x, const int32_t* idx, void* xs,
+                void* stream) {
+  if (!dims_ok(dm) || K <= 0 || K > dm->T) return XMOD_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(idx) || !aligned16(xs)) return XMOD_ERR_INVALID_ARG;
+  Ctx c{(cudaStream_t)stream, nullptr};
+  XMOD_RUN("gather", launch_gather(c, dm->dtype, dm->B, dm->T, dm->T / K, dm->d, x, idx, xs));
+  return XMOD_OK;
+}
+
+int xmod_block_fwd(const xmod_dims* dm, int n_per_seq, const void* xs, const int32_t* idx,
+                   const xmod_layer_weights* w, void* a_out, void* f_out, void* ws,
+                   size_t ws_bytes, void* stream) {
+  if (!dims_ok(dm) || n_per_seq <= 0 || n_per_seq > dm->T) return XMOD_ERR_INVALID_ARG;
+  if (!aligned16(xs) || !aligned16_or_null(idx) || !aligned16(a_out) || !aligned16(f_out) ||
+      !weights_ok(w, false))
+    return XMOD_ERR_INVALID_ARG;
+  if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
+  const int K = dm->T / n_per_seq;
+  int st = check_ws(dm, K, ws, ws_bytes);
+  if (st) return st;
+  const Layout L = layout(dm, K);
+  Ctx c{(cudaStream_t)stream, (int*)at(ws, L.status)};
+  // Without idx the rows come from the compact buffer: view it as B sequences of
+  // n_per_seq tokens.
+  xmod_dims local = *dm;
+  if (!idx) local.T = n_per_seq;
+  return run_block(c, &local, L, ws, n_per_seq, xs, idx, w, a_out, f_out, false, nullptr,
+                   nullptr, -1);
+}
+
+int xmod_gated_scatter(const xmod_dims* dm, int K, void* x_inout, const int32_t* idx,
+                       const float* r_sel, const void* a, const void* f, float varsigma,
+                       xmod_gate gate, void* stream) {
+  if (!dims_ok(dm) || K <= 0 || K > dm->T) return XMOD_ERR_INVALID_ARG;
+  if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
+  if (!aligned16(x_inout) || !aligned16(idx) || !aligned16(r_sel) || !aligned16(a) ||
+      !aligned16_or_null(f) || !isfinite(varsigma))
+    return XMOD_ERR_INVALID_ARG;
+  if (!f && gate != XMOD_GATE_XMOD) return XMOD_ERR_INVALID_ARG;
+  Ctx c{(cudaStream_t)stream, nullptr};
+  XMOD_RUN("gated_scatter", launch_gated_scatter(c, dm->dtype, dm->B, dm->T, dm->T / K, dm->d,
+                                                 x_inout, idx, r_sel, a, f, varsigma, (int)gate));
+  return XMOD_OK;
+}
+
+int xmod_layer_fwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
+                   const xmod_layer_weights* w, void* x_inout, const float* bias,
+                   int32_t* idx_out, float* r_sel_out, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims_ok(dm)) return XMOD_ERR_INVALID_ARG;
+  if (kind != XMOD_LAYER_DENSE && kind != XMOD_LAYER_SPARSE) return XMOD_ERR_INVALID_ARG;
+  if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
+  if (kind == XMOD_LAYER_SPARSE && (K <= 0 || K > dm->T)) return XMOD_ERR_INVALID_ARG;
+  if (!aligned16(x_inout) || !aligned16_or_null(bias) || !aligned16_or_null(idx_out) ||
+      !aligned16_or_null(r_sel_out) || !weights_ok(w, kind == XMOD_LAYER_SPARSE))
+    return XMOD_ERR_INVALID_ARG;
+  if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
+  if (kind == XMOD_LAYER_SPARSE && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
+  const int Kw = kind == XMOD_LAYER_SPARSE ? K : 1;
+  int st = check_ws(dm, Kw, ws, ws_bytes);
+  if (st) return st;
+  return layer_impl(dm, kind, Kw, gate, w, x_inout, bias, idx_out, r_sel_out, ws, layout(dm, Kw),
+                    (cudaStream_t)stream);
+}
+
+int xmod_stack_fwd(const xmod_dims* dm, int K, double A, int N0, int N1, xmod_gate gate,
+                   const xmod_layer_weights* layers, int n_layers, void* x_inout,
+                   const float* bias, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims_ok(dm) || K <= 0 || K > dm->T || N0 < 0 || N1 < 0 || !layers) return XMOD_ERR_INVALID_ARG;
+  if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
+  if (!isfinite(A) || A <= 0) return XMOD_ERR_INVALID_ARG;
+  const double akd = A * (double)K;
+  const long AK = lround(akd);
+  if (AK < 1 || fabs(akd - (double)AK) > 1e-9) return XMOD_ERR_INVALID_ARG;
+  if ((long)n_layers != (long)N0 + (long)N1 * (AK + 1)) return XMOD_ERR_INVALID_ARG;
+  if (!aligned16(x_inout) || !aligned16_or_null(bias)) return XMOD_ERR_INVALID_ARG;
+  // Eq. 3 order: N0 dense, then N1 blocks of AK sparse layers and one dense anchor.
+  for (int l = 0; l < n_layers; ++l) {
+    const bool sparse = l >= N0 && ((l - N0) % (AK + 1)) < AK;
+    if (!weights_ok(&layers[l], sparse)) return XMOD_ERR_INVALID_ARG;
+  }
+  if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
+  if (N1 > 0 && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
+  int st = check_ws(dm, K, ws, ws_bytes);
+  if (st) return st;
+  const Layout L = layout(dm, K);
+  for (int l = 0; l < n_layers; ++l) {
+    const bool sparse = l >= N0 && ((l - N0) % (AK + 1)) < AK;
+    st = layer_impl(dm, sparse ? XMOD_LAYER_SPARSE : XMOD_LAYER_DENSE, K, gate, &layers[l],
+                    x_inout, bias, nullptr, nullptr, ws, L, (cudaStream_t)stream);
+    if (st) return st;
+  }
+  return XMOD_OK;
+}
+
+}  // extern "C"

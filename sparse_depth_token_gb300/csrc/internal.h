@@ -1,0 +1,104 @@
+// Host-side launchers shared between the translation units of the library.
+// Every launcher only enqueues work on ctx.stream and returns the launch status.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "xmod.h"
+
+namespace xmod {
+
+struct Ctx {
+  cudaStream_t stream;
+  int* status;  // device status word (first error wins)
+};
+
+// ---------------------------------------------------------------- measurement
+
+void count_launch();
+
+// Records a CUDA event pair around one launch on `s` while profiling is enabled.
+class ProfScope {
+ public:
+  ProfScope(const char* kind, cudaStream_t s);
+  ~ProfScope();
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
+
+ private:
+  const char* kind_;
+  cudaStream_t stream_;
+  cudaEvent_t start_ = nullptr;
+};
+
+// ---------------------------------------------------------------- routing and row kernels
+
+// s[i] = w_r . x_i + bias[i] (fp32), r[i] = sigmoid(s[i]) if r != NULL.
+cudaError_t launch_router(const Ctx& c, xmod_dtype dt, int64_t rows, int d, const void* x,
+                          const void* w_r, const float* bias, float* s, float* r);
+
+// Largest topk supported T (keys held in shared memory).
+int topk_max_T();
+// Per-sequence top-n of s [B, T]; ties to the lower position; ascending idx [B, n].
+// r_sel [B, n] = sigmoid(s at idx) if not NULL.
+cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32_t* idx,
+                        float* r_sel);
+
+// xs[b*n + j] = x[b, idx[b, j]] (idx NULL: identity, n == T).
+cudaError_t launch_gather(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
+                          const void* x, const int32_t* idx, void* xs);
+
+// u[b*n + j] = RMSNorm(x[b, idx[b, j]]) * gamma (idx NULL: identity).
+cudaError_t launch_gather_rmsnorm(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
+                                  const void* x, const int32_t* idx, const void* gamma,
+                                  float eps, void* u);
+
+// Gated residual in place, see xmod_gated_scatter. gate < 0: dense update x + a + f.
+cudaError_t launch_gated_scatter(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
+                                 void* x, const int32_t* idx, const float* r_sel, const void* a,
+                                 const void* f, float varsigma, int gate);
+
+// ---------------------------------------------------------------- GEMM with fused epilogues
+
+enum EpiKind {
+  EPI_STORE = 0,         // out[m, n] = acc
+  EPI_OPROJ = 1,         // out[m, n] = a = acc; out2[m, n] = h = x_row(m)[n] + acc
+  EPI_SWIGLU = 2,        // out[m, n] = silu(acc_gate) * acc_up
+  EPI_DOWN_SCATTER = 3,  // x_row(m)[n] = gated residual of (a[m, n], f = acc)
+};
+
+// Compact row m of a block belongs to sequence b = m / n_per_seq at position
+// t = idx ? idx[m] : m % n_per_seq; its stream row is x[(b * T + t) * d].
+struct Epilogue {
+  int kind = EPI_STORE;
+  void* out = nullptr;
+  int ldo = 0;
+  void* out2 = nullptr;
+  int ldo2 = 0;
+  void* x = nullptr;            // residual stream [B, T, d] (read for OPROJ, updated for DOWN)
+  const int32_t* idx = nullptr;
+  int T = 0, n_per_seq = 0, d = 0;
+  const void* a = nullptr;      // DOWN: attention residual [M, d]
+  const float* r_sel = nullptr; // DOWN: gates [M]
+  float varsigma = 1.0f;
+  int gate = -1;                // DOWN: XMOD_GATE_XMOD, XMOD_GATE_MOD, or -1 for dense
+};
+
+// C[M, N] = A[M, K] . B[N, K]^T (fp32 accumulate), then the epilogue. For
+// EPI_SWIGLU, B2 [N, K] is the up projection and B the gate projection.
+cudaError_t launch_gemm_simt(const Ctx& c, xmod_dtype dt, int M, int N, int K, const void* A,
+                             int lda, const void* B, int ldb, const void* B2,
+                             const Epilogue& e);
+
+// ---------------------------------------------------------------- attention
+
+// Causal GQA attention within each of B sequences of n tokens.
+// q [B*n, ldq] (head h at column h*hd), k and v [B*n, ldkv] (KV head g at g*hd),
+// o [B*n, hq*hd].
+cudaError_t launch_attention_simt(const Ctx& c, xmod_dtype dt, int B, int n, int hq, int hkv,
+                                  int hd, const void* q, int ldq, const void* k, const void* v,
+                                  int ldkv, void* o);
+
+}  // namespace xmod

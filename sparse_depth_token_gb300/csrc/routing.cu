@@ -1,0 +1,406 @@
+// Memory-bound kernels of a sparse layer: router GEMV, per-sequence top-(T/K)
+// selection, position-ordered gather (optionally fused with RMSNorm), and the
+// gated residual scatter.
+//
+// Sources: "X-MoD: Practical Scaling Laws for Sparse-Depth Routing Beyond
+// Mixture-of-Depths" reading notes -- Eq. 8 (router logit with token bias,
+// sigmoid gate), section "MoD structural limit" (top-1/K tokens per sequence),
+// Eq. 6 and Eq. 7 (gated residuals); "Mixture-of-Depths explained" -- the
+// MoDLayer listing (floor(T * ratio) tokens, position-ordered boolean gather).
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace xmod {
+
+// ================================================================ router GEMV
+//
+// One warp per token row, 16-byte streaming loads of x (read exactly once), the
+// router vector staged once per CTA in shared memory as fp32.
+
+constexpr int ROUTER_WARPS = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(ROUTER_WARPS * 32)
+router_kernel(int64_t rows, int d, const T* __restrict__ x, const T* __restrict__ w_r,
+              const float* __restrict__ bias, float* __restrict__ s, float* __restrict__ r) {
+  extern __shared__ float4 wsh4[];
+  float* wsh = reinterpret_cast<float*>(wsh4);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) wsh[i] = ld_f(w_r + i);
+  __syncthreads();
+  constexpr int V = Vec16<T>::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * ROUTER_WARPS;
+  for (int64_t row = (int64_t)blockIdx.x * ROUTER_WARPS + warp; row < rows; row += stride) {
+    const T* xr = x + row * d;
+    float acc0 = 0.f, acc1 = 0.f;
+    int c = lane * V;
+    // two independent 16-byte loads in flight per lane per iteration
+    for (; c + 32 * V < d; c += 64 * V) {
+      Vec16<T> v0 = ld_vec_stream(xr + c);
+      Vec16<T> v1 = ld_vec_stream(xr + c + 32 * V);
+#pragma unroll
+      for (int e = 0; e < V; e += 4) {
+        float4 w0 = *reinterpret_cast<const float4*>(wsh + c + e);
+        float4 w1 = *reinterpret_cast<const float4*>(wsh + c + 32 * V + e);
+        acc0 = fmaf(v0.get(e), w0.x, acc0);
+        acc0 = fmaf(v0.get(e + 1), w0.y, acc0);
+        acc0 = fmaf(v0.get(e + 2), w0.z, acc0);
+        acc0 = fmaf(v0.get(e + 3), w0.w, acc0);
+        acc1 = fmaf(v1.get(e), w1.x, acc1);
+        acc1 = fmaf(v1.get(e + 1), w1.y, acc1);
+        acc1 = fmaf(v1.get(e + 2), w1.z, acc1);
+        acc1 = fmaf(v1.get(e + 3), w1.w, acc1);
+      }
+    }
+    for (; c < d; c += 32 * V) {
+      Vec16<T> v0 = ld_vec_stream(xr + c);
+#pragma unroll
+      for (int e = 0; e < V; e += 4) {
+        float4 w0 = *reinterpret_cast<const float4*>(wsh + c + e);
+        acc0 = fmaf(v0.get(e), w0.x, acc0);
+        acc0 = fmaf(v0.get(e + 1), w0.y, acc0);
+        acc0 = fmaf(v0.get(e + 2), w0.z, acc0);
+        acc0 = fmaf(v0.get(e + 3), w0.w, acc0);
+      }
+    }
+    float acc = warp_sum(acc0 + acc1);
+    if (lane == 0) {
+      if (bias) acc += bias[row];
+      s[row] = acc;
+      if (r) r[row] = sigmoidf_acc(acc);
+    }
+  }
+}
+
+static int g_num_sms = 0;
+static int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 1;
+  }
+  return g_num_sms;
+}
+
+cudaError_t launch_router(const Ctx& c, xmod_dtype dt, int64_t rows, int d, const void* x,
+                          const void* w_r, const float* bias, float* s, float* r) {
+  if (rows <= 0) return cudaSuccess;
+  int64_t blocks = (rows + ROUTER_WARPS - 1) / ROUTER_WARPS;
+  const int64_t cap = (int64_t)num_sms() * 8;  // 8 resident CTAs of 256 threads per SM
+  if (blocks > cap) blocks = cap;
+  const size_t smem = sizeof(float) * (size_t)d;
+  if (dt == XMOD_BF16) {
+    auto k = router_kernel<__nv_bfloat16>;
+    if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k<<<(unsigned)blocks, ROUTER_WARPS * 32, smem, c.stream>>>(
+        rows, d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)w_r, bias, s, r);
+  } else {
+    auto k = router_kernel<float>;
+    if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k<<<(unsigned)blocks, ROUTER_WARPS * 32, smem, c.stream>>>(rows, d, (const float*)x,
+                                                               (const float*)w_r, bias, s, r);
+  }
+  return cudaGetLastError();
+}
+
+// ================================================================ top-(T/K)
+//
+// One CTA per sequence. Logits become order-preserving 32-bit keys in shared
+// memory (-0 folded onto +0, so equal values compare equal). A 4-pass, 8-bit
+// radix select finds the n-th largest key K* and how many of the keys equal to
+// K* are taken; since ties go to the lower position, those are the first
+// `remaining` equal keys in position order. A warp-ballot compaction then emits
+// the selected positions in ascending order.
+
+constexpr int TOPK_THREADS = 1024;
+constexpr int TOPK_MAX_T = 48 * 1024;  // 192 KB of keys in shared memory
+
+int topk_max_T() { return TOPK_MAX_T; }
+
+__device__ __forceinline__ uint32_t order_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u & 0x7fffffffu) == 0u) u = 0u;  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive scan of one value per warp (32 warps), result broadcast to the warp.
+__device__ __forceinline__ uint32_t warps_exclusive_scan(uint32_t v, uint32_t* sh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t t = sh[lane];
+    uint32_t inc = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    sh[lane] = inc - t;
+  }
+  __syncthreads();
+  uint32_t r = sh[warp];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(TOPK_THREADS)
+topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx,
+            float* __restrict__ r_sel, int* status) {
+  extern __shared__ uint32_t keys[];
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t scan_sh[32];
+  __shared__ uint32_t sh_prefix, sh_remaining;
+  __shared__ int sh_bad;
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* sb = s + (int64_t)b * T;
+  if (threadIdx.x == 0) sh_bad = 0;
+  __syncthreads();
+  for (int t = threadIdx.x; t < T; t += TOPK_THREADS) {
+    const float v = sb[t];
+    if (!isfinite(v)) sh_bad = 1;
+    keys[t] = order_key(v);
+  }
+  __syncthreads();
+  if (sh_bad && threadIdx.x == 0) report_status(status, XMOD_ERR_DEVICE_CHECK);
+
+  uint32_t prefix = 0u, mask = 0u, remaining = (uint32_t)n;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += TOPK_THREADS) hist[i] = 0u;
+    __syncthreads();
+    for (int t = threadIdx.x; t < T; t += TOPK_THREADS) {
+      const uint32_t k = keys[t];
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 0xffu], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits 255-8l .. 248-8l (descending)
+      uint32_t cnt[8], tot = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        cnt[e] = hist[255 - (lane * 8 + e)];
+        tot += cnt[e];
+      }
+      uint32_t inc = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      const uint32_t excl = inc - tot;
+      if (excl < remaining && remaining <= inc) {
+        uint32_t run = excl;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (run + cnt[e] >= remaining) {
+            const uint32_t D = 255u - (uint32_t)(lane * 8 + e);
+            sh_prefix = prefix | (D << shift);
+            sh_remaining = remaining - run;
+            break;
+          }
+          run += cnt[e];
+        }
+      }
+    }
+    __syncthreads();
+    prefix = sh_prefix;
+    remaining = sh_remaining;
+    mask |= 0xffu << shift;
+    __syncthreads();
+  }
+  const uint32_t kth = prefix;
+
+  // Warp w owns positions [w*W, (w+1)*W), visited 32 at a time in order.
+  const int W = ((T + TOPK_THREADS - 1) / TOPK_THREADS) * 32;
+  const int lo = warp * W;
+  const int hi = min(T, lo + W);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint32_t my_eq = 0;
+  for (int base = lo; base < hi; base += 32) {
+    const int t = base + lane;
+    const bool eq = t < hi && keys[t] == kth;
+    my_eq += __popc(__ballot_sync(0xffffffffu, eq));
+  }
+  const uint32_t eq_before = warps_exclusive_scan(my_eq, scan_sh);
+  uint32_t eq_run = eq_before, my_sel = 0;
+  for (int base = lo; base < hi; base += 32) {
+    const int t = base + lane;
+    const uint32_t k = t < hi ? keys[t] : 0u;
+    const bool eq = t < hi && k == kth;
+    const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+    const bool sel = t < hi && (k > kth || (eq && eq_run + __popc(eqm & lt_mask) < remaining));
+    my_sel += __popc(__ballot_sync(0xffffffffu, sel));
+    eq_run += __popc(eqm);
+  }
+  uint32_t out = warps_exclusive_scan(my_sel, scan_sh);
+  eq_run = eq_before;
+  for (int base = lo; base < hi; base += 32) {
+    const int t = base + lane;
+    const uint32_t k = t < hi ? keys[t] : 0u;
+    const bool eq = t < hi && k == kth;
+    const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+    const bool sel = t < hi && (k > kth || (eq && eq_run + __popc(eqm & lt_mask) < remaining));
+    const uint32_t selm = __ballot_sync(0xffffffffu, sel);
+    if (sel) {
+      const uint32_t o = out + __popc(selm & lt_mask);
+      if (o < (uint32_t)n) {
+        idx[(int64_t)b * n + o] = t;
+        if (r_sel) r_sel[(int64_t)b * n + o] = sigmoidf_acc(sb[t]);
+      }
+    }
+    out += __popc(selm);
+    eq_run += __popc(eqm);
+  }
+}
+
+cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32_t* idx,
+                        float* r_sel) {
+  if (B <= 0) return cudaSuccess;
+  const size_t smem = sizeof(uint32_t) * (size_t)T;
+  cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)(sizeof(uint32_t) * TOPK_MAX_T));
+  topk_kernel<<<B, TOPK_THREADS, smem, c.stream>>>(T, n, s, idx, r_sel, c.status);
+  return cudaGetLastError();
+}
+
+// ================================================================ gather (+ RMSNorm)
+
+constexpr int ROW_WARPS = 8;
+
+__device__ __forceinline__ int64_t stream_row(int64_t m, int T, int n, const int32_t* idx) {
+  const int64_t b = m / n;
+  const int64_t t = idx ? (int64_t)idx[m] : (m - b * n);
+  return b * T + t;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+gather_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
+              const int32_t* __restrict__ idx, T* __restrict__ xs) {
+  constexpr int V = Vec16<T>::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
+  if (m >= M) return;
+  const T* src = x + stream_row(m, seqT, n, idx) * d;
+  T* dst = xs + m * d;
+  for (int c = lane * V; c < d; c += 32 * V) st_vec(dst + c, ld_vec(src + c));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+gather_rmsnorm_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
+                      const int32_t* __restrict__ idx, const T* __restrict__ gamma, float eps,
+                      T* __restrict__ u) {
+  constexpr int V = Vec16<T>::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
+  if (m >= M) return;
+  const T* src = x + stream_row(m, seqT, n, idx) * d;
+  float ss = 0.f;
+  for (int c = lane * V; c < d; c += 32 * V) {
+    Vec16<T> v = ld_vec(src + c);
+#pragma unroll
+    for (int e = 0; e < V; ++e) ss = fmaf(v.get(e), v.get(e), ss);
+  }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)d + eps);
+  T* dst = u + m * d;
+  for (int c = lane * V; c < d; c += 32 * V) {
+    Vec16<T> v = ld_vec(src + c);
+    Vec16<T> g = ld_vec(gamma + c);
+    Vec16<T> o;
+#pragma unroll
+    for (int e = 0; e < V; ++e) o.set(e, v.get(e) * inv * g.get(e));
+    st_vec(dst + c, o);
+  }
+}
+
+cudaError_t launch_gather(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
+                          const void* x, const int32_t* idx, void* xs) {
+  const int64_t M = (int64_t)B * n;
+  if (M <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
+  if (dt == XMOD_BF16)
+    gather_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+        M, T, n, d, (const __nv_bfloat16*)x, idx, (__nv_bfloat16*)xs);
+  else
+    gather_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(M, T, n, d, (const float*)x, idx,
+                                                          (float*)xs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rmsnorm(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
+                                  const void* x, const int32_t* idx, const void* gamma,
+                                  float eps, void* u) {
+  const int64_t M = (int64_t)B * n;
+  if (M <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
+  if (dt == XMOD_BF16)
+    gather_rmsnorm_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+        M, T, n, d, (const __nv_bfloat16*)x, idx, (const __nv_bfloat16*)gamma, eps,
+        (__nv_bfloat16*)u);
+  else
+    gather_rmsnorm_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+        M, T, n, d, (const float*)x, idx, (const float*)gamma, eps, (float*)u);
+  return cudaGetLastError();
+}
+
+// ================================================================ gated scatter
+
+template <typename T>
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+gated_scatter_kernel(int64_t M, int seqT, int n, int d, T* __restrict__ x,
+                     const int32_t* __restrict__ idx, const float* __restrict__ r_sel,
+                     const T* __restrict__ a, const T* __restrict__ f, float varsigma, int gate) {
+  constexpr int V = Vec16<T>::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
+  if (m >= M) return;
+  T* row = x + stream_row(m, seqT, n, idx) * d;
+  const float r = (gate >= 0) ? r_sel[m] : 1.0f;
+  const float g7 = varsigma * r;
+  for (int c = lane * V; c < d; c += 32 * V) {
+    Vec16<T> xv = ld_vec(row + c);
+    Vec16<T> av = ld_vec_stream(a + m * d + c);
+    Vec16<T> o;
+    if (f) {
+      Vec16<T> fv = ld_vec_stream(f + m * d + c);
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        const float xa = xv.get(e), aa = av.get(e), ff = fv.get(e);
+        float y;
+        if (gate == XMOD_GATE_XMOD) y = xa + g7 * (aa + ff);       // Eq. 7
+        else if (gate == XMOD_GATE_MOD) y = xa + aa + r * ff;      // Eq. 6
+        else y = xa + aa + ff;                                      // dense layer
+        o.set(e, y);
+      }
+    } else {  // a holds a + f (Eq. 7 only)
+#pragma unroll
+      for (int e = 0; e < V; ++e) o.set(e, xv.get(e) + g7 * av.get(e));
+    }
+    st_vec(row + c, o);
+  }
+}
+
+cudaError_t launch_gated_scatter(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
+                                 void* x, const int32_t* idx, const float* r_sel, const void* a,
+                                 const void* f, float varsigma, int gate) {
+  const int64_t M = (int64_t)B * n;
+  if (M <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
+  if (dt == XMOD_BF16)
+    gated_scatter_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+        M, T, n, d, (__nv_bfloat16*)x, idx, r_sel, (const __nv_bfloat16*)a,
+        (const __nv_bfloat16*)f, varsigma, gate);
+  else
+    gated_scatter_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+        M, T, n, d, (float*)x, idx, r_sel, (const float*)a, (const float*)f, varsigma, gate);
+  return cudaGetLastError();
+}
+
+}  // namespace xmod

@@ -1,0 +1,140 @@
+"""GPU parity of the Eq. 3 stack against the CPU oracle, through the C ABI.
+
+End to end on the tiny fp32 stack; layer by layer (teacher-forced) on bf16
+stacks, including the A4K8 block at its full size in the launch configuration
+the benchmark times, where the oracle computes sampled rows one by one."""
+import numpy as np
+import pytest
+
+import oracle as O
+from oracle import structure as S
+from sparse_depth_token_gb300 import inputs as I
+from tests import _util as U
+from tests._gpu import (dev_layer, from_dev, need_gpu, oracle_dims, oracle_layer, to_dev, torch,
+                        workspace, xmod_dims)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def X():
+    need_gpu()
+    from sparse_depth_token_gb300 import xmod
+    xmod.load()
+    return xmod
+
+
+def _setup(X, w: I.Workload, n_layers=None):
+    layers = I.all_layer_weights(w, n_layers)
+    kinds = S.schedule(w.N0, w.N1, w.A, w.K)
+    assert len(kinds) == len(layers)
+    bias = I.router_bias(w)
+    x = I.residual_stream(w)
+    first_sparse = kinds.index(S.SPARSE)
+    x, _ = U.enforce_routing_margin(x, w.dtype, layers[first_sparse]["w_r"], bias, w.K)
+    dev = [dev_layer(l, w.dtype) for l in layers]
+    abi = [X.layer_weights(d, l["varsigma"]) for d, l in zip(dev, layers)]
+    return layers, kinds, bias, x, dev, abi
+
+
+def test_tiny_fp32_stack_end_to_end(X):
+    w = I.WORKLOADS["tiny_fp32"]
+    layers, kinds, bias, x, dev, abi = _setup(X, w)
+    dm = xmod_dims(w)
+    ws = workspace(dm, w.K)
+    xd = to_dev(x, "fp32")
+    bd = torch.from_numpy(bias).cuda()
+    X.reset_status(ws)
+    X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, xd, bd, ws)
+    assert X.sync_status(ws) == X.OK
+    ref = O.stack_fwd(oracle_dims(w), w.K, w.gate, kinds, [oracle_layer(l, "fp32") for l in layers],
+                      I.to_f64(x, "fp32"), bias=bias)
+    U.assert_close(from_dev(xd, "fp32").reshape(ref.shape), ref, "fp32", "stack")
+
+
+def _teacher_forced(X, w, layers, kinds, bias, x, abi, check_layers, row_mask=None):
+    """Run the stack one layer at a time on the GPU; at the listed layers compare with
+    the oracle run on the GPU layer's own input. Returns the final GPU stream."""
+    dm = xmod_dims(w)
+    ws = workspace(dm, w.K)
+    od = oracle_dims(w)
+    xd = to_dev(x, w.dtype)
+    bd = torch.from_numpy(bias).cuda() if bias is not None else None
+    n = w.T // w.K
+    idx = torch.empty((w.B, n), dtype=torch.int32, device="cuda")
+    r_sel = torch.empty((w.B, n), dtype=torch.float32, device="cuda")
+    X.reset_status(ws)
+    for l, kind in enumerate(kinds):
+        x_in = from_dev(xd, w.dtype).reshape(w.B, w.T, w.d) if l in check_layers else None
+        X.layer_fwd(dm, kind, w.K, w.gate, abi[l], xd, bd, idx if kind else None,
+                    r_sel if kind else None, ws)
+        if l not in check_layers:
+            continue
+        assert X.sync_status(ws) == X.OK
+        L = oracle_layer(layers[l], w.dtype)
+        got = from_dev(xd, w.dtype).reshape(w.B, w.T, w.d)
+        force = None
+        if kind == S.SPARSE:
+            s, _ = O.router(x_in, I.to_f64(layers[l]["w_r"], w.dtype), bias)
+            gidx = idx.cpu().numpy()
+            differ = U.check_selection(gidx, s, n)
+            if l == kinds.index(S.SPARSE):
+                assert differ == 0, "first sparse layer has margin-fixed inputs: must be bit-exact"
+            force = gidx
+        ref = O.layer_fwd(od, kind, w.K, w.gate, L, x_in, bias=bias, idx_force=force,
+                          row_mask=row_mask)
+        m = np.ones((w.B, w.T), bool) if row_mask is None else row_mask.astype(bool)
+        if kind == S.SPARSE:
+            sel = np.zeros((w.B, w.T), bool)
+            np.put_along_axis(sel, force, True, 1)
+            np.testing.assert_array_equal(got[~sel], x_in[~sel])
+            m = m & sel
+        U.assert_close(got[m], ref["y"][m], w.dtype, f"layer {l} y")
+        U.assert_close(got[m] - x_in[m], ref["y"][m] - x_in[m], w.dtype, f"layer {l} update")
+    assert X.sync_status(ws) == X.OK
+    return xd, dm, ws
+
+
+def test_tiny_fp32_teacher_forced(X):
+    w = I.WORKLOADS["tiny_fp32"]
+    layers, kinds, bias, x, dev, abi = _setup(X, w)
+    _teacher_forced(X, w, layers, kinds, bias, x, abi, set(range(len(kinds))))
+
+
+@pytest.mark.parametrize("name", ["a4k8_bf16", "mod_bf16", "a3k16_bf16"])
+def test_bf16_stack_reduced_teacher_forced(X, name):
+    """The bf16 workloads at their widths and heads, shortened: B=2, T=512, one block."""
+    base = I.WORKLOADS[name]
+    if name == "a3k16_bf16":
+        w = base.replace(B=2, T=512, N0=1, N1=1, n_layers=1 + 49)
+    elif name == "mod_bf16":
+        w = base.replace(B=2, T=512, N1=2, n_layers=4)
+    else:
+        w = base.replace(B=2, T=512, A=1, n_layers=9)
+    layers, kinds, bias, x, dev, abi = _setup(X, w)
+    xd, dm, ws = _teacher_forced(X, w, layers, kinds, bias, x, abi, set(range(len(kinds))))
+    # the stack entry point reproduces the layer-by-layer result bit for bit
+    xs = to_dev(x, w.dtype)
+    X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, xs,
+                torch.from_numpy(bias).cuda() if bias is not None else None, ws)
+    assert X.sync_status(ws) == X.OK
+    assert torch.equal(xs.view(torch.int16), xd.view(torch.int16))
+
+
+@pytest.mark.slow
+def test_a4k8_full_size_sampled(X):
+    """A4K8 block (32 Sparse(8) + Dense, d=1536, B=8, T=4096) at full size: sampled rows of
+    the first, a middle and the last sparse layer and of the dense anchor."""
+    w = I.WORKLOADS["a4k8_bf16"]
+    layers, kinds, bias, x, dev, abi = _setup(X, w)
+    mask = np.zeros((w.B, w.T), np.int32)
+    g = np.random.default_rng(0)
+    for b in (0, w.B - 1):
+        mask[b, g.choice(w.T, 48, replace=False)] = 1
+        mask[b, :4] = 1
+        mask[b, -4:] = 1
+    xd, dm, ws = _teacher_forced(X, w, layers, kinds, bias, x, abi, {0, 16, 31, 32}, row_mask=mask)
+    xs = to_dev(x, w.dtype)
+    X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, xs, torch.from_numpy(bias).cuda(), ws)
+    assert X.sync_status(ws) == X.OK
+    assert torch.equal(xs.view(torch.int16), xd.view(torch.int16))

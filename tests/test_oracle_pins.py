@@ -431,3 +431,28 @@ def test_round_bf16_agrees_with_float32_path():
     ref = I.bf16_bits_to_f32(I.f32_to_bf16_bits(v)).astype(np.float64)
     got = np.array([O.round_bf16(float(t)) for t in v])
     np.testing.assert_array_equal(got, ref)
+
+
+def test_gated_scatter_matches_layer_residual():
+    """The standalone scatter step reproduces the layer's own residual on its selected rows."""
+    dm = _small_dims()
+    g = _rng(23)
+    L = O.Layer(_layer_arrays(g, dm.d, dm.hq, dm.hkv, dm.hd, dm.F), varsigma=1.1)
+    x = g.standard_normal((dm.B, dm.T, dm.d))
+    K = 4
+    for gate in (O.GATE_XMOD, O.GATE_MOD):
+        out = O.layer_fwd(dm, O.SPARSE, K, gate, L, x)
+        n = dm.T // K
+        rows = (np.arange(dm.B)[:, None] * dm.T + out["idx"]).reshape(-1)
+        a, f = [], []
+        for b in range(dm.B):
+            ab, fb = O.block(dm, x[b, out["idx"][b]], L)
+            a.append(ab)
+            f.append(fb)
+        a, f = np.concatenate(a), np.concatenate(f)
+        y = O.gated_scatter(x.reshape(-1, dm.d), rows, a, f, out["r_sel"].reshape(-1), 1.1, gate)
+        np.testing.assert_array_equal(y.reshape(x.shape), out["y"])
+        if gate == O.GATE_XMOD:   # a + f passed pre-summed
+            y2 = O.gated_scatter(x.reshape(-1, dm.d), rows, a + f, None, out["r_sel"].reshape(-1),
+                                 1.1, gate)
+            np.testing.assert_allclose(y2.reshape(x.shape), out["y"], rtol=1e-14, atol=1e-14)
