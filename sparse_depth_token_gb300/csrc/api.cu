@@ -51,8 +51,8 @@ Layout layout(const xmod_dims* dm, int K) {
   Layout L{};
   const size_t es = esize(dm->dtype);
   const size_t BT = (size_t)dm->B * dm->T;
-  const size_t n = (size_t)(dm->T / (K > 0 ? K : 1));
-  const size_t Bn = (size_t)dm->B * (n > 0 ? n : 1);
+  (void)K;  // one layout serves every K: selections are sized for n <= T
+  const size_t Bn = BT;
   const size_t M = BT;
   const size_t qkv_w = (size_t)(dm->n_heads + 2 * dm->n_kv_heads) * dm->head_dim;
   size_t off = 0;
@@ -63,7 +63,7 @@ Layout layout(const xmod_dims* dm, int K) {
   L.u = off;      off = align_up(off + es * M * dm->d);
   L.qkv = off;    off = align_up(off + es * M * qkv_w);
   L.o = off;      off = align_up(off + es * M * dm->n_heads * dm->head_dim);
-  L.a = off;      off = align_up(off + es * M * dm->d);
+  L.a = off;      off = align_up(off + 4 * M * dm->d);   // attention residual kept in fp32
   L.h = off;      off = align_up(off + es * M * dm->d);
   L.hidden = off; off = align_up(off + es * M * dm->d_ff);
   L.total = off;
@@ -133,6 +133,7 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   eo.kind = EPI_OPROJ;
   eo.out = a;
   eo.ldo = d;
+  eo.a_f32 = (a_out == nullptr);
   eo.out2 = h;
   eo.ldo2 = d;
   eo.x = (void*)x_src;
@@ -159,6 +160,7 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
     ed.n_per_seq = n;
     ed.d = d;
     ed.a = a;
+    ed.a_f32 = (a_out == nullptr);
     ed.r_sel = r_sel;
     ed.varsigma = w->varsigma;
     ed.gate = gate;

@@ -81,6 +81,7 @@ struct Epilogue {
   const int32_t* idx = nullptr;
   int T = 0, n_per_seq = 0, d = 0;
   const void* a = nullptr;      // DOWN: attention residual [M, d]
+  bool a_f32 = false;           // OPROJ writes / DOWN reads a as fp32 (else the element type)
   const float* r_sel = nullptr; // DOWN: gates [M]
   float varsigma = 1.0f;
   int gate = -1;                // DOWN: XMOD_GATE_XMOD, XMOD_GATE_MOD, or -1 for dense

@@ -133,8 +133,11 @@ def dims(B, T, d, n_heads, n_kv_heads, head_dim, d_ff, dtype=BF16, rms_eps=1e-6)
 
 
 def layer_weights(tensors: dict, varsigma: float = 1.0) -> LayerWeights:
-    """tensors: name -> device tensor for the names of LayerWeights.NAMES."""
-    return LayerWeights(*[_p(tensors.get(n)) for n in LayerWeights.NAMES], float(varsigma))
+    """tensors: name -> device tensor for the names of LayerWeights.NAMES. The struct
+    keeps a reference to the tensors so their memory outlives every call using it."""
+    lw = LayerWeights(*[_p(tensors.get(n)) for n in LayerWeights.NAMES], float(varsigma))
+    lw._keep = dict(tensors)
+    return lw
 
 
 def workspace_bytes(dm: Dims, K: int) -> int:
@@ -189,6 +192,7 @@ def layer_fwd(dm, kind, K, gate, w: LayerWeights, x, bias, idx_out, r_sel_out, w
 
 
 def stack_fwd(dm, K, A, N0, N1, gate, layers, x, bias, ws, stream=None):
+    # the array copies the structs; the caller's LayerWeights keep the tensors alive
     arr = (LayerWeights * len(layers))(*layers)
     _check("xmod_stack_fwd", load().xmod_stack_fwd(
         ctypes.byref(dm), int(K), float(A), int(N0), int(N1), int(gate), arr, len(layers), _p(x),

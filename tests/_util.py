@@ -25,13 +25,29 @@ def rel_l2(got, ref) -> float:
     return float(np.linalg.norm(got - ref) / (den if den > 0 else 1.0))
 
 
-def assert_close(got, ref, dtype: str, what: str = ""):
+def bf16_half_ulp(v) -> np.ndarray:
+    """Half the bf16 spacing at |v| (8 significant bits): the storage rounding of a bf16 output."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - 8), 0.0)
+
+
+def assert_close(got, ref, dtype: str, what: str = "", stored_ref=None):
+    """bf16: max-abs <= 2e-2 and rel-L2 <= 1e-2; fp32: relative 1e-5.
+
+    stored_ref: for a bf16 output that overwrites a bf16 tensor (the residual
+    stream), the values it is stored as; the max-abs bound then applies to the
+    arithmetic beyond the output's own storage rounding (half a bf16 spacing at
+    |stored_ref|, which by itself exceeds 2e-2 for |y| >= 8)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     if dtype == "bf16":
-        mx = float(np.max(np.abs(got - ref))) if got.size else 0.0
+        err = np.abs(got - ref)
+        if stored_ref is not None:
+            err = np.maximum(err - bf16_half_ulp(stored_ref), 0.0)
+        mx = float(np.max(err)) if got.size else 0.0
         rl = rel_l2(got, ref)
         assert mx <= BF16_MAX_ABS and rl <= BF16_REL_L2, f"{what}: max-abs {mx:.3e}, rel-L2 {rl:.3e}"
     else:
@@ -76,7 +92,15 @@ def enforce_routing_margin(x_store, dtype, w_r_store, bias, K, margin=ROUTING_MA
         for t in order[n:]:
             if s[t] < kth - 2 * margin:
                 break
-            for _ in range(100000):
+            bt = None if bias is None else np.array([bias[b, t]])
+            # jump most of the way, then step in storage precision until the gap holds
+            target = I.to_f64(x[b, t, mstar:mstar + 1], dtype)[0] - (
+                s[t] - (kth - 1.25 * margin)) / w64[mstar]
+            t32 = np.array([target], dtype=np.float32)
+            x[b, t, mstar] = I.f32_to_bf16_bits(t32)[0] if dtype == "bf16" else t32[0]
+            for _ in range(10000):
+                row = I.to_f64(x[b, t], dtype)
+                s[t] = O.router(row[None, :], w64, bt)[0][0]
                 if s[t] <= kth - margin:
                     break
                 if dtype == "bf16":
@@ -84,10 +108,7 @@ def enforce_routing_margin(x_store, dtype, w_r_store, bias, K, margin=ROUTING_MA
                 else:
                     x[b, t, mstar] = np.nextafter(x[b, t, mstar],
                                                   np.float32(np.inf if up else -np.inf))
-                row = I.to_f64(x[b, t], dtype)
-                s_t, _ = O.router(row[None, :], w64,
-                                  None if bias is None else np.array([bias[b, t]]))
-                s[t] = s_t[0]
+            assert s[t] <= kth - margin
             touched += 1
     return x, touched
 

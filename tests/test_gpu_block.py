@@ -120,5 +120,6 @@ def test_layer_fwd(X, case, kind, gate):
         np.testing.assert_array_equal(got[~sel], x64[~sel])   # skip path is bitwise identity
     else:
         sel = np.ones((w.B, w.T), bool)
-    U.assert_close(got, ref["y"], dt, "y")
-    U.assert_close(got[sel] - x64[sel], ref["y"][sel] - x64[sel], dt, "update")
+    U.assert_close(got, ref["y"], dt, "y", stored_ref=got)
+    U.assert_close(got[sel] - x64[sel], ref["y"][sel] - x64[sel], dt, "update",
+                   stored_ref=got[sel])

@@ -141,13 +141,15 @@ def test_gated_scatter(X, dtype, gate, fused_af):
     vs = 1.25
     dm = X.dims(B, T, d, 1, 1, 8, 8, X.BF16 if dtype == "bf16" else X.FP32)
     xd = to_dev(x, dtype)
+    af = conv((I.to_f64(a, dtype) + I.to_f64(f, dtype)).astype(np.float32))
     X.gated_scatter(dm, K, xd, torch.from_numpy(idx).cuda(), torch.from_numpy(r).cuda(),
-                    to_dev(a, dtype), None if fused_af else to_dev(f, dtype), vs, gate)
+                    to_dev(af if fused_af else a, dtype), None if fused_af else to_dev(f, dtype),
+                    vs, gate)
     torch.cuda.synchronize()
     rows = (np.arange(B)[:, None] * T + idx).reshape(-1)
     a64, f64 = I.to_f64(a, dtype), I.to_f64(f, dtype)
     if fused_af:
-        ref = O.gated_scatter(I.to_f64(x, dtype).reshape(-1, d), rows, a64 + f64, None,
+        ref = O.gated_scatter(I.to_f64(x, dtype).reshape(-1, d), rows, I.to_f64(af, dtype), None,
                               r.astype(np.float64), vs, gate)
     else:
         ref = O.gated_scatter(I.to_f64(x, dtype).reshape(-1, d), rows, a64, f64,

@@ -89,8 +89,9 @@ def _teacher_forced(X, w, layers, kinds, bias, x, abi, check_layers, row_mask=No
             np.put_along_axis(sel, force, True, 1)
             np.testing.assert_array_equal(got[~sel], x_in[~sel])
             m = m & sel
-        U.assert_close(got[m], ref["y"][m], w.dtype, f"layer {l} y")
-        U.assert_close(got[m] - x_in[m], ref["y"][m] - x_in[m], w.dtype, f"layer {l} update")
+        U.assert_close(got[m], ref["y"][m], w.dtype, f"layer {l} y", stored_ref=got[m])
+        U.assert_close(got[m] - x_in[m], ref["y"][m] - x_in[m], w.dtype, f"layer {l} update",
+                       stored_ref=got[m])
     assert X.sync_status(ws) == X.OK
     return xd, dm, ws
 
