@@ -75,19 +75,17 @@ def algorithmic_work(w: I.Workload) -> dict:
             add("router", w.B * w.T * w.d * es + 4 * w.B * w.T)
             add("topk", 4 * w.B * w.T + 8 * M)
         add("gather_rmsnorm", 2 * M * w.d * es)
-        add("gemm_q", 2 * M * w.d * w.hq * w.hd)
-        add("gemm_k", 2 * M * w.d * w.hkv * w.hd)
-        add("gemm_v", 2 * M * w.d * w.hkv * w.hd)
+        add("gemm_qkv", 2 * M * w.d * (w.hq + 2 * w.hkv) * w.hd)
         add("attention", 2 * w.B * n * n * w.hd * w.hq)
         add("gemm_o_residual", 2 * M * w.hq * w.hd * w.d)
-        add("rmsnorm2", 2 * M * w.d * es)
+        add("rmsnorm2", M * w.d * (4 + es))
         add("gemm_gate_up_swiglu", 4 * M * w.d * w.F)
         add("gemm_down_scatter", 2 * M * w.F * w.d)
     return out
 
 
-TENSOR_KINDS = {"gemm_q", "gemm_k", "gemm_v", "attention", "gemm_o_residual",
-                "gemm_gate_up_swiglu", "gemm_down_scatter"}
+TENSOR_KINDS = {"gemm_qkv", "attention", "gemm_o_residual", "gemm_gate_up_swiglu",
+                "gemm_down_scatter"}
 
 
 def measured_peaks() -> dict:

@@ -64,7 +64,7 @@ Layout layout(const xmod_dims* dm, int K) {
   L.qkv = off;    off = align_up(off + es * M * qkv_w);
   L.o = off;      off = align_up(off + es * M * dm->n_heads * dm->head_dim);
   L.a = off;      off = align_up(off + 4 * M * dm->d);   // attention residual kept in fp32
-  L.h = off;      off = align_up(off + es * M * dm->d);
+  L.h = off;      off = align_up(off + 4 * M * dm->d);   // h = x_sel + a kept in fp32
   L.hidden = off; off = align_up(off + es * M * dm->d_ff);
   L.total = off;
   return L;
@@ -116,18 +116,27 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   // 1. gather + RMSNorm1
   XMOD_RUN("gather_rmsnorm", launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms1, dm->rms_eps, u));
   // 2. q, k, v projections into one [M, qkv_w] buffer
+  const bool tc = dt == XMOD_BF16;
   Epilogue e;
   e.kind = EPI_STORE;
   e.ldo = qkv_w;
   e.out = qkv;
-  XMOD_RUN("gemm_q", launch_gemm_simt(c, dt, M, qw, d, u, d, w->wq, d, nullptr, e));
-  e.out = qkv + es * qw;
-  XMOD_RUN("gemm_k", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wk, d, nullptr, e));
-  e.out = qkv + es * (qw + kw);
-  XMOD_RUN("gemm_v", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wv, d, nullptr, e));
+  GemmTcProblem pq;
+  pq.M = M; pq.N = qkv_w; pq.K = d; pq.A = u; pq.lda = d; pq.ldb = d;
+  pq.B[0] = w->wq; pq.B[1] = w->wk; pq.B[2] = w->wv; pq.nB = 3;
+  pq.split[0] = qw; pq.split[1] = qw + kw;
+  if (tc && gemm_tc_supported(pq, e)) {
+    XMOD_RUN("gemm_qkv", launch_gemm_tc(c, pq, e));
+  } else {
+    XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, qw, d, u, d, w->wq, d, nullptr, e));
+    e.out = qkv + es * qw;
+    XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wk, d, nullptr, e));
+    e.out = qkv + es * (qw + kw);
+    XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wv, d, nullptr, e));
+  }
   // 3. causal GQA attention among the n rows of each sequence
   XMOD_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w, qkv + es * qw,
-                                 qkv + es * (qw + kw), qkv_w, o));
+                                              qkv + es * (qw + kw), qkv_w, o));
   // 4. a = o Wo^T, h = x_sel + a
   Epilogue eo;
   eo.kind = EPI_OPROJ;
@@ -141,15 +150,30 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   eo.T = T;
   eo.n_per_seq = n;
   eo.d = d;
-  XMOD_RUN("gemm_o_residual", launch_gemm_simt(c, dt, M, d, qw, o, qw, w->wo, qw, nullptr, eo));
-  // 5. v2 = RMSNorm(h) * rms2 (in place)
-  XMOD_RUN("rmsnorm2", launch_gather_rmsnorm(c, dt, 1, M, M, d, h, nullptr, w->rms2, dm->rms_eps, h));
+  GemmTcProblem po;
+  po.M = M; po.N = d; po.K = qw; po.A = o; po.lda = qw; po.ldb = qw; po.B[0] = w->wo;
+  if (tc && gemm_tc_supported(po, eo))
+    XMOD_RUN("gemm_o_residual", launch_gemm_tc(c, po, eo));
+  else
+    XMOD_RUN("gemm_o_residual", launch_gemm_simt(c, dt, M, d, qw, o, qw, w->wo, qw, nullptr, eo));
+  // 5. v2 = RMSNorm(h) * rms2
+  // (v2 reuses the buffer of u, which the q/k/v projection has consumed)
+  char* v2 = u;
+  XMOD_RUN("rmsnorm2", launch_rmsnorm_f32in(c, dt, M, d, (const float*)h, w->rms2, dm->rms_eps,
+                                            v2));
   // 6. hidden = silu(v2 Wg^T) * (v2 Wu^T)
   Epilogue eg;
   eg.kind = EPI_SWIGLU;
   eg.out = hidden;
   eg.ldo = F;
-  XMOD_RUN("gemm_gate_up_swiglu", launch_gemm_simt(c, dt, M, F, d, h, d, w->w_gate, d, w->w_up, eg));
+  GemmTcProblem pg;
+  pg.M = M; pg.N = F; pg.K = d; pg.A = v2; pg.lda = d; pg.ldb = d;
+  pg.B[0] = w->w_gate; pg.B[1] = w->w_up; pg.nB = 2;
+  if (tc && gemm_tc_supported(pg, eg))
+    XMOD_RUN("gemm_gate_up_swiglu", launch_gemm_tc(c, pg, eg));
+  else
+    XMOD_RUN("gemm_gate_up_swiglu",
+             launch_gemm_simt(c, dt, M, F, d, v2, d, w->w_gate, d, w->w_up, eg));
   // 7. f = hidden Wd^T, then the gated residual (or f stored)
   Epilogue ed;
   if (scatter) {
@@ -169,7 +193,13 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
     ed.out = f_out;
     ed.ldo = d;
   }
-  XMOD_RUN(scatter ? "gemm_down_scatter" : "gemm_down", launch_gemm_simt(c, dt, M, d, F, hidden, F, w->w_down, F, nullptr, ed));
+  GemmTcProblem pd;
+  pd.M = M; pd.N = d; pd.K = F; pd.A = hidden; pd.lda = F; pd.ldb = F; pd.B[0] = w->w_down;
+  const char* down_name = scatter ? "gemm_down_scatter" : "gemm_down";
+  if (tc && gemm_tc_supported(pd, ed))
+    XMOD_RUN(down_name, launch_gemm_tc(c, pd, ed));
+  else
+    XMOD_RUN(down_name, launch_gemm_simt(c, dt, M, d, F, hidden, F, w->w_down, F, nullptr, ed));
   return XMOD_OK;
 }
 

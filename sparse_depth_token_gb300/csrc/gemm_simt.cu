@@ -32,7 +32,7 @@ __device__ __forceinline__ void epilogue_store(const Epilogue& e, int M, int N, 
       const float xv = ld_f((const T*)e.x + (b * e.T + t) * e.d + n);
       if (e.a_f32) ((float*)e.out)[(int64_t)m * e.ldo + n] = acc;
       else st_f((T*)e.out + (int64_t)m * e.ldo + n, acc);
-      st_f((T*)e.out2 + (int64_t)m * e.ldo2 + n, xv + acc);
+      ((float*)e.out2)[(int64_t)m * e.ldo2 + n] = xv + acc;
       break;
     }
     case EPI_SWIGLU:

@@ -1,0 +1,468 @@
+// Tensor-core GEMM for sm_103a (tcgen05 + TMEM + TMA) with the block's fused
+// epilogues. bf16 operands, fp32 accumulation.
+//
+//   C[M, N] = A[M, K] . B[N, K]^T      (A activations, B weights in [out, in] layout)
+//
+// Persistent CTAs (one per SM) walk the output tiles; inside a CTA the work is
+// split by warp:
+//   warp 0      TMA producer: streams 128 x 64 A tiles and BN x 64 B tiles into a
+//               ring of shared-memory stages (128-byte swizzle)
+//   warp 1      allocates TMEM; one lane issues tcgen05.mma (128 x BN x 16) into one
+//               of two TMEM accumulators, committing each stage back to the producer
+//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one TMEM lane =
+//               one output row per thread), the fused epilogue math, global stores;
+//               the other accumulator is meanwhile filled by the next tile's MMAs.
+// Fused epilogues: plain store (optionally for q|k|v from three weight tensors),
+// O-projection (a and h = x_sel + a), SwiGLU (gate and up halves of one tile), and
+// the down projection's gated scatter back into the residual stream (Eq. 6 / Eq. 7
+// of the X-MoD notes) at the selected rows.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <limits.h>
+#include <string.h>
+
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace xmod {
+
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128, BK = 64;
+constexpr int NUM_THREADS = 192;
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+struct TcArgs {
+  int M, N, K;
+  int mode;            // EpiKind
+  int n_split1, n_split2;  // STORE: first accumulator column served by B map 1 / map 2
+  int tiles_m, tiles;
+  Epilogue e;
+  int* status;
+};
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+__device__ __forceinline__ int64_t stream_row_of(const Epilogue& e, int m) {
+  const int64_t b = m / e.n_per_seq;
+  const int64_t t = e.idx ? (int64_t)e.idx[m] : (m - b * e.n_per_seq);
+  return b * e.T + t;
+}
+
+// Store 32 fp32 values as bf16 at p[0..32), only the first `rem` columns.
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* p, const float (&v)[32], int rem) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (8 * g + 8 <= rem) {
+      uint4 q;
+      q.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
+      q.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
+      q.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
+      q.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
+      *reinterpret_cast<uint4*>(p + 8 * g) = q;
+    } else {
+      for (int i = 8 * g; i < rem && i < 8 * g + 8; ++i) p[i] = __float2bfloat16_rn(v[i]);
+    }
+  }
+}
+
+__device__ __forceinline__ void store32_f32(float* p, const float (&v)[32], int rem) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    if (4 * g + 4 <= rem) {
+      *reinterpret_cast<float4*>(p + 4 * g) =
+          make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+    } else {
+      for (int i = 4 * g; i < rem && i < 4 * g + 4; ++i) p[i] = v[i];
+    }
+  }
+}
+
+__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* p, float (&v)[32], int rem) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (8 * g + 8 <= rem) {
+      const uint4 q = *reinterpret_cast<const uint4*>(p + 8 * g);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v[8 * g + 2 * i] = f.x;
+        v[8 * g + 2 * i + 1] = f.y;
+      }
+    } else {
+      for (int i = 8 * g; i < 8 * g + 8; ++i) v[i] = i < rem ? __bfloat162float(p[i]) : 0.f;
+    }
+  }
+}
+
+__device__ __forceinline__ void load32_f32(const float* p, float (&v)[32], int rem) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    if (4 * g + 4 <= rem) {
+      const float4 q = *reinterpret_cast<const float4*>(p + 4 * g);
+      v[4 * g] = q.x;
+      v[4 * g + 1] = q.y;
+      v[4 * g + 2] = q.z;
+      v[4 * g + 3] = q.w;
+    } else {
+      for (int i = 4 * g; i < 4 * g + 4; ++i) v[i] = i < rem ? p[i] : 0.f;
+    }
+  }
+}
+
+// The epilogue of one tile for this thread's row m (TMEM lane row of t_row).
+// Every thread of the warp executes the TMEM loads (warp-collective); only rows
+// inside the matrix store.
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const TcArgs& a, int m, int n_blk, uint32_t t_row) {
+  const Epilogue& e = a.e;
+  const bool row_ok = m < a.M;
+  if (a.mode == EPI_SWIGLU) {
+    constexpr int HALF = BN / 2;
+#pragma unroll 1
+    for (int c = 0; c < HALF / 32; ++c) {
+      float g[32], u[32];
+      tmem_ld32(t_row + c * 32, g);
+      tmem_ld32(t_row + HALF + c * 32, u);
+      tmem_ld_wait();
+      const int n = n_blk * HALF + c * 32;
+      if (row_ok && n < a.N) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
+        store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + n, g, a.N - n);
+      }
+    }
+    return;
+  }
+  int64_t xrow = 0;
+  float r = 1.0f;
+  if (row_ok && (a.mode == EPI_OPROJ || a.mode == EPI_DOWN_SCATTER)) {
+    xrow = stream_row_of(e, m) * e.d;
+    if (a.mode == EPI_DOWN_SCATTER && e.gate >= 0) r = e.r_sel[m];
+  }
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld32(t_row + c * 32, v);
+    tmem_ld_wait();
+    const int n = n_blk * BN + c * 32;
+    if (!row_ok || n >= a.N) continue;
+    const int rem = a.N - n;
+    if (a.mode == EPI_STORE) {
+      store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + n, v, rem);
+    } else if (a.mode == EPI_OPROJ) {
+      float xv[32];
+      load32_bf16((const __nv_bfloat16*)e.x + xrow + n, xv, rem);
+      if (e.a_f32) store32_f32((float*)e.out + (int64_t)m * e.ldo + n, v, rem);
+      else store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + n, v, rem);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) xv[i] += v[i];
+      store32_f32((float*)e.out2 + (int64_t)m * e.ldo2 + n, xv, rem);
+    } else {  // EPI_DOWN_SCATTER
+      float xv[32], av[32];
+      __nv_bfloat16* xp = (__nv_bfloat16*)e.x + xrow + n;
+      load32_bf16(xp, xv, rem);
+      if (e.a_f32) load32_f32((const float*)e.a + (int64_t)m * e.d + n, av, rem);
+      else load32_bf16((const __nv_bfloat16*)e.a + (int64_t)m * e.d + n, av, rem);
+      if (e.gate == XMOD_GATE_XMOD) {
+        const float g7 = e.varsigma * r;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) xv[i] += g7 * (av[i] + v[i]);      // Eq. 7
+      } else if (e.gate == XMOD_GATE_MOD) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) xv[i] += av[i] + r * v[i];         // Eq. 6
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) xv[i] += av[i] + v[i];             // dense layer
+      }
+      store32_bf16(xp, xv, rem);
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+               const TcArgs args) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = base + C::STAGES * C::A_BYTES;
+  const uint32_t sBar = sB + C::STAGES * C::B_BYTES;
+  const uint32_t sTmem = sBar + 8 * (2 * C::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (sTmem - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (sTmem - base) + 8);
+#define FULL(s) (sBar + 8u * (s))
+#define EMPTY(s) (sBar + 8u * (C::STAGES + (s)))
+#define ACC_FULL(a) (sBar + 8u * (2 * C::STAGES + (a)))
+#define ACC_EMPTY(a) (sBar + 8u * (2 * C::STAGES + 2 + (a)))
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = (args.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(FULL(s), 1);
+      mbar_init(EMPTY(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(ACC_FULL(a), 1);
+      mbar_init(ACC_EMPTY(a), 128);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB0);
+    if (args.mode == EPI_SWIGLU || args.n_split1 < args.N) prefetch_tensormap(&tmB1);
+    if (args.mode != EPI_SWIGLU && args.n_split2 < args.N) prefetch_tensormap(&tmB2);
+  }
+  if (warp == 1) tmem_alloc(sTmem, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      for (int tile = blockIdx.x; tile < args.tiles && !*abort_flag; tile += gridDim.x) {
+        const int m0 = (tile % args.tiles_m) * BM;
+        const int n_blk = tile / args.tiles_m;
+        const CUtensorMap* mp = &tmB0;
+        int brow = n_blk * BN;
+        if (args.mode != EPI_SWIGLU) {
+          if (brow >= args.n_split2) {
+            mp = &tmB2;
+            brow -= args.n_split2;
+          } else if (brow >= args.n_split1) {
+            mp = &tmB1;
+            brow -= args.n_split1;
+          }
+        }
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+          if (!mbar_wait(EMPTY(s), ph ^ 1u, abort_flag, args.status)) break;
+          mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
+          tma_load_2d(sA + s * C::A_BYTES, &tmA, FULL(s), kb * BK, m0);
+          if (args.mode == EPI_SWIGLU) {
+            const int h0 = n_blk * (BN / 2);
+            tma_load_2d(sB + s * C::B_BYTES, &tmB0, FULL(s), kb * BK, h0);
+            tma_load_2d(sB + s * C::B_BYTES + (BN / 2) * 128, &tmB1, FULL(s), kb * BK, h0);
+          } else {
+            tma_load_2d(sB + s * C::B_BYTES, mp, FULL(s), kb * BK, brow);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int it = 0, lt = 0;
+      for (int tile = blockIdx.x; tile < args.tiles && !*abort_flag; tile += gridDim.x, ++lt) {
+        const int acc = lt & 1;
+        const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+        if (!mbar_wait(ACC_EMPTY(acc), aph ^ 1u, abort_flag, args.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+          if (!mbar_wait(FULL(s), ph, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = smem_desc_sw128(sA + s * C::A_BYTES);
+          const uint64_t bd = smem_desc_sw128(sB + s * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          mma_commit(EMPTY(s));
+        }
+        if (!ok) break;
+        mma_commit(ACC_FULL(acc));
+      }
+    }
+  } else {
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 belong to this warp
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < args.tiles; tile += gridDim.x, ++lt) {
+      const int acc = lt & 1;
+      const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+      if (!mbar_wait(ACC_FULL(acc), aph, abort_flag, args.status)) break;
+      tc_fence_after();
+      const int m = (tile % args.tiles_m) * BM + quad * 32 + lane;
+      const int n_blk = tile / args.tiles_m;
+      const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
+      epilogue_tile<BN>(args, m, n_blk, t_row);
+      tc_fence_before();
+      mbar_arrive(ACC_EMPTY(acc));
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // A wait ran out: give copies and MMAs still in flight time to land before the
+    // shared memory and TMEM are released.
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 20000000ull) {
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+#undef FULL
+#undef EMPTY
+#undef ACC_FULL
+#undef ACC_EMPTY
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool encoder() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, inner] matrix with row stride `ld`
+// elements; box = box_rows x 64 elements, 128-byte swizzle, zero fill outside.
+bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int64_t ld,
+              int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_sms = 0;
+int sm_count() {
+  if (!g_sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms <= 0) g_sms = 1;
+  }
+  return g_sms;
+}
+
+template <int BN>
+cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
+  using Cf = Cfg<BN>;
+  CUtensorMap mA, mB0, mB1, mB2;
+  memset(&mB1, 0, sizeof(mB1));
+  memset(&mB2, 0, sizeof(mB2));
+  if (!make_map(&mA, p.A, p.K, p.M, p.lda, BM)) return cudaErrorInvalidValue;
+  TcArgs a;
+  a.M = p.M;
+  a.N = p.N;
+  a.K = p.K;
+  a.mode = e.kind;
+  a.e = e;
+  a.status = c.status;
+  a.n_split1 = INT_MAX;
+  a.n_split2 = INT_MAX;
+  a.tiles_m = (p.M + BM - 1) / BM;
+  int tiles_n;
+  if (e.kind == EPI_SWIGLU) {
+    if (!make_map(&mB0, p.B[0], p.K, p.N, p.ldb, BN / 2)) return cudaErrorInvalidValue;
+    if (!make_map(&mB1, p.B[1], p.K, p.N, p.ldb, BN / 2)) return cudaErrorInvalidValue;
+    tiles_n = (p.N + BN / 2 - 1) / (BN / 2);
+  } else {
+    const int rows0 = p.nB > 1 ? p.split[0] : p.N;
+    if (!make_map(&mB0, p.B[0], p.K, rows0, p.ldb, BN)) return cudaErrorInvalidValue;
+    if (p.nB > 1) {
+      a.n_split1 = p.split[0];
+      const int rows1 = (p.nB > 2 ? p.split[1] : p.N) - p.split[0];
+      if (!make_map(&mB1, p.B[1], p.K, rows1, p.ldb, BN)) return cudaErrorInvalidValue;
+    }
+    if (p.nB > 2) {
+      a.n_split2 = p.split[1];
+      if (!make_map(&mB2, p.B[2], p.K, p.N - p.split[1], p.ldb, BN)) return cudaErrorInvalidValue;
+    }
+    if (p.nB < 2) mB1 = mB0;
+    if (p.nB < 3) mB2 = mB0;
+    tiles_n = (p.N + BN - 1) / BN;
+  }
+  if (e.kind == EPI_SWIGLU) mB2 = mB0;
+  a.tiles = a.tiles_m * tiles_n;
+  if (a.tiles <= 0) return cudaSuccess;
+  auto k = gemm_tc_kernel<BN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    if (err != cudaSuccess) return err;
+    attr_set = true;
+  }
+  const int grid = a.tiles < sm_count() ? a.tiles : sm_count();
+  k<<<grid, NUM_THREADS, Cf::SMEM, c.stream>>>(mA, mB0, mB1, mB2, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e) {
+  if (!encoder()) return false;
+  if (p.M <= 0 || p.N <= 0 || p.K <= 0) return false;
+  if (p.K % 8 || p.lda % 8 || p.ldb % 8 || p.N % 8) return false;
+  if (((uintptr_t)p.A & 15) || ((uintptr_t)p.B[0] & 15)) return false;
+  if (e.kind == EPI_SWIGLU && (p.nB != 2 || ((uintptr_t)p.B[1] & 15))) return false;
+  if (e.kind != EPI_SWIGLU) {
+    for (int i = 1; i < p.nB; ++i) {
+      if ((uintptr_t)p.B[i] & 15) return false;
+      if (p.split[i - 1] % 256) return false;  // tiles must not straddle two weight tensors
+    }
+  }
+  return true;
+}
+
+cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
+  const int tiles_m = (p.M + BM - 1) / BM;
+  const int sms = sm_count();
+  // Pick the tile width with the shorter estimated time: waves x tile width, with
+  // the narrower tile charged for its higher shared-memory traffic per FLOP.
+  int bn = 256;
+  if (e.kind != EPI_SWIGLU) {
+    const long t256 = (long)tiles_m * ((p.N + 255) / 256);
+    const long t128 = (long)tiles_m * ((p.N + 127) / 128);
+    const double c256 = (double)((t256 + sms - 1) / sms) * 256.0;
+    const double c128 = (double)((t128 + sms - 1) / sms) * 128.0 * 1.15;
+    bn = c128 < c256 ? 128 : 256;
+  }
+  return bn == 256 ? launch_bn<256>(c, p, e) : launch_bn<128>(c, p, e);
+}
+
+}  // namespace xmod

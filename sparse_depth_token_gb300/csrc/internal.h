@@ -55,6 +55,10 @@ cudaError_t launch_gather_rmsnorm(const Ctx& c, xmod_dtype dt, int B, int T, int
                                   const void* x, const int32_t* idx, const void* gamma,
                                   float eps, void* u);
 
+// out[m] = RMSNorm(h[m]) * gamma for fp32 rows h [M, d]; out in the element type.
+cudaError_t launch_rmsnorm_f32in(const Ctx& c, xmod_dtype dt, int64_t M, int d, const float* h,
+                                 const void* gamma, float eps, void* out);
+
 // Gated residual in place, see xmod_gated_scatter. gate < 0: dense update x + a + f.
 cudaError_t launch_gated_scatter(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
                                  void* x, const int32_t* idx, const float* r_sel, const void* a,
@@ -64,7 +68,7 @@ cudaError_t launch_gated_scatter(const Ctx& c, xmod_dtype dt, int B, int T, int 
 
 enum EpiKind {
   EPI_STORE = 0,         // out[m, n] = acc
-  EPI_OPROJ = 1,         // out[m, n] = a = acc; out2[m, n] = h = x_row(m)[n] + acc
+  EPI_OPROJ = 1,         // out[m, n] = a = acc; out2[m, n] = h = x_row(m)[n] + acc (fp32)
   EPI_SWIGLU = 2,        // out[m, n] = silu(acc_gate) * acc_up
   EPI_DOWN_SCATTER = 3,  // x_row(m)[n] = gated residual of (a[m, n], f = acc)
 };
@@ -92,6 +96,22 @@ struct Epilogue {
 cudaError_t launch_gemm_simt(const Ctx& c, xmod_dtype dt, int M, int N, int K, const void* A,
                              int lda, const void* B, int ldb, const void* B2,
                              const Epilogue& e);
+
+// Tensor-core (tcgen05) GEMM, bf16 only. Up to three weight tensors can feed one
+// launch: accumulator columns [0, split[0]) come from B[0], [split[0], split[1])
+// from B[1], the rest from B[2] (q | k | v). For EPI_SWIGLU, B[0] is the gate and
+// B[1] the up projection, each [N, K].
+struct GemmTcProblem {
+  int M = 0, N = 0, K = 0;
+  const void* A = nullptr;
+  int lda = 0;
+  const void* B[3] = {nullptr, nullptr, nullptr};
+  int nB = 1;
+  int split[2] = {0, 0};
+  int ldb = 0;
+};
+bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e);
+cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e);
 
 // ---------------------------------------------------------------- attention
 

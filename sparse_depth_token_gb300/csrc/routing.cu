@@ -350,6 +350,45 @@ cudaError_t launch_gather_rmsnorm(const Ctx& c, xmod_dtype dt, int B, int T, int
   return cudaGetLastError();
 }
 
+template <typename T>
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+rmsnorm_f32in_kernel(int64_t M, int d, const float* __restrict__ h, const T* __restrict__ gamma,
+                     float eps, T* __restrict__ out) {
+  constexpr int V = Vec16<T>::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
+  if (m >= M) return;
+  const float* src = h + m * d;
+  float ss = 0.f;
+  for (int c = lane * 4; c < d; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(src + c);
+    ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+  }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)d + eps);
+  T* dst = out + m * d;
+  for (int c = lane * V; c < d; c += 32 * V) {
+    Vec16<T> g = ld_vec(gamma + c);
+    Vec16<T> o;
+#pragma unroll
+    for (int e = 0; e < V; ++e) o.set(e, src[c + e] * inv * g.get(e));
+    st_vec(dst + c, o);
+  }
+}
+
+cudaError_t launch_rmsnorm_f32in(const Ctx& c, xmod_dtype dt, int64_t M, int d, const float* h,
+                                 const void* gamma, float eps, void* out) {
+  if (M <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
+  if (dt == XMOD_BF16)
+    rmsnorm_f32in_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+        M, d, h, (const __nv_bfloat16*)gamma, eps, (__nv_bfloat16*)out);
+  else
+    rmsnorm_f32in_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(M, d, h, (const float*)gamma,
+                                                                 eps, (float*)out);
+  return cudaGetLastError();
+}
+
 // ================================================================ gated scatter
 
 template <typename T>

@@ -51,6 +51,7 @@ class Workload:
     bias_std: float = 0.0          # 0: no bias
     varsigma_range: tuple = (1.0, 1.0)
     eps: float = 1e-6
+    weight_std: float = 0.02      # std of the projection matrices
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -114,7 +115,7 @@ def layer_weights(w: Workload, layer: int) -> dict:
     for t, name in enumerate(_TENSORS):
         key = (1000 + layer, t)
         if name in shapes:
-            out[name] = _normal(w.seed, key, shapes[name], 0.02, w.dtype)
+            out[name] = _normal(w.seed, key, shapes[name], w.weight_std, w.dtype)
         elif name == "w_r":
             out[name] = _normal(w.seed, key, (d,), 1.0 / np.sqrt(d), w.dtype)
         else:  # RMSNorm gains

@@ -49,7 +49,13 @@ def assert_close(got, ref, dtype: str, what: str = "", stored_ref=None):
             err = np.maximum(err - bf16_half_ulp(stored_ref), 0.0)
         mx = float(np.max(err)) if got.size else 0.0
         rl = rel_l2(got, ref)
-        assert mx <= BF16_MAX_ABS and rl <= BF16_REL_L2, f"{what}: max-abs {mx:.3e}, rel-L2 {rl:.3e}"
+        if not (mx <= BF16_MAX_ABS and rl <= BF16_REL_L2):
+            i = int(np.argmax(err))
+            raise AssertionError(
+                f"{what}: max-abs {mx:.3e}, rel-L2 {rl:.3e}; worst element {i}: got "
+                f"{got.flat[i]:.6f} ref {ref.flat[i]:.6f}; max|ref| {np.max(np.abs(ref)):.3f}, "
+                f"rms(ref) {np.sqrt(np.mean(ref ** 2)):.4f}, count(err>2e-2) "
+                f"{int(np.count_nonzero(err > BF16_MAX_ABS))} of {err.size}")
     else:
         rl = rel_l2(got, ref)
         scale = float(np.max(np.abs(ref))) if ref.size else 1.0
