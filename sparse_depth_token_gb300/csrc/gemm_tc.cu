@@ -163,7 +163,20 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int m, int n_blk,
     if (!row_ok || n >= a.N) continue;
     const int rem = a.N - n;
     if (a.mode == EPI_STORE) {
-      store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + n, v, rem);
+      if (e.vt && n >= e.vt_col0) {
+        // v^T: token m of sequence b goes to column t of rows (b, g, dim) -- across a
+        // warp the 32 consecutive tokens of one dim form one contiguous run.
+        const int cv = n - e.vt_col0;
+        const int g = cv / e.vt_hd, dim0 = cv % e.vt_hd;
+        const int64_t b = m / e.n_per_seq, t = m - b * e.n_per_seq;
+        __nv_bfloat16* p =
+            (__nv_bfloat16*)e.vt + ((b * e.vt_hkv + g) * e.vt_hd + dim0) * (int64_t)e.vt_ld + t;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < rem) p[(int64_t)i * e.vt_ld] = __float2bfloat16_rn(v[i]);
+      } else {
+        store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + n, v, rem);
+      }
     } else if (a.mode == EPI_OPROJ) {
       float xv[32];
       load32_bf16((const __nv_bfloat16*)e.x + xrow + n, xv, rem);
@@ -340,32 +353,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-bool encoder() {
-  if (g_encode) return true;
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                       &q) != cudaSuccess ||
-      q != cudaDriverEntryPointSuccess || !fn)
-    return false;
-  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  return true;
-}
-
 // 2-D bf16 tensor map over a row-major [rows, inner] matrix with row stride `ld`
 // elements; box = box_rows x 64 elements, 128-byte swizzle, zero fill outside.
 bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int64_t ld,
               int box_rows) {
-  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const int64_t dims[2] = {inner, rows};
+  const int64_t strides[1] = {ld * 2};
+  const int box[2] = {BK, box_rows};
+  return tma_map_bf16(m, base, 2, dims, strides, box);
 }
 
 int g_sms = 0;
@@ -435,7 +430,7 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
 }  // namespace
 
 bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e) {
-  if (!encoder()) return false;
+  if (!tma_available()) return false;
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return false;
   if (p.K % 8 || p.lda % 8 || p.ldb % 8 || p.N % 8) return false;
   if (((uintptr_t)p.A & 15) || ((uintptr_t)p.B[0] & 15)) return false;

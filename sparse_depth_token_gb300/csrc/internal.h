@@ -2,6 +2,7 @@
 // Every launcher only enqueues work on ctx.stream and returns the launch status.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -14,6 +15,15 @@ struct Ctx {
   cudaStream_t stream;
   int* status;  // device status word (first error wins)
 };
+
+// ---------------------------------------------------------------- TMA tensor maps
+
+bool tma_available();
+// bf16 tensor map of the given rank (2 or 3): dims[0] is the contiguous extent,
+// strides_bytes[i] the byte stride of dimension i+1; box in elements; 128-byte
+// swizzle; reads outside the tensor return zeros.
+bool tma_map_bf16(CUtensorMap* m, const void* base, int rank, const int64_t* dims,
+                  const int64_t* strides_bytes, const int* box);
 
 // ---------------------------------------------------------------- measurement
 
@@ -89,6 +99,10 @@ struct Epilogue {
   const float* r_sel = nullptr; // DOWN: gates [M]
   float varsigma = 1.0f;
   int gate = -1;                // DOWN: XMOD_GATE_XMOD, XMOD_GATE_MOD, or -1 for dense
+  // STORE (tensor-core path): columns >= vt_col0 are the values v; they are written
+  // transposed to vt [B, hkv, hd, vt_ld] (keys contiguous) instead of to `out`.
+  void* vt = nullptr;
+  int vt_col0 = 0, vt_hd = 0, vt_hkv = 0, vt_ld = 0;
 };
 
 // C[M, N] = A[M, K] . B[N, K]^T (fp32 accumulate), then the epilogue. For
