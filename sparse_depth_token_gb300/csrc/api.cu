@@ -42,9 +42,12 @@ bool dims_ok(const xmod_dims* dm) {
 
 bool head_dim_supported(int hd) { return hd == 32 || hd == 64 || hd == 128; }
 
+// Row stride (elements) of the transposed values for n tokens: 16-byte multiple.
+inline int vt_ld(int n) { return (n + 7) / 8 * 8; }
+
 // Workspace carve-up. M rows of block scratch cover a dense layer (M = B*T).
 struct Layout {
-  size_t status, s, idx, r_sel, u, qkv, o, a, h, hidden, total;
+  size_t status, s, idx, r_sel, u, qkv, vt, o, a, h, hidden, total;
 };
 
 Layout layout(const xmod_dims* dm, int K) {
@@ -62,6 +65,9 @@ Layout layout(const xmod_dims* dm, int K) {
   L.r_sel = off;  off = align_up(off + 4 * Bn);
   L.u = off;      off = align_up(off + es * M * dm->d);
   L.qkv = off;    off = align_up(off + es * M * qkv_w);
+  // v transposed for the tensor-core attention: [B, hkv, hd, vt_ld(T)]
+  L.vt = off;     off = align_up(off + es * (size_t)dm->B * dm->n_kv_heads * dm->head_dim *
+                                           (size_t)vt_ld(dm->T));
   L.o = off;      off = align_up(off + es * M * dm->n_heads * dm->head_dim);
   L.a = off;      off = align_up(off + 4 * M * dm->d);   // attention residual kept in fp32
   L.h = off;      off = align_up(off + 4 * M * dm->d);   // h = x_sel + a kept in fp32
@@ -117,17 +123,29 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   XMOD_RUN("gather_rmsnorm", launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms1, dm->rms_eps, u));
   // 2. q, k, v projections into one [M, qkv_w] buffer
   const bool tc = dt == XMOD_BF16;
+  char* vt = at(ws, L.vt);
+  const bool tc_attn = tc && attention_tc_supported(hd, n, qkv_w);
   Epilogue e;
   e.kind = EPI_STORE;
   e.ldo = qkv_w;
   e.out = qkv;
+  if (tc_attn) {  // v goes straight to its transposed layout
+    e.vt = vt;
+    e.vt_col0 = qw + kw;
+    e.vt_hd = hd;
+    e.vt_hkv = hkv;
+    e.vt_ld = vt_ld(n);
+    e.n_per_seq = n;
+  }
   GemmTcProblem pq;
   pq.M = M; pq.N = qkv_w; pq.K = d; pq.A = u; pq.lda = d; pq.ldb = d;
   pq.B[0] = w->wq; pq.B[1] = w->wk; pq.B[2] = w->wv; pq.nB = 3;
   pq.split[0] = qw; pq.split[1] = qw + kw;
-  if (tc && gemm_tc_supported(pq, e)) {
+  const bool tc_qkv = tc && gemm_tc_supported(pq, e);
+  if (tc_qkv) {
     XMOD_RUN("gemm_qkv", launch_gemm_tc(c, pq, e));
   } else {
+    e.vt = nullptr;
     XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, qw, d, u, d, w->wq, d, nullptr, e));
     e.out = qkv + es * qw;
     XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wk, d, nullptr, e));
@@ -135,8 +153,11 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
     XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wv, d, nullptr, e));
   }
   // 3. causal GQA attention among the n rows of each sequence
-  XMOD_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w, qkv + es * qw,
-                                              qkv + es * (qw + kw), qkv_w, o));
+  if (tc_qkv && tc_attn)
+    XMOD_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, vt_ld(n), o));
+  else
+    XMOD_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w,
+                                                qkv + es * qw, qkv + es * (qw + kw), qkv_w, o));
   // 4. a = o Wo^T, h = x_sel + a
   Epilogue eo;
   eo.kind = EPI_OPROJ;

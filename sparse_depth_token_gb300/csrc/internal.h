@@ -136,4 +136,11 @@ cudaError_t launch_attention_simt(const Ctx& c, xmod_dtype dt, int B, int n, int
                                   int hd, const void* q, int ldq, const void* k, const void* v,
                                   int ldkv, void* o);
 
+// Tensor-core attention (bf16, head_dim 128). q and k come from the q|k|v rows
+// [B*n, ldq] (k of KV head g at column hq*128 + g*128); v comes transposed,
+// vt [B, hkv, 128, vt_ld] with keys contiguous; o [B*n, hq*128].
+bool attention_tc_supported(int hd, int n, int ldq);
+cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
+                                int ldq, const void* vt, int vt_ld, void* o);
+
 }  // namespace xmod
