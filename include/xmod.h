@@ -162,6 +162,39 @@ XMOD_API int xmod_stack_fwd(const xmod_dims* dims, int K, double A, int N0, int 
                    const xmod_layer_weights* layers, int n_layers, void* x_inout,
                    const float* bias, void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- allocation-free routing
+ * The paper has no counterpart to this entry point: it exists for callers that
+ * cannot allocate device memory -- a plugin inside another runtime that is given
+ * only its input and output buffers, a serving loop that must not allocate once
+ * running (an allocation can synchronise the device), or a process whose device
+ * memory is held by another framework's caching allocator so that cudaMalloc
+ * fails. It computes exactly what xmod_router_topk computes (router logits with
+ * bias, sigmoid gates at the selected positions, per-sequence top-(T/K) with ties
+ * to the lower position) without a caller workspace.
+ *
+ * Its scratch (fp32 logits and a status word) is a fixed array inside the library
+ * image, sized for at most XMOD_NOALLOC_MAX_TOKENS = B*T tokens (8 MiB of logits),
+ * which every device that loads the library holds until the process exits. Larger
+ * problems are rejected with XMOD_ERR_UNSUPPORTED before anything is launched.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ *
+ * All calls on a device share that array and it keeps the last call's contents;
+ * each call clears the status word first and rewrites every logit it reads, so
+ * back-to-back calls on one stream are independent. Calls that overlap on the GPU
+ * (different streams with no ordering between them) race on the array.
+ * The first call on a device looks up the array's device address with that device
+ * current; make that first call before any stream capture.
+ *
+ *   x, w_r, bias, idx, r_sel: as for xmod_router_topk (device pointers, bias and
+ *   r_sel may be NULL). status_out: NULL or a device int that receives the device
+ *   status of this call (XMOD_OK, or XMOD_ERR_DEVICE_CHECK for a non-finite logit),
+ *   written asynchronously on `stream`. */
+#define XMOD_NOALLOC_MAX_TOKENS (2 * 1024 * 1024)
+
+XMOD_API int xmod_router_topk_noalloc(const xmod_dims* dims, int K, const void* x,
+                                      const void* w_r, const float* bias, int32_t* idx,
+                                      float* r_sel, int* status_out, void* stream);
+
 /* ---------------------------------------------------------------- measurement
  * Not part of the method: support for benchmarking the calls above. */
 

@@ -22,7 +22,10 @@ LAYER_DENSE, LAYER_SPARSE = 0, 1
 EXPORTS = ("xmod_version", "xmod_status_string", "xmod_workspace_bytes", "xmod_reset_status",
            "xmod_sync_status", "xmod_router_topk", "xmod_topk", "xmod_gather", "xmod_block_fwd",
            "xmod_gated_scatter", "xmod_layer_fwd", "xmod_stack_fwd", "xmod_launch_count",
-           "xmod_profile_enable", "xmod_profile_read")
+           "xmod_profile_enable", "xmod_profile_read", "xmod_router_topk_noalloc")
+
+# Largest B*T the allocation-free router entry point accepts (its fixed scratch).
+NOALLOC_MAX_TOKENS = 2 * 1024 * 1024
 
 
 class XmodError(RuntimeError):
@@ -93,6 +96,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.xmod_profile_enable.argtypes = [ctypes.c_int]
     L.xmod_profile_read.argtypes = [ctypes.POINTER(KernelTime), ctypes.c_int,
                                     ctypes.POINTER(ctypes.c_int)]
+    L.xmod_router_topk_noalloc.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _VP, _VP, _VP, _VP,
+                                           _VP, _VP, _VP]
     _lib = L
     return L
 
@@ -213,3 +218,14 @@ def profile_read(max_kinds: int = 64) -> dict:
     n = ctypes.c_int(0)
     _check("xmod_profile_read", load().xmod_profile_read(arr, max_kinds, ctypes.byref(n)))
     return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(n.value)}
+
+
+def router_topk_noalloc(dm, K, x, w_r, bias, idx, r_sel, status=None, stream=None):
+    """xmod_router_topk without a workspace, for callers that cannot allocate device
+    memory: the library's own fixed scratch holds the logits (B*T <= NOALLOC_MAX_TOKENS).
+    `status` (optional device int32 tensor) receives the call's device status."""
+    if dm.B * dm.T > NOALLOC_MAX_TOKENS:
+        raise XmodError("xmod_router_topk_noalloc", ERR_UNSUPPORTED)
+    _check("xmod_router_topk_noalloc", load().xmod_router_topk_noalloc(
+        ctypes.byref(dm), int(K), _p(x), _p(w_r), _p(bias), _p(idx), _p(r_sel), _p(status),
+        _stream(stream)))

@@ -1,0 +1,67 @@
+"""The allocation-free router entry point, for callers that cannot allocate device
+memory (a plugin handed only its input and output buffers, a serving loop that must
+not allocate once running, or a process whose device memory another framework's
+allocator already holds). It must return what the workspace-based xmod_router_topk
+returns -- bit-identical selections, gates within the routing tests' tolerance --
+on consecutive calls that share its fixed scratch.
+
+This file is collected last so that a first-failure run has already run every
+other test; it also passes on its own in a fresh process."""
+import numpy as np
+import pytest
+
+from sparse_depth_token_gb300 import inputs as I
+from tests import _util as U
+from tests._gpu import need_gpu, to_dev, torch, workspace, xmod_dims
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(X, B, T, d, K, seed, dtype, bias_std):
+    w = I.WORKLOADS["routing_bf16"].replace(B=B, T=T, d=d, seed=seed, dtype=dtype,
+                                            bias_std=bias_std)
+    x = I.residual_stream(w)
+    lw = I.layer_weights(w, 0)
+    bias = I.router_bias(w)
+    x, _ = U.enforce_routing_margin(x, dtype, lw["w_r"], bias, K)
+    dm = xmod_dims(w)
+    return dm, to_dev(x, dtype), to_dev(lw["w_r"], dtype), (
+        torch.from_numpy(bias).cuda() if bias is not None else None)
+
+
+def test_router_topk_noalloc_matches_workspace_entry_point():
+    need_gpu()
+    from sparse_depth_token_gb300 import xmod as X
+    X.load()
+    cases = [(4, 2048, 512, 8, 41, "bf16", 0.0), (3, 1000, 256, 4, 42, "bf16", 0.1),
+             (2, 640, 128, 2, 43, "fp32", 0.1)]
+    for B, T, d, K, seed, dtype, bstd in cases:
+        dm, xd, wr, bd = _case(X, B, T, d, K, seed, dtype, bstd)
+        n = T // K
+        ws = workspace(dm, K)
+        idx_ref = torch.empty((B, n), dtype=torch.int32, device="cuda")
+        rs_ref = torch.empty((B, n), dtype=torch.float32, device="cuda")
+        X.reset_status(ws)
+        X.router_topk(dm, K, xd, wr, bd, None, None, idx_ref, rs_ref, ws)
+        assert X.sync_status(ws) == X.OK
+        for call in range(2):   # two calls in a row share the fixed scratch
+            idx = torch.full((B, n), -1, dtype=torch.int32, device="cuda")
+            rs = torch.full((B, n), -1.0, dtype=torch.float32, device="cuda")
+            st = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+            X.router_topk_noalloc(dm, K, xd, wr, bd, idx, rs, st)
+            torch.cuda.synchronize()
+            assert int(st.item()) == X.OK
+            np.testing.assert_array_equal(idx.cpu().numpy(), idx_ref.cpu().numpy())
+            np.testing.assert_allclose(rs.cpu().numpy(), rs_ref.cpu().numpy(), rtol=1e-6, atol=0)
+
+
+def test_router_topk_noalloc_rejects_oversized_problem():
+    need_gpu()
+    from sparse_depth_token_gb300 import xmod as X
+    import ctypes
+    L = X.load()
+    dm = X.dims(B=X.NOALLOC_MAX_TOKENS // 1024 + 1, T=1024, d=64, n_heads=1, n_kv_heads=1,
+                head_dim=8, d_ff=8, dtype=X.BF16)
+    fake = 0x10000   # never dereferenced: the size check comes first
+    assert L.xmod_router_topk_noalloc(ctypes.byref(dm), 8, fake, fake, None, fake, None, None,
+                                      None) == X.ERR_UNSUPPORTED
