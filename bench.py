@@ -427,7 +427,16 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--B", type=int, default=None,
+                    help="override sequences per GPU (small profiling cases only)")
+    ap.add_argument("--A", type=float, default=None,
+                    help="override the anchor stride A (small profiling cases only)")
     args = ap.parse_args()
+    if args.B is not None or args.A is not None:
+        w = I.WORKLOADS[args.workload]
+        A = w.A if args.A is None else args.A
+        n_layers = w.N0 + w.N1 * (int(round(A * w.K)) + 1)
+        I.WORKLOADS[args.workload] = w.replace(B=args.B or w.B, A=A, n_layers=n_layers)
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -8,16 +8,19 @@
 // positions. Query head h reads key/value head h / (hq / hkv).
 //
 // One CTA per (128-query block, query head, sequence):
-//   warp 0      TMA: the Q tile once, then K_j and V_j^T for each 128-key block j
+//   warp 0      TMA: the Q tile once, then K_j and V_j^T of each 128-key block j
 //               into a two-stage ring
-//   warp 1      TMEM owner; one lane issues S_j = Q K_j^T into one of two TMEM
-//               S buffers (S_{j+1} is issued before P_j V_j so the tensor core works
-//               on the next scores while the softmax runs), then P_j V_j^T
-//   warps 2..5  softmax, one query row per thread (a TMEM lane is a row, so row
-//               max and row sum are thread-local): online max in log2 units,
-//               P_j = exp2(s*scale - m) written as bf16 into shared memory in the
-//               swizzled K-major layout the MMA reads, and O = O*alpha + P_j V_j
-//               accumulated in registers.
+//   warp 1      TMEM owner; one lane issues S_j = Q K_j^T into one of two TMEM S
+//               buffers (S_{j+1} is issued before P_j V_j so the tensor core works on
+//               the next scores while the softmax runs), then O += P_j V_j with the
+//               output accumulator O resident in TMEM
+//   warps 2..5  softmax, one query row per thread (a TMEM lane is a row, so row max
+//               and row sum are thread-local), in one pass over the scores held in
+//               registers: P_j = exp2(s*scale - m) is written as bf16 into one of two
+//               shared-memory P buffers in the swizzled K-major layout the MMA reads.
+//               The running max m only moves when a row's max grows by more than 2^8
+//               (P then stays below 256); when it moves, the row of O in TMEM is
+//               rescaled once P_{j-1} V_{j-1} has landed.
 // V arrives transposed ([hd, keys], keys contiguous), written that way by the
 // q/k/v projection's epilogue, so both MMAs read K-major operands.
 
@@ -40,7 +43,8 @@ constexpr int HD = 128;     // head dim
 constexpr int THREADS = 192;
 constexpr int CHUNK = 128 * 128;        // bytes of a 128 x 64 bf16 swizzled chunk
 constexpr int TILE = 2 * CHUNK;         // a 128 x 128 bf16 tile
-constexpr int SMEM = 6 * TILE + 1024 + 256;
+constexpr int SMEM = 7 * TILE + 1024 + 256;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 struct AttnArgs {
   int n, hq, hkv, nqb;
@@ -70,16 +74,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base;
-  const uint32_t sP = base + TILE;
-  const uint32_t sK0 = base + 2 * TILE;   // K stages at sK0 + s * TILE
-  const uint32_t sV0 = base + 4 * TILE;   // V^T stages at sV0 + s * TILE
-  const uint32_t sBar = base + 6 * TILE;
-  // barriers
+  const uint32_t sP0 = base + TILE;       // P buffers at sP0 + b * TILE
+  const uint32_t sK0 = base + 3 * TILE;   // K stages at sK0 + s * TILE
+  const uint32_t sV0 = base + 5 * TILE;   // V^T stages at sV0 + s * TILE
+  const uint32_t sBar = base + 7 * TILE;
   const uint32_t Q_FULL = sBar + 0;
   const uint32_t KV_FULL0 = sBar + 8, KV_EMPTY0 = sBar + 24;
   const uint32_t S_FULL0 = sBar + 40, S_EMPTY0 = sBar + 56;
-  const uint32_t P_FULL = sBar + 72, P_EMPTY = sBar + 80;
-  const uint32_t PV_FULL = sBar + 88, PV_EMPTY = sBar + 96;
+  const uint32_t P_FULL0 = sBar + 72, P_EMPTY0 = sBar + 88;
   const uint32_t sTmem = sBar + 112;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (sTmem - base));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (sTmem - base) + 8);
@@ -99,11 +101,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
       mbar_init(KV_EMPTY0 + 8 * s, 1);
       mbar_init(S_FULL0 + 8 * s, 1);
       mbar_init(S_EMPTY0 + 8 * s, 128);
+      mbar_init(P_FULL0 + 8 * s, 128);
+      mbar_init(P_EMPTY0 + 8 * s, 1);
     }
-    mbar_init(P_FULL, 128);
-    mbar_init(P_EMPTY, 1);
-    mbar_init(PV_FULL, 1);
-    mbar_init(PV_EMPTY, 128);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmQK);
@@ -113,7 +113,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;   // S0: cols 0..127, S1: 128..255, PV: 256..383
+  const uint32_t tmem = *tmem_slot;   // S0: cols 0..127, S1: 128..255, O: 256..383
+  const uint32_t tO = tmem + 256u;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -158,21 +159,19 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
       if (ok) ok = issue_s(0);
       for (int j = 0; ok && j < nkb; ++j) {
         if (j + 1 < nkb && !issue_s(j + 1)) break;
-        const uint32_t pj = (uint32_t)j & 1u;
-        if (!mbar_wait(P_FULL, pj, abort_flag, a.status)) break;
-        if (!mbar_wait(PV_EMPTY, pj ^ 1u, abort_flag, a.status)) break;
-        tc_fence_after();
         const int s = j & 1;
+        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+        if (!mbar_wait(P_FULL0 + 8 * s, ph, abort_flag, a.status)) break;
+        tc_fence_after();
 #pragma unroll
         for (int kc = 0; kc < 2; ++kc) {
-          const uint64_t ad = smem_desc_sw128(sP + kc * CHUNK);
+          const uint64_t ad = smem_desc_sw128(sP0 + s * TILE + kc * CHUNK);
           const uint64_t bd = smem_desc_sw128(sV0 + s * TILE + kc * CHUNK);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16(tmem + 256u, ad + 2ull * k, bd + 2ull * k, idesc, (kc | k) != 0 ? 1u : 0u);
+            mma_bf16(tO, ad + 2ull * k, bd + 2ull * k, idesc, (j | kc | k) != 0 ? 1u : 0u);
         }
-        mma_commit(PV_FULL);
-        mma_commit(P_EMPTY);
+        mma_commit(P_EMPTY0 + 8 * s);
         mma_commit(KV_EMPTY0 + 8 * s);
       }
     }
@@ -181,12 +180,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
     const int row = quad * 32 + lane;
     const int qi = q0 + row;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    float o[HD];
-#pragma unroll
-    for (int i = 0; i < HD; ++i) o[i] = 0.f;
-    float m = -INFINITY, l = 0.f;
-    const uint32_t prow = sP + (uint32_t)row * 128u;
     const uint32_t sw = (uint32_t)(row & 7);
+    float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkb; ++j) {
       const int s = j & 1;
@@ -196,38 +191,70 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
         break;
       }
       tc_fence_after();
-      const uint32_t srow = tmem + lane_off + (uint32_t)(s * 128);
-      const int key0 = j * KB;
-      // pass 1: row max of the unmasked scores
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(srow + c * 32, v);
+      float v[128];
+      {
+        float* vv = v;
+        const uint32_t srow = tmem + lane_off + (uint32_t)(s * 128);
+        tmem_ld32(srow, *reinterpret_cast<float(*)[32]>(vv));
+        tmem_ld32(srow + 32, *reinterpret_cast<float(*)[32]>(vv + 32));
+        tmem_ld32(srow + 64, *reinterpret_cast<float(*)[32]>(vv + 64));
+        tmem_ld32(srow + 96, *reinterpret_cast<float(*)[32]>(vv + 96));
         tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (key0 + c * 32 + i <= qi) mx = fmaxf(mx, v[i]);
       }
-      const float m_new = fmaxf(m, mx * a.scale_log2);
-      const float alpha = exp2f(m - m_new);
-      // pass 2: probabilities into the shared-memory P tile (after P_{j-1} was consumed)
-      if (!mbar_wait(P_EMPTY, ((uint32_t)j & 1u) ^ 1u, abort_flag, a.status)) {
+      tc_fence_before();
+      mbar_arrive(S_EMPTY0 + 8 * s);
+      const int key0 = j * KB;
+      const bool diag = key0 + KB - 1 > q0;   // only the diagonal block needs the mask
+      float mx = -INFINITY;
+      if (diag) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          if (key0 + i > qi) v[i] = -INFINITY;
+          mx = fmaxf(mx, v[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) mx = fmaxf(mx, v[i]);
+      }
+      const float m_cand = mx * a.scale_log2;
+      const bool grow = m_cand > m + kRescaleThreshold;
+      const float m_new = grow ? m_cand : m;
+      const float alpha = grow ? exp2f(m - m_new) : 1.0f;
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        // O holds P_0..j-1 V: wait until the last of those MMAs landed, then rescale.
+        const int jp = j - 1;
+        if (!mbar_wait(P_EMPTY0 + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u, abort_flag,
+                       a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float ov[32];
+          tmem_ld32(tO + lane_off + c * 32, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+          tmem_st32(tO + lane_off + c * 32, ov);
+        }
+        tmem_st_wait();
+      }
+      m = m_new;
+      // the P buffer of this parity is free once P_{j-2} V_{j-2} has completed
+      if (!mbar_wait(P_EMPTY0 + 8 * s, ph ^ 1u, abort_flag, a.status)) {
         ok = false;
         break;
       }
+      const uint32_t prow = sP0 + s * TILE + (uint32_t)row * 128u;
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(srow + c * 32, v);
-        tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = (key0 + c * 32 + i <= qi) ? exp2f(v[i] * a.scale_log2 - m_new) : 0.f;
-          const float p1 =
-              (key0 + c * 32 + i + 1 <= qi) ? exp2f(v[i + 1] * a.scale_log2 - m_new) : 0.f;
+          const float p0 = exp2f(fmaf(v[c * 32 + i], a.scale_log2, -m));
+          const float p1 = exp2f(fmaf(v[c * 32 + i + 1], a.scale_log2, -m));
           sum += p0 + p1;
           pk[i / 2] = pack_bf16x2(p0, p1);
         }
@@ -239,44 +266,40 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
                        pk[4 * u4 + 3]);
         }
       }
+      l = l * alpha + sum;
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(S_EMPTY0 + 8 * s);
-      mbar_arrive(P_FULL);
-      l = l * alpha + sum;
-      m = m_new;
-      // O = O * alpha + P_j V_j
-      if (!mbar_wait(PV_FULL, (uint32_t)j & 1u, abort_flag, a.status)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(tmem + lane_off + 256u + c * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c * 32 + i] = fmaf(o[c * 32 + i], alpha, v[i]);
-      }
-      tc_fence_before();
-      mbar_arrive(PV_EMPTY);
+      mbar_arrive(P_FULL0 + 8 * s);
     }
-    if (ok && qi < a.n) {
+    if (ok) {
+      const int jl = nkb - 1;
+      ok = mbar_wait(P_EMPTY0 + 8 * (jl & 1), (uint32_t)(jl >> 1) & 1u, abort_flag, a.status);
+    }
+    if (ok) {
+      tc_fence_after();
       const float inv = 1.0f / l;
       __nv_bfloat16* dst = a.o + ((int64_t)b * a.n + qi) * a.ldo + h * HD;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float ov[32];
+        tmem_ld32(tO + lane_off + c * 32, ov);
+        tmem_ld_wait();
+        if (qi < a.n) {
 #pragma unroll
-      for (int c = 0; c < HD; c += 8) {
-        uint4 q;
-        q.x = pack_bf16x2(o[c] * inv, o[c + 1] * inv);
-        q.y = pack_bf16x2(o[c + 2] * inv, o[c + 3] * inv);
-        q.z = pack_bf16x2(o[c + 4] * inv, o[c + 5] * inv);
-        q.w = pack_bf16x2(o[c + 6] * inv, o[c + 7] * inv);
-        *reinterpret_cast<uint4*>(dst + c) = q;
+          for (int e = 0; e < 32; e += 8) {
+            uint4 q;
+            q.x = pack_bf16x2(ov[e] * inv, ov[e + 1] * inv);
+            q.y = pack_bf16x2(ov[e + 2] * inv, ov[e + 3] * inv);
+            q.z = pack_bf16x2(ov[e + 4] * inv, ov[e + 5] * inv);
+            q.w = pack_bf16x2(ov[e + 6] * inv, ov[e + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + e) = q;
+          }
+        }
       }
     }
   }
 
+  tc_fence_before();
   __syncthreads();
   if (*abort_flag) {
     const uint64_t t0 = global_timer_ns();
