@@ -47,7 +47,7 @@ inline int vt_ld(int n) { return (n + 7) / 8 * 8; }
 
 // Workspace carve-up. M rows of block scratch cover a dense layer (M = B*T).
 struct Layout {
-  size_t status, s, idx, r_sel, u, qkv, vt, o, a, h, hidden, total;
+  size_t status, s, idx, r_sel, u, qkv, vt, o, h, hidden, total;
 };
 
 Layout layout(const xmod_dims* dm, int K) {
@@ -69,7 +69,6 @@ Layout layout(const xmod_dims* dm, int K) {
   L.vt = off;     off = align_up(off + es * (size_t)dm->B * dm->n_kv_heads * dm->head_dim *
                                            (size_t)vt_ld(dm->T));
   L.o = off;      off = align_up(off + es * M * dm->n_heads * dm->head_dim);
-  L.a = off;      off = align_up(off + 4 * M * dm->d);   // attention residual kept in fp32
   L.h = off;      off = align_up(off + 4 * M * dm->d);   // h = x_sel + a kept in fp32
   L.hidden = off; off = align_up(off + es * M * dm->d_ff);
   L.total = off;
@@ -102,7 +101,7 @@ bool weights_ok(const xmod_layer_weights* w, bool need_router) {
 }
 
 // The block on B*n compact rows (rows of x selected by idx, or identity when
-// idx == NULL and n == T). Writes a to a_out (or the workspace) and either
+// idx == NULL and n == T). Writes a to a_out when given, and either
 // scatters the gated residual into x (scatter == true) or stores f to f_out.
 int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int n,
               const void* x_src, const int32_t* idx, const xmod_layer_weights* w, void* a_out,
@@ -116,7 +115,6 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   char* u = at(ws, L.u);
   char* qkv = at(ws, L.qkv);
   char* o = at(ws, L.o);
-  char* a = a_out ? (char*)a_out : at(ws, L.a);
   char* h = at(ws, L.h);
   char* hidden = at(ws, L.hidden);
   // 1. gather + RMSNorm1
@@ -161,9 +159,8 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   // 4. a = o Wo^T, h = x_sel + a
   Epilogue eo;
   eo.kind = EPI_OPROJ;
-  eo.out = a;
+  eo.out = a_out;   // the attention residual itself only when the caller asks for it
   eo.ldo = d;
-  eo.a_f32 = (a_out == nullptr);
   eo.out2 = h;
   eo.ldo2 = d;
   eo.x = (void*)x_src;
@@ -204,8 +201,7 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
     ed.T = T;
     ed.n_per_seq = n;
     ed.d = d;
-    ed.a = a;
-    ed.a_f32 = (a_out == nullptr);
+    ed.h = (const float*)h;
     ed.r_sel = r_sel;
     ed.varsigma = w->varsigma;
     ed.gate = gate;

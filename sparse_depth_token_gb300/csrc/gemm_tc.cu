@@ -9,16 +9,17 @@
 //               ring of shared-memory stages (128-byte swizzle)
 //   warp 1      allocates TMEM; one lane issues tcgen05.mma (128 x BN x 16) into one
 //               of two TMEM accumulators, committing each stage back to the producer
-//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one TMEM lane =
-//               one output row per thread), the fused epilogue math, global stores;
-//               the other accumulator is meanwhile filled by the next tile's MMAs.
-// Fused epilogues: plain store (optionally for q|k|v from three weight tensors),
-// O-projection (a and h = x_sel + a), SwiGLU (gate and up halves of one tile), and
-// the down projection's gated scatter back into the residual stream (Eq. 6 / Eq. 7
-// of the X-MoD notes) at the selected rows.
+//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (TMEM lane = output
+//               row, 32 columns at a time), the fused epilogue math, and 16-byte global
+//               loads and stores of that row segment. The other accumulator meanwhile
+//               receives the next tile's MMAs.
+// Fused epilogues: plain store (optionally q | k | v from three weight tensors, with
+// v written transposed for the attention kernel), O-projection (h = x_sel + a in
+// fp32, and a itself when asked), SwiGLU (gate and up halves of one tile), and the
+// down projection's gated scatter back into the residual stream at the selected rows
+// (X-MoD notes Eq. 7 / Eq. 6; a dense layer adds a + f), which reads a back as h - x.
 
 #include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <limits.h>
 #include <string.h>
@@ -37,17 +38,17 @@ constexpr int NUM_THREADS = 192;
 
 template <int BN>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
 };
 
 struct TcArgs {
   int M, N, K;
-  int mode;            // EpiKind
+  int mode;                // EpiKind
   int n_split1, n_split2;  // STORE: first accumulator column served by B map 1 / map 2
   int tiles_m, tiles;
   Epilogue e;
@@ -62,49 +63,45 @@ __device__ __forceinline__ int64_t stream_row_of(const Epilogue& e, int m) {
   return b * e.T + t;
 }
 
-// Store 32 fp32 values as bf16 at p[0..32), only the first `rem` columns.
+// Row-segment helpers of the direct epilogue: 32 consecutive columns of one row,
+// of which the first `rem` exist (rem is a multiple of 8 or >= 32).
 __device__ __forceinline__ void store32_bf16(__nv_bfloat16* p, const float (&v)[32], int rem) {
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    if (8 * g + 8 <= rem) {
+    if (8 * g < rem) {
       uint4 q;
       q.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
       q.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
       q.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
       q.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
       *reinterpret_cast<uint4*>(p + 8 * g) = q;
-    } else {
-      for (int i = 8 * g; i < rem && i < 8 * g + 8; ++i) p[i] = __float2bfloat16_rn(v[i]);
     }
   }
 }
 
 __device__ __forceinline__ void store32_f32(float* p, const float (&v)[32], int rem) {
 #pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    if (4 * g + 4 <= rem) {
+  for (int g = 0; g < 8; ++g)
+    if (4 * g < rem)
       *reinterpret_cast<float4*>(p + 4 * g) =
           make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-    } else {
-      for (int i = 4 * g; i < rem && i < 4 * g + 4; ++i) p[i] = v[i];
-    }
-  }
 }
 
 __device__ __forceinline__ void load32_bf16(const __nv_bfloat16* p, float (&v)[32], int rem) {
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    if (8 * g + 8 <= rem) {
+    if (8 * g < rem) {
       const uint4 q = *reinterpret_cast<const uint4*>(p + 8 * g);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&q);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
+        const float2 f = __bfloat1622float2(h2[i]);
         v[8 * g + 2 * i] = f.x;
         v[8 * g + 2 * i + 1] = f.y;
       }
     } else {
-      for (int i = 8 * g; i < 8 * g + 8; ++i) v[i] = i < rem ? __bfloat162float(p[i]) : 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[8 * g + i] = 0.f;
     }
   }
 }
@@ -112,98 +109,116 @@ __device__ __forceinline__ void load32_bf16(const __nv_bfloat16* p, float (&v)[3
 __device__ __forceinline__ void load32_f32(const float* p, float (&v)[32], int rem) {
 #pragma unroll
   for (int g = 0; g < 8; ++g) {
-    if (4 * g + 4 <= rem) {
+    if (4 * g < rem) {
       const float4 q = *reinterpret_cast<const float4*>(p + 4 * g);
       v[4 * g] = q.x;
       v[4 * g + 1] = q.y;
       v[4 * g + 2] = q.z;
       v[4 * g + 3] = q.w;
     } else {
-      for (int i = 4 * g; i < 4 * g + 4; ++i) v[i] = i < rem ? p[i] : 0.f;
+      v[4 * g] = v[4 * g + 1] = v[4 * g + 2] = v[4 * g + 3] = 0.f;
     }
   }
 }
 
-// The epilogue of one tile for this thread's row m (TMEM lane row of t_row).
-// Every thread of the warp executes the TMEM loads (warp-collective); only rows
-// inside the matrix store.
-template <int BN>
-__device__ __forceinline__ void epilogue_tile(const TcArgs& a, int m, int n_blk, uint32_t t_row) {
+// Relative cost per output column of a tile of width 256 / 192 / 128 (the narrower
+// tiles read more shared memory per FLOP), calibrated on the A4K8 block's GEMMs;
+// used to pick the tile width.
+#ifndef XMOD_COST_256
+#define XMOD_COST_256 1.0
+#endif
+#ifndef XMOD_COST_192
+#define XMOD_COST_192 1.15
+#endif
+#ifndef XMOD_COST_128
+#define XMOD_COST_128 1.33
+#endif
+
+// This lane writes its own row's 32 columns. (Passing each 32 x 32 chunk through
+// shared memory to store along rows instead measured 1.3-1.5 ms per step slower on
+// the A4K8 block: the extra shared-memory traffic competes with the MMA operand
+// reads, and one epilogue warp per scheduler cannot hide the added latency.)
+__device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int m, int col0,
+                                                      int64_t xrow, float r, float (&v)[32]) {
   const Epilogue& e = a.e;
-  const bool row_ok = m < a.M;
-  if (a.mode == EPI_SWIGLU) {
-    constexpr int HALF = BN / 2;
-#pragma unroll 1
-    for (int c = 0; c < HALF / 32; ++c) {
-      float g[32], u[32];
-      tmem_ld32(t_row + c * 32, g);
-      tmem_ld32(t_row + HALF + c * 32, u);
-      tmem_ld_wait();
-      const int n = n_blk * HALF + c * 32;
-      if (row_ok && n < a.N) {
+  if (m >= a.M || col0 >= a.N) return;
+  const int rem = a.N - col0;
+  if (a.mode == EPI_STORE || a.mode == EPI_SWIGLU) {
+    store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem);
+  } else if (a.mode == EPI_OPROJ) {
+    float xv[32];
+    load32_bf16((const __nv_bfloat16*)e.x + xrow + col0, xv, rem);
+    if (e.out) store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) g[i] = silu_f(g[i]) * u[i];
-        store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + n, g, a.N - n);
-      }
+    for (int i = 0; i < 32; ++i) xv[i] += v[i];
+    store32_f32((float*)e.out2 + (int64_t)m * e.ldo2 + col0, xv, rem);
+  } else {  // EPI_DOWN_SCATTER, a = h - x
+    float xv[32], hv[32];
+    __nv_bfloat16* xp = (__nv_bfloat16*)e.x + xrow + col0;
+    load32_bf16(xp, xv, rem);
+    load32_f32(e.h + (int64_t)m * e.d + col0, hv, rem);
+    if (e.gate == XMOD_GATE_XMOD) {
+      const float g7 = e.varsigma * r;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) xv[i] += g7 * ((hv[i] - xv[i]) + v[i]);   // Eq. 7
+    } else if (e.gate == XMOD_GATE_MOD) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) xv[i] = hv[i] + r * v[i];                 // Eq. 6
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) xv[i] = hv[i] + v[i];                     // dense layer
     }
-    return;
+    store32_bf16(xp, xv, rem);
   }
-  int64_t xrow = 0;
-  float r = 1.0f;
-  if (row_ok && (a.mode == EPI_OPROJ || a.mode == EPI_DOWN_SCATTER)) {
-    xrow = stream_row_of(e, m) * e.d;
-    if (a.mode == EPI_DOWN_SCATTER && e.gate >= 0) r = e.r_sel[m];
+}
+
+// Epilogue of one tile for this warp's 32-row slab [wrow0, wrow0 + 32).
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const TcArgs& a, int wrow0, int lane, int n_blk,
+                                              uint32_t t_row) {
+  const Epilogue& e = a.e;
+  const bool swiglu = a.mode == EPI_SWIGLU;
+  // the row this lane owns in TMEM: its stream row and gate
+  const int m_own = wrow0 + lane;
+  int64_t xrow_own = 0;
+  float r_own = 1.0f;
+  if ((a.mode == EPI_OPROJ || a.mode == EPI_DOWN_SCATTER) && m_own < a.M) {
+    xrow_own = stream_row_of(e, m_own) * e.d;
+    if (a.mode == EPI_DOWN_SCATTER && e.gate >= 0) r_own = e.r_sel[m_own];
   }
+  constexpr int NCH_FULL = BN / 32;
+  const int nch = swiglu ? NCH_FULL / 2 : NCH_FULL;
+  const int col_tile0 = swiglu ? n_blk * (BN / 2) : n_blk * BN;
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = 0; c < nch; ++c) {
     float v[32];
-    tmem_ld32(t_row + c * 32, v);
-    tmem_ld_wait();
-    const int n = n_blk * BN + c * 32;
-    if (!row_ok || n >= a.N) continue;
-    const int rem = a.N - n;
-    if (a.mode == EPI_STORE) {
-      if (e.vt && n >= e.vt_col0) {
-        // v^T: token m of sequence b goes to column t of rows (b, g, dim) -- across a
-        // warp the 32 consecutive tokens of one dim form one contiguous run.
-        const int cv = n - e.vt_col0;
+    if (swiglu) {
+      float u[32];
+      tmem_ld32(t_row + c * 32, v);
+      tmem_ld32(t_row + BN / 2 + c * 32, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]) * u[i];
+    } else {
+      tmem_ld32(t_row + c * 32, v);
+      tmem_ld_wait();
+    }
+    const int col0 = col_tile0 + c * 32;
+    if (a.mode == EPI_STORE && e.vt && col0 >= e.vt_col0) {
+      // v^T: token m of sequence b goes to column t of rows (b, g, dim). For each dim
+      // the warp's 32 consecutive tokens form one contiguous run, so no staging.
+      if (m_own < a.M && col0 < a.N) {
+        const int cv = col0 - e.vt_col0;
         const int g = cv / e.vt_hd, dim0 = cv % e.vt_hd;
-        const int64_t b = m / e.n_per_seq, t = m - b * e.n_per_seq;
+        const int64_t b = m_own / e.n_per_seq, t = m_own - b * e.n_per_seq;
         __nv_bfloat16* p =
             (__nv_bfloat16*)e.vt + ((b * e.vt_hkv + g) * e.vt_hd + dim0) * (int64_t)e.vt_ld + t;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < rem) p[(int64_t)i * e.vt_ld] = __float2bfloat16_rn(v[i]);
-      } else {
-        store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + n, v, rem);
+        for (int i = 0; i < 32; ++i) p[(int64_t)i * e.vt_ld] = __float2bfloat16_rn(v[i]);
       }
-    } else if (a.mode == EPI_OPROJ) {
-      float xv[32];
-      load32_bf16((const __nv_bfloat16*)e.x + xrow + n, xv, rem);
-      if (e.a_f32) store32_f32((float*)e.out + (int64_t)m * e.ldo + n, v, rem);
-      else store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + n, v, rem);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) xv[i] += v[i];
-      store32_f32((float*)e.out2 + (int64_t)m * e.ldo2 + n, xv, rem);
-    } else {  // EPI_DOWN_SCATTER
-      float xv[32], av[32];
-      __nv_bfloat16* xp = (__nv_bfloat16*)e.x + xrow + n;
-      load32_bf16(xp, xv, rem);
-      if (e.a_f32) load32_f32((const float*)e.a + (int64_t)m * e.d + n, av, rem);
-      else load32_bf16((const __nv_bfloat16*)e.a + (int64_t)m * e.d + n, av, rem);
-      if (e.gate == XMOD_GATE_XMOD) {
-        const float g7 = e.varsigma * r;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) xv[i] += g7 * (av[i] + v[i]);      // Eq. 7
-      } else if (e.gate == XMOD_GATE_MOD) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) xv[i] += av[i] + r * v[i];         // Eq. 6
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) xv[i] += av[i] + v[i];             // dense layer
-      }
-      store32_bf16(xp, xv, rem);
+      continue;
     }
+    epilogue_chunk_direct(a, m_own, col0, xrow_own, r_own, v);
   }
 }
 
@@ -324,15 +339,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
       if (!mbar_wait(ACC_FULL(acc), aph, abort_flag, args.status)) break;
       tc_fence_after();
-      const int m = (tile % args.tiles_m) * BM + quad * 32 + lane;
+      const int wrow0 = (tile % args.tiles_m) * BM + quad * 32;
       const int n_blk = tile / args.tiles_m;
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<BN>(args, m, n_blk, t_row);
+      epilogue_tile<BN>(args, wrow0, lane, n_blk, t_row);
       tc_fence_before();
       mbar_arrive(ACC_EMPTY(acc));
     }
   }
 
+  tc_fence_before();
   __syncthreads();
   if (*abort_flag) {
     // A wait ran out: give copies and MMAs still in flight time to land before the
@@ -395,6 +411,7 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   if (e.kind == EPI_SWIGLU) {
     if (!make_map(&mB0, p.B[0], p.K, p.N, p.ldb, BN / 2)) return cudaErrorInvalidValue;
     if (!make_map(&mB1, p.B[1], p.K, p.N, p.ldb, BN / 2)) return cudaErrorInvalidValue;
+    mB2 = mB0;
     tiles_n = (p.N + BN / 2 - 1) / (BN / 2);
   } else {
     const int rows0 = p.nB > 1 ? p.split[0] : p.N;
@@ -412,7 +429,6 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
     if (p.nB < 3) mB2 = mB0;
     tiles_n = (p.N + BN - 1) / BN;
   }
-  if (e.kind == EPI_SWIGLU) mB2 = mB0;
   a.tiles = a.tiles_m * tiles_n;
   if (a.tiles <= 0) return cudaSuccess;
   auto k = gemm_tc_kernel<BN>;
@@ -427,6 +443,14 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   return cudaGetLastError();
 }
 
+// Tile widths a problem may use: the q|k|v boundaries must fall on tile edges.
+bool bn_ok(const GemmTcProblem& p, const Epilogue& e, int bn) {
+  if (e.kind == EPI_SWIGLU) return bn == 256;
+  for (int i = 1; i < p.nB; ++i)
+    if (p.split[i - 1] % bn) return false;
+  return true;
+}
+
 }  // namespace
 
 bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e) {
@@ -435,29 +459,35 @@ bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e) {
   if (p.K % 8 || p.lda % 8 || p.ldb % 8 || p.N % 8) return false;
   if (((uintptr_t)p.A & 15) || ((uintptr_t)p.B[0] & 15)) return false;
   if (e.kind == EPI_SWIGLU && (p.nB != 2 || ((uintptr_t)p.B[1] & 15))) return false;
-  if (e.kind != EPI_SWIGLU) {
-    for (int i = 1; i < p.nB; ++i) {
+  if (e.kind != EPI_SWIGLU)
+    for (int i = 1; i < p.nB; ++i)
       if ((uintptr_t)p.B[i] & 15) return false;
-      if (p.split[i - 1] % 256) return false;  // tiles must not straddle two weight tensors
-    }
-  }
-  return true;
+  return bn_ok(p, e, 128) || bn_ok(p, e, 256);
 }
 
 cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   const int tiles_m = (p.M + BM - 1) / BM;
   const int sms = sm_count();
-  // Pick the tile width with the shorter estimated time: waves x tile width, with
-  // the narrower tile charged for its higher shared-memory traffic per FLOP.
-  int bn = 256;
-  if (e.kind != EPI_SWIGLU) {
-    const long t256 = (long)tiles_m * ((p.N + 255) / 256);
-    const long t128 = (long)tiles_m * ((p.N + 127) / 128);
-    const double c256 = (double)((t256 + sms - 1) / sms) * 256.0;
-    const double c128 = (double)((t128 + sms - 1) / sms) * 128.0 * 1.15;
-    bn = c128 < c256 ? 128 : 256;
+  // Pick the tile width with the shortest estimated time: waves x tile width, with
+  // narrower tiles charged for their higher shared-memory traffic per FLOP.
+  const int widths[3] = {256, 192, 128};
+  const double cost_per_col[3] = {XMOD_COST_256, XMOD_COST_192, XMOD_COST_128};
+  int best = -1;
+  double best_cost = 0.0;
+  for (int i = 0; i < 3; ++i) {
+    const int bn = widths[i];
+    if (!bn_ok(p, e, bn)) continue;
+    const int cols = e.kind == EPI_SWIGLU ? bn / 2 : bn;
+    const long tiles = (long)tiles_m * ((p.N + cols - 1) / cols);
+    const double cost = (double)((tiles + sms - 1) / sms) * bn * cost_per_col[i];
+    if (best < 0 || cost < best_cost) {
+      best = bn;
+      best_cost = cost;
+    }
   }
-  return bn == 256 ? launch_bn<256>(c, p, e) : launch_bn<128>(c, p, e);
+  if (best == 256) return launch_bn<256>(c, p, e);
+  if (best == 192) return launch_bn<192>(c, p, e);
+  return launch_bn<128>(c, p, e);
 }
 
 }  // namespace xmod

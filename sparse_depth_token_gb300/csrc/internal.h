@@ -78,9 +78,9 @@ cudaError_t launch_gated_scatter(const Ctx& c, xmod_dtype dt, int B, int T, int 
 
 enum EpiKind {
   EPI_STORE = 0,         // out[m, n] = acc
-  EPI_OPROJ = 1,         // out[m, n] = a = acc; out2[m, n] = h = x_row(m)[n] + acc (fp32)
+  EPI_OPROJ = 1,         // out2[m, n] = h = x_row(m)[n] + acc (fp32); out[m, n] = a = acc if out
   EPI_SWIGLU = 2,        // out[m, n] = silu(acc_gate) * acc_up
-  EPI_DOWN_SCATTER = 3,  // x_row(m)[n] = gated residual of (a[m, n], f = acc)
+  EPI_DOWN_SCATTER = 3,  // x_row(m)[n] = gated residual of (a = h[m, n] - x, f = acc)
 };
 
 // Compact row m of a block belongs to sequence b = m / n_per_seq at position
@@ -94,8 +94,7 @@ struct Epilogue {
   void* x = nullptr;            // residual stream [B, T, d] (read for OPROJ, updated for DOWN)
   const int32_t* idx = nullptr;
   int T = 0, n_per_seq = 0, d = 0;
-  const void* a = nullptr;      // DOWN: attention residual [M, d]
-  bool a_f32 = false;           // OPROJ writes / DOWN reads a as fp32 (else the element type)
+  const float* h = nullptr;     // DOWN: h = x_sel + a [M, d] fp32 (the attention residual is h - x)
   const float* r_sel = nullptr; // DOWN: gates [M]
   float varsigma = 1.0f;
   int gate = -1;                // DOWN: XMOD_GATE_XMOD, XMOD_GATE_MOD, or -1 for dense
