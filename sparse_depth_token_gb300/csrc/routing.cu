@@ -86,6 +86,87 @@ static int num_sms() {
   return g_num_sms;
 }
 
+// Register-cached variant for rows of at most 32 * VPL 16-byte vectors: a warp
+// issues every load of its row before reducing, so a whole row is in flight at once.
+template <typename T, int VPL>
+__global__ void __launch_bounds__(ROUTER_WARPS * 32)
+router_rows_kernel(int64_t rows, int d, const T* __restrict__ x, const T* __restrict__ w_r,
+                   const float* __restrict__ bias, float* __restrict__ s, float* __restrict__ r) {
+  extern __shared__ float4 wsh4[];
+  float* wsh = reinterpret_cast<float*>(wsh4);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) wsh[i] = ld_f(w_r + i);
+  __syncthreads();
+  constexpr int V = Vec16<T>::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * ROUTER_WARPS;
+  for (int64_t row = (int64_t)blockIdx.x * ROUTER_WARPS + warp; row < rows; row += stride) {
+    const T* xr = x + row * d;
+    Vec16<T> v[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int c = (i * 32 + lane) * V;
+      if (c < d) v[i] = ld_vec_stream(xr + c);
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int c = (i * 32 + lane) * V;
+      if (c < d) {
+#pragma unroll
+        for (int e = 0; e < V; e += 4) {
+          const float4 w = wsh4[(c + e) >> 2];
+          acc = fmaf(v[i].get(e), w.x, acc);
+          acc = fmaf(v[i].get(e + 1), w.y, acc);
+          acc = fmaf(v[i].get(e + 2), w.z, acc);
+          acc = fmaf(v[i].get(e + 3), w.w, acc);
+        }
+      }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) {
+      if (bias) acc += bias[row];
+      s[row] = acc;
+      if (r) r[row] = sigmoidf_acc(acc);
+    }
+  }
+}
+
+// Smallest supported vectors-per-lane count covering `vecs` 16-byte vectors per row
+// (0 if the row is too long for the register-cached kernels).
+static int pick_vpl(int vecs_per_lane) {
+  const int opts[] = {1, 2, 4, 6, 8, 12, 16};
+  for (int o : opts)
+    if (vecs_per_lane <= o) return o;
+  return 0;
+}
+
+template <typename T>
+static cudaError_t launch_router_rows(const Ctx& c, int vpl, unsigned blocks, size_t smem,
+                                      int64_t rows, int d, const T* x, const T* w_r,
+                                      const float* bias, float* s, float* r) {
+#define XMOD_ROUTER_CASE(N)                                                                  \
+  case N: {                                                                                  \
+    auto k = router_rows_kernel<T, N>;                                                       \
+    if (smem > 48 * 1024)                                                                    \
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);       \
+    k<<<blocks, ROUTER_WARPS * 32, smem, c.stream>>>(rows, d, x, w_r, bias, s, r);           \
+    break;                                                                                   \
+  }
+  switch (vpl) {
+    XMOD_ROUTER_CASE(1)
+    XMOD_ROUTER_CASE(2)
+    XMOD_ROUTER_CASE(4)
+    XMOD_ROUTER_CASE(6)
+    XMOD_ROUTER_CASE(8)
+    XMOD_ROUTER_CASE(12)
+    XMOD_ROUTER_CASE(16)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef XMOD_ROUTER_CASE
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router(const Ctx& c, xmod_dtype dt, int64_t rows, int d, const void* x,
                           const void* w_r, const float* bias, float* s, float* r) {
   if (rows <= 0) return cudaSuccess;
@@ -93,6 +174,16 @@ cudaError_t launch_router(const Ctx& c, xmod_dtype dt, int64_t rows, int d, cons
   const int64_t cap = (int64_t)num_sms() * 8;  // 8 resident CTAs of 256 threads per SM
   if (blocks > cap) blocks = cap;
   const size_t smem = sizeof(float) * (size_t)d;
+  const int vec = dt == XMOD_BF16 ? 8 : 4;
+  const int vpl = pick_vpl((d / vec + 31) / 32);
+  if (vpl) {
+    if (dt == XMOD_BF16)
+      return launch_router_rows<__nv_bfloat16>(c, vpl, (unsigned)blocks, smem, rows, d,
+                                               (const __nv_bfloat16*)x,
+                                               (const __nv_bfloat16*)w_r, bias, s, r);
+    return launch_router_rows<float>(c, vpl, (unsigned)blocks, smem, rows, d, (const float*)x,
+                                     (const float*)w_r, bias, s, r);
+  }
   if (dt == XMOD_BF16) {
     auto k = router_kernel<__nv_bfloat16>;
     if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -320,6 +411,74 @@ gather_rmsnorm_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x
   }
 }
 
+// Register-cached variant (rows of at most 32 * VPL 16-byte vectors): the row is
+// read once with every load in flight, then normalised from registers.
+template <typename T, int VPL>
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+gather_rmsnorm_rows_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
+                           const int32_t* __restrict__ idx, const T* __restrict__ gamma,
+                           float eps, T* __restrict__ u) {
+  constexpr int V = Vec16<T>::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
+  if (m >= M) return;
+  const T* src = x + stream_row(m, seqT, n, idx) * d;
+  Vec16<T> v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = (i * 32 + lane) * V;
+    if (c < d) v[i] = ld_vec(src + c);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = (i * 32 + lane) * V;
+    if (c < d) {
+#pragma unroll
+      for (int e = 0; e < V; ++e) ss = fmaf(v[i].get(e), v[i].get(e), ss);
+    }
+  }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)d + eps);
+  T* dst = u + m * d;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = (i * 32 + lane) * V;
+    if (c < d) {
+      const Vec16<T> g = ld_vec(gamma + c);
+      Vec16<T> o;
+#pragma unroll
+      for (int e = 0; e < V; ++e) o.set(e, v[i].get(e) * inv * g.get(e));
+      st_vec(dst + c, o);
+    }
+  }
+}
+
+template <typename T>
+static cudaError_t launch_gather_rmsnorm_rows(const Ctx& c, int vpl, unsigned blocks, int64_t M,
+                                              int seqT, int n, int d, const T* x,
+                                              const int32_t* idx, const T* gamma, float eps,
+                                              T* u) {
+#define XMOD_GR_CASE(N)                                                                     \
+  case N:                                                                                   \
+    gather_rmsnorm_rows_kernel<T, N><<<blocks, ROW_WARPS * 32, 0, c.stream>>>(              \
+        M, seqT, n, d, x, idx, gamma, eps, u);                                              \
+    break;
+  switch (vpl) {
+    XMOD_GR_CASE(1)
+    XMOD_GR_CASE(2)
+    XMOD_GR_CASE(4)
+    XMOD_GR_CASE(6)
+    XMOD_GR_CASE(8)
+    XMOD_GR_CASE(12)
+    XMOD_GR_CASE(16)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef XMOD_GR_CASE
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gather(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
                           const void* x, const int32_t* idx, void* xs) {
   const int64_t M = (int64_t)B * n;
@@ -340,6 +499,15 @@ cudaError_t launch_gather_rmsnorm(const Ctx& c, xmod_dtype dt, int B, int T, int
   const int64_t M = (int64_t)B * n;
   if (M <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
+  const int vpl = pick_vpl((d / (dt == XMOD_BF16 ? 8 : 4) + 31) / 32);
+  if (vpl) {
+    if (dt == XMOD_BF16)
+      return launch_gather_rmsnorm_rows<__nv_bfloat16>(
+          c, vpl, blocks, M, T, n, d, (const __nv_bfloat16*)x, idx, (const __nv_bfloat16*)gamma,
+          eps, (__nv_bfloat16*)u);
+    return launch_gather_rmsnorm_rows<float>(c, vpl, blocks, M, T, n, d, (const float*)x, idx,
+                                             (const float*)gamma, eps, (float*)u);
+  }
   if (dt == XMOD_BF16)
     gather_rmsnorm_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
         M, T, n, d, (const __nv_bfloat16*)x, idx, (const __nv_bfloat16*)gamma, eps,
@@ -376,10 +544,95 @@ rmsnorm_f32in_kernel(int64_t M, int d, const float* __restrict__ h, const T* __r
   }
 }
 
+// Register-cached variant: units of V = 16 / sizeof(T) elements (one 16-byte output
+// vector, V/4 float4 inputs), at most VPL units per lane.
+template <typename T, int VPL>
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+rmsnorm_f32in_rows_kernel(int64_t M, int d, const float* __restrict__ h,
+                          const T* __restrict__ gamma, float eps, T* __restrict__ out) {
+  constexpr int V = Vec16<T>::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
+  if (m >= M) return;
+  const float* src = h + m * d;
+  float4 v[VPL][V / 4];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = (i * 32 + lane) * V;
+    if (c < d) {
+#pragma unroll
+      for (int q = 0; q < V / 4; ++q) v[i][q] = *reinterpret_cast<const float4*>(src + c + 4 * q);
+    }
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = (i * 32 + lane) * V;
+    if (c < d) {
+#pragma unroll
+      for (int q = 0; q < V / 4; ++q)
+        ss = fmaf(v[i][q].x, v[i][q].x,
+                  fmaf(v[i][q].y, v[i][q].y, fmaf(v[i][q].z, v[i][q].z, fmaf(v[i][q].w, v[i][q].w, ss))));
+    }
+  }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)d + eps);
+  T* dst = out + m * d;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = (i * 32 + lane) * V;
+    if (c < d) {
+      const Vec16<T> g = ld_vec(gamma + c);
+      Vec16<T> o;
+#pragma unroll
+      for (int q = 0; q < V / 4; ++q) {
+        o.set(4 * q + 0, v[i][q].x * inv * g.get(4 * q + 0));
+        o.set(4 * q + 1, v[i][q].y * inv * g.get(4 * q + 1));
+        o.set(4 * q + 2, v[i][q].z * inv * g.get(4 * q + 2));
+        o.set(4 * q + 3, v[i][q].w * inv * g.get(4 * q + 3));
+      }
+      st_vec(dst + c, o);
+    }
+  }
+}
+
+template <typename T>
+static cudaError_t launch_rmsnorm_f32in_rows(const Ctx& c, int vpl, unsigned blocks, int64_t M,
+                                             int d, const float* h, const T* gamma, float eps,
+                                             T* out) {
+#define XMOD_RN_CASE(N)                                                                    \
+  case N:                                                                                  \
+    rmsnorm_f32in_rows_kernel<T, N><<<blocks, ROW_WARPS * 32, 0, c.stream>>>(M, d, h, gamma, \
+                                                                            eps, out);     \
+    break;
+  switch (vpl) {
+    XMOD_RN_CASE(1)
+    XMOD_RN_CASE(2)
+    XMOD_RN_CASE(4)
+    XMOD_RN_CASE(6)
+    XMOD_RN_CASE(8)
+    XMOD_RN_CASE(12)
+    XMOD_RN_CASE(16)
+    default:
+      return cudaErrorInvalidValue;
+  }
+#undef XMOD_RN_CASE
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rmsnorm_f32in(const Ctx& c, xmod_dtype dt, int64_t M, int d, const float* h,
                                  const void* gamma, float eps, void* out) {
   if (M <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
+  const int vpl = pick_vpl((d / (dt == XMOD_BF16 ? 8 : 4) + 31) / 32);
+  if (vpl) {
+    if (dt == XMOD_BF16)
+      return launch_rmsnorm_f32in_rows<__nv_bfloat16>(c, vpl, blocks, M, d, h,
+                                                      (const __nv_bfloat16*)gamma, eps,
+                                                      (__nv_bfloat16*)out);
+    return launch_rmsnorm_f32in_rows<float>(c, vpl, blocks, M, d, h, (const float*)gamma, eps,
+                                            (float*)out);
+  }
   if (dt == XMOD_BF16)
     rmsnorm_f32in_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
         M, d, h, (const __nv_bfloat16*)gamma, eps, (__nv_bfloat16*)out);
