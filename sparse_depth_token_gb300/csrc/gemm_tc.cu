@@ -34,7 +34,13 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BK = 64;
-constexpr int NUM_THREADS = 192;
+// Epilogue warps: two per TMEM lane quadrant, each taking every other 32-column
+// chunk of the tile, so the epilogue of a CTA's last tile finishes sooner.
+#ifndef XMOD_EPI_WARPS
+#define XMOD_EPI_WARPS 8
+#endif
+constexpr int EPI_WARPS = XMOD_EPI_WARPS;
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 
 template <int BN>
 struct Cfg {
@@ -175,7 +181,7 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int m, in
 // Epilogue of one tile for this warp's 32-row slab [wrow0, wrow0 + 32).
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int wrow0, int lane, int n_blk,
-                                              uint32_t t_row) {
+                                              uint32_t t_row, int part, int nparts) {
   const Epilogue& e = a.e;
   const bool swiglu = a.mode == EPI_SWIGLU;
   // the row this lane owns in TMEM: its stream row and gate
@@ -190,7 +196,7 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int wrow0, int la
   const int nch = swiglu ? NCH_FULL / 2 : NCH_FULL;
   const int col_tile0 = swiglu ? n_blk * (BN / 2) : n_blk * BN;
 #pragma unroll 1
-  for (int c = 0; c < nch; ++c) {
+  for (int c = part; c < nch; c += nparts) {
     float v[32];
     if (swiglu) {
       float u[32];
@@ -253,7 +259,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(ACC_FULL(a), 1);
-      mbar_init(ACC_EMPTY(a), 128);
+      mbar_init(ACC_EMPTY(a), 32 * EPI_WARPS);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -342,7 +348,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int wrow0 = (tile % args.tiles_m) * BM + quad * 32;
       const int n_blk = tile / args.tiles_m;
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<BN>(args, wrow0, lane, n_blk, t_row);
+      epilogue_tile<BN>(args, wrow0, lane, n_blk, t_row, (warp - 2) / 4, EPI_WARPS / 4);
       tc_fence_before();
       mbar_arrive(ACC_EMPTY(acc));
     }
