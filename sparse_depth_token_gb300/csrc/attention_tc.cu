@@ -69,6 +69,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __global__ void __launch_bounds__(THREADS, 1)
 attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant__ CUtensorMap tmVt,
                     const AttnArgs a) {
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -115,6 +116,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;   // S0: cols 0..127, S1: 128..255, O: 256..383
   const uint32_t tO = tmem + 256u;
+  pdl_wait();  // everything above overlapped the previous kernel's tail
 
   if (warp == 0) {
     if (lane == 0) {
@@ -352,8 +354,7 @@ cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, con
     attr = true;
   }
   dim3 grid(a.nqb, hq, B);
-  attention_tc_kernel<<<grid, THREADS, SMEM, c.stream>>>(mQK, mVt, a);
-  return cudaGetLastError();
+  return launch_pdl(attention_tc_kernel, grid, dim3(THREADS), SMEM, c.stream, mQK, mVt, a);
 }
 
 }  // namespace xmod

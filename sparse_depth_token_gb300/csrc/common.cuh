@@ -77,4 +77,16 @@ __device__ __forceinline__ void report_status(int* status, int code) {
 
 __device__ __forceinline__ float sigmoidf_acc(float s) { return 1.0f / (1.0f + expf(-s)); }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+//
+// Kernels launched with launch_pdl() may start while the previous kernel on the
+// stream is still finishing. Each such kernel lets its own successor start early
+// (pdl_trigger) and, before its first global-memory access, waits until every
+// earlier grid on the stream has completed and its writes are visible (pdl_wait).
+// Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace xmod

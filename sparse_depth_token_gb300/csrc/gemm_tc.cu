@@ -234,6 +234,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
                const TcArgs args) {
   using C = Cfg<BN>;
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -273,6 +274,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // everything above overlapped the previous kernel's tail
 
   if (warp == 0) {
     if (lane == 0) {
@@ -445,8 +447,7 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
     attr_set = true;
   }
   const int grid = a.tiles < sm_count() ? a.tiles : sm_count();
-  k<<<grid, NUM_THREADS, Cf::SMEM, c.stream>>>(mA, mB0, mB1, mB2, a);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(grid), dim3(NUM_THREADS), Cf::SMEM, c.stream, mA, mB0, mB1, mB2, a);
 }
 
 // Tile widths a problem may use: the q|k|v boundaries must fall on tile edges.

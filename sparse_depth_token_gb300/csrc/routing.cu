@@ -26,6 +26,8 @@ template <typename T>
 __global__ void __launch_bounds__(ROUTER_WARPS * 32)
 router_kernel(int64_t rows, int d, const T* __restrict__ x, const T* __restrict__ w_r,
               const float* __restrict__ bias, float* __restrict__ s, float* __restrict__ r) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float4 wsh4[];
   float* wsh = reinterpret_cast<float*>(wsh4);
   for (int i = threadIdx.x; i < d; i += blockDim.x) wsh[i] = ld_f(w_r + i);
@@ -92,6 +94,8 @@ template <typename T, int VPL>
 __global__ void __launch_bounds__(ROUTER_WARPS * 32)
 router_rows_kernel(int64_t rows, int d, const T* __restrict__ x, const T* __restrict__ w_r,
                    const float* __restrict__ bias, float* __restrict__ s, float* __restrict__ r) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float4 wsh4[];
   float* wsh = reinterpret_cast<float*>(wsh4);
   for (int i = threadIdx.x; i < d; i += blockDim.x) wsh[i] = ld_f(w_r + i);
@@ -149,7 +153,7 @@ static cudaError_t launch_router_rows(const Ctx& c, int vpl, unsigned blocks, si
     auto k = router_rows_kernel<T, N>;                                                       \
     if (smem > 48 * 1024)                                                                    \
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);       \
-    k<<<blocks, ROUTER_WARPS * 32, smem, c.stream>>>(rows, d, x, w_r, bias, s, r);           \
+    launch_pdl(k, dim3(blocks), dim3(ROUTER_WARPS * 32), smem, c.stream, rows, d, x, w_r, bias, s, r);           \
     break;                                                                                   \
   }
   switch (vpl) {
@@ -187,12 +191,12 @@ cudaError_t launch_router(const Ctx& c, xmod_dtype dt, int64_t rows, int d, cons
   if (dt == XMOD_BF16) {
     auto k = router_kernel<__nv_bfloat16>;
     if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<(unsigned)blocks, ROUTER_WARPS * 32, smem, c.stream>>>(
+    launch_pdl(k, dim3((unsigned)blocks), dim3(ROUTER_WARPS * 32), smem, c.stream, 
         rows, d, (const __nv_bfloat16*)x, (const __nv_bfloat16*)w_r, bias, s, r);
   } else {
     auto k = router_kernel<float>;
     if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<(unsigned)blocks, ROUTER_WARPS * 32, smem, c.stream>>>(rows, d, (const float*)x,
+    launch_pdl(k, dim3((unsigned)blocks), dim3(ROUTER_WARPS * 32), smem, c.stream, rows, d, (const float*)x,
                                                                (const float*)w_r, bias, s, r);
   }
   return cudaGetLastError();
@@ -242,6 +246,8 @@ __device__ __forceinline__ uint32_t warps_exclusive_scan(uint32_t v, uint32_t* s
 __global__ void __launch_bounds__(TOPK_THREADS)
 topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx,
             float* __restrict__ r_sel, int* status) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint32_t keys[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t scan_sh[32];
@@ -355,7 +361,7 @@ cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32
   const size_t smem = sizeof(uint32_t) * (size_t)T;
   cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)(sizeof(uint32_t) * TOPK_MAX_T));
-  topk_kernel<<<B, TOPK_THREADS, smem, c.stream>>>(T, n, s, idx, r_sel, c.status);
+  launch_pdl(topk_kernel, dim3(B), dim3(TOPK_THREADS), smem, c.stream, T, n, s, idx, r_sel, c.status);
   return cudaGetLastError();
 }
 
@@ -373,6 +379,8 @@ template <typename T>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 gather_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
               const int32_t* __restrict__ idx, T* __restrict__ xs) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
@@ -387,6 +395,8 @@ __global__ void __launch_bounds__(ROW_WARPS * 32)
 gather_rmsnorm_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
                       const int32_t* __restrict__ idx, const T* __restrict__ gamma, float eps,
                       T* __restrict__ u) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
@@ -418,6 +428,8 @@ __global__ void __launch_bounds__(ROW_WARPS * 32)
 gather_rmsnorm_rows_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
                            const int32_t* __restrict__ idx, const T* __restrict__ gamma,
                            float eps, T* __restrict__ u) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
@@ -461,7 +473,7 @@ static cudaError_t launch_gather_rmsnorm_rows(const Ctx& c, int vpl, unsigned bl
                                               T* u) {
 #define XMOD_GR_CASE(N)                                                                     \
   case N:                                                                                   \
-    gather_rmsnorm_rows_kernel<T, N><<<blocks, ROW_WARPS * 32, 0, c.stream>>>(              \
+    launch_pdl(gather_rmsnorm_rows_kernel<T, N>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream,               \
         M, seqT, n, d, x, idx, gamma, eps, u);                                              \
     break;
   switch (vpl) {
@@ -485,10 +497,10 @@ cudaError_t launch_gather(const Ctx& c, xmod_dtype dt, int B, int T, int n, int 
   if (M <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
   if (dt == XMOD_BF16)
-    gather_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+    launch_pdl(gather_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
         M, T, n, d, (const __nv_bfloat16*)x, idx, (__nv_bfloat16*)xs);
   else
-    gather_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(M, T, n, d, (const float*)x, idx,
+    launch_pdl(gather_kernel<float>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, M, T, n, d, (const float*)x, idx,
                                                           (float*)xs);
   return cudaGetLastError();
 }
@@ -509,11 +521,11 @@ cudaError_t launch_gather_rmsnorm(const Ctx& c, xmod_dtype dt, int B, int T, int
                                              (const float*)gamma, eps, (float*)u);
   }
   if (dt == XMOD_BF16)
-    gather_rmsnorm_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+    launch_pdl(gather_rmsnorm_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
         M, T, n, d, (const __nv_bfloat16*)x, idx, (const __nv_bfloat16*)gamma, eps,
         (__nv_bfloat16*)u);
   else
-    gather_rmsnorm_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+    launch_pdl(gather_rmsnorm_kernel<float>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
         M, T, n, d, (const float*)x, idx, (const float*)gamma, eps, (float*)u);
   return cudaGetLastError();
 }
@@ -522,6 +534,8 @@ template <typename T>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 rmsnorm_f32in_kernel(int64_t M, int d, const float* __restrict__ h, const T* __restrict__ gamma,
                      float eps, T* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
@@ -550,6 +564,8 @@ template <typename T, int VPL>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 rmsnorm_f32in_rows_kernel(int64_t M, int d, const float* __restrict__ h,
                           const T* __restrict__ gamma, float eps, T* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
@@ -602,7 +618,7 @@ static cudaError_t launch_rmsnorm_f32in_rows(const Ctx& c, int vpl, unsigned blo
                                              T* out) {
 #define XMOD_RN_CASE(N)                                                                    \
   case N:                                                                                  \
-    rmsnorm_f32in_rows_kernel<T, N><<<blocks, ROW_WARPS * 32, 0, c.stream>>>(M, d, h, gamma, \
+    launch_pdl(rmsnorm_f32in_rows_kernel<T, N>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, M, d, h, gamma, \
                                                                             eps, out);     \
     break;
   switch (vpl) {
@@ -634,10 +650,10 @@ cudaError_t launch_rmsnorm_f32in(const Ctx& c, xmod_dtype dt, int64_t M, int d, 
                                             (float*)out);
   }
   if (dt == XMOD_BF16)
-    rmsnorm_f32in_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+    launch_pdl(rmsnorm_f32in_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
         M, d, h, (const __nv_bfloat16*)gamma, eps, (__nv_bfloat16*)out);
   else
-    rmsnorm_f32in_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(M, d, h, (const float*)gamma,
+    launch_pdl(rmsnorm_f32in_kernel<float>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, M, d, h, (const float*)gamma,
                                                                  eps, (float*)out);
   return cudaGetLastError();
 }
@@ -649,6 +665,8 @@ __global__ void __launch_bounds__(ROW_WARPS * 32)
 gated_scatter_kernel(int64_t M, int seqT, int n, int d, T* __restrict__ x,
                      const int32_t* __restrict__ idx, const float* __restrict__ r_sel,
                      const T* __restrict__ a, const T* __restrict__ f, float varsigma, int gate) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
@@ -686,11 +704,11 @@ cudaError_t launch_gated_scatter(const Ctx& c, xmod_dtype dt, int B, int T, int 
   if (M <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
   if (dt == XMOD_BF16)
-    gated_scatter_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+    launch_pdl(gated_scatter_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
         M, T, n, d, (__nv_bfloat16*)x, idx, r_sel, (const __nv_bfloat16*)a,
         (const __nv_bfloat16*)f, varsigma, gate);
   else
-    gated_scatter_kernel<<<blocks, ROW_WARPS * 32, 0, c.stream>>>(
+    launch_pdl(gated_scatter_kernel<float>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
         M, T, n, d, (float*)x, idx, r_sel, (const float*)a, (const float*)f, varsigma, gate);
   return cudaGetLastError();
 }
