@@ -143,63 +143,133 @@ __device__ __forceinline__ void load32_f32(const float* p, float (&v)[32], int r
 #define XMOD_COST_128 1.33
 #endif
 
+// Inputs of the O-projection / down-projection epilogues for one 32-column chunk of
+// one row: x (bf16) and, for the down projection, h (fp32). They are loaded one chunk
+// ahead so that their memory latency overlaps the previous chunk's work.
+struct EpiIn {
+  uint4 x[4];
+  float4 h[8];
+};
+
+template <int MODE>
+__device__ __forceinline__ void epi_load_in(const TcArgs& a, int m, int col0, int64_t xrow,
+                                            EpiIn& in) {
+  const Epilogue& e = a.e;
+  if (m >= a.M || col0 >= a.N) return;
+  const int rem = a.N - col0;
+  const uint4* xp = reinterpret_cast<const uint4*>((const __nv_bfloat16*)e.x + xrow + col0);
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    if (8 * g < rem) in.x[g] = xp[g];
+  if (MODE == EPI_DOWN_SCATTER) {
+    const float4* hp = reinterpret_cast<const float4*>(e.h + (int64_t)m * e.d + col0);
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      if (4 * g < rem) in.h[g] = hp[g];
+  }
+}
+
+__device__ __forceinline__ void unpack_x(const EpiIn& in, float (&xv)[32]) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&in.x[g]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h2[i]);
+      xv[8 * g + 2 * i] = f.x;
+      xv[8 * g + 2 * i + 1] = f.y;
+    }
+  }
+}
+
 // This lane writes its own row's 32 columns. (Passing each 32 x 32 chunk through
 // shared memory to store along rows instead measured 1.3-1.5 ms per step slower on
 // the A4K8 block: the extra shared-memory traffic competes with the MMA operand
 // reads, and one epilogue warp per scheduler cannot hide the added latency.)
+template <int MODE>
 __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int m, int col0,
-                                                      int64_t xrow, float r, float (&v)[32]) {
+                                                      int64_t xrow, float r, float (&v)[32],
+                                                      const EpiIn& in) {
   const Epilogue& e = a.e;
   if (m >= a.M || col0 >= a.N) return;
   const int rem = a.N - col0;
-  if (a.mode == EPI_STORE || a.mode == EPI_SWIGLU) {
+  if (MODE == EPI_STORE || MODE == EPI_SWIGLU) {
     store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem);
-  } else if (a.mode == EPI_OPROJ) {
-    float xv[32];
-    load32_bf16((const __nv_bfloat16*)e.x + xrow + col0, xv, rem);
+  } else if (MODE == EPI_OPROJ) {
     if (e.out) store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem);
+    float* hp = (float*)e.out2 + (int64_t)m * e.ldo2 + col0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) xv[i] += v[i];
-    store32_f32((float*)e.out2 + (int64_t)m * e.ldo2 + col0, xv, rem);
-  } else {  // EPI_DOWN_SCATTER, a = h - x
-    float xv[32], hv[32];
-    __nv_bfloat16* xp = (__nv_bfloat16*)e.x + xrow + col0;
-    load32_bf16(xp, xv, rem);
-    load32_f32(e.h + (int64_t)m * e.d + col0, hv, rem);
-    if (e.gate == XMOD_GATE_XMOD) {
-      const float g7 = e.varsigma * r;
+    for (int g = 0; g < 4; ++g) {   // 8 columns at a time: h = x + a
+      if (8 * g >= rem) break;
+      const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&in.x[g]);
+      float hv[8];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) xv[i] += g7 * ((hv[i] - xv[i]) + v[i]);   // Eq. 7
-    } else if (e.gate == XMOD_GATE_MOD) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) xv[i] = hv[i] + r * v[i];                 // Eq. 6
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) xv[i] = hv[i] + v[i];                     // dense layer
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(x2[i]);
+        hv[2 * i] = f.x + v[8 * g + 2 * i];
+        hv[2 * i + 1] = f.y + v[8 * g + 2 * i + 1];
+      }
+      *reinterpret_cast<float4*>(hp + 8 * g) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+      *reinterpret_cast<float4*>(hp + 8 * g + 4) = make_float4(hv[4], hv[5], hv[6], hv[7]);
     }
-    store32_bf16(xp, xv, rem);
+  } else {  // EPI_DOWN_SCATTER, a = h - x
+    __nv_bfloat16* xp = (__nv_bfloat16*)e.x + xrow + col0;
+    const float g7 = e.varsigma * r;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {   // 8 columns at a time
+      if (8 * g >= rem) break;
+      const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&in.x[g]);
+      const float hv[8] = {in.h[2 * g].x, in.h[2 * g].y, in.h[2 * g].z, in.h[2 * g].w,
+                           in.h[2 * g + 1].x, in.h[2 * g + 1].y, in.h[2 * g + 1].z,
+                           in.h[2 * g + 1].w};
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(x2[i]);
+        const float xx[2] = {f.x, f.y};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int j = 2 * i + k;
+          const float fv = v[8 * g + j];
+          if (e.gate == XMOD_GATE_XMOD) y[j] = xx[k] + g7 * ((hv[j] - xx[k]) + fv);   // Eq. 7
+          else if (e.gate == XMOD_GATE_MOD) y[j] = hv[j] + r * fv;                   // Eq. 6
+          else y[j] = hv[j] + fv;                                                     // dense
+        }
+      }
+      uint4 q;
+      q.x = pack_bf16x2(y[0], y[1]);
+      q.y = pack_bf16x2(y[2], y[3]);
+      q.z = pack_bf16x2(y[4], y[5]);
+      q.w = pack_bf16x2(y[6], y[7]);
+      *reinterpret_cast<uint4*>(xp + 8 * g) = q;
+    }
   }
 }
 
 // Epilogue of one tile for this warp's 32-row slab [wrow0, wrow0 + 32).
-template <int BN>
+template <int BN, int MODE>
 __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int wrow0, int lane, int n_blk,
                                               uint32_t t_row, int part, int nparts) {
   const Epilogue& e = a.e;
-  const bool swiglu = a.mode == EPI_SWIGLU;
+  constexpr bool swiglu = MODE == EPI_SWIGLU;
   // the row this lane owns in TMEM: its stream row and gate
   const int m_own = wrow0 + lane;
   int64_t xrow_own = 0;
   float r_own = 1.0f;
-  if ((a.mode == EPI_OPROJ || a.mode == EPI_DOWN_SCATTER) && m_own < a.M) {
+  if ((MODE == EPI_OPROJ || MODE == EPI_DOWN_SCATTER) && m_own < a.M) {
     xrow_own = stream_row_of(e, m_own) * e.d;
-    if (a.mode == EPI_DOWN_SCATTER && e.gate >= 0) r_own = e.r_sel[m_own];
+    if (MODE == EPI_DOWN_SCATTER && e.gate >= 0) r_own = e.r_sel[m_own];
   }
   constexpr int NCH_FULL = BN / 32;
   const int nch = swiglu ? NCH_FULL / 2 : NCH_FULL;
   const int col_tile0 = swiglu ? n_blk * (BN / 2) : n_blk * BN;
+  constexpr bool needs_in = MODE == EPI_OPROJ || MODE == EPI_DOWN_SCATTER;
+  EpiIn cur, nxt;
+  if (needs_in && part < nch) epi_load_in<MODE>(a, m_own, col_tile0 + part * 32, xrow_own, cur);
 #pragma unroll 1
   for (int c = part; c < nch; c += nparts) {
+    if (needs_in && c + nparts < nch)
+      epi_load_in<MODE>(a, m_own, col_tile0 + (c + nparts) * 32, xrow_own, nxt);
     float v[32];
     if (swiglu) {
       float u[32];
@@ -213,7 +283,7 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int wrow0, int la
       tmem_ld_wait();
     }
     const int col0 = col_tile0 + c * 32;
-    if (a.mode == EPI_STORE && e.vt && col0 >= e.vt_col0) {
+    if (MODE == EPI_STORE && e.vt && col0 >= e.vt_col0) {
       // v^T: token m of sequence b goes to column t of rows (b, g, dim). For each dim
       // the warp's 32 consecutive tokens form one contiguous run, so no staging.
       if (m_own < a.M && col0 < a.N) {
@@ -227,11 +297,12 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int wrow0, int la
       }
       continue;
     }
-    epilogue_chunk_direct(a, m_own, col0, xrow_own, r_own, v);
+    epilogue_chunk_direct<MODE>(a, m_own, col0, xrow_own, r_own, v, cur);
+    cur = nxt;
   }
 }
 
-template <int BN>
+template <int BN, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
@@ -269,8 +340,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     fence_barrier_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB0);
-    if (args.mode == EPI_SWIGLU || args.n_split1 < args.N) prefetch_tensormap(&tmB1);
-    if (args.mode != EPI_SWIGLU && args.n_split2 < args.N) prefetch_tensormap(&tmB2);
+    if (MODE == EPI_SWIGLU || args.n_split1 < args.N) prefetch_tensormap(&tmB1);
+    if (MODE != EPI_SWIGLU && args.n_split2 < args.N) prefetch_tensormap(&tmB2);
   }
   if (warp == 1) tmem_alloc(sTmem, C::TMEM_COLS);
   tc_fence_before();
@@ -287,7 +358,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int n_blk = tile / args.tiles_m;
         const CUtensorMap* mp = &tmB0;
         int brow = n_blk * BN;
-        if (args.mode != EPI_SWIGLU) {
+        if (MODE != EPI_SWIGLU) {
           if (brow >= args.n_split2) {
             mp = &tmB2;
             brow -= args.n_split2;
@@ -302,7 +373,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (!mbar_wait(EMPTY(s), ph ^ 1u, abort_flag, args.status)) break;
           mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
           tma_load_2d(sA + s * C::A_BYTES, &tmA, FULL(s), kb * BK, m0);
-          if (args.mode == EPI_SWIGLU) {
+          if (MODE == EPI_SWIGLU) {
             const int h0 = n_blk * (BN / 2);
             tma_load_2d(sB + s * C::B_BYTES, &tmB0, FULL(s), kb * BK, h0);
             tma_load_2d(sB + s * C::B_BYTES + (BN / 2) * 128, &tmB1, FULL(s), kb * BK, h0);
@@ -353,7 +424,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int wrow0 = (tile % args.tiles_m) * BM + quad * 32;
       const int n_blk = tile / args.tiles_m;
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<BN>(args, wrow0, lane, n_blk, t_row, (warp - 2) / 4, EPI_WARPS / 4);
+      epilogue_tile<BN, MODE>(args, wrow0, lane, n_blk, t_row, (warp - 2) / 4, EPI_WARPS / 4);
       tc_fence_before();
       mbar_arrive(ACC_EMPTY(acc));
     }
@@ -442,12 +513,20 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   }
   a.tiles = a.tiles_m * tiles_n;
   if (a.tiles <= 0) return cudaSuccess;
-  auto k = gemm_tc_kernel<BN>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+            const TcArgs) = nullptr;
+  switch (e.kind) {
+    case EPI_STORE: k = gemm_tc_kernel<BN, EPI_STORE>; break;
+    case EPI_OPROJ: k = gemm_tc_kernel<BN, EPI_OPROJ>; break;
+    case EPI_SWIGLU: k = gemm_tc_kernel<BN, EPI_SWIGLU>; break;
+    case EPI_DOWN_SCATTER: k = gemm_tc_kernel<BN, EPI_DOWN_SCATTER>; break;
+    default: return cudaErrorInvalidValue;
+  }
+  static bool attr_set[4] = {false, false, false, false};
+  if (!attr_set[e.kind]) {
     cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     if (err != cudaSuccess) return err;
-    attr_set = true;
+    attr_set[e.kind] = true;
   }
   const int grid = a.tiles < sm_count() ? a.tiles : sm_count();
   return launch_pdl(k, dim3(grid), dim3(NUM_THREADS), Cf::SMEM, c.stream, mA, mB0, mB1, mB2, a);
