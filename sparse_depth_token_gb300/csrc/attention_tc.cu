@@ -11,9 +11,8 @@
 //   warp 0      TMA: the Q tile once, then K_j and V_j^T of each 128-key block j
 //               into a two-stage ring
 //   warp 1      TMEM owner; one lane issues S_j = Q K_j^T into one of two TMEM S
-//               buffers (S_{j+1} is issued before P_j V_j so the tensor core works on
-//               the next scores while the softmax runs), then O += P_j V_j with the
-//               output accumulator O resident in TMEM
+//               buffers and O += P_j V_j (output accumulator O resident in TMEM), each
+//               as soon as its inputs are ready, so S_{j+1} overlaps the softmax of S_j
 //   warps 2..5  softmax, one query row per thread (a TMEM lane is a row, so row max
 //               and row sum are thread-local), in one pass over the scores held in
 //               registers: P_j = exp2(s*scale - m) is written as bf16 into one of two
@@ -38,13 +37,30 @@ namespace {
 using namespace tc;
 
 constexpr int QB = 128;     // query rows per CTA
-constexpr int KB = 128;     // keys per block
 constexpr int HD = 128;     // head dim
 constexpr int THREADS = 192;
-constexpr int CHUNK = 128 * 128;        // bytes of a 128 x 64 bf16 swizzled chunk
-constexpr int TILE = 2 * CHUNK;         // a 128 x 128 bf16 tile
-constexpr int SMEM = 7 * TILE + 1024 + 256;
+constexpr int CHUNK = 128 * 128;        // bytes of a 128-row x 64-column bf16 swizzled chunk
+constexpr int QTILE = 2 * CHUNK;        // the Q tile, 128 x 128
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
+
+// KB keys per block; PBUF shared-memory P buffers. <128, 2> suits long sequences
+// (one CTA per SM); <64, 1> needs half the shared memory and TMEM so that two CTAs
+// share an SM and hide each other's load and set-up latency (short sequences).
+template <int KB, int PBUF>
+struct AttnCfg {
+  static constexpr int K_CHUNK = KB * 128;          // KB rows x 64 head dims
+  static constexpr int K_STAGE = 2 * K_CHUNK;       // KB x 128 head dims
+  static constexpr int V_STAGE = (KB / 64) * CHUNK; // 128 head dims x KB keys
+  static constexpr int P_BYTES = (KB / 64) * CHUNK; // 128 rows x KB keys
+  static constexpr int TMEM_COLS = 2 * KB + 128 <= 256 ? 256 : 512;
+  static constexpr int DATA = QTILE + PBUF * P_BYTES + 2 * K_STAGE + 2 * V_STAGE;
+  // 1024 bytes cover both the alignment of the tiles and the 256-byte barrier
+  // block: the barriers sit in the alignment gap when it is at least 256 bytes,
+  // else after the tiles (then the gap is under 256 bytes).
+  static constexpr int SMEM = DATA + 1024;
+  // two CTAs fit in the 228 KB of an SM (each also takes 1 KB reserved by the system)
+  static constexpr int MIN_BLOCKS = 2 * (SMEM + 1024) <= 228 * 1024 ? 2 : 1;
+};
 
 struct AttnArgs {
   int n, hq, hkv, nqb;
@@ -66,26 +82,27 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
-attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_constant__ CUtensorMap tmVt,
-                    const AttnArgs a) {
+template <int KB, int PBUF>
+__global__ void __launch_bounds__(THREADS, (AttnCfg<KB, PBUF>::MIN_BLOCKS))
+attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmVt, const AttnArgs a) {
+  using C = AttnCfg<KB, PBUF>;
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base;
-  const uint32_t sP0 = base + TILE;       // P buffers at sP0 + b * TILE
-  const uint32_t sK0 = base + 3 * TILE;   // K stages at sK0 + s * TILE
-  const uint32_t sV0 = base + 5 * TILE;   // V^T stages at sV0 + s * TILE
-  const uint32_t sBar = base + 7 * TILE;
+  const uint32_t sP0 = sQ + QTILE;                    // P buffers at sP0 + b * P_BYTES
+  const uint32_t sK0 = sP0 + PBUF * C::P_BYTES;       // K stages at sK0 + s * K_STAGE
+  const uint32_t sV0 = sK0 + 2 * C::K_STAGE;          // V^T stages at sV0 + s * V_STAGE
+  const uint32_t sBar = (base - raw >= 256u) ? raw : base + (uint32_t)C::DATA;
   const uint32_t Q_FULL = sBar + 0;
   const uint32_t KV_FULL0 = sBar + 8, KV_EMPTY0 = sBar + 24;
   const uint32_t S_FULL0 = sBar + 40, S_EMPTY0 = sBar + 56;
   const uint32_t P_FULL0 = sBar + 72, P_EMPTY0 = sBar + 88;
   const uint32_t sTmem = sBar + 112;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (sTmem - base));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (sTmem - base) + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + (sTmem - raw));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + (sTmem - raw) + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qb = a.nqb - 1 - (int)blockIdx.x;   // longest rows first
@@ -102,79 +119,111 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
       mbar_init(KV_EMPTY0 + 8 * s, 1);
       mbar_init(S_FULL0 + 8 * s, 1);
       mbar_init(S_EMPTY0 + 8 * s, 128);
-      mbar_init(P_FULL0 + 8 * s, 128);
-      mbar_init(P_EMPTY0 + 8 * s, 1);
+    }
+    for (int pb = 0; pb < PBUF; ++pb) {
+      mbar_init(P_FULL0 + 8 * pb, 128);
+      mbar_init(P_EMPTY0 + 8 * pb, 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
-    prefetch_tensormap(&tmQK);
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmVt);
   }
-  if (warp == 1) tmem_alloc(sTmem, 512);
+  if (warp == 1) tmem_alloc(sTmem, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;   // S0: cols 0..127, S1: 128..255, O: 256..383
-  const uint32_t tO = tmem + 256u;
+  const uint32_t tmem = *tmem_slot;   // S0: cols [0, KB), S1: [KB, 2KB), O: [2KB, 2KB+128)
+  const uint32_t tO = tmem + 2u * KB;
   pdl_wait();  // everything above overlapped the previous kernel's tail
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(Q_FULL, TILE);
-      tma_load_3d(sQ, &tmQK, Q_FULL, h * HD, q0, b);
-      tma_load_3d(sQ + CHUNK, &tmQK, Q_FULL, h * HD + 64, q0, b);
+      mbar_arrive_expect_tx(Q_FULL, QTILE);
+      tma_load_3d(sQ, &tmQ, Q_FULL, h * HD, q0, b);
+      tma_load_3d(sQ + CHUNK, &tmQ, Q_FULL, h * HD + 64, q0, b);
       const int vt_row = (b * a.hkv + g) * HD;
       for (int j = 0; j < nkb; ++j) {
         const int s = j & 1;
         const uint32_t ph = (uint32_t)(j >> 1) & 1u;
         if (!mbar_wait(KV_EMPTY0 + 8 * s, ph ^ 1u, abort_flag, a.status)) break;
-        mbar_arrive_expect_tx(KV_FULL0 + 8 * s, 2 * TILE);
-        const uint32_t kdst = sK0 + s * TILE, vdst = sV0 + s * TILE;
-        tma_load_3d(kdst, &tmQK, KV_FULL0 + 8 * s, a.qw + g * HD, j * KB, b);
-        tma_load_3d(kdst + CHUNK, &tmQK, KV_FULL0 + 8 * s, a.qw + g * HD + 64, j * KB, b);
-        tma_load_2d(vdst, &tmVt, KV_FULL0 + 8 * s, j * KB, vt_row);
-        tma_load_2d(vdst + CHUNK, &tmVt, KV_FULL0 + 8 * s, j * KB + 64, vt_row);
+        mbar_arrive_expect_tx(KV_FULL0 + 8 * s, C::K_STAGE + C::V_STAGE);
+        const uint32_t kdst = sK0 + s * C::K_STAGE, vdst = sV0 + s * C::V_STAGE;
+        tma_load_3d(kdst, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD, j * KB, b);
+        tma_load_3d(kdst + C::K_CHUNK, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD + 64, j * KB, b);
+#pragma unroll
+        for (int kc = 0; kc < KB / 64; ++kc)
+          tma_load_2d(vdst + kc * CHUNK, &tmVt, KV_FULL0 + 8 * s, j * KB + 64 * kc, vt_row);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 128);
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, KB);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD);
       bool ok = mbar_wait(Q_FULL, 0, abort_flag, a.status);
-      auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-        if (!mbar_wait(KV_FULL0 + 8 * s, ph, abort_flag, a.status)) return false;
-        if (!mbar_wait(S_EMPTY0 + 8 * s, ph ^ 1u, abort_flag, a.status)) return false;
-        tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(s * 128);
+      // Issue S_j = Q K_j^T and O += P_j V_j in whatever order their inputs arrive:
+      // S_{j+1} as soon as K_{j+1} is resident (so it overlaps the softmax of S_j),
+      // P_j V_j as soon as the softmax has written P_j -- never one waiting behind the
+      // other's input.
+      int ns = 0, npv = 0;
+      uint64_t t0 = global_timer_ns();
+      uint32_t spins = 0;
+      while (ok && npv < nkb) {
+        bool progressed = false;
+        if (ns < nkb && ns <= npv + 1) {
+          const int s = ns & 1;
+          const uint32_t ph = (uint32_t)(ns >> 1) & 1u;
+          if (mbar_try_wait(KV_FULL0 + 8 * s, ph) && mbar_try_wait(S_EMPTY0 + 8 * s, ph ^ 1u)) {
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(s * KB);
 #pragma unroll
-        for (int kc = 0; kc < 2; ++kc) {
-          const uint64_t ad = smem_desc_sw128(sQ + kc * CHUNK);
-          const uint64_t bd = smem_desc_sw128(sK0 + s * TILE + kc * CHUNK);
+            for (int kc = 0; kc < 2; ++kc) {
+              const uint64_t ad = smem_desc_sw128(sQ + kc * CHUNK);
+              const uint64_t bd = smem_desc_sw128(sK0 + s * C::K_STAGE + kc * C::K_CHUNK);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc, (kc | k) != 0 ? 1u : 0u);
+              for (int k = 0; k < 4; ++k)
+                mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc_s, (kc | k) != 0 ? 1u : 0u);
+            }
+            mma_commit(S_FULL0 + 8 * s);
+            ++ns;
+            progressed = true;
+          }
         }
-        mma_commit(S_FULL0 + 8 * s);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < nkb; ++j) {
-        if (j + 1 < nkb && !issue_s(j + 1)) break;
-        const int s = j & 1;
-        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-        if (!mbar_wait(P_FULL0 + 8 * s, ph, abort_flag, a.status)) break;
-        tc_fence_after();
+        if (npv < ns) {
+          const int s = npv & 1;                         // K/V stage
+          const int pb = npv % PBUF;                     // P buffer
+          const uint32_t pph = (uint32_t)(npv / PBUF) & 1u;
+          if (mbar_try_wait(P_FULL0 + 8 * pb, pph)) {
+            tc_fence_after();
 #pragma unroll
-        for (int kc = 0; kc < 2; ++kc) {
-          const uint64_t ad = smem_desc_sw128(sP0 + s * TILE + kc * CHUNK);
-          const uint64_t bd = smem_desc_sw128(sV0 + s * TILE + kc * CHUNK);
+            for (int kc = 0; kc < KB / 64; ++kc) {
+              const uint64_t ad = smem_desc_sw128(sP0 + pb * C::P_BYTES + kc * CHUNK);
+              const uint64_t bd = smem_desc_sw128(sV0 + s * C::V_STAGE + kc * CHUNK);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_bf16(tO, ad + 2ull * k, bd + 2ull * k, idesc, (j | kc | k) != 0 ? 1u : 0u);
+              for (int k = 0; k < 4; ++k)
+                mma_bf16(tO, ad + 2ull * k, bd + 2ull * k, idesc_o,
+                         (npv | kc | k) != 0 ? 1u : 0u);
+            }
+            mma_commit(P_EMPTY0 + 8 * pb);
+            mma_commit(KV_EMPTY0 + 8 * s);
+            ++npv;
+            progressed = true;
+          }
         }
-        mma_commit(P_EMPTY0 + 8 * s);
-        mma_commit(KV_EMPTY0 + 8 * s);
+        if (progressed) {
+          t0 = global_timer_ns();
+          spins = 0;
+          continue;
+        }
+        if ((++spins & 255u) == 0u) {
+          if (*abort_flag) break;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            report_status(a.status, XMOD_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+        }
       }
     }
   } else {
@@ -193,14 +242,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
         break;
       }
       tc_fence_after();
-      float v[128];
+      float v[KB];
       {
-        float* vv = v;
-        const uint32_t srow = tmem + lane_off + (uint32_t)(s * 128);
-        tmem_ld32(srow, *reinterpret_cast<float(*)[32]>(vv));
-        tmem_ld32(srow + 32, *reinterpret_cast<float(*)[32]>(vv + 32));
-        tmem_ld32(srow + 64, *reinterpret_cast<float(*)[32]>(vv + 64));
-        tmem_ld32(srow + 96, *reinterpret_cast<float(*)[32]>(vv + 96));
+        const uint32_t srow = tmem + lane_off + (uint32_t)(s * KB);
+#pragma unroll
+        for (int c = 0; c < KB / 32; ++c)
+          tmem_ld32(srow + c * 32, *reinterpret_cast<float(*)[32]>(v + c * 32));
         tmem_ld_wait();
       }
       tc_fence_before();
@@ -210,13 +257,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
       float mx = -INFINITY;
       if (diag) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
+        for (int i = 0; i < KB; ++i) {
           if (key0 + i > qi) v[i] = -INFINITY;
           mx = fmaxf(mx, v[i]);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) mx = fmaxf(mx, v[i]);
+        for (int i = 0; i < KB; ++i) mx = fmaxf(mx, v[i]);
       }
       const float m_cand = mx * a.scale_log2;
       const bool grow = m_cand > m + kRescaleThreshold;
@@ -225,7 +272,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // O holds P_0..j-1 V: wait until the last of those MMAs landed, then rescale.
         const int jp = j - 1;
-        if (!mbar_wait(P_EMPTY0 + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u, abort_flag,
+        if (!mbar_wait(P_EMPTY0 + 8 * (jp % PBUF), (uint32_t)(jp / PBUF) & 1u, abort_flag,
                        a.status)) {
           ok = false;
           break;
@@ -243,15 +290,16 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
         tmem_st_wait();
       }
       m = m_new;
-      // the P buffer of this parity is free once P_{j-2} V_{j-2} has completed
-      if (!mbar_wait(P_EMPTY0 + 8 * s, ph ^ 1u, abort_flag, a.status)) {
+      // this P buffer is free once P_{j-PBUF} V_{j-PBUF} has completed
+      const int pb = j % PBUF;
+      if (!mbar_wait(P_EMPTY0 + 8 * pb, ((uint32_t)(j / PBUF) & 1u) ^ 1u, abort_flag, a.status)) {
         ok = false;
         break;
       }
-      const uint32_t prow = sP0 + s * TILE + (uint32_t)row * 128u;
+      const uint32_t prow = sP0 + pb * C::P_BYTES + (uint32_t)row * 128u;
       float sum = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < KB / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
@@ -271,11 +319,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
       l = l * alpha + sum;
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(P_FULL0 + 8 * s);
+      mbar_arrive(P_FULL0 + 8 * pb);
     }
     if (ok) {
       const int jl = nkb - 1;
-      ok = mbar_wait(P_EMPTY0 + 8 * (jl & 1), (uint32_t)(jl >> 1) & 1u, abort_flag, a.status);
+      ok = mbar_wait(P_EMPTY0 + 8 * (jl % PBUF), (uint32_t)(jl / PBUF) & 1u, abort_flag, a.status);
     }
     if (ok) {
       tc_fence_after();
@@ -310,11 +358,43 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQK, const __grid_const
   }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
+template <int KB, int PBUF>
+cudaError_t launch_attention_cfg(const Ctx& c, int B, int n, int hq, const void* qkv, int ldq,
+                                 const CUtensorMap& mVt, const AttnArgs& a) {
+  using Cf = AttnCfg<KB, PBUF>;
+  CUtensorMap mQ, mK;
+  const int64_t dims[3] = {ldq, n, B};
+  const int64_t strides[2] = {(int64_t)ldq * 2, (int64_t)n * ldq * 2};
+  const int qbox[3] = {64, QB, 1};
+  const int kbox[3] = {64, KB, 1};
+  if (!tma_map_bf16(&mQ, qkv, 3, dims, strides, qbox)) return cudaErrorInvalidValue;
+  if (!tma_map_bf16(&mK, qkv, 3, dims, strides, kbox)) return cudaErrorInvalidValue;
+  auto k = attention_tc_kernel<KB, PBUF>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(a.nqb, hq, B);
+  return launch_pdl(k, grid, dim3(THREADS), Cf::SMEM, c.stream, mQ, mK, mVt, a);
+}
+
 }  // namespace
+
+// A sequence of at most this many tokens is one 128-key block: it runs the
+// <128, 2> configuration; longer ones the two-CTAs-per-SM <64, 1> configuration,
+// which measured 7-15% faster from 256 to 16384 tokens (GB300, 12/4 and 16/4 heads).
+#ifndef XMOD_ATTN_ONE_BLOCK_MAX_N
+#define XMOD_ATTN_ONE_BLOCK_MAX_N 128
+#endif
 
 bool attention_tc_supported(int hd, int n, int ldq) {
   return hd == HD && n > 0 && ldq % 8 == 0 && tma_available();
@@ -323,13 +403,7 @@ bool attention_tc_supported(int hd, int n, int ldq) {
 cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
                                 int ldq, const void* vt, int vt_ld, void* o) {
   if (B <= 0 || n <= 0) return cudaSuccess;
-  CUtensorMap mQK, mVt;
-  {
-    const int64_t dims[3] = {ldq, n, B};
-    const int64_t strides[2] = {(int64_t)ldq * 2, (int64_t)n * ldq * 2};
-    const int box[3] = {64, QB, 1};
-    if (!tma_map_bf16(&mQK, qkv, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  }
+  CUtensorMap mVt;
   {
     const int64_t dims[2] = {n, (int64_t)B * hkv * HD};
     const int64_t strides[1] = {(int64_t)vt_ld * 2};
@@ -346,15 +420,8 @@ cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, con
   a.o = (__nv_bfloat16*)o;
   a.ldo = hq * HD;
   a.status = c.status;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  dim3 grid(a.nqb, hq, B);
-  return launch_pdl(attention_tc_kernel, grid, dim3(THREADS), SMEM, c.stream, mQK, mVt, a);
+  if (n <= XMOD_ATTN_ONE_BLOCK_MAX_N) return launch_attention_cfg<128, 2>(c, B, n, hq, qkv, ldq, mVt, a);
+  return launch_attention_cfg<64, 1>(c, B, n, hq, qkv, ldq, mVt, a);
 }
 
 }  // namespace xmod
