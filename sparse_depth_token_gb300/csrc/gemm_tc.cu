@@ -56,10 +56,29 @@ struct TcArgs {
   int M, N, K;
   int mode;                // EpiKind
   int n_split1, n_split2;  // STORE: first accumulator column served by B map 1 / map 2
-  int tiles_m, tiles;
+  int tiles_m, tiles_n, tiles;
   Epilogue e;
   int* status;
 };
+
+// Row blocks per band of the tile order. Tiles are numbered band by band; inside a
+// band the row block varies fastest. The tiles that run at the same time (one per
+// CTA) then cover a band of XMOD_TILE_BAND row blocks by about 152 / XMOD_TILE_BAND
+// column blocks, so A and B are both re-read from L2 rather than from DRAM when the
+// operands do not fit in L2 together.
+#ifndef XMOD_TILE_BAND
+#define XMOD_TILE_BAND 16
+#endif
+
+__device__ __forceinline__ void tile_coords(const TcArgs& a, int tile, int& m_blk, int& n_blk) {
+  const int per_band = XMOD_TILE_BAND * a.tiles_n;
+  const int band = tile / per_band;
+  const int r = tile - band * per_band;
+  const int m_first = band * XMOD_TILE_BAND;
+  const int rows = min(XMOD_TILE_BAND, a.tiles_m - m_first);
+  m_blk = m_first + r % rows;
+  n_blk = r / rows;
+}
 
 // silu(z) = z * sigmoid(z) with the fast exponential and approximate division (a few
 // ulp of fp32, far below the bf16 rounding of the result). A full-precision division
@@ -354,8 +373,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       int it = 0;
       for (int tile = blockIdx.x; tile < args.tiles && !*abort_flag; tile += gridDim.x) {
-        const int m0 = (tile % args.tiles_m) * BM;
-        const int n_blk = tile / args.tiles_m;
+        int m_blk, n_blk;
+        tile_coords(args, tile, m_blk, n_blk);
+        const int m0 = m_blk * BM;
         const CUtensorMap* mp = &tmB0;
         int brow = n_blk * BN;
         if (MODE != EPI_SWIGLU) {
@@ -421,8 +441,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
       if (!mbar_wait(ACC_FULL(acc), aph, abort_flag, args.status)) break;
       tc_fence_after();
-      const int wrow0 = (tile % args.tiles_m) * BM + quad * 32;
-      const int n_blk = tile / args.tiles_m;
+      int m_blk, n_blk;
+      tile_coords(args, tile, m_blk, n_blk);
+      const int wrow0 = m_blk * BM + quad * 32;
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
       epilogue_tile<BN, MODE>(args, wrow0, lane, n_blk, t_row, (warp - 2) / 4, EPI_WARPS / 4);
       tc_fence_before();
@@ -511,6 +532,7 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
     if (p.nB < 3) mB2 = mB0;
     tiles_n = (p.N + BN - 1) / BN;
   }
+  a.tiles_n = tiles_n;
   a.tiles = a.tiles_m * tiles_n;
   if (a.tiles <= 0) return cudaSuccess;
   void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
