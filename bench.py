@@ -68,11 +68,21 @@ def algorithmic_work(w: I.Workload) -> dict:
     def add(kind, v):
         out[kind] = out.get(kind, 0.0) + float(v)
 
-    for sparse in schedule(w):
+    kinds = schedule(w)
+    run_left = 0   # layers left in the current run of sparse layers (logits kept current)
+    for l, sparse in enumerate(kinds):
         n = w.T // w.K if sparse else w.T
         M = w.B * n
         if sparse:
-            add("router", w.B * w.T * w.d * es + 4 * w.B * w.T)
+            if run_left == 0:   # one pass over the stream: logits of up to 32 layers
+                run = 1
+                while run < ROUTER_RUN and l + run < len(kinds) and kinds[l + run]:
+                    run += 1
+                run_left = run
+                add("router", w.B * w.T * w.d * es + 4 * run * w.B * w.T)
+            run_left -= 1
+            if run_left > 0:    # logits of the updated rows for the rest of the run
+                add("router_refresh", M * w.d * es + 4 * run_left * M)
             add("topk", 4 * w.B * w.T + 8 * M)
         add("gather_rmsnorm", 2 * M * w.d * es)
         add("gemm_qkv", 2 * M * w.d * (w.hq + 2 * w.hkv) * w.hd)
@@ -83,6 +93,10 @@ def algorithmic_work(w: I.Workload) -> dict:
         add("gemm_down_scatter", 2 * M * w.F * w.d)
     return out
 
+
+# Sparse layers whose router logits one pass over the stream computes (the library's
+# run length; later layers of a run only refresh the logits of the rows that changed).
+ROUTER_RUN = 32
 
 TENSOR_KINDS = {"gemm_qkv", "attention", "gemm_o_residual", "gemm_gate_up_swiglu",
                 "gemm_down_scatter"}

@@ -45,9 +45,15 @@ bool head_dim_supported(int hd) { return hd == 32 || hd == 64 || hd == 128; }
 // Row stride (elements) of the transposed values for n tokens: 16-byte multiple.
 inline int vt_ld(int n) { return (n + 7) / 8 * 8; }
 
+// Sparse layers whose router logits one pass over the stream computes (the widest
+// router GEMM tile), and the zero rows that follow them in the stacked router
+// vectors (a 32-row tile read from any starting layer stays inside the buffer).
+constexpr int kRouterRun = RowPtrs::kMax;
+constexpr int kRouterRows = 2 * kRouterRun;
+
 // Workspace carve-up. M rows of block scratch cover a dense layer (M = B*T).
 struct Layout {
-  size_t status, s, idx, r_sel, u, qkv, vt, o, h, hidden, total;
+  size_t status, s, idx, r_sel, u, qkv, vt, o, h, hidden, wr, total;
 };
 
 Layout layout(const xmod_dims* dm, int K) {
@@ -60,7 +66,7 @@ Layout layout(const xmod_dims* dm, int K) {
   const size_t qkv_w = (size_t)(dm->n_heads + 2 * dm->n_kv_heads) * dm->head_dim;
   size_t off = 0;
   L.status = off; off += kAlign;
-  L.s = off;      off = align_up(off + 4 * BT);
+  L.s = off;      off = align_up(off + 4 * BT * kRouterRun);   // logits [run layer, B*T]
   L.idx = off;    off = align_up(off + 4 * Bn);
   L.r_sel = off;  off = align_up(off + 4 * Bn);
   L.u = off;      off = align_up(off + es * M * dm->d);
@@ -71,6 +77,7 @@ Layout layout(const xmod_dims* dm, int K) {
   L.o = off;      off = align_up(off + es * M * dm->n_heads * dm->head_dim);
   L.h = off;      off = align_up(off + 4 * M * dm->d);   // h = x_sel + a kept in fp32
   L.hidden = off; off = align_up(off + es * M * dm->d_ff);
+  L.wr = off;     off = align_up(off + es * (size_t)kRouterRows * dm->d);   // stacked w_r
   L.total = off;
   return L;
 }
@@ -103,9 +110,11 @@ bool weights_ok(const xmod_layer_weights* w, bool need_router) {
 // The block on B*n compact rows (rows of x selected by idx, or identity when
 // idx == NULL and n == T). Writes a to a_out when given, and either
 // scatters the gated residual into x (scatter == true) or stores f to f_out.
+// With scatter, xs_new (if not NULL) receives the updated compact rows [B*n, d].
 int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int n,
               const void* x_src, const int32_t* idx, const xmod_layer_weights* w, void* a_out,
-              void* f_out, bool scatter, void* x_inout, const float* r_sel, int gate) {
+              void* f_out, bool scatter, void* x_inout, const float* r_sel, int gate,
+              void* xs_new = nullptr) {
   const xmod_dtype dt = dm->dtype;
   const int B = dm->B, T = dm->T, d = dm->d, hq = dm->n_heads, hkv = dm->n_kv_heads,
             hd = dm->head_dim, F = dm->d_ff;
@@ -205,6 +214,8 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
     ed.r_sel = r_sel;
     ed.varsigma = w->varsigma;
     ed.gate = gate;
+    ed.out = xs_new;
+    ed.ldo = d;
   } else {
     ed.kind = EPI_STORE;
     ed.out = f_out;
@@ -226,12 +237,83 @@ int check_ws(const xmod_dims* dm, int K, void* ws, size_t ws_bytes) {
   return XMOD_OK;
 }
 
+// Router-logit GEMM: S[j, token(m)] = w_j . rows[m] + bias[token(m)] for the
+// n_vec vectors stacked at wr (bf16, [>= 32 rows from wr, d]).
+GemmTcProblem router_problem(const xmod_dims* dm, int M, const void* rows, const void* wr,
+                             int wr_rows, int n_vec) {
+  GemmTcProblem p;
+  p.M = M; p.N = n_vec; p.K = dm->d; p.A = rows; p.lda = dm->d;
+  p.B[0] = wr; p.ldb = dm->d; p.b_rows = wr_rows;
+  return p;
+}
+Epilogue router_epilogue(const xmod_dims* dm, int n_per_seq, const int32_t* idx, float* S,
+                         const float* bias) {
+  Epilogue e;
+  e.kind = EPI_ROUTER;
+  e.out = S;
+  e.ldo = dm->B * dm->T;
+  e.idx = idx;
+  e.T = dm->T;
+  e.n_per_seq = n_per_seq;
+  e.bias = bias;
+  return e;
+}
+
+// Consecutive sparse layers lw[0..count) (count <= kRouterRun) with the router logits
+// kept current incrementally. Each layer's logits are w_r . x + b on that layer's
+// input stream, and a layer changes only the rows it selected. So one pass over the
+// stream computes the logits of every layer of the run, and after each layer only
+// its B*(T/K) updated rows get their logits for the later layers recomputed (from
+// the compact copy of the new rows that the down-projection epilogue writes).
+// A single sparse layer is a run of one; idx_out / r_sel_out (NULL: workspace) then
+// receive its selection.
+int sparse_run(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int K,
+               xmod_gate gate, const xmod_layer_weights* lw, int count, void* x,
+               const float* bias, int32_t* idx_out = nullptr, float* r_sel_out = nullptr) {
+  const int B = dm->B, T = dm->T, d = dm->d, n = T / K;
+  const int64_t BT = (int64_t)B * T;
+  float* S = (float*)at(ws, L.s);
+  int32_t* idx = idx_out ? idx_out : (int32_t*)at(ws, L.idx);
+  float* r_sel = r_sel_out ? r_sel_out : (float*)at(ws, L.r_sel);
+  char* wr = at(ws, L.wr);
+  void* xs_new = at(ws, L.u);   // free once the gate/up GEMM has read v2
+  RowPtrs rows{};
+  for (int j = 0; j < count; ++j) rows.p[j] = lw[j].w_router;
+  XMOD_RUN("router_stack", launch_stack_rows(c, rows, count, kRouterRows, d, wr));
+  XMOD_RUN("router", launch_gemm_tc(c, router_problem(dm, (int)BT, x, wr, kRouterRows, count),
+                                    router_epilogue(dm, T, nullptr, S, bias)));
+  for (int j = 0; j < count; ++j) {
+    XMOD_RUN("topk", launch_topk(c, B, T, n, S + j * BT, idx, r_sel));
+    const bool refresh = j + 1 < count;
+    const int st = run_block(c, dm, L, ws, n, x, idx, &lw[j], nullptr, nullptr, true, x, r_sel,
+                             (int)gate, refresh ? xs_new : nullptr);
+    if (st) return st;
+    if (refresh)
+      XMOD_RUN("router_refresh",
+               launch_gemm_tc(c, router_problem(dm, B * n, xs_new, wr + (size_t)(j + 1) * d * 2,
+                                                kRouterRows - (j + 1), count - 1 - j),
+                              router_epilogue(dm, n, idx, S + (j + 1) * BT, bias)));
+  }
+  return XMOD_OK;
+}
+
+// Whether sparse_run can serve runs of these dimensions (bf16 tensor-core GEMMs).
+bool sparse_run_supported(const xmod_dims* dm, void* ws, const Layout& L) {
+  if (dm->dtype != XMOD_BF16) return false;
+  if ((int64_t)dm->B * dm->T > INT32_MAX) return false;
+  const GemmTcProblem p = router_problem(dm, dm->B * dm->T, at(ws, L.u), at(ws, L.wr),
+                                         kRouterRows, kRouterRun);
+  return gemm_tc_supported(p, router_epilogue(dm, dm->T, nullptr, (float*)at(ws, L.s), nullptr));
+}
+
 int layer_impl(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
                const xmod_layer_weights* w, void* x, const float* bias, int32_t* idx_out,
                float* r_sel_out, void* ws, const Layout& L, cudaStream_t stream) {
   Ctx c{stream, (int*)at(ws, L.status)};
   if (kind == XMOD_LAYER_DENSE)
     return run_block(c, dm, L, ws, dm->T, x, nullptr, w, nullptr, nullptr, true, x, nullptr, -1);
+  if (sparse_run_supported(dm, ws, L))
+    return sparse_run(c, dm, L, ws, K, gate, w, 1, x, bias, idx_out, r_sel_out);
   const int n = dm->T / K;
   float* s = (float*)at(ws, L.s);
   int32_t* idx = idx_out ? idx_out : (int32_t*)at(ws, L.idx);
@@ -399,11 +481,24 @@ int xmod_stack_fwd(const xmod_dims* dm, int K, double A, int N0, int N1, xmod_ga
   int st = check_ws(dm, K, ws, ws_bytes);
   if (st) return st;
   const Layout L = layout(dm, K);
-  for (int l = 0; l < n_layers; ++l) {
+  const bool runs = sparse_run_supported(dm, ws, L);
+  Ctx c{(cudaStream_t)stream, (int*)at(ws, L.status)};
+  for (int l = 0; l < n_layers;) {
     const bool sparse = l >= N0 && ((l - N0) % (AK + 1)) < AK;
+    if (sparse && runs) {
+      // the sparse layers up to the next dense one, at most kRouterRun at a time
+      int count = 1;
+      while (count < kRouterRun && l + count < n_layers && ((l + count - N0) % (AK + 1)) < AK)
+        ++count;
+      st = sparse_run(c, dm, L, ws, K, gate, &layers[l], count, x_inout, bias);
+      if (st) return st;
+      l += count;
+      continue;
+    }
     st = layer_impl(dm, sparse ? XMOD_LAYER_SPARSE : XMOD_LAYER_DENSE, K, gate, &layers[l],
                     x_inout, bias, nullptr, nullptr, ws, L, (cudaStream_t)stream);
     if (st) return st;
+    ++l;
   }
   return XMOD_OK;
 }

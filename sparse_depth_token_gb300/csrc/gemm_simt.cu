@@ -48,6 +48,7 @@ __device__ __forceinline__ void epilogue_store(const Epilogue& e, int M, int N, 
       else if (e.gate == XMOD_GATE_MOD) y = hv + e.r_sel[m] * acc;                       // Eq. 6
       else y = hv + acc;                                                                  // dense
       st_f(xp, y);
+      if (e.out) st_f((T*)e.out + (int64_t)m * e.ldo + n, y);
       break;
     }
   }

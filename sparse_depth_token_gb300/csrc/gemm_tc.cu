@@ -231,6 +231,12 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int m, in
       *reinterpret_cast<float4*>(hp + 8 * g) = make_float4(hv[0], hv[1], hv[2], hv[3]);
       *reinterpret_cast<float4*>(hp + 8 * g + 4) = make_float4(hv[4], hv[5], hv[6], hv[7]);
     }
+  } else if (MODE == EPI_ROUTER) {   // xrow is the stream token here
+    float* sp = (float*)e.out + (int64_t)col0 * e.ldo + xrow;
+    const float b = e.bias ? e.bias[xrow] : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < rem) sp[(int64_t)i * e.ldo] = v[i] + b;
   } else {  // EPI_DOWN_SCATTER, a = h - x
     __nv_bfloat16* xp = (__nv_bfloat16*)e.x + xrow + col0;
     const float g7 = e.varsigma * r;
@@ -261,6 +267,8 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int m, in
       q.z = pack_bf16x2(y[4], y[5]);
       q.w = pack_bf16x2(y[6], y[7]);
       *reinterpret_cast<uint4*>(xp + 8 * g) = q;
+      if (e.out)
+        *reinterpret_cast<uint4*>((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0 + 8 * g) = q;
     }
   }
 }
@@ -279,6 +287,7 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int wrow0, int la
     xrow_own = stream_row_of(e, m_own) * e.d;
     if (MODE == EPI_DOWN_SCATTER && e.gate >= 0) r_own = e.r_sel[m_own];
   }
+  if (MODE == EPI_ROUTER && m_own < a.M) xrow_own = stream_row_of(e, m_own);
   constexpr int NCH_FULL = BN / 32;
   const int nch = swiglu ? NCH_FULL / 2 : NCH_FULL;
   const int col_tile0 = swiglu ? n_blk * (BN / 2) : n_blk * BN;
@@ -500,6 +509,7 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   memset(&mB1, 0, sizeof(mB1));
   memset(&mB2, 0, sizeof(mB2));
   if (!make_map(&mA, p.A, p.K, p.M, p.lda, BM)) return cudaErrorInvalidValue;
+  if ((e.kind == EPI_ROUTER) != (BN == 32)) return cudaErrorInvalidValue;
   TcArgs a;
   a.M = p.M;
   a.N = p.N;
@@ -517,7 +527,7 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
     mB2 = mB0;
     tiles_n = (p.N + BN / 2 - 1) / (BN / 2);
   } else {
-    const int rows0 = p.nB > 1 ? p.split[0] : p.N;
+    const int rows0 = p.nB > 1 ? p.split[0] : (p.b_rows > 0 ? p.b_rows : p.N);
     if (!make_map(&mB0, p.B[0], p.K, rows0, p.ldb, BN)) return cudaErrorInvalidValue;
     if (p.nB > 1) {
       a.n_split1 = p.split[0];
@@ -537,14 +547,19 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   if (a.tiles <= 0) return cudaSuccess;
   void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
             const TcArgs) = nullptr;
-  switch (e.kind) {
-    case EPI_STORE: k = gemm_tc_kernel<BN, EPI_STORE>; break;
-    case EPI_OPROJ: k = gemm_tc_kernel<BN, EPI_OPROJ>; break;
-    case EPI_SWIGLU: k = gemm_tc_kernel<BN, EPI_SWIGLU>; break;
-    case EPI_DOWN_SCATTER: k = gemm_tc_kernel<BN, EPI_DOWN_SCATTER>; break;
-    default: return cudaErrorInvalidValue;
+  if constexpr (BN == 32) {
+    k = gemm_tc_kernel<BN, EPI_ROUTER>;
+  } else {
+    switch (e.kind) {
+      case EPI_STORE: k = gemm_tc_kernel<BN, EPI_STORE>; break;
+      case EPI_OPROJ: k = gemm_tc_kernel<BN, EPI_OPROJ>; break;
+      case EPI_SWIGLU: k = gemm_tc_kernel<BN, EPI_SWIGLU>; break;
+      case EPI_DOWN_SCATTER: k = gemm_tc_kernel<BN, EPI_DOWN_SCATTER>; break;
+      default: return cudaErrorInvalidValue;
+    }
   }
-  static bool attr_set[4] = {false, false, false, false};
+  if (!k) return cudaErrorInvalidValue;
+  static bool attr_set[5] = {false, false, false, false, false};
   if (!attr_set[e.kind]) {
     cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     if (err != cudaSuccess) return err;
@@ -557,6 +572,9 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
 // Tile widths a problem may use: the q|k|v boundaries must fall on tile edges.
 bool bn_ok(const GemmTcProblem& p, const Epilogue& e, int bn) {
   if (e.kind == EPI_SWIGLU) return bn == 256;
+  // Router logits: 32-wide tiles only, so that a logit's arithmetic never depends on
+  // how many router vectors share its launch.
+  if (e.kind == EPI_ROUTER) return bn == 32 && p.N <= 32 && p.nB == 1;
   for (int i = 1; i < p.nB; ++i)
     if (p.split[i - 1] % bn) return false;
   return true;
@@ -567,16 +585,19 @@ bool bn_ok(const GemmTcProblem& p, const Epilogue& e, int bn) {
 bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e) {
   if (!tma_available()) return false;
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return false;
-  if (p.K % 8 || p.lda % 8 || p.ldb % 8 || p.N % 8) return false;
+  if (p.K % 8 || p.lda % 8 || p.ldb % 8) return false;
+  if (p.N % 8 && e.kind != EPI_ROUTER) return false;   // the others store 8-column groups
+  if (p.b_rows && (p.b_rows < p.N || p.nB != 1)) return false;
   if (((uintptr_t)p.A & 15) || ((uintptr_t)p.B[0] & 15)) return false;
   if (e.kind == EPI_SWIGLU && (p.nB != 2 || ((uintptr_t)p.B[1] & 15))) return false;
   if (e.kind != EPI_SWIGLU)
     for (int i = 1; i < p.nB; ++i)
       if ((uintptr_t)p.B[i] & 15) return false;
-  return bn_ok(p, e, 128) || bn_ok(p, e, 256);
+  return bn_ok(p, e, 32) || bn_ok(p, e, 128) || bn_ok(p, e, 256);
 }
 
 cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
+  if (e.kind == EPI_ROUTER) return launch_bn<32>(c, p, e);
   const int tiles_m = (p.M + BM - 1) / BM;
   const int sms = sm_count();
   // Pick the tile width with the shortest estimated time: waves x tile width, with

@@ -93,13 +93,25 @@ cudaError_t launch_gated_scatter(const Ctx& c, xmod_dtype dt, int B, int T, int 
                                  void* x, const int32_t* idx, const float* r_sel, const void* a,
                                  const void* f, float varsigma, int gate);
 
+// Up to kMax row pointers passed by value to a kernel.
+struct RowPtrs {
+  static constexpr int kMax = 32;
+  const void* p[kMax];
+};
+// dst [total, d] bf16 = the `count` rows, then zero rows up to `total`.
+cudaError_t launch_stack_rows(const Ctx& c, const RowPtrs& rows, int count, int total, int d,
+                              void* dst);
+
 // ---------------------------------------------------------------- GEMM with fused epilogues
 
 enum EpiKind {
   EPI_STORE = 0,         // out[m, n] = acc
   EPI_OPROJ = 1,         // out2[m, n] = h = x_row(m)[n] + acc (fp32); out[m, n] = a = acc if out
   EPI_SWIGLU = 2,        // out[m, n] = silu(acc_gate) * acc_up
-  EPI_DOWN_SCATTER = 3,  // x_row(m)[n] = gated residual of (a = h[m, n] - x, f = acc)
+  EPI_DOWN_SCATTER = 3,  // x_row(m)[n] = gated residual of (a = h[m, n] - x, f = acc);
+                         // also out[m, n] = that new row value (bf16) when out is set
+  EPI_ROUTER = 4,        // out[n * ldo + stream token of m] = acc + bias[token] (fp32);
+                         // tensor-core path only, 32-wide tiles, any N <= 32
 };
 
 // Compact row m of a block belongs to sequence b = m / n_per_seq at position
@@ -115,6 +127,7 @@ struct Epilogue {
   int T = 0, n_per_seq = 0, d = 0;
   const float* h = nullptr;     // DOWN: h = x_sel + a [M, d] fp32 (the attention residual is h - x)
   const float* r_sel = nullptr; // DOWN: gates [M]
+  const float* bias = nullptr;  // ROUTER: per-token logit bias [B*T] or NULL
   float varsigma = 1.0f;
   int gate = -1;                // DOWN: XMOD_GATE_XMOD, XMOD_GATE_MOD, or -1 for dense
   // STORE (tensor-core path): columns >= vt_col0 are the values v; they are written
@@ -141,6 +154,7 @@ struct GemmTcProblem {
   int nB = 1;
   int split[2] = {0, 0};
   int ldb = 0;
+  int b_rows = 0;  // rows of B[0] the tensor map spans (0: N); may exceed N
 };
 bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e);
 cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e);

@@ -10,6 +10,8 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -489,6 +491,32 @@ static cudaError_t launch_gather_rmsnorm_rows(const Ctx& c, int vpl, unsigned bl
   }
 #undef XMOD_GR_CASE
   return cudaGetLastError();
+}
+
+// ================================================================ router vectors as rows
+
+// dst[j, :] = rows.p[j][:] for j < count; rows [count, total) are zeroed. bf16 rows
+// of d elements, d % 8 == 0, one 16-byte vector per thread.
+__global__ void stack_rows_kernel(RowPtrs rows, int count, int total, int d, uint4* dst) {
+  pdl_trigger();
+  pdl_wait();
+  const int vecs = d / 8;
+  const int64_t n = (int64_t)total * vecs;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(i / vecs), v = (int)(i - (int64_t)j * vecs);
+    dst[i] = j < count ? reinterpret_cast<const uint4*>(rows.p[j])[v] : make_uint4(0, 0, 0, 0);
+  }
+}
+
+cudaError_t launch_stack_rows(const Ctx& c, const RowPtrs& rows, int count, int total, int d,
+                              void* dst) {
+  if (count < 0 || count > RowPtrs::kMax || total < count || d % 8) return cudaErrorInvalidValue;
+  const int64_t n = (int64_t)total * (d / 8);
+  if (n <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, 1024);
+  return launch_pdl(stack_rows_kernel, dim3(blocks), dim3(256), 0, c.stream, rows, count, total,
+                    d, (uint4*)dst);
 }
 
 cudaError_t launch_gather(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
