@@ -22,6 +22,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <limits.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "internal.h"
@@ -70,12 +71,13 @@ struct TcArgs {
 #define XMOD_TILE_BAND 16
 #endif
 
-__device__ __forceinline__ void tile_coords(const TcArgs& a, int tile, int& m_blk, int& n_blk) {
-  const int per_band = XMOD_TILE_BAND * a.tiles_n;
+__device__ __forceinline__ void tile_coords(const TcArgs& a, int tile, int& m_blk, int& n_blk,
+                                            int band_rows = XMOD_TILE_BAND) {
+  const int per_band = band_rows * a.tiles_n;
   const int band = tile / per_band;
   const int r = tile - band * per_band;
-  const int m_first = band * XMOD_TILE_BAND;
-  const int rows = min(XMOD_TILE_BAND, a.tiles_m - m_first);
+  const int m_first = band * band_rows;
+  const int rows = min(band_rows, a.tiles_m - m_first);
   m_blk = m_first + r % rows;
   n_blk = r / rows;
 }
@@ -160,6 +162,14 @@ __device__ __forceinline__ void load32_f32(const float* p, float (&v)[32], int r
 #endif
 #ifndef XMOD_COST_128
 #define XMOD_COST_128 1.33
+#endif
+// Waves of 256 x 256 tiles from which a GEMM runs on CTA pairs.
+#ifndef XMOD_PAIR_MIN_WAVES
+#define XMOD_PAIR_MIN_WAVES 6
+#endif
+// 0 disables the CTA-pair kernels.
+#ifndef XMOD_GEMM_PAIRS
+#define XMOD_GEMM_PAIRS 1
 #endif
 
 // Inputs of the O-projection / down-projection epilogues for one 32-column chunk of
@@ -479,6 +489,182 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #undef ACC_EMPTY
 }
 
+// ---------------------------------------------------------------- CTA-pair variant
+//
+// The same GEMM on 256 x BN tiles shared by the two CTAs of a (2, 1, 1) cluster
+// (tcgen05 cta_group::2). CTA r of the pair loads rows [128 r, 128 r + 128) of the A
+// tile and rows [r BN/2, (r+1) BN/2) of the B tile (for SwiGLU: the gate rows in CTA 0,
+// the up rows in CTA 1), so each SM streams half the B bytes per FLOP of the
+// single-CTA kernel. CTA 0 issues every MMA; completion of a stage is signalled to
+// both CTAs' producers, completion of a tile to both CTAs' epilogues, which then
+// work exactly as in the single-CTA kernel on their own 128 TMEM lanes.
+template <int BN>
+struct Cfg2 {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+};
+
+// Row blocks (of 256) per band of the pair kernel's tile order.
+#ifndef XMOD_TILE_BAND2
+#define XMOD_TILE_BAND2 8
+#endif
+
+template <int BN, int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+                const TcArgs args) {
+  using C = Cfg2<BN>;
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = sA + C::STAGES * C::A_BYTES;
+  const uint32_t sBar = sB + C::STAGES * C::B_BYTES;
+  const uint32_t sTmem = sBar + 8 * (2 * C::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (sTmem - base));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (sTmem - base) + 8);
+#define FULL(s) (sBar + 8u * (s))
+#define EMPTY(s) (sBar + 8u * (C::STAGES + (s)))
+#define ACC_FULL(a) (sBar + 8u * (2 * C::STAGES + (a)))
+#define ACC_EMPTY(a) (sBar + 8u * (2 * C::STAGES + 2 + (a)))
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = (args.K + BK - 1) / BK;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = (int)cluster_id_x(), npairs = (int)cluster_count_x();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(FULL(s), 1);     // used in CTA 0: its producer's arrival + both CTAs' bytes
+      mbar_init(EMPTY(s), 1);    // one multicast commit per use
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(ACC_FULL(a), 1);
+      mbar_init(ACC_EMPTY(a), 2 * EPI_WARPS);   // used in CTA 0: one lane per epilogue warp
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB0);
+    if (MODE == EPI_SWIGLU || args.n_split1 < args.N) prefetch_tensormap(&tmB1);
+    if (MODE != EPI_SWIGLU && args.n_split2 < args.N) prefetch_tensormap(&tmB2);
+  }
+  if (warp == 1) tmem_alloc_pair(sTmem, C::TMEM_COLS);
+  tc_fence_before();
+  cluster_sync_all();   // both CTAs' barriers initialised, TMEM address written
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // everything above overlapped the previous kernel's tail
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;
+      for (int tile = pair; tile < args.tiles && !*abort_flag; tile += npairs) {
+        int m_blk, n_blk;
+        tile_coords(args, tile, m_blk, n_blk, XMOD_TILE_BAND2);
+        const int m0 = m_blk * (2 * BM) + (int)rank * BM;
+        const CUtensorMap* mp = &tmB0;
+        int brow = n_blk * BN;
+        if (MODE == EPI_SWIGLU) {
+          if (rank) mp = &tmB1;          // up rows in CTA 1, gate rows in CTA 0
+          brow = n_blk * (BN / 2);
+        } else {
+          if (brow >= args.n_split2) {
+            mp = &tmB2;
+            brow -= args.n_split2;
+          } else if (brow >= args.n_split1) {
+            mp = &tmB1;
+            brow -= args.n_split1;
+          }
+          brow += (int)rank * (BN / 2);
+        }
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+          if (!mbar_wait_cluster(EMPTY(s), ph ^ 1u, abort_flag, args.status)) break;
+          const uint32_t full0 = mapa_shared(FULL(s), 0);
+          if (rank == 0) mbar_arrive_expect_tx(FULL(s), 2 * C::STAGE_BYTES);
+          tma_load_2d_pair(sA + s * C::A_BYTES, &tmA, full0, kb * BK, m0);
+          tma_load_2d_pair(sB + s * C::B_BYTES, mp, full0, kb * BK, brow);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+      int it = 0, lt = 0;
+      for (int tile = pair; tile < args.tiles && !*abort_flag; tile += npairs, ++lt) {
+        const int acc = lt & 1;
+        const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+        if (!mbar_wait_cluster(ACC_EMPTY(acc), aph ^ 1u, abort_flag, args.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+          if (!mbar_wait_cluster(FULL(s), ph, abort_flag, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = smem_desc_sw128(sA + s * C::A_BYTES);
+          const uint64_t bd = smem_desc_sw128(sB + s * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16_pair(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair(EMPTY(s));
+        }
+        if (!ok) break;
+        mma_commit_pair(ACC_FULL(acc));
+      }
+    }
+  } else {
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 belong to this warp
+    int lt = 0;
+    for (int tile = pair; tile < args.tiles; tile += npairs, ++lt) {
+      const int acc = lt & 1;
+      const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+      if (!mbar_wait_cluster(ACC_FULL(acc), aph, abort_flag, args.status)) break;
+      tc_fence_after();
+      int m_blk, n_blk;
+      tile_coords(args, tile, m_blk, n_blk, XMOD_TILE_BAND2);
+      const int wrow0 = m_blk * (2 * BM) + (int)rank * BM + quad * 32;
+      const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
+      epilogue_tile<BN, MODE>(args, wrow0, lane, n_blk, t_row, (warp - 2) / 4, EPI_WARPS / 4);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(ACC_EMPTY(acc), 0));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // A wait ran out: give copies and MMAs still in flight time to land before the
+    // shared memory and TMEM are released.
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 20000000ull) {
+    }
+  }
+  cluster_sync_all();   // neither CTA leaves while the pair's MMAs or arrivals may touch it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  }
+#undef FULL
+#undef EMPTY
+#undef ACC_FULL
+#undef ACC_EMPTY
+}
+
 // ---------------------------------------------------------------- host side
 
 // 2-D bf16 tensor map over a row-major [rows, inner] matrix with row stride `ld`
@@ -502,15 +688,14 @@ int sm_count() {
   return g_sms;
 }
 
+// Tensor maps and kernel arguments for tiles of tile_m x BN. B tiles are loaded
+// b_box rows at a time (BN, or BN / 2 when a CTA pair splits them).
 template <int BN>
-cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
-  using Cf = Cfg<BN>;
-  CUtensorMap mA, mB0, mB1, mB2;
+bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, int b_box,
+           CUtensorMap& mA, CUtensorMap& mB0, CUtensorMap& mB1, CUtensorMap& mB2, TcArgs& a) {
   memset(&mB1, 0, sizeof(mB1));
   memset(&mB2, 0, sizeof(mB2));
-  if (!make_map(&mA, p.A, p.K, p.M, p.lda, BM)) return cudaErrorInvalidValue;
-  if ((e.kind == EPI_ROUTER) != (BN == 32)) return cudaErrorInvalidValue;
-  TcArgs a;
+  if (!make_map(&mA, p.A, p.K, p.M, p.lda, BM)) return false;
   a.M = p.M;
   a.N = p.N;
   a.K = p.K;
@@ -519,24 +704,24 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   a.status = c.status;
   a.n_split1 = INT_MAX;
   a.n_split2 = INT_MAX;
-  a.tiles_m = (p.M + BM - 1) / BM;
+  a.tiles_m = (p.M + tile_m - 1) / tile_m;
   int tiles_n;
   if (e.kind == EPI_SWIGLU) {
-    if (!make_map(&mB0, p.B[0], p.K, p.N, p.ldb, BN / 2)) return cudaErrorInvalidValue;
-    if (!make_map(&mB1, p.B[1], p.K, p.N, p.ldb, BN / 2)) return cudaErrorInvalidValue;
+    if (!make_map(&mB0, p.B[0], p.K, p.N, p.ldb, BN / 2)) return false;
+    if (!make_map(&mB1, p.B[1], p.K, p.N, p.ldb, BN / 2)) return false;
     mB2 = mB0;
     tiles_n = (p.N + BN / 2 - 1) / (BN / 2);
   } else {
     const int rows0 = p.nB > 1 ? p.split[0] : (p.b_rows > 0 ? p.b_rows : p.N);
-    if (!make_map(&mB0, p.B[0], p.K, rows0, p.ldb, BN)) return cudaErrorInvalidValue;
+    if (!make_map(&mB0, p.B[0], p.K, rows0, p.ldb, b_box)) return false;
     if (p.nB > 1) {
       a.n_split1 = p.split[0];
       const int rows1 = (p.nB > 2 ? p.split[1] : p.N) - p.split[0];
-      if (!make_map(&mB1, p.B[1], p.K, rows1, p.ldb, BN)) return cudaErrorInvalidValue;
+      if (!make_map(&mB1, p.B[1], p.K, rows1, p.ldb, b_box)) return false;
     }
     if (p.nB > 2) {
       a.n_split2 = p.split[1];
-      if (!make_map(&mB2, p.B[2], p.K, p.N - p.split[1], p.ldb, BN)) return cudaErrorInvalidValue;
+      if (!make_map(&mB2, p.B[2], p.K, p.N - p.split[1], p.ldb, b_box)) return false;
     }
     if (p.nB < 2) mB1 = mB0;
     if (p.nB < 3) mB2 = mB0;
@@ -544,6 +729,16 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   }
   a.tiles_n = tiles_n;
   a.tiles = a.tiles_m * tiles_n;
+  return true;
+}
+
+template <int BN>
+cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
+  using Cf = Cfg<BN>;
+  if ((e.kind == EPI_ROUTER) != (BN == 32)) return cudaErrorInvalidValue;
+  CUtensorMap mA, mB0, mB1, mB2;
+  TcArgs a;
+  if (!setup<BN>(c, p, e, BM, BN, mA, mB0, mB1, mB2, a)) return cudaErrorInvalidValue;
   if (a.tiles <= 0) return cudaSuccess;
   void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
             const TcArgs) = nullptr;
@@ -567,6 +762,56 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   }
   const int grid = a.tiles < sm_count() ? a.tiles : sm_count();
   return launch_pdl(k, dim3(grid), dim3(NUM_THREADS), Cf::SMEM, c.stream, mA, mB0, mB1, mB2, a);
+}
+
+// CTA pairs that fit on the device at once with the pair kernel's shared memory
+// (SMs of a GPC that cannot be paired stay unused).
+template <int BN>
+int max_pairs() {
+  static int cached = 0;
+  if (!cached) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (unsigned)sm_count());
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = Cfg2<BN>::SMEM;
+    auto k = gemm_tc2_kernel<BN, EPI_STORE>;
+    int n = 0;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<BN>::SMEM) ==
+            cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n > 0)
+      cached = n;
+    else
+      cached = sm_count() / 2;
+    (void)cudaGetLastError();
+  }
+  return cached;
+}
+
+template <int BN>
+cudaError_t launch_bn2(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
+  using Cf = Cfg2<BN>;
+  if (e.kind == EPI_ROUTER) return cudaErrorInvalidValue;
+  CUtensorMap mA, mB0, mB1, mB2;
+  TcArgs a;
+  if (!setup<BN>(c, p, e, 2 * BM, BN / 2, mA, mB0, mB1, mB2, a)) return cudaErrorInvalidValue;
+  if (a.tiles <= 0) return cudaSuccess;
+  void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+            const TcArgs) = nullptr;
+  switch (e.kind) {
+    case EPI_STORE: k = gemm_tc2_kernel<BN, EPI_STORE>; break;
+    case EPI_OPROJ: k = gemm_tc2_kernel<BN, EPI_OPROJ>; break;
+    case EPI_SWIGLU: k = gemm_tc2_kernel<BN, EPI_SWIGLU>; break;
+    case EPI_DOWN_SCATTER: k = gemm_tc2_kernel<BN, EPI_DOWN_SCATTER>; break;
+    default: return cudaErrorInvalidValue;
+  }
+  static bool attr_set[4] = {false, false, false, false};
+  if (!attr_set[e.kind]) {
+    cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+    if (err != cudaSuccess) return err;
+    attr_set[e.kind] = true;
+  }
+  const int pairs = a.tiles < max_pairs<BN>() ? a.tiles : max_pairs<BN>();
+  return launch_pdl(k, dim3(2 * pairs), dim3(NUM_THREADS), Cf::SMEM, c.stream, mA, mB0, mB1, mB2, a);
 }
 
 // Tile widths a problem may use: the q|k|v boundaries must fall on tile edges.
@@ -596,12 +841,36 @@ bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e) {
   return bn_ok(p, e, 32) || bn_ok(p, e, 128) || bn_ok(p, e, 256);
 }
 
+// The pair threshold in waves; the environment variable XMOD_PAIR_MIN_WAVES (read at
+// every launch) overrides it, e.g. 0 to run every eligible GEMM on CTA pairs.
+int pair_min_waves() {
+  const char* v = getenv("XMOD_PAIR_MIN_WAVES");
+  if (v && *v) {
+    char* end = nullptr;
+    const long w = strtol(v, &end, 10);
+    if (end && *end == '\0' && w >= 0 && w < 1000000) return (int)w;
+  }
+  return XMOD_PAIR_MIN_WAVES;
+}
+
 cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   if (e.kind == EPI_ROUTER) return launch_bn<32>(c, p, e);
-  const int tiles_m = (p.M + BM - 1) / BM;
+  // CTA pairs on 256 x 256 tiles when there are enough of them. Measured on GB300
+  // against the best single-CTA tiling (A4K8 block, d = 1536): 256 x 256 pair tiles cost
+  // 18% less time per tile but about 5 us more per launch, so they win from six waves
+  // up (gate/up at M = 4096: 58.7 -> 53.9 us; every dense-layer GEMM at M = 32768:
+  // 7-17%) and lose below three (q|k|v, o-proj, down at M = 4096: 3-12%). Narrower
+  // pair tiles were slower than single-CTA tiles of the same width.
+  if (XMOD_GEMM_PAIRS && p.M > BM && bn_ok(p, e, 256)) {
+    const long tiles_m = (p.M + 2 * BM - 1) / (2 * BM);
+    const int cols = e.kind == EPI_SWIGLU ? 128 : 256;
+    const long tiles = tiles_m * ((p.N + cols - 1) / cols);
+    if (tiles >= (long)pair_min_waves() * max_pairs<256>()) return launch_bn2<256>(c, p, e);
+  }
   const int sms = sm_count();
-  // Pick the tile width with the shortest estimated time: waves x tile width, with
-  // narrower tiles charged for their higher shared-memory traffic per FLOP.
+  // Otherwise the tile width with the shortest estimated time: waves x tile width,
+  // with narrower tiles charged for their higher shared-memory traffic per FLOP.
+  const int tiles_m = (p.M + BM - 1) / BM;
   const int widths[3] = {256, 192, 128};
   const double cost_per_col[3] = {XMOD_COST_256, XMOD_COST_192, XMOD_COST_128};
   int best = -1;

@@ -1,0 +1,76 @@
+"""The CTA-pair GEMM kernels (tcgen05 cta_group::2, 256 x 256 tiles) against the
+single-CTA kernels and the oracle.
+
+The library puts a GEMM on CTA pairs only from six waves of pair tiles up (about 450
+tiles), so at test sizes they run only when XMOD_PAIR_MIN_WAVES=0 asks for them.
+Single layers (dense and sparse) run once each way: the q|k|v, o-projection, gate/up
+and down-projection epilogues all run on pairs, with ragged row and column tiles."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+from sparse_depth_token_gb300 import inputs as I
+from tests import _util as U
+from tests._gpu import dev_layer, from_dev, need_gpu, oracle_dims, oracle_layer, to_dev, torch, workspace, xmod_dims
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def X():
+    need_gpu()
+    from sparse_depth_token_gb300 import xmod
+    xmod.load()
+    return xmod
+
+
+CASES = {
+    # M = 1024 dense rows: 4 pair rows of tiles; q|k|v N = 1024, d = 256, F = 384
+    "bf16_small": I.WORKLOADS["a4k8_bf16"].replace(B=2, T=512, d=256, hq=4, hkv=2, F=384,
+                                                   seed=41, weight_std=0.049),
+    # M = 2000 dense / 250 sparse rows (the last pair tile half empty), F = 264 (ragged)
+    "bf16_ragged": I.WORKLOADS["a4k8_bf16"].replace(B=2, T=1000, d=256, hq=6, hkv=2, F=264,
+                                                    seed=42, weight_std=0.049),
+}
+
+
+def _run(X, w, kind, x, lw, bias, pairs):
+    dt = w.dtype
+    dm = xmod_dims(w)
+    ws = workspace(dm, w.K)
+    xd = to_dev(x, dt)
+    old = os.environ.get("XMOD_PAIR_MIN_WAVES")
+    os.environ["XMOD_PAIR_MIN_WAVES"] = "0" if pairs else "1000000"
+    try:
+        X.reset_status(ws)
+        X.layer_fwd(dm, kind, w.K, 0, X.layer_weights(dev_layer(lw, dt), lw["varsigma"]), xd,
+                    torch.from_numpy(bias).cuda() if bias is not None else None, None, None, ws)
+        assert X.sync_status(ws) == X.OK
+    finally:
+        if old is None:
+            del os.environ["XMOD_PAIR_MIN_WAVES"]
+        else:
+            os.environ["XMOD_PAIR_MIN_WAVES"] = old
+    return xd
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+@pytest.mark.parametrize("kind", [0, 1])
+def test_pair_gemms_match_single_cta_and_oracle(X, case, kind):
+    w = CASES[case]
+    dt = w.dtype
+    lw = I.layer_weights(w, 2)
+    bias = I.router_bias(w)
+    x = I.residual_stream(w)
+    if kind == 1:
+        x, _ = U.enforce_routing_margin(x, dt, lw["w_r"], bias, w.K)
+    y_pair = _run(X, w, kind, x, lw, bias, pairs=True)
+    y_single = _run(X, w, kind, x, lw, bias, pairs=False)
+    # each output element is the same dot product in the same k order either way
+    assert torch.equal(y_pair.view(torch.int16), y_single.view(torch.int16))
+    ref = O.layer_fwd(oracle_dims(w), kind, w.K, 0, oracle_layer(lw, dt), I.to_f64(x, dt),
+                      bias=bias)
+    got = from_dev(y_pair, dt).reshape(w.B, w.T, w.d)
+    U.assert_close(got, ref["y"], dt, "y", stored_ref=got)
