@@ -58,6 +58,7 @@ struct TcArgs {
   int mode;                // EpiKind
   int n_split1, n_split2;  // STORE: first accumulator column served by B map 1 / map 2
   int tiles_m, tiles_n, tiles;
+  int v8;                  // epilogue row segments may use 32-byte accesses
   Epilogue e;
   int* status;
 };
@@ -93,62 +94,92 @@ __device__ __forceinline__ int64_t stream_row_of(const Epilogue& e, int m) {
   return b * e.T + t;
 }
 
-// Row-segment helpers of the direct epilogue: 32 consecutive columns of one row,
-// of which the first `rem` exist (rem is a multiple of 8 or >= 32).
-__device__ __forceinline__ void store32_bf16(__nv_bfloat16* p, const float (&v)[32], int rem) {
+// Row-segment helpers of the direct epilogue: 32 consecutive columns of one row, of
+// which the first `rem` exist (rem a multiple of 8, or >= 32). With `v8` (every
+// tensor the epilogue touches is 32-byte aligned with 32-byte-multiple row strides)
+// a lane moves 32 bytes per access -- a whole sector -- instead of 16.
+__device__ __forceinline__ void st_v8(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x),
+               "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+__device__ __forceinline__ void ld_v8(const void* p, uint4& a, uint4& b) {
+  asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
+                 "=r"(b.w)
+               : "l"(p));
+}
+
+// bf16 segment: q[g] holds columns 8g .. 8g+7.
+__device__ __forceinline__ void st_seg_bf16(__nv_bfloat16* p, const uint4 (&q)[4], int rem,
+                                            bool v8) {
+  if (v8) {
+#pragma unroll
+    for (int g = 0; g < 4; g += 2) {
+      if (8 * g + 16 <= rem) st_v8(p + 8 * g, q[g], q[g + 1]);
+      else if (8 * g < rem) *reinterpret_cast<uint4*>(p + 8 * g) = q[g];
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (8 * g < rem) *reinterpret_cast<uint4*>(p + 8 * g) = q[g];
+  }
+}
+__device__ __forceinline__ void ld_seg_bf16(const __nv_bfloat16* p, uint4 (&q)[4], int rem,
+                                            bool v8) {
+  if (v8) {
+#pragma unroll
+    for (int g = 0; g < 4; g += 2) {
+      if (8 * g + 16 <= rem) ld_v8(p + 8 * g, q[g], q[g + 1]);
+      else if (8 * g < rem) q[g] = *reinterpret_cast<const uint4*>(p + 8 * g);
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (8 * g < rem) q[g] = *reinterpret_cast<const uint4*>(p + 8 * g);
+  }
+}
+// fp32 segment: f[g] holds columns 4g .. 4g+3.
+__device__ __forceinline__ void st_seg_f32(float* p, const float4 (&f)[8], int rem, bool v8) {
+  if (v8) {
+#pragma unroll
+    for (int g = 0; g < 8; g += 2) {
+      if (4 * g + 8 <= rem)
+        st_v8(p + 4 * g, reinterpret_cast<const uint4&>(f[g]), reinterpret_cast<const uint4&>(f[g + 1]));
+      else if (4 * g < rem) *reinterpret_cast<float4*>(p + 4 * g) = f[g];
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      if (4 * g < rem) *reinterpret_cast<float4*>(p + 4 * g) = f[g];
+  }
+}
+__device__ __forceinline__ void ld_seg_f32(const float* p, float4 (&f)[8], int rem, bool v8) {
+  if (v8) {
+#pragma unroll
+    for (int g = 0; g < 8; g += 2) {
+      if (4 * g + 8 <= rem)
+        ld_v8(p + 4 * g, reinterpret_cast<uint4&>(f[g]), reinterpret_cast<uint4&>(f[g + 1]));
+      else if (4 * g < rem) f[g] = *reinterpret_cast<const float4*>(p + 4 * g);
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      if (4 * g < rem) f[g] = *reinterpret_cast<const float4*>(p + 4 * g);
+  }
+}
+
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* p, const float (&v)[32], int rem,
+                                             bool v8) {
+  uint4 q[4];
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    if (8 * g < rem) {
-      uint4 q;
-      q.x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
-      q.y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
-      q.z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
-      q.w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
-      *reinterpret_cast<uint4*>(p + 8 * g) = q;
-    }
+    q[g].x = pack_bf16x2(v[8 * g + 0], v[8 * g + 1]);
+    q[g].y = pack_bf16x2(v[8 * g + 2], v[8 * g + 3]);
+    q[g].z = pack_bf16x2(v[8 * g + 4], v[8 * g + 5]);
+    q[g].w = pack_bf16x2(v[8 * g + 6], v[8 * g + 7]);
   }
-}
-
-__device__ __forceinline__ void store32_f32(float* p, const float (&v)[32], int rem) {
-#pragma unroll
-  for (int g = 0; g < 8; ++g)
-    if (4 * g < rem)
-      *reinterpret_cast<float4*>(p + 4 * g) =
-          make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-}
-
-__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* p, float (&v)[32], int rem) {
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    if (8 * g < rem) {
-      const uint4 q = *reinterpret_cast<const uint4*>(p + 8 * g);
-      const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&q);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h2[i]);
-        v[8 * g + 2 * i] = f.x;
-        v[8 * g + 2 * i + 1] = f.y;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[8 * g + i] = 0.f;
-    }
-  }
-}
-
-__device__ __forceinline__ void load32_f32(const float* p, float (&v)[32], int rem) {
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    if (4 * g < rem) {
-      const float4 q = *reinterpret_cast<const float4*>(p + 4 * g);
-      v[4 * g] = q.x;
-      v[4 * g + 1] = q.y;
-      v[4 * g + 2] = q.z;
-      v[4 * g + 3] = q.w;
-    } else {
-      v[4 * g] = v[4 * g + 1] = v[4 * g + 2] = v[4 * g + 3] = 0.f;
-    }
-  }
+  st_seg_bf16(p, q, rem, v8);
 }
 
 // Relative cost per output column of a tile of width 256 / 192 / 128 (the narrower
@@ -186,16 +217,8 @@ __device__ __forceinline__ void epi_load_in(const TcArgs& a, int m, int col0, in
   const Epilogue& e = a.e;
   if (m >= a.M || col0 >= a.N) return;
   const int rem = a.N - col0;
-  const uint4* xp = reinterpret_cast<const uint4*>((const __nv_bfloat16*)e.x + xrow + col0);
-#pragma unroll
-  for (int g = 0; g < 4; ++g)
-    if (8 * g < rem) in.x[g] = xp[g];
-  if (MODE == EPI_DOWN_SCATTER) {
-    const float4* hp = reinterpret_cast<const float4*>(e.h + (int64_t)m * e.d + col0);
-#pragma unroll
-    for (int g = 0; g < 8; ++g)
-      if (4 * g < rem) in.h[g] = hp[g];
-  }
+  ld_seg_bf16((const __nv_bfloat16*)e.x + xrow + col0, in.x, rem, a.v8);
+  if (MODE == EPI_DOWN_SCATTER) ld_seg_f32(e.h + (int64_t)m * e.d + col0, in.h, rem, a.v8);
 }
 
 __device__ __forceinline__ void unpack_x(const EpiIn& in, float (&xv)[32]) {
@@ -223,24 +246,21 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int m, in
   if (m >= a.M || col0 >= a.N) return;
   const int rem = a.N - col0;
   if (MODE == EPI_STORE || MODE == EPI_SWIGLU) {
-    store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem);
+    store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem, a.v8);
   } else if (MODE == EPI_OPROJ) {
-    if (e.out) store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem);
-    float* hp = (float*)e.out2 + (int64_t)m * e.ldo2 + col0;
+    if (e.out) store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem, a.v8);
+    float4 hv[8];   // h = x + a
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {   // 8 columns at a time: h = x + a
-      if (8 * g >= rem) break;
+    for (int g = 0; g < 4; ++g) {
       const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&in.x[g]);
-      float hv[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(x2[i]);
-        hv[2 * i] = f.x + v[8 * g + 2 * i];
-        hv[2 * i + 1] = f.y + v[8 * g + 2 * i + 1];
-      }
-      *reinterpret_cast<float4*>(hp + 8 * g) = make_float4(hv[0], hv[1], hv[2], hv[3]);
-      *reinterpret_cast<float4*>(hp + 8 * g + 4) = make_float4(hv[4], hv[5], hv[6], hv[7]);
+      const float2 f0 = __bfloat1622float2(x2[0]), f1 = __bfloat1622float2(x2[1]);
+      const float2 f2 = __bfloat1622float2(x2[2]), f3 = __bfloat1622float2(x2[3]);
+      hv[2 * g] = make_float4(f0.x + v[8 * g], f0.y + v[8 * g + 1], f1.x + v[8 * g + 2],
+                              f1.y + v[8 * g + 3]);
+      hv[2 * g + 1] = make_float4(f2.x + v[8 * g + 4], f2.y + v[8 * g + 5], f3.x + v[8 * g + 6],
+                                  f3.y + v[8 * g + 7]);
     }
+    st_seg_f32((float*)e.out2 + (int64_t)m * e.ldo2 + col0, hv, rem, a.v8);
   } else if (MODE == EPI_ROUTER) {   // xrow is the stream token here
     float* sp = (float*)e.out + (int64_t)col0 * e.ldo + xrow;
     const float b = e.bias ? e.bias[xrow] : 0.0f;
@@ -248,11 +268,10 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int m, in
     for (int i = 0; i < 32; ++i)
       if (i < rem) sp[(int64_t)i * e.ldo] = v[i] + b;
   } else {  // EPI_DOWN_SCATTER, a = h - x
-    __nv_bfloat16* xp = (__nv_bfloat16*)e.x + xrow + col0;
     const float g7 = e.varsigma * r;
+    uint4 qo[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {   // 8 columns at a time
-      if (8 * g >= rem) break;
       const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&in.x[g]);
       const float hv[8] = {in.h[2 * g].x, in.h[2 * g].y, in.h[2 * g].z, in.h[2 * g].w,
                            in.h[2 * g + 1].x, in.h[2 * g + 1].y, in.h[2 * g + 1].z,
@@ -271,15 +290,13 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int m, in
           else y[j] = hv[j] + fv;                                                     // dense
         }
       }
-      uint4 q;
-      q.x = pack_bf16x2(y[0], y[1]);
-      q.y = pack_bf16x2(y[2], y[3]);
-      q.z = pack_bf16x2(y[4], y[5]);
-      q.w = pack_bf16x2(y[6], y[7]);
-      *reinterpret_cast<uint4*>(xp + 8 * g) = q;
-      if (e.out)
-        *reinterpret_cast<uint4*>((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0 + 8 * g) = q;
+      qo[g].x = pack_bf16x2(y[0], y[1]);
+      qo[g].y = pack_bf16x2(y[2], y[3]);
+      qo[g].z = pack_bf16x2(y[4], y[5]);
+      qo[g].w = pack_bf16x2(y[6], y[7]);
     }
+    st_seg_bf16((__nv_bfloat16*)e.x + xrow + col0, qo, rem, a.v8);
+    if (e.out) st_seg_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, qo, rem, a.v8);
   }
 }
 
@@ -704,6 +721,16 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
   a.status = c.status;
   a.n_split1 = INT_MAX;
   a.n_split2 = INT_MAX;
+  // 32-byte epilogue accesses need every row segment the epilogue touches aligned
+  auto seg_ok = [](const void* base, int64_t row_bytes) {
+    return ((uintptr_t)base & 31) == 0 && row_bytes % 32 == 0;
+  };
+  bool v8 = true;
+  if (e.out && e.kind != EPI_ROUTER) v8 = v8 && seg_ok(e.out, (int64_t)e.ldo * 2);
+  if (e.out2) v8 = v8 && seg_ok(e.out2, (int64_t)e.ldo2 * 4);
+  if (e.x) v8 = v8 && seg_ok(e.x, (int64_t)e.d * 2);
+  if (e.h) v8 = v8 && seg_ok(e.h, (int64_t)e.d * 4);
+  a.v8 = v8 ? 1 : 0;
   a.tiles_m = (p.M + tile_m - 1) / tile_m;
   int tiles_n;
   if (e.kind == EPI_SWIGLU) {
