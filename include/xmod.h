@@ -162,6 +162,37 @@ XMOD_API int xmod_stack_fwd(const xmod_dims* dims, int K, double A, int N0, int 
                    const xmod_layer_weights* layers, int n_layers, void* x_inout,
                    const float* bias, void* ws, size_t ws_bytes, void* stream);
 
+/* Options of xmod_stack_fwd_ex.
+ *
+ * bias_step: the token-choice bias dynamics of X-MoD notes Eq. 8 and the paragraph
+ *   after it -- inside a sparse-dense block a token's bias grows each time it is
+ *   selected and is cleared at the next dense anchor. The pages publish neither the
+ *   increment nor tau; here a sparse layer ranks and gates with
+ *     s_i = w_r . x_i + bias_i - bias_step * c_i,
+ *   c_i = how many earlier sparse layers of the block selected token i. 0 gives the
+ *   constant-bias stack of xmod_stack_fwd; must be finite and >= 0.
+ * layer_stats: NULL or device int32 [n_sparse, B, 4], per sparse layer (stack order)
+ *   and sequence: tokens selected (T / K); tokens whose ranked logit is >= 0 (the
+ *   causal threshold rule r >= 1/2 of X-MoD notes "top-k in training, causal threshold
+ *   at evaluation"); tokens on which the two rules agree (both select or both skip);
+ *   selected tokens that the previous sparse layer of the block also selected.
+ * update_hist: NULL or device int32 [N1, B, AK + 1]: for each sparse-dense block and
+ *   sequence, how many tokens the block's AK sparse layers updated 0, 1, ..., AK times.
+ * These are the inputs of the routing diagnostics of X-MoD notes Table 10 (coverage,
+ * adjacent-layer Jaccard overlap, threshold / top-k mask agreement, update counts). */
+typedef struct {
+  float bias_step;
+  int32_t* layer_stats;
+  int32_t* update_hist;
+} xmod_stack_opts;
+
+/* xmod_stack_fwd with options (opts NULL: exactly xmod_stack_fwd). The workspace
+ * size is the same (xmod_workspace_bytes). Invalid options: XMOD_ERR_INVALID_ARG. */
+XMOD_API int xmod_stack_fwd_ex(const xmod_dims* dims, int K, double A, int N0, int N1,
+                               xmod_gate gate, const xmod_layer_weights* layers, int n_layers,
+                               void* x_inout, const float* bias, const xmod_stack_opts* opts,
+                               void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------- allocation-free routing
  * The paper has no counterpart to this entry point: it exists for callers that
  * cannot allocate device memory -- a plugin inside another runtime that is given

@@ -62,6 +62,10 @@ def lib():
         L.oracle_stack_fwd.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                        ctypes.POINTER(LayerW), _DP, _DP, ctypes.c_int, _IP]
+        L.oracle_stack_dyn.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                       ctypes.POINTER(LayerW), _DP, _DP, ctypes.c_double,
+                                       ctypes.c_int, _IP, _DP]
         _lib = L
     return _lib
 
@@ -218,6 +222,28 @@ def layer_fwd(dm: Dims, kind, K, gate, layer: Layer, x, bias=None, idx_force=Non
     _check(lib().oracle_layer_fwd(ctypes.byref(dm), kind, K, gate, ctypes.byref(layer.struct),
                                   xp, bp, y.ctypes.data_as(_DP), *args, fp, mp))
     return out
+
+
+def stack_dyn(dm: Dims, K, gate, kinds, layers, x, bias=None, bias_step=0.0,
+              mirror_bf16=False):
+    """Whole stack with the token-choice bias dynamics (X-MoD notes, Eq. 8 and the
+    paragraph after it): a sparse layer's logit is w_r.x + bias - bias_step * (times
+    the token was selected since the last dense layer). Returns (x, idx, s): the final
+    stream and, per sparse layer in order, its selection [B, n] and logits [B, T]."""
+    x = np.array(x, dtype=np.float64, copy=True, order="C")
+    bias_a, bp = _d(bias)
+    n_sparse = sum(1 for k in kinds if k == SPARSE)
+    n = dm.T // K
+    idx = np.zeros((max(n_sparse, 1), dm.B, n), np.int32)
+    s = np.zeros((max(n_sparse, 1), dm.B, dm.T), np.float64)
+    kinds_a = (ctypes.c_int * len(kinds))(*kinds)
+    arr = (LayerW * len(layers))(*[l.struct for l in layers])
+    _check(lib().oracle_stack_dyn(ctypes.byref(dm), K, gate, len(kinds), kinds_a, arr,
+                                  x.ctypes.data_as(_DP), bp, ctypes.c_double(bias_step),
+                                  int(bool(mirror_bf16)),
+                                  idx.ctypes.data_as(_IP),
+                                  s.ctypes.data_as(_DP)))
+    return x, idx[:n_sparse], s[:n_sparse]
 
 
 def stack_fwd(dm: Dims, K, gate, kinds, layers, x, bias=None, mirror_bf16=False,

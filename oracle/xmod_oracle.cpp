@@ -387,4 +387,49 @@ int oracle_stack_fwd(const oracle_dims* dm, int K, int gate, int n_layers, const
   return ORACLE_OK;
 }
 
+// Stack with the token-choice bias dynamics of X-MoD notes Eq. 8 and the paragraph
+// after it: inside a sparse-dense block, every time token i is selected its bias
+// b_i grows, and it is cleared at the next dense anchor. The pages give neither the
+// increment nor tau; the reading taken here: the logit of sparse layer l is
+//   s_i = w_r . x_i + bias0_i - bias_step * c_i,
+// where c_i counts the earlier sparse layers of the current block (since the last
+// dense layer or the start of the stack) that selected token i, and bias_step stands
+// for tau times the increment. bias_step = 0 is the constant-bias stack.
+// Optional outputs, per sparse layer in stack order (n_sparse of them):
+//   idx_out [n_sparse, B, n]  its selection;
+//   s_out   [n_sparse, B, T]  its logits (with the bias above).
+int oracle_stack_dyn(const oracle_dims* dm, int K, int gate, int n_layers, const int* kinds,
+                     const oracle_layer_w* layers, double* x, const double* bias0,
+                     double bias_step, int mirror_bf16, int32_t* idx_out, double* s_out) {
+  const int64_t BT = (int64_t)dm->B * dm->T;
+  const int64_t N = BT * dm->d;
+  const int n = K > 0 ? dm->T / K : 0;
+  std::vector<double> y(N), bias(BT), s(BT);
+  std::vector<int32_t> count(BT, 0), idx((int64_t)dm->B * (n > 0 ? n : 1));
+  int ls = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    const bool sparse = kinds[l] == ORACLE_SPARSE;
+    if (sparse)
+      for (int64_t i = 0; i < BT; ++i)
+        bias[i] = (bias0 ? bias0[i] : 0.0) - bias_step * (double)count[i];
+    int st = oracle_layer_fwd(dm, kinds[l], K, gate, &layers[l], x, sparse ? bias.data() : nullptr,
+                              y.data(), sparse ? s.data() : nullptr, nullptr,
+                              sparse ? idx.data() : nullptr, nullptr, nullptr, nullptr);
+    if (st != ORACLE_OK) return st;
+    if (sparse) {
+      for (int b = 0; b < dm->B; ++b)
+        for (int j = 0; j < n; ++j) ++count[(int64_t)b * dm->T + idx[(int64_t)b * n + j]];
+      if (idx_out) std::memcpy(idx_out + (int64_t)ls * dm->B * n, idx.data(), sizeof(int32_t) * dm->B * n);
+      if (s_out) std::memcpy(s_out + (int64_t)ls * BT, s.data(), sizeof(double) * BT);
+      ++ls;
+    } else {
+      std::fill(count.begin(), count.end(), 0);   // the dense anchor clears the bias
+    }
+    if (mirror_bf16)
+      for (int64_t i = 0; i < N; ++i) y[i] = oracle_round_bf16(y[i]);
+    std::memcpy(x, y.data(), sizeof(double) * N);
+  }
+  return ORACLE_OK;
+}
+
 }  // extern "C"

@@ -53,7 +53,7 @@ constexpr int kRouterRows = 2 * kRouterRun;
 
 // Workspace carve-up. M rows of block scratch cover a dense layer (M = B*T).
 struct Layout {
-  size_t status, s, idx, r_sel, u, qkv, vt, o, h, hidden, wr, total;
+  size_t status, s, idx, r_sel, u, qkv, vt, o, h, hidden, wr, count, last, total;
 };
 
 Layout layout(const xmod_dims* dm, int K) {
@@ -78,6 +78,8 @@ Layout layout(const xmod_dims* dm, int K) {
   L.h = off;      off = align_up(off + 4 * M * dm->d);   // h = x_sel + a kept in fp32
   L.hidden = off; off = align_up(off + es * M * dm->d_ff);
   L.wr = off;     off = align_up(off + es * (size_t)kRouterRows * dm->d);   // stacked w_r
+  L.count = off;  off = align_up(off + 4 * BT);   // token-choice bias state of a block
+  L.last = off;   off = align_up(off + 4 * BT);
   L.total = off;
   return L;
 }
@@ -266,10 +268,20 @@ Epilogue router_epilogue(const xmod_dims* dm, int n_per_seq, const int32_t* idx,
 // its B*(T/K) updated rows get their logits for the later layers recomputed (from
 // the compact copy of the new rows that the down-projection epilogue writes).
 // A single sparse layer is a run of one; idx_out / r_sel_out (NULL: workspace) then
-// receive its selection.
+// receive its selection. track (NULL: none) carries the block's token-choice bias
+// state; its `layer` is the stack index of lw[0] among the sparse layers, and its
+// stats pointer addresses that layer's [B, 4] statistics.
+RouteTrack track_for(const RouteTrack* track, int j, int B) {
+  RouteTrack t = *track;
+  t.layer += j;
+  if (t.stats) t.stats += (int64_t)j * B * 4;
+  return t;
+}
+
 int sparse_run(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int K,
                xmod_gate gate, const xmod_layer_weights* lw, int count, void* x,
-               const float* bias, int32_t* idx_out = nullptr, float* r_sel_out = nullptr) {
+               const float* bias, int32_t* idx_out = nullptr, float* r_sel_out = nullptr,
+               const RouteTrack* track = nullptr) {
   const int B = dm->B, T = dm->T, d = dm->d, n = T / K;
   const int64_t BT = (int64_t)B * T;
   float* S = (float*)at(ws, L.s);
@@ -283,7 +295,8 @@ int sparse_run(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int
   XMOD_RUN("router", launch_gemm_tc(c, router_problem(dm, (int)BT, x, wr, kRouterRows, count),
                                     router_epilogue(dm, T, nullptr, S, bias)));
   for (int j = 0; j < count; ++j) {
-    XMOD_RUN("topk", launch_topk(c, B, T, n, S + j * BT, idx, r_sel));
+    const RouteTrack tj = track ? track_for(track, j, B) : RouteTrack{};
+    XMOD_RUN("topk", launch_topk(c, B, T, n, S + j * BT, idx, r_sel, track ? &tj : nullptr));
     const bool refresh = j + 1 < count;
     const int st = run_block(c, dm, L, ws, n, x, idx, &lw[j], nullptr, nullptr, true, x, r_sel,
                              (int)gate, refresh ? xs_new : nullptr);
@@ -308,19 +321,20 @@ bool sparse_run_supported(const xmod_dims* dm, void* ws, const Layout& L) {
 
 int layer_impl(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
                const xmod_layer_weights* w, void* x, const float* bias, int32_t* idx_out,
-               float* r_sel_out, void* ws, const Layout& L, cudaStream_t stream) {
+               float* r_sel_out, void* ws, const Layout& L, cudaStream_t stream,
+               const RouteTrack* track = nullptr) {
   Ctx c{stream, (int*)at(ws, L.status)};
   if (kind == XMOD_LAYER_DENSE)
     return run_block(c, dm, L, ws, dm->T, x, nullptr, w, nullptr, nullptr, true, x, nullptr, -1);
   if (sparse_run_supported(dm, ws, L))
-    return sparse_run(c, dm, L, ws, K, gate, w, 1, x, bias, idx_out, r_sel_out);
+    return sparse_run(c, dm, L, ws, K, gate, w, 1, x, bias, idx_out, r_sel_out, track);
   const int n = dm->T / K;
   float* s = (float*)at(ws, L.s);
   int32_t* idx = idx_out ? idx_out : (int32_t*)at(ws, L.idx);
   float* r_sel = r_sel_out ? r_sel_out : (float*)at(ws, L.r_sel);
   XMOD_RUN("router", launch_router(c, dm->dtype, (int64_t)dm->B * dm->T, dm->d, x, w->w_router, bias, s,
                          nullptr));
-  XMOD_RUN("topk", launch_topk(c, dm->B, dm->T, n, s, idx, r_sel));
+  XMOD_RUN("topk", launch_topk(c, dm->B, dm->T, n, s, idx, r_sel, track));
   return run_block(c, dm, L, ws, n, x, idx, w, nullptr, nullptr, true, x, r_sel, (int)gate);
 }
 
@@ -463,6 +477,14 @@ int xmod_layer_fwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate g
 int xmod_stack_fwd(const xmod_dims* dm, int K, double A, int N0, int N1, xmod_gate gate,
                    const xmod_layer_weights* layers, int n_layers, void* x_inout,
                    const float* bias, void* ws, size_t ws_bytes, void* stream) {
+  return xmod_stack_fwd_ex(dm, K, A, N0, N1, gate, layers, n_layers, x_inout, bias, nullptr, ws,
+                           ws_bytes, stream);
+}
+
+int xmod_stack_fwd_ex(const xmod_dims* dm, int K, double A, int N0, int N1, xmod_gate gate,
+                      const xmod_layer_weights* layers, int n_layers, void* x_inout,
+                      const float* bias, const xmod_stack_opts* opts, void* ws, size_t ws_bytes,
+                      void* stream) {
   if (!dims_ok(dm) || K <= 0 || K > dm->T || N0 < 0 || N1 < 0 || !layers) return XMOD_ERR_INVALID_ARG;
   if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
   if (!isfinite(A) || A <= 0) return XMOD_ERR_INVALID_ARG;
@@ -471,11 +493,13 @@ int xmod_stack_fwd(const xmod_dims* dm, int K, double A, int N0, int N1, xmod_ga
   if (AK < 1 || fabs(akd - (double)AK) > 1e-9) return XMOD_ERR_INVALID_ARG;
   if ((long)n_layers != (long)N0 + (long)N1 * (AK + 1)) return XMOD_ERR_INVALID_ARG;
   if (!aligned16(x_inout) || !aligned16_or_null(bias)) return XMOD_ERR_INVALID_ARG;
+  if (opts && (!isfinite(opts->bias_step) || opts->bias_step < 0.0f)) return XMOD_ERR_INVALID_ARG;
+  if (opts && (((uintptr_t)opts->layer_stats & 3) || ((uintptr_t)opts->update_hist & 3)))
+    return XMOD_ERR_INVALID_ARG;
   // Eq. 3 order: N0 dense, then N1 blocks of AK sparse layers and one dense anchor.
-  for (int l = 0; l < n_layers; ++l) {
-    const bool sparse = l >= N0 && ((l - N0) % (AK + 1)) < AK;
-    if (!weights_ok(&layers[l], sparse)) return XMOD_ERR_INVALID_ARG;
-  }
+  auto is_sparse = [&](int l) { return l >= N0 && ((l - N0) % (AK + 1)) < AK; };
+  for (int l = 0; l < n_layers; ++l)
+    if (!weights_ok(&layers[l], is_sparse(l))) return XMOD_ERR_INVALID_ARG;
   if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
   if (N1 > 0 && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
   int st = check_ws(dm, K, ws, ws_bytes);
@@ -483,20 +507,50 @@ int xmod_stack_fwd(const xmod_dims* dm, int K, double A, int N0, int N1, xmod_ga
   const Layout L = layout(dm, K);
   const bool runs = sparse_run_supported(dm, ws, L);
   Ctx c{(cudaStream_t)stream, (int*)at(ws, L.status)};
+  const int64_t BT = (int64_t)dm->B * dm->T;
+  // Token-choice bias state, only when an option needs it (else the plain top-k).
+  const bool tracked = opts && (opts->bias_step != 0.0f || opts->layer_stats || opts->update_hist);
+  RouteTrack track;
+  if (tracked) {
+    track.count = (int32_t*)at(ws, L.count);
+    track.last = (int32_t*)at(ws, L.last);
+    track.bias_step = opts->bias_step;
+    track.stats = opts->layer_stats;
+  }
+  int sparse_index = 0;
   for (int l = 0; l < n_layers;) {
-    const bool sparse = l >= N0 && ((l - N0) % (AK + 1)) < AK;
-    if (sparse && runs) {
+    if (is_sparse(l)) {
+      const int in_block = (l - N0) % (AK + 1);   // position inside its sparse-dense block
+      if (tracked && in_block == 0) {   // a new block: clear the bias state
+        if (cudaMemsetAsync(track.count, 0, 4 * BT, c.stream) != cudaSuccess) return XMOD_ERR_CUDA;
+        if (cudaMemsetAsync(track.last, 0x80, 4 * BT, c.stream) != cudaSuccess) return XMOD_ERR_CUDA;
+      }
       // the sparse layers up to the next dense one, at most kRouterRun at a time
       int count = 1;
-      while (count < kRouterRun && l + count < n_layers && ((l + count - N0) % (AK + 1)) < AK)
-        ++count;
-      st = sparse_run(c, dm, L, ws, K, gate, &layers[l], count, x_inout, bias);
+      if (runs)
+        while (count < kRouterRun && l + count < n_layers && is_sparse(l + count)) ++count;
+      RouteTrack tl = track;
+      tl.layer = sparse_index;
+      if (tl.stats) tl.stats += (int64_t)sparse_index * dm->B * 4;
+      if (runs)
+        st = sparse_run(c, dm, L, ws, K, gate, &layers[l], count, x_inout, bias, nullptr, nullptr,
+                        tracked ? &tl : nullptr);
+      else
+        st = layer_impl(dm, XMOD_LAYER_SPARSE, K, gate, &layers[l], x_inout, bias, nullptr,
+                        nullptr, ws, L, (cudaStream_t)stream, tracked ? &tl : nullptr);
       if (st) return st;
       l += count;
+      sparse_index += count;
+      if (tracked && opts->update_hist && in_block + count == AK) {   // the block's last sparse layer
+        const int block = (l - 1 - N0) / (AK + 1);
+        XMOD_RUN("update_hist",
+                 launch_count_hist(c, dm->B, dm->T, (int)AK, track.count,
+                                   opts->update_hist + (int64_t)block * dm->B * (AK + 1)));
+      }
       continue;
     }
-    st = layer_impl(dm, sparse ? XMOD_LAYER_SPARSE : XMOD_LAYER_DENSE, K, gate, &layers[l],
-                    x_inout, bias, nullptr, nullptr, ws, L, (cudaStream_t)stream);
+    st = layer_impl(dm, XMOD_LAYER_DENSE, K, gate, &layers[l], x_inout, bias, nullptr, nullptr, ws,
+                    L, (cudaStream_t)stream);
     if (st) return st;
     ++l;
   }

@@ -70,10 +70,29 @@ cudaError_t launch_router(const Ctx& c, xmod_dtype dt, int64_t rows, int d, cons
 
 // Largest topk supported T (keys held in shared memory).
 int topk_max_T();
+
+// Token-choice bias state of a sparse-dense block (all pointers may be NULL).
+//   count [B, T]  times each token was selected by the block's earlier sparse layers;
+//                 the layer ranks s - bias_step * count, and its selection adds 1;
+//   last  [B, T]  index of the last sparse layer that selected the token;
+//   stats [B, 4]  this layer's selected count, tokens with a ranked logit >= 0,
+//                 tokens where the two rules agree, and selected tokens the previous
+//                 sparse layer (index layer - 1) also selected.
+struct RouteTrack {
+  int32_t* count = nullptr;
+  int32_t* last = nullptr;
+  float bias_step = 0.0f;
+  int layer = 0;
+  int32_t* stats = nullptr;
+};
+
 // Per-sequence top-n of s [B, T]; ties to the lower position; ascending idx [B, n].
-// r_sel [B, n] = sigmoid(s at idx) if not NULL.
+// r_sel [B, n] = sigmoid(ranked logit at idx) if not NULL.
 cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32_t* idx,
-                        float* r_sel);
+                        float* r_sel, const RouteTrack* tr = nullptr);
+// update_hist [B, max_count + 1]: histogram of count [B, T] per sequence.
+cudaError_t launch_count_hist(const Ctx& c, int B, int T, int max_count, const int32_t* count,
+                              int32_t* update_hist);
 
 // xs[b*n + j] = x[b, idx[b, j]] (idx NULL: identity, n == T).
 cudaError_t launch_gather(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,

@@ -247,7 +247,7 @@ __device__ __forceinline__ uint32_t warps_exclusive_scan(uint32_t v, uint32_t* s
 
 __global__ void __launch_bounds__(TOPK_THREADS)
 topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx,
-            float* __restrict__ r_sel, int* status) {
+            float* __restrict__ r_sel, int* status, RouteTrack tr) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ uint32_t keys[];
@@ -255,13 +255,19 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
   __shared__ uint32_t scan_sh[32];
   __shared__ uint32_t sh_prefix, sh_remaining;
   __shared__ int sh_bad;
+  __shared__ uint32_t sh_stat[3];   // threshold-selected, agreeing, also selected before
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* sb = s + (int64_t)b * T;
+  int32_t* cnt = tr.count ? tr.count + (int64_t)b * T : nullptr;
+  int32_t* last = tr.last ? tr.last + (int64_t)b * T : nullptr;
+  // the logit this layer ranks: s minus the block's accumulated token-choice bias
+  auto logit = [&](int t) { return cnt ? sb[t] - tr.bias_step * (float)cnt[t] : sb[t]; };
   if (threadIdx.x == 0) sh_bad = 0;
+  if (threadIdx.x < 3) sh_stat[threadIdx.x] = 0u;
   __syncthreads();
   for (int t = threadIdx.x; t < T; t += TOPK_THREADS) {
-    const float v = sb[t];
+    const float v = logit(t);
     if (!isfinite(v)) sh_bad = 1;
     keys[t] = order_key(v);
   }
@@ -338,6 +344,7 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
   }
   uint32_t out = warps_exclusive_scan(my_sel, scan_sh);
   eq_run = eq_before;
+  uint32_t n_thr = 0, n_agree = 0, n_again = 0;
   for (int base = lo; base < hi; base += 32) {
     const int t = base + lane;
     const uint32_t k = t < hi ? keys[t] : 0u;
@@ -349,22 +356,82 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
       const uint32_t o = out + __popc(selm & lt_mask);
       if (o < (uint32_t)n) {
         idx[(int64_t)b * n + o] = t;
-        if (r_sel) r_sel[(int64_t)b * n + o] = sigmoidf_acc(sb[t]);
+        if (r_sel) r_sel[(int64_t)b * n + o] = sigmoidf_acc(logit(t));
       }
+    }
+    if (tr.stats) {
+      const bool thr = t < hi && k >= 0x80000000u;   // logit >= 0, i.e. r >= 1/2
+      n_thr += __popc(__ballot_sync(0xffffffffu, thr));
+      n_agree += __popc(__ballot_sync(0xffffffffu, t < hi && thr == sel));
+      n_again += __popc(__ballot_sync(0xffffffffu, sel && last && last[t] == tr.layer - 1));
     }
     out += __popc(selm);
     eq_run += __popc(eqm);
   }
+  if (tr.stats) {
+    if (lane == 0) {
+      atomicAdd(&sh_stat[0], n_thr);
+      atomicAdd(&sh_stat[1], n_agree);
+      atomicAdd(&sh_stat[2], n_again);
+    }
+  }
+  if (cnt || last) {
+    // record this layer's selection for the block's later layers (after every read of
+    // cnt and last above: the logits and the overlap with the previous layer)
+    __syncthreads();
+    for (int j = threadIdx.x; j < n; j += TOPK_THREADS) {
+      const int t = idx[(int64_t)b * n + j];
+      if (cnt) cnt[t] += 1;
+      if (last) last[t] = tr.layer;
+    }
+  }
+  if (tr.stats) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int32_t* st = tr.stats + (int64_t)b * 4;
+      st[0] = n;
+      st[1] = (int32_t)sh_stat[0];
+      st[2] = (int32_t)sh_stat[1];
+      st[3] = (int32_t)sh_stat[2];
+    }
+  }
 }
 
 cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32_t* idx,
-                        float* r_sel) {
+                        float* r_sel, const RouteTrack* tr) {
   if (B <= 0) return cudaSuccess;
   const size_t smem = sizeof(uint32_t) * (size_t)T;
   cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)(sizeof(uint32_t) * TOPK_MAX_T));
-  launch_pdl(topk_kernel, dim3(B), dim3(TOPK_THREADS), smem, c.stream, T, n, s, idx, r_sel, c.status);
+  const RouteTrack none{};
+  launch_pdl(topk_kernel, dim3(B), dim3(TOPK_THREADS), smem, c.stream, T, n, s, idx, r_sel,
+             c.status, tr ? *tr : none);
   return cudaGetLastError();
+}
+
+// update_hist[b, c] = number of tokens of sequence b whose count is c (0 <= c <= max_count).
+__global__ void count_hist_kernel(int T, int max_count, const int32_t* __restrict__ count,
+                                  int32_t* __restrict__ update_hist) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ uint32_t h[];
+  const int b = blockIdx.x;
+  for (int i = threadIdx.x; i <= max_count; i += blockDim.x) h[i] = 0u;
+  __syncthreads();
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    const int c = count[(int64_t)b * T + t];
+    atomicAdd(&h[c < 0 ? 0 : (c > max_count ? max_count : c)], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i <= max_count; i += blockDim.x)
+    update_hist[(int64_t)b * (max_count + 1) + i] = (int32_t)h[i];
+}
+
+cudaError_t launch_count_hist(const Ctx& c, int B, int T, int max_count, const int32_t* count,
+                              int32_t* update_hist) {
+  if (B <= 0) return cudaSuccess;
+  return launch_pdl(count_hist_kernel, dim3(B), dim3(512), sizeof(uint32_t) * (size_t)(max_count + 1),
+                    c.stream, T, max_count, count, update_hist);
 }
 
 // ================================================================ gather (+ RMSNorm)
