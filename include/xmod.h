@@ -162,6 +162,25 @@ XMOD_API int xmod_stack_fwd(const xmod_dims* dims, int K, double A, int N0, int 
                    const xmod_layer_weights* layers, int n_layers, void* x_inout,
                    const float* bias, void* ws, size_t ws_bytes, void* stream);
 
+/* Token selection rule of a sparse layer. TOPK: the top-(T/K) of each sequence
+ * (training rule). THRESHOLD: the causal rule of X-MoD notes "top-k in training,
+ * causal threshold at evaluation" -- every token whose routing probability
+ * r = sigmoid(s) is at least 1/2 (s >= 0; -0 counts as 0) enters the layer, each token
+ * deciding alone, so a sequence takes a variable number of tokens (possibly none);
+ * the selected tokens attend causally among themselves in position order and get the
+ * gated residual with their own r. THRESHOLD needs bf16 and head_dim 128 (the
+ * tensor-core path; otherwise XMOD_ERR_UNSUPPORTED). */
+typedef enum { XMOD_ROUTE_TOPK = 0, XMOD_ROUTE_THRESHOLD = 1 } xmod_routing;
+
+/* One sparse layer under the causal threshold rule (see xmod_routing), in place on
+ * x [B, T, d] (bf16). bias: [B, T] fp32 or NULL, added to the logit. count_out: NULL
+ * or device int32 [B], the number of tokens each sequence routed through the layer.
+ * Workspace: xmod_workspace_bytes(dims, any K). */
+XMOD_API int xmod_layer_fwd_threshold(const xmod_dims* dims, xmod_gate gate,
+                                      const xmod_layer_weights* w, void* x_inout,
+                                      const float* bias, int32_t* count_out, void* ws,
+                                      size_t ws_bytes, void* stream);
+
 /* Options of xmod_stack_fwd_ex.
  *
  * bias_step: the token-choice bias dynamics of X-MoD notes Eq. 8 and the paragraph
@@ -179,11 +198,15 @@ XMOD_API int xmod_stack_fwd(const xmod_dims* dims, int K, double A, int N0, int 
  * update_hist: NULL or device int32 [N1, B, AK + 1]: for each sparse-dense block and
  *   sequence, how many tokens the block's AK sparse layers updated 0, 1, ..., AK times.
  * These are the inputs of the routing diagnostics of X-MoD notes Table 10 (coverage,
- * adjacent-layer Jaccard overlap, threshold / top-k mask agreement, update counts). */
+ * adjacent-layer Jaccard overlap, threshold / top-k mask agreement, update counts).
+ * Under THRESHOLD routing the selected count is the threshold count and every
+ * decision agrees; update_hist then needs no K (the selections vary).
+ * routing: xmod_routing of every sparse layer (K still fixes the Eq. 3 schedule). */
 typedef struct {
   float bias_step;
   int32_t* layer_stats;
   int32_t* update_hist;
+  int routing;
 } xmod_stack_opts;
 
 /* xmod_stack_fwd with options (opts NULL: exactly xmod_stack_fwd). The workspace

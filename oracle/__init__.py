@@ -65,7 +65,9 @@ def lib():
         L.oracle_stack_dyn.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                        ctypes.POINTER(LayerW), _DP, _DP, ctypes.c_double,
-                                       ctypes.c_int, _IP, _DP]
+                                       ctypes.c_int, _IP, _DP, ctypes.c_int, _IP]
+        L.oracle_layer_threshold.argtypes = [ctypes.POINTER(Dims), ctypes.c_int,
+                                             ctypes.POINTER(LayerW), _DP, _DP, _DP, _DP, _IP]
         _lib = L
     return _lib
 
@@ -224,26 +226,47 @@ def layer_fwd(dm: Dims, kind, K, gate, layer: Layer, x, bias=None, idx_force=Non
     return out
 
 
+TOPK, THRESHOLD = 0, 1
+
+
 def stack_dyn(dm: Dims, K, gate, kinds, layers, x, bias=None, bias_step=0.0,
-              mirror_bf16=False):
+              mirror_bf16=False, routing=TOPK):
     """Whole stack with the token-choice bias dynamics (X-MoD notes, Eq. 8 and the
     paragraph after it): a sparse layer's logit is w_r.x + bias - bias_step * (times
-    the token was selected since the last dense layer). Returns (x, idx, s): the final
-    stream and, per sparse layer in order, its selection [B, n] and logits [B, T]."""
+    the token was selected since the last dense layer). routing TOPK selects T/K per
+    sequence, THRESHOLD every token with logit >= 0 (X-MoD notes, causal threshold
+    rule at evaluation). Returns (x, idx, s, mask): the final stream and, per sparse
+    layer in order, its selection [B, n] (top-k only, else None), logits [B, T] and
+    decisions [B, T] (bool)."""
     x = np.array(x, dtype=np.float64, copy=True, order="C")
     bias_a, bp = _d(bias)
     n_sparse = sum(1 for k in kinds if k == SPARSE)
-    n = dm.T // K
+    n = dm.T // K if routing == TOPK else 1
     idx = np.zeros((max(n_sparse, 1), dm.B, n), np.int32)
     s = np.zeros((max(n_sparse, 1), dm.B, dm.T), np.float64)
+    mask = np.zeros((max(n_sparse, 1), dm.B, dm.T), np.int32)
     kinds_a = (ctypes.c_int * len(kinds))(*kinds)
     arr = (LayerW * len(layers))(*[l.struct for l in layers])
     _check(lib().oracle_stack_dyn(ctypes.byref(dm), K, gate, len(kinds), kinds_a, arr,
                                   x.ctypes.data_as(_DP), bp, ctypes.c_double(bias_step),
                                   int(bool(mirror_bf16)),
-                                  idx.ctypes.data_as(_IP),
-                                  s.ctypes.data_as(_DP)))
-    return x, idx[:n_sparse], s[:n_sparse]
+                                  idx.ctypes.data_as(_IP) if routing == TOPK else None,
+                                  s.ctypes.data_as(_DP), int(routing), mask.ctypes.data_as(_IP)))
+    return (x, idx[:n_sparse] if routing == TOPK else None, s[:n_sparse],
+            mask[:n_sparse].astype(bool))
+
+
+def layer_threshold(dm: Dims, gate, layer, x, bias=None):
+    """One sparse layer under the causal threshold rule; returns (y, s, mask)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    s = np.empty((dm.B, dm.T), np.float64)
+    mask = np.empty((dm.B, dm.T), np.int32)
+    bias_a, bp = _d(bias)
+    _check(lib().oracle_layer_threshold(ctypes.byref(dm), gate, ctypes.byref(layer.struct),
+                                        x.ctypes.data_as(_DP), bp, y.ctypes.data_as(_DP),
+                                        s.ctypes.data_as(_DP), mask.ctypes.data_as(_IP)))
+    return y, s, mask.astype(bool)
 
 
 def stack_fwd(dm: Dims, K, gate, kinds, layers, x, bias=None, mirror_bf16=False,

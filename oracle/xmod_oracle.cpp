@@ -387,6 +387,53 @@ int oracle_stack_fwd(const oracle_dims* dm, int K, int gate, int n_layers, const
   return ORACLE_OK;
 }
 
+// Sparse layer under the causal threshold rule of X-MoD notes "top-k in training,
+// causal threshold at evaluation": token i enters the block when its routing
+// probability r_i = sigmoid(s_i) is at least 1/2, i.e. s_i >= 0 (-0 counts as 0),
+// each token deciding alone, so a sequence takes a variable number of tokens (none
+// at all is allowed: then the sequence is unchanged). The selected tokens go through
+// the block in position order, attention causal among them, and the gated residual
+// (Eq. 7 / Eq. 6) with their own r. mask_out [B, T] (nullable) receives the decisions.
+int oracle_layer_threshold(const oracle_dims* dm, int gate, const oracle_layer_w* w,
+                           const double* x_in, const double* bias, double* y, double* s_out,
+                           int32_t* mask_out) {
+  const int B = dm->B, T = dm->T, d = dm->d;
+  if (B <= 0 || T <= 0 || d <= 0 || dm->hq % dm->hkv != 0) return ORACLE_BAD_ARG;
+  const int64_t BT = (int64_t)B * T;
+  std::memcpy(y, x_in, sizeof(double) * BT * d);
+  std::vector<double> s(BT), r(BT);
+  oracle_router(BT, d, x_in, w->w_r, bias, s.data(), r.data());
+  for (int64_t i = 0; i < BT; ++i)
+    if (!std::isfinite(s[i])) return ORACLE_NONFINITE;
+  if (s_out) std::memcpy(s_out, s.data(), sizeof(double) * BT);
+  for (int b = 0; b < B; ++b) {
+    std::vector<int32_t> pos;   // ascending positions
+    for (int t = 0; t < T; ++t) {
+      const bool take = s[(int64_t)b * T + t] >= 0.0;
+      if (mask_out) mask_out[(int64_t)b * T + t] = take ? 1 : 0;
+      if (take) pos.push_back(t);
+    }
+    const int n = (int)pos.size();
+    if (n == 0) continue;
+    std::vector<double> xs((int64_t)n * d);
+    for (int j = 0; j < n; ++j)
+      std::memcpy(&xs[(int64_t)j * d], x_in + ((int64_t)b * T + pos[j]) * d, sizeof(double) * d);
+    std::vector<int32_t> rows(n);
+    std::iota(rows.begin(), rows.end(), 0);
+    std::vector<double> a((size_t)n * d), f((size_t)n * d);
+    oracle_block_rows(dm, n, xs.data(), w, rows.data(), n, a.data(), f.data());
+    for (int j = 0; j < n; ++j) {
+      const int t = pos[j];
+      const double rt = r[(int64_t)b * T + t];
+      for (int c = 0; c < d; ++c) {
+        const int64_t o = ((int64_t)b * T + t) * d + c;
+        y[o] = gated(x_in[o], a[(size_t)j * d + c], f[(size_t)j * d + c], rt, w->varsigma, gate);
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
 // Stack with the token-choice bias dynamics of X-MoD notes Eq. 8 and the paragraph
 // after it: inside a sparse-dense block, every time token i is selected its bias
 // b_i grows, and it is cleared at the next dense anchor. The pages give neither the
@@ -398,27 +445,43 @@ int oracle_stack_fwd(const oracle_dims* dm, int K, int gate, int n_layers, const
 // Optional outputs, per sparse layer in stack order (n_sparse of them):
 //   idx_out [n_sparse, B, n]  its selection;
 //   s_out   [n_sparse, B, T]  its logits (with the bias above).
+// routing 0: top-(T/K) per sequence; 1: the causal threshold rule above (then K is
+// unused by the sparse layers and idx_out must be NULL).
+// mask_out [n_sparse, B, T] (nullable): each sparse layer's decisions.
 int oracle_stack_dyn(const oracle_dims* dm, int K, int gate, int n_layers, const int* kinds,
                      const oracle_layer_w* layers, double* x, const double* bias0,
-                     double bias_step, int mirror_bf16, int32_t* idx_out, double* s_out) {
+                     double bias_step, int mirror_bf16, int32_t* idx_out, double* s_out,
+                     int routing, int32_t* mask_out) {
+  if (routing != 0 && (routing != 1 || idx_out)) return ORACLE_BAD_ARG;
   const int64_t BT = (int64_t)dm->B * dm->T;
   const int64_t N = BT * dm->d;
   const int n = K > 0 ? dm->T / K : 0;
   std::vector<double> y(N), bias(BT), s(BT);
-  std::vector<int32_t> count(BT, 0), idx((int64_t)dm->B * (n > 0 ? n : 1));
+  std::vector<int32_t> count(BT, 0), idx((int64_t)dm->B * (n > 0 ? n : 1)), mask(BT);
   int ls = 0;
   for (int l = 0; l < n_layers; ++l) {
     const bool sparse = kinds[l] == ORACLE_SPARSE;
     if (sparse)
       for (int64_t i = 0; i < BT; ++i)
         bias[i] = (bias0 ? bias0[i] : 0.0) - bias_step * (double)count[i];
-    int st = oracle_layer_fwd(dm, kinds[l], K, gate, &layers[l], x, sparse ? bias.data() : nullptr,
-                              y.data(), sparse ? s.data() : nullptr, nullptr,
-                              sparse ? idx.data() : nullptr, nullptr, nullptr, nullptr);
+    int st;
+    if (sparse && routing == 1) {
+      st = oracle_layer_threshold(dm, gate, &layers[l], x, bias.data(), y.data(), s.data(),
+                                  mask.data());
+    } else {
+      st = oracle_layer_fwd(dm, kinds[l], K, gate, &layers[l], x, sparse ? bias.data() : nullptr,
+                            y.data(), sparse ? s.data() : nullptr, nullptr,
+                            sparse ? idx.data() : nullptr, nullptr, nullptr, nullptr);
+      if (sparse) {
+        std::fill(mask.begin(), mask.end(), 0);
+        for (int b = 0; b < dm->B; ++b)
+          for (int j = 0; j < n; ++j) mask[(int64_t)b * dm->T + idx[(int64_t)b * n + j]] = 1;
+      }
+    }
     if (st != ORACLE_OK) return st;
     if (sparse) {
-      for (int b = 0; b < dm->B; ++b)
-        for (int j = 0; j < n; ++j) ++count[(int64_t)b * dm->T + idx[(int64_t)b * n + j]];
+      for (int64_t i = 0; i < BT; ++i) count[i] += mask[i];
+      if (mask_out) std::memcpy(mask_out + (int64_t)ls * BT, mask.data(), sizeof(int32_t) * BT);
       if (idx_out) std::memcpy(idx_out + (int64_t)ls * dm->B * n, idx.data(), sizeof(int32_t) * dm->B * n);
       if (s_out) std::memcpy(s_out + (int64_t)ls * BT, s.data(), sizeof(double) * BT);
       ++ls;

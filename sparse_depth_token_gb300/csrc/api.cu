@@ -53,7 +53,7 @@ constexpr int kRouterRows = 2 * kRouterRun;
 
 // Workspace carve-up. M rows of block scratch cover a dense layer (M = B*T).
 struct Layout {
-  size_t status, s, idx, r_sel, u, qkv, vt, o, h, hidden, wr, count, last, total;
+  size_t status, s, idx, r_sel, u, qkv, vt, o, h, hidden, wr, count, last, seq, total;
 };
 
 Layout layout(const xmod_dims* dm, int K) {
@@ -80,6 +80,7 @@ Layout layout(const xmod_dims* dm, int K) {
   L.wr = off;     off = align_up(off + es * (size_t)kRouterRows * dm->d);   // stacked w_r
   L.count = off;  off = align_up(off + 4 * BT);   // token-choice bias state of a block
   L.last = off;   off = align_up(off + 4 * BT);
+  L.seq = off;    off = align_up(off + 4 * (2 * (size_t)dm->B + 1));   // threshold rows
   L.total = off;
   return L;
 }
@@ -112,15 +113,27 @@ bool weights_ok(const xmod_layer_weights* w, bool need_router) {
 // The block on B*n compact rows (rows of x selected by idx, or identity when
 // idx == NULL and n == T). Writes a to a_out when given, and either
 // scatters the gated residual into x (scatter == true) or stores f to f_out.
+// Rows of a threshold-routed layer: a variable count per sequence, known only on the
+// device. tok [B*T]: compact row -> stream row; seq_count / seq_off [B]; M [1].
+struct Ragged {
+  const int32_t* tok = nullptr;
+  const int32_t* seq_count = nullptr;
+  const int32_t* seq_off = nullptr;
+  const int32_t* M = nullptr;
+};
+
 // With scatter, xs_new (if not NULL) receives the updated compact rows [B*n, d].
+// With rg (threshold routing), n is T: buffers are sized for every token, kernels
+// compute the rows the routing picked (tensor-core path only).
 int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int n,
               const void* x_src, const int32_t* idx, const xmod_layer_weights* w, void* a_out,
               void* f_out, bool scatter, void* x_inout, const float* r_sel, int gate,
-              void* xs_new = nullptr) {
+              void* xs_new = nullptr, const Ragged* rg = nullptr) {
   const xmod_dtype dt = dm->dtype;
   const int B = dm->B, T = dm->T, d = dm->d, hq = dm->n_heads, hkv = dm->n_kv_heads,
             hd = dm->head_dim, F = dm->d_ff;
   const int M = B * n;
+  const int32_t* M_dev = rg ? rg->M : nullptr;
   const int qw = hq * hd, kw = hkv * hd, qkv_w = qw + 2 * kw;
   const size_t es = esize(dt);
   char* u = at(ws, L.u);
@@ -129,7 +142,13 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   char* h = at(ws, L.h);
   char* hidden = at(ws, L.hidden);
   // 1. gather + RMSNorm1
-  XMOD_RUN("gather_rmsnorm", launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms1, dm->rms_eps, u));
+  RowMap rm;
+  if (rg) {
+    rm.tok = rg->tok;
+    rm.M_dev = M_dev;
+  }
+  XMOD_RUN("gather_rmsnorm",
+           launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms1, dm->rms_eps, u, rm));
   // 2. q, k, v projections into one [M, qkv_w] buffer
   const bool tc = dt == XMOD_BF16;
   char* vt = at(ws, L.vt);
@@ -151,6 +170,17 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   pq.B[0] = w->wq; pq.B[1] = w->wk; pq.B[2] = w->wv; pq.nB = 3;
   pq.split[0] = qw; pq.split[1] = qw + kw;
   const bool tc_qkv = tc && gemm_tc_supported(pq, e);
+  if (rg) {
+    if (!tc_qkv || !tc_attn) return XMOD_ERR_UNSUPPORTED;
+    e.tok = rg->tok;
+    e.seq_off = rg->seq_off;
+    e.T = T;
+    pq.M_dev = M_dev;
+    // keys past a sequence's count are read (and multiplied by zero weights): keep
+    // them finite
+    if (cudaMemsetAsync(vt, 0, es * (size_t)B * hkv * hd * vt_ld(n), c.stream) != cudaSuccess)
+      return XMOD_ERR_CUDA;
+  }
   if (tc_qkv) {
     XMOD_RUN("gemm_qkv", launch_gemm_tc(c, pq, e));
   } else {
@@ -163,7 +193,9 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   }
   // 3. causal GQA attention among the n rows of each sequence
   if (tc_qkv && tc_attn)
-    XMOD_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, vt_ld(n), o));
+    XMOD_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, vt_ld(n), o,
+                                              rg ? rg->seq_count : nullptr,
+                                              rg ? rg->seq_off : nullptr));
   else
     XMOD_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w,
                                                 qkv + es * qw, qkv + es * (qw + kw), qkv_w, o));
@@ -181,6 +213,11 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   eo.d = d;
   GemmTcProblem po;
   po.M = M; po.N = d; po.K = qw; po.A = o; po.lda = qw; po.ldb = qw; po.B[0] = w->wo;
+  if (rg) {
+    eo.tok = rg->tok;
+    po.M_dev = M_dev;
+    if (!gemm_tc_supported(po, eo)) return XMOD_ERR_UNSUPPORTED;
+  }
   if (tc && gemm_tc_supported(po, eo))
     XMOD_RUN("gemm_o_residual", launch_gemm_tc(c, po, eo));
   else
@@ -189,7 +226,7 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   // (v2 reuses the buffer of u, which the q/k/v projection has consumed)
   char* v2 = u;
   XMOD_RUN("rmsnorm2", launch_rmsnorm_f32in(c, dt, M, d, (const float*)h, w->rms2, dm->rms_eps,
-                                            v2));
+                                            v2, M_dev));
   // 6. hidden = silu(v2 Wg^T) * (v2 Wu^T)
   Epilogue eg;
   eg.kind = EPI_SWIGLU;
@@ -198,6 +235,8 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   GemmTcProblem pg;
   pg.M = M; pg.N = F; pg.K = d; pg.A = v2; pg.lda = d; pg.ldb = d;
   pg.B[0] = w->w_gate; pg.B[1] = w->w_up; pg.nB = 2;
+  pg.M_dev = M_dev;
+  if (rg && !gemm_tc_supported(pg, eg)) return XMOD_ERR_UNSUPPORTED;
   if (tc && gemm_tc_supported(pg, eg))
     XMOD_RUN("gemm_gate_up_swiglu", launch_gemm_tc(c, pg, eg));
   else
@@ -225,6 +264,11 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   }
   GemmTcProblem pd;
   pd.M = M; pd.N = d; pd.K = F; pd.A = hidden; pd.lda = F; pd.ldb = F; pd.B[0] = w->w_down;
+  if (rg) {
+    ed.tok = rg->tok;
+    pd.M_dev = M_dev;
+    if (!gemm_tc_supported(pd, ed)) return XMOD_ERR_UNSUPPORTED;
+  }
   const char* down_name = scatter ? "gemm_down_scatter" : "gemm_down";
   if (tc && gemm_tc_supported(pd, ed))
     XMOD_RUN(down_name, launch_gemm_tc(c, pd, ed));
@@ -278,15 +322,23 @@ RouteTrack track_for(const RouteTrack* track, int j, int B) {
   return t;
 }
 
+// threshold: the causal threshold rule instead of top-(T/K) (K unused); the layers
+// then take a variable number of tokens per sequence (device-side row counts).
 int sparse_run(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int K,
                xmod_gate gate, const xmod_layer_weights* lw, int count, void* x,
                const float* bias, int32_t* idx_out = nullptr, float* r_sel_out = nullptr,
-               const RouteTrack* track = nullptr) {
-  const int B = dm->B, T = dm->T, d = dm->d, n = T / K;
+               const RouteTrack* track = nullptr, bool threshold = false) {
+  const int B = dm->B, T = dm->T, d = dm->d, n = threshold ? T : T / K;
   const int64_t BT = (int64_t)B * T;
   float* S = (float*)at(ws, L.s);
   int32_t* idx = idx_out ? idx_out : (int32_t*)at(ws, L.idx);
   float* r_sel = r_sel_out ? r_sel_out : (float*)at(ws, L.r_sel);
+  int32_t* seq = (int32_t*)at(ws, L.seq);   // seq_count [B], seq_off [B], M
+  Ragged rg;
+  rg.tok = idx;
+  rg.seq_count = seq;
+  rg.seq_off = seq + B;
+  rg.M = seq + 2 * B;
   char* wr = at(ws, L.wr);
   void* xs_new = at(ws, L.u);   // free once the gate/up GEMM has read v2
   RowPtrs rows{};
@@ -296,16 +348,26 @@ int sparse_run(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int
                                     router_epilogue(dm, T, nullptr, S, bias)));
   for (int j = 0; j < count; ++j) {
     const RouteTrack tj = track ? track_for(track, j, B) : RouteTrack{};
-    XMOD_RUN("topk", launch_topk(c, B, T, n, S + j * BT, idx, r_sel, track ? &tj : nullptr));
+    if (threshold)
+      XMOD_RUN("threshold", launch_threshold_select(c, B, T, S + j * BT, idx, r_sel, seq, seq + B,
+                                                    seq + 2 * B, track ? &tj : nullptr));
+    else
+      XMOD_RUN("topk", launch_topk(c, B, T, n, S + j * BT, idx, r_sel, track ? &tj : nullptr));
     const bool refresh = j + 1 < count;
-    const int st = run_block(c, dm, L, ws, n, x, idx, &lw[j], nullptr, nullptr, true, x, r_sel,
-                             (int)gate, refresh ? xs_new : nullptr);
+    const int st = run_block(c, dm, L, ws, n, x, threshold ? nullptr : idx, &lw[j], nullptr,
+                             nullptr, true, x, r_sel, (int)gate, refresh ? xs_new : nullptr,
+                             threshold ? &rg : nullptr);
     if (st) return st;
-    if (refresh)
-      XMOD_RUN("router_refresh",
-               launch_gemm_tc(c, router_problem(dm, B * n, xs_new, wr + (size_t)(j + 1) * d * 2,
-                                                kRouterRows - (j + 1), count - 1 - j),
-                              router_epilogue(dm, n, idx, S + (j + 1) * BT, bias)));
+    if (refresh) {
+      GemmTcProblem p = router_problem(dm, B * n, xs_new, wr + (size_t)(j + 1) * d * 2,
+                                       kRouterRows - (j + 1), count - 1 - j);
+      Epilogue e = router_epilogue(dm, n, threshold ? nullptr : idx, S + (j + 1) * BT, bias);
+      if (threshold) {
+        p.M_dev = rg.M;
+        e.tok = rg.tok;
+      }
+      XMOD_RUN("router_refresh", launch_gemm_tc(c, p, e));
+    }
   }
   return XMOD_OK;
 }
@@ -317,6 +379,13 @@ bool sparse_run_supported(const xmod_dims* dm, void* ws, const Layout& L) {
   const GemmTcProblem p = router_problem(dm, dm->B * dm->T, at(ws, L.u), at(ws, L.wr),
                                          kRouterRows, kRouterRun);
   return gemm_tc_supported(p, router_epilogue(dm, dm->T, nullptr, (float*)at(ws, L.s), nullptr));
+}
+
+// Whether the threshold rule can run: the variable-length block needs the tensor-core
+// GEMMs and attention.
+bool threshold_supported(const xmod_dims* dm, void* ws, const Layout& L) {
+  const int qkv_w = (dm->n_heads + 2 * dm->n_kv_heads) * dm->head_dim;
+  return sparse_run_supported(dm, ws, L) && attention_tc_supported(dm->head_dim, dm->T, qkv_w);
 }
 
 int layer_impl(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
@@ -474,6 +543,27 @@ int xmod_layer_fwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate g
                     (cudaStream_t)stream);
 }
 
+int xmod_layer_fwd_threshold(const xmod_dims* dm, xmod_gate gate, const xmod_layer_weights* w,
+                             void* x_inout, const float* bias, int32_t* count_out, void* ws,
+                             size_t ws_bytes, void* stream) {
+  if (!dims_ok(dm) || !weights_ok(w, true)) return XMOD_ERR_INVALID_ARG;
+  if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
+  if (!aligned16(x_inout) || !aligned16_or_null(bias) || ((uintptr_t)count_out & 3))
+    return XMOD_ERR_INVALID_ARG;
+  if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
+  int st = check_ws(dm, 1, ws, ws_bytes);
+  if (st) return st;
+  const Layout L = layout(dm, 1);
+  if (!threshold_supported(dm, ws, L)) return XMOD_ERR_UNSUPPORTED;
+  Ctx c{(cudaStream_t)stream, (int*)at(ws, L.status)};
+  st = sparse_run(c, dm, L, ws, 1, gate, w, 1, x_inout, bias, nullptr, nullptr, nullptr, true);
+  if (st) return st;
+  if (count_out && cudaMemcpyAsync(count_out, at(ws, L.seq), sizeof(int32_t) * dm->B,
+                                   cudaMemcpyDeviceToDevice, c.stream) != cudaSuccess)
+    return XMOD_ERR_CUDA;
+  return XMOD_OK;
+}
+
 int xmod_stack_fwd(const xmod_dims* dm, int K, double A, int N0, int N1, xmod_gate gate,
                    const xmod_layer_weights* layers, int n_layers, void* x_inout,
                    const float* bias, void* ws, size_t ws_bytes, void* stream) {
@@ -496,6 +586,9 @@ int xmod_stack_fwd_ex(const xmod_dims* dm, int K, double A, int N0, int N1, xmod
   if (opts && (!isfinite(opts->bias_step) || opts->bias_step < 0.0f)) return XMOD_ERR_INVALID_ARG;
   if (opts && (((uintptr_t)opts->layer_stats & 3) || ((uintptr_t)opts->update_hist & 3)))
     return XMOD_ERR_INVALID_ARG;
+  if (opts && opts->routing != XMOD_ROUTE_TOPK && opts->routing != XMOD_ROUTE_THRESHOLD)
+    return XMOD_ERR_INVALID_ARG;
+  const bool threshold = opts && opts->routing == XMOD_ROUTE_THRESHOLD;
   // Eq. 3 order: N0 dense, then N1 blocks of AK sparse layers and one dense anchor.
   auto is_sparse = [&](int l) { return l >= N0 && ((l - N0) % (AK + 1)) < AK; };
   for (int l = 0; l < n_layers; ++l)
@@ -506,6 +599,7 @@ int xmod_stack_fwd_ex(const xmod_dims* dm, int K, double A, int N0, int N1, xmod
   if (st) return st;
   const Layout L = layout(dm, K);
   const bool runs = sparse_run_supported(dm, ws, L);
+  if (threshold && !threshold_supported(dm, ws, L)) return XMOD_ERR_UNSUPPORTED;
   Ctx c{(cudaStream_t)stream, (int*)at(ws, L.status)};
   const int64_t BT = (int64_t)dm->B * dm->T;
   // Token-choice bias state, only when an option needs it (else the plain top-k).
@@ -534,7 +628,7 @@ int xmod_stack_fwd_ex(const xmod_dims* dm, int K, double A, int N0, int N1, xmod
       if (tl.stats) tl.stats += (int64_t)sparse_index * dm->B * 4;
       if (runs)
         st = sparse_run(c, dm, L, ws, K, gate, &layers[l], count, x_inout, bias, nullptr, nullptr,
-                        tracked ? &tl : nullptr);
+                        tracked ? &tl : nullptr, threshold);
       else
         st = layer_impl(dm, XMOD_LAYER_SPARSE, K, gate, &layers[l], x_inout, bias, nullptr,
                         nullptr, ws, L, (cudaStream_t)stream, tracked ? &tl : nullptr);

@@ -69,6 +69,11 @@ struct AttnArgs {
   __nv_bfloat16* o;
   int ldo;
   int* status;
+  // Variable tokens per sequence (threshold routing): sequence b has seq_count[b]
+  // (<= n) rows starting at compact row seq_off[b]; the Q and K maps are then 2-D over
+  // the compact rows. NULL: every sequence has n rows at b * n.
+  const int32_t* seq_count;
+  const int32_t* seq_off;
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -109,8 +114,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
   const int h = blockIdx.y, b = blockIdx.z;
   const int g = h / (a.hq / a.hkv);
   const int q0 = qb * QB;
-  const int last_q = min(q0 + QB, a.n) - 1;
-  const int nkb = last_q / KB + 1;
 
   if (threadIdx.x == 0) {
     mbar_init(Q_FULL, 1);
@@ -137,12 +140,25 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
   const uint32_t tmem = *tmem_slot;   // S0: cols [0, KB), S1: [KB, 2KB), O: [2KB, 2KB+128)
   const uint32_t tO = tmem + 2u * KB;
   pdl_wait();  // everything above overlapped the previous kernel's tail
+  int n_b = a.n;
+  int64_t row0 = (int64_t)b * a.n;   // compact row of the sequence's first token
+  if (a.seq_count) {
+    n_b = min(max(a.seq_count[b], 0), a.n);
+    row0 = a.seq_off[b];
+  }
+  const int last_q = min(q0 + QB, n_b) - 1;
+  const int nkb = q0 < n_b ? last_q / KB + 1 : 0;   // 0: this query block is empty
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && nkb > 0) {
       mbar_arrive_expect_tx(Q_FULL, QTILE);
-      tma_load_3d(sQ, &tmQ, Q_FULL, h * HD, q0, b);
-      tma_load_3d(sQ + CHUNK, &tmQ, Q_FULL, h * HD + 64, q0, b);
+      if (a.seq_count) {
+        tma_load_2d(sQ, &tmQ, Q_FULL, h * HD, (int)(row0 + q0));
+        tma_load_2d(sQ + CHUNK, &tmQ, Q_FULL, h * HD + 64, (int)(row0 + q0));
+      } else {
+        tma_load_3d(sQ, &tmQ, Q_FULL, h * HD, q0, b);
+        tma_load_3d(sQ + CHUNK, &tmQ, Q_FULL, h * HD + 64, q0, b);
+      }
       const int vt_row = (b * a.hkv + g) * HD;
       for (int j = 0; j < nkb; ++j) {
         const int s = j & 1;
@@ -150,8 +166,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         if (!mbar_wait(KV_EMPTY0 + 8 * s, ph ^ 1u, abort_flag, a.status)) break;
         mbar_arrive_expect_tx(KV_FULL0 + 8 * s, C::K_STAGE + C::V_STAGE);
         const uint32_t kdst = sK0 + s * C::K_STAGE, vdst = sV0 + s * C::V_STAGE;
-        tma_load_3d(kdst, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD, j * KB, b);
-        tma_load_3d(kdst + C::K_CHUNK, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD + 64, j * KB, b);
+        if (a.seq_count) {
+          tma_load_2d(kdst, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD, (int)(row0 + j * KB));
+          tma_load_2d(kdst + C::K_CHUNK, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD + 64,
+                      (int)(row0 + j * KB));
+        } else {
+          tma_load_3d(kdst, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD, j * KB, b);
+          tma_load_3d(kdst + C::K_CHUNK, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD + 64, j * KB, b);
+        }
 #pragma unroll
         for (int kc = 0; kc < KB / 64; ++kc)
           tma_load_2d(vdst + kc * CHUNK, &tmVt, KV_FULL0 + 8 * s, j * KB + 64 * kc, vt_row);
@@ -161,7 +183,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, KB);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD);
-      bool ok = mbar_wait(Q_FULL, 0, abort_flag, a.status);
+      bool ok = nkb > 0 && mbar_wait(Q_FULL, 0, abort_flag, a.status);
       // Issue S_j = Q K_j^T and O += P_j V_j in whatever order their inputs arrive:
       // S_{j+1} as soon as K_{j+1} is resident (so it overlaps the softmax of S_j),
       // P_j V_j as soon as the softmax has written P_j -- never one waiting behind the
@@ -321,6 +343,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
       tc_fence_before();
       mbar_arrive(P_FULL0 + 8 * pb);
     }
+    if (nkb == 0) ok = false;   // nothing was computed for this query block
     if (ok) {
       const int jl = nkb - 1;
       ok = mbar_wait(P_EMPTY0 + 8 * (jl % PBUF), (uint32_t)(jl / PBUF) & 1u, abort_flag, a.status);
@@ -328,13 +351,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     if (ok) {
       tc_fence_after();
       const float inv = 1.0f / l;
-      __nv_bfloat16* dst = a.o + ((int64_t)b * a.n + qi) * a.ldo + h * HD;
+      __nv_bfloat16* dst = a.o + (row0 + qi) * a.ldo + h * HD;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float ov[32];
         tmem_ld32(tO + lane_off + c * 32, ov);
         tmem_ld_wait();
-        if (qi < a.n) {
+        if (qi < n_b) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 q;
@@ -367,12 +390,21 @@ cudaError_t launch_attention_cfg(const Ctx& c, int B, int n, int hq, const void*
                                  const CUtensorMap& mVt, const AttnArgs& a) {
   using Cf = AttnCfg<KB, PBUF>;
   CUtensorMap mQ, mK;
-  const int64_t dims[3] = {ldq, n, B};
-  const int64_t strides[2] = {(int64_t)ldq * 2, (int64_t)n * ldq * 2};
-  const int qbox[3] = {64, QB, 1};
-  const int kbox[3] = {64, KB, 1};
-  if (!tma_map_bf16(&mQ, qkv, 3, dims, strides, qbox)) return cudaErrorInvalidValue;
-  if (!tma_map_bf16(&mK, qkv, 3, dims, strides, kbox)) return cudaErrorInvalidValue;
+  if (a.seq_count) {   // 2-D over the B * n compact rows
+    const int64_t dims[2] = {ldq, (int64_t)B * n};
+    const int64_t strides[1] = {(int64_t)ldq * 2};
+    const int qbox[2] = {64, QB};
+    const int kbox[2] = {64, KB};
+    if (!tma_map_bf16(&mQ, qkv, 2, dims, strides, qbox)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(&mK, qkv, 2, dims, strides, kbox)) return cudaErrorInvalidValue;
+  } else {
+    const int64_t dims[3] = {ldq, n, B};
+    const int64_t strides[2] = {(int64_t)ldq * 2, (int64_t)n * ldq * 2};
+    const int qbox[3] = {64, QB, 1};
+    const int kbox[3] = {64, KB, 1};
+    if (!tma_map_bf16(&mQ, qkv, 3, dims, strides, qbox)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(&mK, qkv, 3, dims, strides, kbox)) return cudaErrorInvalidValue;
+  }
   auto k = attention_tc_kernel<KB, PBUF>;
   static bool attr = false;
   if (!attr) {
@@ -401,7 +433,8 @@ bool attention_tc_supported(int hd, int n, int ldq) {
 }
 
 cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
-                                int ldq, const void* vt, int vt_ld, void* o) {
+                                int ldq, const void* vt, int vt_ld, void* o,
+                                const int32_t* seq_count, const int32_t* seq_off) {
   if (B <= 0 || n <= 0) return cudaSuccess;
   CUtensorMap mVt;
   {
@@ -420,6 +453,8 @@ cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, con
   a.o = (__nv_bfloat16*)o;
   a.ldo = hq * HD;
   a.status = c.status;
+  a.seq_count = seq_count;
+  a.seq_off = seq_off;
   if (n <= XMOD_ATTN_ONE_BLOCK_MAX_N) return launch_attention_cfg<128, 2>(c, B, n, hq, qkv, ldq, mVt, a);
   return launch_attention_cfg<64, 1>(c, B, n, hq, qkv, ldq, mVt, a);
 }

@@ -58,6 +58,7 @@ struct TcArgs {
   int mode;                // EpiKind
   int n_split1, n_split2;  // STORE: first accumulator column served by B map 1 / map 2
   int tiles_m, tiles_n, tiles;
+  const int32_t* M_dev;    // if set, the rows are min(*M_dev, M), read on the device
   int v8;                  // epilogue row segments may use 32-byte accesses
   Epilogue e;
   int* status;
@@ -72,15 +73,32 @@ struct TcArgs {
 #define XMOD_TILE_BAND 16
 #endif
 
-__device__ __forceinline__ void tile_coords(const TcArgs& a, int tile, int& m_blk, int& n_blk,
-                                            int band_rows = XMOD_TILE_BAND) {
+__device__ __forceinline__ void tile_coords(const TcArgs& a, int tiles_m, int tile, int& m_blk,
+                                            int& n_blk, int band_rows = XMOD_TILE_BAND) {
   const int per_band = band_rows * a.tiles_n;
   const int band = tile / per_band;
   const int r = tile - band * per_band;
   const int m_first = band * band_rows;
-  const int rows = min(band_rows, a.tiles_m - m_first);
+  const int rows = min(band_rows, tiles_m - m_first);
   m_blk = m_first + r % rows;
   n_blk = r / rows;
+}
+
+// Rows and tiles of one launch: fixed at launch, or -- with M_dev -- the row count
+// written by an earlier kernel (a variable number of routed tokens), read after
+// griddepcontrol.wait. Tiles past it are skipped.
+struct Extent {
+  int M, tiles_m, tiles;
+};
+__device__ __forceinline__ Extent launch_extent(const TcArgs& a, int tile_rows) {
+  Extent x{a.M, a.tiles_m, a.tiles};
+  if (a.M_dev) {
+    const int m = *a.M_dev;
+    x.M = m < 0 ? 0 : (m < a.M ? m : a.M);
+    x.tiles_m = (x.M + tile_rows - 1) / tile_rows;
+    x.tiles = x.tiles_m * a.tiles_n;
+  }
+  return x;
 }
 
 // silu(z) = z * sigmoid(z) with the fast exponential and approximate division (a few
@@ -89,6 +107,7 @@ __device__ __forceinline__ void tile_coords(const TcArgs& a, int tile, int& m_bl
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ int64_t stream_row_of(const Epilogue& e, int m) {
+  if (e.tok) return e.tok[m];
   const int64_t b = m / e.n_per_seq;
   const int64_t t = e.idx ? (int64_t)e.idx[m] : (m - b * e.n_per_seq);
   return b * e.T + t;
@@ -212,10 +231,10 @@ struct EpiIn {
 };
 
 template <int MODE>
-__device__ __forceinline__ void epi_load_in(const TcArgs& a, int m, int col0, int64_t xrow,
+__device__ __forceinline__ void epi_load_in(const TcArgs& a, int M, int m, int col0, int64_t xrow,
                                             EpiIn& in) {
   const Epilogue& e = a.e;
-  if (m >= a.M || col0 >= a.N) return;
+  if (m >= M || col0 >= a.N) return;
   const int rem = a.N - col0;
   ld_seg_bf16((const __nv_bfloat16*)e.x + xrow + col0, in.x, rem, a.v8);
   if (MODE == EPI_DOWN_SCATTER) ld_seg_f32(e.h + (int64_t)m * e.d + col0, in.h, rem, a.v8);
@@ -239,11 +258,11 @@ __device__ __forceinline__ void unpack_x(const EpiIn& in, float (&xv)[32]) {
 // the A4K8 block: the extra shared-memory traffic competes with the MMA operand
 // reads, and one epilogue warp per scheduler cannot hide the added latency.)
 template <int MODE>
-__device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int m, int col0,
+__device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, int m, int col0,
                                                       int64_t xrow, float r, float (&v)[32],
                                                       const EpiIn& in) {
   const Epilogue& e = a.e;
-  if (m >= a.M || col0 >= a.N) return;
+  if (m >= M || col0 >= a.N) return;
   const int rem = a.N - col0;
   if (MODE == EPI_STORE || MODE == EPI_SWIGLU) {
     store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem, a.v8);
@@ -302,29 +321,29 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int m, in
 
 // Epilogue of one tile for this warp's 32-row slab [wrow0, wrow0 + 32).
 template <int BN, int MODE>
-__device__ __forceinline__ void epilogue_tile(const TcArgs& a, int wrow0, int lane, int n_blk,
-                                              uint32_t t_row, int part, int nparts) {
+__device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0, int lane,
+                                              int n_blk, uint32_t t_row, int part, int nparts) {
   const Epilogue& e = a.e;
   constexpr bool swiglu = MODE == EPI_SWIGLU;
   // the row this lane owns in TMEM: its stream row and gate
   const int m_own = wrow0 + lane;
   int64_t xrow_own = 0;
   float r_own = 1.0f;
-  if ((MODE == EPI_OPROJ || MODE == EPI_DOWN_SCATTER) && m_own < a.M) {
+  if ((MODE == EPI_OPROJ || MODE == EPI_DOWN_SCATTER) && m_own < M) {
     xrow_own = stream_row_of(e, m_own) * e.d;
     if (MODE == EPI_DOWN_SCATTER && e.gate >= 0) r_own = e.r_sel[m_own];
   }
-  if (MODE == EPI_ROUTER && m_own < a.M) xrow_own = stream_row_of(e, m_own);
+  if (MODE == EPI_ROUTER && m_own < M) xrow_own = stream_row_of(e, m_own);
   constexpr int NCH_FULL = BN / 32;
   const int nch = swiglu ? NCH_FULL / 2 : NCH_FULL;
   const int col_tile0 = swiglu ? n_blk * (BN / 2) : n_blk * BN;
   constexpr bool needs_in = MODE == EPI_OPROJ || MODE == EPI_DOWN_SCATTER;
   EpiIn cur, nxt;
-  if (needs_in && part < nch) epi_load_in<MODE>(a, m_own, col_tile0 + part * 32, xrow_own, cur);
+  if (needs_in && part < nch) epi_load_in<MODE>(a, M, m_own, col_tile0 + part * 32, xrow_own, cur);
 #pragma unroll 1
   for (int c = part; c < nch; c += nparts) {
     if (needs_in && c + nparts < nch)
-      epi_load_in<MODE>(a, m_own, col_tile0 + (c + nparts) * 32, xrow_own, nxt);
+      epi_load_in<MODE>(a, M, m_own, col_tile0 + (c + nparts) * 32, xrow_own, nxt);
     float v[32];
     if (swiglu) {
       float u[32];
@@ -341,10 +360,17 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int wrow0, int la
     if (MODE == EPI_STORE && e.vt && col0 >= e.vt_col0) {
       // v^T: token m of sequence b goes to column t of rows (b, g, dim). For each dim
       // the warp's 32 consecutive tokens form one contiguous run, so no staging.
-      if (m_own < a.M && col0 < a.N) {
+      if (m_own < M && col0 < a.N) {
         const int cv = col0 - e.vt_col0;
         const int g = cv / e.vt_hd, dim0 = cv % e.vt_hd;
-        const int64_t b = m_own / e.n_per_seq, t = m_own - b * e.n_per_seq;
+        int64_t b, t;
+        if (e.tok) {   // variable tokens per sequence: local index from the row offsets
+          b = e.tok[m_own] / e.T;
+          t = m_own - e.seq_off[b];
+        } else {
+          b = m_own / e.n_per_seq;
+          t = m_own - b * e.n_per_seq;
+        }
         __nv_bfloat16* p =
             (__nv_bfloat16*)e.vt + ((b * e.vt_hkv + g) * e.vt_hd + dim0) * (int64_t)e.vt_ld + t;
 #pragma unroll
@@ -352,7 +378,7 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int wrow0, int la
       }
       continue;
     }
-    epilogue_chunk_direct<MODE>(a, m_own, col0, xrow_own, r_own, v, cur);
+    epilogue_chunk_direct<MODE>(a, M, m_own, col0, xrow_own, r_own, v, cur);
     cur = nxt;
   }
 }
@@ -404,13 +430,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // everything above overlapped the previous kernel's tail
+  const Extent ext = launch_extent(args, BM);
 
   if (warp == 0) {
     if (lane == 0) {
       int it = 0;
-      for (int tile = blockIdx.x; tile < args.tiles && !*abort_flag; tile += gridDim.x) {
+      for (int tile = blockIdx.x; tile < ext.tiles && !*abort_flag; tile += gridDim.x) {
         int m_blk, n_blk;
-        tile_coords(args, tile, m_blk, n_blk);
+        tile_coords(args, ext.tiles_m, tile, m_blk, n_blk);
         const int m0 = m_blk * BM;
         const CUtensorMap* mp = &tmB0;
         int brow = n_blk * BN;
@@ -443,7 +470,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
       int it = 0, lt = 0;
-      for (int tile = blockIdx.x; tile < args.tiles && !*abort_flag; tile += gridDim.x, ++lt) {
+      for (int tile = blockIdx.x; tile < ext.tiles && !*abort_flag; tile += gridDim.x, ++lt) {
         const int acc = lt & 1;
         const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
         if (!mbar_wait(ACC_EMPTY(acc), aph ^ 1u, abort_flag, args.status)) break;
@@ -472,16 +499,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else {
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 belong to this warp
     int lt = 0;
-    for (int tile = blockIdx.x; tile < args.tiles; tile += gridDim.x, ++lt) {
+    for (int tile = blockIdx.x; tile < ext.tiles; tile += gridDim.x, ++lt) {
       const int acc = lt & 1;
       const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
       if (!mbar_wait(ACC_FULL(acc), aph, abort_flag, args.status)) break;
       tc_fence_after();
       int m_blk, n_blk;
-      tile_coords(args, tile, m_blk, n_blk);
+      tile_coords(args, ext.tiles_m, tile, m_blk, n_blk);
       const int wrow0 = m_blk * BM + quad * 32;
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<BN, MODE>(args, wrow0, lane, n_blk, t_row, (warp - 2) / 4, EPI_WARPS / 4);
+      epilogue_tile<BN, MODE>(args, ext.M, wrow0, lane, n_blk, t_row, (warp - 2) / 4,
+                              EPI_WARPS / 4);
       tc_fence_before();
       mbar_arrive(ACC_EMPTY(acc));
     }
@@ -585,7 +613,7 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int it = 0;
       for (int tile = pair; tile < args.tiles && !*abort_flag; tile += npairs) {
         int m_blk, n_blk;
-        tile_coords(args, tile, m_blk, n_blk, XMOD_TILE_BAND2);
+        tile_coords(args, args.tiles_m, tile, m_blk, n_blk, XMOD_TILE_BAND2);
         const int m0 = m_blk * (2 * BM) + (int)rank * BM;
         const CUtensorMap* mp = &tmB0;
         int brow = n_blk * BN;
@@ -652,10 +680,11 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       if (!mbar_wait_cluster(ACC_FULL(acc), aph, abort_flag, args.status)) break;
       tc_fence_after();
       int m_blk, n_blk;
-      tile_coords(args, tile, m_blk, n_blk, XMOD_TILE_BAND2);
+      tile_coords(args, args.tiles_m, tile, m_blk, n_blk, XMOD_TILE_BAND2);
       const int wrow0 = m_blk * (2 * BM) + (int)rank * BM + quad * 32;
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<BN, MODE>(args, wrow0, lane, n_blk, t_row, (warp - 2) / 4, EPI_WARPS / 4);
+      epilogue_tile<BN, MODE>(args, args.M, wrow0, lane, n_blk, t_row, (warp - 2) / 4,
+                              EPI_WARPS / 4);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(ACC_EMPTY(acc), 0));
@@ -714,6 +743,7 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
   memset(&mB2, 0, sizeof(mB2));
   if (!make_map(&mA, p.A, p.K, p.M, p.lda, BM)) return false;
   a.M = p.M;
+  a.M_dev = p.M_dev;
   a.N = p.N;
   a.K = p.K;
   a.mode = e.kind;
@@ -888,7 +918,7 @@ cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue&
   // up (gate/up at M = 4096: 58.7 -> 53.9 us; every dense-layer GEMM at M = 32768:
   // 7-17%) and lose below three (q|k|v, o-proj, down at M = 4096: 3-12%). Narrower
   // pair tiles were slower than single-CTA tiles of the same width.
-  if (XMOD_GEMM_PAIRS && p.M > BM && bn_ok(p, e, 256)) {
+  if (XMOD_GEMM_PAIRS && p.M > BM && !p.M_dev && bn_ok(p, e, 256)) {
     const long tiles_m = (p.M + 2 * BM - 1) / (2 * BM);
     const int cols = e.kind == EPI_SWIGLU ? 128 : 256;
     const long tiles = tiles_m * ((p.N + cols - 1) / cols);

@@ -90,6 +90,12 @@ struct RouteTrack {
 // r_sel [B, n] = sigmoid(ranked logit at idx) if not NULL.
 cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32_t* idx,
                         float* r_sel, const RouteTrack* tr = nullptr);
+// Causal threshold rule over s [B, T] (ranked logit s - bias_step * count >= 0):
+// compact rows tok [<= B*T] (= b * T + t, sequence then position order), r_sel
+// [<= B*T], seq_count [B], seq_off [B] and the total in *M_out (all device).
+cudaError_t launch_threshold_select(const Ctx& c, int B, int T, const float* s, int32_t* tok,
+                                    float* r_sel, int32_t* seq_count, int32_t* seq_off,
+                                    int32_t* M_out, const RouteTrack* tr = nullptr);
 // update_hist [B, max_count + 1]: histogram of count [B, T] per sequence.
 cudaError_t launch_count_hist(const Ctx& c, int B, int T, int max_count, const int32_t* count,
                               int32_t* update_hist);
@@ -98,14 +104,29 @@ cudaError_t launch_count_hist(const Ctx& c, int B, int T, int max_count, const i
 cudaError_t launch_gather(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
                           const void* x, const int32_t* idx, void* xs);
 
-// u[b*n + j] = RMSNorm(x[b, idx[b, j]]) * gamma (idx NULL: identity).
+// Compact rows with a variable count (threshold routing): row m reads stream row
+// tok[m], and only rows below *M_dev exist. Both NULL: the fixed layout.
+struct RowMap {
+  const int32_t* tok = nullptr;
+  const int32_t* M_dev = nullptr;
+  __device__ __forceinline__ int64_t rows(int64_t M) const {
+    if (!M_dev) return M;
+    const int64_t m = *M_dev;
+    return m < M ? m : M;
+  }
+};
+
+// u[b*n + j] = RMSNorm(x[b, idx[b, j]]) * gamma (idx NULL: identity); with rm.tok,
+// u[m] = RMSNorm(x[tok[m]]) * gamma for the rows rm gives.
 cudaError_t launch_gather_rmsnorm(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
                                   const void* x, const int32_t* idx, const void* gamma,
-                                  float eps, void* u);
+                                  float eps, void* u, RowMap rm = RowMap{});
 
-// out[m] = RMSNorm(h[m]) * gamma for fp32 rows h [M, d]; out in the element type.
+// out[m] = RMSNorm(h[m]) * gamma for fp32 rows h [M, d] (only m < *M_dev if given);
+// out in the element type.
 cudaError_t launch_rmsnorm_f32in(const Ctx& c, xmod_dtype dt, int64_t M, int d, const float* h,
-                                 const void* gamma, float eps, void* out);
+                                 const void* gamma, float eps, void* out,
+                                 const int32_t* M_dev = nullptr);
 
 // Gated residual in place, see xmod_gated_scatter. gate < 0: dense update x + a + f.
 cudaError_t launch_gated_scatter(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
@@ -144,6 +165,10 @@ struct Epilogue {
   void* x = nullptr;            // residual stream [B, T, d] (read for OPROJ, updated for DOWN)
   const int32_t* idx = nullptr;
   int T = 0, n_per_seq = 0, d = 0;
+  // Variable tokens per sequence (threshold routing): the stream row of compact row m
+  // is tok[m] (= b * T + t), and seq_off[b] is sequence b's first compact row.
+  const int32_t* tok = nullptr;
+  const int32_t* seq_off = nullptr;
   const float* h = nullptr;     // DOWN: h = x_sel + a [M, d] fp32 (the attention residual is h - x)
   const float* r_sel = nullptr; // DOWN: gates [M]
   const float* bias = nullptr;  // ROUTER: per-token logit bias [B*T] or NULL
@@ -174,6 +199,9 @@ struct GemmTcProblem {
   int split[2] = {0, 0};
   int ldb = 0;
   int b_rows = 0;  // rows of B[0] the tensor map spans (0: N); may exceed N
+  // If set, the launch covers M rows of buffers sized for M, but only the first
+  // min(*M_dev, M) rows (a count an earlier kernel wrote) are computed.
+  const int32_t* M_dev = nullptr;
 };
 bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e);
 cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e);
@@ -190,8 +218,12 @@ cudaError_t launch_attention_simt(const Ctx& c, xmod_dtype dt, int B, int n, int
 // Tensor-core attention (bf16, head_dim 128). q and k come from the q|k|v rows
 // [B*n, ldq] (k of KV head g at column hq*128 + g*128); v comes transposed,
 // vt [B, hkv, 128, vt_ld] with keys contiguous; o [B*n, hq*128].
+// With seq_count / seq_off (device [B]): sequence b has seq_count[b] <= n tokens at
+// compact rows seq_off[b] ...; its keys past seq_count[b] in vt must be finite.
 bool attention_tc_supported(int hd, int n, int ldq);
 cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
-                                int ldq, const void* vt, int vt_ld, void* o);
+                                int ldq, const void* vt, int vt_ld, void* o,
+                                const int32_t* seq_count = nullptr,
+                                const int32_t* seq_off = nullptr);
 
 }  // namespace xmod

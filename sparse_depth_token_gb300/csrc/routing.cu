@@ -409,6 +409,109 @@ cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32
   return cudaGetLastError();
 }
 
+// ================================================================ causal threshold rule
+//
+// X-MoD notes, "top-k in training, causal threshold at evaluation": token t enters the
+// layer when its routing probability is at least 1/2, i.e. its ranked logit
+// s - bias_step * count is >= 0 (-0 included), each token on its own. One CTA walks
+// the sequences in order and each sequence in 1024-token chunks, so the compact rows
+// come out in (sequence, position) order: tok[m] = b * T + t, r_sel[m] = sigmoid of
+// the logit, seq_count[b], seq_off[b] and *M_out = total.
+
+// Sum of one value per thread over the CTA: (exclusive prefix of this thread's warp,
+// CTA total), both uniform within a warp.
+__device__ __forceinline__ uint2 warps_scan_total(uint32_t v, uint32_t* sh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t t = sh[lane];
+    uint32_t inc = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    sh[lane] = inc - t;
+    if (lane == 31) sh[32] = inc;
+  }
+  __syncthreads();
+  const uint2 r = make_uint2(sh[warp], sh[32]);
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(TOPK_THREADS)
+threshold_select_kernel(int B, int T, const float* __restrict__ s, int32_t* __restrict__ tok,
+                        float* __restrict__ r_sel, int32_t* __restrict__ seq_count,
+                        int32_t* __restrict__ seq_off, int32_t* __restrict__ M_out, int* status,
+                        RouteTrack tr) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ uint32_t sh[33];
+  __shared__ int sh_bad;
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  if (threadIdx.x == 0) sh_bad = 0;
+  __syncthreads();
+  uint32_t out = 0;   // next compact row (the same in every thread)
+  for (int b = 0; b < B; ++b) {
+    const float* sb = s + (int64_t)b * T;
+    int32_t* cnt = tr.count ? tr.count + (int64_t)b * T : nullptr;
+    int32_t* last = tr.last ? tr.last + (int64_t)b * T : nullptr;
+    const uint32_t first = out;
+    uint32_t again = 0;
+    for (int t0 = 0; t0 < T; t0 += TOPK_THREADS) {
+      const int t = t0 + (int)threadIdx.x;
+      float v = 0.0f;
+      bool take = false;
+      if (t < T) {
+        v = cnt ? sb[t] - tr.bias_step * (float)cnt[t] : sb[t];
+        if (!isfinite(v)) sh_bad = 1;
+        take = v >= 0.0f;
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, take);
+      const uint2 sc = warps_scan_total((uint32_t)__popc(bal), sh);
+      if (take) {
+        const uint32_t m = out + sc.x + (uint32_t)__popc(bal & lt_mask);
+        tok[m] = b * T + t;
+        r_sel[m] = sigmoidf_acc(v);
+        if (last && last[t] == tr.layer - 1) ++again;
+        if (cnt) cnt[t] += 1;
+        if (last) last[t] = tr.layer;
+      }
+      out += sc.y;
+    }
+    if (tr.stats) {   // reduce `again` over the CTA (only the stats use it)
+      const uint2 sc = warps_scan_total((uint32_t)__reduce_add_sync(0xffffffffu, again), sh);
+      if (threadIdx.x == 0) {
+        int32_t* st = tr.stats + (int64_t)b * 4;
+        st[0] = (int32_t)(out - first);
+        st[1] = (int32_t)(out - first);   // the rule's own picks are its threshold picks
+        st[2] = T;
+        st[3] = (int32_t)sc.y;
+      }
+    }
+    if (threadIdx.x == 0) {
+      seq_count[b] = (int32_t)(out - first);
+      seq_off[b] = (int32_t)first;
+    }
+  }
+  if (threadIdx.x == 0) {
+    *M_out = (int32_t)out;
+    if (sh_bad) report_status(status, XMOD_ERR_DEVICE_CHECK);
+  }
+}
+
+cudaError_t launch_threshold_select(const Ctx& c, int B, int T, const float* s, int32_t* tok,
+                                    float* r_sel, int32_t* seq_count, int32_t* seq_off,
+                                    int32_t* M_out, const RouteTrack* tr) {
+  if (B <= 0 || T <= 0) return cudaErrorInvalidValue;
+  const RouteTrack none{};
+  return launch_pdl(threshold_select_kernel, dim3(1), dim3(TOPK_THREADS), 0, c.stream, B, T, s,
+                    tok, r_sel, seq_count, seq_off, M_out, c.status, tr ? *tr : none);
+}
+
 // update_hist[b, c] = number of tokens of sequence b whose count is c (0 <= c <= max_count).
 __global__ void count_hist_kernel(int T, int max_count, const int32_t* __restrict__ count,
                                   int32_t* __restrict__ update_hist) {
@@ -496,14 +599,14 @@ template <typename T, int VPL>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 gather_rmsnorm_rows_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
                            const int32_t* __restrict__ idx, const T* __restrict__ gamma,
-                           float eps, T* __restrict__ u) {
+                           float eps, T* __restrict__ u, RowMap rm) {
   pdl_trigger();
   pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
-  if (m >= M) return;
-  const T* src = x + stream_row(m, seqT, n, idx) * d;
+  if (m >= rm.rows(M)) return;
+  const T* src = x + (rm.tok ? (int64_t)rm.tok[m] : stream_row(m, seqT, n, idx)) * d;
   Vec16<T> v[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
@@ -539,11 +642,11 @@ template <typename T>
 static cudaError_t launch_gather_rmsnorm_rows(const Ctx& c, int vpl, unsigned blocks, int64_t M,
                                               int seqT, int n, int d, const T* x,
                                               const int32_t* idx, const T* gamma, float eps,
-                                              T* u) {
+                                              T* u, RowMap rm) {
 #define XMOD_GR_CASE(N)                                                                     \
   case N:                                                                                   \
     launch_pdl(gather_rmsnorm_rows_kernel<T, N>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream,               \
-        M, seqT, n, d, x, idx, gamma, eps, u);                                              \
+        M, seqT, n, d, x, idx, gamma, eps, u, rm);                                          \
     break;
   switch (vpl) {
     XMOD_GR_CASE(1)
@@ -602,7 +705,7 @@ cudaError_t launch_gather(const Ctx& c, xmod_dtype dt, int B, int T, int n, int 
 
 cudaError_t launch_gather_rmsnorm(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
                                   const void* x, const int32_t* idx, const void* gamma,
-                                  float eps, void* u) {
+                                  float eps, void* u, RowMap rm) {
   const int64_t M = (int64_t)B * n;
   if (M <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
@@ -611,10 +714,11 @@ cudaError_t launch_gather_rmsnorm(const Ctx& c, xmod_dtype dt, int B, int T, int
     if (dt == XMOD_BF16)
       return launch_gather_rmsnorm_rows<__nv_bfloat16>(
           c, vpl, blocks, M, T, n, d, (const __nv_bfloat16*)x, idx, (const __nv_bfloat16*)gamma,
-          eps, (__nv_bfloat16*)u);
+          eps, (__nv_bfloat16*)u, rm);
     return launch_gather_rmsnorm_rows<float>(c, vpl, blocks, M, T, n, d, (const float*)x, idx,
-                                             (const float*)gamma, eps, (float*)u);
+                                             (const float*)gamma, eps, (float*)u, rm);
   }
+  if (rm.tok || rm.M_dev) return cudaErrorInvalidValue;   // rows beyond the cached widths
   if (dt == XMOD_BF16)
     launch_pdl(gather_rmsnorm_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
         M, T, n, d, (const __nv_bfloat16*)x, idx, (const __nv_bfloat16*)gamma, eps,
@@ -658,13 +762,14 @@ rmsnorm_f32in_kernel(int64_t M, int d, const float* __restrict__ h, const T* __r
 template <typename T, int VPL>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 rmsnorm_f32in_rows_kernel(int64_t M, int d, const float* __restrict__ h,
-                          const T* __restrict__ gamma, float eps, T* __restrict__ out) {
+                          const T* __restrict__ gamma, float eps, T* __restrict__ out,
+                          const int32_t* __restrict__ M_dev) {
   pdl_trigger();
   pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
-  if (m >= M) return;
+  if (m >= M || (M_dev && m >= *M_dev)) return;
   const float* src = h + m * d;
   float4 v[VPL][V / 4];
 #pragma unroll
@@ -710,11 +815,11 @@ rmsnorm_f32in_rows_kernel(int64_t M, int d, const float* __restrict__ h,
 template <typename T>
 static cudaError_t launch_rmsnorm_f32in_rows(const Ctx& c, int vpl, unsigned blocks, int64_t M,
                                              int d, const float* h, const T* gamma, float eps,
-                                             T* out) {
+                                             T* out, const int32_t* M_dev) {
 #define XMOD_RN_CASE(N)                                                                    \
   case N:                                                                                  \
     launch_pdl(rmsnorm_f32in_rows_kernel<T, N>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, M, d, h, gamma, \
-                                                                            eps, out);     \
+                                                                            eps, out, M_dev); \
     break;
   switch (vpl) {
     XMOD_RN_CASE(1)
@@ -732,7 +837,7 @@ static cudaError_t launch_rmsnorm_f32in_rows(const Ctx& c, int vpl, unsigned blo
 }
 
 cudaError_t launch_rmsnorm_f32in(const Ctx& c, xmod_dtype dt, int64_t M, int d, const float* h,
-                                 const void* gamma, float eps, void* out) {
+                                 const void* gamma, float eps, void* out, const int32_t* M_dev) {
   if (M <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
   const int vpl = pick_vpl((d / (dt == XMOD_BF16 ? 8 : 4) + 31) / 32);
@@ -740,10 +845,11 @@ cudaError_t launch_rmsnorm_f32in(const Ctx& c, xmod_dtype dt, int64_t M, int d, 
     if (dt == XMOD_BF16)
       return launch_rmsnorm_f32in_rows<__nv_bfloat16>(c, vpl, blocks, M, d, h,
                                                       (const __nv_bfloat16*)gamma, eps,
-                                                      (__nv_bfloat16*)out);
+                                                      (__nv_bfloat16*)out, M_dev);
     return launch_rmsnorm_f32in_rows<float>(c, vpl, blocks, M, d, h, (const float*)gamma, eps,
-                                            (float*)out);
+                                            (float*)out, M_dev);
   }
+  if (M_dev) return cudaErrorInvalidValue;   // rows beyond the cached widths
   if (dt == XMOD_BF16)
     launch_pdl(rmsnorm_f32in_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
         M, d, h, (const __nv_bfloat16*)gamma, eps, (__nv_bfloat16*)out);

@@ -23,7 +23,7 @@ EXPORTS = ("xmod_version", "xmod_status_string", "xmod_workspace_bytes", "xmod_r
            "xmod_sync_status", "xmod_router_topk", "xmod_topk", "xmod_gather", "xmod_block_fwd",
            "xmod_gated_scatter", "xmod_layer_fwd", "xmod_stack_fwd", "xmod_launch_count",
            "xmod_profile_enable", "xmod_profile_read", "xmod_router_topk_noalloc",
-           "xmod_stack_fwd_ex")
+           "xmod_stack_fwd_ex", "xmod_layer_fwd_threshold")
 
 # Largest B*T the allocation-free router entry point accepts (its fixed scratch).
 NOALLOC_MAX_TOKENS = 2 * 1024 * 1024
@@ -47,9 +47,12 @@ class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in NAMES] + [("varsigma", ctypes.c_float)]
 
 
+ROUTE_TOPK, ROUTE_THRESHOLD = 0, 1
+
+
 class StackOpts(ctypes.Structure):
     _fields_ = [("bias_step", ctypes.c_float), ("layer_stats", ctypes.c_void_p),
-                ("update_hist", ctypes.c_void_p)]
+                ("update_hist", ctypes.c_void_p), ("routing", ctypes.c_int)]
 
 
 class KernelTime(ctypes.Structure):
@@ -102,6 +105,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.POINTER(LayerWeights), ctypes.c_int, _VP, _VP,
                                     ctypes.POINTER(StackOpts), _VP, ctypes.c_size_t, _VP]
+    L.xmod_layer_fwd_threshold.argtypes = [ctypes.POINTER(Dims), ctypes.c_int,
+                                           ctypes.POINTER(LayerWeights), _VP, _VP, _VP, _VP,
+                                           ctypes.c_size_t, _VP]
     L.xmod_launch_count.restype = ctypes.c_uint64
     L.xmod_profile_enable.argtypes = [ctypes.c_int]
     L.xmod_profile_read.argtypes = [ctypes.POINTER(KernelTime), ctypes.c_int,
@@ -215,15 +221,24 @@ def stack_fwd(dm, K, A, N0, N1, gate, layers, x, bias, ws, stream=None):
 
 
 def stack_fwd_ex(dm, K, A, N0, N1, gate, layers, x, bias, ws, bias_step=0.0, layer_stats=None,
-                 update_hist=None, stream=None):
-    """xmod_stack_fwd_ex: the stack with the token-choice bias dynamics (bias_step) and,
-    when given, the routing statistics: layer_stats int32 [n_sparse, B, 4] and
-    update_hist int32 [N1, B, AK + 1] (device tensors)."""
+                 update_hist=None, routing=ROUTE_TOPK, stream=None):
+    """xmod_stack_fwd_ex: the stack with the token-choice bias dynamics (bias_step), the
+    selection rule (ROUTE_TOPK or ROUTE_THRESHOLD) and, when given, the routing
+    statistics: layer_stats int32 [n_sparse, B, 4] and update_hist int32
+    [N1, B, AK + 1] (device tensors)."""
     arr = (LayerWeights * len(layers))(*layers)
-    opts = StackOpts(float(bias_step), _p(layer_stats), _p(update_hist))
+    opts = StackOpts(float(bias_step), _p(layer_stats), _p(update_hist), int(routing))
     _check("xmod_stack_fwd_ex", load().xmod_stack_fwd_ex(
         ctypes.byref(dm), int(K), float(A), int(N0), int(N1), int(gate), arr, len(layers), _p(x),
         _p(bias), ctypes.byref(opts), _p(ws), _wsb(ws), _stream(stream)))
+
+
+def layer_fwd_threshold(dm, gate, w, x, bias, ws, count_out=None, stream=None):
+    """xmod_layer_fwd_threshold: one sparse layer under the causal threshold rule;
+    count_out (device int32 [B]) receives each sequence's routed token count."""
+    _check("xmod_layer_fwd_threshold", load().xmod_layer_fwd_threshold(
+        ctypes.byref(dm), int(gate), ctypes.byref(w), _p(x), _p(bias), _p(count_out), _p(ws),
+        _wsb(ws), _stream(stream)))
 
 
 def launch_count() -> int:

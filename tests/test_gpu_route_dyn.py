@@ -67,7 +67,7 @@ def test_tiny_fp32_dynamics_end_to_end(X, bias_step):
     w = I.WORKLOADS["tiny_fp32"].replace(N1=2, n_layers=11)
     layers, kinds, bias, x, abi = _setup(X, w)
     xd, st, uh = _run(X, w, kinds, x, bias, abi, bias_step)
-    ref, idx, s = O.stack_dyn(oracle_dims(w), w.K, w.gate, kinds,
+    ref, idx, s, _ = O.stack_dyn(oracle_dims(w), w.K, w.gate, kinds,
                               [oracle_layer(l, "fp32") for l in layers], I.to_f64(x, "fp32"),
                               bias=bias, bias_step=bias_step)
     U.assert_close(from_dev(xd, "fp32").reshape(ref.shape), ref, "fp32", "stack")

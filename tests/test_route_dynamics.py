@@ -124,7 +124,7 @@ def _tiny(**over):
 def test_oracle_dynamics_without_growth_is_the_constant_bias_stack():
     w, kinds, od, ol, x, bias = _tiny()
     y0 = O.stack_fwd(od, w.K, w.gate, kinds, ol, x, bias=bias)
-    y1, idx, s = O.stack_dyn(od, w.K, w.gate, kinds, ol, x, bias=bias, bias_step=0.0)
+    y1, idx, s, _ = O.stack_dyn(od, w.K, w.gate, kinds, ol, x, bias=bias, bias_step=0.0)
     assert np.array_equal(y0, y1)
     assert idx.shape == (kinds.count(S.SPARSE), w.B, w.T // w.K)
 
@@ -133,7 +133,7 @@ def test_oracle_dynamics_overwhelming_growth_rotates_tokens():
     # [D] + ([S(4)] x 4 + [D]) x 2: blocks of K = 4 sparse layers over T = 64 tokens
     w, kinds, od, ol, x, bias = _tiny(N1=2, n_layers=1 + 2 * 5)
     big = 1e6
-    y, idx, s = O.stack_dyn(od, w.K, w.gate, kinds, ol, x, bias=bias, bias_step=big)
+    y, idx, s, _ = O.stack_dyn(od, w.K, w.gate, kinds, ol, x, bias=bias, bias_step=big)
     AK, n = w.K, w.T // w.K
     masks = D.masks_from_idx(idx, w.T)
     for k in range(w.N1):
