@@ -59,9 +59,11 @@ def workload_config(w: I.Workload) -> dict:
     }
 
 
-def algorithmic_work(w: I.Workload) -> dict:
+def algorithmic_work(w: I.Workload, sel_counts=None) -> dict:
     """Algorithmic FLOPs (tensor kinds) or bytes (memory kinds) per step, per kernel kind.
-    Sparse layers count only the selected tokens; attention is causal (half the square)."""
+    Sparse layers count only the selected tokens; attention is causal (half the square).
+    sel_counts [n_sparse, B]: tokens each sparse layer routed per sequence (threshold
+    routing); None: T / K each."""
     es = 2 if w.dtype == "bf16" else 4
     out = {}
 
@@ -70,9 +72,16 @@ def algorithmic_work(w: I.Workload) -> dict:
 
     kinds = schedule(w)
     run_left = 0   # layers left in the current run of sparse layers (logits kept current)
+    ls = 0
     for l, sparse in enumerate(kinds):
         n = w.T // w.K if sparse else w.T
         M = w.B * n
+        ns = [n] * w.B
+        if sparse and sel_counts is not None:
+            ns = [int(v) for v in sel_counts[ls]]
+            M = sum(ns)
+        if sparse:
+            ls += 1
         if sparse:
             if run_left == 0:   # one pass over the stream: logits of up to 32 layers
                 run = 1
@@ -86,7 +95,7 @@ def algorithmic_work(w: I.Workload) -> dict:
             add("topk", 4 * w.B * w.T + 8 * M)
         add("gather_rmsnorm", 2 * M * w.d * es)
         add("gemm_qkv", 2 * M * w.d * (w.hq + 2 * w.hkv) * w.hd)
-        add("attention", 2 * w.B * n * n * w.hd * w.hq)
+        add("attention", 2 * sum(v * v for v in ns) * w.hd * w.hq)
         add("gemm_o_residual", 2 * M * w.hq * w.hd * w.d)
         add("rmsnorm2", M * w.d * (4 + es))
         add("gemm_gate_up_swiglu", 4 * M * w.d * w.F)
@@ -283,9 +292,29 @@ def run_xmod(args):
     ws = torch.zeros(X.workspace_bytes(dm, w.K), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    plain = args.routing == "topk" and args.bias_step == 0.0
+
+    def run_stack(stats=None):
+        if plain and stats is None:
+            X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, x, bias, ws, stream)
+        else:
+            X.stack_fwd_ex(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, x, bias, ws,
+                           bias_step=args.bias_step, layer_stats=stats,
+                           routing=X.ROUTE_THRESHOLD if args.routing == "threshold" else X.ROUTE_TOPK,
+                           stream=stream)
+
     def step():
         x.copy_(x0, non_blocking=True)
-        X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, x, bias, ws, stream)
+        run_stack()
+
+    sel_counts = None
+    if not plain:
+        # tokens each sparse layer routes (the same every step: the input is restored)
+        stats = torch.zeros((n_sparse, w.B, 4), dtype=torch.int32, device=dev)
+        x.copy_(x0)
+        run_stack(stats)
+        sel_counts = stats[:, :, 0].cpu().numpy()
+        sel_per_step = int(sel_counts.sum())
 
     def barrier():
         if dist is not None:
@@ -332,7 +361,7 @@ def run_xmod(args):
     torch.cuda.synchronize()
     X.profile_enable(False)
     prof = X.profile_read()
-    work = algorithmic_work(w)
+    work = algorithmic_work(w, sel_counts)
     peaks = measured_peaks()
     total_ms = sum(v[1] for v in prof.values())
     kernels = {}
@@ -381,7 +410,7 @@ def run_xmod(args):
             x.copy_(xh, non_blocking=True)
             if bh is not None:
                 bias.copy_(bh, non_blocking=True)
-            X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, x, bias, ws, stream)
+            run_stack()
             out_h.copy_(x, non_blocking=True)
 
         for _ in range(2):
@@ -415,6 +444,10 @@ def run_xmod(args):
     if rank == 0:
         cfg = workload_config(w)
         cfg["parallelism"] = f"replicas x{world} (sequences sharded, no collective)"
+        if not plain:
+            cfg["routing"] = args.routing
+            cfg["bias_step"] = args.bias_step
+            cfg["selected_tokens_per_step_per_gpu"] = sel_per_step
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -445,6 +478,10 @@ def main():
                     help="override sequences per GPU (small profiling cases only)")
     ap.add_argument("--A", type=float, default=None,
                     help="override the anchor stride A (small profiling cases only)")
+    ap.add_argument("--routing", choices=["topk", "threshold"], default="topk",
+                    help="token selection of the sparse layers (threshold: r >= 1/2)")
+    ap.add_argument("--bias-step", type=float, default=0.0,
+                    help="token-choice bias growth per selection inside a block (0: constant)")
     args = ap.parse_args()
     if args.B is not None or args.A is not None:
         w = I.WORKLOADS[args.workload]

@@ -245,9 +245,13 @@ __device__ __forceinline__ uint32_t warps_exclusive_scan(uint32_t v, uint32_t* s
   return r;
 }
 
+// TRACK: the token-choice bias state / statistics of tr are used (else tr is ignored
+// and the kernel is the plain top-(T/K)).
+template <bool TRACK>
 __global__ void __launch_bounds__(TOPK_THREADS)
 topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx,
             float* __restrict__ r_sel, int* status, RouteTrack tr) {
+  if (!TRACK) tr = RouteTrack{};
   pdl_trigger();
   pdl_wait();
   extern __shared__ uint32_t keys[];
@@ -401,11 +405,16 @@ cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32
                         float* r_sel, const RouteTrack* tr) {
   if (B <= 0) return cudaSuccess;
   const size_t smem = sizeof(uint32_t) * (size_t)T;
-  cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)(sizeof(uint32_t) * TOPK_MAX_T));
-  const RouteTrack none{};
-  launch_pdl(topk_kernel, dim3(B), dim3(TOPK_THREADS), smem, c.stream, T, n, s, idx, r_sel,
-             c.status, tr ? *tr : none);
+  cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)(sizeof(uint32_t) * TOPK_MAX_T));
+  if (tr)
+    launch_pdl(topk_kernel<true>, dim3(B), dim3(TOPK_THREADS), smem, c.stream, T, n, s, idx,
+               r_sel, c.status, *tr);
+  else
+    launch_pdl(topk_kernel<false>, dim3(B), dim3(TOPK_THREADS), smem, c.stream, T, n, s, idx,
+               r_sel, c.status, RouteTrack{});
   return cudaGetLastError();
 }
 
