@@ -216,6 +216,19 @@ XMOD_API int xmod_stack_fwd_ex(const xmod_dims* dims, int K, double A, int N0, i
                                void* x_inout, const float* bias, const xmod_stack_opts* opts,
                                void* ws, size_t ws_bytes, void* stream);
 
+/* A stack in an explicit layer order: kinds (host array of n_layers values,
+ * XMOD_LAYER_DENSE or XMOD_LAYER_SPARSE) and `layers` in execution order. This is
+ * how the heterogeneous segment stacks of X-MoD notes Eq. 35 and Eq. 36 (a shorter
+ * first sparse segment, then A4K8 / A3K16 segments) and MoD's Eq. 34 run. Blocks are
+ * the maximal runs of consecutive sparse layers; each sparse layer selects T / K
+ * tokens (or follows opts->routing). With opts->update_hist the histogram has one
+ * [B, L_max + 1] slab per block, L_max the longest block; layer_stats is as for
+ * xmod_stack_fwd_ex. opts may be NULL. */
+XMOD_API int xmod_stack_fwd_sched(const xmod_dims* dims, int K, const int32_t* kinds,
+                                  int n_layers, xmod_gate gate, const xmod_layer_weights* layers,
+                                  void* x_inout, const float* bias, const xmod_stack_opts* opts,
+                                  void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------- allocation-free routing
  * The paper has no counterpart to this entry point: it exists for callers that
  * cannot allocate device memory -- a plugin inside another runtime that is given

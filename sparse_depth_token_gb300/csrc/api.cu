@@ -12,6 +12,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <vector>
+
 #include "internal.h"
 #include "xmod.h"
 
@@ -407,6 +409,90 @@ int layer_impl(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
   return run_block(c, dm, L, ws, n, x, idx, w, nullptr, nullptr, true, x, r_sel, (int)gate);
 }
 
+// A stack in the given layer order. Blocks are the maximal runs of consecutive sparse
+// layers (each ended by a dense layer or the end of the stack); the token-choice bias
+// state is cleared at the start of each, and update_hist has one [B, L_max + 1] slab
+// per block, L_max the longest block.
+int stack_impl(const xmod_dims* dm, int K, const int32_t* kinds, int n_layers, xmod_gate gate,
+               const xmod_layer_weights* layers, void* x_inout, const float* bias,
+               const xmod_stack_opts* opts, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
+  if (!aligned16(x_inout) || !aligned16_or_null(bias)) return XMOD_ERR_INVALID_ARG;
+  if (opts && (!isfinite(opts->bias_step) || opts->bias_step < 0.0f)) return XMOD_ERR_INVALID_ARG;
+  if (opts && (((uintptr_t)opts->layer_stats & 3) || ((uintptr_t)opts->update_hist & 3)))
+    return XMOD_ERR_INVALID_ARG;
+  if (opts && opts->routing != XMOD_ROUTE_TOPK && opts->routing != XMOD_ROUTE_THRESHOLD)
+    return XMOD_ERR_INVALID_ARG;
+  const bool threshold = opts && opts->routing == XMOD_ROUTE_THRESHOLD;
+  auto is_sparse = [&](int l) { return kinds[l] == XMOD_LAYER_SPARSE; };
+  bool any_sparse = false;
+  int max_block = 0;
+  for (int l = 0, run = 0; l < n_layers; ++l) {
+    if (!weights_ok(&layers[l], is_sparse(l))) return XMOD_ERR_INVALID_ARG;
+    run = is_sparse(l) ? run + 1 : 0;
+    any_sparse = any_sparse || is_sparse(l);
+    max_block = run > max_block ? run : max_block;
+  }
+  if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
+  if (any_sparse && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
+  int st = check_ws(dm, K, ws, ws_bytes);
+  if (st) return st;
+  const Layout L = layout(dm, K);
+  const bool runs = sparse_run_supported(dm, ws, L);
+  if (threshold && !threshold_supported(dm, ws, L)) return XMOD_ERR_UNSUPPORTED;
+  Ctx c{stream, (int*)at(ws, L.status)};
+  const int64_t BT = (int64_t)dm->B * dm->T;
+  // Token-choice bias state, only when an option needs it (else the plain top-k).
+  const bool tracked = opts && (opts->bias_step != 0.0f || opts->layer_stats || opts->update_hist);
+  RouteTrack track;
+  if (tracked) {
+    track.count = (int32_t*)at(ws, L.count);
+    track.last = (int32_t*)at(ws, L.last);
+    track.bias_step = opts->bias_step;
+    track.stats = opts->layer_stats;
+  }
+  int sparse_index = 0, block = -1, in_block = 0;
+  for (int l = 0; l < n_layers;) {
+    if (is_sparse(l)) {
+      if (l == 0 || !is_sparse(l - 1)) {   // a new block
+        ++block;
+        in_block = 0;
+        if (tracked) {   // clear the bias state
+          if (cudaMemsetAsync(track.count, 0, 4 * BT, c.stream) != cudaSuccess) return XMOD_ERR_CUDA;
+          if (cudaMemsetAsync(track.last, 0x80, 4 * BT, c.stream) != cudaSuccess) return XMOD_ERR_CUDA;
+        }
+      }
+      // the sparse layers up to the next dense one, at most kRouterRun at a time
+      int count = 1;
+      if (runs)
+        while (count < kRouterRun && l + count < n_layers && is_sparse(l + count)) ++count;
+      RouteTrack tl = track;
+      tl.layer = sparse_index;
+      if (tl.stats) tl.stats += (int64_t)sparse_index * dm->B * 4;
+      if (runs)
+        st = sparse_run(c, dm, L, ws, K, gate, &layers[l], count, x_inout, bias, nullptr, nullptr,
+                        tracked ? &tl : nullptr, threshold);
+      else
+        st = layer_impl(dm, XMOD_LAYER_SPARSE, K, gate, &layers[l], x_inout, bias, nullptr,
+                        nullptr, ws, L, stream, tracked ? &tl : nullptr);
+      if (st) return st;
+      l += count;
+      sparse_index += count;
+      in_block += count;
+      if (tracked && opts->update_hist && (l == n_layers || !is_sparse(l)))   // block ends
+        XMOD_RUN("update_hist",
+                 launch_count_hist(c, dm->B, dm->T, max_block, track.count,
+                                   opts->update_hist + (int64_t)block * dm->B * (max_block + 1)));
+      continue;
+    }
+    st = layer_impl(dm, XMOD_LAYER_DENSE, K, gate, &layers[l], x_inout, bias, nullptr, nullptr, ws,
+                    L, stream);
+    if (st) return st;
+    ++l;
+  }
+  return XMOD_OK;
+}
+
 }  // namespace
 }  // namespace xmod
 
@@ -576,79 +662,29 @@ int xmod_stack_fwd_ex(const xmod_dims* dm, int K, double A, int N0, int N1, xmod
                       const float* bias, const xmod_stack_opts* opts, void* ws, size_t ws_bytes,
                       void* stream) {
   if (!dims_ok(dm) || K <= 0 || K > dm->T || N0 < 0 || N1 < 0 || !layers) return XMOD_ERR_INVALID_ARG;
-  if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
   if (!isfinite(A) || A <= 0) return XMOD_ERR_INVALID_ARG;
   const double akd = A * (double)K;
   const long AK = lround(akd);
   if (AK < 1 || fabs(akd - (double)AK) > 1e-9) return XMOD_ERR_INVALID_ARG;
   if ((long)n_layers != (long)N0 + (long)N1 * (AK + 1)) return XMOD_ERR_INVALID_ARG;
-  if (!aligned16(x_inout) || !aligned16_or_null(bias)) return XMOD_ERR_INVALID_ARG;
-  if (opts && (!isfinite(opts->bias_step) || opts->bias_step < 0.0f)) return XMOD_ERR_INVALID_ARG;
-  if (opts && (((uintptr_t)opts->layer_stats & 3) || ((uintptr_t)opts->update_hist & 3)))
-    return XMOD_ERR_INVALID_ARG;
-  if (opts && opts->routing != XMOD_ROUTE_TOPK && opts->routing != XMOD_ROUTE_THRESHOLD)
-    return XMOD_ERR_INVALID_ARG;
-  const bool threshold = opts && opts->routing == XMOD_ROUTE_THRESHOLD;
   // Eq. 3 order: N0 dense, then N1 blocks of AK sparse layers and one dense anchor.
-  auto is_sparse = [&](int l) { return l >= N0 && ((l - N0) % (AK + 1)) < AK; };
+  std::vector<int32_t> kinds(n_layers);
   for (int l = 0; l < n_layers; ++l)
-    if (!weights_ok(&layers[l], is_sparse(l))) return XMOD_ERR_INVALID_ARG;
-  if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
-  if (N1 > 0 && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
-  int st = check_ws(dm, K, ws, ws_bytes);
-  if (st) return st;
-  const Layout L = layout(dm, K);
-  const bool runs = sparse_run_supported(dm, ws, L);
-  if (threshold && !threshold_supported(dm, ws, L)) return XMOD_ERR_UNSUPPORTED;
-  Ctx c{(cudaStream_t)stream, (int*)at(ws, L.status)};
-  const int64_t BT = (int64_t)dm->B * dm->T;
-  // Token-choice bias state, only when an option needs it (else the plain top-k).
-  const bool tracked = opts && (opts->bias_step != 0.0f || opts->layer_stats || opts->update_hist);
-  RouteTrack track;
-  if (tracked) {
-    track.count = (int32_t*)at(ws, L.count);
-    track.last = (int32_t*)at(ws, L.last);
-    track.bias_step = opts->bias_step;
-    track.stats = opts->layer_stats;
-  }
-  int sparse_index = 0;
-  for (int l = 0; l < n_layers;) {
-    if (is_sparse(l)) {
-      const int in_block = (l - N0) % (AK + 1);   // position inside its sparse-dense block
-      if (tracked && in_block == 0) {   // a new block: clear the bias state
-        if (cudaMemsetAsync(track.count, 0, 4 * BT, c.stream) != cudaSuccess) return XMOD_ERR_CUDA;
-        if (cudaMemsetAsync(track.last, 0x80, 4 * BT, c.stream) != cudaSuccess) return XMOD_ERR_CUDA;
-      }
-      // the sparse layers up to the next dense one, at most kRouterRun at a time
-      int count = 1;
-      if (runs)
-        while (count < kRouterRun && l + count < n_layers && is_sparse(l + count)) ++count;
-      RouteTrack tl = track;
-      tl.layer = sparse_index;
-      if (tl.stats) tl.stats += (int64_t)sparse_index * dm->B * 4;
-      if (runs)
-        st = sparse_run(c, dm, L, ws, K, gate, &layers[l], count, x_inout, bias, nullptr, nullptr,
-                        tracked ? &tl : nullptr, threshold);
-      else
-        st = layer_impl(dm, XMOD_LAYER_SPARSE, K, gate, &layers[l], x_inout, bias, nullptr,
-                        nullptr, ws, L, (cudaStream_t)stream, tracked ? &tl : nullptr);
-      if (st) return st;
-      l += count;
-      sparse_index += count;
-      if (tracked && opts->update_hist && in_block + count == AK) {   // the block's last sparse layer
-        const int block = (l - 1 - N0) / (AK + 1);
-        XMOD_RUN("update_hist",
-                 launch_count_hist(c, dm->B, dm->T, (int)AK, track.count,
-                                   opts->update_hist + (int64_t)block * dm->B * (AK + 1)));
-      }
-      continue;
-    }
-    st = layer_impl(dm, XMOD_LAYER_DENSE, K, gate, &layers[l], x_inout, bias, nullptr, nullptr, ws,
-                    L, (cudaStream_t)stream);
-    if (st) return st;
-    ++l;
-  }
-  return XMOD_OK;
+    kinds[l] = (l >= N0 && ((l - N0) % (AK + 1)) < AK) ? XMOD_LAYER_SPARSE : XMOD_LAYER_DENSE;
+  return stack_impl(dm, K, kinds.data(), n_layers, gate, layers, x_inout, bias, opts, ws, ws_bytes,
+                    (cudaStream_t)stream);
+}
+
+int xmod_stack_fwd_sched(const xmod_dims* dm, int K, const int32_t* kinds, int n_layers,
+                         xmod_gate gate, const xmod_layer_weights* layers, void* x_inout,
+                         const float* bias, const xmod_stack_opts* opts, void* ws,
+                         size_t ws_bytes, void* stream) {
+  if (!dims_ok(dm) || K <= 0 || K > dm->T || !kinds || n_layers < 0 || !layers)
+    return XMOD_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l)
+    if (kinds[l] != XMOD_LAYER_DENSE && kinds[l] != XMOD_LAYER_SPARSE) return XMOD_ERR_INVALID_ARG;
+  return stack_impl(dm, K, kinds, n_layers, gate, layers, x_inout, bias, opts, ws, ws_bytes,
+                    (cudaStream_t)stream);
 }
 
 }  // extern "C"

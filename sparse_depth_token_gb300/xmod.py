@@ -23,7 +23,7 @@ EXPORTS = ("xmod_version", "xmod_status_string", "xmod_workspace_bytes", "xmod_r
            "xmod_sync_status", "xmod_router_topk", "xmod_topk", "xmod_gather", "xmod_block_fwd",
            "xmod_gated_scatter", "xmod_layer_fwd", "xmod_stack_fwd", "xmod_launch_count",
            "xmod_profile_enable", "xmod_profile_read", "xmod_router_topk_noalloc",
-           "xmod_stack_fwd_ex", "xmod_layer_fwd_threshold")
+           "xmod_stack_fwd_ex", "xmod_layer_fwd_threshold", "xmod_stack_fwd_sched")
 
 # Largest B*T the allocation-free router entry point accepts (its fixed scratch).
 NOALLOC_MAX_TOKENS = 2 * 1024 * 1024
@@ -105,6 +105,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.POINTER(LayerWeights), ctypes.c_int, _VP, _VP,
                                     ctypes.POINTER(StackOpts), _VP, ctypes.c_size_t, _VP]
+    L.xmod_stack_fwd_sched.argtypes = [ctypes.POINTER(Dims), ctypes.c_int,
+                                       ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_int,
+                                       ctypes.POINTER(LayerWeights), _VP, _VP,
+                                       ctypes.POINTER(StackOpts), _VP, ctypes.c_size_t, _VP]
     L.xmod_layer_fwd_threshold.argtypes = [ctypes.POINTER(Dims), ctypes.c_int,
                                            ctypes.POINTER(LayerWeights), _VP, _VP, _VP, _VP,
                                            ctypes.c_size_t, _VP]
@@ -231,6 +235,18 @@ def stack_fwd_ex(dm, K, A, N0, N1, gate, layers, x, bias, ws, bias_step=0.0, lay
     _check("xmod_stack_fwd_ex", load().xmod_stack_fwd_ex(
         ctypes.byref(dm), int(K), float(A), int(N0), int(N1), int(gate), arr, len(layers), _p(x),
         _p(bias), ctypes.byref(opts), _p(ws), _wsb(ws), _stream(stream)))
+
+
+def stack_fwd_sched(dm, K, kinds, gate, layers, x, bias, ws, bias_step=0.0, layer_stats=None,
+                    update_hist=None, routing=ROUTE_TOPK, stream=None):
+    """xmod_stack_fwd_sched: the stack in an explicit layer order (kinds: DENSE / SPARSE
+    per layer), e.g. the segment stacks of X-MoD notes Eq. 35 / 36."""
+    arr = (LayerWeights * len(layers))(*layers)
+    ks = (ctypes.c_int32 * len(kinds))(*[int(k) for k in kinds])
+    opts = StackOpts(float(bias_step), _p(layer_stats), _p(update_hist), int(routing))
+    _check("xmod_stack_fwd_sched", load().xmod_stack_fwd_sched(
+        ctypes.byref(dm), int(K), ks, len(kinds), int(gate), arr, _p(x), _p(bias),
+        ctypes.byref(opts), _p(ws), _wsb(ws), _stream(stream)))
 
 
 def layer_fwd_threshold(dm, gate, w, x, bias, ws, count_out=None, stream=None):
