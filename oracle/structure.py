@@ -7,11 +7,14 @@ Mixture-of-Depths" reading notes --
   Eq. 3   X-MoD stack [Dense] x N0 + ([Sparse(K)] x AK + [Dense]) x N1
   Eq. 4   total parameters N = N_layer (N0 + N1 (1 + AK))
   Eq. 5   active-equivalent parameters N_act = N_layer (N0 + N1 (1 + A))
-  Eq. 34-36, Table 6, Table 9: the concrete stacks and their sizes.
+  Eq. 34-36, Table 6, Table 9: the concrete stacks and their sizes;
+  "mechanism controls", Table 2 / Table 7: the Routed-FFN variant, where each group of
+  K routed layers keeps its FFN only and one full-sequence attention module serves the
+  group: ([FullAttn] + [Routed-FFN] x K) x A between the dense anchors.
 """
 from fractions import Fraction
 
-DENSE, SPARSE = 0, 1
+DENSE, SPARSE, ATTN, RFFN = 0, 1, 2, 3
 
 
 def _ak(A, K) -> int:
@@ -34,6 +37,28 @@ def schedule_segments(N0: int, segments) -> list:
     for ak, reps in segments:
         kinds += ([SPARSE] * int(ak) + [DENSE]) * int(reps)
     return kinds
+
+
+def schedule_routed_ffn(N0: int, segments, K: int) -> list:
+    """The Routed-FFN counterpart of schedule_segments: every segment (AK, repeats)
+    becomes (([FullAttn] + [Routed-FFN] x K) x A + [Dense]) x repeats, A = AK / K."""
+    kinds = [DENSE] * N0
+    for ak, reps in segments:
+        A, rem = divmod(int(ak), K)
+        if rem:
+            raise ValueError("a Routed-FFN segment needs AK divisible by K")
+        kinds += (([ATTN] + [RFFN] * K) * A + [DENSE]) * int(reps)
+    return kinds
+
+
+def attention_modules(kinds) -> int:
+    """Full-sequence attention modules: the dense anchors' and the FullAttn layers'."""
+    return sum(1 for k in kinds if k in (DENSE, ATTN))
+
+
+def ffn_depth(kinds) -> int:
+    """Depth counted by FFN layers (Table 7 counts the Routed-FFN variants this way)."""
+    return sum(1 for k in kinds if k in (DENSE, SPARSE, RFFN))
 
 
 def physical_layers(kinds) -> int:
@@ -64,10 +89,13 @@ def eq5_active(N_layer, N0, N1, A):
     return N_layer * (N0 + N1 * (1 + Fraction(A)))
 
 
-def layer_params(d, hq, hkv, hd, F, router=False) -> int:
+def layer_params(d, hq, hkv, hd, F, router=False, kind=DENSE) -> int:
     """Parameters of one block as the oracle's block uses them: Wq, Wk, Wv, Wo,
-    SwiGLU (gate, up, down), two RMSNorm gains, plus the router vector if asked."""
-    p = d * hq * hd + 2 * d * hkv * hd + hq * hd * d + 3 * d * F + 2 * d
+    SwiGLU (gate, up, down), two RMSNorm gains, plus the router vector if asked.
+    kind ATTN keeps the attention half (and its gain), RFFN the FFN half."""
+    att = d * hq * hd + 2 * d * hkv * hd + hq * hd * d + d
+    ffn = 3 * d * F + d
+    p = att if kind == ATTN else ffn if kind == RFFN else att + ffn
     return p + (d if router else 0)
 
 
@@ -75,6 +103,6 @@ def model_params(kinds, d, hq, hkv, hd, F, vocab=0, tied=False, router=False) ->
     """Total parameters of a stack plus (un)tied input/output embeddings."""
     n = 0
     for k in kinds:
-        n += layer_params(d, hq, hkv, hd, F, router=(router and k == SPARSE))
+        n += layer_params(d, hq, hkv, hd, F, router=(router and k in (SPARSE, RFFN)), kind=k)
     n += (1 if tied else 2) * vocab * d
     return n

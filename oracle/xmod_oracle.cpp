@@ -58,7 +58,10 @@ typedef struct {
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_NONFINITE = -5 };
 enum { ORACLE_GATE_XMOD = 0, ORACLE_GATE_MOD = 1 };
-enum { ORACLE_DENSE = 0, ORACLE_SPARSE = 1 };
+// Layer kinds. ATTN and RFFN are the two halves of the Routed-FFN variant of X-MoD
+// notes "mechanism controls" (Table 2 / Table 7): attention over the full sequence with
+// its residual, and an FFN-only refinement applied to the top-(T/K) tokens.
+enum { ORACLE_DENSE = 0, ORACLE_SPARSE = 1, ORACLE_ATTN = 2, ORACLE_RFFN = 3 };
 
 int oracle_num_threads(void) {
 #ifdef _OPENMP
@@ -269,10 +272,28 @@ void oracle_block_rows(const oracle_dims* dm, int n, const double* xs,
   oracle_linear(nr, F, d, hid.data(), w->wd, f_out);
 }
 
+// FFN of the block without attention, on nr rows xs [nr, d]:
+//   f = W_down(silu(W_gate v2) * (W_up v2)), v2 = RMSNorm(xs) * g2.
+void oracle_ffn_rows(const oracle_dims* dm, int nr, const double* xs, const oracle_layer_w* w,
+                     double* f_out) {
+  const int d = dm->d, F = dm->F;
+  if (nr <= 0) return;
+  std::vector<double> v2((int64_t)nr * d);
+  oracle_rmsnorm(nr, d, xs, w->g2, dm->eps, v2.data());
+  std::vector<double> g((int64_t)nr * F), up((int64_t)nr * F), hid((int64_t)nr * F);
+  oracle_linear(nr, d, F, v2.data(), w->wg, g.data());
+  oracle_linear(nr, d, F, v2.data(), w->wu, up.data());
+  for (int64_t i = 0; i < (int64_t)nr * F; ++i) hid[i] = silu(g[i]) * up[i];
+  oracle_linear(nr, F, d, hid.data(), w->wd, f_out);
+}
+
 // One layer of the stack on x_in [B, T, d] -> y [B, T, d].
 //   sparse: router (Eq. 8) -> top-(T/K) -> gather -> block -> gated residual
 //           (Eq. 7 if gate == XMOD, Eq. 6 if gate == MOD); unselected rows y = x.
 //   dense:  block on all T tokens, y = x + a + f.
+//   attn:   attention half of the block on all T tokens, y = x + a.
+//   rffn:   router -> top-(T/K) -> gather -> FFN half on the selected tokens ->
+//           gated residual with a = 0 (Eq. 7: x + varsigma r f; Eq. 6: x + r f).
 // Optional arguments:
 //   bias      [B, T]  signed per-token router bias, added to the logit;
 //   s_out     [B, T]  router logits; r_out [B, T] gates;
@@ -291,7 +312,7 @@ int oracle_layer_fwd(const oracle_dims* dm, int kind, int K, int gate,
   if (B <= 0 || T <= 0 || d <= 0 || dm->hq % dm->hkv != 0) return ORACLE_BAD_ARG;
   const int64_t BT = (int64_t)B * T;
   std::memcpy(y, x_in, sizeof(double) * BT * d);
-  if (kind == ORACLE_DENSE) {
+  if (kind == ORACLE_DENSE || kind == ORACLE_ATTN) {
     for (int b = 0; b < B; ++b) {
       std::vector<int32_t> rows;
       for (int t = 0; t < T; ++t)
@@ -303,12 +324,12 @@ int oracle_layer_fwd(const oracle_dims* dm, int kind, int K, int gate,
       for (size_t i = 0; i < rows.size(); ++i)
         for (int c = 0; c < d; ++c) {
           const int64_t o = ((int64_t)b * T + rows[i]) * d + c;
-          y[o] = x_in[o] + a[i * d + c] + f[i * d + c];
+          y[o] = kind == ORACLE_ATTN ? x_in[o] + a[i * d + c] : x_in[o] + a[i * d + c] + f[i * d + c];
         }
     }
     return ORACLE_OK;
   }
-  if (kind != ORACLE_SPARSE || K <= 0) return ORACLE_BAD_ARG;
+  if ((kind != ORACLE_SPARSE && kind != ORACLE_RFFN) || K <= 0) return ORACLE_BAD_ARG;
   const int n = T / K;
   if (n <= 0) return ORACLE_BAD_ARG;
   std::vector<double> s(BT), r(BT);
@@ -343,8 +364,15 @@ int oracle_layer_fwd(const oracle_dims* dm, int kind, int K, int gate,
     for (int j = 0; j < n; ++j)
       if (!row_mask || row_mask[(int64_t)b * T + idx[(int64_t)b * n + j]]) rows.push_back(j);
     if (rows.empty()) continue;
-    std::vector<double> a(rows.size() * (size_t)d), f(rows.size() * (size_t)d);
-    oracle_block_rows(dm, n, xs.data(), w, rows.data(), (int)rows.size(), a.data(), f.data());
+    std::vector<double> a(rows.size() * (size_t)d, 0.0), f(rows.size() * (size_t)d);
+    if (kind == ORACLE_RFFN) {   // FFN only, row by row: attention context plays no part
+      std::vector<double> xr(rows.size() * (size_t)d);
+      for (size_t i = 0; i < rows.size(); ++i)
+        std::memcpy(&xr[i * d], &xs[(int64_t)rows[i] * d], sizeof(double) * d);
+      oracle_ffn_rows(dm, (int)rows.size(), xr.data(), w, f.data());
+    } else {
+      oracle_block_rows(dm, n, xs.data(), w, rows.data(), (int)rows.size(), a.data(), f.data());
+    }
     for (size_t i = 0; i < rows.size(); ++i) {
       const int j = rows[i];
       const int t = idx[(int64_t)b * n + j];
@@ -460,12 +488,13 @@ int oracle_stack_dyn(const oracle_dims* dm, int K, int gate, int n_layers, const
   std::vector<int32_t> count(BT, 0), idx((int64_t)dm->B * (n > 0 ? n : 1)), mask(BT);
   int ls = 0;
   for (int l = 0; l < n_layers; ++l) {
-    const bool sparse = kinds[l] == ORACLE_SPARSE;
+    const bool sparse = kinds[l] == ORACLE_SPARSE || kinds[l] == ORACLE_RFFN;   // routed
     if (sparse)
       for (int64_t i = 0; i < BT; ++i)
         bias[i] = (bias0 ? bias0[i] : 0.0) - bias_step * (double)count[i];
     int st;
     if (sparse && routing == 1) {
+      if (kinds[l] != ORACLE_SPARSE) return ORACLE_BAD_ARG;
       st = oracle_layer_threshold(dm, gate, &layers[l], x, bias.data(), y.data(), s.data(),
                                   mask.data());
     } else {
@@ -485,7 +514,7 @@ int oracle_stack_dyn(const oracle_dims* dm, int K, int gate, int n_layers, const
       if (idx_out) std::memcpy(idx_out + (int64_t)ls * dm->B * n, idx.data(), sizeof(int32_t) * dm->B * n);
       if (s_out) std::memcpy(s_out + (int64_t)ls * BT, s.data(), sizeof(double) * BT);
       ++ls;
-    } else {
+    } else if (kinds[l] == ORACLE_DENSE) {
       std::fill(count.begin(), count.end(), 0);   // the dense anchor clears the bias
     }
     if (mirror_bf16)

@@ -105,3 +105,23 @@ def test_router_params_negligible():
     a = S.model_params(kinds, d, hq, hkv, hd, F, vocab=50257)
     b = S.model_params(kinds, d, hq, hkv, hd, F, vocab=50257, router=True)
     assert 0 < (b - a) / a < 1e-3
+
+
+@pytest.mark.parametrize("row", GOLD["routed_ffn"], ids=lambda r: r["name"])
+def test_routed_ffn_structure(row):
+    """The Routed-FFN control keeps the X-MoD stack's segments, each group of K routed
+    layers sharing one full-sequence attention module: the printed module counts and
+    FFN depth follow exactly; the printed totals sit within 0.5% of the weight-set
+    formula (the page's rounding or parameter accounting differs) and are recorded as
+    mismatches."""
+    base = next(s for s in GOLD["stacks"] if s["name"] == row["like"])
+    kinds = S.schedule_routed_ffn(base["N0"], base["segments"], base["K"])
+    assert S.attention_modules(kinds) == row["attention_modules"]
+    assert sum(1 for k in kinds if k == S.RFFN) == row["routed_ffn"]
+    assert S.ffn_depth(kinds) == row["ffn_depth"]
+    d, hq, hkv, hd, F = _backbone("936M")
+    n = S.model_params(kinds, d, hq, hkv, hd, F, vocab=GOLD["backbones"]["vocab"])
+    printed = row["printed_B"]
+    agrees = round(n / 1e9, 2) == printed
+    assert agrees != row["mismatch"]
+    assert abs(n / 1e9 - printed) / printed < 0.005
