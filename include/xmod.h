@@ -62,7 +62,20 @@ typedef enum { XMOD_BF16 = 0, XMOD_FP32 = 1 } xmod_dtype;
 /* Residual gate: Eq. 7 (X-MoD) x + varsigma * r * (a + f); Eq. 6 (MoD) x + a + r * f. */
 typedef enum { XMOD_GATE_XMOD = 0, XMOD_GATE_MOD = 1 } xmod_gate;
 
-typedef enum { XMOD_LAYER_DENSE = 0, XMOD_LAYER_SPARSE = 1 } xmod_layer_kind;
+/* Layer kinds. DENSE: the block on every token. SPARSE: the block on the routed tokens.
+ * ATTN and ROUTED_FFN are the two halves of the Routed-FFN variant of X-MoD notes
+ * "mechanism controls" (Table 2, Table 7; ([FullAttn] + [Routed-FFN] x K) x A between
+ * dense anchors): ATTN is the attention half on every token, x += a (weights used:
+ * rms1, wq, wk, wv, wo); ROUTED_FFN routes top-(T/K) tokens through the FFN half only,
+ * f = FFN(RMSNorm(x) * rms2), with the gated residual taken with a = 0 (Eq. 7:
+ * x + varsigma r f; Eq. 6: x + r f) (weights used: w_router, rms2, w_gate, w_up,
+ * w_down, varsigma). Weights a kind does not use may be NULL. */
+typedef enum {
+  XMOD_LAYER_DENSE = 0,
+  XMOD_LAYER_SPARSE = 1,
+  XMOD_LAYER_ATTN = 2,
+  XMOD_LAYER_ROUTED_FFN = 3
+} xmod_layer_kind;
 
 /* Problem sizes in the pages' notation: B sequences of T tokens, model width d,
  * n_heads query heads and n_kv_heads key/value heads of head_dim (GQA), SwiGLU
@@ -190,13 +203,14 @@ XMOD_API int xmod_layer_fwd_threshold(const xmod_dims* dims, xmod_gate gate,
  *     s_i = w_r . x_i + bias_i - bias_step * c_i,
  *   c_i = how many earlier sparse layers of the block selected token i. 0 gives the
  *   constant-bias stack of xmod_stack_fwd; must be finite and >= 0.
- * layer_stats: NULL or device int32 [n_sparse, B, 4], per sparse layer (stack order)
- *   and sequence: tokens selected (T / K); tokens whose ranked logit is >= 0 (the
+ * layer_stats: NULL or device int32 [n_sparse, B, 4], per routed layer (SPARSE or
+ *   ROUTED_FFN, stack order) and sequence: tokens selected (T / K); tokens whose ranked logit is >= 0 (the
  *   causal threshold rule r >= 1/2 of X-MoD notes "top-k in training, causal threshold
  *   at evaluation"); tokens on which the two rules agree (both select or both skip);
  *   selected tokens that the previous sparse layer of the block also selected.
- * update_hist: NULL or device int32 [N1, B, AK + 1]: for each sparse-dense block and
- *   sequence, how many tokens the block's AK sparse layers updated 0, 1, ..., AK times.
+ * update_hist: NULL or device int32 [N1, B, AK + 1]: for each sparse-dense block (the
+ *   routed layers between two dense layers) and sequence, how many tokens the block's
+ *   AK routed layers updated 0, 1, ..., AK times.
  * These are the inputs of the routing diagnostics of X-MoD notes Table 10 (coverage,
  * adjacent-layer Jaccard overlap, threshold / top-k mask agreement, update counts).
  * Under THRESHOLD routing the selected count is the threshold count and every
@@ -217,11 +231,12 @@ XMOD_API int xmod_stack_fwd_ex(const xmod_dims* dims, int K, double A, int N0, i
                                void* ws, size_t ws_bytes, void* stream);
 
 /* A stack in an explicit layer order: kinds (host array of n_layers values,
- * XMOD_LAYER_DENSE or XMOD_LAYER_SPARSE) and `layers` in execution order. This is
+ * an xmod_layer_kind) and `layers` in execution order. This is
  * how the heterogeneous segment stacks of X-MoD notes Eq. 35 and Eq. 36 (a shorter
- * first sparse segment, then A4K8 / A3K16 segments) and MoD's Eq. 34 run. Blocks are
- * the maximal runs of consecutive sparse layers; each sparse layer selects T / K
- * tokens (or follows opts->routing). With opts->update_hist the histogram has one
+ * first sparse segment, then A4K8 / A3K16 segments), MoD's Eq. 34 and the Routed-FFN
+ * control (([ATTN] + [ROUTED_FFN] x K) x A between dense anchors) run. A block is the
+ * set of routed layers between two dense layers; each routed layer selects T / K
+ * tokens (or follows opts->routing; THRESHOLD with ROUTED_FFN is unsupported). With opts->update_hist the histogram has one
  * [B, L_max + 1] slab per block, L_max the longest block; layer_stats is as for
  * xmod_stack_fwd_ex. opts may be NULL. */
 XMOD_API int xmod_stack_fwd_sched(const xmod_dims* dims, int K, const int32_t* kinds,

@@ -103,12 +103,23 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? XMOD_OK : XMOD_ERR_CU
     if (_e != cudaSuccess) return XMOD_ERR_CUDA;     \
   } while (0)
 
-bool weights_ok(const xmod_layer_weights* w, bool need_router) {
-  if (!w) return false;
-  if (need_router && !aligned16(w->w_router)) return false;
-  const void* ps[] = {w->rms1, w->wq, w->wk, w->wv, w->wo, w->rms2, w->w_gate, w->w_up, w->w_down};
-  for (const void* p : ps)
-    if (!aligned16(p)) return false;
+bool routed(int kind) { return kind == XMOD_LAYER_SPARSE || kind == XMOD_LAYER_ROUTED_FFN; }
+bool kind_ok(int kind) { return kind >= XMOD_LAYER_DENSE && kind <= XMOD_LAYER_ROUTED_FFN; }
+
+// The weights a layer kind uses must be present and 16-byte aligned.
+bool weights_ok(const xmod_layer_weights* w, int kind) {
+  if (!w || !kind_ok(kind)) return false;
+  if (routed(kind) && !aligned16(w->w_router)) return false;
+  if (kind != XMOD_LAYER_ROUTED_FFN) {
+    const void* ps[] = {w->rms1, w->wq, w->wk, w->wv, w->wo};
+    for (const void* p : ps)
+      if (!aligned16(p)) return false;
+  }
+  if (kind != XMOD_LAYER_ATTN) {
+    const void* ps[] = {w->rms2, w->w_gate, w->w_up, w->w_down};
+    for (const void* p : ps)
+      if (!aligned16(p)) return false;
+  }
   return isfinite(w->varsigma);
 }
 
@@ -127,10 +138,15 @@ struct Ragged {
 // With scatter, xs_new (if not NULL) receives the updated compact rows [B*n, d].
 // With rg (threshold routing), n is T: buffers are sized for every token, kernels
 // compute the rows the routing picked (tensor-core path only).
+// Which part of the block runs: all of it, the attention half (its residual written
+// straight into the stream: x += a, for ATTN layers), or the FFN half on RMSNorm(x) *
+// rms2 with a = 0 (ROUTED_FFN layers).
+enum BlockPart { PART_ALL = 0, PART_ATTN = 1, PART_FFN = 2 };
+
 int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int n,
               const void* x_src, const int32_t* idx, const xmod_layer_weights* w, void* a_out,
               void* f_out, bool scatter, void* x_inout, const float* r_sel, int gate,
-              void* xs_new = nullptr, const Ragged* rg = nullptr) {
+              void* xs_new = nullptr, const Ragged* rg = nullptr, int part = PART_ALL) {
   const xmod_dtype dt = dm->dtype;
   const int B = dm->B, T = dm->T, d = dm->d, hq = dm->n_heads, hkv = dm->n_kv_heads,
             hd = dm->head_dim, F = dm->d_ff;
@@ -143,92 +159,115 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   char* o = at(ws, L.o);
   char* h = at(ws, L.h);
   char* hidden = at(ws, L.hidden);
-  // 1. gather + RMSNorm1
+  const bool tc = dt == XMOD_BF16;
+  char* v2 = u;   // RMSNorm2 output, in the buffer of u (consumed by the q/k/v projection)
+  const float* h_in = (const float*)h;   // h = x_sel + a for the down projection
   RowMap rm;
   if (rg) {
     rm.tok = rg->tok;
     rm.M_dev = M_dev;
   }
-  XMOD_RUN("gather_rmsnorm",
-           launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms1, dm->rms_eps, u, rm));
-  // 2. q, k, v projections into one [M, qkv_w] buffer
-  const bool tc = dt == XMOD_BF16;
-  char* vt = at(ws, L.vt);
-  const bool tc_attn = tc && attention_tc_supported(hd, n, qkv_w);
-  Epilogue e;
-  e.kind = EPI_STORE;
-  e.ldo = qkv_w;
-  e.out = qkv;
-  if (tc_attn) {  // v goes straight to its transposed layout
-    e.vt = vt;
-    e.vt_col0 = qw + kw;
-    e.vt_hd = hd;
-    e.vt_hkv = hkv;
-    e.vt_ld = vt_ld(n);
-    e.n_per_seq = n;
-  }
-  GemmTcProblem pq;
-  pq.M = M; pq.N = qkv_w; pq.K = d; pq.A = u; pq.lda = d; pq.ldb = d;
-  pq.B[0] = w->wq; pq.B[1] = w->wk; pq.B[2] = w->wv; pq.nB = 3;
-  pq.split[0] = qw; pq.split[1] = qw + kw;
-  const bool tc_qkv = tc && gemm_tc_supported(pq, e);
-  if (rg) {
-    if (!tc_qkv || !tc_attn) return XMOD_ERR_UNSUPPORTED;
-    e.tok = rg->tok;
-    e.seq_off = rg->seq_off;
-    e.T = T;
-    pq.M_dev = M_dev;
-    // keys past a sequence's count are read (and multiplied by zero weights): keep
-    // them finite
-    if (cudaMemsetAsync(vt, 0, es * (size_t)B * hkv * hd * vt_ld(n), c.stream) != cudaSuccess)
-      return XMOD_ERR_CUDA;
-  }
-  if (tc_qkv) {
-    XMOD_RUN("gemm_qkv", launch_gemm_tc(c, pq, e));
+  if (part == PART_FFN) {   // FFN half only: v2 = RMSNorm(x_sel) * rms2, a = 0
+    XMOD_RUN("gather_rmsnorm",
+             launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms2, dm->rms_eps, v2, rm));
+    h_in = nullptr;
   } else {
-    e.vt = nullptr;
-    XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, qw, d, u, d, w->wq, d, nullptr, e));
-    e.out = qkv + es * qw;
-    XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wk, d, nullptr, e));
-    e.out = qkv + es * (qw + kw);
-    XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wv, d, nullptr, e));
+    // 1. gather + RMSNorm1
+    XMOD_RUN("gather_rmsnorm",
+             launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms1, dm->rms_eps, u, rm));
+    // 2. q, k, v projections into one [M, qkv_w] buffer
+    char* vt = at(ws, L.vt);
+    const bool tc_attn = tc && attention_tc_supported(hd, n, qkv_w);
+    Epilogue e;
+    e.kind = EPI_STORE;
+    e.ldo = qkv_w;
+    e.out = qkv;
+    if (tc_attn) {  // v goes straight to its transposed layout
+      e.vt = vt;
+      e.vt_col0 = qw + kw;
+      e.vt_hd = hd;
+      e.vt_hkv = hkv;
+      e.vt_ld = vt_ld(n);
+      e.n_per_seq = n;
+    }
+    GemmTcProblem pq;
+    pq.M = M; pq.N = qkv_w; pq.K = d; pq.A = u; pq.lda = d; pq.ldb = d;
+    pq.B[0] = w->wq; pq.B[1] = w->wk; pq.B[2] = w->wv; pq.nB = 3;
+    pq.split[0] = qw; pq.split[1] = qw + kw;
+    const bool tc_qkv = tc && gemm_tc_supported(pq, e);
+    if (rg) {
+      if (!tc_qkv || !tc_attn) return XMOD_ERR_UNSUPPORTED;
+      e.tok = rg->tok;
+      e.seq_off = rg->seq_off;
+      e.T = T;
+      pq.M_dev = M_dev;
+      // keys past a sequence's count are read (and multiplied by zero weights): keep
+      // them finite
+      if (cudaMemsetAsync(vt, 0, es * (size_t)B * hkv * hd * vt_ld(n), c.stream) != cudaSuccess)
+        return XMOD_ERR_CUDA;
+    }
+    if (tc_qkv) {
+      XMOD_RUN("gemm_qkv", launch_gemm_tc(c, pq, e));
+    } else {
+      e.vt = nullptr;
+      XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, qw, d, u, d, w->wq, d, nullptr, e));
+      e.out = qkv + es * qw;
+      XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wk, d, nullptr, e));
+      e.out = qkv + es * (qw + kw);
+      XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wv, d, nullptr, e));
+    }
+    // 3. causal GQA attention among the n rows of each sequence
+    if (tc_qkv && tc_attn)
+      XMOD_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, vt_ld(n), o,
+                                                rg ? rg->seq_count : nullptr,
+                                                rg ? rg->seq_off : nullptr));
+    else
+      XMOD_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w,
+                                                  qkv + es * qw, qkv + es * (qw + kw), qkv_w, o));
+    if (part == PART_ATTN) {   // x += a straight into the stream: the down epilogue's
+      Epilogue ea;            // dense form y = h + f with no h (h = x) and f = a
+      ea.kind = EPI_DOWN_SCATTER;
+      ea.x = x_inout;
+      ea.idx = idx;
+      ea.T = T;
+      ea.n_per_seq = n;
+      ea.d = d;
+      ea.gate = -1;
+      GemmTcProblem pa;
+      pa.M = M; pa.N = d; pa.K = qw; pa.A = o; pa.lda = qw; pa.ldb = qw; pa.B[0] = w->wo;
+      if (tc && gemm_tc_supported(pa, ea))
+        XMOD_RUN("gemm_o_residual", launch_gemm_tc(c, pa, ea));
+      else
+        XMOD_RUN("gemm_o_residual", launch_gemm_simt(c, dt, M, d, qw, o, qw, w->wo, qw, nullptr, ea));
+      return XMOD_OK;
+    }
+    // 4. a = o Wo^T, h = x_sel + a
+    Epilogue eo;
+    eo.kind = EPI_OPROJ;
+    eo.out = a_out;   // the attention residual itself only when the caller asks for it
+    eo.ldo = d;
+    eo.out2 = h;
+    eo.ldo2 = d;
+    eo.x = (void*)x_src;
+    eo.idx = idx;
+    eo.T = T;
+    eo.n_per_seq = n;
+    eo.d = d;
+    GemmTcProblem po;
+    po.M = M; po.N = d; po.K = qw; po.A = o; po.lda = qw; po.ldb = qw; po.B[0] = w->wo;
+    if (rg) {
+      eo.tok = rg->tok;
+      po.M_dev = M_dev;
+      if (!gemm_tc_supported(po, eo)) return XMOD_ERR_UNSUPPORTED;
+    }
+    if (tc && gemm_tc_supported(po, eo))
+      XMOD_RUN("gemm_o_residual", launch_gemm_tc(c, po, eo));
+    else
+      XMOD_RUN("gemm_o_residual", launch_gemm_simt(c, dt, M, d, qw, o, qw, w->wo, qw, nullptr, eo));
+    // 5. v2 = RMSNorm(h) * rms2
+    XMOD_RUN("rmsnorm2", launch_rmsnorm_f32in(c, dt, M, d, (const float*)h, w->rms2, dm->rms_eps,
+                                              v2, M_dev));
   }
-  // 3. causal GQA attention among the n rows of each sequence
-  if (tc_qkv && tc_attn)
-    XMOD_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, vt_ld(n), o,
-                                              rg ? rg->seq_count : nullptr,
-                                              rg ? rg->seq_off : nullptr));
-  else
-    XMOD_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w,
-                                                qkv + es * qw, qkv + es * (qw + kw), qkv_w, o));
-  // 4. a = o Wo^T, h = x_sel + a
-  Epilogue eo;
-  eo.kind = EPI_OPROJ;
-  eo.out = a_out;   // the attention residual itself only when the caller asks for it
-  eo.ldo = d;
-  eo.out2 = h;
-  eo.ldo2 = d;
-  eo.x = (void*)x_src;
-  eo.idx = idx;
-  eo.T = T;
-  eo.n_per_seq = n;
-  eo.d = d;
-  GemmTcProblem po;
-  po.M = M; po.N = d; po.K = qw; po.A = o; po.lda = qw; po.ldb = qw; po.B[0] = w->wo;
-  if (rg) {
-    eo.tok = rg->tok;
-    po.M_dev = M_dev;
-    if (!gemm_tc_supported(po, eo)) return XMOD_ERR_UNSUPPORTED;
-  }
-  if (tc && gemm_tc_supported(po, eo))
-    XMOD_RUN("gemm_o_residual", launch_gemm_tc(c, po, eo));
-  else
-    XMOD_RUN("gemm_o_residual", launch_gemm_simt(c, dt, M, d, qw, o, qw, w->wo, qw, nullptr, eo));
-  // 5. v2 = RMSNorm(h) * rms2
-  // (v2 reuses the buffer of u, which the q/k/v projection has consumed)
-  char* v2 = u;
-  XMOD_RUN("rmsnorm2", launch_rmsnorm_f32in(c, dt, M, d, (const float*)h, w->rms2, dm->rms_eps,
-                                            v2, M_dev));
   // 6. hidden = silu(v2 Wg^T) * (v2 Wu^T)
   Epilogue eg;
   eg.kind = EPI_SWIGLU;
@@ -253,7 +292,7 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
     ed.T = T;
     ed.n_per_seq = n;
     ed.d = d;
-    ed.h = (const float*)h;
+    ed.h = h_in;
     ed.r_sel = r_sel;
     ed.varsigma = w->varsigma;
     ed.gate = gate;
@@ -329,7 +368,7 @@ RouteTrack track_for(const RouteTrack* track, int j, int B) {
 int sparse_run(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int K,
                xmod_gate gate, const xmod_layer_weights* lw, int count, void* x,
                const float* bias, int32_t* idx_out = nullptr, float* r_sel_out = nullptr,
-               const RouteTrack* track = nullptr, bool threshold = false) {
+               const RouteTrack* track = nullptr, bool threshold = false, int part = PART_ALL) {
   const int B = dm->B, T = dm->T, d = dm->d, n = threshold ? T : T / K;
   const int64_t BT = (int64_t)B * T;
   float* S = (float*)at(ws, L.s);
@@ -358,7 +397,7 @@ int sparse_run(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int
     const bool refresh = j + 1 < count;
     const int st = run_block(c, dm, L, ws, n, x, threshold ? nullptr : idx, &lw[j], nullptr,
                              nullptr, true, x, r_sel, (int)gate, refresh ? xs_new : nullptr,
-                             threshold ? &rg : nullptr);
+                             threshold ? &rg : nullptr, part);
     if (st) return st;
     if (refresh) {
       GemmTcProblem p = router_problem(dm, B * n, xs_new, wr + (size_t)(j + 1) * d * 2,
@@ -397,8 +436,13 @@ int layer_impl(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
   Ctx c{stream, (int*)at(ws, L.status)};
   if (kind == XMOD_LAYER_DENSE)
     return run_block(c, dm, L, ws, dm->T, x, nullptr, w, nullptr, nullptr, true, x, nullptr, -1);
+  if (kind == XMOD_LAYER_ATTN)
+    return run_block(c, dm, L, ws, dm->T, x, nullptr, w, nullptr, nullptr, true, x, nullptr, -1,
+                     nullptr, nullptr, PART_ATTN);
+  const int part = kind == XMOD_LAYER_ROUTED_FFN ? PART_FFN : PART_ALL;
   if (sparse_run_supported(dm, ws, L))
-    return sparse_run(c, dm, L, ws, K, gate, w, 1, x, bias, idx_out, r_sel_out, track);
+    return sparse_run(c, dm, L, ws, K, gate, w, 1, x, bias, idx_out, r_sel_out, track, false,
+                      part);
   const int n = dm->T / K;
   float* s = (float*)at(ws, L.s);
   int32_t* idx = idx_out ? idx_out : (int32_t*)at(ws, L.idx);
@@ -406,13 +450,15 @@ int layer_impl(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
   XMOD_RUN("router", launch_router(c, dm->dtype, (int64_t)dm->B * dm->T, dm->d, x, w->w_router, bias, s,
                          nullptr));
   XMOD_RUN("topk", launch_topk(c, dm->B, dm->T, n, s, idx, r_sel, track));
-  return run_block(c, dm, L, ws, n, x, idx, w, nullptr, nullptr, true, x, r_sel, (int)gate);
+  return run_block(c, dm, L, ws, n, x, idx, w, nullptr, nullptr, true, x, r_sel, (int)gate,
+                   nullptr, nullptr, part);
 }
 
-// A stack in the given layer order. Blocks are the maximal runs of consecutive sparse
-// layers (each ended by a dense layer or the end of the stack); the token-choice bias
-// state is cleared at the start of each, and update_hist has one [B, L_max + 1] slab
-// per block, L_max the longest block.
+// A stack in the given layer order. A block is the set of routed layers (SPARSE or
+// ROUTED_FFN) between two dense layers (or the stack's ends): the token-choice bias
+// state is cleared at its first routed layer, and update_hist has one [B, L_max + 1]
+// slab per block, L_max the most routed layers of a block. Consecutive routed layers
+// of one kind share their router-logit pass (sparse_run).
 int stack_impl(const xmod_dims* dm, int K, const int32_t* kinds, int n_layers, xmod_gate gate,
                const xmod_layer_weights* layers, void* x_inout, const float* bias,
                const xmod_stack_opts* opts, void* ws, size_t ws_bytes, cudaStream_t stream) {
@@ -424,17 +470,29 @@ int stack_impl(const xmod_dims* dm, int K, const int32_t* kinds, int n_layers, x
   if (opts && opts->routing != XMOD_ROUTE_TOPK && opts->routing != XMOD_ROUTE_THRESHOLD)
     return XMOD_ERR_INVALID_ARG;
   const bool threshold = opts && opts->routing == XMOD_ROUTE_THRESHOLD;
-  auto is_sparse = [&](int l) { return kinds[l] == XMOD_LAYER_SPARSE; };
-  bool any_sparse = false;
-  int max_block = 0;
-  for (int l = 0, run = 0; l < n_layers; ++l) {
-    if (!weights_ok(&layers[l], is_sparse(l))) return XMOD_ERR_INVALID_ARG;
-    run = is_sparse(l) ? run + 1 : 0;
-    any_sparse = any_sparse || is_sparse(l);
-    max_block = run > max_block ? run : max_block;
+  // block of each routed layer, and whether it is the block's last routed layer
+  std::vector<int> block_of(n_layers, -1);
+  std::vector<char> block_last(n_layers, 0);
+  bool any_routed = false;
+  int max_block = 0, blocks = 0, in_block = 0, last_routed = -1;
+  for (int l = 0; l < n_layers; ++l) {
+    if (!weights_ok(&layers[l], kinds[l])) return XMOD_ERR_INVALID_ARG;
+    if (threshold && kinds[l] == XMOD_LAYER_ROUTED_FFN) return XMOD_ERR_UNSUPPORTED;
+    if (kinds[l] == XMOD_LAYER_DENSE) {
+      if (last_routed >= 0) block_last[last_routed] = 1;
+      last_routed = -1;
+      in_block = 0;
+    } else if (routed(kinds[l])) {
+      if (last_routed < 0) ++blocks;
+      block_of[l] = blocks - 1;
+      last_routed = l;
+      any_routed = true;
+      max_block = ++in_block > max_block ? in_block : max_block;
+    }
   }
+  if (last_routed >= 0) block_last[last_routed] = 1;
   if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
-  if (any_sparse && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
+  if (any_routed && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
   int st = check_ws(dm, K, ws, ws_bytes);
   if (st) return st;
   const Layout L = layout(dm, K);
@@ -451,44 +509,43 @@ int stack_impl(const xmod_dims* dm, int K, const int32_t* kinds, int n_layers, x
     track.bias_step = opts->bias_step;
     track.stats = opts->layer_stats;
   }
-  int sparse_index = 0, block = -1, in_block = 0;
+  int routed_index = 0, cur_block = -1;
   for (int l = 0; l < n_layers;) {
-    if (is_sparse(l)) {
-      if (l == 0 || !is_sparse(l - 1)) {   // a new block
-        ++block;
-        in_block = 0;
-        if (tracked) {   // clear the bias state
-          if (cudaMemsetAsync(track.count, 0, 4 * BT, c.stream) != cudaSuccess) return XMOD_ERR_CUDA;
-          if (cudaMemsetAsync(track.last, 0x80, 4 * BT, c.stream) != cudaSuccess) return XMOD_ERR_CUDA;
-        }
-      }
-      // the sparse layers up to the next dense one, at most kRouterRun at a time
-      int count = 1;
-      if (runs)
-        while (count < kRouterRun && l + count < n_layers && is_sparse(l + count)) ++count;
-      RouteTrack tl = track;
-      tl.layer = sparse_index;
-      if (tl.stats) tl.stats += (int64_t)sparse_index * dm->B * 4;
-      if (runs)
-        st = sparse_run(c, dm, L, ws, K, gate, &layers[l], count, x_inout, bias, nullptr, nullptr,
-                        tracked ? &tl : nullptr, threshold);
-      else
-        st = layer_impl(dm, XMOD_LAYER_SPARSE, K, gate, &layers[l], x_inout, bias, nullptr,
-                        nullptr, ws, L, stream, tracked ? &tl : nullptr);
+    const int kind = kinds[l];
+    if (!routed(kind)) {
+      st = layer_impl(dm, (xmod_layer_kind)kind, K, gate, &layers[l], x_inout, bias, nullptr,
+                      nullptr, ws, L, stream);
       if (st) return st;
-      l += count;
-      sparse_index += count;
-      in_block += count;
-      if (tracked && opts->update_hist && (l == n_layers || !is_sparse(l)))   // block ends
-        XMOD_RUN("update_hist",
-                 launch_count_hist(c, dm->B, dm->T, max_block, track.count,
-                                   opts->update_hist + (int64_t)block * dm->B * (max_block + 1)));
+      ++l;
       continue;
     }
-    st = layer_impl(dm, XMOD_LAYER_DENSE, K, gate, &layers[l], x_inout, bias, nullptr, nullptr, ws,
-                    L, stream);
+    if (tracked && block_of[l] != cur_block) {   // a new block: clear the bias state
+      cur_block = block_of[l];
+      if (cudaMemsetAsync(track.count, 0, 4 * BT, c.stream) != cudaSuccess) return XMOD_ERR_CUDA;
+      if (cudaMemsetAsync(track.last, 0x80, 4 * BT, c.stream) != cudaSuccess) return XMOD_ERR_CUDA;
+    }
+    // the following layers of the same kind, at most kRouterRun at a time
+    int count = 1;
+    if (runs)
+      while (count < kRouterRun && l + count < n_layers && kinds[l + count] == kind) ++count;
+    RouteTrack tl = track;
+    tl.layer = routed_index;
+    if (tl.stats) tl.stats += (int64_t)routed_index * dm->B * 4;
+    const int part = kind == XMOD_LAYER_ROUTED_FFN ? PART_FFN : PART_ALL;
+    if (runs)
+      st = sparse_run(c, dm, L, ws, K, gate, &layers[l], count, x_inout, bias, nullptr, nullptr,
+                      tracked ? &tl : nullptr, threshold, part);
+    else
+      st = layer_impl(dm, (xmod_layer_kind)kind, K, gate, &layers[l], x_inout, bias, nullptr,
+                      nullptr, ws, L, stream, tracked ? &tl : nullptr);
     if (st) return st;
-    ++l;
+    l += count;
+    routed_index += count;
+    if (tracked && opts->update_hist && block_last[l - 1])
+      XMOD_RUN("update_hist",
+               launch_count_hist(c, dm->B, dm->T, max_block, track.count,
+                                 opts->update_hist + (int64_t)block_of[l - 1] * dm->B *
+                                                         (max_block + 1)));
   }
   return XMOD_OK;
 }
@@ -579,7 +636,7 @@ int xmod_block_fwd(const xmod_dims* dm, int n_per_seq, const void* xs, const int
                    size_t ws_bytes, void* stream) {
   if (!dims_ok(dm) || n_per_seq <= 0 || n_per_seq > dm->T) return XMOD_ERR_INVALID_ARG;
   if (!aligned16(xs) || !aligned16_or_null(idx) || !aligned16(a_out) || !aligned16(f_out) ||
-      !weights_ok(w, false))
+      !weights_ok(w, XMOD_LAYER_DENSE))
     return XMOD_ERR_INVALID_ARG;
   if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
   const int K = dm->T / n_per_seq;
@@ -614,15 +671,15 @@ int xmod_layer_fwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate g
                    const xmod_layer_weights* w, void* x_inout, const float* bias,
                    int32_t* idx_out, float* r_sel_out, void* ws, size_t ws_bytes, void* stream) {
   if (!dims_ok(dm)) return XMOD_ERR_INVALID_ARG;
-  if (kind != XMOD_LAYER_DENSE && kind != XMOD_LAYER_SPARSE) return XMOD_ERR_INVALID_ARG;
+  if (!kind_ok(kind)) return XMOD_ERR_INVALID_ARG;
   if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
-  if (kind == XMOD_LAYER_SPARSE && (K <= 0 || K > dm->T)) return XMOD_ERR_INVALID_ARG;
+  if (routed(kind) && (K <= 0 || K > dm->T)) return XMOD_ERR_INVALID_ARG;
   if (!aligned16(x_inout) || !aligned16_or_null(bias) || !aligned16_or_null(idx_out) ||
-      !aligned16_or_null(r_sel_out) || !weights_ok(w, kind == XMOD_LAYER_SPARSE))
+      !aligned16_or_null(r_sel_out) || !weights_ok(w, kind))
     return XMOD_ERR_INVALID_ARG;
   if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
-  if (kind == XMOD_LAYER_SPARSE && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
-  const int Kw = kind == XMOD_LAYER_SPARSE ? K : 1;
+  if (routed(kind) && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
+  const int Kw = routed(kind) ? K : 1;
   int st = check_ws(dm, Kw, ws, ws_bytes);
   if (st) return st;
   return layer_impl(dm, kind, Kw, gate, w, x_inout, bias, idx_out, r_sel_out, ws, layout(dm, Kw),
@@ -632,7 +689,7 @@ int xmod_layer_fwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate g
 int xmod_layer_fwd_threshold(const xmod_dims* dm, xmod_gate gate, const xmod_layer_weights* w,
                              void* x_inout, const float* bias, int32_t* count_out, void* ws,
                              size_t ws_bytes, void* stream) {
-  if (!dims_ok(dm) || !weights_ok(w, true)) return XMOD_ERR_INVALID_ARG;
+  if (!dims_ok(dm) || !weights_ok(w, XMOD_LAYER_SPARSE)) return XMOD_ERR_INVALID_ARG;
   if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
   if (!aligned16(x_inout) || !aligned16_or_null(bias) || ((uintptr_t)count_out & 3))
     return XMOD_ERR_INVALID_ARG;
@@ -682,7 +739,7 @@ int xmod_stack_fwd_sched(const xmod_dims* dm, int K, const int32_t* kinds, int n
   if (!dims_ok(dm) || K <= 0 || K > dm->T || !kinds || n_layers < 0 || !layers)
     return XMOD_ERR_INVALID_ARG;
   for (int l = 0; l < n_layers; ++l)
-    if (kinds[l] != XMOD_LAYER_DENSE && kinds[l] != XMOD_LAYER_SPARSE) return XMOD_ERR_INVALID_ARG;
+    if (!kind_ok(kinds[l])) return XMOD_ERR_INVALID_ARG;
   return stack_impl(dm, K, kinds, n_layers, gate, layers, x_inout, bias, opts, ws, ws_bytes,
                     (cudaStream_t)stream);
 }

@@ -42,7 +42,7 @@ __device__ __forceinline__ void epilogue_store(const Epilogue& e, int M, int N, 
       const int64_t t = e.idx ? (int64_t)e.idx[m] : (m - b * e.n_per_seq);
       T* xp = (T*)e.x + (b * e.T + t) * e.d + n;
       const float xv = ld_f(xp);
-      const float hv = e.h[(int64_t)m * e.d + n];   // h = x + a
+      const float hv = e.h ? e.h[(int64_t)m * e.d + n] : xv;   // h = x + a (no h: a = 0)
       float y;
       if (e.gate == XMOD_GATE_XMOD) y = xv + e.varsigma * e.r_sel[m] * ((hv - xv) + acc);  // Eq. 7
       else if (e.gate == XMOD_GATE_MOD) y = hv + e.r_sel[m] * acc;                       // Eq. 6

@@ -237,7 +237,7 @@ __device__ __forceinline__ void epi_load_in(const TcArgs& a, int M, int m, int c
   if (m >= M || col0 >= a.N) return;
   const int rem = a.N - col0;
   ld_seg_bf16((const __nv_bfloat16*)e.x + xrow + col0, in.x, rem, a.v8);
-  if (MODE == EPI_DOWN_SCATTER) ld_seg_f32(e.h + (int64_t)m * e.d + col0, in.h, rem, a.v8);
+  if (MODE == EPI_DOWN_SCATTER && e.h) ld_seg_f32(e.h + (int64_t)m * e.d + col0, in.h, rem, a.v8);
 }
 
 __device__ __forceinline__ void unpack_x(const EpiIn& in, float (&xv)[32]) {
@@ -304,9 +304,10 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, in
         for (int k = 0; k < 2; ++k) {
           const int j = 2 * i + k;
           const float fv = v[8 * g + j];
-          if (e.gate == XMOD_GATE_XMOD) y[j] = xx[k] + g7 * ((hv[j] - xx[k]) + fv);   // Eq. 7
-          else if (e.gate == XMOD_GATE_MOD) y[j] = hv[j] + r * fv;                   // Eq. 6
-          else y[j] = hv[j] + fv;                                                     // dense
+          const float hj = e.h ? hv[j] : xx[k];   // no h: no attention residual (a = 0)
+          if (e.gate == XMOD_GATE_XMOD) y[j] = xx[k] + g7 * ((hj - xx[k]) + fv);   // Eq. 7
+          else if (e.gate == XMOD_GATE_MOD) y[j] = hj + r * fv;                   // Eq. 6
+          else y[j] = hj + fv;                                                     // dense
         }
       }
       qo[g].x = pack_bf16x2(y[0], y[1]);

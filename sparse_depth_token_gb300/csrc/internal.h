@@ -169,7 +169,8 @@ struct Epilogue {
   // is tok[m] (= b * T + t), and seq_off[b] is sequence b's first compact row.
   const int32_t* tok = nullptr;
   const int32_t* seq_off = nullptr;
-  const float* h = nullptr;     // DOWN: h = x_sel + a [M, d] fp32 (the attention residual is h - x)
+  const float* h = nullptr;     // DOWN: h = x_sel + a [M, d] fp32 (the attention residual is
+                                //       h - x); NULL: no attention residual (a = 0)
   const float* r_sel = nullptr; // DOWN: gates [M]
   const float* bias = nullptr;  // ROUTER: per-token logit bias [B*T] or NULL
   float varsigma = 1.0f;
