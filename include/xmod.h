@@ -69,12 +69,17 @@ typedef enum { XMOD_GATE_XMOD = 0, XMOD_GATE_MOD = 1 } xmod_gate;
  * rms1, wq, wk, wv, wo); ROUTED_FFN routes top-(T/K) tokens through the FFN half only,
  * f = FFN(RMSNorm(x) * rms2), with the gated residual taken with a = 0 (Eq. 7:
  * x + varsigma r f; Eq. 6: x + r f) (weights used: w_router, rms2, w_gate, w_up,
- * w_down, varsigma). Weights a kind does not use may be NULL. */
+ * w_down, varsigma). Weights a kind does not use may be NULL.
+ * SPARSE_FULLKV is the Selected-Q / full-KV control of the same section: routed like
+ * SPARSE, but every token of the sequence provides keys and values (RMSNorm(x) * rms1
+ * of all T tokens through wk, wv) and a selected token attends to every token at or
+ * before its own position; the rest of the block and the residual are SPARSE's. */
 typedef enum {
   XMOD_LAYER_DENSE = 0,
   XMOD_LAYER_SPARSE = 1,
   XMOD_LAYER_ATTN = 2,
-  XMOD_LAYER_ROUTED_FFN = 3
+  XMOD_LAYER_ROUTED_FFN = 3,
+  XMOD_LAYER_SPARSE_FULLKV = 4
 } xmod_layer_kind;
 
 /* Problem sizes in the pages' notation: B sequences of T tokens, model width d,

@@ -15,7 +15,8 @@ import numpy as np
 
 from . import build as _build
 
-DENSE, SPARSE, ATTN, RFFN = 0, 1, 2, 3   # ATTN / RFFN: the Routed-FFN variant's halves
+# ATTN / RFFN: the Routed-FFN control's halves; FULLKV: the Selected-Q / full-KV control
+DENSE, SPARSE, ATTN, RFFN, FULLKV = 0, 1, 2, 3, 4
 GATE_XMOD, GATE_MOD = 0, 1
 OK, BAD_ARG, NONFINITE = 0, -1, -5
 
@@ -211,7 +212,7 @@ def layer_fwd(dm: Dims, kind, K, gate, layer: Layer, x, bias=None, idx_force=Non
     y = np.empty_like(x)
     out = {"y": y}
     args = [None] * 4
-    if kind in (SPARSE, RFFN):
+    if kind in (SPARSE, RFFN, FULLKV):
         n = T // K
         out["s"] = np.empty((B, T))
         out["r"] = np.empty((B, T))
@@ -240,7 +241,7 @@ def stack_dyn(dm: Dims, K, gate, kinds, layers, x, bias=None, bias_step=0.0,
     decisions [B, T] (bool)."""
     x = np.array(x, dtype=np.float64, copy=True, order="C")
     bias_a, bp = _d(bias)
-    n_sparse = sum(1 for k in kinds if k in (SPARSE, RFFN))
+    n_sparse = sum(1 for k in kinds if k in (SPARSE, RFFN, FULLKV))
     n = dm.T // K if routing == TOPK else 1
     idx = np.zeros((max(n_sparse, 1), dm.B, n), np.int32)
     s = np.zeros((max(n_sparse, 1), dm.B, dm.T), np.float64)

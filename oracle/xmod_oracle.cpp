@@ -61,7 +61,9 @@ enum { ORACLE_GATE_XMOD = 0, ORACLE_GATE_MOD = 1 };
 // Layer kinds. ATTN and RFFN are the two halves of the Routed-FFN variant of X-MoD
 // notes "mechanism controls" (Table 2 / Table 7): attention over the full sequence with
 // its residual, and an FFN-only refinement applied to the top-(T/K) tokens.
-enum { ORACLE_DENSE = 0, ORACLE_SPARSE = 1, ORACLE_ATTN = 2, ORACLE_RFFN = 3 };
+// FULLKV is the Selected-Q / full-KV control of the same section: a sparse layer
+// whose selected tokens attend to every token at or before their position.
+enum { ORACLE_DENSE = 0, ORACLE_SPARSE = 1, ORACLE_ATTN = 2, ORACLE_RFFN = 3, ORACLE_FULLKV = 4 };
 
 int oracle_num_threads(void) {
 #ifdef _OPENMP
@@ -287,6 +289,43 @@ void oracle_ffn_rows(const oracle_dims* dm, int nr, const double* xs, const orac
   oracle_linear(nr, F, d, hid.data(), w->wd, f_out);
 }
 
+// Block of a Selected-Q / full-KV layer for one sequence x_seq [T, d]: the n selected
+// tokens (ascending positions pos) are the queries; every token provides keys and
+// values (RMSNorm1 of every token); query j attends to the positions <= pos[j].
+// a_out, f_out [n, d].
+void oracle_block_fullkv(const oracle_dims* dm, int T, const double* x_seq,
+                         const oracle_layer_w* w, const int32_t* pos, int n, double* a_out,
+                         double* f_out) {
+  const int d = dm->d, hq = dm->hq, hkv = dm->hkv, hd = dm->hd, F = dm->F;
+  if (n <= 0) return;
+  std::vector<double> u((int64_t)T * d);
+  oracle_rmsnorm(T, d, x_seq, w->g1, dm->eps, u.data());
+  std::vector<double> kk((int64_t)T * hkv * hd), vv((int64_t)T * hkv * hd);
+  oracle_linear(T, d, hkv * hd, u.data(), w->wk, kk.data());
+  oracle_linear(T, d, hkv * hd, u.data(), w->wv, vv.data());
+  std::vector<double> us((int64_t)n * d), xr((int64_t)n * d), qs((int64_t)n * hq * hd);
+  for (int j = 0; j < n; ++j) {
+    std::memcpy(&us[(int64_t)j * d], &u[(int64_t)pos[j] * d], sizeof(double) * d);
+    std::memcpy(&xr[(int64_t)j * d], &x_seq[(int64_t)pos[j] * d], sizeof(double) * d);
+  }
+  oracle_linear(n, d, hq * hd, us.data(), w->wq, qs.data());
+  std::vector<double> qfull((int64_t)T * hq * hd, 0.0);
+  for (int j = 0; j < n; ++j)
+    std::memcpy(&qfull[(int64_t)pos[j] * hq * hd], &qs[(int64_t)j * hq * hd],
+                sizeof(double) * hq * hd);
+  std::vector<double> o((int64_t)n * hq * hd);
+  oracle_attention_rows(T, hq, hkv, hd, qfull.data(), kk.data(), vv.data(), o.data(), pos, n);
+  oracle_linear(n, hq * hd, d, o.data(), w->wo, a_out);
+  std::vector<double> h((int64_t)n * d), v2((int64_t)n * d);
+  for (int64_t i = 0; i < (int64_t)n * d; ++i) h[i] = xr[i] + a_out[i];
+  oracle_rmsnorm(n, d, h.data(), w->g2, dm->eps, v2.data());
+  std::vector<double> g((int64_t)n * F), up((int64_t)n * F), hid((int64_t)n * F);
+  oracle_linear(n, d, F, v2.data(), w->wg, g.data());
+  oracle_linear(n, d, F, v2.data(), w->wu, up.data());
+  for (int64_t i = 0; i < (int64_t)n * F; ++i) hid[i] = silu(g[i]) * up[i];
+  oracle_linear(n, F, d, hid.data(), w->wd, f_out);
+}
+
 // One layer of the stack on x_in [B, T, d] -> y [B, T, d].
 //   sparse: router (Eq. 8) -> top-(T/K) -> gather -> block -> gated residual
 //           (Eq. 7 if gate == XMOD, Eq. 6 if gate == MOD); unselected rows y = x.
@@ -294,6 +333,8 @@ void oracle_ffn_rows(const oracle_dims* dm, int nr, const double* xs, const orac
 //   attn:   attention half of the block on all T tokens, y = x + a.
 //   rffn:   router -> top-(T/K) -> gather -> FFN half on the selected tokens ->
 //           gated residual with a = 0 (Eq. 7: x + varsigma r f; Eq. 6: x + r f).
+//   fullkv: as sparse, but the selected tokens attend to every token (keys and values
+//           of all T) at or before their own position.
 // Optional arguments:
 //   bias      [B, T]  signed per-token router bias, added to the logit;
 //   s_out     [B, T]  router logits; r_out [B, T] gates;
@@ -329,7 +370,8 @@ int oracle_layer_fwd(const oracle_dims* dm, int kind, int K, int gate,
     }
     return ORACLE_OK;
   }
-  if ((kind != ORACLE_SPARSE && kind != ORACLE_RFFN) || K <= 0) return ORACLE_BAD_ARG;
+  if ((kind != ORACLE_SPARSE && kind != ORACLE_RFFN && kind != ORACLE_FULLKV) || K <= 0)
+    return ORACLE_BAD_ARG;
   const int n = T / K;
   if (n <= 0) return ORACLE_BAD_ARG;
   std::vector<double> s(BT), r(BT);
@@ -365,7 +407,11 @@ int oracle_layer_fwd(const oracle_dims* dm, int kind, int K, int gate,
       if (!row_mask || row_mask[(int64_t)b * T + idx[(int64_t)b * n + j]]) rows.push_back(j);
     if (rows.empty()) continue;
     std::vector<double> a(rows.size() * (size_t)d, 0.0), f(rows.size() * (size_t)d);
-    if (kind == ORACLE_RFFN) {   // FFN only, row by row: attention context plays no part
+    if (kind == ORACLE_FULLKV) {
+      if (rows.size() != (size_t)n) return ORACLE_BAD_ARG;   // no row mask here
+      oracle_block_fullkv(dm, T, x_in + (int64_t)b * T * d, w, &idx[(int64_t)b * n], n, a.data(),
+                          f.data());
+    } else if (kind == ORACLE_RFFN) {   // FFN only, row by row: attention context plays no part
       std::vector<double> xr(rows.size() * (size_t)d);
       for (size_t i = 0; i < rows.size(); ++i)
         std::memcpy(&xr[i * d], &xs[(int64_t)rows[i] * d], sizeof(double) * d);
@@ -488,7 +534,8 @@ int oracle_stack_dyn(const oracle_dims* dm, int K, int gate, int n_layers, const
   std::vector<int32_t> count(BT, 0), idx((int64_t)dm->B * (n > 0 ? n : 1)), mask(BT);
   int ls = 0;
   for (int l = 0; l < n_layers; ++l) {
-    const bool sparse = kinds[l] == ORACLE_SPARSE || kinds[l] == ORACLE_RFFN;   // routed
+    const bool sparse = kinds[l] == ORACLE_SPARSE || kinds[l] == ORACLE_RFFN ||
+                        kinds[l] == ORACLE_FULLKV;   // routed
     if (sparse)
       for (int64_t i = 0; i < BT; ++i)
         bias[i] = (bias0 ? bias0[i] : 0.0) - bias_step * (double)count[i];

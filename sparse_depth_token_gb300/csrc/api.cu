@@ -103,8 +103,21 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? XMOD_OK : XMOD_ERR_CU
     if (_e != cudaSuccess) return XMOD_ERR_CUDA;     \
   } while (0)
 
-bool routed(int kind) { return kind == XMOD_LAYER_SPARSE || kind == XMOD_LAYER_ROUTED_FFN; }
-bool kind_ok(int kind) { return kind >= XMOD_LAYER_DENSE && kind <= XMOD_LAYER_ROUTED_FFN; }
+bool routed(int kind) {
+  return kind == XMOD_LAYER_SPARSE || kind == XMOD_LAYER_ROUTED_FFN ||
+         kind == XMOD_LAYER_SPARSE_FULLKV;
+}
+bool kind_ok(int kind) { return kind >= XMOD_LAYER_DENSE && kind <= XMOD_LAYER_SPARSE_FULLKV; }
+// Which part of the block runs: all of it, the attention half (its residual written
+// straight into the stream: x += a, for ATTN layers), the FFN half on RMSNorm(x) *
+// rms2 with a = 0 (ROUTED_FFN layers), or all of it with every token's keys and
+// values (SPARSE_FULLKV layers).
+enum BlockPart { PART_ALL = 0, PART_ATTN = 1, PART_FFN = 2, PART_FULLKV = 3 };
+
+int block_part(int kind) {
+  return kind == XMOD_LAYER_ROUTED_FFN ? PART_FFN
+         : kind == XMOD_LAYER_SPARSE_FULLKV ? PART_FULLKV : PART_ALL;
+}
 
 // The weights a layer kind uses must be present and 16-byte aligned.
 bool weights_ok(const xmod_layer_weights* w, int kind) {
@@ -138,10 +151,82 @@ struct Ragged {
 // With scatter, xs_new (if not NULL) receives the updated compact rows [B*n, d].
 // With rg (threshold routing), n is T: buffers are sized for every token, kernels
 // compute the rows the routing picked (tensor-core path only).
-// Which part of the block runs: all of it, the attention half (its residual written
-// straight into the stream: x += a, for ATTN layers), or the FFN half on RMSNorm(x) *
-// rms2 with a = 0 (ROUTED_FFN layers).
-enum BlockPart { PART_ALL = 0, PART_ATTN = 1, PART_FFN = 2 };
+
+// Attention of a Selected-Q / full-KV layer (X-MoD notes, "mechanism controls": the
+// selected tokens are the queries, every token provides keys and values): o [B*n, qw]
+// for the n selected rows of each sequence (idx, ascending positions), each attending
+// to every token at or before its own position.
+int fullkv_attention(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int n,
+                     const void* x, const int32_t* idx, const xmod_layer_weights* w) {
+  const xmod_dtype dt = dm->dtype;
+  const int B = dm->B, T = dm->T, d = dm->d, hq = dm->n_heads, hkv = dm->n_kv_heads,
+            hd = dm->head_dim;
+  const int qw = hq * hd, kw = hkv * hd;
+  const size_t es = esize(dt);
+  // scratch: RMSNorm1 of every token in u, their k | v in qkv (v transposed into vt on
+  // the tensor-core path), the selected tokens' RMSNorm1 and q in the fp32 h buffer
+  char* u_all = at(ws, L.u);
+  char* kv = at(ws, L.qkv);
+  char* vt = at(ws, L.vt);
+  char* o = at(ws, L.o);
+  char* u_sel = at(ws, L.h);
+  char* q = u_sel + align_up(es * (size_t)B * n * d);
+  if (align_up(es * (size_t)B * n * d) + es * (size_t)B * n * qw > 4 * (size_t)B * T * d)
+    return XMOD_ERR_UNSUPPORTED;
+  XMOD_RUN("gather_rmsnorm", launch_gather_rmsnorm(c, dt, B, T, T, d, x, nullptr, w->rms1,
+                                                   dm->rms_eps, u_all));
+  Epilogue ek;
+  ek.kind = EPI_STORE;
+  ek.out = kv;
+  ek.ldo = 2 * kw;
+  GemmTcProblem pk;
+  pk.M = B * T; pk.N = 2 * kw; pk.K = d; pk.A = u_all; pk.lda = d; pk.ldb = d;
+  pk.B[0] = w->wk; pk.B[1] = w->wv; pk.nB = 2; pk.split[0] = kw;
+  Epilogue eq;
+  eq.kind = EPI_STORE;
+  eq.out = q;
+  eq.ldo = qw;
+  GemmTcProblem pq;
+  pq.M = B * n; pq.N = qw; pq.K = d; pq.A = u_sel; pq.lda = d; pq.ldb = d; pq.B[0] = w->wq;
+  bool tc = dt == XMOD_BF16 && attention_tc_supported(hd, n, qw) &&
+            attention_tc_supported(hd, T, 2 * kw) && gemm_tc_supported(pq, eq);
+  if (tc) {
+    ek.vt = vt;
+    ek.vt_col0 = kw;
+    ek.vt_hd = hd;
+    ek.vt_hkv = hkv;
+    ek.vt_ld = vt_ld(T);
+    ek.n_per_seq = T;
+    tc = gemm_tc_supported(pk, ek);
+  }
+  if (tc) {
+    XMOD_RUN("gemm_qkv", launch_gemm_tc(c, pk, ek));
+  } else {
+    ek.vt = nullptr;
+    XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, B * T, kw, d, u_all, d, w->wk, d, nullptr, ek));
+    ek.out = kv + es * kw;
+    XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, B * T, kw, d, u_all, d, w->wv, d, nullptr, ek));
+  }
+  XMOD_RUN("gather_rmsnorm", launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1,
+                                                   dm->rms_eps, u_sel));
+  if (tc)
+    XMOD_RUN("gemm_qkv", launch_gemm_tc(c, pq, eq));
+  else
+    XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, B * n, qw, d, u_sel, d, w->wq, d, nullptr, eq));
+  if (tc) {
+    AttnKv akv;
+    akv.k = kv;
+    akv.ldk = 2 * kw;
+    akv.nkv = T;
+    akv.qpos = idx;
+    XMOD_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, q, qw, vt, vt_ld(T), o, nullptr,
+                                              nullptr, &akv));
+  } else {
+    XMOD_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, q, qw, kv,
+                                                kv + es * kw, 2 * kw, o, idx, T));
+  }
+  return XMOD_OK;
+}
 
 int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int n,
               const void* x_src, const int32_t* idx, const xmod_layer_weights* w, void* a_out,
@@ -172,58 +257,64 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
              launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms2, dm->rms_eps, v2, rm));
     h_in = nullptr;
   } else {
-    // 1. gather + RMSNorm1
-    XMOD_RUN("gather_rmsnorm",
-             launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms1, dm->rms_eps, u, rm));
-    // 2. q, k, v projections into one [M, qkv_w] buffer
-    char* vt = at(ws, L.vt);
-    const bool tc_attn = tc && attention_tc_supported(hd, n, qkv_w);
-    Epilogue e;
-    e.kind = EPI_STORE;
-    e.ldo = qkv_w;
-    e.out = qkv;
-    if (tc_attn) {  // v goes straight to its transposed layout
-      e.vt = vt;
-      e.vt_col0 = qw + kw;
-      e.vt_hd = hd;
-      e.vt_hkv = hkv;
-      e.vt_ld = vt_ld(n);
-      e.n_per_seq = n;
-    }
-    GemmTcProblem pq;
-    pq.M = M; pq.N = qkv_w; pq.K = d; pq.A = u; pq.lda = d; pq.ldb = d;
-    pq.B[0] = w->wq; pq.B[1] = w->wk; pq.B[2] = w->wv; pq.nB = 3;
-    pq.split[0] = qw; pq.split[1] = qw + kw;
-    const bool tc_qkv = tc && gemm_tc_supported(pq, e);
-    if (rg) {
-      if (!tc_qkv || !tc_attn) return XMOD_ERR_UNSUPPORTED;
-      e.tok = rg->tok;
-      e.seq_off = rg->seq_off;
-      e.T = T;
-      pq.M_dev = M_dev;
-      // keys past a sequence's count are read (and multiplied by zero weights): keep
-      // them finite
-      if (cudaMemsetAsync(vt, 0, es * (size_t)B * hkv * hd * vt_ld(n), c.stream) != cudaSuccess)
-        return XMOD_ERR_CUDA;
-    }
-    if (tc_qkv) {
-      XMOD_RUN("gemm_qkv", launch_gemm_tc(c, pq, e));
+    if (part == PART_FULLKV) {   // steps 1-3 with every token's keys and values
+      if (rg || !idx) return XMOD_ERR_UNSUPPORTED;
+      const int st = fullkv_attention(c, dm, L, ws, n, x_src, idx, w);
+      if (st) return st;
     } else {
-      e.vt = nullptr;
-      XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, qw, d, u, d, w->wq, d, nullptr, e));
-      e.out = qkv + es * qw;
-      XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wk, d, nullptr, e));
-      e.out = qkv + es * (qw + kw);
-      XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wv, d, nullptr, e));
+      // 1. gather + RMSNorm1
+      XMOD_RUN("gather_rmsnorm",
+               launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms1, dm->rms_eps, u, rm));
+      // 2. q, k, v projections into one [M, qkv_w] buffer
+      char* vt = at(ws, L.vt);
+      const bool tc_attn = tc && attention_tc_supported(hd, n, qkv_w);
+      Epilogue e;
+      e.kind = EPI_STORE;
+      e.ldo = qkv_w;
+      e.out = qkv;
+      if (tc_attn) {  // v goes straight to its transposed layout
+        e.vt = vt;
+        e.vt_col0 = qw + kw;
+        e.vt_hd = hd;
+        e.vt_hkv = hkv;
+        e.vt_ld = vt_ld(n);
+        e.n_per_seq = n;
+      }
+      GemmTcProblem pq;
+      pq.M = M; pq.N = qkv_w; pq.K = d; pq.A = u; pq.lda = d; pq.ldb = d;
+      pq.B[0] = w->wq; pq.B[1] = w->wk; pq.B[2] = w->wv; pq.nB = 3;
+      pq.split[0] = qw; pq.split[1] = qw + kw;
+      const bool tc_qkv = tc && gemm_tc_supported(pq, e);
+      if (rg) {
+        if (!tc_qkv || !tc_attn) return XMOD_ERR_UNSUPPORTED;
+        e.tok = rg->tok;
+        e.seq_off = rg->seq_off;
+        e.T = T;
+        pq.M_dev = M_dev;
+        // keys past a sequence's count are read (and multiplied by zero weights): keep
+        // them finite
+        if (cudaMemsetAsync(vt, 0, es * (size_t)B * hkv * hd * vt_ld(n), c.stream) != cudaSuccess)
+          return XMOD_ERR_CUDA;
+      }
+      if (tc_qkv) {
+        XMOD_RUN("gemm_qkv", launch_gemm_tc(c, pq, e));
+      } else {
+        e.vt = nullptr;
+        XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, qw, d, u, d, w->wq, d, nullptr, e));
+        e.out = qkv + es * qw;
+        XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wk, d, nullptr, e));
+        e.out = qkv + es * (qw + kw);
+        XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wv, d, nullptr, e));
+      }
+      // 3. causal GQA attention among the n rows of each sequence
+      if (tc_qkv && tc_attn)
+        XMOD_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, vt_ld(n), o,
+                                                  rg ? rg->seq_count : nullptr,
+                                                  rg ? rg->seq_off : nullptr));
+      else
+        XMOD_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w,
+                                                    qkv + es * qw, qkv + es * (qw + kw), qkv_w, o));
     }
-    // 3. causal GQA attention among the n rows of each sequence
-    if (tc_qkv && tc_attn)
-      XMOD_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, vt_ld(n), o,
-                                                rg ? rg->seq_count : nullptr,
-                                                rg ? rg->seq_off : nullptr));
-    else
-      XMOD_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w,
-                                                  qkv + es * qw, qkv + es * (qw + kw), qkv_w, o));
     if (part == PART_ATTN) {   // x += a straight into the stream: the down epilogue's
       Epilogue ea;            // dense form y = h + f with no h (h = x) and f = a
       ea.kind = EPI_DOWN_SCATTER;
@@ -439,7 +530,7 @@ int layer_impl(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
   if (kind == XMOD_LAYER_ATTN)
     return run_block(c, dm, L, ws, dm->T, x, nullptr, w, nullptr, nullptr, true, x, nullptr, -1,
                      nullptr, nullptr, PART_ATTN);
-  const int part = kind == XMOD_LAYER_ROUTED_FFN ? PART_FFN : PART_ALL;
+  const int part = block_part(kind);
   if (sparse_run_supported(dm, ws, L))
     return sparse_run(c, dm, L, ws, K, gate, w, 1, x, bias, idx_out, r_sel_out, track, false,
                       part);
@@ -477,7 +568,8 @@ int stack_impl(const xmod_dims* dm, int K, const int32_t* kinds, int n_layers, x
   int max_block = 0, blocks = 0, in_block = 0, last_routed = -1;
   for (int l = 0; l < n_layers; ++l) {
     if (!weights_ok(&layers[l], kinds[l])) return XMOD_ERR_INVALID_ARG;
-    if (threshold && kinds[l] == XMOD_LAYER_ROUTED_FFN) return XMOD_ERR_UNSUPPORTED;
+    if (threshold && routed(kinds[l]) && kinds[l] != XMOD_LAYER_SPARSE)
+      return XMOD_ERR_UNSUPPORTED;
     if (kinds[l] == XMOD_LAYER_DENSE) {
       if (last_routed >= 0) block_last[last_routed] = 1;
       last_routed = -1;
@@ -531,7 +623,7 @@ int stack_impl(const xmod_dims* dm, int K, const int32_t* kinds, int n_layers, x
     RouteTrack tl = track;
     tl.layer = routed_index;
     if (tl.stats) tl.stats += (int64_t)routed_index * dm->B * 4;
-    const int part = kind == XMOD_LAYER_ROUTED_FFN ? PART_FFN : PART_ALL;
+    const int part = block_part(kind);
     if (runs)
       st = sparse_run(c, dm, L, ws, K, gate, &layers[l], count, x_inout, bias, nullptr, nullptr,
                       tracked ? &tl : nullptr, threshold, part);

@@ -74,6 +74,13 @@ struct AttnArgs {
   // the compact rows. NULL: every sequence has n rows at b * n.
   const int32_t* seq_count;
   const int32_t* seq_off;
+  // Selected-Q / full-KV: query row q of sequence b sits at position qpos[b * n + q]
+  // (ascending in q) and attends to the keys at positions <= it among nkv keys per
+  // sequence, read from a separate K map (columns from k_col0). qpos NULL: the keys
+  // are the n query rows themselves (causal among them), nkv = n.
+  const int32_t* qpos;
+  int nkv;
+  int k_col0;
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -147,7 +154,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     row0 = a.seq_off[b];
   }
   const int last_q = min(q0 + QB, n_b) - 1;
-  const int nkb = q0 < n_b ? last_q / KB + 1 : 0;   // 0: this query block is empty
+  // last key position any row of the block may see
+  const int last_key = a.qpos && q0 < n_b ? a.qpos[(int64_t)b * a.n + last_q] : last_q;
+  const int nkb = q0 < n_b ? last_key / KB + 1 : 0;   // 0: this query block is empty
 
   if (warp == 0) {
     if (lane == 0 && nkb > 0) {
@@ -167,12 +176,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         mbar_arrive_expect_tx(KV_FULL0 + 8 * s, C::K_STAGE + C::V_STAGE);
         const uint32_t kdst = sK0 + s * C::K_STAGE, vdst = sV0 + s * C::V_STAGE;
         if (a.seq_count) {
-          tma_load_2d(kdst, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD, (int)(row0 + j * KB));
-          tma_load_2d(kdst + C::K_CHUNK, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD + 64,
+          tma_load_2d(kdst, &tmK, KV_FULL0 + 8 * s, a.k_col0 + g * HD, (int)(row0 + j * KB));
+          tma_load_2d(kdst + C::K_CHUNK, &tmK, KV_FULL0 + 8 * s, a.k_col0 + g * HD + 64,
                       (int)(row0 + j * KB));
         } else {
-          tma_load_3d(kdst, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD, j * KB, b);
-          tma_load_3d(kdst + C::K_CHUNK, &tmK, KV_FULL0 + 8 * s, a.qw + g * HD + 64, j * KB, b);
+          tma_load_3d(kdst, &tmK, KV_FULL0 + 8 * s, a.k_col0 + g * HD, j * KB, b);
+          tma_load_3d(kdst + C::K_CHUNK, &tmK, KV_FULL0 + 8 * s, a.k_col0 + g * HD + 64, j * KB, b);
         }
 #pragma unroll
         for (int kc = 0; kc < KB / 64; ++kc)
@@ -251,7 +260,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
   } else {
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const int qi = q0 + row;
+    const int qi = q0 + row;   // compact query row
+    // position that bounds this row's keys, and the smallest one in the block (rows
+    // past the sequence's end repeat its last position; their output is not stored)
+    int qp = qi, qp_min = q0;
+    if (a.qpos && nkb > 0) {
+      const int64_t base_row = (int64_t)b * a.n;
+      qp = a.qpos[base_row + min(qi, n_b - 1)];
+      qp_min = a.qpos[base_row + q0];
+    }
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t sw = (uint32_t)(row & 7);
     float m = -INFINITY, l = 0.f;
@@ -275,12 +292,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
       tc_fence_before();
       mbar_arrive(S_EMPTY0 + 8 * s);
       const int key0 = j * KB;
-      const bool diag = key0 + KB - 1 > q0;   // only the diagonal block needs the mask
+      const bool diag = key0 + KB - 1 > qp_min;   // only blocks reaching past a row need the mask
       float mx = -INFINITY;
       if (diag) {
 #pragma unroll
         for (int i = 0; i < KB; ++i) {
-          if (key0 + i > qi) v[i] = -INFINITY;
+          if (key0 + i > qp) v[i] = -INFINITY;
           mx = fmaxf(mx, v[i]);
         }
       } else {
@@ -387,10 +404,19 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
 template <int KB, int PBUF>
 cudaError_t launch_attention_cfg(const Ctx& c, int B, int n, int hq, const void* qkv, int ldq,
-                                 const CUtensorMap& mVt, const AttnArgs& a) {
+                                 const CUtensorMap& mVt, const AttnArgs& a, const AttnKv* kv) {
   using Cf = AttnCfg<KB, PBUF>;
   CUtensorMap mQ, mK;
-  if (a.seq_count) {   // 2-D over the B * n compact rows
+  if (kv) {   // queries [B, n, ldq]; keys [B, nkv, ldk] from their own tensor
+    const int64_t qdims[3] = {ldq, n, B};
+    const int64_t qstrides[2] = {(int64_t)ldq * 2, (int64_t)n * ldq * 2};
+    const int qbox[3] = {64, QB, 1};
+    const int64_t kdims[3] = {kv->ldk, kv->nkv, B};
+    const int64_t kstrides[2] = {(int64_t)kv->ldk * 2, (int64_t)kv->nkv * kv->ldk * 2};
+    const int kbox[3] = {64, KB, 1};
+    if (!tma_map_bf16(&mQ, qkv, 3, qdims, qstrides, qbox)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(&mK, kv->k, 3, kdims, kstrides, kbox)) return cudaErrorInvalidValue;
+  } else if (a.seq_count) {   // 2-D over the B * n compact rows
     const int64_t dims[2] = {ldq, (int64_t)B * n};
     const int64_t strides[1] = {(int64_t)ldq * 2};
     const int qbox[2] = {64, QB};
@@ -434,11 +460,14 @@ bool attention_tc_supported(int hd, int n, int ldq) {
 
 cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
                                 int ldq, const void* vt, int vt_ld, void* o,
-                                const int32_t* seq_count, const int32_t* seq_off) {
+                                const int32_t* seq_count, const int32_t* seq_off,
+                                const AttnKv* kv) {
   if (B <= 0 || n <= 0) return cudaSuccess;
+  if (kv && (seq_count || !kv->qpos || kv->nkv <= 0 || kv->ldk % 8)) return cudaErrorInvalidValue;
+  const int nkv = kv ? kv->nkv : n;
   CUtensorMap mVt;
   {
-    const int64_t dims[2] = {n, (int64_t)B * hkv * HD};
+    const int64_t dims[2] = {nkv, (int64_t)B * hkv * HD};
     const int64_t strides[1] = {(int64_t)vt_ld * 2};
     const int box[2] = {64, HD};
     if (!tma_map_bf16(&mVt, vt, 2, dims, strides, box)) return cudaErrorInvalidValue;
@@ -455,8 +484,12 @@ cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, con
   a.status = c.status;
   a.seq_count = seq_count;
   a.seq_off = seq_off;
-  if (n <= XMOD_ATTN_ONE_BLOCK_MAX_N) return launch_attention_cfg<128, 2>(c, B, n, hq, qkv, ldq, mVt, a);
-  return launch_attention_cfg<64, 1>(c, B, n, hq, qkv, ldq, mVt, a);
+  a.qpos = kv ? kv->qpos : nullptr;
+  a.nkv = nkv;
+  a.k_col0 = kv ? 0 : a.qw;
+  if (nkv <= XMOD_ATTN_ONE_BLOCK_MAX_N)
+    return launch_attention_cfg<128, 2>(c, B, n, hq, qkv, ldq, mVt, a, kv);
+  return launch_attention_cfg<64, 1>(c, B, n, hq, qkv, ldq, mVt, a, kv);
 }
 
 }  // namespace xmod

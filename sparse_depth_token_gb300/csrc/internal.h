@@ -212,19 +212,31 @@ cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue&
 // Causal GQA attention within each of B sequences of n tokens.
 // q [B*n, ldq] (head h at column h*hd), k and v [B*n, ldkv] (KV head g at g*hd),
 // o [B*n, hq*hd].
+// With qpos [B, n] (ascending positions): query row i sees the keys at positions <=
+// qpos[b * n + i] among nkv keys per sequence in k, v [B * nkv, ldkv].
 cudaError_t launch_attention_simt(const Ctx& c, xmod_dtype dt, int B, int n, int hq, int hkv,
                                   int hd, const void* q, int ldq, const void* k, const void* v,
-                                  int ldkv, void* o);
+                                  int ldkv, void* o, const int32_t* qpos = nullptr,
+                                  int nkv = 0);
 
 // Tensor-core attention (bf16, head_dim 128). q and k come from the q|k|v rows
 // [B*n, ldq] (k of KV head g at column hq*128 + g*128); v comes transposed,
 // vt [B, hkv, 128, vt_ld] with keys contiguous; o [B*n, hq*128].
 // With seq_count / seq_off (device [B]): sequence b has seq_count[b] <= n tokens at
 // compact rows seq_off[b] ...; its keys past seq_count[b] in vt must be finite.
+// With kv (Selected-Q / full-KV): the n query rows of sequence b sit at positions
+// qpos[b * n + q] (ascending); keys come from k [B, nkv, ldk] (KV head g at column
+// g * 128) and vt covers nkv keys; query row q sees the keys at positions <= its own.
+struct AttnKv {
+  const void* k = nullptr;
+  int ldk = 0;
+  int nkv = 0;
+  const int32_t* qpos = nullptr;
+};
 bool attention_tc_supported(int hd, int n, int ldq);
 cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
                                 int ldq, const void* vt, int vt_ld, void* o,
                                 const int32_t* seq_count = nullptr,
-                                const int32_t* seq_off = nullptr);
+                                const int32_t* seq_off = nullptr, const AttnKv* kv = nullptr);
 
 }  // namespace xmod

@@ -17,7 +17,7 @@ ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE_CHECK, ERR_W
     -1, -2, -3, -4, -5, -6)
 BF16, FP32 = 0, 1
 GATE_XMOD, GATE_MOD = 0, 1
-LAYER_DENSE, LAYER_SPARSE, LAYER_ATTN, LAYER_ROUTED_FFN = 0, 1, 2, 3
+LAYER_DENSE, LAYER_SPARSE, LAYER_ATTN, LAYER_ROUTED_FFN, LAYER_SPARSE_FULLKV = 0, 1, 2, 3, 4
 
 EXPORTS = ("xmod_version", "xmod_status_string", "xmod_workspace_bytes", "xmod_reset_status",
            "xmod_sync_status", "xmod_router_topk", "xmod_topk", "xmod_gather", "xmod_block_fwd",

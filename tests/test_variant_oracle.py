@@ -47,3 +47,35 @@ def test_routed_ffn_selects_like_the_sparse_layer():
     np.put_along_axis(sel, a["idx"], True, 1)
     x3 = x.reshape(w.B, w.T, w.d)
     assert np.array_equal(a["y"].reshape(x3.shape)[~sel], x3[~sel])
+
+
+# Selected-Q / full-KV control (same section): the selected tokens query every token's
+# keys and values at or before their position. Pinned where the two contexts coincide.
+
+def test_fullkv_with_every_token_selected_is_the_sparse_layer():
+    w, lw, od, x = _setup()
+    bias = I.router_bias(w)
+    a = O.layer_fwd(od, O.FULLKV, 1, 0, O.Layer(lw), x, bias=bias)
+    b = O.layer_fwd(od, O.SPARSE, 1, 0, O.Layer(lw), x, bias=bias)
+    assert np.array_equal(a["y"], b["y"])
+
+
+def test_fullkv_with_a_selected_prefix_is_the_sparse_layer():
+    w, lw, od, x = _setup()
+    n = w.T // w.K
+    # the first n positions win: their compact order is the position order and every
+    # key at or before a selected position is itself selected
+    bias = np.where(np.arange(w.T)[None, :] < n, 50.0, -50.0) * np.ones((w.B, 1))
+    a = O.layer_fwd(od, O.FULLKV, w.K, 0, O.Layer(lw), x, bias=bias)
+    b = O.layer_fwd(od, O.SPARSE, w.K, 0, O.Layer(lw), x, bias=bias)
+    assert np.array_equal(a["idx"], np.tile(np.arange(n, dtype=np.int32), (w.B, 1)))
+    np.testing.assert_allclose(a["y"], b["y"], rtol=0, atol=1e-12 * np.abs(b["y"]).max())
+
+
+def test_fullkv_sees_unselected_keys():
+    w, lw, od, x = _setup()
+    bias = I.router_bias(w)
+    a = O.layer_fwd(od, O.FULLKV, w.K, 0, O.Layer(lw), x, bias=bias)
+    b = O.layer_fwd(od, O.SPARSE, w.K, 0, O.Layer(lw), x, bias=bias)
+    assert np.array_equal(a["idx"], b["idx"])
+    assert np.abs(a["y"] - b["y"]).max() > 1e-3
