@@ -33,7 +33,7 @@ _IP = ctypes.POINTER(ctypes.c_int32)
 
 class LayerW(ctypes.Structure):
     _fields_ = [(n, _DP) for n in ("w_r", "g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")] + [
-        ("varsigma", ctypes.c_double)]
+        ("varsigma", ctypes.c_double), ("gq", _DP), ("gk", _DP), ("rope_theta", ctypes.c_double)]
 
 
 _lib = None
@@ -54,6 +54,11 @@ def lib():
         L.oracle_attention_rows.argtypes = [ctypes.c_int] * 4 + [_DP, _DP, _DP, _DP, _IP, ctypes.c_int]
         L.oracle_block_rows.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _DP,
                                         ctypes.POINTER(LayerW), _IP, ctypes.c_int, _DP, _DP]
+        L.oracle_block_rows_pos.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _DP,
+                                            ctypes.POINTER(LayerW), _IP, ctypes.c_int, _DP, _DP,
+                                            _IP]
+        L.oracle_qk_transform.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _DP, _DP,
+                                          ctypes.c_double, ctypes.c_double, _IP]
         L.oracle_layer_fwd.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.POINTER(LayerW), _DP, _DP, _DP,
                                        _DP, _DP, _IP, _DP, _IP, _IP]
@@ -180,25 +185,42 @@ class Layer:
 
     def __init__(self, arrays: dict, varsigma: float = 1.0):
         self.arrays = {n: np.ascontiguousarray(arrays[n], dtype=np.float64) for n in self.NAMES}
+        # optional Qwen3-style attention extras: QK-norm gains [hd] and the rotary base
+        for n in ("gq", "gk"):
+            if arrays.get(n) is not None:
+                self.arrays[n] = np.ascontiguousarray(arrays[n], dtype=np.float64)
         self.varsigma = float(varsigma)
+        self.rope_theta = float(arrays.get("rope_theta", 0.0) or 0.0)
+        opt = [self.arrays[n].ctypes.data_as(_DP) if n in self.arrays else None for n in ("gq", "gk")]
         self.struct = LayerW(*[self.arrays[n].ctypes.data_as(_DP) for n in self.NAMES],
-                             self.varsigma)
+                             self.varsigma, *opt, self.rope_theta)
+
+
+def qk_transform(x, heads, hd, gain=None, eps=1e-6, theta=0.0, pos=None):
+    """QK-norm (gain) and rotary embedding (theta) of x [rows, heads * hd]; returns a copy."""
+    x = np.array(x, dtype=np.float64, copy=True, order="C")
+    g_a, gp = _d(gain)
+    p_a, pp = _i(pos)
+    lib().oracle_qk_transform(x.shape[0], heads, hd, x.ctypes.data_as(_DP), gp, eps, theta, pp)
+    return x
 
 
 def dims(B, T, d, hq, hkv, hd, F, eps=1e-6) -> Dims:
     return Dims(B, T, d, hq, hkv, hd, F, eps)
 
 
-def block(dm: Dims, xs, layer: Layer, rows=None):
-    """Block on one sequence's compact buffer xs [n, d] -> (a, f) for the requested rows."""
+def block(dm: Dims, xs, layer: Layer, rows=None, pos=None):
+    """Block on one sequence's compact buffer xs [n, d] -> (a, f) for the requested rows.
+    pos [n]: original positions of the compact rows (rotary embedding only)."""
     xs, xp = _d(xs)
     n = xs.shape[0]
     rows_a, rp = _i(rows)
+    pos_a, pp = _i(pos)
     nr = n if rows is None else len(rows_a)
     a = np.empty((nr, dm.d))
     f = np.empty((nr, dm.d))
-    lib().oracle_block_rows(ctypes.byref(dm), n, xp, ctypes.byref(layer.struct), rp, nr,
-                            a.ctypes.data_as(_DP), f.ctypes.data_as(_DP))
+    lib().oracle_block_rows_pos(ctypes.byref(dm), n, xp, ctypes.byref(layer.struct), rp, nr,
+                                a.ctypes.data_as(_DP), f.ctypes.data_as(_DP), pp)
     return a, f
 
 

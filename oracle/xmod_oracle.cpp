@@ -51,9 +51,16 @@ typedef struct {
 // Matrices are [out, in] row-major (the nn.Linear layout):
 //   wq [hq*hd, d], wk [hkv*hd, d], wv [hkv*hd, d], wo [d, hq*hd],
 //   wg [F, d], wu [F, d], wd [d, F]; w_r, g1, g2 are [d].
+// Optional, Qwen3-style (X-MoD notes, "backbone configuration": Qwen3 backbones):
+//   gq, gk [hd]   QK-norm gains: each head's q and k vector is RMS-normalised and
+//                 scaled by them before the rotation (NULL: no QK-norm);
+//   rope_theta    rotary position embedding base (0: none), applied to q and k at the
+//                 token's original position in its sequence.
 typedef struct {
   const double *w_r, *g1, *wq, *wk, *wv, *wo, *g2, *wg, *wu, *wd;
   double varsigma;
+  const double *gq, *gk;
+  double rope_theta;
 } oracle_layer_w;
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_NONFINITE = -5 };
@@ -153,6 +160,38 @@ void oracle_linear(int64_t rows, int in, int out, const double* x, const double*
 // q [n, hq*hd], k and v [n, hkv*hd]; query head h reads KV head h / (hq/hkv).
 // o[i, h] = sum_{j<=i} softmax_j(q_i.k_j / sqrt(hd)) v_j.
 // Only the rows listed in `rows` (nrows of them) are computed; rows == NULL means all.
+// QK-norm and rotary embedding of `rows` vectors x [rows, heads * hd] in place. Row i
+// sits at position pos[i] (NULL: i). QK-norm: x_h <- x_h / sqrt(mean(x_h^2) + eps) *
+// gain. Rotation (the rotate-half pairing of the Qwen / LLaMA family): for
+// c < hd/2, angle = pos * theta^(-2c/hd), (x_c, x_{c+hd/2}) <- (x_c cos - x_{c+hd/2} sin,
+// x_c sin + x_{c+hd/2} cos).
+void oracle_qk_transform(int rows, int heads, int hd, double* x, const double* gain, double eps,
+                         double theta, const int32_t* pos) {
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < rows; ++i) {
+    const double p = pos ? (double)pos[i] : (double)i;
+    for (int h = 0; h < heads; ++h) {
+      double* v = x + ((int64_t)i * heads + h) * hd;
+      if (gain) {
+        double ss = 0.0;
+        for (int c = 0; c < hd; ++c) ss += v[c] * v[c];
+        const double inv = 1.0 / std::sqrt(ss / hd + eps);
+        for (int c = 0; c < hd; ++c) v[c] = v[c] * inv * gain[c];
+      }
+      if (theta > 0.0) {
+        const int half = hd / 2;
+        for (int c = 0; c < half; ++c) {
+          const double ang = p * std::pow(theta, -2.0 * c / hd);
+          const double cs = std::cos(ang), sn = std::sin(ang);
+          const double a = v[c], b = v[c + half];
+          v[c] = a * cs - b * sn;
+          v[c + half] = a * sn + b * cs;
+        }
+      }
+    }
+  }
+}
+
 void oracle_attention_rows(int n, int hq, int hkv, int hd, const double* q,
                            const double* k, const double* v, double* o,
                            const int32_t* rows, int nrows) {
@@ -218,9 +257,21 @@ void oracle_gated_scatter(int64_t M, int d, double* x, const int64_t* rows, cons
 //   u = RMSNorm(xs) * g1;  q,k,v = u Wq^T, u Wk^T, u Wv^T
 //   o = causal GQA attention;  a = o Wo^T;  h = xs + a
 //   v2 = RMSNorm(h) * g2;  f = (silu(v2 Wg^T) * (v2 Wu^T)) Wd^T
+// As oracle_block_rows; compact row j sits at original position pos[j] (NULL: j),
+// which only the rotary embedding sees.
+void oracle_block_rows_pos(const oracle_dims* dm, int n, const double* xs,
+                           const oracle_layer_w* w, const int32_t* rows, int nrows,
+                           double* a_out, double* f_out, const int32_t* pos);
+
 void oracle_block_rows(const oracle_dims* dm, int n, const double* xs,
                        const oracle_layer_w* w, const int32_t* rows, int nrows,
                        double* a_out, double* f_out) {
+  oracle_block_rows_pos(dm, n, xs, w, rows, nrows, a_out, f_out, nullptr);
+}
+
+void oracle_block_rows_pos(const oracle_dims* dm, int n, const double* xs,
+                           const oracle_layer_w* w, const int32_t* rows, int nrows,
+                           double* a_out, double* f_out, const int32_t* pos) {
   const int d = dm->d, hq = dm->hq, hkv = dm->hkv, hd = dm->hd, F = dm->F;
   const int nr = rows ? nrows : n;
   if (nr <= 0) return;
@@ -236,6 +287,8 @@ void oracle_block_rows(const oracle_dims* dm, int n, const double* xs,
   std::vector<double> kk((int64_t)nkv * hkv * hd), vv((int64_t)nkv * hkv * hd);
   oracle_linear(nkv, d, hkv * hd, u.data(), w->wk, kk.data());
   oracle_linear(nkv, d, hkv * hd, u.data(), w->wv, vv.data());
+  if (w->gk || w->rope_theta > 0.0)
+    oracle_qk_transform(nkv, hkv, hd, kk.data(), w->gk, dm->eps, w->rope_theta, pos);
   // Queries for the requested rows only.
   std::vector<double> ur((int64_t)nr * d), xr((int64_t)nr * d);
   for (int i = 0; i < nr; ++i) {
@@ -247,6 +300,14 @@ void oracle_block_rows(const oracle_dims* dm, int n, const double* xs,
   {
     std::vector<double> qr((int64_t)nr * hq * hd);
     oracle_linear(nr, d, hq * hd, ur.data(), w->wq, qr.data());
+    if (w->gq || w->rope_theta > 0.0) {
+      std::vector<int32_t> qpos(nr);
+      for (int i = 0; i < nr; ++i) {
+        const int src = rows ? rows[i] : i;
+        qpos[i] = pos ? pos[src] : src;
+      }
+      oracle_qk_transform(nr, hq, hd, qr.data(), w->gq, dm->eps, w->rope_theta, qpos.data());
+    }
     for (int i = 0; i < nr; ++i) {
       const int dst = rows ? rows[i] : i;
       std::memcpy(&qfull[(int64_t)dst * hq * hd], &qr[(int64_t)i * hq * hd],
@@ -303,12 +364,16 @@ void oracle_block_fullkv(const oracle_dims* dm, int T, const double* x_seq,
   std::vector<double> kk((int64_t)T * hkv * hd), vv((int64_t)T * hkv * hd);
   oracle_linear(T, d, hkv * hd, u.data(), w->wk, kk.data());
   oracle_linear(T, d, hkv * hd, u.data(), w->wv, vv.data());
+  if (w->gk || w->rope_theta > 0.0)
+    oracle_qk_transform(T, hkv, hd, kk.data(), w->gk, dm->eps, w->rope_theta, nullptr);
   std::vector<double> us((int64_t)n * d), xr((int64_t)n * d), qs((int64_t)n * hq * hd);
   for (int j = 0; j < n; ++j) {
     std::memcpy(&us[(int64_t)j * d], &u[(int64_t)pos[j] * d], sizeof(double) * d);
     std::memcpy(&xr[(int64_t)j * d], &x_seq[(int64_t)pos[j] * d], sizeof(double) * d);
   }
   oracle_linear(n, d, hq * hd, us.data(), w->wq, qs.data());
+  if (w->gq || w->rope_theta > 0.0)
+    oracle_qk_transform(n, hq, hd, qs.data(), w->gq, dm->eps, w->rope_theta, pos);
   std::vector<double> qfull((int64_t)T * hq * hd, 0.0);
   for (int j = 0; j < n; ++j)
     std::memcpy(&qfull[(int64_t)pos[j] * hq * hd], &qs[(int64_t)j * hq * hd],
@@ -417,7 +482,8 @@ int oracle_layer_fwd(const oracle_dims* dm, int kind, int K, int gate,
         std::memcpy(&xr[i * d], &xs[(int64_t)rows[i] * d], sizeof(double) * d);
       oracle_ffn_rows(dm, (int)rows.size(), xr.data(), w, f.data());
     } else {
-      oracle_block_rows(dm, n, xs.data(), w, rows.data(), (int)rows.size(), a.data(), f.data());
+      oracle_block_rows_pos(dm, n, xs.data(), w, rows.data(), (int)rows.size(), a.data(), f.data(),
+                            &idx[(int64_t)b * n]);   // original positions for the rotation
     }
     for (size_t i = 0; i < rows.size(); ++i) {
       const int j = rows[i];
@@ -495,7 +561,7 @@ int oracle_layer_threshold(const oracle_dims* dm, int gate, const oracle_layer_w
     std::vector<int32_t> rows(n);
     std::iota(rows.begin(), rows.end(), 0);
     std::vector<double> a((size_t)n * d), f((size_t)n * d);
-    oracle_block_rows(dm, n, xs.data(), w, rows.data(), n, a.data(), f.data());
+    oracle_block_rows_pos(dm, n, xs.data(), w, rows.data(), n, a.data(), f.data(), pos.data());
     for (int j = 0; j < n; ++j) {
       const int t = pos[j];
       const double rt = r[(int64_t)b * T + t];
