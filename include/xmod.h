@@ -92,10 +92,20 @@ typedef struct {
 } xmod_dims;
 
 /* One layer's weights (device pointers, dims->dtype). w_router is used by sparse
- * layers only; varsigma is the per-layer scalar of Eq. 7. */
+ * layers only; varsigma is the per-layer scalar of Eq. 7.
+ * Optional Qwen3-style attention extras (the X-MoD notes name Qwen3 backbones; the
+ * NEXT item "RoPE at original positions, QK-norm"), all off when zero / NULL:
+ *   q_norm, k_norm  [head_dim] QK-norm gains: every head's q (k) vector is
+ *                   RMS-normalised (rms_eps) and scaled by them after the projection;
+ *   rope_theta      rotary embedding base: after QK-norm, q and k are rotated at the
+ *                   token's ORIGINAL position t in its sequence (not its compact index),
+ *                   pairing dimension c with c + head_dim/2 at angle
+ *                   t * rope_theta^(-2c/head_dim). */
 typedef struct {
   const void *w_router, *rms1, *wq, *wk, *wv, *wo, *rms2, *w_gate, *w_up, *w_down;
   float varsigma;
+  const void *q_norm, *k_norm;
+  float rope_theta;
 } xmod_layer_weights;
 
 /* Library version string. */

@@ -133,6 +133,8 @@ bool weights_ok(const xmod_layer_weights* w, int kind) {
     for (const void* p : ps)
       if (!aligned16(p)) return false;
   }
+  if (!aligned16_or_null(w->q_norm) || !aligned16_or_null(w->k_norm)) return false;
+  if (!isfinite(w->rope_theta) || w->rope_theta < 0.0f) return false;
   return isfinite(w->varsigma);
 }
 
@@ -151,6 +153,20 @@ struct Ragged {
 // With scatter, xs_new (if not NULL) receives the updated compact rows [B*n, d].
 // With rg (threshold routing), n is T: buffers are sized for every token, kernels
 // compute the rows the routing picked (tensor-core path only).
+
+bool qk_extras(const xmod_layer_weights* w) {
+  return w->q_norm || w->k_norm || w->rope_theta > 0.0f;
+}
+
+// QK-norm and rotary embedding of a projection's q (or k) heads, in place.
+int qk_extras_run(const Ctx& c, const xmod_dims* dm, int64_t M, const int32_t* M_dev, void* x,
+                  int ld, int col0, int heads, const void* gain, const xmod_layer_weights* w,
+                  const int32_t* pos_idx, const int32_t* pos_tok, int seqT) {
+  XMOD_RUN("qk_norm_rope",
+           launch_qk_transform(c, dm->dtype, M, M_dev, x, ld, col0, heads, dm->head_dim, gain,
+                               dm->rms_eps, w->rope_theta, pos_idx, pos_tok, seqT));
+  return XMOD_OK;
+}
 
 // Attention of a Selected-Q / full-KV layer (X-MoD notes, "mechanism controls": the
 // selected tokens are the queries, every token provides keys and values): o [B*n, qw]
@@ -207,12 +223,22 @@ int fullkv_attention(const Ctx& c, const xmod_dims* dm, const Layout& L, void* w
     ek.out = kv + es * kw;
     XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, B * T, kw, d, u_all, d, w->wv, d, nullptr, ek));
   }
+  if (qk_extras(w)) {   // keys of every token at their positions
+    const int st = qk_extras_run(c, dm, (int64_t)B * T, nullptr, kv, 2 * kw, 0, hkv, w->k_norm,
+                                 w, nullptr, nullptr, T);
+    if (st) return st;
+  }
   XMOD_RUN("gather_rmsnorm", launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1,
                                                    dm->rms_eps, u_sel));
   if (tc)
     XMOD_RUN("gemm_qkv", launch_gemm_tc(c, pq, eq));
   else
     XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, B * n, qw, d, u_sel, d, w->wq, d, nullptr, eq));
+  if (qk_extras(w)) {   // queries at their original positions
+    const int st = qk_extras_run(c, dm, (int64_t)B * n, nullptr, q, qw, 0, hq, w->q_norm, w, idx,
+                                 nullptr, T);
+    if (st) return st;
+  }
   if (tc) {
     AttnKv akv;
     akv.k = kv;
@@ -305,6 +331,14 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
         XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wk, d, nullptr, e));
         e.out = qkv + es * (qw + kw);
         XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wv, d, nullptr, e));
+      }
+      if (qk_extras(w)) {   // q and k heads at the tokens' original positions
+        const int32_t* ptok = rg ? rg->tok : nullptr;
+        const int seqT = rg ? T : n;
+        int st = qk_extras_run(c, dm, M, M_dev, qkv, qkv_w, 0, hq, w->q_norm, w, idx, ptok, seqT);
+        if (!st)
+          st = qk_extras_run(c, dm, M, M_dev, qkv, qkv_w, qw, hkv, w->k_norm, w, idx, ptok, seqT);
+        if (st) return st;
       }
       // 3. causal GQA attention among the n rows of each sequence
       if (tc_qkv && tc_attn)

@@ -868,6 +868,89 @@ cudaError_t launch_rmsnorm_f32in(const Ctx& c, xmod_dtype dt, int64_t M, int d, 
   return cudaGetLastError();
 }
 
+// ================================================================ QK-norm and rotary embedding
+
+// One warp per row of x [rows, ld] (bf16 or fp32), heads of hd (a multiple of 32)
+// starting at column col0. Each lane holds E = hd / 32 consecutive elements, so the
+// rotation partner c + hd/2 of a lane's element c sits in lane ^ 16 at the same slot.
+// Position of row m: pos_idx ? pos_idx[m] : pos_tok ? pos_tok[m] % seqT : m % seqT.
+template <typename T, int E>
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+qk_transform_kernel(int64_t M, const int32_t* __restrict__ M_dev, T* __restrict__ x, int ld,
+                    int col0, int heads, const T* __restrict__ gain, float eps, double theta,
+                    const int32_t* __restrict__ pos_idx, const int32_t* __restrict__ pos_tok,
+                    int seqT) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int HD = 32 * E;
+  __shared__ double inv_freq[HD / 2];
+  for (int c = threadIdx.x; c < HD / 2; c += blockDim.x)
+    inv_freq[c] = theta > 0.0 ? exp2(-(2.0 * c / HD) * log2(theta)) : 0.0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
+  if (m >= M || (M_dev && m >= *M_dev)) return;
+  const int64_t pos = pos_idx ? pos_idx[m] : pos_tok ? pos_tok[m] % seqT : m % seqT;
+  const bool first = lane < 16;
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int h = 0; h < heads; ++h) {
+    T* p = x + m * ld + col0 + h * HD + lane * E;
+    float v[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = Elem<T>::to_f(p[e]);
+    if (gain) {
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
+      const float inv = rsqrtf(warp_sum(ss) / (float)HD + eps);
+#pragma unroll
+      for (int e = 0; e < E; ++e) v[e] = v[e] * inv * Elem<T>::to_f(gain[lane * E + e]);
+    }
+    if (theta > 0.0) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float other = __shfl_xor_sync(0xffffffffu, v[e], 16);
+        const int c = (first ? lane : lane - 16) * E + e;   // pair index, < HD / 2
+        double ang = (double)pos * inv_freq[c];
+        ang -= two_pi * floor(ang / two_pi);
+        float sn, cs;
+        sincosf((float)ang, &sn, &cs);
+        v[e] = first ? v[e] * cs - other * sn : other * sn + v[e] * cs;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) p[e] = Elem<T>::from_f(v[e]);
+  }
+}
+
+cudaError_t launch_qk_transform(const Ctx& c, xmod_dtype dt, int64_t M, const int32_t* M_dev,
+                                void* x, int ld, int col0, int heads, int hd, const void* gain,
+                                float eps, float theta, const int32_t* pos_idx,
+                                const int32_t* pos_tok, int seqT) {
+  if (M <= 0 || heads <= 0) return cudaSuccess;
+  if (hd % 32 || hd > 128 || seqT <= 0) return cudaErrorInvalidValue;
+  const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
+#define XMOD_QK_CASE(TT, EE)                                                                  \
+  return launch_pdl(qk_transform_kernel<TT, EE>, dim3(blocks), dim3(ROW_WARPS * 32), 0,        \
+                    c.stream, M, M_dev, (TT*)x, ld, col0, heads, (const TT*)gain, eps,         \
+                    (double)theta, pos_idx, pos_tok, seqT);
+  if (dt == XMOD_BF16) {
+    switch (hd / 32) {
+      case 1: XMOD_QK_CASE(__nv_bfloat16, 1)
+      case 2: XMOD_QK_CASE(__nv_bfloat16, 2)
+      case 4: XMOD_QK_CASE(__nv_bfloat16, 4)
+    }
+  } else {
+    switch (hd / 32) {
+      case 1: XMOD_QK_CASE(float, 1)
+      case 2: XMOD_QK_CASE(float, 2)
+      case 4: XMOD_QK_CASE(float, 4)
+    }
+  }
+#undef XMOD_QK_CASE
+  return cudaErrorInvalidValue;
+}
+
 // ================================================================ gated scatter
 
 template <typename T>

@@ -44,7 +44,9 @@ class Dims(ctypes.Structure):
 
 class LayerWeights(ctypes.Structure):
     NAMES = ("w_router", "rms1", "wq", "wk", "wv", "wo", "rms2", "w_gate", "w_up", "w_down")
-    _fields_ = [(n, ctypes.c_void_p) for n in NAMES] + [("varsigma", ctypes.c_float)]
+    _fields_ = [(n, ctypes.c_void_p) for n in NAMES] + [
+        ("varsigma", ctypes.c_float), ("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p),
+        ("rope_theta", ctypes.c_float)]
 
 
 ROUTE_TOPK, ROUTE_THRESHOLD = 0, 1
@@ -157,10 +159,13 @@ def dims(B, T, d, n_heads, n_kv_heads, head_dim, d_ff, dtype=BF16, rms_eps=1e-6)
     return Dims(B, T, d, n_heads, n_kv_heads, head_dim, d_ff, dtype, rms_eps)
 
 
-def layer_weights(tensors: dict, varsigma: float = 1.0) -> LayerWeights:
-    """tensors: name -> device tensor for the names of LayerWeights.NAMES. The struct
-    keeps a reference to the tensors so their memory outlives every call using it."""
-    lw = LayerWeights(*[_p(tensors.get(n)) for n in LayerWeights.NAMES], float(varsigma))
+def layer_weights(tensors: dict, varsigma: float = 1.0, rope_theta: float = 0.0) -> LayerWeights:
+    """tensors: name -> device tensor for the names of LayerWeights.NAMES, plus the
+    optional QK-norm gains "q_norm" / "k_norm" [head_dim]; rope_theta > 0 turns on the
+    rotary embedding. The struct keeps a reference to the tensors so their memory
+    outlives every call using it."""
+    lw = LayerWeights(*[_p(tensors.get(n)) for n in LayerWeights.NAMES], float(varsigma),
+                      _p(tensors.get("q_norm")), _p(tensors.get("k_norm")), float(rope_theta))
     lw._keep = dict(tensors)
     return lw
 

@@ -11,7 +11,8 @@ from sparse_depth_token_gb300 import inputs as I
 torch = pytest.importorskip("torch")
 
 ABI_NAMES = {"w_r": "w_router", "g1": "rms1", "wq": "wq", "wk": "wk", "wv": "wv", "wo": "wo",
-             "g2": "rms2", "wg": "w_gate", "wu": "w_up", "wd": "w_down"}
+             "g2": "rms2", "wg": "w_gate", "wu": "w_up", "wd": "w_down",
+             "gq": "q_norm", "gk": "k_norm"}
 
 
 def need_gpu():
@@ -42,8 +43,10 @@ def dev_layer(arrs: dict, dtype: str):
 
 
 def oracle_layer(arrs: dict, dtype: str) -> O.Layer:
-    return O.Layer({k: I.to_f64(v, dtype) for k, v in arrs.items() if k in ABI_NAMES},
-                   arrs["varsigma"])
+    d = {k: I.to_f64(v, dtype) for k, v in arrs.items() if k in ABI_NAMES}
+    if arrs.get("rope_theta"):
+        d["rope_theta"] = float(arrs["rope_theta"])
+    return O.Layer(d, arrs["varsigma"])
 
 
 def xmod_dims(w: I.Workload, **over):
