@@ -37,21 +37,44 @@ ABI_NAMES = {"w_r": "w_router", "g1": "rms1", "wq": "wq", "wk": "wk", "wv": "wv"
              "g2": "rms2", "wg": "w_gate", "wu": "w_up", "wd": "w_down"}
 
 
-def schedule(w: I.Workload):
-    """Layer kinds of the Eq. 3 stack (1 = sparse) for counting work."""
+DENSE, SPARSE, ATTN, RFFN, FULLKV = 0, 1, 2, 3, 4   # the library's layer kinds
+VARIANT = "xmod"   # set from --variant before any schedule is built
+
+
+def schedule(w: I.Workload, variant=None):
+    """Layer kinds in execution order. xmod: the Eq. 3 stack; routed_ffn: the Routed-FFN
+    control (([FullAttn] + [Routed-FFN] x K) x A between the anchors); fullkv: the
+    Selected-Q / full-KV control (the Eq. 3 stack with full-sequence keys and values)."""
+    variant = variant or VARIANT
     ak = int(round(w.A * w.K))
-    return [0] * w.N0 + ([1] * ak + [0]) * w.N1
+    if variant == "routed_ffn":
+        A = ak // w.K
+        return [DENSE] * w.N0 + (([ATTN] + [RFFN] * w.K) * A + [DENSE]) * w.N1
+    sp = FULLKV if variant == "fullkv" else SPARSE
+    return [DENSE] * w.N0 + ([sp] * ak + [DENSE]) * w.N1
+
+
+def routed(k) -> bool:
+    return k in (SPARSE, RFFN, FULLKV)
 
 
 def workload_config(w: I.Workload) -> dict:
     kinds = schedule(w)
+    n_routed = sum(1 for k in kinds if routed(k))
+    if VARIANT == "routed_ffn":
+        what = (f"Routed-FFN control {n_routed} Routed-FFN(K={w.K}) + {kinds.count(ATTN)} "
+                f"FullAttn + {kinds.count(DENSE)} Dense")
+    elif VARIANT == "fullkv":
+        what = f"Selected-Q/full-KV control {n_routed} Sparse(K={w.K}) + {kinds.count(DENSE)} Dense"
+    else:
+        what = f"X-MoD stack {n_routed} Sparse(K={w.K}) + {kinds.count(DENSE)} Dense"
     return {
-        "workload": f"{w.name}: X-MoD stack {sum(kinds)} Sparse(K={w.K}) + {len(kinds) - sum(kinds)} "
-                    f"Dense (Eq. 3, N0={w.N0}, N1={w.N1}, A={w.A}), Eq. "
+        "workload": f"{w.name}: {what} "
+                    f"(Eq. 3, N0={w.N0}, N1={w.N1}, A={w.A}), Eq. "
                     f"{'7' if w.gate == 0 else '6'} gating, d={w.d}, {w.hq}/{w.hkv} heads, "
                     f"head_dim {w.hd}, SwiGLU d_ff={w.F}",
         "B_per_gpu": w.B, "T": w.T, "K": w.K,
-        "selected_tokens_per_step_per_gpu": sum(kinds) * w.B * (w.T // w.K),
+        "selected_tokens_per_step_per_gpu": n_routed * w.B * (w.T // w.K),
         "l2": "no flush: one step streams 1.7 GB of distinct layer weights and a 100 MB "
               "stream, both larger than the 129 MB L2",
         "inputs": "seeded synthetic: x~N(0,1), matrices~N(0,0.02^2), w_r~N(0,1/d), "
@@ -73,7 +96,8 @@ def algorithmic_work(w: I.Workload, sel_counts=None) -> dict:
     kinds = schedule(w)
     run_left = 0   # layers left in the current run of sparse layers (logits kept current)
     ls = 0
-    for l, sparse in enumerate(kinds):
+    for l, kind in enumerate(kinds):
+        sparse = routed(kind)
         n = w.T // w.K if sparse else w.T
         M = w.B * n
         ns = [n] * w.B
@@ -85,7 +109,7 @@ def algorithmic_work(w: I.Workload, sel_counts=None) -> dict:
         if sparse:
             if run_left == 0:   # one pass over the stream: logits of up to 32 layers
                 run = 1
-                while run < ROUTER_RUN and l + run < len(kinds) and kinds[l + run]:
+                while run < ROUTER_RUN and l + run < len(kinds) and kinds[l + run] == kind:
                     run += 1
                 run_left = run
                 add("router", w.B * w.T * w.d * es + 4 * run * w.B * w.T)
@@ -93,10 +117,24 @@ def algorithmic_work(w: I.Workload, sel_counts=None) -> dict:
             if run_left > 0:    # logits of the updated rows for the rest of the run
                 add("router_refresh", M * w.d * es + 4 * run_left * M)
             add("topk", 4 * w.B * w.T + 8 * M)
-        add("gather_rmsnorm", 2 * M * w.d * es)
-        add("gemm_qkv", 2 * M * w.d * (w.hq + 2 * w.hkv) * w.hd)
-        add("attention", 2 * sum(v * v for v in ns) * w.hd * w.hq)
+        if kind == RFFN:   # FFN half only: RMSNorm2 fused into the gather
+            add("gather_rmsnorm", 2 * M * w.d * es)
+            add("gemm_gate_up_swiglu", 4 * M * w.d * w.F)
+            add("gemm_down_scatter", 2 * M * w.F * w.d)
+            continue
+        if kind == FULLKV:   # every token's RMSNorm1 and k, v; q for the selected
+            BT = w.B * w.T
+            add("gather_rmsnorm", 2 * (BT + M) * w.d * es)
+            add("gemm_qkv", 2 * BT * w.d * 2 * w.hkv * w.hd + 2 * M * w.d * w.hq * w.hd)
+            # a query at position p sees p + 1 keys: T / 2 on average
+            add("attention", 4 * M * (w.T / 2) * w.hd * w.hq)
+        else:
+            add("gather_rmsnorm", 2 * M * w.d * es)
+            add("gemm_qkv", 2 * M * w.d * (w.hq + 2 * w.hkv) * w.hd)
+            add("attention", 2 * sum(v * v for v in ns) * w.hd * w.hq)
         add("gemm_o_residual", 2 * M * w.hq * w.hd * w.d)
+        if kind == ATTN:
+            continue
         add("rmsnorm2", M * w.d * (4 + es))
         add("gemm_gate_up_swiglu", 4 * M * w.d * w.F)
         add("gemm_down_scatter", 2 * M * w.F * w.d)
@@ -197,7 +235,8 @@ def oracle_sample(w: I.Workload, budget_s: float = 15.0, max_reps: int = 50):
     n = w.T // w.K
     reps, t0 = 0, time.perf_counter()
     while True:
-        O.layer_fwd(dm, O.SPARSE, w.K, w.gate, L, x, bias=bias)
+        O.layer_fwd(dm, {"routed_ffn": O.RFFN, "fullkv": O.FULLKV}.get(VARIANT, O.SPARSE), w.K,
+                    w.gate, L, x, bias=bias)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= max_reps:
@@ -224,7 +263,8 @@ def run_reference(args):
     n = w.T // w.K
 
     def step():
-        O.layer_fwd(dm, O.SPARSE, w.K, w.gate, L, x, bias=bias)
+        O.layer_fwd(dm, {"routed_ffn": O.RFFN, "fullkv": O.FULLKV}.get(VARIANT, O.SPARSE), w.K,
+                    w.gate, L, x, bias=bias)
 
     for _ in range(args.warmup):
         step()
@@ -268,11 +308,11 @@ def run_xmod(args):
 
     w = I.WORKLOADS[args.workload]
     kinds = schedule(w)
-    n_sparse = sum(kinds)
+    n_sparse = sum(1 for k in kinds if routed(k))
     sel_per_step = n_sparse * w.B * (w.T // w.K)
     # per-rank data: the same weights, different sequences
     wr = w.replace(seed=w.seed + 1000 * rank) if rank else w
-    layers = I.all_layer_weights(w)
+    layers = I.all_layer_weights(w, len(kinds))
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
 
     def to_dev(a):
@@ -281,7 +321,13 @@ def run_xmod(args):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     dev_layers = [{ABI_NAMES[k]: to_dev(v) for k, v in l.items() if k in ABI_NAMES} for l in layers]
-    abi = [X.layer_weights(d, l["varsigma"]) for d, l in zip(dev_layers, layers)]
+    if args.qwen3:   # QK-norm (unit gains) and RoPE at the tokens' original positions
+        ones = to_dev(np.ones(w.hd, np.float32) if w.dtype != "bf16" else
+                      I.f32_to_bf16_bits(np.ones(w.hd, np.float32)))
+        for dl in dev_layers:
+            dl["q_norm"] = dl["k_norm"] = ones
+    theta = 1e6 if args.qwen3 else 0.0
+    abi = [X.layer_weights(d, l["varsigma"], theta) for d, l in zip(dev_layers, layers)]
     x_host = I.residual_stream(wr)
     bias_host = I.router_bias(wr)
     x0 = to_dev(x_host)
@@ -295,7 +341,12 @@ def run_xmod(args):
     plain = args.routing == "topk" and args.bias_step == 0.0
 
     def run_stack(stats=None):
-        if plain and stats is None:
+        if VARIANT != "xmod":
+            X.stack_fwd_sched(dm, w.K, kinds, w.gate, abi, x, bias, ws,
+                              bias_step=args.bias_step, layer_stats=stats,
+                              routing=X.ROUTE_THRESHOLD if args.routing == "threshold"
+                              else X.ROUTE_TOPK, stream=stream)
+        elif plain and stats is None:
             X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, x, bias, ws, stream)
         else:
             X.stack_fwd_ex(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, x, bias, ws,
@@ -444,6 +495,10 @@ def run_xmod(args):
     if rank == 0:
         cfg = workload_config(w)
         cfg["parallelism"] = f"replicas x{world} (sequences sharded, no collective)"
+        if VARIANT != "xmod":
+            cfg["variant"] = VARIANT
+        if args.qwen3:
+            cfg["attention"] = "QK-norm + RoPE (theta 1e6) at original positions"
         if not plain:
             cfg["routing"] = args.routing
             cfg["bias_step"] = args.bias_step
@@ -482,7 +537,13 @@ def main():
                     help="token selection of the sparse layers (threshold: r >= 1/2)")
     ap.add_argument("--bias-step", type=float, default=0.0,
                     help="token-choice bias growth per selection inside a block (0: constant)")
+    ap.add_argument("--variant", choices=["xmod", "routed_ffn", "fullkv"], default="xmod",
+                    help="X-MoD stack, or one of the mechanism controls")
+    ap.add_argument("--qwen3", action="store_true",
+                    help="QK-norm and RoPE (base 1e6) in every attending layer")
     args = ap.parse_args()
+    global VARIANT
+    VARIANT = args.variant
     if args.B is not None or args.A is not None:
         w = I.WORKLOADS[args.workload]
         A = w.A if args.A is None else args.A

@@ -158,13 +158,16 @@ bool qk_extras(const xmod_layer_weights* w) {
   return w->q_norm || w->k_norm || w->rope_theta > 0.0f;
 }
 
-// QK-norm and rotary embedding of a projection's q (or k) heads, in place.
+// QK-norm and rotary embedding of a projection's q heads (from q_col0) and k heads
+// (from k_col0) in the same rows, in place.
 int qk_extras_run(const Ctx& c, const xmod_dims* dm, int64_t M, const int32_t* M_dev, void* x,
-                  int ld, int col0, int heads, const void* gain, const xmod_layer_weights* w,
-                  const int32_t* pos_idx, const int32_t* pos_tok, int seqT) {
+                  int ld, int q_col0, int q_heads, int k_col0, int k_heads,
+                  const xmod_layer_weights* w, const int32_t* pos_idx, const int32_t* pos_tok,
+                  int seqT) {
   XMOD_RUN("qk_norm_rope",
-           launch_qk_transform(c, dm->dtype, M, M_dev, x, ld, col0, heads, dm->head_dim, gain,
-                               dm->rms_eps, w->rope_theta, pos_idx, pos_tok, seqT));
+           launch_qk_transform(c, dm->dtype, M, M_dev, x, ld, q_col0, q_heads, w->q_norm, k_col0,
+                               k_heads, w->k_norm, dm->head_dim, dm->rms_eps, w->rope_theta,
+                               pos_idx, pos_tok, seqT));
   return XMOD_OK;
 }
 
@@ -224,8 +227,8 @@ int fullkv_attention(const Ctx& c, const xmod_dims* dm, const Layout& L, void* w
     XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, B * T, kw, d, u_all, d, w->wv, d, nullptr, ek));
   }
   if (qk_extras(w)) {   // keys of every token at their positions
-    const int st = qk_extras_run(c, dm, (int64_t)B * T, nullptr, kv, 2 * kw, 0, hkv, w->k_norm,
-                                 w, nullptr, nullptr, T);
+    const int st = qk_extras_run(c, dm, (int64_t)B * T, nullptr, kv, 2 * kw, 0, 0, 0, hkv, w,
+                                 nullptr, nullptr, T);
     if (st) return st;
   }
   XMOD_RUN("gather_rmsnorm", launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1,
@@ -235,7 +238,7 @@ int fullkv_attention(const Ctx& c, const xmod_dims* dm, const Layout& L, void* w
   else
     XMOD_RUN("gemm_qkv", launch_gemm_simt(c, dt, B * n, qw, d, u_sel, d, w->wq, d, nullptr, eq));
   if (qk_extras(w)) {   // queries at their original positions
-    const int st = qk_extras_run(c, dm, (int64_t)B * n, nullptr, q, qw, 0, hq, w->q_norm, w, idx,
+    const int st = qk_extras_run(c, dm, (int64_t)B * n, nullptr, q, qw, 0, hq, 0, 0, w, idx,
                                  nullptr, T);
     if (st) return st;
   }
@@ -335,9 +338,8 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
       if (qk_extras(w)) {   // q and k heads at the tokens' original positions
         const int32_t* ptok = rg ? rg->tok : nullptr;
         const int seqT = rg ? T : n;
-        int st = qk_extras_run(c, dm, M, M_dev, qkv, qkv_w, 0, hq, w->q_norm, w, idx, ptok, seqT);
-        if (!st)
-          st = qk_extras_run(c, dm, M, M_dev, qkv, qkv_w, qw, hkv, w->k_norm, w, idx, ptok, seqT);
+        const int st =
+            qk_extras_run(c, dm, M, M_dev, qkv, qkv_w, 0, hq, qw, hkv, w, idx, ptok, seqT);
         if (st) return st;
       }
       // 3. causal GQA attention among the n rows of each sequence

@@ -90,13 +90,15 @@ struct RouteTrack {
 // r_sel [B, n] = sigmoid(ranked logit at idx) if not NULL.
 cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32_t* idx,
                         float* r_sel, const RouteTrack* tr = nullptr);
-// QK-norm (gain [hd], NULL: none) and rotary embedding (theta, 0: none) of the heads
-// of hd columns starting at col0 in rows x [M, ld] (only m < *M_dev if given), in place.
-// Row m sits at position pos_idx[m], else pos_tok[m] % seqT, else m % seqT.
+// QK-norm (gains [hd], NULL: none) and rotary embedding (theta, 0: none), in place, of
+// q_heads heads from column q_col0 and k_heads heads from k_col0 (hd columns each) in
+// rows x [M, ld] (only m < *M_dev if given). Row m sits at position pos_idx[m], else
+// pos_tok[m] % seqT, else m % seqT.
 cudaError_t launch_qk_transform(const Ctx& c, xmod_dtype dt, int64_t M, const int32_t* M_dev,
-                                void* x, int ld, int col0, int heads, int hd, const void* gain,
-                                float eps, float theta, const int32_t* pos_idx,
-                                const int32_t* pos_tok, int seqT);
+                                void* x, int ld, int q_col0, int q_heads, const void* q_gain,
+                                int k_col0, int k_heads, const void* k_gain, int hd, float eps,
+                                float theta, const int32_t* pos_idx, const int32_t* pos_tok,
+                                int seqT);
 
 // Causal threshold rule over s [B, T] (ranked logit s - bias_step * count >= 0):
 // compact rows tok [<= B*T] (= b * T + t, sequence then position order), r_sel

@@ -870,70 +870,108 @@ cudaError_t launch_rmsnorm_f32in(const Ctx& c, xmod_dtype dt, int64_t M, int d, 
 
 // ================================================================ QK-norm and rotary embedding
 
-// One warp per row of x [rows, ld] (bf16 or fp32), heads of hd (a multiple of 32)
-// starting at column col0. Each lane holds E = hd / 32 consecutive elements, so the
-// rotation partner c + hd/2 of a lane's element c sits in lane ^ 16 at the same slot.
+// One warp per row of x [rows, ld] (bf16 or fp32), QK_HEADS heads loaded at a time:
+// the q heads (columns from q_col0, gains q_gain) come before the k heads (k_col0,
+// k_gain), each head of hd (a multiple of 32) elements. Each lane holds E = hd / 32 consecutive elements, so the rotation
+// partner c + hd/2 of a lane's element c sits in lane ^ 16 at the same slot.
 // Position of row m: pos_idx ? pos_idx[m] : pos_tok ? pos_tok[m] % seqT : m % seqT.
+// The angle pos * theta^(-2c/hd) is taken modulo one turn without losing the position's
+// bits: per pair c the turns per position, theta^(-2c/hd) / (2 pi), are kept as a
+// float hi + lo sum, and pos * hi is split exactly with an fma.
+constexpr int QK_HEADS = 4;
+
 template <typename T, int E>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 qk_transform_kernel(int64_t M, const int32_t* __restrict__ M_dev, T* __restrict__ x, int ld,
-                    int col0, int heads, const T* __restrict__ gain, float eps, double theta,
+                    int q_col0, int q_heads, const T* __restrict__ q_gain, int k_col0,
+                    int k_heads, const T* __restrict__ k_gain, float eps, double theta,
                     const int32_t* __restrict__ pos_idx, const int32_t* __restrict__ pos_tok,
                     int seqT) {
   pdl_trigger();
-  pdl_wait();
   constexpr int HD = 32 * E;
-  __shared__ double inv_freq[HD / 2];
-  for (int c = threadIdx.x; c < HD / 2; c += blockDim.x)
-    inv_freq[c] = theta > 0.0 ? exp2(-(2.0 * c / HD) * log2(theta)) : 0.0;
+  __shared__ float2 turns[HD / 2];
+  for (int c = threadIdx.x; c < HD / 2; c += blockDim.x) {
+    const double r = theta > 0.0 ? exp2(-(2.0 * c / HD) * log2(theta)) / 6.283185307179586 : 0.0;
+    const float hi = (float)r;
+    turns[c] = make_float2(hi, (float)(r - (double)hi));
+  }
   __syncthreads();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
   if (m >= M || (M_dev && m >= *M_dev)) return;
   const int64_t pos = pos_idx ? pos_idx[m] : pos_tok ? pos_tok[m] % seqT : m % seqT;
+  const float pf = (float)pos;   // exact: positions stay below 2^24
   const bool first = lane < 16;
-  const double two_pi = 6.283185307179586476925286766559;
-  for (int h = 0; h < heads; ++h) {
-    T* p = x + m * ld + col0 + h * HD + lane * E;
-    float v[E];
+  // the angles depend on the position and the pair only: once per row for every head
+  float cs[E], sn[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) v[e] = Elem<T>::to_f(p[e]);
-    if (gain) {
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
-      const float inv = rsqrtf(warp_sum(ss) / (float)HD + eps);
-#pragma unroll
-      for (int e = 0; e < E; ++e) v[e] = v[e] * inv * Elem<T>::to_f(gain[lane * E + e]);
-    }
+  for (int e = 0; e < E; ++e) {
+    cs[e] = 1.0f;
+    sn[e] = 0.0f;
     if (theta > 0.0) {
+      const float2 t = turns[(first ? lane : lane - 16) * E + e];
+      const float a = pf * t.x;
+      const float frac = (a - rintf(a)) + fmaf(pf, t.y, fmaf(pf, t.x, -a));
+      __sincosf(frac * 6.2831853f, &sn[e], &cs[e]);   // |angle| <= pi: the fast form suffices
+    }
+  }
+  const int heads = q_heads + k_heads;
+  for (int h0 = 0; h0 < heads; h0 += QK_HEADS) {
+    const int h_end = min(heads, h0 + QK_HEADS);
+    T* hp[QK_HEADS];   // QK_HEADS heads loaded together
+    float v[QK_HEADS][E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float other = __shfl_xor_sync(0xffffffffu, v[e], 16);
-        const int c = (first ? lane : lane - 16) * E + e;   // pair index, < HD / 2
-        double ang = (double)pos * inv_freq[c];
-        ang -= two_pi * floor(ang / two_pi);
-        float sn, cs;
-        sincosf((float)ang, &sn, &cs);
-        v[e] = first ? v[e] * cs - other * sn : other * sn + v[e] * cs;
+    for (int i = 0; i < QK_HEADS; ++i) {
+      const int h = h0 + i;
+      hp[i] = nullptr;
+      if (h < h_end) {
+        const bool is_q = h < q_heads;
+        hp[i] = x + m * ld + (is_q ? q_col0 + h * HD : k_col0 + (h - q_heads) * HD) + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[i][e] = Elem<T>::to_f(hp[i][e]);
       }
     }
 #pragma unroll
-    for (int e = 0; e < E; ++e) p[e] = Elem<T>::from_f(v[e]);
+    for (int i = 0; i < QK_HEADS; ++i) {
+      const int h = h0 + i;
+      if (h >= h_end) break;
+      const bool is_q = h < q_heads;
+      const T* gain = is_q ? q_gain : k_gain;
+      if (gain) {
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) ss = fmaf(v[i][e], v[i][e], ss);
+        const float inv = rsqrtf(warp_sum(ss) / (float)HD + eps);
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[i][e] = v[i][e] * inv * Elem<T>::to_f(gain[lane * E + e]);
+      }
+      if (theta > 0.0) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float other = __shfl_xor_sync(0xffffffffu, v[i][e], 16);
+          v[i][e] = first ? v[i][e] * cs[e] - other * sn[e] : other * sn[e] + v[i][e] * cs[e];
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) hp[i][e] = Elem<T>::from_f(v[i][e]);
+    }
   }
 }
 
 cudaError_t launch_qk_transform(const Ctx& c, xmod_dtype dt, int64_t M, const int32_t* M_dev,
-                                void* x, int ld, int col0, int heads, int hd, const void* gain,
-                                float eps, float theta, const int32_t* pos_idx,
-                                const int32_t* pos_tok, int seqT) {
-  if (M <= 0 || heads <= 0) return cudaSuccess;
-  if (hd % 32 || hd > 128 || seqT <= 0) return cudaErrorInvalidValue;
+                                void* x, int ld, int q_col0, int q_heads, const void* q_gain,
+                                int k_col0, int k_heads, const void* k_gain, int hd, float eps,
+                                float theta, const int32_t* pos_idx, const int32_t* pos_tok,
+                                int seqT) {
+  if (M <= 0 || q_heads + k_heads <= 0) return cudaSuccess;
+  if (hd % 32 || hd > 128 || seqT <= 0 || seqT >= (1 << 24)) return cudaErrorInvalidValue;
   const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
 #define XMOD_QK_CASE(TT, EE)                                                                  \
   return launch_pdl(qk_transform_kernel<TT, EE>, dim3(blocks), dim3(ROW_WARPS * 32), 0,        \
-                    c.stream, M, M_dev, (TT*)x, ld, col0, heads, (const TT*)gain, eps,         \
-                    (double)theta, pos_idx, pos_tok, seqT);
+                    c.stream, M, M_dev, (TT*)x, ld, q_col0, q_heads, (const TT*)q_gain,        \
+                    k_col0, k_heads, (const TT*)k_gain, eps, (double)theta, pos_idx, pos_tok,  \
+                    seqT);
   if (dt == XMOD_BF16) {
     switch (hd / 32) {
       case 1: XMOD_QK_CASE(__nv_bfloat16, 1)
