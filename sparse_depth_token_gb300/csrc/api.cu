@@ -55,7 +55,7 @@ constexpr int kRouterRows = 2 * kRouterRun;
 
 // Workspace carve-up. M rows of block scratch cover a dense layer (M = B*T).
 struct Layout {
-  size_t status, s, idx, r_sel, u, qkv, vt, o, h, hidden, wr, count, last, seq, total;
+  size_t status, s, idx, r_sel, u, qkv, vt, o, h, hidden, wr, count, last, seq, rowss, total;
 };
 
 Layout layout(const xmod_dims* dm, int K) {
@@ -83,6 +83,7 @@ Layout layout(const xmod_dims* dm, int K) {
   L.count = off;  off = align_up(off + 4 * BT);   // token-choice bias state of a block
   L.last = off;   off = align_up(off + 4 * BT);
   L.seq = off;    off = align_up(off + 4 * (2 * (size_t)dm->B + 1));   // threshold rows
+  L.rowss = off;  off = align_up(off + 4 * M * (size_t)(dm->d / 32));   // h^2 sums per chunk
   L.total = off;
   return L;
 }
@@ -281,6 +282,18 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
     rm.tok = rg->tok;
     rm.M_dev = M_dev;
   }
+  // RMSNorm2 folded into the o-projection and gate/up epilogues (tensor-core path)
+  float* rowss = (float*)at(ws, L.rowss);
+  Epilogue eg;   // 6. hidden = silu(v2 Wg^T) * (v2 Wu^T), set up here for the fold test
+  eg.kind = EPI_SWIGLU;
+  eg.out = hidden;
+  eg.ldo = F;
+  GemmTcProblem pg;
+  pg.M = M; pg.N = F; pg.K = d; pg.A = v2; pg.lda = d; pg.ldb = d;
+  pg.B[0] = w->w_gate; pg.B[1] = w->w_up; pg.nB = 2;
+  pg.M_dev = M_dev;
+  const bool gate_up_tc = tc && gemm_tc_supported(pg, eg);
+  bool fold2 = gate_up_tc && part == PART_ALL && d % 128 == 0;
   if (part == PART_FFN) {   // FFN half only: v2 = RMSNorm(x_sel) * rms2, a = 0
     XMOD_RUN("gather_rmsnorm",
              launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms2, dm->rms_eps, v2, rm));
@@ -387,25 +400,31 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
       po.M_dev = M_dev;
       if (!gemm_tc_supported(po, eo)) return XMOD_ERR_UNSUPPORTED;
     }
-    if (tc && gemm_tc_supported(po, eo))
+    const bool oproj_tc = tc && gemm_tc_supported(po, eo);
+    fold2 = fold2 && oproj_tc;
+    if (fold2) {   // 5. folded: the epilogue writes h * rms2 and the row sums
+      eo.out3 = v2;
+      eo.g2 = w->rms2;
+      eo.rowss = rowss;
+      eo.norm_d = d;
+    }
+    if (oproj_tc)
       XMOD_RUN("gemm_o_residual", launch_gemm_tc(c, po, eo));
     else
       XMOD_RUN("gemm_o_residual", launch_gemm_simt(c, dt, M, d, qw, o, qw, w->wo, qw, nullptr, eo));
     // 5. v2 = RMSNorm(h) * rms2
-    XMOD_RUN("rmsnorm2", launch_rmsnorm_f32in(c, dt, M, d, (const float*)h, w->rms2, dm->rms_eps,
-                                              v2, M_dev));
+    if (!fold2)
+      XMOD_RUN("rmsnorm2", launch_rmsnorm_f32in(c, dt, M, d, (const float*)h, w->rms2,
+                                                dm->rms_eps, v2, M_dev));
   }
-  // 6. hidden = silu(v2 Wg^T) * (v2 Wu^T)
-  Epilogue eg;
-  eg.kind = EPI_SWIGLU;
-  eg.out = hidden;
-  eg.ldo = F;
-  GemmTcProblem pg;
-  pg.M = M; pg.N = F; pg.K = d; pg.A = v2; pg.lda = d; pg.ldb = d;
-  pg.B[0] = w->w_gate; pg.B[1] = w->w_up; pg.nB = 2;
-  pg.M_dev = M_dev;
-  if (rg && !gemm_tc_supported(pg, eg)) return XMOD_ERR_UNSUPPORTED;
-  if (tc && gemm_tc_supported(pg, eg))
+  // 6. hidden = silu(v2 Wg^T) * (v2 Wu^T) (or, folded, of (h * rms2) scaled by 1 / rms(h))
+  if (fold2) {
+    eg.rowss = rowss;
+    eg.eps = dm->rms_eps;
+    eg.norm_d = d;
+  }
+  if (rg && !gate_up_tc) return XMOD_ERR_UNSUPPORTED;
+  if (gate_up_tc)
     XMOD_RUN("gemm_gate_up_swiglu", launch_gemm_tc(c, pg, eg));
   else
     XMOD_RUN("gemm_gate_up_swiglu",

@@ -280,6 +280,28 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, in
                                   f3.y + v[8 * g + 7]);
     }
     st_seg_f32((float*)e.out2 + (int64_t)m * e.ldo2 + col0, hv, rem, a.v8);
+    if (e.out3) {   // RMSNorm2 folded: h * g2 in bf16, and this chunk's sum of squares
+      const uint4* gp = reinterpret_cast<const uint4*>((const __nv_bfloat16*)e.g2 + col0);
+      uint4 q[4];
+      float ss = 0.0f;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const uint4 gg = 8 * g < rem ? gp[g] : make_uint4(0, 0, 0, 0);
+        const __nv_bfloat162* g2v = reinterpret_cast<const __nv_bfloat162*>(&gg);
+        const float4 h0 = hv[2 * g], h1 = hv[2 * g + 1];
+        const float2 a0 = __bfloat1622float2(g2v[0]), a1 = __bfloat1622float2(g2v[1]);
+        const float2 a2 = __bfloat1622float2(g2v[2]), a3 = __bfloat1622float2(g2v[3]);
+        if (8 * g < rem)
+          ss += h0.x * h0.x + h0.y * h0.y + h0.z * h0.z + h0.w * h0.w + h1.x * h1.x +
+                h1.y * h1.y + h1.z * h1.z + h1.w * h1.w;
+        q[g].x = pack_bf16x2(h0.x * a0.x, h0.y * a0.y);
+        q[g].y = pack_bf16x2(h0.z * a1.x, h0.w * a1.y);
+        q[g].z = pack_bf16x2(h1.x * a2.x, h1.y * a2.y);
+        q[g].w = pack_bf16x2(h1.z * a3.x, h1.w * a3.y);
+      }
+      st_seg_bf16((__nv_bfloat16*)e.out3 + (int64_t)m * e.ldo2 + col0, q, rem, a.v8);
+      e.rowss[(int64_t)m * (e.norm_d / 32) + col0 / 32] = ss;
+    }
   } else if (MODE == EPI_ROUTER) {   // xrow is the stream token here
     float* sp = (float*)e.out + (int64_t)col0 * e.ldo + xrow;
     const float b = e.bias ? e.bias[xrow] : 0.0f;
@@ -335,6 +357,21 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0,
     if (MODE == EPI_DOWN_SCATTER && e.gate >= 0) r_own = e.r_sel[m_own];
   }
   if (MODE == EPI_ROUTER && m_own < M) xrow_own = stream_row_of(e, m_own);
+  // RMSNorm2 folded (see Epilogue::rowss): the row's 1 / rms for the SwiGLU inputs,
+  // its chunk sums added in order
+  float rstd_own = 1.0f;
+  if (MODE == EPI_SWIGLU && e.rowss && m_own < M) {
+    const float4* p = reinterpret_cast<const float4*>(e.rowss + (int64_t)m_own * (e.norm_d / 32));
+    float ss = 0.0f;
+    for (int i = 0; i < e.norm_d / 128; ++i) {
+      const float4 q = p[i];
+      ss += q.x;
+      ss += q.y;
+      ss += q.z;
+      ss += q.w;
+    }
+    rstd_own = rsqrtf(ss / (float)e.norm_d + e.eps);
+  }
   constexpr int NCH_FULL = BN / 32;
   const int nch = swiglu ? NCH_FULL / 2 : NCH_FULL;
   const int col_tile0 = swiglu ? n_blk * (BN / 2) : n_blk * BN;
@@ -352,7 +389,7 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0,
       tmem_ld32(t_row + BN / 2 + c * 32, u);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]) * u[i];
+      for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i] * rstd_own) * (u[i] * rstd_own);
     } else {
       tmem_ld32(t_row + c * 32, v);
       tmem_ld_wait();

@@ -183,6 +183,16 @@ struct Epilogue {
                                 //       h - x); NULL: no attention residual (a = 0)
   const float* r_sel = nullptr; // DOWN: gates [M]
   const float* bias = nullptr;  // ROUTER: per-token logit bias [B*T] or NULL
+  // RMSNorm2 folded into the GEMMs (tensor-core path, norm_d % 128 == 0): OPROJ also
+  // writes out3[m, n] = bf16(h * g2[n]) and, per 32-column chunk c, the chunk's
+  // sum of h^2 to rowss[m * norm_d / 32 + c]; SWIGLU then adds a row's chunk sums in
+  // order (deterministic, unlike atomics) and scales both accumulators of the row by
+  // rsqrt(sum / norm_d + eps) -- RMSNorm(h) * g2 projected, by linearity.
+  void* out3 = nullptr;
+  const void* g2 = nullptr;
+  float* rowss = nullptr;
+  float eps = 0.0f;
+  int norm_d = 0;
   float varsigma = 1.0f;
   int gate = -1;                // DOWN: XMOD_GATE_XMOD, XMOD_GATE_MOD, or -1 for dense
   // STORE (tensor-core path): columns >= vt_col0 are the values v; they are written
