@@ -52,6 +52,17 @@ inline int vt_ld(int n) { return (n + 7) / 8 * 8; }
 // vectors (a 32-row tile read from any starting layer stays inside the buffer).
 constexpr int kRouterRun = RowPtrs::kMax;
 constexpr int kRouterRows = 2 * kRouterRun;
+// k slices of the router-logit GEMM: the refresh after a layer has only B*T/K rows,
+// so splitting the d-long dot products spreads it over 4x the SMs; the selection
+// kernels add the slices' planes in order.
+#ifndef XMOD_ROUTER_SPLIT
+#define XMOD_ROUTER_SPLIT 4
+#endif
+constexpr int kRouterSplit = XMOD_ROUTER_SPLIT;
+inline int router_split(const xmod_dims* dm) {
+  const int nk = (dm->d + 63) / 64;
+  return nk < kRouterSplit ? nk : kRouterSplit;
+}
 
 // Workspace carve-up. M rows of block scratch cover a dense layer (M = B*T).
 struct Layout {
@@ -68,7 +79,8 @@ Layout layout(const xmod_dims* dm, int K) {
   const size_t qkv_w = (size_t)(dm->n_heads + 2 * dm->n_kv_heads) * dm->head_dim;
   size_t off = 0;
   L.status = off; off += kAlign;
-  L.s = off;      off = align_up(off + 4 * BT * kRouterRun);   // logits [run layer, B*T]
+  // logits [k slice, run layer, B*T]
+  L.s = off;      off = align_up(off + 4 * BT * kRouterRun * kRouterSplit);
   L.idx = off;    off = align_up(off + 4 * Bn);
   L.r_sel = off;  off = align_up(off + 4 * Bn);
   L.u = off;      off = align_up(off + es * M * dm->d);
@@ -477,6 +489,7 @@ GemmTcProblem router_problem(const xmod_dims* dm, int M, const void* rows, const
   GemmTcProblem p;
   p.M = M; p.N = n_vec; p.K = dm->d; p.A = rows; p.lda = dm->d;
   p.B[0] = wr; p.ldb = dm->d; p.b_rows = wr_rows;
+  p.ksplit = router_split(dm);
   return p;
 }
 Epilogue router_epilogue(const xmod_dims* dm, int n_per_seq, const int32_t* idx, float* S,
@@ -485,6 +498,7 @@ Epilogue router_epilogue(const xmod_dims* dm, int n_per_seq, const int32_t* idx,
   e.kind = EPI_ROUTER;
   e.out = S;
   e.ldo = dm->B * dm->T;
+  e.plane = (int64_t)kRouterRun * dm->B * dm->T;
   e.idx = idx;
   e.T = dm->T;
   e.n_per_seq = n_per_seq;
@@ -535,11 +549,15 @@ int sparse_run(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int
                                     router_epilogue(dm, T, nullptr, S, bias)));
   for (int j = 0; j < count; ++j) {
     const RouteTrack tj = track ? track_for(track, j, B) : RouteTrack{};
+    const int planes = router_split(dm);
+    const int64_t plane = (int64_t)kRouterRun * BT;
     if (threshold)
       XMOD_RUN("threshold", launch_threshold_select(c, B, T, S + j * BT, idx, r_sel, seq, seq + B,
-                                                    seq + 2 * B, track ? &tj : nullptr));
+                                                    seq + 2 * B, track ? &tj : nullptr, planes,
+                                                    plane));
     else
-      XMOD_RUN("topk", launch_topk(c, B, T, n, S + j * BT, idx, r_sel, track ? &tj : nullptr));
+      XMOD_RUN("topk", launch_topk(c, B, T, n, S + j * BT, idx, r_sel, track ? &tj : nullptr,
+                                   planes, plane));
     const bool refresh = j + 1 < count;
     const int st = run_block(c, dm, L, ws, n, x, threshold ? nullptr : idx, &lw[j], nullptr,
                              nullptr, true, x, r_sel, (int)gate, refresh ? xs_new : nullptr,

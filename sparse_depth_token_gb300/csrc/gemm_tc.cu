@@ -57,7 +57,8 @@ struct TcArgs {
   int M, N, K;
   int mode;                // EpiKind
   int n_split1, n_split2;  // STORE: first accumulator column served by B map 1 / map 2
-  int tiles_m, tiles_n, tiles;
+  int tiles_m, tiles_n, tiles;   // tiles counts every k slice
+  int ksplit;              // k slices per output tile (ROUTER only; else 1)
   const int32_t* M_dev;    // if set, the rows are min(*M_dev, M), read on the device
   int v8;                  // epilogue row segments may use 32-byte accesses
   Epilogue e;
@@ -96,7 +97,7 @@ __device__ __forceinline__ Extent launch_extent(const TcArgs& a, int tile_rows) 
     const int m = *a.M_dev;
     x.M = m < 0 ? 0 : (m < a.M ? m : a.M);
     x.tiles_m = (x.M + tile_rows - 1) / tile_rows;
-    x.tiles = x.tiles_m * a.tiles_n;
+    x.tiles = x.tiles_m * a.tiles_n * a.ksplit;
   }
   return x;
 }
@@ -260,7 +261,7 @@ __device__ __forceinline__ void unpack_x(const EpiIn& in, float (&xv)[32]) {
 template <int MODE>
 __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, int m, int col0,
                                                       int64_t xrow, float r, float (&v)[32],
-                                                      const EpiIn& in) {
+                                                      const EpiIn& in, int ks) {
   const Epilogue& e = a.e;
   if (m >= M || col0 >= a.N) return;
   const int rem = a.N - col0;
@@ -302,9 +303,9 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, in
       st_seg_bf16((__nv_bfloat16*)e.out3 + (int64_t)m * e.ldo2 + col0, q, rem, a.v8);
       e.rowss[(int64_t)m * (e.norm_d / 32) + col0 / 32] = ss;
     }
-  } else if (MODE == EPI_ROUTER) {   // xrow is the stream token here
-    float* sp = (float*)e.out + (int64_t)col0 * e.ldo + xrow;
-    const float b = e.bias ? e.bias[xrow] : 0.0f;
+  } else if (MODE == EPI_ROUTER) {   // xrow is the stream token here; k slice ks -> plane ks
+    float* sp = (float*)e.out + ks * e.plane + (int64_t)col0 * e.ldo + xrow;
+    const float b = e.bias && ks == 0 ? e.bias[xrow] : 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       if (i < rem) sp[(int64_t)i * e.ldo] = v[i] + b;
@@ -345,7 +346,8 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, in
 // Epilogue of one tile for this warp's 32-row slab [wrow0, wrow0 + 32).
 template <int BN, int MODE>
 __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0, int lane,
-                                              int n_blk, uint32_t t_row, int part, int nparts) {
+                                              int n_blk, uint32_t t_row, int part, int nparts,
+                                              int ks = 0) {
   const Epilogue& e = a.e;
   constexpr bool swiglu = MODE == EPI_SWIGLU;
   // the row this lane owns in TMEM: its stream row and gate
@@ -416,7 +418,7 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0,
       }
       continue;
     }
-    epilogue_chunk_direct<MODE>(a, M, m_own, col0, xrow_own, r_own, v, cur);
+    epilogue_chunk_direct<MODE>(a, M, m_own, col0, xrow_own, r_own, v, cur, ks);
     cur = nxt;
   }
 }
@@ -474,8 +476,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       int it = 0;
       for (int tile = blockIdx.x; tile < ext.tiles && !*abort_flag; tile += gridDim.x) {
+        const int ks = tile % args.ksplit;
         int m_blk, n_blk;
-        tile_coords(args, ext.tiles_m, tile, m_blk, n_blk);
+        tile_coords(args, ext.tiles_m, tile / args.ksplit, m_blk, n_blk);
+        const int kb0 = ks * nk / args.ksplit, kb1 = (ks + 1) * nk / args.ksplit;
         const int m0 = m_blk * BM;
         const CUtensorMap* mp = &tmB0;
         int brow = n_blk * BN;
@@ -488,7 +492,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             brow -= args.n_split1;
           }
         }
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
           if (!mbar_wait(EMPTY(s), ph ^ 1u, abort_flag, args.status)) break;
@@ -514,8 +518,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!mbar_wait(ACC_EMPTY(acc), aph ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const int ks = tile % args.ksplit;
+        const int kb0 = ks * nk / args.ksplit, kb1 = (ks + 1) * nk / args.ksplit;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
           if (!mbar_wait(FULL(s), ph, abort_flag, args.status)) {
@@ -527,7 +533,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint64_t bd = smem_desc_sw128(sB + s * C::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            mma_bf16(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb != kb0 || k) ? 1u : 0u);
           mma_commit(EMPTY(s));
         }
         if (!ok) break;
@@ -543,11 +549,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (!mbar_wait(ACC_FULL(acc), aph, abort_flag, args.status)) break;
       tc_fence_after();
       int m_blk, n_blk;
-      tile_coords(args, ext.tiles_m, tile, m_blk, n_blk);
+      tile_coords(args, ext.tiles_m, tile / args.ksplit, m_blk, n_blk);
       const int wrow0 = m_blk * BM + quad * 32;
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
       epilogue_tile<BN, MODE>(args, ext.M, wrow0, lane, n_blk, t_row, (warp - 2) / 4,
-                              EPI_WARPS / 4);
+                              EPI_WARPS / 4, tile % args.ksplit);
       tc_fence_before();
       mbar_arrive(ACC_EMPTY(acc));
     }
@@ -782,6 +788,7 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
   if (!make_map(&mA, p.A, p.K, p.M, p.lda, BM)) return false;
   a.M = p.M;
   a.M_dev = p.M_dev;
+  a.ksplit = p.ksplit > 1 ? p.ksplit : 1;
   a.N = p.N;
   a.K = p.K;
   a.mode = e.kind;
@@ -823,7 +830,7 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
     tiles_n = (p.N + BN - 1) / BN;
   }
   a.tiles_n = tiles_n;
-  a.tiles = a.tiles_m * tiles_n;
+  a.tiles = a.tiles_m * tiles_n * a.ksplit;
   return true;
 }
 
@@ -928,6 +935,7 @@ bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e) {
   if (p.K % 8 || p.lda % 8 || p.ldb % 8) return false;
   if (p.N % 8 && e.kind != EPI_ROUTER) return false;   // the others store 8-column groups
   if (p.b_rows && (p.b_rows < p.N || p.nB != 1)) return false;
+  if (p.ksplit > 1 && (e.kind != EPI_ROUTER || p.ksplit > (p.K + BK - 1) / BK)) return false;
   if (((uintptr_t)p.A & 15) || ((uintptr_t)p.B[0] & 15)) return false;
   if (e.kind == EPI_SWIGLU && (p.nB != 2 || ((uintptr_t)p.B[1] & 15))) return false;
   if (e.kind != EPI_SWIGLU)

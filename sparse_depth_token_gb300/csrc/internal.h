@@ -87,9 +87,11 @@ struct RouteTrack {
 };
 
 // Per-sequence top-n of s [B, T]; ties to the lower position; ascending idx [B, n].
-// r_sel [B, n] = sigmoid(ranked logit at idx) if not NULL.
+// r_sel [B, n] = sigmoid(ranked logit at idx) if not NULL. With nplanes > 1 the logit
+// is the in-order sum of the planes s + k * plane (partial sums of a k-split GEMM).
 cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32_t* idx,
-                        float* r_sel, const RouteTrack* tr = nullptr);
+                        float* r_sel, const RouteTrack* tr = nullptr, int nplanes = 1,
+                        int64_t plane = 0);
 // QK-norm (gains [hd], NULL: none) and rotary embedding (theta, 0: none), in place, of
 // q_heads heads from column q_col0 and k_heads heads from k_col0 (hd columns each) in
 // rows x [M, ld] (only m < *M_dev if given). Row m sits at position pos_idx[m], else
@@ -105,7 +107,8 @@ cudaError_t launch_qk_transform(const Ctx& c, xmod_dtype dt, int64_t M, const in
 // [<= B*T], seq_count [B], seq_off [B] and the total in *M_out (all device).
 cudaError_t launch_threshold_select(const Ctx& c, int B, int T, const float* s, int32_t* tok,
                                     float* r_sel, int32_t* seq_count, int32_t* seq_off,
-                                    int32_t* M_out, const RouteTrack* tr = nullptr);
+                                    int32_t* M_out, const RouteTrack* tr = nullptr,
+                                    int nplanes = 1, int64_t plane = 0);
 // update_hist [B, max_count + 1]: histogram of count [B, T] per sequence.
 cudaError_t launch_count_hist(const Ctx& c, int B, int T, int max_count, const int32_t* count,
                               int32_t* update_hist);
@@ -182,7 +185,8 @@ struct Epilogue {
   const float* h = nullptr;     // DOWN: h = x_sel + a [M, d] fp32 (the attention residual is
                                 //       h - x); NULL: no attention residual (a = 0)
   const float* r_sel = nullptr; // DOWN: gates [M]
-  const float* bias = nullptr;  // ROUTER: per-token logit bias [B*T] or NULL
+  const float* bias = nullptr;  // ROUTER: per-token logit bias [B*T] or NULL (k slice 0)
+  int64_t plane = 0;            // ROUTER with k slices: elements between slice planes
   // RMSNorm2 folded into the GEMMs (tensor-core path, norm_d % 128 == 0): OPROJ also
   // writes out3[m, n] = bf16(h * g2[n]) and, per 32-column chunk c, the chunk's
   // sum of h^2 to rowss[m * norm_d / 32 + c]; SWIGLU then adds a row's chunk sums in
@@ -223,6 +227,9 @@ struct GemmTcProblem {
   // If set, the launch covers M rows of buffers sized for M, but only the first
   // min(*M_dev, M) rows (a count an earlier kernel wrote) are computed.
   const int32_t* M_dev = nullptr;
+  // ROUTER only: the K range split in ksplit slices (at most the number of 64-deep
+  // k-blocks); slice k's partial sums go to the output plane k (Epilogue::plane apart).
+  int ksplit = 1;
 };
 bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e);
 cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e);

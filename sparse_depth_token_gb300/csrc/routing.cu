@@ -250,7 +250,7 @@ __device__ __forceinline__ uint32_t warps_exclusive_scan(uint32_t v, uint32_t* s
 template <bool TRACK>
 __global__ void __launch_bounds__(TOPK_THREADS)
 topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx,
-            float* __restrict__ r_sel, int* status, RouteTrack tr) {
+            float* __restrict__ r_sel, int* status, RouteTrack tr, int nplanes, int64_t plane) {
   if (!TRACK) tr = RouteTrack{};
   pdl_trigger();
   pdl_wait();
@@ -265,15 +265,40 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
   const float* sb = s + (int64_t)b * T;
   int32_t* cnt = tr.count ? tr.count + (int64_t)b * T : nullptr;
   int32_t* last = tr.last ? tr.last + (int64_t)b * T : nullptr;
-  // the logit this layer ranks: s minus the block's accumulated token-choice bias
-  auto logit = [&](int t) { return cnt ? sb[t] - tr.bias_step * (float)cnt[t] : sb[t]; };
+  // the logit this layer ranks: s (the sum of its planes, in order) minus the block's
+  // accumulated token-choice bias
+  auto logit = [&](int t) {
+    float v = sb[t];
+    for (int k = 1; k < nplanes; ++k) v += sb[k * plane + t];
+    return cnt ? v - tr.bias_step * (float)cnt[t] : v;
+  };
   if (threadIdx.x == 0) sh_bad = 0;
   if (threadIdx.x < 3) sh_stat[threadIdx.x] = 0u;
   __syncthreads();
-  for (int t = threadIdx.x; t < T; t += TOPK_THREADS) {
-    const float v = logit(t);
-    if (!isfinite(v)) sh_bad = 1;
-    keys[t] = order_key(v);
+  // four positions per thread at a time, every plane's load issued before any is used
+  for (int t0 = threadIdx.x; t0 < T; t0 += 4 * TOPK_THREADS) {
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = t0 + i * TOPK_THREADS;
+      v[i] = t < T ? sb[t] : 0.0f;
+    }
+    for (int k = 1; k < nplanes; ++k) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = t0 + i * TOPK_THREADS;
+        if (t < T) v[i] += sb[k * plane + t];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = t0 + i * TOPK_THREADS;
+      if (t < T) {
+        const float x = cnt ? v[i] - tr.bias_step * (float)cnt[t] : v[i];
+        if (!isfinite(x)) sh_bad = 1;
+        keys[t] = order_key(x);
+      }
+    }
   }
   __syncthreads();
   if (sh_bad && threadIdx.x == 0) report_status(status, XMOD_ERR_DEVICE_CHECK);
@@ -402,7 +427,8 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
 }
 
 cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32_t* idx,
-                        float* r_sel, const RouteTrack* tr) {
+                        float* r_sel, const RouteTrack* tr, int nplanes, int64_t plane) {
+  if (nplanes < 1) return cudaErrorInvalidValue;
   if (B <= 0) return cudaSuccess;
   const size_t smem = sizeof(uint32_t) * (size_t)T;
   cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -411,10 +437,10 @@ cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32
                        (int)(sizeof(uint32_t) * TOPK_MAX_T));
   if (tr)
     launch_pdl(topk_kernel<true>, dim3(B), dim3(TOPK_THREADS), smem, c.stream, T, n, s, idx,
-               r_sel, c.status, *tr);
+               r_sel, c.status, *tr, nplanes, plane);
   else
     launch_pdl(topk_kernel<false>, dim3(B), dim3(TOPK_THREADS), smem, c.stream, T, n, s, idx,
-               r_sel, c.status, RouteTrack{});
+               r_sel, c.status, RouteTrack{}, nplanes, plane);
   return cudaGetLastError();
 }
 
@@ -454,7 +480,7 @@ __global__ void __launch_bounds__(TOPK_THREADS)
 threshold_select_kernel(int B, int T, const float* __restrict__ s, int32_t* __restrict__ tok,
                         float* __restrict__ r_sel, int32_t* __restrict__ seq_count,
                         int32_t* __restrict__ seq_off, int32_t* __restrict__ M_out, int* status,
-                        RouteTrack tr) {
+                        RouteTrack tr, int nplanes, int64_t plane) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t sh[33];
@@ -475,7 +501,9 @@ threshold_select_kernel(int B, int T, const float* __restrict__ s, int32_t* __re
       float v = 0.0f;
       bool take = false;
       if (t < T) {
-        v = cnt ? sb[t] - tr.bias_step * (float)cnt[t] : sb[t];
+        v = sb[t];
+        for (int k = 1; k < nplanes; ++k) v += sb[k * plane + t];
+        if (cnt) v -= tr.bias_step * (float)cnt[t];
         if (!isfinite(v)) sh_bad = 1;
         take = v >= 0.0f;
       }
@@ -514,11 +542,13 @@ threshold_select_kernel(int B, int T, const float* __restrict__ s, int32_t* __re
 
 cudaError_t launch_threshold_select(const Ctx& c, int B, int T, const float* s, int32_t* tok,
                                     float* r_sel, int32_t* seq_count, int32_t* seq_off,
-                                    int32_t* M_out, const RouteTrack* tr) {
-  if (B <= 0 || T <= 0) return cudaErrorInvalidValue;
+                                    int32_t* M_out, const RouteTrack* tr, int nplanes,
+                                    int64_t plane) {
+  if (B <= 0 || T <= 0 || nplanes < 1) return cudaErrorInvalidValue;
   const RouteTrack none{};
   return launch_pdl(threshold_select_kernel, dim3(1), dim3(TOPK_THREADS), 0, c.stream, B, T, s,
-                    tok, r_sel, seq_count, seq_off, M_out, c.status, tr ? *tr : none);
+                    tok, r_sel, seq_count, seq_off, M_out, c.status, tr ? *tr : none, nplanes,
+                    plane);
 }
 
 // update_hist[b, c] = number of tokens of sequence b whose count is c (0 <= c <= max_count).
