@@ -90,6 +90,21 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// 2^x by the PTX ex2.approx instruction: its error is far below the bf16 rounding the
+// probabilities get right after. Inputs are <= 0 here; -inf gives 0.
+#ifndef XMOD_ATTN_EX2_APPROX
+#define XMOD_ATTN_EX2_APPROX 1
+#endif
+__device__ __forceinline__ float exp2_p(float x) {
+#if XMOD_ATTN_EX2_APPROX
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+#else
+  return exp2f(x);
+#endif
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -342,8 +357,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = exp2f(fmaf(v[c * 32 + i], a.scale_log2, -m));
-          const float p1 = exp2f(fmaf(v[c * 32 + i + 1], a.scale_log2, -m));
+          const float p0 = exp2_p(fmaf(v[c * 32 + i], a.scale_log2, -m));
+          const float p1 = exp2_p(fmaf(v[c * 32 + i + 1], a.scale_log2, -m));
           sum += p0 + p1;
           pk[i / 2] = pack_bf16x2(p0, p1);
         }
