@@ -66,8 +66,13 @@ inline int router_split(const xmod_dims* dm) {
 
 // Workspace carve-up. M rows of block scratch cover a dense layer (M = B*T).
 struct Layout {
-  size_t status, s, idx, r_sel, u, qkv, vt, o, h, hidden, wr, count, last, seq, rowss, total;
+  size_t status, s, idx, r_sel, u, qkv, vt, o, h, a, hidden, wr, count, last, seq, rowss, skflag,
+      skpart, total;
 };
+
+// Stream-K scratch of the tensor-core GEMMs (bf16 layouts): one 128 x 256 fp32 partial
+// accumulator and one flag per CTA, for up to kSkSlots CTAs (one per SM).
+constexpr int kSkSlots = 192;
 
 Layout layout(const xmod_dims* dm, int K) {
   Layout L{};
@@ -90,17 +95,35 @@ Layout layout(const xmod_dims* dm, int K) {
                                            (size_t)vt_ld(dm->T));
   L.o = off;      off = align_up(off + es * M * dm->n_heads * dm->head_dim);
   L.h = off;      off = align_up(off + 4 * M * dm->d);   // h = x_sel + a kept in fp32
+  L.a = off;      off = align_up(off + es * M * dm->d);  // a, the attention residual
   L.hidden = off; off = align_up(off + es * M * dm->d_ff);
   L.wr = off;     off = align_up(off + es * (size_t)kRouterRows * dm->d);   // stacked w_r
   L.count = off;  off = align_up(off + 4 * BT);   // token-choice bias state of a block
   L.last = off;   off = align_up(off + 4 * BT);
   L.seq = off;    off = align_up(off + 4 * (2 * (size_t)dm->B + 1));   // threshold rows
   L.rowss = off;  off = align_up(off + 4 * M * (size_t)(dm->d / 32));   // h^2 sums per chunk
+  const size_t slots = dm->dtype == XMOD_BF16 ? kSkSlots : 0;
+  L.skflag = off; off = align_up(off + 4 * slots);
+  L.skpart = off; off = align_up(off + 4 * slots * 128 * 256);
   L.total = off;
   return L;
 }
 
 inline char* at(void* ws, size_t off) { return (char*)ws + off; }
+
+// The launch context of an entry point: its stream, the status word and the GEMMs'
+// stream-K scratch, whose flags are cleared here (each launch leaves them clear, but
+// a launch that gave up on a wait may not have, and the workspace starts unset).
+int make_ctx(const xmod_dims* dm, void* ws, const Layout& L, void* stream, Ctx& c) {
+  c = Ctx{(cudaStream_t)stream, (int*)at(ws, L.status)};
+  if (dm->dtype != XMOD_BF16) return XMOD_OK;
+  c.sk_flag = (int*)at(ws, L.skflag);
+  c.sk_part = (float*)at(ws, L.skpart);
+  c.sk_slots = kSkSlots;
+  return cudaMemsetAsync(c.sk_flag, 0, 4 * (size_t)kSkSlots, c.stream) == cudaSuccess
+             ? XMOD_OK
+             : XMOD_ERR_CUDA;
+}
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? XMOD_OK : XMOD_ERR_CUDA; }
 
@@ -288,7 +311,9 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   char* hidden = at(ws, L.hidden);
   const bool tc = dt == XMOD_BF16;
   char* v2 = u;   // RMSNorm2 output, in the buffer of u (consumed by the q/k/v projection)
-  const float* h_in = (const float*)h;   // h = x_sel + a for the down projection
+  // a, the attention residual, for the down projection's scatter (the caller's a_out
+  // when given); NULL for an FFN-only block (a = 0)
+  void* a_res = a_out ? a_out : (void*)at(ws, L.a);
   RowMap rm;
   if (rg) {
     rm.tok = rg->tok;
@@ -309,7 +334,7 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   if (part == PART_FFN) {   // FFN half only: v2 = RMSNorm(x_sel) * rms2, a = 0
     XMOD_RUN("gather_rmsnorm",
              launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms2, dm->rms_eps, v2, rm));
-    h_in = nullptr;
+    a_res = nullptr;
   } else {
     if (part == PART_FULLKV) {   // steps 1-3 with every token's keys and values
       if (rg || !idx) return XMOD_ERR_UNSUPPORTED;
@@ -396,7 +421,7 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
     // 4. a = o Wo^T, h = x_sel + a
     Epilogue eo;
     eo.kind = EPI_OPROJ;
-    eo.out = a_out;   // the attention residual itself only when the caller asks for it
+    eo.out = scatter || a_out ? a_res : nullptr;
     eo.ldo = d;
     eo.out2 = h;
     eo.ldo2 = d;
@@ -414,7 +439,8 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
     }
     const bool oproj_tc = tc && gemm_tc_supported(po, eo);
     fold2 = fold2 && oproj_tc;
-    if (fold2) {   // 5. folded: the epilogue writes h * rms2 and the row sums
+    if (fold2) {   // 5. folded: the epilogue writes h * rms2 and the row sums (no h)
+      eo.out2 = nullptr;
       eo.out3 = v2;
       eo.g2 = w->rms2;
       eo.rowss = rowss;
@@ -450,7 +476,7 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
     ed.T = T;
     ed.n_per_seq = n;
     ed.d = d;
-    ed.h = h_in;
+    ed.a = a_res;
     ed.r_sel = r_sel;
     ed.varsigma = w->varsigma;
     ed.gate = gate;
@@ -593,11 +619,9 @@ bool threshold_supported(const xmod_dims* dm, void* ws, const Layout& L) {
   return sparse_run_supported(dm, ws, L) && attention_tc_supported(dm->head_dim, dm->T, qkv_w);
 }
 
-int layer_impl(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
+int layer_impl(const Ctx& c, const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
                const xmod_layer_weights* w, void* x, const float* bias, int32_t* idx_out,
-               float* r_sel_out, void* ws, const Layout& L, cudaStream_t stream,
-               const RouteTrack* track = nullptr) {
-  Ctx c{stream, (int*)at(ws, L.status)};
+               float* r_sel_out, void* ws, const Layout& L, const RouteTrack* track = nullptr) {
   if (kind == XMOD_LAYER_DENSE)
     return run_block(c, dm, L, ws, dm->T, x, nullptr, w, nullptr, nullptr, true, x, nullptr, -1);
   if (kind == XMOD_LAYER_ATTN)
@@ -663,7 +687,9 @@ int stack_impl(const xmod_dims* dm, int K, const int32_t* kinds, int n_layers, x
   const Layout L = layout(dm, K);
   const bool runs = sparse_run_supported(dm, ws, L);
   if (threshold && !threshold_supported(dm, ws, L)) return XMOD_ERR_UNSUPPORTED;
-  Ctx c{stream, (int*)at(ws, L.status)};
+  Ctx c;
+  st = make_ctx(dm, ws, L, stream, c);
+  if (st) return st;
   const int64_t BT = (int64_t)dm->B * dm->T;
   // Token-choice bias state, only when an option needs it (else the plain top-k).
   const bool tracked = opts && (opts->bias_step != 0.0f || opts->layer_stats || opts->update_hist);
@@ -678,8 +704,8 @@ int stack_impl(const xmod_dims* dm, int K, const int32_t* kinds, int n_layers, x
   for (int l = 0; l < n_layers;) {
     const int kind = kinds[l];
     if (!routed(kind)) {
-      st = layer_impl(dm, (xmod_layer_kind)kind, K, gate, &layers[l], x_inout, bias, nullptr,
-                      nullptr, ws, L, stream);
+      st = layer_impl(c, dm, (xmod_layer_kind)kind, K, gate, &layers[l], x_inout, bias, nullptr,
+                      nullptr, ws, L);
       if (st) return st;
       ++l;
       continue;
@@ -701,8 +727,8 @@ int stack_impl(const xmod_dims* dm, int K, const int32_t* kinds, int n_layers, x
       st = sparse_run(c, dm, L, ws, K, gate, &layers[l], count, x_inout, bias, nullptr, nullptr,
                       tracked ? &tl : nullptr, threshold, part);
     else
-      st = layer_impl(dm, (xmod_layer_kind)kind, K, gate, &layers[l], x_inout, bias, nullptr,
-                      nullptr, ws, L, stream, tracked ? &tl : nullptr);
+      st = layer_impl(c, dm, (xmod_layer_kind)kind, K, gate, &layers[l], x_inout, bias, nullptr,
+                      nullptr, ws, L, tracked ? &tl : nullptr);
     if (st) return st;
     l += count;
     routed_index += count;
@@ -808,7 +834,9 @@ int xmod_block_fwd(const xmod_dims* dm, int n_per_seq, const void* xs, const int
   int st = check_ws(dm, K, ws, ws_bytes);
   if (st) return st;
   const Layout L = layout(dm, K);
-  Ctx c{(cudaStream_t)stream, (int*)at(ws, L.status)};
+  Ctx c;
+  st = make_ctx(dm, ws, L, stream, c);
+  if (st) return st;
   // Without idx the rows come from the compact buffer: view it as B sequences of
   // n_per_seq tokens.
   xmod_dims local = *dm;
@@ -847,8 +875,11 @@ int xmod_layer_fwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate g
   const int Kw = routed(kind) ? K : 1;
   int st = check_ws(dm, Kw, ws, ws_bytes);
   if (st) return st;
-  return layer_impl(dm, kind, Kw, gate, w, x_inout, bias, idx_out, r_sel_out, ws, layout(dm, Kw),
-                    (cudaStream_t)stream);
+  const Layout L = layout(dm, Kw);
+  Ctx c;
+  st = make_ctx(dm, ws, L, stream, c);
+  if (st) return st;
+  return layer_impl(c, dm, kind, Kw, gate, w, x_inout, bias, idx_out, r_sel_out, ws, L);
 }
 
 int xmod_layer_fwd_threshold(const xmod_dims* dm, xmod_gate gate, const xmod_layer_weights* w,
@@ -863,7 +894,9 @@ int xmod_layer_fwd_threshold(const xmod_dims* dm, xmod_gate gate, const xmod_lay
   if (st) return st;
   const Layout L = layout(dm, 1);
   if (!threshold_supported(dm, ws, L)) return XMOD_ERR_UNSUPPORTED;
-  Ctx c{(cudaStream_t)stream, (int*)at(ws, L.status)};
+  Ctx c;
+  st = make_ctx(dm, ws, L, stream, c);
+  if (st) return st;
   st = sparse_run(c, dm, L, ws, 1, gate, w, 1, x_inout, bias, nullptr, nullptr, nullptr, true);
   if (st) return st;
   if (count_out && cudaMemcpyAsync(count_out, at(ws, L.seq), sizeof(int32_t) * dm->B,

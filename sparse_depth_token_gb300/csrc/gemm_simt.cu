@@ -31,7 +31,7 @@ __device__ __forceinline__ void epilogue_store(const Epilogue& e, int M, int N, 
       const int64_t t = e.idx ? (int64_t)e.idx[m] : (m - b * e.n_per_seq);
       const float xv = ld_f((const T*)e.x + (b * e.T + t) * e.d + n);
       if (e.out) st_f((T*)e.out + (int64_t)m * e.ldo + n, acc);
-      ((float*)e.out2)[(int64_t)m * e.ldo2 + n] = xv + acc;
+      if (e.out2) ((float*)e.out2)[(int64_t)m * e.ldo2 + n] = xv + acc;
       break;
     }
     case EPI_SWIGLU:
@@ -42,11 +42,11 @@ __device__ __forceinline__ void epilogue_store(const Epilogue& e, int M, int N, 
       const int64_t t = e.idx ? (int64_t)e.idx[m] : (m - b * e.n_per_seq);
       T* xp = (T*)e.x + (b * e.T + t) * e.d + n;
       const float xv = ld_f(xp);
-      const float hv = e.h ? e.h[(int64_t)m * e.d + n] : xv;   // h = x + a (no h: a = 0)
+      const float av = e.a ? ld_f((const T*)e.a + (int64_t)m * e.d + n) : 0.0f;
       float y;
-      if (e.gate == XMOD_GATE_XMOD) y = xv + e.varsigma * e.r_sel[m] * ((hv - xv) + acc);  // Eq. 7
-      else if (e.gate == XMOD_GATE_MOD) y = hv + e.r_sel[m] * acc;                       // Eq. 6
-      else y = hv + acc;                                                                  // dense
+      if (e.gate == XMOD_GATE_XMOD) y = xv + e.varsigma * e.r_sel[m] * (av + acc);  // Eq. 7
+      else if (e.gate == XMOD_GATE_MOD) y = (xv + av) + e.r_sel[m] * acc;         // Eq. 6
+      else y = (xv + av) + acc;                                                    // dense
       st_f(xp, y);
       if (e.out) st_f((T*)e.out + (int64_t)m * e.ldo + n, y);
       break;

@@ -14,10 +14,11 @@
 //               loads and stores of that row segment. The other accumulator meanwhile
 //               receives the next tile's MMAs.
 // Fused epilogues: plain store (optionally q | k | v from three weight tensors, with
-// v written transposed for the attention kernel), O-projection (h = x_sel + a in
-// fp32, and a itself when asked), SwiGLU (gate and up halves of one tile), and the
-// down projection's gated scatter back into the residual stream at the selected rows
-// (X-MoD notes Eq. 7 / Eq. 6; a dense layer adds a + f), which reads a back as h - x.
+// v written transposed for the attention kernel), O-projection (a in bf16; h = x_sel
+// + a in fp32 when a separate RMSNorm needs it, or h * rms2 and h's sums of squares
+// when RMSNorm2 is folded), SwiGLU (gate and up halves of one tile), and the down
+// projection's gated scatter back into the residual stream at the selected rows
+// (X-MoD notes Eq. 7 / Eq. 6; a dense layer adds a + f), which reads a back.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -51,6 +52,8 @@ struct Cfg {
   static constexpr int STAGES = (200 * 1024) / STAGE_BYTES;
   static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
+  // the last 256 bytes: 2 * STAGES + 5 mbarriers, the TMEM address and the abort flag
+  static_assert((2 * STAGES + 5) * 8 + 12 <= 256, "barrier block overflows");
 };
 
 struct TcArgs {
@@ -61,6 +64,11 @@ struct TcArgs {
   int ksplit;              // k slices per output tile (ROUTER only; else 1)
   const int32_t* M_dev;    // if set, the rows are min(*M_dev, M), read on the device
   int v8;                  // epilogue row segments may use 32-byte accesses
+  // Stream-K (see Work): the tiles' k-blocks split evenly over the CTAs
+  int sk;
+  int64_t units;           // tiles x k-blocks
+  float* sk_part;          // per-CTA partial accumulator slots, BM x BN fp32 each
+  int* sk_flag;            // per-CTA "slot published" flags, 0 between launches
   Epilogue e;
   int* status;
 };
@@ -100,6 +108,95 @@ __device__ __forceinline__ Extent launch_extent(const TcArgs& a, int tile_rows) 
     x.tiles = x.tiles_m * a.tiles_n * a.ksplit;
   }
   return x;
+}
+
+// What one CTA does next: output tile `tile` (k slice `ks` for the router), k-blocks
+// [kb0, kb1). Data-parallel launches give every CTA whole tiles, round robin.
+//
+// Stream-K launches line up the k-blocks of all tiles, tile after tile, and give
+// CTA c the c-th of gridDim.x equal shares, so every SM issues the same number of
+// MMAs whatever the tile count (no partial last wave). A tile cut between CTAs c and
+// c + 1 is finished by c, which holds its first k-blocks and reaches it last, at the
+// end of its share (WORK_OWNER); c + 1 takes the tile's last k-blocks first, leaves
+// its fp32 accumulator in slot c + 1 and raises flag c + 1 (WORK_PART). The owner
+// waits for the flag (bounded), adds the slot into its TMEM accumulator -- one fixed
+// order, so results do not depend on timing -- clears the flag for the next launch
+// and runs the epilogue. A CTA starts inside a tile at most once per launch, and the
+// host takes this path only when each share covers a whole tile's k-blocks, so a tile
+// spans at most two CTAs and each slot serves one tile. The producer, the MMA issuer
+// and the epilogue walk the same sequence.
+enum { WORK_FULL = 0, WORK_PART = 1, WORK_OWNER = 2 };
+struct Work {
+  int tile, ks, kb0, kb1, role;
+};
+__device__ __forceinline__ bool work_at(const TcArgs& a, const Extent& ext, int nk, int i,
+                                        Work& w) {
+  if (a.sk) {
+    const int64_t P = gridDim.x, cta = blockIdx.x;
+    const int64_t u0 = cta * a.units / P, u1 = (cta + 1) * a.units / P;
+    const int64_t tile = u0 / nk + i;
+    const int64_t s = max(u0, tile * nk), e = min(u1, (tile + 1) * nk);
+    if (s >= e) return false;
+    w.tile = (int)tile;
+    w.ks = 0;
+    w.kb0 = (int)(s - tile * nk);
+    w.kb1 = (int)(e - tile * nk);
+    w.role = w.kb0 > 0 ? WORK_PART : (w.kb1 < nk ? WORK_OWNER : WORK_FULL);
+    return true;
+  }
+  const int t = (int)blockIdx.x + i * (int)gridDim.x;
+  if (t >= ext.tiles) return false;
+  w.ks = t % a.ksplit;
+  w.tile = t / a.ksplit;
+  w.kb0 = w.ks * nk / a.ksplit;
+  w.kb1 = (w.ks + 1) * nk / a.ksplit;
+  w.role = WORK_FULL;
+  return true;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Bounded wait for a neighbour's published slot (as mbar_wait: on timeout the status
+// word gets XMOD_ERR_TIMEOUT and the CTA's abort flag is raised).
+__device__ __noinline__ bool flag_wait(const int* f, volatile int* abort_flag, int* status) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (ld_acquire_gpu(f) != 0) return true;
+    if ((i & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        report_status(status, XMOD_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+    __nanosleep(100);
+  }
+}
+
+// All epilogue warps meet (an mbarrier of EPI_WARPS arrivals, so the wait is bounded);
+// n counts the meetings for the phase parity.
+__device__ __forceinline__ bool epi_meet(uint32_t bar, int& n, int lane, volatile int* abort_flag,
+                                         int* status) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, (uint32_t)(n & 1), abort_flag, status);
+  ++n;
+  return ok;
 }
 
 // silu(z) = z * sigmoid(z) with the fast exponential and approximate division (a few
@@ -223,12 +320,87 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* p, const float (&v)[
 #define XMOD_GEMM_PAIRS 1
 #endif
 
+// WORK_PART: this lane's accumulator row, every 32-column chunk of this warp's share,
+// into the CTA's slot (row-major, BN floats per row).
+template <int BN>
+__device__ __forceinline__ void sk_leave_partial(const TcArgs& a, int row, uint32_t t_row,
+                                                 int part, int nparts) {
+  float* dst = a.sk_part + ((int64_t)blockIdx.x * BM + row) * BN;
+#pragma unroll 1
+  for (int c = part; c < BN / 32; c += nparts) {
+    float v[32];
+    tmem_ld32(t_row + c * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int g = 0; g < 32; g += 8)
+      st_v8(dst + c * 32 + g,
+            make_uint4(__float_as_uint(v[g]), __float_as_uint(v[g + 1]), __float_as_uint(v[g + 2]),
+                       __float_as_uint(v[g + 3])),
+            make_uint4(__float_as_uint(v[g + 4]), __float_as_uint(v[g + 5]),
+                       __float_as_uint(v[g + 6]), __float_as_uint(v[g + 7])));
+  }
+}
+
+// WORK_OWNER: add the next CTA's slot into this lane's accumulator row in TMEM, the
+// slot's next chunk loaded while the current one is added.
+template <int BN>
+__device__ __forceinline__ void sk_add_partial(const TcArgs& a, int row, uint32_t t_row, int part,
+                                               int nparts) {
+  const float* src = a.sk_part + ((int64_t)(blockIdx.x + 1) * BM + row) * BN;
+  float4 pc[8], pn[8];
+#pragma unroll
+  for (int g = 0; g < 8; ++g) pc[g] = ld_cg_f4(src + part * 32 + 4 * g);
+#pragma unroll 1
+  for (int c = part; c < BN / 32; c += nparts) {
+    if (c + nparts < BN / 32) {
+#pragma unroll
+      for (int g = 0; g < 8; ++g) pn[g] = ld_cg_f4(src + (c + nparts) * 32 + 4 * g);
+    }
+    float v[32];
+    tmem_ld32(t_row + c * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      v[4 * g] += pc[g].x;
+      v[4 * g + 1] += pc[g].y;
+      v[4 * g + 2] += pc[g].z;
+      v[4 * g + 3] += pc[g].w;
+    }
+    tmem_st32(t_row + c * 32, v);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) pc[g] = pn[g];
+  }
+  tmem_st_wait();
+}
+
+// L2 prefetch of `bytes` bytes at p (16-byte aligned, a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// The epilogue inputs of this lane's row of the next tile -- the x row segment and,
+// for the down projection, the a row segment -- brought into L2 while the tile's MMAs
+// run, so that the epilogue's loads (issued only once the accumulator is complete)
+// do not wait on DRAM. Row segments are 16-byte aligned: d and N are multiples of 8.
+template <int BN, int MODE>
+__device__ __forceinline__ void epi_prefetch(const TcArgs& a, int M, int m, int n_blk, int part) {
+  if (MODE != EPI_OPROJ && MODE != EPI_DOWN_SCATTER) return;
+  const Epilogue& e = a.e;
+  const int col0 = n_blk * BN;
+  if (m >= M || col0 >= a.N) return;
+  const uint32_t bytes = 2u * (uint32_t)min(BN, a.N - col0);
+  if (part == 0)
+    prefetch_l2((const __nv_bfloat16*)e.x + stream_row_of(e, m) * e.d + col0, bytes);
+  else if (MODE == EPI_DOWN_SCATTER && e.a)
+    prefetch_l2((const __nv_bfloat16*)e.a + (int64_t)m * e.d + col0, bytes);
+}
+
 // Inputs of the O-projection / down-projection epilogues for one 32-column chunk of
-// one row: x (bf16) and, for the down projection, h (fp32). They are loaded one chunk
-// ahead so that their memory latency overlaps the previous chunk's work.
+// one row: x and, for the down projection, a (bf16). They are loaded one chunk ahead
+// so that their memory latency overlaps the previous chunk's work.
 struct EpiIn {
   uint4 x[4];
-  float4 h[8];
+  uint4 a[4];
 };
 
 template <int MODE>
@@ -238,7 +410,8 @@ __device__ __forceinline__ void epi_load_in(const TcArgs& a, int M, int m, int c
   if (m >= M || col0 >= a.N) return;
   const int rem = a.N - col0;
   ld_seg_bf16((const __nv_bfloat16*)e.x + xrow + col0, in.x, rem, a.v8);
-  if (MODE == EPI_DOWN_SCATTER && e.h) ld_seg_f32(e.h + (int64_t)m * e.d + col0, in.h, rem, a.v8);
+  if (MODE == EPI_DOWN_SCATTER && e.a)
+    ld_seg_bf16((const __nv_bfloat16*)e.a + (int64_t)m * e.d + col0, in.a, rem, a.v8);
 }
 
 __device__ __forceinline__ void unpack_x(const EpiIn& in, float (&xv)[32]) {
@@ -280,7 +453,7 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, in
       hv[2 * g + 1] = make_float4(f2.x + v[8 * g + 4], f2.y + v[8 * g + 5], f3.x + v[8 * g + 6],
                                   f3.y + v[8 * g + 7]);
     }
-    st_seg_f32((float*)e.out2 + (int64_t)m * e.ldo2 + col0, hv, rem, a.v8);
+    if (e.out2) st_seg_f32((float*)e.out2 + (int64_t)m * e.ldo2 + col0, hv, rem, a.v8);
     if (e.out3) {   // RMSNorm2 folded: h * g2 in bf16, and this chunk's sum of squares
       const uint4* gp = reinterpret_cast<const uint4*>((const __nv_bfloat16*)e.g2 + col0);
       uint4 q[4];
@@ -309,28 +482,26 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, in
 #pragma unroll
     for (int i = 0; i < 32; ++i)
       if (i < rem) sp[(int64_t)i * e.ldo] = v[i] + b;
-  } else {  // EPI_DOWN_SCATTER, a = h - x
+  } else {  // EPI_DOWN_SCATTER with the attention residual a (none: a = 0)
     const float g7 = e.varsigma * r;
     uint4 qo[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {   // 8 columns at a time
       const __nv_bfloat162* x2 = reinterpret_cast<const __nv_bfloat162*>(&in.x[g]);
-      const float hv[8] = {in.h[2 * g].x, in.h[2 * g].y, in.h[2 * g].z, in.h[2 * g].w,
-                           in.h[2 * g + 1].x, in.h[2 * g + 1].y, in.h[2 * g + 1].z,
-                           in.h[2 * g + 1].w};
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&in.a[g]);
       float y[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 f = __bfloat1622float2(x2[i]);
-        const float xx[2] = {f.x, f.y};
+        const float2 af = e.a ? __bfloat1622float2(a2[i]) : make_float2(0.0f, 0.0f);
+        const float xx[2] = {f.x, f.y}, aa[2] = {af.x, af.y};
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int j = 2 * i + k;
           const float fv = v[8 * g + j];
-          const float hj = e.h ? hv[j] : xx[k];   // no h: no attention residual (a = 0)
-          if (e.gate == XMOD_GATE_XMOD) y[j] = xx[k] + g7 * ((hj - xx[k]) + fv);   // Eq. 7
-          else if (e.gate == XMOD_GATE_MOD) y[j] = hj + r * fv;                   // Eq. 6
-          else y[j] = hj + fv;                                                     // dense
+          if (e.gate == XMOD_GATE_XMOD) y[j] = xx[k] + g7 * (aa[k] + fv);   // Eq. 7
+          else if (e.gate == XMOD_GATE_MOD) y[j] = (xx[k] + aa[k]) + r * fv;   // Eq. 6
+          else y[j] = (xx[k] + aa[k]) + fv;                                      // dense
         }
       }
       qo[g].x = pack_bf16x2(y[0], y[1]);
@@ -437,13 +608,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t sA = base;
   const uint32_t sB = base + C::STAGES * C::A_BYTES;
   const uint32_t sBar = sB + C::STAGES * C::B_BYTES;
-  const uint32_t sTmem = sBar + 8 * (2 * C::STAGES + 4);
+  const uint32_t sTmem = sBar + 8 * (2 * C::STAGES + 5);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (sTmem - base));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (sTmem - base) + 8);
 #define FULL(s) (sBar + 8u * (s))
 #define EMPTY(s) (sBar + 8u * (C::STAGES + (s)))
 #define ACC_FULL(a) (sBar + 8u * (2 * C::STAGES + (a)))
 #define ACC_EMPTY(a) (sBar + 8u * (2 * C::STAGES + 2 + (a)))
+#define EPI_MEET (sBar + 8u * (2 * C::STAGES + 4))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = (args.K + BK - 1) / BK;
@@ -457,6 +629,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_init(ACC_FULL(a), 1);
       mbar_init(ACC_EMPTY(a), 32 * EPI_WARPS);
     }
+    mbar_init(EPI_MEET, EPI_WARPS);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
@@ -475,11 +648,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (warp == 0) {
     if (lane == 0) {
       int it = 0;
-      for (int tile = blockIdx.x; tile < ext.tiles && !*abort_flag; tile += gridDim.x) {
-        const int ks = tile % args.ksplit;
+      Work w;
+      for (int i = 0; work_at(args, ext, nk, i, w) && !*abort_flag; ++i) {
         int m_blk, n_blk;
-        tile_coords(args, ext.tiles_m, tile / args.ksplit, m_blk, n_blk);
-        const int kb0 = ks * nk / args.ksplit, kb1 = (ks + 1) * nk / args.ksplit;
+        tile_coords(args, ext.tiles_m, w.tile, m_blk, n_blk);
+        const int kb0 = w.kb0, kb1 = w.kb1;
         const int m0 = m_blk * BM;
         const CUtensorMap* mp = &tmB0;
         int brow = n_blk * BN;
@@ -511,15 +684,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
-      int it = 0, lt = 0;
-      for (int tile = blockIdx.x; tile < ext.tiles && !*abort_flag; tile += gridDim.x, ++lt) {
+      int it = 0;
+      Work w;
+      for (int lt = 0; work_at(args, ext, nk, lt, w) && !*abort_flag; ++lt) {
         const int acc = lt & 1;
         const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
         if (!mbar_wait(ACC_EMPTY(acc), aph ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        const int ks = tile % args.ksplit;
-        const int kb0 = ks * nk / args.ksplit, kb1 = (ks + 1) * nk / args.ksplit;
+        const int kb0 = w.kb0, kb1 = w.kb1;
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % C::STAGES;
@@ -542,20 +715,39 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else {
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 belong to this warp
-    int lt = 0;
-    for (int tile = blockIdx.x; tile < ext.tiles; tile += gridDim.x, ++lt) {
+    const int part = (warp - 2) / 4, nparts = EPI_WARPS / 4;
+    int meets = 0;
+    Work w;
+    for (int lt = 0; work_at(args, ext, nk, lt, w); ++lt) {
       const int acc = lt & 1;
       const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+      int m_blk, n_blk;
+      tile_coords(args, ext.tiles_m, w.tile, m_blk, n_blk);
+      const int wrow0 = m_blk * BM + quad * 32;
+      if (w.role != WORK_PART) epi_prefetch<BN, MODE>(args, ext.M, wrow0 + lane, n_blk, part);
       if (!mbar_wait(ACC_FULL(acc), aph, abort_flag, args.status)) break;
       tc_fence_after();
-      int m_blk, n_blk;
-      tile_coords(args, ext.tiles_m, tile / args.ksplit, m_blk, n_blk);
-      const int wrow0 = m_blk * BM + quad * 32;
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<BN, MODE>(args, ext.M, wrow0, lane, n_blk, t_row, (warp - 2) / 4,
-                              EPI_WARPS / 4, tile % args.ksplit);
+      bool ok = true;
+      if (w.role == WORK_PART) {
+        sk_leave_partial<BN>(args, quad * 32 + lane, t_row, part, nparts);
+        __threadfence();
+        ok = epi_meet(EPI_MEET, meets, lane, abort_flag, args.status);
+        if (ok && warp == 2 && lane == 0) st_release_gpu(args.sk_flag + blockIdx.x, 1);
+      } else {
+        if (w.role == WORK_OWNER) {
+          if (warp == 2 && lane == 0 &&
+              flag_wait(args.sk_flag + blockIdx.x + 1, abort_flag, args.status))
+            args.sk_flag[blockIdx.x + 1] = 0;   // consumed: clear for the next launch
+          ok = epi_meet(EPI_MEET, meets, lane, abort_flag, args.status) && !*abort_flag;
+          if (ok) sk_add_partial<BN>(args, quad * 32 + lane, t_row, part, nparts);
+        }
+        if (ok)
+          epilogue_tile<BN, MODE>(args, ext.M, wrow0, lane, n_blk, t_row, part, nparts, w.ks);
+      }
       tc_fence_before();
       mbar_arrive(ACC_EMPTY(acc));
+      if (!ok) break;
     }
   }
 
@@ -576,6 +768,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #undef EMPTY
 #undef ACC_FULL
 #undef ACC_EMPTY
+#undef EPI_MEET
 }
 
 // ---------------------------------------------------------------- CTA-pair variant
@@ -721,11 +914,12 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     for (int tile = pair; tile < args.tiles; tile += npairs, ++lt) {
       const int acc = lt & 1;
       const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
-      if (!mbar_wait_cluster(ACC_FULL(acc), aph, abort_flag, args.status)) break;
-      tc_fence_after();
       int m_blk, n_blk;
       tile_coords(args, args.tiles_m, tile, m_blk, n_blk, XMOD_TILE_BAND2);
       const int wrow0 = m_blk * (2 * BM) + (int)rank * BM + quad * 32;
+      epi_prefetch<BN, MODE>(args, args.M, wrow0 + lane, n_blk, (warp - 2) / 4);
+      if (!mbar_wait_cluster(ACC_FULL(acc), aph, abort_flag, args.status)) break;
+      tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
       epilogue_tile<BN, MODE>(args, args.M, wrow0, lane, n_blk, t_row, (warp - 2) / 4,
                               EPI_WARPS / 4);
@@ -794,6 +988,10 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
   a.mode = e.kind;
   a.e = e;
   a.status = c.status;
+  a.sk = 0;
+  a.units = 0;
+  a.sk_part = nullptr;
+  a.sk_flag = nullptr;
   a.n_split1 = INT_MAX;
   a.n_split2 = INT_MAX;
   // 32-byte epilogue accesses need every row segment the epilogue touches aligned
@@ -804,7 +1002,7 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
   if (e.out && e.kind != EPI_ROUTER) v8 = v8 && seg_ok(e.out, (int64_t)e.ldo * 2);
   if (e.out2) v8 = v8 && seg_ok(e.out2, (int64_t)e.ldo2 * 4);
   if (e.x) v8 = v8 && seg_ok(e.x, (int64_t)e.d * 2);
-  if (e.h) v8 = v8 && seg_ok(e.h, (int64_t)e.d * 4);
+  if (e.a) v8 = v8 && seg_ok(e.a, (int64_t)e.d * 2);
   a.v8 = v8 ? 1 : 0;
   a.tiles_m = (p.M + tile_m - 1) / tile_m;
   int tiles_n;
@@ -834,14 +1032,41 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
   return true;
 }
 
+// Stream-K grid for a launch of `tiles` tiles of nk k-blocks: one CTA per SM (at most
+// the scratch slots), and only when every CTA's share spans a whole tile's k-blocks
+// (then a tile spans at most two CTAs); 0 when stream-K does not apply.
+// XMOD_STREAM_K_CTAS (read at every launch) caps the grid, so that small problems
+// can exercise tiles cut at many places.
+int stream_k_grid(const Ctx& c, long tiles, int nk) {
+  if (!c.sk_part || !c.sk_flag || c.sk_slots <= 0 || nk <= 0) return 0;
+  int P = sm_count() < c.sk_slots ? sm_count() : c.sk_slots;
+  const char* v = getenv("XMOD_STREAM_K_CTAS");
+  if (v && *v) {
+    char* end = nullptr;
+    const long cap = strtol(v, &end, 10);
+    if (end && *end == '\0' && cap > 0 && cap < P) P = (int)cap;
+  }
+  return tiles >= P ? P : 0;
+}
+
 template <int BN>
-cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
+cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, bool sk = false) {
   using Cf = Cfg<BN>;
   if ((e.kind == EPI_ROUTER) != (BN == 32)) return cudaErrorInvalidValue;
   CUtensorMap mA, mB0, mB1, mB2;
   TcArgs a;
   if (!setup<BN>(c, p, e, BM, BN, mA, mB0, mB1, mB2, a)) return cudaErrorInvalidValue;
   if (a.tiles <= 0) return cudaSuccess;
+  int grid = a.tiles < sm_count() ? a.tiles : sm_count();
+  if (sk) {
+    const int nk = (p.K + BK - 1) / BK;
+    grid = p.M_dev || a.ksplit != 1 ? 0 : stream_k_grid(c, a.tiles, nk);
+    if (grid <= 0) return cudaErrorInvalidValue;
+    a.sk = 1;
+    a.units = (int64_t)a.tiles * nk;
+    a.sk_part = c.sk_part;
+    a.sk_flag = c.sk_flag;
+  }
   void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
             const TcArgs) = nullptr;
   if constexpr (BN == 32) {
@@ -862,7 +1087,6 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
     if (err != cudaSuccess) return err;
     attr_set[e.kind] = true;
   }
-  const int grid = a.tiles < sm_count() ? a.tiles : sm_count();
   return launch_pdl(k, dim3(grid), dim3(NUM_THREADS), Cf::SMEM, c.stream, mA, mB0, mB1, mB2, a);
 }
 
@@ -956,6 +1180,14 @@ int pair_min_waves() {
   return XMOD_PAIR_MIN_WAVES;
 }
 
+// Stream-K choice: XMOD_STREAM_K=1 (read at every launch) runs every GEMM it applies
+// to as stream-K; otherwise none.
+int stream_k_mode() {
+  const char* v = getenv("XMOD_STREAM_K");
+  if (v && (v[0] == '0' || v[0] == '1') && v[1] == '\0') return v[0] - '0';
+  return -1;
+}
+
 cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   if (e.kind == EPI_ROUTER) return launch_bn<32>(c, p, e);
   // CTA pairs on 256 x 256 tiles when there are enough of them. Measured on GB300
@@ -988,6 +1220,15 @@ cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue&
       best = bn;
       best_cost = cost;
     }
+  }
+  // Stream-K at 256-wide tiles, on request only: on the A4K8 block's sparse-layer GEMMs
+  // (1.3-2.1 waves) it measured 10-50% slower than the tiling above -- storing and
+  // re-reading the fp32 partial tiles (128 KB per CTA, all CTAs at once) costs more
+  // than the partial last wave it removes.
+  if (stream_k_mode() == 1 && bn_ok(p, e, 256) && !p.M_dev && p.ksplit <= 1) {
+    const int cols = e.kind == EPI_SWIGLU ? 128 : 256;
+    const long tiles = (long)tiles_m * ((p.N + cols - 1) / cols);
+    if (stream_k_grid(c, tiles, (p.K + BK - 1) / BK) > 0) return launch_bn<256>(c, p, e, true);
   }
   if (best == 256) return launch_bn<256>(c, p, e);
   if (best == 192) return launch_bn<192>(c, p, e);

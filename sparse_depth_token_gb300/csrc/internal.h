@@ -14,6 +14,11 @@ namespace xmod {
 struct Ctx {
   cudaStream_t stream;
   int* status;  // device status word (first error wins)
+  // Stream-K scratch of the tensor-core GEMMs: sk_slots partial accumulators of
+  // 128 x 256 fp32 and as many flags, all zero between launches. NULL: no stream-K.
+  float* sk_part = nullptr;
+  int* sk_flag = nullptr;
+  int sk_slots = 0;
 };
 
 // Launch with programmatic stream serialization: the kernel may begin while the
@@ -159,10 +164,11 @@ cudaError_t launch_stack_rows(const Ctx& c, const RowPtrs& rows, int count, int 
 
 enum EpiKind {
   EPI_STORE = 0,         // out[m, n] = acc
-  EPI_OPROJ = 1,         // out2[m, n] = h = x_row(m)[n] + acc (fp32); out[m, n] = a = acc if out
+  EPI_OPROJ = 1,         // out[m, n] = a = acc if out; out2[m, n] = h = x_row(m)[n] + acc
+                         // (fp32) if out2
   EPI_SWIGLU = 2,        // out[m, n] = silu(acc_gate) * acc_up
-  EPI_DOWN_SCATTER = 3,  // x_row(m)[n] = gated residual of (a = h[m, n] - x, f = acc);
-                         // also out[m, n] = that new row value (bf16) when out is set
+  EPI_DOWN_SCATTER = 3,  // x_row(m)[n] = gated residual of (a[m, n], f = acc);
+                         // also out[m, n] = that new row value when out is set
   EPI_ROUTER = 4,        // out[n * ldo + stream token of m] = acc + bias[token] (fp32);
                          // tensor-core path only, 32-wide tiles, any N <= 32
 };
@@ -182,8 +188,8 @@ struct Epilogue {
   // is tok[m] (= b * T + t), and seq_off[b] is sequence b's first compact row.
   const int32_t* tok = nullptr;
   const int32_t* seq_off = nullptr;
-  const float* h = nullptr;     // DOWN: h = x_sel + a [M, d] fp32 (the attention residual is
-                                //       h - x); NULL: no attention residual (a = 0)
+  const void* a = nullptr;      // DOWN: the attention residual a [M, d] (the layer's dtype,
+                                //       row stride d); NULL: none (a = 0)
   const float* r_sel = nullptr; // DOWN: gates [M]
   const float* bias = nullptr;  // ROUTER: per-token logit bias [B*T] or NULL (k slice 0)
   int64_t plane = 0;            // ROUTER with k slices: elements between slice planes

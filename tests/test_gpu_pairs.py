@@ -42,7 +42,9 @@ def _run(X, w, kind, x, lw, bias, pairs):
     ws = workspace(dm, w.K)
     xd = to_dev(x, dt)
     old = os.environ.get("XMOD_PAIR_MIN_WAVES")
+    old_sk = os.environ.get("XMOD_STREAM_K")
     os.environ["XMOD_PAIR_MIN_WAVES"] = "0" if pairs else "1000000"
+    os.environ["XMOD_STREAM_K"] = "0"   # data-parallel single-CTA tiles: the same k order
     try:
         X.reset_status(ws)
         X.layer_fwd(dm, kind, w.K, 0, X.layer_weights(dev_layer(lw, dt), lw["varsigma"]), xd,
@@ -53,6 +55,10 @@ def _run(X, w, kind, x, lw, bias, pairs):
             del os.environ["XMOD_PAIR_MIN_WAVES"]
         else:
             os.environ["XMOD_PAIR_MIN_WAVES"] = old
+        if old_sk is None:
+            del os.environ["XMOD_STREAM_K"]
+        else:
+            os.environ["XMOD_STREAM_K"] = old_sk
     return xd
 
 
