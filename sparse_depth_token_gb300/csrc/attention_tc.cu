@@ -8,8 +8,9 @@
 // positions. Query head h reads key/value head h / (hq / hkv).
 //
 // One CTA per (128-query block, query head, sequence):
-//   warp 0      TMA: the Q tile once, then K_j and V_j^T of each 128-key block j
-//               into a two-stage ring
+//   warp 0      TMA: the Q tile once, then K_j and V_j^T of each key block j, each
+//               into its own two-stage ring (a K stage comes free when S_j has been
+//               computed, a V stage when P_j V_j has), whichever has a free stage first
 //   warp 1      TMEM owner; one lane issues S_j = Q K_j^T into one of two TMEM S
 //               buffers and O += P_j V_j (output accumulator O resident in TMEM), each
 //               as soon as its inputs are ready, so S_{j+1} overlaps the softmax of S_j
@@ -123,11 +124,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
   const uint32_t sK0 = sP0 + PBUF * C::P_BYTES;       // K stages at sK0 + s * K_STAGE
   const uint32_t sV0 = sK0 + 2 * C::K_STAGE;          // V^T stages at sV0 + s * V_STAGE
   const uint32_t sBar = (base - raw >= 256u) ? raw : base + (uint32_t)C::DATA;
+  // K_j and V_j^T have separate stages and barriers: a K stage is free again once
+  // S_j = Q K_j^T has completed, a V stage once P_j V_j has, so K loads run ahead of
+  // the P V MMAs instead of waiting for them.
   const uint32_t Q_FULL = sBar + 0;
-  const uint32_t KV_FULL0 = sBar + 8, KV_EMPTY0 = sBar + 24;
+  const uint32_t K_FULL0 = sBar + 8, K_EMPTY0 = sBar + 24;
   const uint32_t S_FULL0 = sBar + 40, S_EMPTY0 = sBar + 56;
   const uint32_t P_FULL0 = sBar + 72, P_EMPTY0 = sBar + 88;
-  const uint32_t sTmem = sBar + 112;
+  const uint32_t V_FULL0 = sBar + 104, V_EMPTY0 = sBar + 120;
+  const uint32_t sTmem = sBar + 144;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + (sTmem - raw));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + (sTmem - raw) + 8);
 
@@ -140,8 +145,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
   if (threadIdx.x == 0) {
     mbar_init(Q_FULL, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(KV_FULL0 + 8 * s, 1);
-      mbar_init(KV_EMPTY0 + 8 * s, 1);
+      mbar_init(K_FULL0 + 8 * s, 1);
+      mbar_init(K_EMPTY0 + 8 * s, 1);
+      mbar_init(V_FULL0 + 8 * s, 1);
+      mbar_init(V_EMPTY0 + 8 * s, 1);
       mbar_init(S_FULL0 + 8 * s, 1);
       mbar_init(S_EMPTY0 + 8 * s, 128);
     }
@@ -184,23 +191,55 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         tma_load_3d(sQ + CHUNK, &tmQ, Q_FULL, h * HD + 64, q0, b);
       }
       const int vt_row = (b * a.hkv + g) * HD;
-      for (int j = 0; j < nkb; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (uint32_t)(j >> 1) & 1u;
-        if (!mbar_wait(KV_EMPTY0 + 8 * s, ph ^ 1u, abort_flag, a.status)) break;
-        mbar_arrive_expect_tx(KV_FULL0 + 8 * s, C::K_STAGE + C::V_STAGE);
-        const uint32_t kdst = sK0 + s * C::K_STAGE, vdst = sV0 + s * C::V_STAGE;
-        if (a.seq_count) {
-          tma_load_2d(kdst, &tmK, KV_FULL0 + 8 * s, a.k_col0 + g * HD, (int)(row0 + j * KB));
-          tma_load_2d(kdst + C::K_CHUNK, &tmK, KV_FULL0 + 8 * s, a.k_col0 + g * HD + 64,
-                      (int)(row0 + j * KB));
-        } else {
-          tma_load_3d(kdst, &tmK, KV_FULL0 + 8 * s, a.k_col0 + g * HD, j * KB, b);
-          tma_load_3d(kdst + C::K_CHUNK, &tmK, KV_FULL0 + 8 * s, a.k_col0 + g * HD + 64, j * KB, b);
+      // issue whichever of the next K block and the next V block has a free stage
+      int jk = 0, jv = 0;
+      uint64_t t0 = global_timer_ns();
+      uint32_t spins = 0;
+      while (jv < nkb) {
+        bool progressed = false;
+        if (jk < nkb) {
+          const int s = jk & 1;
+          if (mbar_try_wait(K_EMPTY0 + 8 * s, ((uint32_t)(jk >> 1) & 1u) ^ 1u)) {
+            mbar_arrive_expect_tx(K_FULL0 + 8 * s, C::K_STAGE);
+            const uint32_t kdst = sK0 + s * C::K_STAGE;
+            if (a.seq_count) {
+              tma_load_2d(kdst, &tmK, K_FULL0 + 8 * s, a.k_col0 + g * HD, (int)(row0 + jk * KB));
+              tma_load_2d(kdst + C::K_CHUNK, &tmK, K_FULL0 + 8 * s, a.k_col0 + g * HD + 64,
+                          (int)(row0 + jk * KB));
+            } else {
+              tma_load_3d(kdst, &tmK, K_FULL0 + 8 * s, a.k_col0 + g * HD, jk * KB, b);
+              tma_load_3d(kdst + C::K_CHUNK, &tmK, K_FULL0 + 8 * s, a.k_col0 + g * HD + 64,
+                          jk * KB, b);
+            }
+            ++jk;
+            progressed = true;
+          }
         }
+        if (jv < jk) {
+          const int s = jv & 1;
+          if (mbar_try_wait(V_EMPTY0 + 8 * s, ((uint32_t)(jv >> 1) & 1u) ^ 1u)) {
+            mbar_arrive_expect_tx(V_FULL0 + 8 * s, C::V_STAGE);
+            const uint32_t vdst = sV0 + s * C::V_STAGE;
 #pragma unroll
-        for (int kc = 0; kc < KB / 64; ++kc)
-          tma_load_2d(vdst + kc * CHUNK, &tmVt, KV_FULL0 + 8 * s, j * KB + 64 * kc, vt_row);
+            for (int kc = 0; kc < KB / 64; ++kc)
+              tma_load_2d(vdst + kc * CHUNK, &tmVt, V_FULL0 + 8 * s, jv * KB + 64 * kc, vt_row);
+            ++jv;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t0 = global_timer_ns();
+          spins = 0;
+          continue;
+        }
+        if ((++spins & 255u) == 0u) {
+          if (*abort_flag) break;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            report_status(a.status, XMOD_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+        }
       }
     }
   } else if (warp == 1) {
@@ -220,7 +259,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         if (ns < nkb && ns <= npv + 1) {
           const int s = ns & 1;
           const uint32_t ph = (uint32_t)(ns >> 1) & 1u;
-          if (mbar_try_wait(KV_FULL0 + 8 * s, ph) && mbar_try_wait(S_EMPTY0 + 8 * s, ph ^ 1u)) {
+          if (mbar_try_wait(K_FULL0 + 8 * s, ph) && mbar_try_wait(S_EMPTY0 + 8 * s, ph ^ 1u)) {
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(s * KB);
 #pragma unroll
@@ -232,15 +271,17 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc_s, (kc | k) != 0 ? 1u : 0u);
             }
             mma_commit(S_FULL0 + 8 * s);
+            mma_commit(K_EMPTY0 + 8 * s);
             ++ns;
             progressed = true;
           }
         }
         if (npv < ns) {
-          const int s = npv & 1;                         // K/V stage
+          const int s = npv & 1;                         // V stage
           const int pb = npv % PBUF;                     // P buffer
           const uint32_t pph = (uint32_t)(npv / PBUF) & 1u;
-          if (mbar_try_wait(P_FULL0 + 8 * pb, pph)) {
+          if (mbar_try_wait(P_FULL0 + 8 * pb, pph) &&
+              mbar_try_wait(V_FULL0 + 8 * s, (uint32_t)(npv >> 1) & 1u)) {
             tc_fence_after();
 #pragma unroll
             for (int kc = 0; kc < KB / 64; ++kc) {
@@ -252,7 +293,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                          (npv | kc | k) != 0 ? 1u : 0u);
             }
             mma_commit(P_EMPTY0 + 8 * pb);
-            mma_commit(KV_EMPTY0 + 8 * s);
+            mma_commit(V_EMPTY0 + 8 * s);
             ++npv;
             progressed = true;
           }

@@ -224,26 +224,9 @@ __device__ __forceinline__ uint32_t order_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive scan of one value per warp (32 warps), result broadcast to the warp.
-__device__ __forceinline__ uint32_t warps_exclusive_scan(uint32_t v, uint32_t* sh) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) sh[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t t = sh[lane];
-    uint32_t inc = t;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += y;
-    }
-    sh[lane] = inc - t;
-  }
-  __syncthreads();
-  uint32_t r = sh[warp];
-  __syncthreads();
-  return r;
-}
+// Largest T whose logits are kept in shared memory beside the keys (for the gates of
+// the selected tokens); longer sequences read them again from global memory.
+constexpr int TOPK_CACHE_MAX_T = 24 * 1024;
 
 // TRACK: the token-choice bias state / statistics of tr are used (else tr is ignored
 // and the kernel is the plain top-(T/K)).
@@ -255,9 +238,10 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
   pdl_trigger();
   pdl_wait();
   extern __shared__ uint32_t keys[];
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t scan_sh[32];
-  __shared__ uint32_t sh_prefix, sh_remaining;
+  float* lsh = T <= TOPK_CACHE_MAX_T ? reinterpret_cast<float*>(keys + T) : nullptr;
+  __shared__ uint32_t hist[2][256];
+  __shared__ uint32_t scan_sh[2][32];
+  __shared__ uint32_t sh_prefix[2], sh_remaining[2];
   __shared__ int sh_bad;
   __shared__ uint32_t sh_stat[3];   // threshold-selected, agreeing, also selected before
   const int b = blockIdx.x;
@@ -265,17 +249,13 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
   const float* sb = s + (int64_t)b * T;
   int32_t* cnt = tr.count ? tr.count + (int64_t)b * T : nullptr;
   int32_t* last = tr.last ? tr.last + (int64_t)b * T : nullptr;
-  // the logit this layer ranks: s (the sum of its planes, in order) minus the block's
-  // accumulated token-choice bias
-  auto logit = [&](int t) {
-    float v = sb[t];
-    for (int k = 1; k < nplanes; ++k) v += sb[k * plane + t];
-    return cnt ? v - tr.bias_step * (float)cnt[t] : v;
-  };
   if (threadIdx.x == 0) sh_bad = 0;
   if (threadIdx.x < 3) sh_stat[threadIdx.x] = 0u;
+  for (int i = threadIdx.x; i < 256; i += TOPK_THREADS) hist[0][i] = 0u;
   __syncthreads();
-  // four positions per thread at a time, every plane's load issued before any is used
+  // The logit this layer ranks: s (the sum of its planes, in order) minus the block's
+  // accumulated token-choice bias. Four positions per thread at a time, every plane's
+  // load issued before any is used.
   for (int t0 = threadIdx.x; t0 < T; t0 += 4 * TOPK_THREADS) {
     float v[4];
 #pragma unroll
@@ -297,28 +277,33 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
         const float x = cnt ? v[i] - tr.bias_step * (float)cnt[t] : v[i];
         if (!isfinite(x)) sh_bad = 1;
         keys[t] = order_key(x);
+        if (lsh) lsh[t] = x;
       }
     }
   }
   __syncthreads();
   if (sh_bad && threadIdx.x == 0) report_status(status, XMOD_ERR_DEVICE_CHECK);
 
+  // Radix select, 8 bits per pass from the top. Histograms and results alternate
+  // between two buffers, so one pass needs two barriers: the next pass's histogram
+  // is cleared while this one is counted.
   uint32_t prefix = 0u, mask = 0u, remaining = (uint32_t)n;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += TOPK_THREADS) hist[i] = 0u;
-    __syncthreads();
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass, cur = pass & 1;
     for (int t = threadIdx.x; t < T; t += TOPK_THREADS) {
       const uint32_t k = keys[t];
-      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 0xffu], 1u);
+      if ((k & mask) == prefix) atomicAdd(&hist[cur][(k >> shift) & 0xffu], 1u);
     }
+    if (pass < 3)
+      for (int i = threadIdx.x; i < 256; i += TOPK_THREADS) hist[cur ^ 1][i] = 0u;
     __syncthreads();
     if (warp == 0) {
       // lane l owns digits 255-8l .. 248-8l (descending)
-      uint32_t cnt[8], tot = 0;
+      uint32_t c8[8], tot = 0;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        cnt[e] = hist[255 - (lane * 8 + e)];
-        tot += cnt[e];
+        c8[e] = hist[cur][255 - (lane * 8 + e)];
+        tot += c8[e];
       }
       uint32_t inc = tot;
 #pragma unroll
@@ -331,48 +316,56 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
         uint32_t run = excl;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          if (run + cnt[e] >= remaining) {
+          if (run + c8[e] >= remaining) {
             const uint32_t D = 255u - (uint32_t)(lane * 8 + e);
-            sh_prefix = prefix | (D << shift);
-            sh_remaining = remaining - run;
+            sh_prefix[cur] = prefix | (D << shift);
+            sh_remaining[cur] = remaining - run;
             break;
           }
-          run += cnt[e];
+          run += c8[e];
         }
       }
     }
     __syncthreads();
-    prefix = sh_prefix;
-    remaining = sh_remaining;
+    prefix = sh_prefix[cur];
+    remaining = sh_remaining[cur];
     mask |= 0xffu << shift;
-    __syncthreads();
   }
   const uint32_t kth = prefix;
 
-  // Warp w owns positions [w*W, (w+1)*W), visited 32 at a time in order.
+  // Warp w owns positions [w*W, (w+1)*W), visited 32 at a time in order. One sweep
+  // counts the keys above K* and equal to it per warp; one scan of both counts gives
+  // each warp its first output slot: the keys above K* before it, plus the equal keys
+  // before it up to `remaining` (ties go to the lower position).
   const int W = ((T + TOPK_THREADS - 1) / TOPK_THREADS) * 32;
   const int lo = warp * W;
   const int hi = min(T, lo + W);
   const uint32_t lt_mask = (1u << lane) - 1u;
-  uint32_t my_eq = 0;
-  for (int base = lo; base < hi; base += 32) {
-    const int t = base + lane;
-    const bool eq = t < hi && keys[t] == kth;
-    my_eq += __popc(__ballot_sync(0xffffffffu, eq));
-  }
-  const uint32_t eq_before = warps_exclusive_scan(my_eq, scan_sh);
-  uint32_t eq_run = eq_before, my_sel = 0;
+  uint32_t my_gt = 0, my_eq = 0;
   for (int base = lo; base < hi; base += 32) {
     const int t = base + lane;
     const uint32_t k = t < hi ? keys[t] : 0u;
-    const bool eq = t < hi && k == kth;
-    const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
-    const bool sel = t < hi && (k > kth || (eq && eq_run + __popc(eqm & lt_mask) < remaining));
-    my_sel += __popc(__ballot_sync(0xffffffffu, sel));
-    eq_run += __popc(eqm);
+    my_gt += __popc(__ballot_sync(0xffffffffu, t < hi && k > kth));
+    my_eq += __popc(__ballot_sync(0xffffffffu, t < hi && k == kth));
   }
-  uint32_t out = warps_exclusive_scan(my_sel, scan_sh);
-  eq_run = eq_before;
+  if (lane == 0) {
+    scan_sh[0][warp] = my_gt;
+    scan_sh[1][warp] = my_eq;
+  }
+  __syncthreads();
+  if (warp < 2) {
+    const uint32_t v = scan_sh[warp][lane];
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    scan_sh[warp][lane] = inc - v;
+  }
+  __syncthreads();
+  uint32_t eq_run = scan_sh[1][warp];
+  uint32_t out = scan_sh[0][warp] + min(eq_run, remaining);
   uint32_t n_thr = 0, n_agree = 0, n_again = 0;
   for (int base = lo; base < hi; base += 32) {
     const int t = base + lane;
@@ -381,18 +374,32 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
     const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
     const bool sel = t < hi && (k > kth || (eq && eq_run + __popc(eqm & lt_mask) < remaining));
     const uint32_t selm = __ballot_sync(0xffffffffu, sel);
-    if (sel) {
-      const uint32_t o = out + __popc(selm & lt_mask);
-      if (o < (uint32_t)n) {
-        idx[(int64_t)b * n + o] = t;
-        if (r_sel) r_sel[(int64_t)b * n + o] = sigmoidf_acc(logit(t));
-      }
-    }
     if (tr.stats) {
       const bool thr = t < hi && k >= 0x80000000u;   // logit >= 0, i.e. r >= 1/2
       n_thr += __popc(__ballot_sync(0xffffffffu, thr));
       n_agree += __popc(__ballot_sync(0xffffffffu, t < hi && thr == sel));
       n_again += __popc(__ballot_sync(0xffffffffu, sel && last && last[t] == tr.layer - 1));
+    }
+    if (sel) {
+      const uint32_t o = out + __popc(selm & lt_mask);
+      if (o < (uint32_t)n) {
+        idx[(int64_t)b * n + o] = t;
+        if (r_sel) {
+          float x;
+          if (lsh) {
+            x = lsh[t];
+          } else {
+            x = sb[t];
+            for (int k2 = 1; k2 < nplanes; ++k2) x += sb[k2 * plane + t];
+            if (cnt) x -= tr.bias_step * (float)cnt[t];
+          }
+          r_sel[(int64_t)b * n + o] = sigmoidf_acc(x);
+        }
+      }
+      // this thread alone owns position t: record the selection for the block's later
+      // layers after its last read of cnt[t] and last[t] above
+      if (cnt) cnt[t] += 1;
+      if (last) last[t] = tr.layer;
     }
     out += __popc(selm);
     eq_run += __popc(eqm);
@@ -403,18 +410,6 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
       atomicAdd(&sh_stat[1], n_agree);
       atomicAdd(&sh_stat[2], n_again);
     }
-  }
-  if (cnt || last) {
-    // record this layer's selection for the block's later layers (after every read of
-    // cnt and last above: the logits and the overlap with the previous layer)
-    __syncthreads();
-    for (int j = threadIdx.x; j < n; j += TOPK_THREADS) {
-      const int t = idx[(int64_t)b * n + j];
-      if (cnt) cnt[t] += 1;
-      if (last) last[t] = tr.layer;
-    }
-  }
-  if (tr.stats) {
     __syncthreads();
     if (threadIdx.x == 0) {
       int32_t* st = tr.stats + (int64_t)b * 4;
@@ -430,7 +425,8 @@ cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32
                         float* r_sel, const RouteTrack* tr, int nplanes, int64_t plane) {
   if (nplanes < 1) return cudaErrorInvalidValue;
   if (B <= 0) return cudaSuccess;
-  const size_t smem = sizeof(uint32_t) * (size_t)T;
+  // keys, and the logits too up to TOPK_CACHE_MAX_T
+  const size_t smem = sizeof(uint32_t) * (size_t)T * (T <= TOPK_CACHE_MAX_T ? 2 : 1);
   cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)(sizeof(uint32_t) * TOPK_MAX_T));
   cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
