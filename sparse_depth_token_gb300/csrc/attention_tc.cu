@@ -16,8 +16,9 @@
 //               as soon as its inputs are ready, so S_{j+1} overlaps the softmax of S_j
 //   warps 2..5  softmax, one query row per thread (a TMEM lane is a row, so row max
 //               and row sum are thread-local), in one pass over the scores held in
-//               registers: P_j = exp2(s*scale - m) is written as bf16 into one of two
-//               shared-memory P buffers in the swizzled K-major layout the MMA reads.
+//               registers: P_j = exp2(s*scale - m) goes back to TMEM as bf16 pairs, over
+//               the first half of S_j's own columns, and the P V MMA reads its A operand
+//               from there (no shared-memory P buffer; that space holds a third V stage).
 //               The running max m only moves when a row's max grows by more than 2^8
 //               (P then stays below 256); when it moves, the row of O in TMEM is
 //               rescaled once P_{j-1} V_{j-1} has landed.
@@ -44,23 +45,25 @@ constexpr int CHUNK = 128 * 128;        // bytes of a 128-row x 64-column bf16 s
 constexpr int QTILE = 2 * CHUNK;        // the Q tile, 128 x 128
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
-// KB keys per block; PBUF shared-memory P buffers. <128, 2> suits long sequences
-// (one CTA per SM); <64, 1> needs half the shared memory and TMEM so that two CTAs
-// share an SM and hide each other's load and set-up latency (short sequences).
-template <int KB, int PBUF>
+// KB keys per block; KST K stages and VST V stages. <128, 3, 3> (one CTA per SM) serves
+// sequences of one key block; <64, 2, 3> needs half the shared memory and TMEM so that
+// two CTAs share an SM and hide each other's load and set-up latency.
+template <int KB, int KST, int VST>
 struct AttnCfg {
   static constexpr int K_CHUNK = KB * 128;          // KB rows x 64 head dims
   static constexpr int K_STAGE = 2 * K_CHUNK;       // KB x 128 head dims
   static constexpr int V_STAGE = (KB / 64) * CHUNK; // 128 head dims x KB keys
-  static constexpr int P_BYTES = (KB / 64) * CHUNK; // 128 rows x KB keys
   static constexpr int TMEM_COLS = 2 * KB + 128 <= 256 ? 256 : 512;
-  static constexpr int DATA = QTILE + PBUF * P_BYTES + 2 * K_STAGE + 2 * V_STAGE;
+  static constexpr int DATA = QTILE + KST * K_STAGE + VST * V_STAGE;
   // 1024 bytes cover both the alignment of the tiles and the 256-byte barrier
   // block: the barriers sit in the alignment gap when it is at least 256 bytes,
   // else after the tiles (then the gap is under 256 bytes).
   static constexpr int SMEM = DATA + 1024;
   // two CTAs fit in the 228 KB of an SM (each also takes 1 KB reserved by the system)
   static constexpr int MIN_BLOCKS = 2 * (SMEM + 1024) <= 228 * 1024 ? 2 : 1;
+  // barriers: Q, K full/empty per stage, V full/empty per stage, S and P full/empty x2;
+  // then the TMEM address and the abort flag
+  static_assert((1 + 2 * KST + 2 * VST + 8) * 8 + 16 <= 256, "barrier block overflows");
 };
 
 struct AttnArgs {
@@ -84,13 +87,6 @@ struct AttnArgs {
   int k_col0;
 };
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-
 // 2^x by the PTX ex2.approx instruction: its error is far below the bf16 rounding the
 // probabilities get right after. Inputs are <= 0 here; -inf gives 0.
 #ifndef XMOD_ATTN_EX2_APPROX
@@ -106,33 +102,29 @@ __device__ __forceinline__ float exp2_p(float x) {
 #endif
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-template <int KB, int PBUF>
-__global__ void __launch_bounds__(THREADS, (AttnCfg<KB, PBUF>::MIN_BLOCKS))
+template <int KB, int KST, int VST>
+__global__ void __launch_bounds__(THREADS, (AttnCfg<KB, KST, VST>::MIN_BLOCKS))
 attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmVt, const AttnArgs a) {
-  using C = AttnCfg<KB, PBUF>;
+  using C = AttnCfg<KB, KST, VST>;
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   const uint32_t sQ = base;
-  const uint32_t sP0 = sQ + QTILE;                    // P buffers at sP0 + b * P_BYTES
-  const uint32_t sK0 = sP0 + PBUF * C::P_BYTES;       // K stages at sK0 + s * K_STAGE
-  const uint32_t sV0 = sK0 + 2 * C::K_STAGE;          // V^T stages at sV0 + s * V_STAGE
+  const uint32_t sK0 = sQ + QTILE;                    // K stages at sK0 + s * K_STAGE
+  const uint32_t sV0 = sK0 + KST * C::K_STAGE;        // V^T stages at sV0 + s * V_STAGE
   const uint32_t sBar = (base - raw >= 256u) ? raw : base + (uint32_t)C::DATA;
   // K_j and V_j^T have separate stages and barriers: a K stage is free again once
   // S_j = Q K_j^T has completed, a V stage once P_j V_j has, so K loads run ahead of
   // the P V MMAs instead of waiting for them.
+  // P_FULL(b): P_j is in TMEM buffer b = j & 1; P_EMPTY(b): P_j V_j has completed.
   const uint32_t Q_FULL = sBar + 0;
-  const uint32_t K_FULL0 = sBar + 8, K_EMPTY0 = sBar + 24;
-  const uint32_t S_FULL0 = sBar + 40, S_EMPTY0 = sBar + 56;
-  const uint32_t P_FULL0 = sBar + 72, P_EMPTY0 = sBar + 88;
-  const uint32_t V_FULL0 = sBar + 104, V_EMPTY0 = sBar + 120;
-  const uint32_t sTmem = sBar + 144;
+  const uint32_t K_FULL0 = sBar + 8, K_EMPTY0 = K_FULL0 + 8 * KST;
+  const uint32_t V_FULL0 = K_EMPTY0 + 8 * KST, V_EMPTY0 = V_FULL0 + 8 * VST;
+  const uint32_t S_FULL0 = V_EMPTY0 + 8 * VST, S_EMPTY0 = S_FULL0 + 16;
+  const uint32_t P_FULL0 = S_EMPTY0 + 16, P_EMPTY0 = P_FULL0 + 16;
+  const uint32_t sTmem = P_EMPTY0 + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + (sTmem - raw));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + (sTmem - raw) + 8);
 
@@ -144,17 +136,19 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
 
   if (threadIdx.x == 0) {
     mbar_init(Q_FULL, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(K_FULL0 + 8 * s, 1);
       mbar_init(K_EMPTY0 + 8 * s, 1);
+    }
+    for (int s = 0; s < VST; ++s) {
       mbar_init(V_FULL0 + 8 * s, 1);
       mbar_init(V_EMPTY0 + 8 * s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(S_FULL0 + 8 * s, 1);
       mbar_init(S_EMPTY0 + 8 * s, 128);
-    }
-    for (int pb = 0; pb < PBUF; ++pb) {
-      mbar_init(P_FULL0 + 8 * pb, 128);
-      mbar_init(P_EMPTY0 + 8 * pb, 1);
+      mbar_init(P_FULL0 + 8 * s, 128);
+      mbar_init(P_EMPTY0 + 8 * s, 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -198,8 +192,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
       while (jv < nkb) {
         bool progressed = false;
         if (jk < nkb) {
-          const int s = jk & 1;
-          if (mbar_try_wait(K_EMPTY0 + 8 * s, ((uint32_t)(jk >> 1) & 1u) ^ 1u)) {
+          const int s = jk % KST;
+          if (mbar_try_wait(K_EMPTY0 + 8 * s, ((uint32_t)(jk / KST) & 1u) ^ 1u)) {
             mbar_arrive_expect_tx(K_FULL0 + 8 * s, C::K_STAGE);
             const uint32_t kdst = sK0 + s * C::K_STAGE;
             if (a.seq_count) {
@@ -216,8 +210,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
           }
         }
         if (jv < jk) {
-          const int s = jv & 1;
-          if (mbar_try_wait(V_EMPTY0 + 8 * s, ((uint32_t)(jv >> 1) & 1u) ^ 1u)) {
+          const int s = jv % VST;
+          if (mbar_try_wait(V_EMPTY0 + 8 * s, ((uint32_t)(jv / VST) & 1u) ^ 1u)) {
             mbar_arrive_expect_tx(V_FULL0 + 8 * s, C::V_STAGE);
             const uint32_t vdst = sV0 + s * C::V_STAGE;
 #pragma unroll
@@ -256,44 +250,46 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
       uint32_t spins = 0;
       while (ok && npv < nkb) {
         bool progressed = false;
+        // S_{j+2} overwrites buffer j & 1, which holds P_j: it is issued after P_j V_j
+        // (MMAs of one thread run in order)
         if (ns < nkb && ns <= npv + 1) {
-          const int s = ns & 1;
+          const int s = ns & 1, ks = ns % KST;
           const uint32_t ph = (uint32_t)(ns >> 1) & 1u;
-          if (mbar_try_wait(K_FULL0 + 8 * s, ph) && mbar_try_wait(S_EMPTY0 + 8 * s, ph ^ 1u)) {
+          if (mbar_try_wait(K_FULL0 + 8 * ks, (uint32_t)(ns / KST) & 1u) &&
+              mbar_try_wait(S_EMPTY0 + 8 * s, ph ^ 1u)) {
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(s * KB);
 #pragma unroll
             for (int kc = 0; kc < 2; ++kc) {
               const uint64_t ad = smem_desc_sw128(sQ + kc * CHUNK);
-              const uint64_t bd = smem_desc_sw128(sK0 + s * C::K_STAGE + kc * C::K_CHUNK);
+              const uint64_t bd = smem_desc_sw128(sK0 + ks * C::K_STAGE + kc * C::K_CHUNK);
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc_s, (kc | k) != 0 ? 1u : 0u);
             }
             mma_commit(S_FULL0 + 8 * s);
-            mma_commit(K_EMPTY0 + 8 * s);
+            mma_commit(K_EMPTY0 + 8 * ks);
             ++ns;
             progressed = true;
           }
         }
         if (npv < ns) {
-          const int s = npv & 1;                         // V stage
-          const int pb = npv % PBUF;                     // P buffer
-          const uint32_t pph = (uint32_t)(npv / PBUF) & 1u;
-          if (mbar_try_wait(P_FULL0 + 8 * pb, pph) &&
-              mbar_try_wait(V_FULL0 + 8 * s, (uint32_t)(npv >> 1) & 1u)) {
+          const int pb = npv & 1, vs = npv % VST;       // P buffer (TMEM), V stage
+          if (mbar_try_wait(P_FULL0 + 8 * pb, (uint32_t)(npv >> 1) & 1u) &&
+              mbar_try_wait(V_FULL0 + 8 * vs, (uint32_t)(npv / VST) & 1u)) {
             tc_fence_after();
+            // A = P_j from TMEM: 16 keys (8 columns of bf16 pairs) per MMA
+            const uint32_t tp = tmem + (uint32_t)(pb * KB);
 #pragma unroll
             for (int kc = 0; kc < KB / 64; ++kc) {
-              const uint64_t ad = smem_desc_sw128(sP0 + pb * C::P_BYTES + kc * CHUNK);
-              const uint64_t bd = smem_desc_sw128(sV0 + s * C::V_STAGE + kc * CHUNK);
+              const uint64_t bd = smem_desc_sw128(sV0 + vs * C::V_STAGE + kc * CHUNK);
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_bf16(tO, ad + 2ull * k, bd + 2ull * k, idesc_o,
-                         (npv | kc | k) != 0 ? 1u : 0u);
+                mma_bf16_tmem_a(tO, tp + (uint32_t)(32 * kc + 8 * k), bd + 2ull * k, idesc_o,
+                                (npv | kc | k) != 0 ? 1u : 0u);
             }
             mma_commit(P_EMPTY0 + 8 * pb);
-            mma_commit(V_EMPTY0 + 8 * s);
+            mma_commit(V_EMPTY0 + 8 * vs);
             ++npv;
             progressed = true;
           }
@@ -326,7 +322,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
       qp_min = a.qpos[base_row + q0];
     }
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t sw = (uint32_t)(row & 7);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkb; ++j) {
@@ -367,7 +362,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // O holds P_0..j-1 V: wait until the last of those MMAs landed, then rescale.
         const int jp = j - 1;
-        if (!mbar_wait(P_EMPTY0 + 8 * (jp % PBUF), (uint32_t)(jp / PBUF) & 1u, abort_flag,
+        if (!mbar_wait(P_EMPTY0 + 8 * (jp & 1), (uint32_t)(jp >> 1) & 1u, abort_flag,
                        a.status)) {
           ok = false;
           break;
@@ -385,41 +380,31 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         tmem_st_wait();
       }
       m = m_new;
-      // this P buffer is free once P_{j-PBUF} V_{j-PBUF} has completed
-      const int pb = j % PBUF;
-      if (!mbar_wait(P_EMPTY0 + 8 * pb, ((uint32_t)(j / PBUF) & 1u) ^ 1u, abort_flag, a.status)) {
-        ok = false;
-        break;
-      }
-      const uint32_t prow = sP0 + pb * C::P_BYTES + (uint32_t)row * 128u;
+      // P_j as bf16 pairs over the first KB / 2 columns of S_j's buffer (S_j has been
+      // read; P_{j-2}, which the buffer held before S_j, was consumed by then)
       float sum = 0.f;
+      const uint32_t prow = tmem + lane_off + (uint32_t)(s * KB);
 #pragma unroll
-      for (int c = 0; c < KB / 32; ++c) {
-        uint32_t pk[16];
+      for (int c = 0; c < KB / 64; ++c) {
+        float pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = exp2_p(fmaf(v[c * 32 + i], a.scale_log2, -m));
-          const float p1 = exp2_p(fmaf(v[c * 32 + i + 1], a.scale_log2, -m));
+        for (int i = 0; i < 64; i += 2) {
+          const float p0 = exp2_p(fmaf(v[c * 64 + i], a.scale_log2, -m));
+          const float p1 = exp2_p(fmaf(v[c * 64 + i + 1], a.scale_log2, -m));
           sum += p0 + p1;
-          pk[i / 2] = pack_bf16x2(p0, p1);
+          pk[i / 2] = __uint_as_float(pack_bf16x2(p0, p1));
         }
-        const uint32_t chunk = prow + (uint32_t)(c >> 1) * CHUNK;
-#pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {
-          const uint32_t unit = (uint32_t)((c & 1) * 4 + u4);
-          st_shared_v4(chunk + ((unit ^ sw) << 4), pk[4 * u4], pk[4 * u4 + 1], pk[4 * u4 + 2],
-                       pk[4 * u4 + 3]);
-        }
+        tmem_st32(prow + (uint32_t)(32 * c), pk);
       }
+      tmem_st_wait();
       l = l * alpha + sum;
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(P_FULL0 + 8 * pb);
+      mbar_arrive(P_FULL0 + 8 * s);
     }
     if (nkb == 0) ok = false;   // nothing was computed for this query block
     if (ok) {
       const int jl = nkb - 1;
-      ok = mbar_wait(P_EMPTY0 + 8 * (jl % PBUF), (uint32_t)(jl / PBUF) & 1u, abort_flag, a.status);
+      ok = mbar_wait(P_EMPTY0 + 8 * (jl & 1), (uint32_t)(jl >> 1) & 1u, abort_flag, a.status);
     }
     if (ok) {
       tc_fence_after();
@@ -458,10 +443,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
   }
 }
 
-template <int KB, int PBUF>
+template <int KB, int KST, int VST>
 cudaError_t launch_attention_cfg(const Ctx& c, int B, int n, int hq, const void* qkv, int ldq,
                                  const CUtensorMap& mVt, const AttnArgs& a, const AttnKv* kv) {
-  using Cf = AttnCfg<KB, PBUF>;
+  using Cf = AttnCfg<KB, KST, VST>;
   CUtensorMap mQ, mK;
   if (kv) {   // queries [B, n, ldq]; keys [B, nkv, ldk] from their own tensor
     const int64_t qdims[3] = {ldq, n, B};
@@ -487,7 +472,7 @@ cudaError_t launch_attention_cfg(const Ctx& c, int B, int n, int hq, const void*
     if (!tma_map_bf16(&mQ, qkv, 3, dims, strides, qbox)) return cudaErrorInvalidValue;
     if (!tma_map_bf16(&mK, qkv, 3, dims, strides, kbox)) return cudaErrorInvalidValue;
   }
-  auto k = attention_tc_kernel<KB, PBUF>;
+  auto k = attention_tc_kernel<KB, KST, VST>;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
@@ -504,7 +489,7 @@ cudaError_t launch_attention_cfg(const Ctx& c, int B, int n, int hq, const void*
 }  // namespace
 
 // A sequence of at most this many tokens is one 128-key block: it runs the
-// <128, 2> configuration; longer ones the two-CTAs-per-SM <64, 1> configuration,
+// <128, 3, 3> configuration; longer ones the two-CTAs-per-SM <64, 2, 3> configuration,
 // which measured 7-15% faster from 256 to 16384 tokens (GB300, 12/4 and 16/4 heads).
 #ifndef XMOD_ATTN_ONE_BLOCK_MAX_N
 #define XMOD_ATTN_ONE_BLOCK_MAX_N 128
@@ -544,8 +529,8 @@ cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, con
   a.nkv = nkv;
   a.k_col0 = kv ? 0 : a.qw;
   if (nkv <= XMOD_ATTN_ONE_BLOCK_MAX_N)
-    return launch_attention_cfg<128, 2>(c, B, n, hq, qkv, ldq, mVt, a, kv);
-  return launch_attention_cfg<64, 1>(c, B, n, hq, qkv, ldq, mVt, a, kv);
+    return launch_attention_cfg<128, 3, 3>(c, B, n, hq, qkv, ldq, mVt, a, kv);
+  return launch_attention_cfg<64, 2, 3>(c, B, n, hq, qkv, ldq, mVt, a, kv);
 }
 
 }  // namespace xmod
