@@ -129,8 +129,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + (sTmem - raw) + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qb = a.nqb - 1 - (int)blockIdx.x;   // longest rows first
-  const int h = blockIdx.y, b = blockIdx.z;
+  // CTAs start in blockIdx order, x fastest: every (head, sequence) pair's last query
+  // block (the most keys) first, then the next-to-last ones, ... (longest first)
+  const int qb = a.nqb - 1 - (int)blockIdx.z;
+  const int h = blockIdx.x, b = blockIdx.y;
   const int g = h / (a.hq / a.hkv);
   const int q0 = qb * QB;
 
@@ -193,7 +195,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         bool progressed = false;
         if (jk < nkb) {
           const int s = jk % KST;
-          if (mbar_try_wait(K_EMPTY0 + 8 * s, ((uint32_t)(jk / KST) & 1u) ^ 1u)) {
+          if (mbar_test_wait(K_EMPTY0 + 8 * s, ((uint32_t)(jk / KST) & 1u) ^ 1u)) {
             mbar_arrive_expect_tx(K_FULL0 + 8 * s, C::K_STAGE);
             const uint32_t kdst = sK0 + s * C::K_STAGE;
             if (a.seq_count) {
@@ -211,7 +213,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
         if (jv < jk) {
           const int s = jv % VST;
-          if (mbar_try_wait(V_EMPTY0 + 8 * s, ((uint32_t)(jv / VST) & 1u) ^ 1u)) {
+          if (mbar_test_wait(V_EMPTY0 + 8 * s, ((uint32_t)(jv / VST) & 1u) ^ 1u)) {
             mbar_arrive_expect_tx(V_FULL0 + 8 * s, C::V_STAGE);
             const uint32_t vdst = sV0 + s * C::V_STAGE;
 #pragma unroll
@@ -255,8 +257,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         if (ns < nkb && ns <= npv + 1) {
           const int s = ns & 1, ks = ns % KST;
           const uint32_t ph = (uint32_t)(ns >> 1) & 1u;
-          if (mbar_try_wait(K_FULL0 + 8 * ks, (uint32_t)(ns / KST) & 1u) &&
-              mbar_try_wait(S_EMPTY0 + 8 * s, ph ^ 1u)) {
+          if (mbar_test_wait(K_FULL0 + 8 * ks, (uint32_t)(ns / KST) & 1u) &&
+              mbar_test_wait(S_EMPTY0 + 8 * s, ph ^ 1u)) {
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(s * KB);
 #pragma unroll
@@ -275,8 +277,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
         }
         if (npv < ns) {
           const int pb = npv & 1, vs = npv % VST;       // P buffer (TMEM), V stage
-          if (mbar_try_wait(P_FULL0 + 8 * pb, (uint32_t)(npv >> 1) & 1u) &&
-              mbar_try_wait(V_FULL0 + 8 * vs, (uint32_t)(npv / VST) & 1u)) {
+          if (mbar_test_wait(P_FULL0 + 8 * pb, (uint32_t)(npv >> 1) & 1u) &&
+              mbar_test_wait(V_FULL0 + 8 * vs, (uint32_t)(npv / VST) & 1u)) {
             tc_fence_after();
             // A = P_j from TMEM: 16 keys (8 columns of bf16 pairs) per MMA
             const uint32_t tp = tmem + (uint32_t)(pb * KB);
@@ -482,7 +484,7 @@ cudaError_t launch_attention_cfg(const Ctx& c, int B, int n, int hq, const void*
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(a.nqb, hq, B);
+  dim3 grid(hq, B, a.nqb);
   return launch_pdl(k, grid, dim3(THREADS), Cf::SMEM, c.stream, mQ, mK, mVt, a);
 }
 
