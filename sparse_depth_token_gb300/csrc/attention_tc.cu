@@ -46,7 +46,7 @@ constexpr int QTILE = 2 * CHUNK;        // the Q tile, 128 x 128
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
 // KB keys per block; KST K stages and VST V stages. <128, 3, 3> (one CTA per SM) serves
-// sequences of one key block; <64, 2, 3> needs half the shared memory and TMEM so that
+// sequences of one key block; <64, 3, 2> needs half the shared memory and TMEM so that
 // two CTAs share an SM and hide each other's load and set-up latency.
 template <int KB, int KST, int VST>
 struct AttnCfg {
@@ -491,8 +491,13 @@ cudaError_t launch_attention_cfg(const Ctx& c, int B, int n, int hq, const void*
 }  // namespace
 
 // A sequence of at most this many tokens is one 128-key block: it runs the
-// <128, 3, 3> configuration; longer ones the two-CTAs-per-SM <64, 2, 3> configuration,
+// <128, 3, 3> configuration; longer ones the two-CTAs-per-SM <64, 3, 2> configuration,
 // which measured 7-15% faster from 256 to 16384 tokens (GB300, 12/4 and 16/4 heads).
+// K stages of the 64-key configuration (the V stages take the rest of the five its
+// shared memory holds).
+#ifndef XMOD_ATTN_K_STAGES
+#define XMOD_ATTN_K_STAGES 3
+#endif
 #ifndef XMOD_ATTN_ONE_BLOCK_MAX_N
 #define XMOD_ATTN_ONE_BLOCK_MAX_N 128
 #endif
@@ -532,7 +537,8 @@ cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, con
   a.k_col0 = kv ? 0 : a.qw;
   if (nkv <= XMOD_ATTN_ONE_BLOCK_MAX_N)
     return launch_attention_cfg<128, 3, 3>(c, B, n, hq, qkv, ldq, mVt, a, kv);
-  return launch_attention_cfg<64, 2, 3>(c, B, n, hq, qkv, ldq, mVt, a, kv);
+  return launch_attention_cfg<64, XMOD_ATTN_K_STAGES, 5 - XMOD_ATTN_K_STAGES>(c, B, n, hq, qkv,
+                                                                            ldq, mVt, a, kv);
 }
 
 }  // namespace xmod
