@@ -43,7 +43,7 @@ def _run(X, w, kind, x, lw, bias, pairs):
     xd = to_dev(x, dt)
     old = os.environ.get("XMOD_PAIR_MIN_WAVES")
     old_sk = os.environ.get("XMOD_STREAM_K")
-    os.environ["XMOD_PAIR_MIN_WAVES"] = "0" if pairs else "1000000"
+    os.environ["XMOD_PAIR_MIN_WAVES"] = "0" if pairs else "999999"
     os.environ["XMOD_STREAM_K"] = "0"   # data-parallel single-CTA tiles: the same k order
     try:
         X.reset_status(ws)

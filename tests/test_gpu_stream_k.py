@@ -57,7 +57,7 @@ def _run(X, w, kind, x, lw, bias, **env):
     dm = xmod_dims(w)
     ws = workspace(dm, w.K)
     xd = to_dev(x, dt)
-    with _Env(XMOD_PAIR_MIN_WAVES=1000000, **env):
+    with _Env(XMOD_PAIR_MIN_WAVES=999999, **env):
         X.reset_status(ws)
         X.layer_fwd(dm, kind, w.K, 0, X.layer_weights(dev_layer(lw, dt), lw["varsigma"]), xd,
                     torch.from_numpy(bias).cuda() if bias is not None else None, None, None, ws)
