@@ -519,6 +519,300 @@ def run_xmod(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------- routing microbench
+
+ROUTING_KS = (2, 8, 16)
+ROUTING_HEADLINE_K = 8
+
+
+def routing_work(w: I.Workload, K: int) -> dict:
+    """Compulsory HBM bytes per step of the routing-only pipeline, per kernel kind: the
+    router reads x once and writes the logits; top-k reads the logits and writes idx and
+    the gates; the gather reads and writes M rows; the scatter reads a+f and the x rows
+    and writes the x rows."""
+    es = 2 if w.dtype == "bf16" else 4
+    BT, M = w.B * w.T, w.B * (w.T // K)
+    return {"router": BT * w.d * es + 4 * BT,
+            "topk": 4 * BT + 8 * M,
+            "gather": 2 * M * w.d * es + 4 * M,
+            "gated_scatter": 3 * M * w.d * es + 8 * M}
+
+
+def routing_config(w: I.Workload, K: int) -> dict:
+    return {
+        "workload": f"{w.name}: routing-only microbench (router GEMV + top-(T/K) + gather + "
+                    f"Eq. 7 gated scatter of a given block output a+f~N(0,1)), "
+                    f"B={w.B}, T={w.T}, d={w.d}, K={K}",
+        "B_per_gpu": w.B, "T": w.T, "d": w.d, "K": K,
+        "selected_tokens_per_step_per_gpu": w.B * (w.T // K),
+        "l2": f"no flush: x is {w.B * w.T * w.d * 2 / 1e9:.2f} GB, far above the 129 MB L2",
+        "inputs": "seeded synthetic: x~N(0,1), w_r~N(0,1/d), bias 0, a+f~N(0,1), varsigma 1",
+    }
+
+
+def oracle_routing_sample(w: I.Workload, K: int, budget_s: float = 15.0, max_reps: int = 5000):
+    """The oracle's router, top-k, gather and Eq. 7 scatter on one sequence of the
+    workload, repeated until `budget_s` elapses. Returns (selected tokens/s, threads,
+    description)."""
+    import oracle as O
+    w1 = w.replace(B=1)
+    n = w.T // K
+    x = I.to_f64(I.residual_stream(w1), w.dtype).reshape(w.T, w.d)
+    w_r = I.to_f64(I.layer_weights(w1, 0)["w_r"], w.dtype)
+    af = I.to_f64(I.given_block_output(w1, n), w.dtype)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        s, r = O.router(x[None], w_r)
+        idx = O.topk(s, n)[0]
+        xs = x[idx]                                   # the position-ordered gather
+        O.gated_scatter(x, idx, af, None, r[0, idx], 1.0, O.GATE_XMOD)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            break
+    del xs
+    return reps * n / el, O.num_threads(), (
+        f"router + top-{n} + gather + Eq. 7 scatter on 1 of the {w.B} sequences "
+        f"(T={w.T}, d={w.d}, K={K}), {reps} repetition(s) in {el:.1f} s")
+
+
+def run_routing_reference(args):
+    """--impl reference on the routing microbench: the oracle, rank 0 only."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    w = I.WORKLOADS[args.workload]
+    K = args.K or ROUTING_HEADLINE_K
+    import oracle as O
+    n = w.T // K
+    w1 = w.replace(B=1)
+    x = I.to_f64(I.residual_stream(w1), w.dtype).reshape(w.T, w.d)
+    w_r = I.to_f64(I.layer_weights(w1, 0)["w_r"], w.dtype)
+    af = I.to_f64(I.given_block_output(w1, n), w.dtype)
+
+    def step():
+        s, r = O.router(x[None], w_r)
+        idx = O.topk(s, n)[0]
+        _ = x[idx]
+        O.gated_scatter(x, idx, af, None, r[0, idx], 1.0, O.GATE_XMOD)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = args.steps * n / el
+    sample = (f"each step: router + top-{n} + gather + Eq. 7 scatter on 1 of the workload's "
+              f"{w.B} sequences (T={w.T}, d={w.d})")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": routing_config(w, K),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def run_routing(args):
+    """The routing-only microbench: per step, xmod_router_topk (router GEMV + top-(T/K)),
+    xmod_gather and xmod_gated_scatter (Eq. 7, varsigma 1) of a given block output a+f,
+    on the B x T x d stream, which the scatter updates in place. K = 8 is the headline;
+    K = 2 and 16 are timed too and reported under "sweep"."""
+    import torch
+    from sparse_depth_token_gb300 import xmod as X
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    X.load()
+    w = I.WORKLOADS[args.workload]
+    wr = w.replace(seed=w.seed + 1000 * rank) if rank else w
+    Ks = [args.K] if args.K else list(ROUTING_KS)
+    head_K = args.K or ROUTING_HEADLINE_K
+
+    def bf16_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    x_host = I.residual_stream(wr)
+    x = bf16_dev(x_host)
+    w_r = bf16_dev(I.layer_weights(w, 0)["w_r"])
+    M_max = w.B * (w.T // min(Ks))
+    af_host = I.given_block_output(wr, M_max)
+    af_all = bf16_dev(af_host)
+    # the block's widths do not enter the routing kernels: one head of 8, d_ff 8
+    dm = X.dims(w.B, w.T, w.d, 1, 1, 8, 8, X.BF16, w.eps)
+    ws = torch.zeros(X.workspace_bytes(dm, min(Ks)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    peaks = measured_peaks()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(ms):
+        if dist is None:
+            return ms
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    results = {}
+    for K in Ks:
+        n = w.T // K
+        M = w.B * n
+        idx = torch.empty((w.B, n), dtype=torch.int32, device=dev)
+        r_sel = torch.empty((w.B, n), dtype=torch.float32, device=dev)
+        logits = torch.empty((w.B, w.T), dtype=torch.float32, device=dev)
+        xs = torch.empty((M, w.d), dtype=torch.bfloat16, device=dev)
+        af = af_all[:M]
+
+        def step():
+            X.router_topk(dm, K, x, w_r, None, logits, None, idx, r_sel, ws, stream)
+            X.gather(dm, K, x, idx, xs, stream)
+            X.gated_scatter(dm, K, x, idx, r_sel, af, None, 1.0, X.GATE_XMOD, stream)
+
+        X.reset_status(ws)
+        for _ in range(max(args.warmup, 3)):
+            step()
+        st = X.sync_status(ws)
+        if st != X.OK:
+            raise RuntimeError(f"device status after warm-up: {X.status_string(st)}")
+        clocks = ClockSampler(local if world > 1 else 0)
+        barrier()
+        torch.cuda.synchronize()
+        clocks.start()
+        time.sleep(0.3)
+        launches0 = X.launch_count()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        launches = (X.launch_count() - launches0) // args.steps
+        clock_info = clocks.stop()
+        barrier()
+        ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+
+        # per-kernel CUDA-event times on the launching stream
+        X.profile_read()
+        X.profile_enable(True)
+        prof_steps = max(1, min(args.steps, 5))
+        for _ in range(prof_steps):
+            step()
+        torch.cuda.synchronize()
+        X.profile_enable(False)
+        prof = X.profile_read()
+        work = routing_work(w, K)
+        kernels = {}
+        for kind, (cnt, kms) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+            pms = kms / prof_steps
+            e = {"launches_per_step": cnt // prof_steps, "ms_per_step": pms}
+            if kind in work and pms > 0:
+                e["gbs"] = work[kind] / (pms / 1e3) / 1e9
+                e["frac_hbm"] = e["gbs"] / peaks["hbm_gbs"]
+            kernels[kind] = e
+        top = max(prof.items(), key=lambda kv: kv[1][1])[0]
+        cnt, kms = prof[top]
+        ach = work[top] / (kms / prof_steps / 1e3) / 1e9
+        roofline = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                    "peak_source": f"{peaks['source']} HBM copy",
+                    "algorithmic_per_launch": work[top] / (cnt / prof_steps)}
+        total = sum(work.values())
+        results[K] = {"value": world * M / (ms / 1e3), "ms_per_step": ms,
+                      "pipeline_gbs": total / (ms / 1e3) / 1e9,
+                      "pipeline_frac_hbm": total / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                      "roofline": roofline, "kernels": kernels, "clocks": clock_info,
+                      "gpu_launches_per_step": int(launches)}
+        st = X.sync_status(ws)
+        if st != X.OK:
+            raise RuntimeError(f"device status after K={K}: {X.status_string(st)}")
+        del idx, r_sel, logits, xs
+
+    # ---- end to end through the C ABI with host buffers: x and a+f in, x out, each step
+    e2e = None
+    K = head_K
+    if not args.no_e2e:
+        n = w.T // K
+        M = w.B * n
+        xh = torch.from_numpy(np.ascontiguousarray(x_host).view(np.int16)).view(
+            torch.bfloat16).pin_memory()
+        afh = torch.from_numpy(np.ascontiguousarray(af_host[:M]).view(np.int16)).view(
+            torch.bfloat16).pin_memory()
+        out_h = torch.empty_like(xh).pin_memory()
+        idx = torch.empty((w.B, n), dtype=torch.int32, device=dev)
+        r_sel = torch.empty((w.B, n), dtype=torch.float32, device=dev)
+        logits = torch.empty((w.B, w.T), dtype=torch.float32, device=dev)
+        xs = torch.empty((M, w.d), dtype=torch.bfloat16, device=dev)
+        af = af_all[:M]
+
+        def e2e_step():
+            x.copy_(xh, non_blocking=True)
+            af.copy_(afh, non_blocking=True)
+            X.router_topk(dm, K, x, w_r, None, logits, None, idx, r_sel, ws, stream)
+            X.gather(dm, K, x, idx, xs, stream)
+            X.gated_scatter(dm, K, x, idx, r_sel, af, None, 1.0, X.GATE_XMOD, stream)
+            out_h.copy_(x, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e_steps = max(1, min(args.steps, 5))
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1) / e_steps)
+        e2e = {"value": world * M / (ems / 1e3), "unit": UNIT, "ms_per_step": ems,
+               "steps": e_steps,
+               "h2d_bytes_per_step": int(xh.numel() * 2 + afh.numel() * 2),
+               "d2h_bytes_per_step": int(out_h.numel() * 2)}
+        st = X.sync_status(ws)
+        if st != X.OK:
+            raise RuntimeError(f"device status after the e2e run: {X.status_string(st)}")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = oracle_routing_sample(w, K, budget_s=args.cpu_budget)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        h = results[K]
+        cfg = routing_config(w, K)
+        cfg["parallelism"] = f"replicas x{world} (sequences sharded, no collective)"
+        line = {"metric": METRIC, "value": h["value"], "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": h["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded)", "config": cfg,
+                "roofline": h["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": h["gpu_launches_per_step"] * args.steps,
+                "gpu_launches_per_step": h["gpu_launches_per_step"],
+                "clocks": h["clocks"],
+                "pipeline_gbs": h["pipeline_gbs"], "pipeline_frac_hbm": h["pipeline_frac_hbm"],
+                "kernels": h["kernels"],
+                "sweep": {str(k): {kk: v[kk] for kk in ("value", "ms_per_step", "pipeline_gbs",
+                                                        "pipeline_frac_hbm", "kernels")}
+                          for k, v in results.items() if k != K}}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -541,6 +835,9 @@ def main():
                     help="X-MoD stack, or one of the mechanism controls")
     ap.add_argument("--qwen3", action="store_true",
                     help="QK-norm and RoPE (base 1e6) in every attending layer")
+    ap.add_argument("--K", type=int, default=None,
+                    help="routing_bf16 only: one sparsity K (default: 8 as the headline, with "
+                         "2 and 16 under \"sweep\")")
     args = ap.parse_args()
     global VARIANT
     VARIANT = args.variant
@@ -549,7 +846,12 @@ def main():
         A = w.A if args.A is None else args.A
         n_layers = w.N0 + w.N1 * (int(round(A * w.K)) + 1)
         I.WORKLOADS[args.workload] = w.replace(B=args.B or w.B, A=A, n_layers=n_layers)
-    if args.impl == "reference":
+    if args.workload == "routing_bf16":   # the routing-only microbench: no block
+        if args.impl == "reference":
+            run_routing_reference(args)
+        else:
+            run_routing(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_xmod(args)

@@ -724,11 +724,61 @@ cudaError_t launch_stack_rows(const Ctx& c, const RowPtrs& rows, int count, int 
                     d, (uint4*)dst);
 }
 
+// Register-cached gather (rows of at most 32 * VPL 16-byte vectors): every load of a
+// row is issued before its first store, so a whole row is in flight per warp.
+template <typename T, int VPL>
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+gather_rows_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
+                   const int32_t* __restrict__ idx, T* __restrict__ xs) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int V = Vec16<T>::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
+  if (m >= M) return;
+  const T* src = x + stream_row(m, seqT, n, idx) * d;
+  T* dst = xs + m * d;
+  Vec16<T> v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = (i * 32 + lane) * V;
+    if (c < d) v[i] = ld_vec(src + c);
+  }
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int c = (i * 32 + lane) * V;
+    if (c < d) st_vec(dst + c, v[i]);
+  }
+}
+
 cudaError_t launch_gather(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
                           const void* x, const int32_t* idx, void* xs) {
   const int64_t M = (int64_t)B * n;
   if (M <= 0) return cudaSuccess;
   const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
+  const int vpl = pick_vpl((d / (dt == XMOD_BF16 ? 8 : 4) + 31) / 32);
+  if (vpl) {
+#define XMOD_GA_CASE(TT, N)                                                                  \
+  case N:                                                                                    \
+    return launch_pdl(gather_rows_kernel<TT, N>, dim3(blocks), dim3(ROW_WARPS * 32), 0,      \
+                      c.stream, M, T, n, d, (const TT*)x, idx, (TT*)xs);
+    if (dt == XMOD_BF16) {
+      switch (vpl) {
+        XMOD_GA_CASE(__nv_bfloat16, 1) XMOD_GA_CASE(__nv_bfloat16, 2)
+        XMOD_GA_CASE(__nv_bfloat16, 4) XMOD_GA_CASE(__nv_bfloat16, 6)
+        XMOD_GA_CASE(__nv_bfloat16, 8) XMOD_GA_CASE(__nv_bfloat16, 12)
+        XMOD_GA_CASE(__nv_bfloat16, 16)
+      }
+    } else {
+      switch (vpl) {
+        XMOD_GA_CASE(float, 1) XMOD_GA_CASE(float, 2) XMOD_GA_CASE(float, 4)
+        XMOD_GA_CASE(float, 6) XMOD_GA_CASE(float, 8) XMOD_GA_CASE(float, 12)
+        XMOD_GA_CASE(float, 16)
+      }
+    }
+#undef XMOD_GA_CASE
+    return cudaErrorInvalidValue;
+  }
   if (dt == XMOD_BF16)
     launch_pdl(gather_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
         M, T, n, d, (const __nv_bfloat16*)x, idx, (__nv_bfloat16*)xs);
@@ -1017,6 +1067,10 @@ cudaError_t launch_qk_transform(const Ctx& c, xmod_dtype dt, int64_t M, const in
 
 // ================================================================ gated scatter
 
+// One warp per selected row, the row taken in chunks of SCATTER_CHUNK 16-byte vectors
+// per lane: every load of a chunk (x, a and f) is issued before the chunk's first store.
+constexpr int SCATTER_CHUNK = 8;
+
 template <typename T>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 gated_scatter_kernel(int64_t M, int seqT, int n, int d, T* __restrict__ x,
@@ -1029,28 +1083,42 @@ gated_scatter_kernel(int64_t M, int seqT, int n, int d, T* __restrict__ x,
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
   if (m >= M) return;
   T* row = x + stream_row(m, seqT, n, idx) * d;
+  const T* arow = a + m * d;
+  const T* frow = f ? f + m * d : nullptr;
   const float r = (gate >= 0) ? r_sel[m] : 1.0f;
   const float g7 = varsigma * r;
-  for (int c = lane * V; c < d; c += 32 * V) {
-    Vec16<T> xv = ld_vec(row + c);
-    Vec16<T> av = ld_vec_stream(a + m * d + c);
-    Vec16<T> o;
-    if (f) {
-      Vec16<T> fv = ld_vec_stream(f + m * d + c);
+  for (int c0 = lane * V; c0 < d; c0 += SCATTER_CHUNK * 32 * V) {
+    Vec16<T> xv[SCATTER_CHUNK], av[SCATTER_CHUNK], fv[SCATTER_CHUNK];
 #pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const float xa = xv.get(e), aa = av.get(e), ff = fv.get(e);
-        float y;
-        if (gate == XMOD_GATE_XMOD) y = xa + g7 * (aa + ff);       // Eq. 7
-        else if (gate == XMOD_GATE_MOD) y = xa + aa + r * ff;      // Eq. 6
-        else y = xa + aa + ff;                                      // dense layer
-        o.set(e, y);
+    for (int i = 0; i < SCATTER_CHUNK; ++i) {
+      const int c = c0 + i * 32 * V;
+      if (c < d) {
+        xv[i] = ld_vec(row + c);
+        av[i] = ld_vec_stream(arow + c);
+        if (frow) fv[i] = ld_vec_stream(frow + c);
       }
-    } else {  // a holds a + f (Eq. 7 only)
-#pragma unroll
-      for (int e = 0; e < V; ++e) o.set(e, xv.get(e) + g7 * av.get(e));
     }
-    st_vec(row + c, o);
+#pragma unroll
+    for (int i = 0; i < SCATTER_CHUNK; ++i) {
+      const int c = c0 + i * 32 * V;
+      if (c >= d) break;
+      Vec16<T> o;
+      if (frow) {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          const float xa = xv[i].get(e), aa = av[i].get(e), ff = fv[i].get(e);
+          float y;
+          if (gate == XMOD_GATE_XMOD) y = xa + g7 * (aa + ff);       // Eq. 7
+          else if (gate == XMOD_GATE_MOD) y = xa + aa + r * ff;      // Eq. 6
+          else y = xa + aa + ff;                                      // dense layer
+          o.set(e, y);
+        }
+      } else {  // a holds a + f (Eq. 7 only)
+#pragma unroll
+        for (int e = 0; e < V; ++e) o.set(e, xv[i].get(e) + g7 * av[i].get(e));
+      }
+      st_vec(row + c, o);
+    }
   }
 }
 
