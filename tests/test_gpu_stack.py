@@ -78,7 +78,8 @@ def _teacher_forced(X, w, layers, kinds, bias, x, abi, check_layers, row_mask=No
             s, _ = O.router(x_in, I.to_f64(layers[l]["w_r"], w.dtype), bias)
             gidx = idx.cpu().numpy()
             differ = U.check_selection(gidx, s, n)
-            if l == kinds.index(S.SPARSE):
+            if l == kinds.index(S.SPARSE) == 0:
+                # the margin was enforced on the stack's input, which is this layer's input
                 assert differ == 0, "first sparse layer has margin-fixed inputs: must be bit-exact"
             force = gidx
         ref = O.layer_fwd(od, kind, w.K, w.gate, L, x_in, bias=bias, idx_force=force,
