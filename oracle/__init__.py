@@ -36,6 +36,11 @@ class LayerW(ctypes.Structure):
         ("varsigma", ctypes.c_double), ("gq", _DP), ("gk", _DP), ("rope_theta", ctypes.c_double)]
 
 
+class LayerGrad(ctypes.Structure):
+    _fields_ = [(n, _DP) for n in ("w_r", "g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")] + [
+        ("varsigma", ctypes.c_double)]
+
+
 _lib = None
 
 
@@ -74,6 +79,9 @@ def lib():
                                        ctypes.c_int, _IP, _DP, ctypes.c_int, _IP]
         L.oracle_layer_threshold.argtypes = [ctypes.POINTER(Dims), ctypes.c_int,
                                              ctypes.POINTER(LayerW), _DP, _DP, _DP, _DP, _IP]
+        L.oracle_layer_bwd.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.POINTER(LayerW), _DP, _DP, _IP, _DP,
+                                       ctypes.c_double, _DP, ctypes.POINTER(LayerGrad), _IP, _DP]
         _lib = L
     return _lib
 
@@ -247,6 +255,33 @@ def layer_fwd(dm: Dims, kind, K, gate, layer: Layer, x, bias=None, idx_force=Non
     _check(lib().oracle_layer_fwd(ctypes.byref(dm), kind, K, gate, ctypes.byref(layer.struct),
                                   xp, bp, y.ctypes.data_as(_DP), *args, fp, mp))
     return out
+
+
+def layer_bwd(dm: Dims, kind, K, gate, layer: Layer, x, dy, bias=None, idx_force=None,
+              route_coef=0.0):
+    """Backward of one layer (DENSE or SPARSE) for the objective sum(dy * y) + route_coef *
+    L_route (Eq. 9 on the layer's top-(T/K) decisions), the selection held fixed.
+    Returns dict(dx, grads {name: array shaped as the weight}, varsigma, route_loss, idx)."""
+    x, xp = _d(x)
+    dy, gp = _d(dy)
+    B, T, d = dm.B, dm.T, dm.d
+    assert x.shape == (B, T, d) and dy.shape == (B, T, d)
+    bias_a, bp = _d(bias)
+    f_a, fp = _i(idx_force)
+    qw, kw = dm.hq * dm.hd, dm.hkv * dm.hd
+    shapes = {"w_r": (d,), "g1": (d,), "wq": (qw, d), "wk": (kw, d), "wv": (kw, d),
+              "wo": (d, qw), "g2": (d,), "wg": (dm.F, d), "wu": (dm.F, d), "wd": (d, dm.F)}
+    grads = {k: np.zeros(v) for k, v in shapes.items()}
+    gs = LayerGrad(*[grads[k].ctypes.data_as(_DP) for k in shapes], 0.0)
+    dx = np.empty_like(x)
+    n = T // K if kind == SPARSE else 1
+    idx = np.zeros((B, n), np.int32)
+    loss = ctypes.c_double(0.0)
+    _check(lib().oracle_layer_bwd(ctypes.byref(dm), kind, K, gate, ctypes.byref(layer.struct),
+                                  xp, bp, fp, gp, float(route_coef), dx.ctypes.data_as(_DP),
+                                  ctypes.byref(gs), idx.ctypes.data_as(_IP), ctypes.byref(loss)))
+    return {"dx": dx, "grads": grads, "varsigma": gs.varsigma, "route_loss": loss.value,
+            "idx": idx if kind == SPARSE else None}
 
 
 TOPK, THRESHOLD = 0, 1

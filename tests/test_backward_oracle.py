@@ -1,0 +1,125 @@
+"""Pins of the oracle's layer backward (CPU only).
+
+The backward is held against finite differences of the forward oracle (itself pinned
+in test_oracle_pins.py): for J = sum(dy * y) + route_coef * L_route (Eq. 9 of the X-MoD
+notes, section "top-k in training, causal threshold at evaluation"), the central
+difference of J along a random direction of x, of every weight and of varsigma must
+equal the inner product of that direction with the returned gradient. The selection is
+held fixed on both sides (forced indices), as the backward holds it. Plus closed forms:
+the skip path of unselected rows, the Eq. 9 value at p = 1/2, an FFN with W_down = 0.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+B, T, d, HQ, HKV, HD, F, K = 2, 12, 16, 4, 2, 4, 24, 3
+NAMES = ("w_r", "g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")
+
+
+def _weights(g, scale=0.3):
+    return {"w_r": g.standard_normal(d) / 4, "g1": 1 + 0.1 * g.standard_normal(d),
+            "wq": g.standard_normal((HQ * HD, d)) * scale,
+            "wk": g.standard_normal((HKV * HD, d)) * scale,
+            "wv": g.standard_normal((HKV * HD, d)) * scale,
+            "wo": g.standard_normal((d, HQ * HD)) * scale, "g2": 1 + 0.1 * g.standard_normal(d),
+            "wg": g.standard_normal((F, d)) * scale, "wu": g.standard_normal((F, d)) * scale,
+            "wd": g.standard_normal((d, F)) * scale}
+
+
+def _objective(dm, kind, gate, W, vs, x, dy, bias, idx, coef):
+    out = O.layer_fwd(dm, kind, K, gate, O.Layer(W, vs), x, bias=bias, idx_force=idx)
+    val = float((dy * out["y"]).sum())
+    if kind == O.SPARSE and coef:
+        s = out["s"]
+        p = 1.0 / (1.0 + np.exp(-s))
+        q = np.zeros_like(s)
+        np.put_along_axis(q, idx, 1.0, 1)
+        val += coef * float(-(q * np.log(p) + (1 - q) * np.log(1 - p)).mean())
+    return val
+
+
+@pytest.mark.parametrize("kind,gate,coef", [(O.SPARSE, O.GATE_XMOD, 0.0),
+                                            (O.SPARSE, O.GATE_MOD, 0.0),
+                                            (O.SPARSE, O.GATE_XMOD, 0.7),
+                                            (O.SPARSE, O.GATE_MOD, 0.3),
+                                            (O.DENSE, O.GATE_XMOD, 0.0)])
+def test_layer_bwd_matches_finite_differences(kind, gate, coef):
+    g = np.random.default_rng(10 + 3 * kind + gate)
+    dm = O.dims(B, T, d, HQ, HKV, HD, F)
+    W = _weights(g)
+    vs = 0.8
+    x = g.standard_normal((B, T, d))
+    dy = g.standard_normal((B, T, d))
+    bias = 0.1 * g.standard_normal((B, T))
+    r = O.layer_bwd(dm, kind, K, gate, O.Layer(W, vs), x, dy, bias=bias, route_coef=coef)
+    idx = r["idx"]
+    eps = 1e-6
+
+    def fd(x_=x, W_=W, vs_=vs):
+        return _objective(dm, kind, gate, W_, vs_, x_, dy, bias, idx, coef)
+
+    def check(num, ana, what):
+        assert abs(num - ana) <= 1e-6 * max(1.0, abs(num)), f"{what}: fd {num} vs grad {ana}"
+
+    v = g.standard_normal(x.shape)
+    check((fd(x_=x + eps * v) - fd(x_=x - eps * v)) / (2 * eps), float((r["dx"] * v).sum()), "x")
+    for name in NAMES:
+        v = g.standard_normal(W[name].shape)
+        Wp, Wm = dict(W), dict(W)
+        Wp[name] = W[name] + eps * v
+        Wm[name] = W[name] - eps * v
+        check((fd(W_=Wp) - fd(W_=Wm)) / (2 * eps), float((r["grads"][name] * v).sum()), name)
+    check((fd(vs_=vs + eps) - fd(vs_=vs - eps)) / (2 * eps), r["varsigma"], "varsigma")
+    if kind == O.DENSE or gate == O.GATE_MOD:
+        assert r["varsigma"] == 0.0
+    if kind == O.DENSE:
+        assert np.all(r["grads"]["w_r"] == 0.0)
+
+
+def test_unselected_rows_pass_the_gradient_through():
+    """With no Eq. 9 term, a token the layer skipped has y = x, so dx = dy exactly."""
+    g = np.random.default_rng(3)
+    dm = O.dims(B, T, d, HQ, HKV, HD, F)
+    x = g.standard_normal((B, T, d))
+    dy = g.standard_normal((B, T, d))
+    r = O.layer_bwd(dm, O.SPARSE, K, O.GATE_XMOD, O.Layer(_weights(g), 1.1), x, dy)
+    sel = np.zeros((B, T), bool)
+    np.put_along_axis(sel, r["idx"], True, 1)
+    np.testing.assert_array_equal(r["dx"][~sel], dy[~sel])
+    assert np.any(r["dx"][sel] != dy[sel])
+
+
+def test_route_loss_at_even_odds():
+    """w_r = 0 and no bias give p = 1/2 for every token: L_route = ln 2, and the Eq. 9 term
+    alone moves the logits by coef * (1/2 - q) / (B*T) each."""
+    g = np.random.default_rng(4)
+    dm = O.dims(B, T, d, HQ, HKV, HD, F)
+    W = _weights(g)
+    W["w_r"] = np.zeros(d)
+    x = g.standard_normal((B, T, d))
+    zero = np.zeros((B, T, d))
+    coef = 5.0
+    r = O.layer_bwd(dm, O.SPARSE, K, O.GATE_XMOD, O.Layer(W, 1.0), x, zero, route_coef=coef)
+    assert r["route_loss"] == pytest.approx(np.log(2.0), rel=1e-14)
+    q = np.zeros((B, T))
+    np.put_along_axis(q, r["idx"], 1.0, 1)
+    ds = coef * (0.5 - q) / (B * T)
+    np.testing.assert_allclose(r["grads"]["w_r"], np.einsum("bt,btc->c", ds, x), rtol=1e-12)
+    np.testing.assert_allclose(r["dx"], np.zeros_like(x), atol=0)   # w_r = 0: no path to x
+
+
+def test_zero_down_projection():
+    """W_down = 0 makes f = 0: no gradient reaches W_gate or W_up, while W_down's gradient
+    is df^T H with H = silu(G) U, which is not zero."""
+    g = np.random.default_rng(5)
+    dm = O.dims(B, T, d, HQ, HKV, HD, F)
+    W = _weights(g)
+    W["wd"] = np.zeros((d, F))
+    x = g.standard_normal((B, T, d))
+    dy = g.standard_normal((B, T, d))
+    r = O.layer_bwd(dm, O.SPARSE, K, O.GATE_MOD, O.Layer(W, 1.0), x, dy)
+    assert np.all(r["grads"]["wg"] == 0.0) and np.all(r["grads"]["wu"] == 0.0)
+    assert np.any(r["grads"]["wd"] != 0.0)
