@@ -259,6 +259,48 @@ XMOD_API int xmod_stack_fwd_sched(const xmod_dims* dims, int K, const int32_t* k
                                   void* x_inout, const float* bias, const xmod_stack_opts* opts,
                                   void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- backward of one layer
+ * The gradient of one DENSE or SPARSE layer (Eq. 7 or Eq. 6 gating) for training: for
+ * the layer y = layer(x) of xmod_layer_fwd and a caller-given upstream gradient dy,
+ * the call returns the gradients of the scalar
+ *     J = sum(dy * y) + route_coef * L_route
+ * with respect to x and to every weight of the layer. L_route is the binary
+ * cross-entropy of X-MoD notes Eq. 9 (section "top-k in training, causal threshold at
+ * evaluation"), which aligns the router with the deployable threshold rule:
+ *     L_route = -(1/N) sum_i [q_i log p_i + (1 - q_i) log(1 - p_i)],
+ * q_i = 1 for the layer's top-(T/K) tokens, p_i = sigmoid(s_i) on the same biased logit
+ * the selection ranks, N = B*T (every token of the layer's input). The pages sweep the
+ * coefficient over 1e-2 .. 1e-5 and keep 1e-4; route_coef = 0 leaves Eq. 9 out. The
+ * top-(T/K) selection is piecewise constant and is held fixed: the router learns
+ * through the gate r of the residual and through Eq. 9.
+ *
+ * The call recomputes the layer's forward from x (routing included) and then runs
+ * the backward; it does not modify x.
+ *   x, dy     [B, T, d]  the layer's input and the gradient at its output (dtype)
+ *   bias      [B, T] fp32 as for xmod_layer_fwd, or NULL
+ *   dx        [B, T, d]  out (dtype): dJ/dx; may not alias x or dy
+ *   grads     fp32 device arrays shaped as the weights (overwritten); w_router is
+ *             ignored for DENSE layers; varsigma (one float) receives dJ/dvarsigma (0
+ *             under Eq. 6 and for DENSE); route_loss (one float, NULL allowed)
+ *             receives L_route (SPARSE only)
+ *   ws        at least xmod_bwd_workspace_bytes(dims, K) bytes
+ * The QK-norm / rotary extras and the other layer kinds return XMOD_ERR_UNSUPPORTED.
+ * bf16 runs the projections and their gradients on the tensor cores (bf16 operands,
+ * fp32 accumulation, fp32 weight gradients); fp32 runs FFMA kernels throughout. */
+typedef struct {
+  float *w_router, *rms1, *wq, *wk, *wv, *wo, *rms2, *w_gate, *w_up, *w_down;
+  float* varsigma;
+  float* route_loss;
+} xmod_layer_grads;
+
+XMOD_API size_t xmod_bwd_workspace_bytes(const xmod_dims* dims, int K);
+
+XMOD_API int xmod_layer_bwd(const xmod_dims* dims, xmod_layer_kind kind, int K, xmod_gate gate,
+                            const xmod_layer_weights* w, const void* x, const float* bias,
+                            const void* dy, float route_coef, void* dx,
+                            const xmod_layer_grads* grads, void* ws, size_t ws_bytes,
+                            void* stream);
+
 /* ---------------------------------------------------------------- allocation-free routing
  * The paper has no counterpart to this entry point: it exists for callers that
  * cannot allocate device memory -- a plugin inside another runtime that is given

@@ -860,6 +860,36 @@ int xmod_gated_scatter(const xmod_dims* dm, int K, void* x_inout, const int32_t*
   return XMOD_OK;
 }
 
+size_t xmod_bwd_workspace_bytes(const xmod_dims* dm, int K) {
+  if (!dims_ok(dm) || K <= 0 || K > dm->T) return 0;
+  return bwd_workspace_bytes(dm);
+}
+
+int xmod_layer_bwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
+                   const xmod_layer_weights* w, const void* x, const float* bias, const void* dy,
+                   float route_coef, void* dx, const xmod_layer_grads* g, void* ws,
+                   size_t ws_bytes, void* stream) {
+  if (!dims_ok(dm) || K <= 0 || K > dm->T) return XMOD_ERR_INVALID_ARG;
+  if (kind != XMOD_LAYER_DENSE && kind != XMOD_LAYER_SPARSE) return XMOD_ERR_UNSUPPORTED;
+  if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
+  if (!weights_ok(w, kind) || !aligned16(x) || !aligned16(dy) || !aligned16(dx) ||
+      !aligned16_or_null(bias) || !g || !isfinite(route_coef))
+    return XMOD_ERR_INVALID_ARG;
+  if (dx == x || dx == dy) return XMOD_ERR_INVALID_ARG;
+  const float* gp[] = {g->rms1, g->wq, g->wk, g->wv, g->wo, g->rms2, g->w_gate, g->w_up,
+                       g->w_down};
+  for (const float* p : gp)
+    if (!aligned16(p)) return XMOD_ERR_INVALID_ARG;
+  if (!g->varsigma || (kind == XMOD_LAYER_SPARSE && !aligned16(g->w_router)) ||
+      !aligned16_or_null(g->w_router))
+    return XMOD_ERR_INVALID_ARG;
+  if (qk_extras(w) || !head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
+  if (kind == XMOD_LAYER_SPARSE && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
+  if (!aligned16(ws) || ws_bytes < bwd_workspace_bytes(dm)) return XMOD_ERR_WORKSPACE;
+  return run_layer_bwd((cudaStream_t)stream, dm, kind, K, gate, w, x, bias, dy, route_coef, dx,
+                       g, ws);
+}
+
 int xmod_layer_fwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
                    const xmod_layer_weights* w, void* x_inout, const float* bias,
                    int32_t* idx_out, float* r_sel_out, void* ws, size_t ws_bytes, void* stream) {

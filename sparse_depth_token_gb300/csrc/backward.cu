@@ -1,0 +1,986 @@
+// Backward of one sparse-depth layer: the gradient of sum(dy * y) + route_coef * L_route
+// with respect to the layer input and every weight, the top-(T/K) selection held fixed.
+//
+// Sources: "X-MoD: Practical Scaling Laws for Sparse-Depth Routing Beyond
+// Mixture-of-Depths" reading notes -- Eq. 8 (router logit, sigmoid gate), Eq. 6 and
+// Eq. 7 (gated residuals, the only place the gate r and varsigma enter), Eq. 9 (the
+// binary cross-entropy between the top-k decisions and the threshold predictor,
+// section "top-k in training, causal threshold at evaluation"); the block of the
+// "backbone configuration" (pre-norm RMSNorm, GQA attention, SwiGLU FFN).
+//
+// The layer's forward is recomputed from x with the forward kernels (router, top-k,
+// gather + RMSNorm1, projections, attention), keeping the intermediates the backward
+// reads; then every step is differentiated in reverse order. Weight gradients are
+// GEMMs over the token dimension: their operands are transposed into token-contiguous
+// buffers (padded with zero tokens to a multiple of 8) so that the same K-major GEMM
+// kernels (tcgen05 for bf16, FFMA for fp32) compute them. Column sums (RMSNorm gains,
+// router vector) are taken in a fixed order: partial sums per row chunk, then the
+// chunks in order, so every result is deterministic.
+
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace xmod {
+
+namespace {
+
+constexpr int BW_WARPS = 8;   // warps per CTA of the row kernels
+
+__device__ __forceinline__ int64_t bw_stream_row(int64_t m, int T, int n, const int32_t* idx) {
+  const int64_t b = m / n;
+  const int64_t t = idx ? (int64_t)idx[m] : (m - b * n);
+  return b * T + t;
+}
+
+__device__ __forceinline__ float softplus_f(float z) {
+  return fmaxf(z, 0.0f) + log1pf(expf(-fabsf(z)));
+}
+
+// ---------------------------------------------------------------- transpose
+// out[c, r] = in[r, c] for r < R, c < C; out[c, r] = 0 for R <= r < Rpad (zero tokens).
+template <typename T>
+__global__ void transpose_kernel(int R, int Rpad, int C, const T* __restrict__ in, int64_t ldi,
+                                 T* __restrict__ out, int64_t ldo) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ T tile[32][33];
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = r0 + ty + 8 * k, c = c0 + tx;
+    tile[ty + 8 * k][tx] = (r < R && c < C) ? in[(int64_t)r * ldi + c] : Elem<T>::from_f(0.0f);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int c = c0 + ty + 8 * k, r = r0 + tx;
+    if (c < C && r < Rpad) out[(int64_t)c * ldo + r] = tile[tx][ty + 8 * k];
+  }
+}
+
+// ---------------------------------------------------------------- gated residual backward
+// Selected row m (stream row of idx): Eq. 7 y = x + vs r (a + f): df = vs r dy (also the
+// gradient reaching a), dr = vs <dy, a + f>, dvs_m = r <dy, a + f>. Eq. 6 y = x + a + r f:
+// dae = dy (gradient reaching a), df = r dy, dr = <dy, f>.
+template <typename T>
+__global__ void __launch_bounds__(BW_WARPS * 32)
+scatter_bwd_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ dy,
+                   const int32_t* __restrict__ idx, const float* __restrict__ r_sel,
+                   const T* __restrict__ a, const T* __restrict__ f, float vs, int gate,
+                   T* __restrict__ df, T* __restrict__ dae, float* __restrict__ dr,
+                   float* __restrict__ dvs) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * BW_WARPS + warp;
+  if (m >= M) return;
+  const T* g = dy + bw_stream_row(m, seqT, n, idx) * d;
+  const float r = r_sel[m];
+  float dot = 0.0f;
+  for (int c = lane; c < d; c += 32) {
+    const float gv = Elem<T>::to_f(g[c]);
+    const float fv = Elem<T>::to_f(f[m * d + c]);
+    if (gate == XMOD_GATE_XMOD) {
+      dot += gv * (Elem<T>::to_f(a[m * d + c]) + fv);
+      df[m * d + c] = Elem<T>::from_f(vs * r * gv);
+    } else {
+      dot += gv * fv;
+      df[m * d + c] = Elem<T>::from_f(r * gv);
+      dae[m * d + c] = g[c];
+    }
+  }
+  dot = warp_sum(dot);
+  if (lane == 0) {
+    dr[m] = gate == XMOD_GATE_XMOD ? vs * dot : dot;
+    dvs[m] = gate == XMOD_GATE_XMOD ? r * dot : 0.0f;
+  }
+}
+
+// ---------------------------------------------------------------- router logit gradient
+// One CTA per sequence: ds[t] = coef_n * (sigmoid(s_t) - q_t) + (selected) dr * r (1 - r),
+// and loss_part[b] = sum_t of the Eq. 9 terms (-log p for q = 1, -log(1 - p) for q = 0).
+// Shared memory: T floats (the gate term of each selected token) and T flags.
+__global__ void __launch_bounds__(1024)
+route_bwd_kernel(int T, int n, const float* __restrict__ s, const int32_t* __restrict__ idx,
+                 const float* __restrict__ r_sel, const float* __restrict__ dr, float coef_n,
+                 float* __restrict__ ds, float* __restrict__ loss_part) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ float gsh[];
+  uint8_t* sel = reinterpret_cast<uint8_t*>(gsh + T);
+  __shared__ float red[32];
+  const int b = blockIdx.x;
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    gsh[t] = 0.0f;
+    sel[t] = 0;
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const int64_t m = (int64_t)b * n + j;
+    const int t = idx[m];
+    const float r = r_sel[m];
+    gsh[t] = dr[m] * r * (1.0f - r);
+    sel[t] = 1;
+  }
+  __syncthreads();
+  float loss = 0.0f;
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    const float z = s[(int64_t)b * T + t];
+    const float p = 1.0f / (1.0f + expf(-z));
+    const bool q = sel[t] != 0;
+    ds[(int64_t)b * T + t] = coef_n * (p - (q ? 1.0f : 0.0f)) + gsh[t];
+    loss += q ? softplus_f(-z) : softplus_f(z);
+  }
+  loss = warp_sum(loss);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = loss;
+  __syncthreads();
+  if (warp == 0) {
+    float v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.0f;
+    v = warp_sum(v);
+    if (lane == 0) loss_part[b] = v;
+  }
+}
+
+// dx = dy + ds[row] * w_r (every stream row).
+template <typename T>
+__global__ void __launch_bounds__(BW_WARPS * 32)
+dx_init_kernel(int64_t rows, int d, const T* __restrict__ dy, const float* __restrict__ ds,
+               const T* __restrict__ w_r, T* __restrict__ dx) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * BW_WARPS + warp;
+  if (row >= rows) return;
+  const float g = ds[row];
+  for (int c = lane; c < d; c += 32)
+    dx[row * d + c] = Elem<T>::from_f(Elem<T>::to_f(dy[row * d + c]) + g * Elem<T>::to_f(w_r[c]));
+}
+
+// ---------------------------------------------------------------- column reductions
+// part[chunk, c] = sum over the chunk's rows m of (A ? A[m, c] : 1) * Bv[row(m), c] *
+// (w ? w[m] : 1), rows in order; row(m) is the stream row of compact row m (idx NULL:
+// m). One thread per column; grid (column blocks, row chunks).
+template <typename TB>
+__global__ void __launch_bounds__(256)
+coldot_kernel(int64_t M, int d, const float* __restrict__ A, const TB* __restrict__ Bv,
+              const int32_t* __restrict__ idx, int seqT, int n, const float* __restrict__ w,
+              int64_t rows_per_chunk, float* __restrict__ part) {
+  pdl_trigger();
+  pdl_wait();
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= d) return;
+  const int64_t m0 = (int64_t)blockIdx.y * rows_per_chunk;
+  const int64_t m1 = min(M, m0 + rows_per_chunk);
+  float acc = 0.0f;
+  for (int64_t m = m0; m < m1; ++m) {
+    const int64_t row = idx ? bw_stream_row(m, seqT, n, idx) : m;
+    float v = Elem<TB>::to_f(Bv[row * d + c]);
+    if (A) v *= A[m * d + c];
+    if (w) v *= w[m];
+    acc += v;
+  }
+  part[(int64_t)blockIdx.y * d + c] = acc;
+}
+
+// out[c] = sum over chunks k (in order) of part[k, c].
+__global__ void colsum_kernel(int nchunks, int d, const float* __restrict__ part,
+                              float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= d) return;
+  float acc = 0.0f;
+  for (int k = 0; k < nchunks; ++k) acc += part[(int64_t)k * d + c];
+  out[c] = acc;
+}
+
+// out[0] = scale * sum of in[0 .. n): each thread sums a fixed strided subset in order,
+// then a fixed tree; one CTA of 1024 threads.
+__global__ void __launch_bounds__(1024)
+sum_kernel(int64_t n, const float* __restrict__ in, float scale, float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float sh[1024];
+  float acc = 0.0f;
+  for (int64_t i = threadIdx.x; i < n; i += 1024) acc += in[i];
+  sh[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 512; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) sh[threadIdx.x] += sh[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) out[0] = sh[0] * scale;
+}
+
+// ---------------------------------------------------------------- SwiGLU
+// gu [M, 2F]: the gate pre-activation G in columns [0, F), the up projection U in [F, 2F).
+template <typename T>
+__global__ void swiglu_fwd_kernel(int64_t M, int F, const T* __restrict__ gu, T* __restrict__ H) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t total = M * F;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / F;
+    const int e = (int)(i - m * F);
+    const float g = Elem<T>::to_f(gu[m * 2 * F + e]);
+    const float u = Elem<T>::to_f(gu[m * 2 * F + F + e]);
+    H[i] = Elem<T>::from_f(g / (1.0f + expf(-g)) * u);
+  }
+}
+
+// dG = dH U silu'(G), dU = dH silu(G); silu'(z) = sigmoid(z) (1 + z (1 - sigmoid(z))).
+template <typename T>
+__global__ void swiglu_bwd_kernel(int64_t M, int F, const T* __restrict__ gu,
+                                  const float* __restrict__ dH, T* __restrict__ dgu) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t total = M * F;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / F;
+    const int e = (int)(i - m * F);
+    const float g = Elem<T>::to_f(gu[m * 2 * F + e]);
+    const float u = Elem<T>::to_f(gu[m * 2 * F + F + e]);
+    const float sg = 1.0f / (1.0f + expf(-g));
+    const float dh = dH[i];
+    dgu[m * 2 * F + e] = Elem<T>::from_f(dh * u * sg * (1.0f + g * (1.0f - sg)));
+    dgu[m * 2 * F + F + e] = Elem<T>::from_f(dh * g * sg);
+  }
+}
+
+// ---------------------------------------------------------------- RMSNorm backward
+// Row m of z = x rho g (rho = (mean x^2 + eps)^-1/2), x = xin[row(m)] (TIN; row(m) the
+// stream row through idx, or m): grad = rho (dz g - xhat mean(dz g xhat)).
+// RMSNorm2 use (dh_out): dh_out[m] = grad; da_out[m] = grad + dae[m].
+// RMSNorm1 use (dx_io): dx_io[row(m)] += dadd[m] + grad.
+// rstd_out[m] = rho.
+template <typename TIN, typename T>
+__global__ void __launch_bounds__(BW_WARPS * 32)
+rms_bwd_kernel(int64_t M, int d, const float* __restrict__ dz, const T* __restrict__ g,
+               const TIN* __restrict__ xin, const int32_t* __restrict__ idx, int seqT, int n,
+               float eps, const T* __restrict__ dae, float* __restrict__ dh_out,
+               T* __restrict__ da_out, const float* __restrict__ dadd, T* __restrict__ dx_io,
+               float* __restrict__ rstd_out) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * BW_WARPS + warp;
+  if (m >= M) return;
+  const int64_t row = idx ? bw_stream_row(m, seqT, n, idx) : m;
+  const TIN* xr = xin + row * d;
+  const float* dzr = dz + m * d;
+  float ss = 0.0f;
+  for (int c = lane; c < d; c += 32) {
+    const float v = Elem<TIN>::to_f(xr[c]);
+    ss += v * v;
+  }
+  const float rho = rsqrtf(warp_sum(ss) / (float)d + eps);
+  float dot = 0.0f;
+  for (int c = lane; c < d; c += 32)
+    dot += dzr[c] * Elem<T>::to_f(g[c]) * Elem<TIN>::to_f(xr[c]) * rho;
+  const float mean = warp_sum(dot) / (float)d;
+  for (int c = lane; c < d; c += 32) {
+    const float xh = Elem<TIN>::to_f(xr[c]) * rho;
+    const float gr = rho * (dzr[c] * Elem<T>::to_f(g[c]) - xh * mean);
+    if (dh_out) {
+      dh_out[m * d + c] = gr;
+      da_out[m * d + c] = Elem<T>::from_f(gr + Elem<T>::to_f(dae[m * d + c]));
+    } else {
+      T* p = dx_io + row * d + c;
+      *p = Elem<T>::from_f(Elem<T>::to_f(*p) + (dadd[m * d + c] + gr));
+    }
+  }
+  if (lane == 0) rstd_out[m] = rho;
+}
+
+
+// ---------------------------------------------------------------- attention backward
+// Causal GQA attention on each sequence's n compact rows (query head h reads KV head
+// h / (hq / hkv)); FFMA tiles of 32 queries x 32 keys in shared memory (fp32).
+// bwd_q: per (32-query tile, head, sequence): the row statistics lse = m + log l, D =
+//        <dO, O>, then dQ = scale * sum_j P (dP - D) K_j with P = exp(scale q.k - lse),
+//        dP = dO . v_j.
+// bwd_kv: per (32-key tile, KV head, sequence), over the group's query heads and the
+//        query tiles at or after the key tile: dV = sum_i P dO_i, dK = scale * sum_i
+//        P (dP - D) q_i. Every key row is owned by one CTA: no atomics.
+struct AttnBwd {
+  int n, hq, hkv;
+  const void* qkv;   // q of head h at column h*HD, k of KV head g at column qw + g*HD
+  int ldq;
+  const void* v;     // vt_mode 0: the qkv buffer (v at column qw + kw + g*HD, stride ldq);
+  int vt_mode;       // 1: v transposed, [B, hkv, HD, vt_ld] (keys contiguous)
+  int vt_ld;
+  const void* o;     // [B*n, hq*HD]
+  const float* dO;   // [B*n, hq*HD]
+  float* lse;        // [B*n, hq]
+  float* Dd;         // [B*n, hq]
+  void* dqkv;        // dq, dk, dv at the q, k, v columns of [B*n, ldg]
+  int ldg;
+  float scale;
+};
+
+constexpr int AB_T = 32;   // queries and keys per tile
+
+template <typename T, int HD>
+__device__ __forceinline__ float ab_v(const AttnBwd& p, int b, int g, int j, int c) {
+  const int qw = p.hq * HD, kw = p.hkv * HD;
+  if (p.vt_mode)
+    return Elem<T>::to_f(((const T*)p.v)[(((int64_t)b * p.hkv + g) * HD + c) * p.vt_ld + j]);
+  return Elem<T>::to_f(((const T*)p.qkv)[((int64_t)b * p.n + j) * p.ldq + qw + kw + g * HD + c]);
+}
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(256)
+attn_bwd_q_kernel(const AttnBwd p) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int P = HD + 1, KC = HD / 32;
+  extern __shared__ float sm[];
+  float* Qs = sm;
+  float* dOs = Qs + AB_T * P;
+  float* Ks = dOs + AB_T * P;
+  float* Vs = Ks + AB_T * P;
+  float* dSs = Vs + AB_T * P;   // [AB_T][AB_T + 1]
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / (p.hq / p.hkv);
+  const int qw = p.hq * HD;
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+  const int q0 = qt * AB_T;
+  const T* qkv = (const T*)p.qkv;
+  for (int e = tid; e < AB_T * HD; e += 256) {
+    const int i = e / HD, c = e - i * HD, qi = q0 + i;
+    const int64_t row = (int64_t)b * p.n + qi;
+    Qs[i * P + c] = qi < p.n ? Elem<T>::to_f(qkv[row * p.ldq + h * HD + c]) : 0.0f;
+    dOs[i * P + c] = qi < p.n ? p.dO[row * qw + h * HD + c] : 0.0f;
+  }
+  __syncthreads();
+  float Dr[4], mr[4], lr[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = ty + 8 * r, qi = q0 + i;
+    float acc = 0.0f;
+    if (qi < p.n)
+      for (int c = tx; c < HD; c += 32)
+        acc += dOs[i * P + c] *
+               Elem<T>::to_f(((const T*)p.o)[((int64_t)b * p.n + qi) * qw + h * HD + c]);
+    Dr[r] = warp_sum(acc);
+    mr[r] = -INFINITY;
+    lr[r] = 0.0f;
+  }
+  // pass 1: row max and sum over the keys at or before each query
+  for (int kt = 0; kt <= qt; ++kt) {
+    const int k0 = kt * AB_T;
+    for (int e = tid; e < AB_T * HD; e += 256) {
+      const int j = e / HD, c = e - j * HD, kj = k0 + j;
+      Ks[j * P + c] = kj < p.n
+          ? Elem<T>::to_f(qkv[((int64_t)b * p.n + kj) * p.ldq + qw + g * HD + c]) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = ty + 8 * r, qi = q0 + i, kj = k0 + tx;
+      float s = 0.0f;
+#pragma unroll 8
+      for (int c = 0; c < HD; ++c) s += Qs[i * P + c] * Ks[tx * P + c];
+      s *= p.scale;
+      const bool ok = qi < p.n && kj < p.n && kj <= qi;
+      const float mx = warp_max(ok ? s : -INFINITY);
+      if (mx > -INFINITY) {
+        const float mn = fmaxf(mr[r], mx);
+        const float add = warp_sum(ok ? expf(s - mn) : 0.0f);
+        lr[r] = lr[r] * expf(mr[r] - mn) + add;
+        mr[r] = mn;
+      }
+    }
+    __syncthreads();
+  }
+  float lse[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = ty + 8 * r, qi = q0 + i;
+    lse[r] = mr[r] + logf(lr[r]);
+    if (tx == 0 && qi < p.n) {
+      p.lse[((int64_t)b * p.n + qi) * p.hq + h] = lse[r];
+      p.Dd[((int64_t)b * p.n + qi) * p.hq + h] = Dr[r];
+    }
+  }
+  // pass 2: dQ
+  float dq[4][KC];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int k = 0; k < KC; ++k) dq[r][k] = 0.0f;
+  for (int kt = 0; kt <= qt; ++kt) {
+    const int k0 = kt * AB_T;
+    for (int e = tid; e < AB_T * HD; e += 256) {
+      const int j = e / HD, c = e - j * HD, kj = k0 + j;
+      const bool ok = kj < p.n;
+      Ks[j * P + c] = ok
+          ? Elem<T>::to_f(qkv[((int64_t)b * p.n + kj) * p.ldq + qw + g * HD + c]) : 0.0f;
+      Vs[j * P + c] = ok ? ab_v<T, HD>(p, b, g, kj, c) : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = ty + 8 * r, qi = q0 + i, kj = k0 + tx;
+      float s = 0.0f, dp = 0.0f;
+#pragma unroll 8
+      for (int c = 0; c < HD; ++c) {
+        s += Qs[i * P + c] * Ks[tx * P + c];
+        dp += dOs[i * P + c] * Vs[tx * P + c];
+      }
+      const bool ok = qi < p.n && kj < p.n && kj <= qi;
+      const float pr = ok ? expf(s * p.scale - lse[r]) : 0.0f;
+      dSs[i * (AB_T + 1) + tx] = pr * (dp - Dr[r]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = ty + 8 * r;
+#pragma unroll
+      for (int k = 0; k < KC; ++k) {
+        const int c = tx + 32 * k;
+        float acc = 0.0f;
+#pragma unroll 8
+        for (int j = 0; j < AB_T; ++j) acc += dSs[i * (AB_T + 1) + j] * Ks[j * P + c];
+        dq[r][k] += acc;
+      }
+    }
+    __syncthreads();
+  }
+  T* out = (T*)p.dqkv;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int qi = q0 + ty + 8 * r;
+    if (qi >= p.n) continue;
+#pragma unroll
+    for (int k = 0; k < KC; ++k)
+      out[((int64_t)b * p.n + qi) * p.ldg + h * HD + tx + 32 * k] =
+          Elem<T>::from_f(dq[r][k] * p.scale);
+  }
+}
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(256)
+attn_bwd_kv_kernel(const AttnBwd p) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int P = HD + 1, KC = HD / 32;
+  extern __shared__ float sm[];
+  float* Ks = sm;
+  float* Vs = Ks + AB_T * P;
+  float* Qs = Vs + AB_T * P;
+  float* dOs = Qs + AB_T * P;
+  float* Ps = dOs + AB_T * P;          // [key][query], AB_T + 1 wide
+  float* dSs = Ps + AB_T * (AB_T + 1);
+  float* lse_s = dSs + AB_T * (AB_T + 1);
+  float* D_s = lse_s + AB_T;
+  const int kt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int G = p.hq / p.hkv;
+  const int qw = p.hq * HD, kw = p.hkv * HD;
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+  const int k0 = kt * AB_T;
+  const T* qkv = (const T*)p.qkv;
+  for (int e = tid; e < AB_T * HD; e += 256) {
+    const int j = e / HD, c = e - j * HD, kj = k0 + j;
+    const bool ok = kj < p.n;
+    Ks[j * P + c] = ok
+        ? Elem<T>::to_f(qkv[((int64_t)b * p.n + kj) * p.ldq + qw + g * HD + c]) : 0.0f;
+    Vs[j * P + c] = ok ? ab_v<T, HD>(p, b, g, kj, c) : 0.0f;
+  }
+  float dk[4][KC], dv[4][KC];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int k = 0; k < KC; ++k) dk[r][k] = dv[r][k] = 0.0f;
+  for (int hh = 0; hh < G; ++hh) {
+    const int h = g * G + hh;
+    for (int q0 = k0; q0 < p.n; q0 += AB_T) {
+      __syncthreads();   // the previous tile's readers are done
+      for (int e = tid; e < AB_T * HD; e += 256) {
+        const int i = e / HD, c = e - i * HD, qi = q0 + i;
+        const int64_t row = (int64_t)b * p.n + qi;
+        Qs[i * P + c] = qi < p.n ? Elem<T>::to_f(qkv[row * p.ldq + h * HD + c]) : 0.0f;
+        dOs[i * P + c] = qi < p.n ? p.dO[row * qw + h * HD + c] : 0.0f;
+      }
+      if (tid < AB_T) {
+        const int qi = q0 + tid;
+        lse_s[tid] = qi < p.n ? p.lse[((int64_t)b * p.n + qi) * p.hq + h] : 0.0f;
+        D_s[tid] = qi < p.n ? p.Dd[((int64_t)b * p.n + qi) * p.hq + h] : 0.0f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int j = ty + 8 * r, kj = k0 + j, qi = q0 + tx;
+        float s = 0.0f, dp = 0.0f;
+#pragma unroll 8
+        for (int c = 0; c < HD; ++c) {
+          s += Ks[j * P + c] * Qs[tx * P + c];
+          dp += Vs[j * P + c] * dOs[tx * P + c];
+        }
+        const bool ok = qi < p.n && kj < p.n && kj <= qi;
+        const float pr = ok ? expf(s * p.scale - lse_s[tx]) : 0.0f;
+        Ps[j * (AB_T + 1) + tx] = pr;
+        dSs[j * (AB_T + 1) + tx] = pr * (dp - D_s[tx]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int j = ty + 8 * r;
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+          const int c = tx + 32 * k;
+          float av = 0.0f, ak = 0.0f;
+#pragma unroll 8
+          for (int i = 0; i < AB_T; ++i) {
+            av += Ps[j * (AB_T + 1) + i] * dOs[i * P + c];
+            ak += dSs[j * (AB_T + 1) + i] * Qs[i * P + c];
+          }
+          dv[r][k] += av;
+          dk[r][k] += ak;
+        }
+      }
+    }
+  }
+  T* out = (T*)p.dqkv;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int kj = k0 + ty + 8 * r;
+    if (kj >= p.n) continue;
+    const int64_t row = ((int64_t)b * p.n + kj) * p.ldg;
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+      const int c = tx + 32 * k;
+      out[row + qw + g * HD + c] = Elem<T>::from_f(dk[r][k] * p.scale);
+      out[row + qw + kw + g * HD + c] = Elem<T>::from_f(dv[r][k]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+constexpr size_t kBwAlign = 256;
+inline size_t bw_align(size_t v) { return (v + kBwAlign - 1) / kBwAlign * kBwAlign; }
+inline int64_t round8(int64_t v) { return (v + 7) / 8 * 8; }
+
+// Workspace carve-up of the backward; M = B*T rows cover a dense layer.
+struct BwLayout {
+  size_t status, s, r, idx, r_sel, dr, dvs, ds, lossp, u, qkv, vt, o, a, h, v2, gu, H, f, df,
+      dae, dH, dGU, dv2, dh, da, dO, lse, Dd, dqkv, du, rstd1, rstd2, tA, tB, tW, part, total;
+};
+
+constexpr int kMaxChunks = 512;   // row chunks of the column reductions
+
+BwLayout bw_layout(const xmod_dims* dm) {
+  BwLayout L{};
+  const size_t es = dm->dtype == XMOD_BF16 ? 2 : 4;
+  const size_t BT = (size_t)dm->B * dm->T, M = BT, Mp = (size_t)round8((int64_t)M);
+  const size_t d = dm->d, F = dm->d_ff, hq = dm->n_heads, hd = dm->head_dim;
+  const size_t qw = hq * hd, kw = (size_t)dm->n_kv_heads * hd, qkv_w = qw + 2 * kw;
+  const size_t vtl = (size_t)round8(dm->T);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { const size_t o = off; off = bw_align(off + bytes); return o; };
+  L.status = take(kBwAlign);
+  L.s = take(4 * BT);
+  L.r = take(4 * BT);
+  L.idx = take(4 * BT);
+  L.r_sel = take(4 * BT);
+  L.dr = take(4 * BT);
+  L.dvs = take(4 * BT);
+  L.ds = take(4 * BT);
+  L.lossp = take(4 * (size_t)dm->B);
+  L.u = take(es * M * d);
+  L.qkv = take(es * M * qkv_w);
+  L.vt = take(es * (size_t)dm->B * dm->n_kv_heads * hd * vtl);
+  L.o = take(es * M * qw);
+  L.a = take(es * M * d);
+  L.h = take(4 * M * d);
+  L.v2 = take(es * M * d);
+  L.gu = take(es * M * 2 * F);
+  L.H = take(es * M * F);
+  L.f = take(es * M * d);
+  L.df = take(es * M * d);
+  L.dae = take(es * M * d);
+  L.dH = take(4 * M * F);
+  L.dGU = take(es * M * 2 * F);
+  L.dv2 = take(4 * M * d);
+  L.dh = take(4 * M * d);
+  L.da = take(es * M * d);
+  L.dO = take(4 * M * qw);
+  L.lse = take(4 * M * hq);
+  L.Dd = take(4 * M * hq);
+  L.dqkv = take(es * M * qkv_w);
+  L.du = take(4 * M * d);
+  L.rstd1 = take(4 * M);
+  L.rstd2 = take(4 * M);
+  L.tA = take(es * Mp * std::max(std::max(d, 2 * F), qkv_w));
+  L.tB = take(es * Mp * std::max(std::max(d, F), qw));
+  L.tW = take(es * d * std::max(2 * F, qkv_w));
+  L.part = take(4 * (size_t)kMaxChunks * std::max(d, (size_t)1));
+  L.total = off;
+  return L;
+}
+
+inline char* bat(void* ws, size_t off) { return (char*)ws + off; }
+
+#define BW_RUN(kind, expr)                        \
+  do {                                            \
+    cudaError_t _e;                               \
+    {                                             \
+      ProfScope _p(kind, c.stream);               \
+      _e = (expr);                                \
+    }                                             \
+    count_launch();                               \
+    if (_e != cudaSuccess) return XMOD_ERR_CUDA;  \
+  } while (0)
+
+template <typename T>
+cudaError_t transpose_t(const Ctx& c, int R, int Rpad, int C, const void* in, int64_t ldi,
+                        void* out, int64_t ldo) {
+  if (R <= 0 || C <= 0) return cudaSuccess;
+  const dim3 grid((C + 31) / 32, (Rpad + 31) / 32);
+  return launch_pdl(transpose_kernel<T>, grid, dim3(32, 8), 0, c.stream, R, Rpad, C,
+                    (const T*)in, ldi, (T*)out, ldo);
+}
+
+cudaError_t transpose(const Ctx& c, xmod_dtype dt, int R, int Rpad, int C, const void* in,
+                      int64_t ldi, void* out, int64_t ldo) {
+  return dt == XMOD_BF16
+             ? transpose_t<__nv_bfloat16>(c, R, Rpad, C, in, ldi, out, ldo)
+             : transpose_t<float>(c, R, Rpad, C, in, ldi, out, ldo);
+}
+
+// C[M, N] = A[M, K] B[N, K]^T, both K-contiguous, stored plain (fp32 if f32out, else
+// the layer's type): tcgen05 for bf16 when the shape allows, FFMA otherwise.
+cudaError_t bw_gemm(const Ctx& c, xmod_dtype dt, int M, int N, int K, const void* A, int lda,
+                    const void* Bm, int ldb, void* out, int ldo, bool f32out) {
+  Epilogue e;
+  e.kind = EPI_STORE;
+  e.out = out;
+  e.ldo = ldo;
+  e.out_f32 = f32out;
+  if (dt == XMOD_BF16) {
+    GemmTcProblem p;
+    p.M = M; p.N = N; p.K = K; p.A = A; p.lda = lda; p.B[0] = Bm; p.ldb = ldb;
+    if (gemm_tc_supported(p, e)) return launch_gemm_tc(c, p, e);
+  }
+  return launch_gemm_simt(c, dt, M, N, K, A, lda, Bm, ldb, nullptr, e);
+}
+
+// Column sums out[c] = sum_m (A ? A[m, c] : 1) * Bv[row(m), c] * (w ? w[m] : 1).
+template <typename TB>
+int bw_coldot(const Ctx& c, int64_t M, int d, const float* A, const TB* Bv, const int32_t* idx,
+              int seqT, int n, const float* w, float* part, float* out) {
+  int64_t chunks = std::min<int64_t>(kMaxChunks, std::max<int64_t>(1, (M + 63) / 64));
+  const int64_t rpc = (M + chunks - 1) / chunks;
+  chunks = (M + rpc - 1) / rpc;
+  const dim3 grid((d + 255) / 256, (unsigned)chunks);
+  BW_RUN("bwd_reduce", launch_pdl(coldot_kernel<TB>, grid, dim3(256), 0, c.stream, M, d, A, Bv,
+                                  idx, seqT, n, w, rpc, part));
+  BW_RUN("bwd_reduce", launch_pdl(colsum_kernel, dim3((d + 255) / 256), dim3(256), 0, c.stream,
+                                  (int)chunks, d, (const float*)part, out));
+  return XMOD_OK;
+}
+
+template <typename T, int HD>
+cudaError_t launch_attn_bwd_t(const Ctx& c, int B, const AttnBwd& p) {
+  constexpr int P = HD + 1;
+  const size_t smq = sizeof(float) * (4 * AB_T * P + AB_T * (AB_T + 1));
+  const size_t smk = sizeof(float) * (4 * AB_T * P + 2 * AB_T * (AB_T + 1) + 2 * AB_T);
+  cudaFuncSetAttribute(attn_bwd_q_kernel<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)smq);
+  cudaFuncSetAttribute(attn_bwd_kv_kernel<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)smk);
+  const int tiles = (p.n + AB_T - 1) / AB_T;
+  cudaError_t e = launch_pdl(attn_bwd_q_kernel<T, HD>, dim3(tiles, p.hq, B), dim3(256), smq,
+                             c.stream, p);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(attn_bwd_kv_kernel<T, HD>, dim3(tiles, p.hkv, B), dim3(256), smk, c.stream,
+                    p);
+}
+
+cudaError_t launch_attn_bwd(const Ctx& c, xmod_dtype dt, int B, int hd, const AttnBwd& p) {
+  if (dt == XMOD_BF16) {
+    switch (hd) {
+      case 32: return launch_attn_bwd_t<__nv_bfloat16, 32>(c, B, p);
+      case 64: return launch_attn_bwd_t<__nv_bfloat16, 64>(c, B, p);
+      case 128: return launch_attn_bwd_t<__nv_bfloat16, 128>(c, B, p);
+    }
+  } else {
+    switch (hd) {
+      case 32: return launch_attn_bwd_t<float, 32>(c, B, p);
+      case 64: return launch_attn_bwd_t<float, 64>(c, B, p);
+      case 128: return launch_attn_bwd_t<float, 128>(c, B, p);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <typename E>
+int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
+                const xmod_layer_weights* w, const void* x, const float* bias, const void* dy,
+                float route_coef, void* dx, const xmod_layer_grads* gr, void* ws,
+                const BwLayout& L) {
+  const xmod_dtype dt = dm->dtype;
+  const int B = dm->B, T = dm->T, d = dm->d, hq = dm->n_heads, hkv = dm->n_kv_heads,
+            hd = dm->head_dim, F = dm->d_ff;
+  const bool sparse = kind == XMOD_LAYER_SPARSE;
+  const int n = sparse ? T / K : T;
+  const int M = B * n;
+  const int Mp = (int)round8(M);
+  const int64_t BT = (int64_t)B * T;
+  const int qw = hq * hd, kw = hkv * hd, qkv_w = qw + 2 * kw;
+  const size_t es = sizeof(E);
+  const bool tc = dt == XMOD_BF16;
+  // route_bwd_kernel keeps a float and a flag per token of a sequence in shared memory
+  if (sparse && (size_t)T * (sizeof(float) + 1) > 200 * 1024) return XMOD_ERR_UNSUPPORTED;
+  float* s = (float*)bat(ws, L.s);
+  float* rr = (float*)bat(ws, L.r);
+  int32_t* idx = sparse ? (int32_t*)bat(ws, L.idx) : nullptr;
+  float* r_sel = (float*)bat(ws, L.r_sel);
+  E* u = (E*)bat(ws, L.u);
+  E* qkv = (E*)bat(ws, L.qkv);
+  E* vt = (E*)bat(ws, L.vt);
+  E* o = (E*)bat(ws, L.o);
+  E* a = (E*)bat(ws, L.a);
+  float* h = (float*)bat(ws, L.h);
+  E* v2 = (E*)bat(ws, L.v2);
+  E* gu = (E*)bat(ws, L.gu);
+  E* H = (E*)bat(ws, L.H);
+  E* f = (E*)bat(ws, L.f);
+  E* tA = (E*)bat(ws, L.tA);
+  E* tB = (E*)bat(ws, L.tB);
+  E* tW = (E*)bat(ws, L.tW);
+  float* part = (float*)bat(ws, L.part);
+  const unsigned rowblk = (unsigned)((M + BW_WARPS - 1) / BW_WARPS);
+
+  // ======== forward recompute
+  if (sparse) {
+    BW_RUN("router", launch_router(c, dt, BT, d, x, w->w_router, bias, s, rr));
+    BW_RUN("topk", launch_topk(c, B, T, n, s, idx, r_sel));
+  }
+  BW_RUN("gather_rmsnorm",
+         launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1, dm->rms_eps, u));
+  const bool tc_attn = tc && attention_tc_supported(hd, n, qkv_w);
+  bool v_transposed = false;   // v kept only in its transposed layout (tensor-core path)
+  {
+    Epilogue e;
+    e.kind = EPI_STORE;
+    e.out = qkv;
+    e.ldo = qkv_w;
+    if (tc_attn) {
+      e.vt = vt;
+      e.vt_col0 = qw + kw;
+      e.vt_hd = hd;
+      e.vt_hkv = hkv;
+      e.vt_ld = (int)round8(n);
+      e.n_per_seq = n;
+    }
+    GemmTcProblem pq;
+    pq.M = M; pq.N = qkv_w; pq.K = d; pq.A = u; pq.lda = d; pq.ldb = d;
+    pq.B[0] = w->wq; pq.B[1] = w->wk; pq.B[2] = w->wv; pq.nB = 3;
+    pq.split[0] = qw; pq.split[1] = qw + kw;
+    v_transposed = tc_attn && gemm_tc_supported(pq, e);
+    if (v_transposed) {
+      BW_RUN("gemm_qkv", launch_gemm_tc(c, pq, e));
+      BW_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, (int)round8(n), o));
+    } else {
+      e.vt = nullptr;
+      BW_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, qw, d, u, d, w->wq, d, nullptr, e));
+      e.out = (char*)qkv + es * qw;
+      BW_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wk, d, nullptr, e));
+      e.out = (char*)qkv + es * (qw + kw);
+      BW_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wv, d, nullptr, e));
+      BW_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w,
+                                                (char*)qkv + es * qw, (char*)qkv + es * (qw + kw),
+                                                qkv_w, o));
+    }
+  }
+  {
+    Epilogue eo;
+    eo.kind = EPI_OPROJ;
+    eo.out = a;
+    eo.ldo = d;
+    eo.out2 = h;
+    eo.ldo2 = d;
+    eo.x = (void*)x;
+    eo.idx = idx;
+    eo.T = T;
+    eo.n_per_seq = n;
+    eo.d = d;
+    GemmTcProblem po;
+    po.M = M; po.N = d; po.K = qw; po.A = o; po.lda = qw; po.ldb = qw; po.B[0] = w->wo;
+    if (tc && gemm_tc_supported(po, eo))
+      BW_RUN("gemm_o_residual", launch_gemm_tc(c, po, eo));
+    else
+      BW_RUN("gemm_o_residual", launch_gemm_simt(c, dt, M, d, qw, o, qw, w->wo, qw, nullptr, eo));
+  }
+  BW_RUN("rmsnorm2", launch_rmsnorm_f32in(c, dt, M, d, h, w->rms2, dm->rms_eps, v2));
+  BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_gate, d, gu, 2 * F, false));
+  BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_up, d, gu + F, 2 * F, false));
+  {
+    const int64_t tot = (int64_t)M * F;
+    const unsigned blk = (unsigned)std::min<int64_t>((tot + 255) / 256, 4096);
+    BW_RUN("swiglu", launch_pdl(swiglu_fwd_kernel<E>, dim3(blk), dim3(256), 0, c.stream,
+                                (int64_t)M, F, (const E*)gu, H));
+  }
+  BW_RUN("gemm_down", bw_gemm(c, dt, M, d, F, H, F, w->w_down, F, f, d, false));
+
+  // ======== backward: residual rule and router
+  E* df;
+  const E* dae;
+  if (sparse) {
+    df = (E*)bat(ws, L.df);
+    E* dae_buf = (E*)bat(ws, L.dae);
+    float* dr = (float*)bat(ws, L.dr);
+    float* dvs = (float*)bat(ws, L.dvs);
+    float* ds = (float*)bat(ws, L.ds);
+    float* lossp = (float*)bat(ws, L.lossp);
+    BW_RUN("bwd_rows", launch_pdl(scatter_bwd_kernel<E>, dim3(rowblk), dim3(BW_WARPS * 32), 0,
+                                  c.stream, (int64_t)M, T, n, d, (const E*)dy, (const int32_t*)idx,
+                                  (const float*)r_sel, (const E*)a, (const E*)f, w->varsigma, gate,
+                                  df, dae_buf, dr, dvs));
+    dae = gate == XMOD_GATE_XMOD ? df : dae_buf;
+    const size_t smr = (size_t)T * (sizeof(float) + 1);
+    cudaFuncSetAttribute(route_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smr);
+    BW_RUN("bwd_rows", launch_pdl(route_bwd_kernel, dim3(B), dim3(1024), smr, c.stream, T, n,
+                                  (const float*)s, (const int32_t*)idx, (const float*)r_sel,
+                                  (const float*)dr, route_coef / (float)BT, ds, lossp));
+    BW_RUN("bwd_rows", launch_pdl(dx_init_kernel<E>, dim3((unsigned)((BT + BW_WARPS - 1) / BW_WARPS)),
+                                  dim3(BW_WARPS * 32), 0, c.stream, BT, d, (const E*)dy,
+                                  (const float*)ds, (const E*)w->w_router, (E*)dx));
+    int st = bw_coldot<E>(c, BT, d, nullptr, (const E*)x, nullptr, T, T, ds, part, gr->w_router);
+    if (st) return st;
+    BW_RUN("bwd_reduce", launch_pdl(sum_kernel, dim3(1), dim3(1024), 0, c.stream, (int64_t)M,
+                                    (const float*)dvs, 1.0f, gr->varsigma));
+    if (gr->route_loss)
+      BW_RUN("bwd_reduce", launch_pdl(sum_kernel, dim3(1), dim3(1024), 0, c.stream, (int64_t)B,
+                                      (const float*)lossp, 1.0f / (float)BT, gr->route_loss));
+  } else {   // dense: y = x + a + f, so both residuals receive dy; dx starts as dy
+    df = (E*)dy;
+    dae = (const E*)dy;
+    if (cudaMemcpyAsync(dx, dy, es * (size_t)BT * d, cudaMemcpyDeviceToDevice, c.stream) !=
+        cudaSuccess)
+      return XMOD_ERR_CUDA;
+    if (cudaMemsetAsync(gr->varsigma, 0, sizeof(float), c.stream) != cudaSuccess)
+      return XMOD_ERR_CUDA;
+    if (gr->w_router &&
+        cudaMemsetAsync(gr->w_router, 0, sizeof(float) * (size_t)d, c.stream) != cudaSuccess)
+      return XMOD_ERR_CUDA;
+    if (gr->route_loss && cudaMemsetAsync(gr->route_loss, 0, sizeof(float), c.stream) != cudaSuccess)
+      return XMOD_ERR_CUDA;
+  }
+
+  // ======== FFN: f = H Wd^T, H = silu(G) U, [G | U] = v2 [Wg | Wu]^T
+  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, df, d, tA, Mp));      // df^T [d, Mp]
+  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, F, H, F, tB, Mp));       // H^T [F, Mp]
+  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, d, F, Mp, tA, Mp, tB, Mp, gr->w_down, F, true));
+  BW_RUN("bwd_transpose", transpose(c, dt, d, d, F, w->w_down, F, tW, d));  // Wd^T [F, d]
+  float* dH = (float*)bat(ws, L.dH);
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, F, d, df, d, tW, d, dH, F, true));
+  E* dGU = (E*)bat(ws, L.dGU);
+  {
+    const int64_t tot = (int64_t)M * F;
+    const unsigned blk = (unsigned)std::min<int64_t>((tot + 255) / 256, 4096);
+    BW_RUN("swiglu", launch_pdl(swiglu_bwd_kernel<E>, dim3(blk), dim3(256), 0, c.stream,
+                                (int64_t)M, F, (const E*)gu, (const float*)dH, dGU));
+  }
+  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, 2 * F, dGU, 2 * F, tA, Mp));  // [2F, Mp]
+  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, v2, d, tB, Mp));           // v2^T [d, Mp]
+  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, F, d, Mp, tA, Mp, tB, Mp, gr->w_gate, d, true));
+  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, F, d, Mp, tA + (size_t)F * Mp, Mp, tB, Mp, gr->w_up, d,
+                                true));
+  BW_RUN("bwd_transpose", transpose(c, dt, F, F, d, w->w_gate, d, tW, 2 * F));  // [d, 2F]
+  BW_RUN("bwd_transpose", transpose(c, dt, F, F, d, w->w_up, d, tW + F, 2 * F));
+  float* dv2 = (float*)bat(ws, L.dv2);
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, 2 * F, dGU, 2 * F, tW, 2 * F, dv2, d, true));
+  // v2 = RMSNorm(h) g2; h = x_sel + a: dh reaches x_sel and (with dae) a
+  float* dh = (float*)bat(ws, L.dh);
+  E* da = (E*)bat(ws, L.da);
+  float* rstd2 = (float*)bat(ws, L.rstd2);
+  BW_RUN("bwd_rows", launch_pdl(rms_bwd_kernel<float, E>, dim3(rowblk), dim3(BW_WARPS * 32), 0,
+                                c.stream, (int64_t)M, d, (const float*)dv2, (const E*)w->rms2,
+                                (const float*)h, (const int32_t*)nullptr, T, n, dm->rms_eps, dae,
+                                dh, da, (const float*)nullptr, (E*)nullptr, rstd2));
+  {
+    const int st = bw_coldot<float>(c, M, d, dv2, h, nullptr, T, n, rstd2, part, gr->rms2);
+    if (st) return st;
+  }
+
+  // ======== a = o Wo^T
+  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, da, d, tA, Mp));     // da^T [d, Mp]
+  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, qw, o, qw, tB, Mp));    // o^T [qw, Mp]
+  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, d, qw, Mp, tA, Mp, tB, Mp, gr->wo, qw, true));
+  BW_RUN("bwd_transpose", transpose(c, dt, d, d, qw, w->wo, qw, tW, d));  // Wo^T [qw, d]
+  float* dO = (float*)bat(ws, L.dO);
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, qw, d, da, d, tW, d, dO, qw, true));
+
+  // ======== attention
+  E* dqkv = (E*)bat(ws, L.dqkv);
+  {
+    AttnBwd p;
+    p.n = n;
+    p.hq = hq;
+    p.hkv = hkv;
+    p.qkv = qkv;
+    p.ldq = qkv_w;
+    p.v = v_transposed ? (const void*)vt : (const void*)qkv;
+    p.vt_mode = v_transposed ? 1 : 0;
+    p.vt_ld = (int)round8(n);
+    p.o = o;
+    p.dO = dO;
+    p.lse = (float*)bat(ws, L.lse);
+    p.Dd = (float*)bat(ws, L.Dd);
+    p.dqkv = dqkv;
+    p.ldg = qkv_w;
+    p.scale = 1.0f / sqrtf((float)hd);
+    BW_RUN("bwd_attention", launch_attn_bwd(c, dt, B, hd, p));
+  }
+
+  // ======== q, k, v = u [Wq | Wk | Wv]^T
+  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, qkv_w, dqkv, qkv_w, tA, Mp));  // [qkv_w, Mp]
+  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, u, d, tB, Mp));              // u^T [d, Mp]
+  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, qw, d, Mp, tA, Mp, tB, Mp, gr->wq, d, true));
+  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, kw, d, Mp, tA + (size_t)qw * Mp, Mp, tB, Mp, gr->wk, d,
+                                true));
+  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, kw, d, Mp, tA + (size_t)(qw + kw) * Mp, Mp, tB, Mp, gr->wv,
+                                d, true));
+  BW_RUN("bwd_transpose", transpose(c, dt, qw, qw, d, w->wq, d, tW, qkv_w));      // [d, qkv_w]
+  BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wk, d, tW + qw, qkv_w));
+  BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wv, d, tW + qw + kw, qkv_w));
+  float* du = (float*)bat(ws, L.du);
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qkv_w, dqkv, qkv_w, tW, qkv_w, du, d, true));
+  // u = RMSNorm(x_sel) g1; the gather's backward adds into the token's row of dx
+  float* rstd1 = (float*)bat(ws, L.rstd1);
+  BW_RUN("bwd_rows", launch_pdl(rms_bwd_kernel<E, E>, dim3(rowblk), dim3(BW_WARPS * 32), 0,
+                                c.stream, (int64_t)M, d, (const float*)du, (const E*)w->rms1,
+                                (const E*)x, (const int32_t*)idx, T, n, dm->rms_eps,
+                                (const E*)nullptr, (float*)nullptr, (E*)nullptr,
+                                (const float*)dh, (E*)dx, rstd1));
+  return bw_coldot<E>(c, M, d, du, (const E*)x, idx, T, n, rstd1, part, gr->rms1);
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(const xmod_dims* dm) { return bw_layout(dm).total; }
+
+int run_layer_bwd(cudaStream_t stream, const xmod_dims* dm, int kind, int K, int gate,
+                  const xmod_layer_weights* w, const void* x, const float* bias, const void* dy,
+                  float route_coef, void* dx, const xmod_layer_grads* gr, void* ws) {
+  const BwLayout L = bw_layout(dm);
+  Ctx c{stream, (int*)bat(ws, L.status)};
+  if (dm->dtype == XMOD_BF16)
+    return layer_bwd_t<__nv_bfloat16>(c, dm, kind, K, gate, w, x, bias, dy, route_coef, dx, gr,
+                                      ws, L);
+  return layer_bwd_t<float>(c, dm, kind, K, gate, w, x, bias, dy, route_coef, dx, gr, ws, L);
+}
+
+}  // namespace xmod

@@ -24,7 +24,8 @@ __device__ __forceinline__ void epilogue_store(const Epilogue& e, int M, int N, 
   if (m >= M || n >= N) return;
   switch (e.kind) {
     case EPI_STORE:
-      st_f((T*)e.out + (int64_t)m * e.ldo + n, acc);
+      if (e.out_f32) ((float*)e.out)[(int64_t)m * e.ldo + n] = acc;
+      else st_f((T*)e.out + (int64_t)m * e.ldo + n, acc);
       break;
     case EPI_OPROJ: {
       const int64_t b = m / e.n_per_seq;

@@ -438,7 +438,13 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, in
   const Epilogue& e = a.e;
   if (m >= M || col0 >= a.N) return;
   const int rem = a.N - col0;
-  if (MODE == EPI_STORE || MODE == EPI_SWIGLU) {
+  if (MODE == EPI_STORE && e.out_f32) {
+    float4 fv[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      fv[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+    st_seg_f32((float*)e.out + (int64_t)m * e.ldo + col0, fv, rem, a.v8);
+  } else if (MODE == EPI_STORE || MODE == EPI_SWIGLU) {
     store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem, a.v8);
   } else if (MODE == EPI_OPROJ) {
     if (e.out) store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem, a.v8);
@@ -999,7 +1005,8 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
     return ((uintptr_t)base & 31) == 0 && row_bytes % 32 == 0;
   };
   bool v8 = true;
-  if (e.out && e.kind != EPI_ROUTER) v8 = v8 && seg_ok(e.out, (int64_t)e.ldo * 2);
+  if (e.out && e.kind != EPI_ROUTER)
+    v8 = v8 && seg_ok(e.out, (int64_t)e.ldo * (e.out_f32 ? 4 : 2));
   if (e.out2) v8 = v8 && seg_ok(e.out2, (int64_t)e.ldo2 * 4);
   if (e.x) v8 = v8 && seg_ok(e.x, (int64_t)e.d * 2);
   if (e.a) v8 = v8 && seg_ok(e.a, (int64_t)e.d * 2);

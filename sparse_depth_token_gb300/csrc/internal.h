@@ -209,6 +209,9 @@ struct Epilogue {
   // transposed to vt [B, hkv, hd, vt_ld] (keys contiguous) instead of to `out`.
   void* vt = nullptr;
   int vt_col0 = 0, vt_hd = 0, vt_hkv = 0, vt_ld = 0;
+  // STORE: write the fp32 accumulator itself (out is float [M, ldo]) instead of
+  // rounding it to the layer's element type
+  bool out_f32 = false;
 };
 
 // C[M, N] = A[M, K] . B[N, K]^T (fp32 accumulate), then the epilogue. For
@@ -271,5 +274,14 @@ cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, con
                                 int ldq, const void* vt, int vt_ld, void* o,
                                 const int32_t* seq_count = nullptr,
                                 const int32_t* seq_off = nullptr, const AttnKv* kv = nullptr);
+
+// ---------------------------------------------------------------- backward of one layer
+
+// Workspace bytes of run_layer_bwd for these sizes (covers a dense layer).
+size_t bwd_workspace_bytes(const xmod_dims* dm);
+// See xmod_layer_bwd; arguments already validated by the caller.
+int run_layer_bwd(cudaStream_t stream, const xmod_dims* dm, int kind, int K, int gate,
+                  const xmod_layer_weights* w, const void* x, const float* bias, const void* dy,
+                  float route_coef, void* dx, const xmod_layer_grads* gr, void* ws);
 
 }  // namespace xmod

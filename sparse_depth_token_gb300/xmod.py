@@ -23,7 +23,8 @@ EXPORTS = ("xmod_version", "xmod_status_string", "xmod_workspace_bytes", "xmod_r
            "xmod_sync_status", "xmod_router_topk", "xmod_topk", "xmod_gather", "xmod_block_fwd",
            "xmod_gated_scatter", "xmod_layer_fwd", "xmod_stack_fwd", "xmod_launch_count",
            "xmod_profile_enable", "xmod_profile_read", "xmod_router_topk_noalloc",
-           "xmod_stack_fwd_ex", "xmod_layer_fwd_threshold", "xmod_stack_fwd_sched")
+           "xmod_stack_fwd_ex", "xmod_layer_fwd_threshold", "xmod_stack_fwd_sched",
+           "xmod_bwd_workspace_bytes", "xmod_layer_bwd")
 
 # Largest B*T the allocation-free router entry point accepts (its fixed scratch).
 NOALLOC_MAX_TOKENS = 2 * 1024 * 1024
@@ -47,6 +48,12 @@ class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in NAMES] + [
         ("varsigma", ctypes.c_float), ("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p),
         ("rope_theta", ctypes.c_float)]
+
+
+class LayerGrads(ctypes.Structure):
+    NAMES = ("w_router", "rms1", "wq", "wk", "wv", "wo", "rms2", "w_gate", "w_up", "w_down",
+             "varsigma", "route_loss")
+    _fields_ = [(n, ctypes.c_void_p) for n in NAMES]
 
 
 ROUTE_TOPK, ROUTE_THRESHOLD = 0, 1
@@ -120,6 +127,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                     ctypes.POINTER(ctypes.c_int)]
     L.xmod_router_topk_noalloc.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _VP, _VP, _VP, _VP,
                                            _VP, _VP, _VP]
+    L.xmod_bwd_workspace_bytes.restype = ctypes.c_size_t
+    L.xmod_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Dims), ctypes.c_int]
+    L.xmod_layer_bwd.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                 ctypes.POINTER(LayerWeights), _VP, _VP, _VP, ctypes.c_float,
+                                 _VP, ctypes.POINTER(LayerGrads), _VP, ctypes.c_size_t, _VP]
     _lib = L
     return L
 
@@ -287,3 +299,20 @@ def router_topk_noalloc(dm, K, x, w_r, bias, idx, r_sel, status=None, stream=Non
     _check("xmod_router_topk_noalloc", load().xmod_router_topk_noalloc(
         ctypes.byref(dm), int(K), _p(x), _p(w_r), _p(bias), _p(idx), _p(r_sel), _p(status),
         _stream(stream)))
+
+
+def bwd_workspace_bytes(dm: Dims, K: int) -> int:
+    return int(load().xmod_bwd_workspace_bytes(ctypes.byref(dm), int(K)))
+
+
+def layer_grads(tensors: dict) -> LayerGrads:
+    """LayerGrads from fp32 device tensors keyed by LayerGrads.NAMES (missing: NULL)."""
+    return LayerGrads(*[_p(tensors.get(n)) for n in LayerGrads.NAMES])
+
+
+def layer_bwd(dm, kind, K, gate, w: LayerWeights, x, bias, dy, route_coef, dx, grads: LayerGrads,
+              ws, stream=None):
+    """xmod_layer_bwd: dx and the weight gradients of sum(dy * y) + route_coef * L_route."""
+    _check("xmod_layer_bwd", load().xmod_layer_bwd(
+        ctypes.byref(dm), int(kind), int(K), int(gate), ctypes.byref(w), _p(x), _p(bias), _p(dy),
+        float(route_coef), _p(dx), ctypes.byref(grads), _p(ws), _wsb(ws), _stream(stream)))
