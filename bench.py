@@ -519,6 +519,164 @@ def run_xmod(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------- backward pass
+
+BWD_METRIC = "selected tokens/s per X-MoD sparse-layer bwd (bf16, 1xGB300); % tensor roofline"
+
+
+def backward_work(w: I.Workload) -> dict:
+    """Algorithmic FLOPs per backward step (every layer of the stack once, in reverse):
+    the forward each layer recomputes, the activation- and weight-gradient GEMMs (each
+    as many FLOPs as the forward projection) and the attention backward (S recomputed,
+    dP, dV, dQ, dK: five causal n x n x head_dim products per head)."""
+    out = {}
+
+    def add(kind, v):
+        out[kind] = out.get(kind, 0.0) + float(v)
+
+    qw, kw = w.hq * w.hd, w.hkv * w.hd
+    for kind in schedule(w, "xmod"):
+        n = w.T // w.K if kind == SPARSE else w.T
+        M = w.B * n
+        add("gemm_qkv", 2 * M * w.d * (qw + 2 * kw))
+        add("attention", 2 * w.B * n * n * w.hd * w.hq)
+        add("gemm_o_residual", 2 * M * qw * w.d)
+        add("gemm_gate_up", 4 * M * w.d * w.F)
+        add("gemm_down", 2 * M * w.F * w.d)
+        proj = 2 * M * w.d * (qw + 2 * kw) + 2 * M * qw * w.d + 6 * M * w.d * w.F
+        add("bwd_gemm_dw", proj)
+        add("bwd_gemm_dx", proj)
+        add("bwd_attention", 5 * w.B * n * n * w.hd * w.hq)
+    return out
+
+
+BWD_TENSOR_KINDS = {"gemm_qkv", "attention", "gemm_o_residual", "gemm_gate_up", "gemm_down",
+                    "bwd_gemm_dw", "bwd_gemm_dx", "bwd_attention"}
+
+
+def run_backward(args):
+    """--pass bwd: the backward of the whole stack, layer by layer in reverse
+    (xmod_layer_bwd, Eq. 9 coefficient 1e-4 as the pages chose), from the layer inputs a
+    forward pass stored, with a synthetic upstream gradient dy ~ N(0, 1) at the top. One
+    step = every layer's backward once; the weight gradients of a layer are written to
+    one shared set of fp32 buffers (a trainer would keep one set per layer)."""
+    import torch
+    from sparse_depth_token_gb300 import xmod as X
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    X.load()
+    w = I.WORKLOADS[args.workload]
+    kinds = schedule(w, "xmod")
+    n_sparse = sum(1 for k in kinds if k == SPARSE)
+    sel_per_step = n_sparse * w.B * (w.T // w.K)
+    layers = I.all_layer_weights(w, len(kinds))
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    dev_layers = [{ABI_NAMES[k]: to_dev(v) for k, v in l.items() if k in ABI_NAMES} for l in layers]
+    abi = [X.layer_weights(d, l["varsigma"]) for d, l in zip(dev_layers, layers)]
+    bias_host = I.router_bias(w)
+    bias = torch.from_numpy(bias_host).to(dev) if bias_host is not None else None
+    dm = X.dims(w.B, w.T, w.d, w.hq, w.hkv, w.hd, w.F, X.BF16, w.eps)
+    # the layer inputs of one forward pass
+    ws_f = torch.zeros(X.workspace_bytes(dm, w.K), dtype=torch.uint8, device=dev)
+    xs = [to_dev(I.residual_stream(w))]
+    for l, kind in enumerate(kinds):
+        x = xs[-1].clone()
+        X.layer_fwd(dm, kind, w.K, w.gate, abi[l], x, bias if kind == SPARSE else None, None,
+                    None, ws_f)
+        xs.append(x)
+    del ws_f
+    ws = torch.zeros(X.bwd_workspace_bytes(dm, w.K), dtype=torch.uint8, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    dy_top = torch.randn(xs[0].shape, generator=g, device=dev).to(torch.bfloat16)
+    dbuf = [torch.empty_like(dy_top), torch.empty_like(dy_top)]
+    qw, kw = w.hq * w.hd, w.hkv * w.hd
+    shapes = {"w_router": (w.d,), "rms1": (w.d,), "wq": (qw, w.d), "wk": (kw, w.d),
+              "wv": (kw, w.d), "wo": (w.d, qw), "rms2": (w.d,), "w_gate": (w.F, w.d),
+              "w_up": (w.F, w.d), "w_down": (w.d, w.F), "varsigma": (4,), "route_loss": (4,)}
+    gd = {k: torch.empty(v, dtype=torch.float32, device=dev) for k, v in shapes.items()}
+    grads = X.layer_grads(gd)
+    stream = torch.cuda.current_stream()
+    coef = 1e-4
+
+    def step():
+        dy = dy_top
+        for l in range(len(kinds) - 1, -1, -1):
+            dx = dbuf[l & 1]
+            X.layer_bwd(dm, kinds[l], w.K, w.gate, abi[l], xs[l],
+                        bias if kinds[l] == SPARSE else None, dy, coef, dx, grads, ws, stream)
+            dy = dx
+
+    X.reset_status(ws)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    st = X.sync_status(ws)
+    if st != X.OK:
+        raise RuntimeError(f"device status after warm-up: {X.status_string(st)}")
+    clocks = ClockSampler(0)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = X.launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = (X.launch_count() - launches0) // args.steps
+    clock_info = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    X.profile_read()
+    X.profile_enable(True)
+    prof_steps = max(1, min(args.steps, 2))
+    for _ in range(prof_steps):
+        step()
+    torch.cuda.synchronize()
+    X.profile_enable(False)
+    prof = X.profile_read()
+    st = X.sync_status(ws)
+    if st != X.OK:
+        raise RuntimeError(f"device status after the run: {X.status_string(st)}")
+    work = backward_work(w)
+    peaks = measured_peaks()
+    total_ms = sum(v[1] for v in prof.values())
+    kernels = {}
+    for kind, (cnt, kms) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+        pms = kms / prof_steps
+        e = {"launches_per_step": cnt // prof_steps, "ms_per_step": pms,
+             "share": kms / total_ms if total_ms else None}
+        if kind in work and pms > 0:
+            e["tflops"] = work[kind] / (pms / 1e3) / 1e12
+        kernels[kind] = e
+    top = max(prof.items(), key=lambda kv: kv[1][1])[0]
+    roofline = None
+    if top in work:
+        cnt, kms = prof[top]
+        ach = work[top] / (kms / prof_steps / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roofline = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": peak,
+                    "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                    "peak_source": f"{peaks['source']} bf16 sustained",
+                    "algorithmic_per_launch": work[top] / (cnt / prof_steps)}
+    cfg = workload_config(w)
+    cfg["pass"] = "backward of every layer (xmod_layer_bwd, forward recomputed inside), " \
+                  "Eq. 9 coefficient 1e-4, synthetic upstream gradient dy~N(0,1)"
+    print(json.dumps({
+        "metric": BWD_METRIC, "value": sel_per_step / (ms / 1e3), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights)", "config": cfg,
+        "roofline": roofline, "gpu_launches": int(launches) * args.steps,
+        "gpu_launches_per_step": int(launches), "clocks": clock_info,
+        "step_tflops": sum(work.values()) / (ms / 1e3) / 1e12, "kernels": kernels}), flush=True)
+
+
 # ---------------------------------------------------------------------- routing microbench
 
 ROUTING_KS = (2, 8, 16)
@@ -835,6 +993,8 @@ def main():
                     help="X-MoD stack, or one of the mechanism controls")
     ap.add_argument("--qwen3", action="store_true",
                     help="QK-norm and RoPE (base 1e6) in every attending layer")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="bwd: time the backward of every layer of the stack (xmod_layer_bwd)")
     ap.add_argument("--K", type=int, default=None,
                     help="routing_bf16 only: one sparsity K (default: 8 as the headline, with "
                          "2 and 16 under \"sweep\")")
@@ -846,7 +1006,9 @@ def main():
         A = w.A if args.A is None else args.A
         n_layers = w.N0 + w.N1 * (int(round(A * w.K)) + 1)
         I.WORKLOADS[args.workload] = w.replace(B=args.B or w.B, A=A, n_layers=n_layers)
-    if args.workload == "routing_bf16":   # the routing-only microbench: no block
+    if args.pass_ == "bwd":
+        run_backward(args)
+    elif args.workload == "routing_bf16":   # the routing-only microbench: no block
         if args.impl == "reference":
             run_routing_reference(args)
         else:

@@ -791,6 +791,8 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     v_transposed = tc_attn && gemm_tc_supported(pq, e);
     if (v_transposed) {
       BW_RUN("gemm_qkv", launch_gemm_tc(c, pq, e));
+      // the backward also reads v by rows: the v projection once more into the v columns
+      BW_RUN("gemm_qkv", bw_gemm(c, dt, M, kw, d, u, d, w->wv, d, qkv + qw + kw, qkv_w, false));
       BW_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, (int)round8(n), o));
     } else {
       e.vt = nullptr;
@@ -921,11 +923,16 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, d, qw, Mp, tA, Mp, tB, Mp, gr->wo, qw, true));
   BW_RUN("bwd_transpose", transpose(c, dt, d, d, qw, w->wo, qw, tW, d));  // Wo^T [qw, d]
   float* dO = (float*)bat(ws, L.dO);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, qw, d, da, d, tW, d, dO, qw, true));
+  const bool mma_attn = tc && attn_bwd_mma_supported(hd, qkv_w, qw);
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, qw, d, da, d, tW, d, dO, qw, !mma_attn));
 
   // ======== attention
   E* dqkv = (E*)bat(ws, L.dqkv);
-  {
+  if (mma_attn) {   // bf16: warp-level tensor-core MMA, v rows and dO in bf16
+    BW_RUN("bwd_attention", launch_attn_bwd_mma(c, B, n, hq, hkv, hd, qkv, qkv_w, o, dO,
+                                                (float*)bat(ws, L.lse), (float*)bat(ws, L.Dd),
+                                                dqkv, qkv_w));
+  } else {
     AttnBwd p;
     p.n = n;
     p.hq = hq;

@@ -277,6 +277,15 @@ cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, con
 
 // ---------------------------------------------------------------- backward of one layer
 
+// Attention backward on the warp-level tensor-core MMA (bf16, head_dim 64 or 128):
+// qkv rows [B*n, ldq] (q, k AND v columns written), o and dO [B*n, hq*hd] bf16;
+// writes lse / Dd [B*n, hq] (log2 units / <dO, o>) and dq, dk, dv into the q, k, v
+// columns of dqkv [B*n, ldg].
+bool attn_bwd_mma_supported(int hd, int ldq, int ldo);
+cudaError_t launch_attn_bwd_mma(const Ctx& c, int B, int n, int hq, int hkv, int hd,
+                                const void* qkv, int ldq, const void* o, const void* dO,
+                                float* lse, float* Dd, void* dqkv, int ldg);
+
 // Workspace bytes of run_layer_bwd for these sizes (covers a dense layer).
 size_t bwd_workspace_bytes(const xmod_dims* dm);
 // See xmod_layer_bwd; arguments already validated by the caller.
