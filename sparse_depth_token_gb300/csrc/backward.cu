@@ -37,6 +37,23 @@ __device__ __forceinline__ int64_t bw_stream_row(int64_t m, int T, int n, const 
   return b * T + t;
 }
 
+// Four consecutive elements (16 bytes of fp32, 8 of bf16) as a float4, and back.
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
 __device__ __forceinline__ float softplus_f(float z) {
   return fmaxf(z, 0.0f) + log1pf(expf(-fabsf(z)));
 }
@@ -82,18 +99,27 @@ scatter_bwd_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ dy,
   if (m >= M) return;
   const T* g = dy + bw_stream_row(m, seqT, n, idx) * d;
   const float r = r_sel[m];
+  constexpr int V = Vec16<T>::N;
   float dot = 0.0f;
-  for (int c = lane; c < d; c += 32) {
-    const float gv = Elem<T>::to_f(g[c]);
-    const float fv = Elem<T>::to_f(f[m * d + c]);
+  for (int c = lane * V; c < d; c += 32 * V) {
+    const Vec16<T> gv = ld_vec(g + c), fv = ld_vec(f + m * d + c);
+    Vec16<T> o;
     if (gate == XMOD_GATE_XMOD) {
-      dot += gv * (Elem<T>::to_f(a[m * d + c]) + fv);
-      df[m * d + c] = Elem<T>::from_f(vs * r * gv);
+      const Vec16<T> av = ld_vec(a + m * d + c);
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        dot += gv.get(k) * (av.get(k) + fv.get(k));
+        o.set(k, vs * r * gv.get(k));
+      }
     } else {
-      dot += gv * fv;
-      df[m * d + c] = Elem<T>::from_f(r * gv);
-      dae[m * d + c] = g[c];
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        dot += gv.get(k) * fv.get(k);
+        o.set(k, r * gv.get(k));
+      }
+      st_vec(dae + m * d + c, gv);
     }
+    st_vec(df + m * d + c, o);
   }
   dot = warp_sum(dot);
   if (lane == 0) {
@@ -159,14 +185,20 @@ dx_init_kernel(int64_t rows, int d, const T* __restrict__ dy, const float* __res
   const int64_t row = (int64_t)blockIdx.x * BW_WARPS + warp;
   if (row >= rows) return;
   const float g = ds[row];
-  for (int c = lane; c < d; c += 32)
-    dx[row * d + c] = Elem<T>::from_f(Elem<T>::to_f(dy[row * d + c]) + g * Elem<T>::to_f(w_r[c]));
+  constexpr int V = Vec16<T>::N;
+  for (int c = lane * V; c < d; c += 32 * V) {
+    const Vec16<T> yv = ld_vec(dy + row * d + c), wv = ld_vec(w_r + c);
+    Vec16<T> o;
+#pragma unroll
+    for (int k = 0; k < V; ++k) o.set(k, yv.get(k) + g * wv.get(k));
+    st_vec(dx + row * d + c, o);
+  }
 }
 
 // ---------------------------------------------------------------- column reductions
 // part[chunk, c] = sum over the chunk's rows m of (A ? A[m, c] : 1) * Bv[row(m), c] *
 // (w ? w[m] : 1), rows in order; row(m) is the stream row of compact row m (idx NULL:
-// m). One thread per column; grid (column blocks, row chunks).
+// m). One thread per 16-byte vector of columns; grid (column blocks, row chunks).
 template <typename TB>
 __global__ void __launch_bounds__(256)
 coldot_kernel(int64_t M, int d, const float* __restrict__ A, const TB* __restrict__ Bv,
@@ -174,19 +206,34 @@ coldot_kernel(int64_t M, int d, const float* __restrict__ A, const TB* __restric
               int64_t rows_per_chunk, float* __restrict__ part) {
   pdl_trigger();
   pdl_wait();
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  constexpr int V = Vec16<TB>::N;
+  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * V;
   if (c >= d) return;
   const int64_t m0 = (int64_t)blockIdx.y * rows_per_chunk;
   const int64_t m1 = min(M, m0 + rows_per_chunk);
-  float acc = 0.0f;
+  float acc[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) acc[k] = 0.0f;
   for (int64_t m = m0; m < m1; ++m) {
     const int64_t row = idx ? bw_stream_row(m, seqT, n, idx) : m;
-    float v = Elem<TB>::to_f(Bv[row * d + c]);
-    if (A) v *= A[m * d + c];
-    if (w) v *= w[m];
-    acc += v;
+    const Vec16<TB> bv = ld_vec(Bv + row * d + c);
+    const float wm = w ? w[m] : 1.0f;
+    if (A) {
+#pragma unroll
+      for (int k = 0; k < V; k += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(A + m * d + c + k);
+        acc[k] += a.x * bv.get(k) * wm;
+        acc[k + 1] += a.y * bv.get(k + 1) * wm;
+        acc[k + 2] += a.z * bv.get(k + 2) * wm;
+        acc[k + 3] += a.w * bv.get(k + 3) * wm;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < V; ++k) acc[k] += bv.get(k) * wm;
+    }
   }
-  part[(int64_t)blockIdx.y * d + c] = acc;
+#pragma unroll
+  for (int k = 0; k < V; ++k) part[(int64_t)blockIdx.y * d + c + k] = acc[k];
 }
 
 // out[c] = sum over chunks k (in order) of part[k, c].
@@ -221,18 +268,26 @@ sum_kernel(int64_t n, const float* __restrict__ in, float scale, float* __restri
 
 // ---------------------------------------------------------------- SwiGLU
 // gu [M, 2F]: the gate pre-activation G in columns [0, F), the up projection U in [F, 2F).
+// One 16-byte vector (V elements) per thread and step; F % V == 0.
 template <typename T>
 __global__ void swiglu_fwd_kernel(int64_t M, int F, const T* __restrict__ gu, T* __restrict__ H) {
   pdl_trigger();
   pdl_wait();
-  const int64_t total = M * F;
+  constexpr int V = Vec16<T>::N;
+  const int FV = F / V;
+  const int64_t total = M * FV;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t m = i / F;
-    const int e = (int)(i - m * F);
-    const float g = Elem<T>::to_f(gu[m * 2 * F + e]);
-    const float u = Elem<T>::to_f(gu[m * 2 * F + F + e]);
-    H[i] = Elem<T>::from_f(g / (1.0f + expf(-g)) * u);
+    const int64_t m = i / FV;
+    const int e = (int)(i - m * FV) * V;
+    const Vec16<T> g = ld_vec(gu + m * 2 * F + e), u = ld_vec(gu + m * 2 * F + F + e);
+    Vec16<T> h;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const float gv = g.get(k);
+      h.set(k, gv / (1.0f + expf(-gv)) * u.get(k));
+    }
+    st_vec(H + m * F + e, h);
   }
 }
 
@@ -242,17 +297,30 @@ __global__ void swiglu_bwd_kernel(int64_t M, int F, const T* __restrict__ gu,
                                   const float* __restrict__ dH, T* __restrict__ dgu) {
   pdl_trigger();
   pdl_wait();
-  const int64_t total = M * F;
+  constexpr int V = Vec16<T>::N;
+  const int FV = F / V;
+  const int64_t total = M * FV;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t m = i / F;
-    const int e = (int)(i - m * F);
-    const float g = Elem<T>::to_f(gu[m * 2 * F + e]);
-    const float u = Elem<T>::to_f(gu[m * 2 * F + F + e]);
-    const float sg = 1.0f / (1.0f + expf(-g));
-    const float dh = dH[i];
-    dgu[m * 2 * F + e] = Elem<T>::from_f(dh * u * sg * (1.0f + g * (1.0f - sg)));
-    dgu[m * 2 * F + F + e] = Elem<T>::from_f(dh * g * sg);
+    const int64_t m = i / FV;
+    const int e = (int)(i - m * FV) * V;
+    const Vec16<T> g = ld_vec(gu + m * 2 * F + e), u = ld_vec(gu + m * 2 * F + F + e);
+    float dh[V];
+#pragma unroll
+    for (int k = 0; k < V; k += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(dH + m * F + e + k);
+      dh[k] = q.x; dh[k + 1] = q.y; dh[k + 2] = q.z; dh[k + 3] = q.w;
+    }
+    Vec16<T> dg, du;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      const float gv = g.get(k), uv = u.get(k);
+      const float sg = 1.0f / (1.0f + expf(-gv));
+      dg.set(k, dh[k] * uv * sg * (1.0f + gv * (1.0f - sg)));
+      du.set(k, dh[k] * gv * sg);
+    }
+    st_vec(dgu + m * 2 * F + e, dg);
+    st_vec(dgu + m * 2 * F + F + e, du);
   }
 }
 
@@ -278,24 +346,33 @@ rms_bwd_kernel(int64_t M, int d, const float* __restrict__ dz, const T* __restri
   const TIN* xr = xin + row * d;
   const float* dzr = dz + m * d;
   float ss = 0.0f;
-  for (int c = lane; c < d; c += 32) {
-    const float v = Elem<TIN>::to_f(xr[c]);
-    ss += v * v;
+  for (int c = lane * 4; c < d; c += 128) {
+    const float4 v = ld4(xr + c);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
   const float rho = rsqrtf(warp_sum(ss) / (float)d + eps);
   float dot = 0.0f;
-  for (int c = lane; c < d; c += 32)
-    dot += dzr[c] * Elem<T>::to_f(g[c]) * Elem<TIN>::to_f(xr[c]) * rho;
+  for (int c = lane * 4; c < d; c += 128) {
+    const float4 z = *reinterpret_cast<const float4*>(dzr + c), gg = ld4(g + c), x = ld4(xr + c);
+    dot += (z.x * gg.x * x.x + z.y * gg.y * x.y + z.z * gg.z * x.z + z.w * gg.w * x.w) * rho;
+  }
   const float mean = warp_sum(dot) / (float)d;
-  for (int c = lane; c < d; c += 32) {
-    const float xh = Elem<TIN>::to_f(xr[c]) * rho;
-    const float gr = rho * (dzr[c] * Elem<T>::to_f(g[c]) - xh * mean);
+  for (int c = lane * 4; c < d; c += 128) {
+    const float4 z = *reinterpret_cast<const float4*>(dzr + c), gg = ld4(g + c), x = ld4(xr + c);
+    float4 gr;
+    gr.x = rho * (z.x * gg.x - x.x * rho * mean);
+    gr.y = rho * (z.y * gg.y - x.y * rho * mean);
+    gr.z = rho * (z.z * gg.z - x.z * rho * mean);
+    gr.w = rho * (z.w * gg.w - x.w * rho * mean);
     if (dh_out) {
-      dh_out[m * d + c] = gr;
-      da_out[m * d + c] = Elem<T>::from_f(gr + Elem<T>::to_f(dae[m * d + c]));
+      *reinterpret_cast<float4*>(dh_out + m * d + c) = gr;
+      const float4 e = ld4(dae + m * d + c);
+      st4(da_out + m * d + c, make_float4(gr.x + e.x, gr.y + e.y, gr.z + e.z, gr.w + e.w));
     } else {
       T* p = dx_io + row * d + c;
-      *p = Elem<T>::from_f(Elem<T>::to_f(*p) + (dadd[m * d + c] + gr));
+      const float4 cur = ld4(p), ad = *reinterpret_cast<const float4*>(dadd + m * d + c);
+      st4(p, make_float4(cur.x + (ad.x + gr.x), cur.y + (ad.y + gr.y), cur.z + (ad.z + gr.z),
+                         cur.w + (ad.w + gr.w)));
     }
   }
   if (lane == 0) rstd_out[m] = rho;
@@ -679,10 +756,11 @@ cudaError_t bw_gemm(const Ctx& c, xmod_dtype dt, int M, int N, int K, const void
 template <typename TB>
 int bw_coldot(const Ctx& c, int64_t M, int d, const float* A, const TB* Bv, const int32_t* idx,
               int seqT, int n, const float* w, float* part, float* out) {
+  constexpr int V = 16 / sizeof(TB);
   int64_t chunks = std::min<int64_t>(kMaxChunks, std::max<int64_t>(1, (M + 63) / 64));
   const int64_t rpc = (M + chunks - 1) / chunks;
   chunks = (M + rpc - 1) / rpc;
-  const dim3 grid((d + 255) / 256, (unsigned)chunks);
+  const dim3 grid((d / V + 255) / 256, (unsigned)chunks);
   BW_RUN("bwd_reduce", launch_pdl(coldot_kernel<TB>, grid, dim3(256), 0, c.stream, M, d, A, Bv,
                                   idx, seqT, n, w, rpc, part));
   BW_RUN("bwd_reduce", launch_pdl(colsum_kernel, dim3((d + 255) / 256), dim3(256), 0, c.stream,
@@ -829,8 +907,8 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_gate, d, gu, 2 * F, false));
   BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_up, d, gu + F, 2 * F, false));
   {
-    const int64_t tot = (int64_t)M * F;
-    const unsigned blk = (unsigned)std::min<int64_t>((tot + 255) / 256, 4096);
+    const int64_t tot = (int64_t)M * F / (16 / sizeof(E));
+    const unsigned blk = (unsigned)std::min<int64_t>((tot + 255) / 256, 8192);
     BW_RUN("swiglu", launch_pdl(swiglu_fwd_kernel<E>, dim3(blk), dim3(256), 0, c.stream,
                                 (int64_t)M, F, (const E*)gu, H));
   }
@@ -890,8 +968,8 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, F, d, df, d, tW, d, dH, F, true));
   E* dGU = (E*)bat(ws, L.dGU);
   {
-    const int64_t tot = (int64_t)M * F;
-    const unsigned blk = (unsigned)std::min<int64_t>((tot + 255) / 256, 4096);
+    const int64_t tot = (int64_t)M * F / (16 / sizeof(E));
+    const unsigned blk = (unsigned)std::min<int64_t>((tot + 255) / 256, 8192);
     BW_RUN("swiglu", launch_pdl(swiglu_bwd_kernel<E>, dim3(blk), dim3(256), 0, c.stream,
                                 (int64_t)M, F, (const E*)gu, (const float*)dH, dGU));
   }
