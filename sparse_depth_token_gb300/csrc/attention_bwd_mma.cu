@@ -73,6 +73,34 @@ __device__ __forceinline__ void am_load_tile(__nv_bfloat16* dst, const __nv_bflo
   }
 }
 
+// Asynchronous copies (cp.async): 16 bytes, or 4; an invalid source is zero-filled (no
+// bytes read; the address given is still a valid one).
+__device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(am_smem(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp4(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(am_smem(dst)), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// am_load_tile with asynchronous copies (complete at the caller's cp_wait).
+template <int HD>
+__device__ __forceinline__ void am_load_tile_async(__nv_bfloat16* dst, const __nv_bfloat16* src,
+                                                   int64_t ld, int r0, int n, int col0) {
+  constexpr int P = HD + 8, V = HD / 8;
+  for (int e = threadIdx.x; e < AM_T * V; e += AM_WARPS * 32) {
+    const int r = e / V, v = e - r * V;
+    const bool ok = r0 + r < n;
+    cp16(dst + r * P + 8 * v, src + (ok ? (int64_t)(r0 + r) * ld + col0 + 8 * v : 0), ok);
+  }
+}
+
 // A fragments of the 16 rows [row0, row0 + 16) x columns [k0, k0 + 16) of a [.][P] tile.
 template <int P>
 __device__ __forceinline__ void am_lda(const __nv_bfloat16* s, int row0, int k0,
@@ -166,16 +194,27 @@ attn_bwd_q_mma(const AmArgs p) {
   extern __shared__ __align__(16) unsigned char am_raw[];
   __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(am_raw);
   __nv_bfloat16* dOs = Qs + AM_T * P;
-  __nv_bfloat16* Ks = dOs + AM_T * P;
-  __nv_bfloat16* Vs = Ks + AM_T * P;
+  __nv_bfloat16* Kb = dOs + AM_T * P;   // two key tiles
+  __nv_bfloat16* Vb = Kb + 2 * AM_T * P;   // two value tiles
   const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int g = h / (p.hq / p.hkv);
   const int qw = p.hq * HD, kw = p.hkv * HD;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q0 = qt * AM_T;
   const __nv_bfloat16* base = p.qkv + (int64_t)b * p.n * p.ldq;
-  am_load_tile<HD>(Qs, base, p.ldq, q0, p.n, h * HD);
-  am_load_tile<HD>(dOs, p.dO + (int64_t)b * p.n * qw, qw, q0, p.n, h * HD);
+  // Key tiles 0..qt (pass 1: keys only), then again with values (pass 2): item i loads
+  // into buffer i % 2 while item i - 1 is computed.
+  const int items = 2 * (qt + 1);
+  auto issue = [&](int it) {
+    const int kt = it <= qt ? it : it - qt - 1, buf = it & 1;
+    am_load_tile_async<HD>(Kb + buf * AM_T * P, base, p.ldq, kt * AM_T, p.n, qw + g * HD);
+    if (it > qt)
+      am_load_tile_async<HD>(Vb + buf * AM_T * P, base, p.ldq, kt * AM_T, p.n, qw + kw + g * HD);
+    cp_commit();
+  };
+  am_load_tile_async<HD>(Qs, base, p.ldq, q0, p.n, h * HD);
+  am_load_tile_async<HD>(dOs, p.dO + (int64_t)b * p.n * qw, qw, q0, p.n, h * HD);
+  issue(0);
   // D_i = <dO_i, o_i>: four lanes per row of this warp's 16 (rows lane/4 and lane/4 + 8
   // are this lane's rows in the MMA fragments)
   float Dr[2];
@@ -201,8 +240,9 @@ attn_bwd_q_mma(const AmArgs p) {
   float mr[2] = {-INFINITY, -INFINITY}, lr[2] = {0.0f, 0.0f};
   for (int kt = 0; kt <= qt; ++kt) {
     const int k0 = kt * AM_T;
-    __syncthreads();
-    am_load_tile<HD>(Ks, base, p.ldq, k0, p.n, qw + g * HD);
+    const __nv_bfloat16* Ks = Kb + (kt & 1) * AM_T * P;
+    issue(kt + 1);   // the next item exists: pass 2 follows
+    cp_wait<1>();
     __syncthreads();
     float s[8][4];
     am_qk<HD>(Qs, warp * 16, Ks, s);
@@ -236,6 +276,7 @@ attn_bwd_q_mma(const AmArgs p) {
         mr[hr] = mn;
       }
     }
+    __syncthreads();   // this buffer is refilled by the item after next
   }
   float lse2[2];   // log2-sum-exp2 of the scaled logits
 #pragma unroll
@@ -252,10 +293,15 @@ attn_bwd_q_mma(const AmArgs p) {
 #pragma unroll
   for (int j = 0; j < HD / 8; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = 0.0f;
   for (int kt = 0; kt <= qt; ++kt) {
-    const int k0 = kt * AM_T;
-    __syncthreads();
-    am_load_tile<HD>(Ks, base, p.ldq, k0, p.n, qw + g * HD);
-    am_load_tile<HD>(Vs, base, p.ldq, k0, p.n, qw + kw + g * HD);
+    const int k0 = kt * AM_T, it = qt + 1 + kt;
+    const __nv_bfloat16* Ks = Kb + (it & 1) * AM_T * P;
+    const __nv_bfloat16* Vs = Vb + (it & 1) * AM_T * P;
+    if (it + 1 < items) {
+      issue(it + 1);
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
+    }
     __syncthreads();
     float s[8][4], dp[8][4];
     am_qk<HD>(Qs, warp * 16, Ks, s);
@@ -272,6 +318,7 @@ attn_bwd_q_mma(const AmArgs p) {
         s[j][e] = pr * (dp[j][e] - Dr[hr]);   // dS
       }
     am_pv<HD>(s, Ks, dq);
+    __syncthreads();
   }
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
@@ -294,54 +341,74 @@ attn_bwd_kv_mma(const AmArgs p) {
   extern __shared__ __align__(16) unsigned char am_raw[];
   __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(am_raw);
   __nv_bfloat16* Vs = Ks + AM_T * P;
-  __nv_bfloat16* Qs = Vs + AM_T * P;
-  __nv_bfloat16* dOs = Qs + AM_T * P;
-  float* lse_s = reinterpret_cast<float*>(dOs + AM_T * P);
-  float* D_s = lse_s + AM_T;
+  __nv_bfloat16* Qb = Vs + AM_T * P;        // two query tiles
+  __nv_bfloat16* dOb = Qb + 2 * AM_T * P;   // two dO tiles
+  float* lse_b = reinterpret_cast<float*>(dOb + 2 * AM_T * P);   // [2][AM_T]
+  float* D_b = lse_b + 2 * AM_T;                                   // [2][AM_T]
   const int kt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = p.hq / p.hkv;
   const int qw = p.hq * HD, kw = p.hkv * HD;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int k0 = kt * AM_T;
   const __nv_bfloat16* base = p.qkv + (int64_t)b * p.n * p.ldq;
-  am_load_tile<HD>(Ks, base, p.ldq, k0, p.n, qw + g * HD);
-  am_load_tile<HD>(Vs, base, p.ldq, k0, p.n, qw + kw + g * HD);
+  // items: (query head of the group, query tile at or after the key tile); item i loads
+  // into buffer i % 2 while item i - 1 is computed
+  const int nq = (p.n - k0 + AM_T - 1) / AM_T;
+  const int items = G * nq;
+  auto issue = [&](int it) {
+    const int h = g * G + it / nq, q0 = k0 + (it % nq) * AM_T, buf = it & 1;
+    am_load_tile_async<HD>(Qb + buf * AM_T * P, base, p.ldq, q0, p.n, h * HD);
+    am_load_tile_async<HD>(dOb + buf * AM_T * P, p.dO + (int64_t)b * p.n * qw, qw, q0, p.n,
+                           h * HD);
+    for (int i = threadIdx.x; i < AM_T; i += AM_WARPS * 32) {
+      const int qi = q0 + i;
+      const bool ok = qi < p.n;
+      const int64_t o = ok ? ((int64_t)b * p.n + qi) * p.hq + h : 0;
+      cp4(lse_b + buf * AM_T + i, p.lse + o, ok);
+      cp4(D_b + buf * AM_T + i, p.Dd + o, ok);
+    }
+    cp_commit();
+  };
+  am_load_tile_async<HD>(Ks, base, p.ldq, k0, p.n, qw + g * HD);
+  am_load_tile_async<HD>(Vs, base, p.ldq, k0, p.n, qw + kw + g * HD);
+  issue(0);
   const float sl2 = p.scale * 1.4426950408889634f;
   float dk[HD / 8][4], dv[HD / 8][4];
 #pragma unroll
   for (int j = 0; j < HD / 8; ++j)
 #pragma unroll
     for (int e = 0; e < 4; ++e) dk[j][e] = dv[j][e] = 0.0f;
-  for (int hh = 0; hh < G; ++hh) {
-    const int h = g * G + hh;
-    for (int q0 = k0; q0 < p.n; q0 += AM_T) {
-      __syncthreads();
-      am_load_tile<HD>(Qs, base, p.ldq, q0, p.n, h * HD);
-      am_load_tile<HD>(dOs, p.dO + (int64_t)b * p.n * qw, qw, q0, p.n, h * HD);
-      for (int i = threadIdx.x; i < AM_T; i += AM_WARPS * 32) {
-        const int qi = q0 + i;
-        lse_s[i] = qi < p.n ? p.lse[((int64_t)b * p.n + qi) * p.hq + h] : 0.0f;
-        D_s[i] = qi < p.n ? p.Dd[((int64_t)b * p.n + qi) * p.hq + h] : 0.0f;
-      }
-      __syncthreads();
-      float s[8][4], dp[8][4];
-      am_qk<HD>(Ks, warp * 16, Qs, s);    // S^T: rows keys, columns queries
-      am_qk<HD>(Vs, warp * 16, dOs, dp);  // dP^T
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int kj = k0 + warp * 16 + (lane >> 2) + 8 * (e >> 1);
-          const int ci = j * 8 + (lane & 3) * 2 + (e & 1);   // query within the tile
-          const int qi = q0 + ci;
-          const bool ok = qi < p.n && kj < p.n && kj <= qi;
-          const float pr = ok ? exp2f(s[j][e] * sl2 - lse_s[ci]) : 0.0f;
-          s[j][e] = pr;
-          dp[j][e] = pr * (dp[j][e] - D_s[ci]);   // dS^T
-        }
-      am_pv<HD>(s, dOs, dv);
-      am_pv<HD>(dp, Qs, dk);
+  for (int it = 0; it < items; ++it) {
+    const int q0 = k0 + (it % nq) * AM_T, buf = it & 1;
+    const __nv_bfloat16* Qs = Qb + buf * AM_T * P;
+    const __nv_bfloat16* dOs = dOb + buf * AM_T * P;
+    const float* lse_s = lse_b + buf * AM_T;
+    const float* D_s = D_b + buf * AM_T;
+    if (it + 1 < items) {
+      issue(it + 1);
+      cp_wait<1>();
+    } else {
+      cp_wait<0>();
     }
+    __syncthreads();
+    float s[8][4], dp[8][4];
+    am_qk<HD>(Ks, warp * 16, Qs, s);    // S^T: rows keys, columns queries
+    am_qk<HD>(Vs, warp * 16, dOs, dp);  // dP^T
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int kj = k0 + warp * 16 + (lane >> 2) + 8 * (e >> 1);
+        const int ci = j * 8 + (lane & 3) * 2 + (e & 1);   // query within the tile
+        const int qi = q0 + ci;
+        const bool ok = qi < p.n && kj < p.n && kj <= qi;
+        const float pr = ok ? exp2f(s[j][e] * sl2 - lse_s[ci]) : 0.0f;
+        s[j][e] = pr;
+        dp[j][e] = pr * (dp[j][e] - D_s[ci]);   // dS^T
+      }
+    am_pv<HD>(s, dOs, dv);
+    am_pv<HD>(dp, Qs, dk);
+    __syncthreads();   // this buffer is refilled by the item after next
   }
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
@@ -362,8 +429,8 @@ attn_bwd_kv_mma(const AmArgs p) {
 template <int HD>
 cudaError_t launch_am(int B, const AmArgs& a, cudaStream_t st) {
   constexpr int P = HD + 8;
-  const size_t smq = sizeof(__nv_bfloat16) * 4 * AM_T * P;
-  const size_t smk = smq + sizeof(float) * 2 * AM_T;
+  const size_t smq = sizeof(__nv_bfloat16) * 6 * AM_T * P;
+  const size_t smk = smq + sizeof(float) * 4 * AM_T;
   cudaFuncSetAttribute(attn_bwd_q_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
   cudaFuncSetAttribute(attn_bwd_kv_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
   const int tiles = (a.n + AM_T - 1) / AM_T;
