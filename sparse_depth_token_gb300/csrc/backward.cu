@@ -60,25 +60,34 @@ __device__ __forceinline__ float softplus_f(float z) {
 
 // ---------------------------------------------------------------- transpose
 // out[c, r] = in[r, c] for r < R, c < C; out[c, r] = 0 for R <= r < Rpad (zero tokens).
+// 64 x 64 tiles, 256 threads: each thread moves 16 elements, all loads in flight.
+constexpr int TR_T = 64;
+
 template <typename T>
-__global__ void transpose_kernel(int R, int Rpad, int C, const T* __restrict__ in, int64_t ldi,
-                                 T* __restrict__ out, int64_t ldo) {
+__global__ void __launch_bounds__(256)
+transpose_kernel(int R, int Rpad, int C, const T* __restrict__ in, int64_t ldi,
+                 T* __restrict__ out, int64_t ldo) {
   pdl_trigger();
   pdl_wait();
-  __shared__ T tile[32][33];
-  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  __shared__ T tile[TR_T][TR_T + 1];
+  const int r0 = blockIdx.y * TR_T, c0 = blockIdx.x * TR_T;
   const int tx = threadIdx.x, ty = threadIdx.y;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int r = r0 + ty + 8 * k, c = c0 + tx;
-    tile[ty + 8 * k][tx] = (r < R && c < C) ? in[(int64_t)r * ldi + c] : Elem<T>::from_f(0.0f);
-  }
+  for (int k = 0; k < TR_T / 8; ++k)
+#pragma unroll
+    for (int h = 0; h < TR_T; h += 32) {
+      const int r = r0 + ty + 8 * k, c = c0 + tx + h;
+      tile[ty + 8 * k][tx + h] =
+          (r < R && c < C) ? in[(int64_t)r * ldi + c] : Elem<T>::from_f(0.0f);
+    }
   __syncthreads();
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int c = c0 + ty + 8 * k, r = r0 + tx;
-    if (c < C && r < Rpad) out[(int64_t)c * ldo + r] = tile[tx][ty + 8 * k];
-  }
+  for (int k = 0; k < TR_T / 8; ++k)
+#pragma unroll
+    for (int h = 0; h < TR_T; h += 32) {
+      const int c = c0 + ty + 8 * k, r = r0 + tx + h;
+      if (c < C && r < Rpad) out[(int64_t)c * ldo + r] = tile[tx + h][ty + 8 * k];
+    }
 }
 
 // ---------------------------------------------------------------- gated residual backward
@@ -214,6 +223,7 @@ coldot_kernel(int64_t M, int d, const float* __restrict__ A, const TB* __restric
   float acc[V];
 #pragma unroll
   for (int k = 0; k < V; ++k) acc[k] = 0.0f;
+#pragma unroll 8
   for (int64_t m = m0; m < m1; ++m) {
     const int64_t row = idx ? bw_stream_row(m, seqT, n, idx) : m;
     const Vec16<TB> bv = ld_vec(Bv + row * d + c);
@@ -236,16 +246,28 @@ coldot_kernel(int64_t M, int d, const float* __restrict__ A, const TB* __restric
   for (int k = 0; k < V; ++k) part[(int64_t)blockIdx.y * d + c + k] = acc[k];
 }
 
-// out[c] = sum over chunks k (in order) of part[k, c].
-__global__ void colsum_kernel(int nchunks, int d, const float* __restrict__ part,
-                              float* __restrict__ out) {
+// out[c] = sum over chunks k of part[k, c] in a fixed order: a CTA of 32 x 32 threads
+// serves 32 columns; thread (x, y) sums the chunks k = y, y + 32, ... of column x in
+// order, then the 32 partial sums are added in order of y.
+__global__ void __launch_bounds__(1024)
+colsum_kernel(int nchunks, int d, const float* __restrict__ part, float* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= d) return;
+  __shared__ float sh[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + tx;
   float acc = 0.0f;
-  for (int k = 0; k < nchunks; ++k) acc += part[(int64_t)k * d + c];
-  out[c] = acc;
+  if (c < d) {
+#pragma unroll 4
+    for (int k = ty; k < nchunks; k += 32) acc += part[(int64_t)k * d + c];
+  }
+  sh[ty][tx] = acc;
+  __syncthreads();
+  if (ty == 0 && c < d) {
+    float t = 0.0f;
+    for (int y = 0; y < 32; ++y) t += sh[y][tx];
+    out[c] = t;
+  }
 }
 
 // out[0] = scale * sum of in[0 .. n): each thread sums a fixed strided subset in order,
@@ -654,7 +676,7 @@ struct BwLayout {
       dae, dH, dGU, dv2, dh, da, dO, lse, Dd, dqkv, du, rstd1, rstd2, tA, tB, tW, part, total;
 };
 
-constexpr int kMaxChunks = 512;   // row chunks of the column reductions
+constexpr int kMaxChunks = 1024;   // row chunks of the column reductions
 
 BwLayout bw_layout(const xmod_dims* dm) {
   BwLayout L{};
@@ -723,7 +745,7 @@ template <typename T>
 cudaError_t transpose_t(const Ctx& c, int R, int Rpad, int C, const void* in, int64_t ldi,
                         void* out, int64_t ldo) {
   if (R <= 0 || C <= 0) return cudaSuccess;
-  const dim3 grid((C + 31) / 32, (Rpad + 31) / 32);
+  const dim3 grid((C + TR_T - 1) / TR_T, (Rpad + TR_T - 1) / TR_T);
   return launch_pdl(transpose_kernel<T>, grid, dim3(32, 8), 0, c.stream, R, Rpad, C,
                     (const T*)in, ldi, (T*)out, ldo);
 }
@@ -757,13 +779,13 @@ template <typename TB>
 int bw_coldot(const Ctx& c, int64_t M, int d, const float* A, const TB* Bv, const int32_t* idx,
               int seqT, int n, const float* w, float* part, float* out) {
   constexpr int V = 16 / sizeof(TB);
-  int64_t chunks = std::min<int64_t>(kMaxChunks, std::max<int64_t>(1, (M + 63) / 64));
+  int64_t chunks = std::min<int64_t>(kMaxChunks, std::max<int64_t>(1, (M + 15) / 16));
   const int64_t rpc = (M + chunks - 1) / chunks;
   chunks = (M + rpc - 1) / rpc;
   const dim3 grid((d / V + 255) / 256, (unsigned)chunks);
   BW_RUN("bwd_reduce", launch_pdl(coldot_kernel<TB>, grid, dim3(256), 0, c.stream, M, d, A, Bv,
                                   idx, seqT, n, w, rpc, part));
-  BW_RUN("bwd_reduce", launch_pdl(colsum_kernel, dim3((d + 255) / 256), dim3(256), 0, c.stream,
+  BW_RUN("bwd_reduce", launch_pdl(colsum_kernel, dim3((d + 31) / 32), dim3(1024), 0, c.stream,
                                   (int)chunks, d, (const float*)part, out));
   return XMOD_OK;
 }
