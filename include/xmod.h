@@ -1,5 +1,6 @@
 /*
- * xmod.h -- C ABI of the X-MoD / MoD sparse-depth layer forward pass on one GPU.
+ * xmod.h -- C ABI of the X-MoD / MoD sparse-depth layer stack on one GPU (forward, and
+ * the backward of dense and sparse layers for training).
  *
  * The method (page "X-MoD: Practical Scaling Laws for Sparse-Depth Routing Beyond
  * Mixture-of-Depths", reading notes): every sparse layer scores each token with a
@@ -300,6 +301,28 @@ XMOD_API int xmod_layer_bwd(const xmod_dims* dims, xmod_layer_kind kind, int K, 
                             const void* dy, float route_coef, void* dx,
                             const xmod_layer_grads* grads, void* ws, size_t ws_bytes,
                             void* stream);
+
+/* Backward of the Eq. 3 stack, for training: every layer's input is recomputed with
+ * xmod_layer_fwd (the layer-by-layer forward, equal bit for bit to xmod_stack_fwd) into
+ * `checkpoints` ([n_layers, B, T, d], dtype; checkpoint l = the input of layer l), then
+ * xmod_layer_bwd runs from the last layer to the first, each layer's dx becoming the dy
+ * of the layer before it.
+ *   x, bias, K, A, N0, N1, gate, layers, n_layers: as for xmod_stack_fwd (x is not
+ *             modified; every sparse layer uses the same bias)
+ *   dy        [B, T, d]  the gradient at the stack's output (dtype)
+ *   route_coef the Eq. 9 coefficient of every sparse layer
+ *   dx        [B, T, d]  out: the gradient at the stack's input; may not alias x, dy or
+ *             the checkpoints
+ *   grads     host array of n_layers xmod_layer_grads, layer order (device arrays,
+ *             overwritten; as for xmod_layer_bwd)
+ *   ws        at least xmod_stack_bwd_workspace_bytes(dims, K) bytes */
+XMOD_API size_t xmod_stack_bwd_workspace_bytes(const xmod_dims* dims, int K);
+
+XMOD_API int xmod_stack_bwd(const xmod_dims* dims, int K, double A, int N0, int N1,
+                            xmod_gate gate, const xmod_layer_weights* layers, int n_layers,
+                            const void* x, const float* bias, const void* dy, float route_coef,
+                            void* dx, const xmod_layer_grads* grads, void* checkpoints,
+                            void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- allocation-free routing
  * The paper has no counterpart to this entry point: it exists for callers that

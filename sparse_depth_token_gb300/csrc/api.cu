@@ -890,6 +890,76 @@ int xmod_layer_bwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate g
                        g, ws);
 }
 
+// The stack backward's workspace: one region the forward recompute and then the
+// backward use in turn (both keep the status word at offset 0), then two gradient
+// buffers [B, T, d] that the layers' dy / dx alternate between.
+static size_t stack_bwd_region(const xmod_dims* dm, int K) {
+  const size_t f = layout(dm, K).total, b = bwd_workspace_bytes(dm);
+  return align_up(f > b ? f : b);
+}
+
+size_t xmod_stack_bwd_workspace_bytes(const xmod_dims* dm, int K) {
+  if (!dims_ok(dm) || K <= 0 || K > dm->T) return 0;
+  const size_t g = align_up(esize(dm->dtype) * (size_t)dm->B * dm->T * dm->d);
+  return stack_bwd_region(dm, K) + 2 * g;
+}
+
+int xmod_stack_bwd(const xmod_dims* dm, int K, double A, int N0, int N1, xmod_gate gate,
+                   const xmod_layer_weights* layers, int n_layers, const void* x,
+                   const float* bias, const void* dy, float route_coef, void* dx,
+                   const xmod_layer_grads* grads, void* checkpoints, void* ws, size_t ws_bytes,
+                   void* stream) {
+  if (!dims_ok(dm) || K <= 0 || K > dm->T || N0 < 0 || N1 < 0 || !layers || !grads)
+    return XMOD_ERR_INVALID_ARG;
+  if (!isfinite(A) || A <= 0) return XMOD_ERR_INVALID_ARG;
+  const double akd = A * (double)K;
+  const long AK = lround(akd);
+  if (AK < 1 || fabs(akd - (double)AK) > 1e-9) return XMOD_ERR_INVALID_ARG;
+  if (n_layers < 1 || (long)n_layers != (long)N0 + (long)N1 * (AK + 1))
+    return XMOD_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(dx) || !aligned16(checkpoints) ||
+      !aligned16_or_null(bias))
+    return XMOD_ERR_INVALID_ARG;
+  const size_t sz = esize(dm->dtype) * (size_t)dm->B * dm->T * dm->d;
+  const char* ck = (const char*)checkpoints;
+  if (dx == x || dx == dy || ((const char*)dx + sz > ck && (const char*)dx < ck + sz * n_layers))
+    return XMOD_ERR_INVALID_ARG;
+  if (!aligned16(ws) || ws_bytes < xmod_stack_bwd_workspace_bytes(dm, K))
+    return XMOD_ERR_WORKSPACE;
+  const size_t region = stack_bwd_region(dm, K);
+  char* gbuf[2] = {(char*)ws + region, (char*)ws + region + align_up(sz)};
+  cudaStream_t st = (cudaStream_t)stream;
+  auto kind_of = [&](int l) {
+    return (l >= N0 && ((l - N0) % (AK + 1)) < AK) ? XMOD_LAYER_SPARSE : XMOD_LAYER_DENSE;
+  };
+  // forward: checkpoint l is the input of layer l
+  char* ckp = (char*)checkpoints;
+  if (cudaMemcpyAsync(ckp, x, sz, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return XMOD_ERR_CUDA;
+  for (int l = 0; l + 1 < n_layers; ++l) {
+    char* nxt = ckp + sz * (l + 1);
+    if (cudaMemcpyAsync(nxt, ckp + sz * l, sz, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+      return XMOD_ERR_CUDA;
+    const int k = kind_of(l);
+    const int r = xmod_layer_fwd(dm, (xmod_layer_kind)k, K, gate, &layers[l], nxt,
+                                 k == XMOD_LAYER_SPARSE ? bias : nullptr, nullptr, nullptr, ws,
+                                 region, stream);
+    if (r) return r;
+  }
+  // backward, last layer first
+  const void* g = dy;
+  for (int l = n_layers - 1; l >= 0; --l) {
+    void* out = l == 0 ? dx : (void*)gbuf[l & 1];
+    const int k = kind_of(l);
+    const int r = xmod_layer_bwd(dm, (xmod_layer_kind)k, K, gate, &layers[l], ckp + sz * l,
+                                 k == XMOD_LAYER_SPARSE ? bias : nullptr, g, route_coef, out,
+                                 &grads[l], ws, region, stream);
+    if (r) return r;
+    g = out;
+  }
+  return XMOD_OK;
+}
+
 int xmod_layer_fwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate gate,
                    const xmod_layer_weights* w, void* x_inout, const float* bias,
                    int32_t* idx_out, float* r_sel_out, void* ws, size_t ws_bytes, void* stream) {

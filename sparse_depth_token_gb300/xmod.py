@@ -24,7 +24,8 @@ EXPORTS = ("xmod_version", "xmod_status_string", "xmod_workspace_bytes", "xmod_r
            "xmod_gated_scatter", "xmod_layer_fwd", "xmod_stack_fwd", "xmod_launch_count",
            "xmod_profile_enable", "xmod_profile_read", "xmod_router_topk_noalloc",
            "xmod_stack_fwd_ex", "xmod_layer_fwd_threshold", "xmod_stack_fwd_sched",
-           "xmod_bwd_workspace_bytes", "xmod_layer_bwd")
+           "xmod_bwd_workspace_bytes", "xmod_layer_bwd", "xmod_stack_bwd_workspace_bytes",
+           "xmod_stack_bwd")
 
 # Largest B*T the allocation-free router entry point accepts (its fixed scratch).
 NOALLOC_MAX_TOKENS = 2 * 1024 * 1024
@@ -132,6 +133,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     L.xmod_layer_bwd.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                  ctypes.POINTER(LayerWeights), _VP, _VP, _VP, ctypes.c_float,
                                  _VP, ctypes.POINTER(LayerGrads), _VP, ctypes.c_size_t, _VP]
+    L.xmod_stack_bwd_workspace_bytes.restype = ctypes.c_size_t
+    L.xmod_stack_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Dims), ctypes.c_int]
+    L.xmod_stack_bwd.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_double,
+                                 ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                 ctypes.POINTER(LayerWeights), ctypes.c_int, _VP, _VP, _VP,
+                                 ctypes.c_float, _VP, ctypes.POINTER(LayerGrads), _VP, _VP,
+                                 ctypes.c_size_t, _VP]
     _lib = L
     return L
 
@@ -316,3 +324,19 @@ def layer_bwd(dm, kind, K, gate, w: LayerWeights, x, bias, dy, route_coef, dx, g
     _check("xmod_layer_bwd", load().xmod_layer_bwd(
         ctypes.byref(dm), int(kind), int(K), int(gate), ctypes.byref(w), _p(x), _p(bias), _p(dy),
         float(route_coef), _p(dx), ctypes.byref(grads), _p(ws), _wsb(ws), _stream(stream)))
+
+
+def stack_bwd_workspace_bytes(dm: Dims, K: int) -> int:
+    return int(load().xmod_stack_bwd_workspace_bytes(ctypes.byref(dm), int(K)))
+
+
+def stack_bwd(dm, K, A, N0, N1, gate, layers, x, bias, dy, route_coef, dx, grads, checkpoints,
+              ws, stream=None):
+    """xmod_stack_bwd: the Eq. 3 stack's backward; grads is a list of LayerGrads (one per
+    layer), checkpoints a device buffer [n_layers, B, T, d]."""
+    arr = (LayerWeights * len(layers))(*layers)
+    garr = (LayerGrads * len(grads))(*grads)
+    _check("xmod_stack_bwd", load().xmod_stack_bwd(
+        ctypes.byref(dm), int(K), float(A), int(N0), int(N1), int(gate), arr, len(layers), _p(x),
+        _p(bias), _p(dy), float(route_coef), _p(dx), garr, _p(checkpoints), _p(ws), _wsb(ws),
+        _stream(stream)))

@@ -112,3 +112,112 @@ def test_layer_bwd_bf16_tensor_core(X, T, K, kind, gate, coef):
     w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=T, K=K, d=256, hq=4, hkv=2, F=512, seed=31,
                                          weight_std=0.02 * np.sqrt(1536 / 256))
     _run(X, w, kind, gate, coef, seed=40 + T + K)
+
+
+def _grad_set(w, n_layers):
+    qw, kw = w.hq * w.hd, w.hkv * w.hd
+    shapes = {"w_router": (w.d,), "rms1": (w.d,), "wq": (qw, w.d), "wk": (kw, w.d),
+              "wv": (kw, w.d), "wo": (w.d, qw), "rms2": (w.d,), "w_gate": (w.F, w.d),
+              "w_up": (w.F, w.d), "w_down": (w.d, w.F), "varsigma": (4,), "route_loss": (4,)}
+    return [{k: torch.full(v, float("nan"), dtype=torch.float32, device="cuda")
+             for k, v in shapes.items()} for _ in range(n_layers)]
+
+
+def _stack_case(X, w):
+    from oracle import structure as S
+    layers = I.all_layer_weights(w)
+    kinds = S.schedule(w.N0, w.N1, w.A, w.K)
+    bias = I.router_bias(w)
+    x = I.residual_stream(w)
+    x, _ = U.enforce_routing_margin(x, w.dtype, layers[kinds.index(S.SPARSE)]["w_r"], bias, w.K)
+    g = np.random.default_rng(77)
+    dyf = g.standard_normal((w.B, w.T, w.d)).astype(np.float32)
+    dy = I.f32_to_bf16_bits(dyf) if w.dtype == "bf16" else dyf
+    abi = [X.layer_weights(dev_layer(l, w.dtype), l["varsigma"]) for l in layers]
+    return layers, kinds, bias, x, dy, abi
+
+
+def test_stack_bwd_fp32_tiny_against_oracle(X):
+    """xmod_stack_bwd on the tiny fp32 stack (Dense + 4 Sparse(4) + Dense) against the
+    oracle's layer backward chained from the last layer to the first on the oracle's own
+    forward layer inputs."""
+    w = I.WORKLOADS["tiny_fp32"]
+    layers, kinds, bias, x, dy, abi = _stack_case(X, w)
+    coef = 0.3
+    dm = xmod_dims(w)
+    ws = torch.zeros(X.stack_bwd_workspace_bytes(dm, w.K), dtype=torch.uint8, device="cuda")
+    ck = torch.empty((len(kinds), w.B, w.T, w.d), dtype=torch.float32, device="cuda")
+    xd, dyd = to_dev(x, "fp32"), to_dev(dy, "fp32")
+    dx = torch.empty_like(xd)
+    gd = _grad_set(w, len(kinds))
+    X.reset_status(ws)
+    X.stack_bwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, xd, torch.from_numpy(bias).cuda(), dyd,
+                coef, dx, [X.layer_grads(g) for g in gd], ck, ws)
+    assert X.sync_status(ws) == X.OK
+    od = U_dims(w)
+    ol = [oracle_layer(l, "fp32") for l in layers]
+    xs = [I.to_f64(x, "fp32")]
+    for l, kind in enumerate(kinds[:-1]):
+        xs.append(O.layer_fwd(od, kind, w.K, w.gate, ol[l], xs[-1],
+                              bias=bias if kind == O.SPARSE else None)["y"])
+    g = I.to_f64(dy, "fp32")
+    for l in range(len(kinds) - 1, -1, -1):
+        kind = kinds[l]
+        r = O.layer_bwd(od, kind, w.K, w.gate, ol[l], xs[l], g,
+                        bias=bias if kind == O.SPARSE else None, route_coef=coef)
+        for on, an in GRAD_NAMES.items():
+            if kind == O.DENSE and on == "w_r":
+                continue
+            _check(gd[l][an].cpu().numpy(), r["grads"][on], "fp32", f"layer {l} d{on}")
+        g = r["dx"]
+    _check(from_dev(dx, "fp32"), g, "fp32", "stack dx")
+
+
+def test_stack_bwd_bf16_equals_layer_chain(X):
+    """bf16 (tensor-core path): xmod_stack_bwd equals, bit for bit, xmod_layer_fwd
+    checkpoints followed by xmod_layer_bwd chained by hand."""
+    w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=256, A=1, n_layers=9, d=256, hq=4, hkv=2,
+                                         F=512, seed=5, weight_std=0.02 * np.sqrt(1536 / 256))
+    layers, kinds, bias, x, dy, abi = _stack_case(X, w)
+    coef = 1e-2
+    dm = xmod_dims(w)
+    bd = torch.from_numpy(bias).cuda()
+    ws = torch.zeros(X.stack_bwd_workspace_bytes(dm, w.K), dtype=torch.uint8, device="cuda")
+    ck = torch.empty((len(kinds), w.B, w.T, w.d), dtype=torch.bfloat16, device="cuda")
+    xd, dyd = to_dev(x, "bf16"), to_dev(dy, "bf16")
+    dx = torch.empty_like(xd)
+    gd = _grad_set(w, len(kinds))
+    X.reset_status(ws)
+    X.stack_bwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, xd, bd, dyd, coef, dx,
+                [X.layer_grads(g) for g in gd], ck, ws)
+    assert X.sync_status(ws) == X.OK
+    # by hand
+    wsf = torch.zeros(X.workspace_bytes(dm, w.K), dtype=torch.uint8, device="cuda")
+    wsb = torch.zeros(X.bwd_workspace_bytes(dm, w.K), dtype=torch.uint8, device="cuda")
+    xs = [xd.clone()]
+    for l, kind in enumerate(kinds[:-1]):
+        nxt = xs[-1].clone()
+        X.layer_fwd(dm, kind, w.K, w.gate, abi[l], nxt, bd if kind == X.LAYER_SPARSE else None,
+                    None, None, wsf)
+        xs.append(nxt)
+    for l in range(len(kinds)):
+        assert torch.equal(ck[l].view(torch.int16), xs[l].view(torch.int16)), f"checkpoint {l}"
+    g = dyd
+    hand = _grad_set(w, len(kinds))
+    for l in range(len(kinds) - 1, -1, -1):
+        out = torch.empty_like(xd)
+        X.layer_bwd(dm, kinds[l], w.K, w.gate, abi[l], xs[l],
+                    bd if kinds[l] == X.LAYER_SPARSE else None, g, coef, out,
+                    X.layer_grads(hand[l]), wsb)
+        g = out
+    assert X.sync_status(wsb) == X.OK
+    assert torch.equal(dx.view(torch.int16), g.view(torch.int16))
+    for l in range(len(kinds)):
+        for k in ("w_router", "rms1", "wq", "wk", "wv", "wo", "rms2", "w_gate", "w_up", "w_down",
+                  "varsigma"):
+            if kinds[l] == X.LAYER_DENSE and k == "w_router":
+                continue
+            a, b = gd[l][k], hand[l][k]
+            if k == "varsigma":
+                a, b = a[:1], b[:1]
+            assert torch.equal(a, b), f"layer {l} {k}"
