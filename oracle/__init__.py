@@ -38,7 +38,7 @@ class LayerW(ctypes.Structure):
 
 class LayerGrad(ctypes.Structure):
     _fields_ = [(n, _DP) for n in ("w_r", "g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")] + [
-        ("varsigma", ctypes.c_double)]
+        ("varsigma", ctypes.c_double), ("gq", _DP), ("gk", _DP)]
 
 
 _lib = None
@@ -271,8 +271,13 @@ def layer_bwd(dm: Dims, kind, K, gate, layer: Layer, x, dy, bias=None, idx_force
     qw, kw = dm.hq * dm.hd, dm.hkv * dm.hd
     shapes = {"w_r": (d,), "g1": (d,), "wq": (qw, d), "wk": (kw, d), "wv": (kw, d),
               "wo": (d, qw), "g2": (d,), "wg": (dm.F, d), "wu": (dm.F, d), "wd": (d, dm.F)}
+    for k in ("gq", "gk"):   # QK-norm gains, when the layer has them
+        if k in layer.arrays:
+            shapes[k] = (dm.hd,)
     grads = {k: np.zeros(v) for k, v in shapes.items()}
-    gs = LayerGrad(*[grads[k].ctypes.data_as(_DP) for k in shapes], 0.0)
+    main = ("w_r", "g1", "wq", "wk", "wv", "wo", "g2", "wg", "wu", "wd")
+    gs = LayerGrad(*[grads[k].ctypes.data_as(_DP) for k in main], 0.0,
+                   *[grads[k].ctypes.data_as(_DP) if k in grads else None for k in ("gq", "gk")])
     dx = np.empty_like(x)
     n = T // K if kind == SPARSE else 1
     idx = np.zeros((B, n), np.int32)

@@ -47,10 +47,12 @@ typedef struct {
   double rope_theta;
 } oracle_layer_w;
 
-// Gradients, shaped as the weights; every array is overwritten.
+// Gradients, shaped as the weights; every array is overwritten. gq, gk [hd] (the
+// QK-norm gains' gradients) may be NULL when the layer has no QK-norm.
 typedef struct {
   double *w_r, *g1, *wq, *wk, *wv, *wo, *g2, *wg, *wu, *wd;
   double varsigma;
+  double *gq, *gk;
 } oracle_layer_grad;
 
 // forward helpers of xmod_oracle.cpp
@@ -58,6 +60,8 @@ void oracle_router(int64_t rows, int d, const double* x, const double* w_r,
                    const double* bias, double* s, double* r);
 int oracle_topk(int B, int T, int k, const double* s, int32_t* idx);
 void oracle_linear(int64_t rows, int in, int out, const double* x, const double* W, double* y);
+void oracle_qk_transform(int rows, int heads, int hd, double* x, const double* gain, double eps,
+                         double theta, const int32_t* pos);
 
 }  // extern "C"
 
@@ -118,10 +122,50 @@ void linear_dx(int n, int in, int out, const double* dy, const double* W, double
     }
 }
 
+// Backward of the QK-norm and rotation of oracle_qk_transform (z = R(p) (v rho g) per
+// head vector v of hd, rho = (mean(v^2) + eps)^(-1/2), R(p) rotating the pairs
+// (c, c + hd/2) by the angle p * theta^(-2c/hd)): dz [rows, heads * hd] becomes dv in
+// place (R is orthogonal: its transpose rotates back); the gain gradient is added to
+// dgain [hd].
+void qk_bwd(int rows, int heads, int hd, const double* pre, const double* gain, double eps,
+            double theta, const int32_t* pos, double* dz, double* dgain) {
+  const int half = hd / 2;
+  for (int i = 0; i < rows; ++i) {
+    const double p = pos ? (double)pos[i] : (double)i;
+    for (int h = 0; h < heads; ++h) {
+      const double* v = pre + ((int64_t)i * heads + h) * hd;
+      double* g = dz + ((int64_t)i * heads + h) * hd;
+      if (theta > 0.0)
+        for (int c = 0; c < half; ++c) {
+          const double ang = p * std::pow(theta, -2.0 * c / hd);
+          const double cs = std::cos(ang), sn = std::sin(ang);
+          const double a = g[c], b = g[c + half];
+          g[c] = a * cs + b * sn;
+          g[c + half] = -a * sn + b * cs;
+        }
+      if (gain) {
+        double ss = 0.0;
+        for (int c = 0; c < hd; ++c) ss += v[c] * v[c];
+        const double rho = 1.0 / std::sqrt(ss / hd + eps);
+        double dot = 0.0;
+        for (int c = 0; c < hd; ++c) dot += g[c] * gain[c] * v[c] * rho;
+        const double mean = dot / hd;
+        for (int c = 0; c < hd; ++c) {
+          const double vh = v[c] * rho;
+          if (dgain) dgain[c] += g[c] * vh;
+          g[c] = rho * (g[c] * gain[c] - vh * mean);
+        }
+      }
+    }
+  }
+}
+
 // The block's backward on one sequence's compact rows xs [n, d], given the gradients
 // reaching its two residuals, da_ext and df [n, d]. Adds to dxs [n, d] and to gw.
+// Compact row j sits at original position pos[j] (NULL: j), which only the rotation sees.
 void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_layer_w* w,
-               const double* da_ext, const double* df, double* dxs, oracle_layer_grad* gw) {
+               const double* da_ext, const double* df, double* dxs, oracle_layer_grad* gw,
+               const int32_t* pos) {
   const int d = dm->d, hq = dm->hq, hkv = dm->hkv, hd = dm->hd, F = dm->F;
   const int G = hq / hkv, qw = hq * hd, kw = hkv * hd;
   const double scale = 1.0 / std::sqrt((double)hd);
@@ -132,6 +176,15 @@ void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_laye
   oracle_linear(n, d, qw, u.data(), w->wq, q.data());
   oracle_linear(n, d, kw, u.data(), w->wk, k.data());
   oracle_linear(n, d, kw, u.data(), w->wv, v.data());
+  // QK-norm and rotation at the original positions, the projections kept for the backward
+  const bool extras = w->gq || w->gk || w->rope_theta > 0.0;
+  std::vector<double> q_pre, k_pre;
+  if (extras) {
+    q_pre = q;
+    k_pre = k;
+    oracle_qk_transform(n, hq, hd, q.data(), w->gq, dm->eps, w->rope_theta, pos);
+    oracle_qk_transform(n, hkv, hd, k.data(), w->gk, dm->eps, w->rope_theta, pos);
+  }
   // P[h][i][j], causal (j <= i), and o
   std::vector<double> P((int64_t)hq * n * n, 0.0), o((int64_t)n * qw, 0.0);
   for (int h = 0; h < hq; ++h) {
@@ -222,6 +275,10 @@ void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_laye
       }
     }
   }
+  if (extras) {   // back through the rotation and the QK-norm
+    qk_bwd(n, hq, hd, q_pre.data(), w->gq, dm->eps, w->rope_theta, pos, dq.data(), gw->gq);
+    qk_bwd(n, hkv, hd, k_pre.data(), w->gk, dm->eps, w->rope_theta, pos, dk.data(), gw->gk);
+  }
   // ---- q, k, v = u W^T
   linear_dw(n, d, qw, dq.data(), u.data(), gw->wq);
   linear_dw(n, d, kw, dk.data(), u.data(), gw->wk);
@@ -236,15 +293,15 @@ void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_laye
 
 // a and f of the block on compact rows xs [n, d] (all rows), for the gate derivatives.
 void block_af(const oracle_dims* dm, int n, const double* xs, const oracle_layer_w* w,
-              double* a_out, double* f_out);
+              double* a_out, double* f_out, const int32_t* pos);
 
 }  // namespace
 
 extern "C" {
 
-void oracle_block_rows(const oracle_dims* dm, int n, const double* xs,
-                       const oracle_layer_w* w, const int32_t* rows, int nrows,
-                       double* a_out, double* f_out);
+void oracle_block_rows_pos(const oracle_dims* dm, int n, const double* xs,
+                           const oracle_layer_w* w, const int32_t* rows, int nrows,
+                           double* a_out, double* f_out, const int32_t* pos);
 
 // Backward of one layer (kind DENSE or SPARSE; Eq. 7 or Eq. 6 gating), see the file
 // comment. x_in, dy, dx [B, T, d]; bias [B, T] or NULL; idx_force [B, n] or NULL (the
@@ -258,7 +315,7 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
   const int qw = dm->hq * dm->hd, kw = dm->hkv * dm->hd;
   if (B <= 0 || T <= 0 || d <= 0 || dm->hq % dm->hkv) return BAD_ARG;
   if (kind != DENSE && kind != SPARSE) return BAD_ARG;
-  if (w->gq || w->gk || w->rope_theta > 0.0) return BAD_ARG;   // forward extras: not here
+  if ((w->gq && !gw->gq) || (w->gk && !gw->gk)) return BAD_ARG;
   const int64_t BT = (int64_t)B * T;
   std::memset(gw->w_r, 0, sizeof(double) * d);
   std::memset(gw->g1, 0, sizeof(double) * d);
@@ -271,6 +328,8 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
   std::memset(gw->wu, 0, sizeof(double) * (int64_t)F * d);
   std::memset(gw->wd, 0, sizeof(double) * (int64_t)d * F);
   gw->varsigma = 0.0;
+  if (gw->gq) std::memset(gw->gq, 0, sizeof(double) * dm->hd);
+  if (gw->gk) std::memset(gw->gk, 0, sizeof(double) * dm->hd);
   if (route_loss) *route_loss = 0.0;
   // the skip path: y = x + (residual) for every token
   std::memcpy(dx, dy, sizeof(double) * BT * d);
@@ -279,7 +338,7 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
     for (int b = 0; b < B; ++b) {
       const double* xb = x_in + (int64_t)b * T * d;
       const double* gb = dy + (int64_t)b * T * d;
-      block_bwd(dm, T, xb, w, gb, gb, dx + (int64_t)b * T * d, gw);
+      block_bwd(dm, T, xb, w, gb, gb, dx + (int64_t)b * T * d, gw, nullptr);
     }
     return OK;
   }
@@ -315,7 +374,7 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
     std::vector<double> xs((int64_t)n * d), a((int64_t)n * d), f((int64_t)n * d);
     for (int j = 0; j < n; ++j)
       std::memcpy(&xs[(int64_t)j * d], x_in + ((int64_t)b * T + ib[j]) * d, sizeof(double) * d);
-    block_af(dm, n, xs.data(), w, a.data(), f.data());
+    block_af(dm, n, xs.data(), w, a.data(), f.data(), ib);
     std::vector<double> da_ext((int64_t)n * d), df((int64_t)n * d), dxs((int64_t)n * d, 0.0);
     for (int j = 0; j < n; ++j) {
       const int64_t t = (int64_t)b * T + ib[j];
@@ -336,7 +395,7 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
       }
       ds[t] += dr * rt * (1.0 - rt);
     }
-    block_bwd(dm, n, xs.data(), w, da_ext.data(), df.data(), dxs.data(), gw);
+    block_bwd(dm, n, xs.data(), w, da_ext.data(), df.data(), dxs.data(), gw, ib);
     for (int j = 0; j < n; ++j)   // the gather's backward: back to the token's row
       for (int c = 0; c < d; ++c) dx[((int64_t)b * T + ib[j]) * d + c] += dxs[(int64_t)j * d + c];
   }
@@ -355,7 +414,7 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
 
 namespace {
 void block_af(const oracle_dims* dm, int n, const double* xs, const oracle_layer_w* w,
-              double* a_out, double* f_out) {
-  oracle_block_rows(dm, n, xs, w, nullptr, n, a_out, f_out);
+              double* a_out, double* f_out, const int32_t* pos) {
+  oracle_block_rows_pos(dm, n, xs, w, nullptr, n, a_out, f_out, pos);
 }
 }  // namespace

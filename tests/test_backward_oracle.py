@@ -5,8 +5,9 @@ in test_oracle_pins.py): for J = sum(dy * y) + route_coef * L_route (Eq. 9 of th
 notes, section "top-k in training, causal threshold at evaluation"), the central
 difference of J along a random direction of x, of every weight and of varsigma must
 equal the inner product of that direction with the returned gradient. The selection is
-held fixed on both sides (forced indices), as the backward holds it. Plus closed forms:
-the skip path of unselected rows, the Eq. 9 value at p = 1/2, an FFN with W_down = 0.
+held fixed on both sides (forced indices), as the backward holds it; with the optional
+QK-norm gains and rotary embedding too. Plus closed forms: the skip path of unselected
+rows, the Eq. 9 value at p = 1/2, an FFN with W_down = 0.
 """
 import numpy as np
 import pytest
@@ -123,3 +124,45 @@ def test_zero_down_projection():
     r = O.layer_bwd(dm, O.SPARSE, K, O.GATE_MOD, O.Layer(W, 1.0), x, dy)
     assert np.all(r["grads"]["wg"] == 0.0) and np.all(r["grads"]["wu"] == 0.0)
     assert np.any(r["grads"]["wd"] != 0.0)
+
+
+@pytest.mark.parametrize("kind,gq,gk,theta", [(O.SPARSE, True, True, 1e4), (O.SPARSE, False, True, 0.0),
+                                              (O.SPARSE, True, False, 500.0),
+                                              (O.DENSE, True, True, 1e4)])
+def test_layer_bwd_qk_norm_rope_matches_finite_differences(kind, gq, gk, theta):
+    """The Qwen3-style extras: QK-norm gains (their own gradients) and the rotary embedding
+    at the tokens' original positions; central differences of the forward oracle along
+    random directions of x, of the projections and of the gains."""
+    g = np.random.default_rng(50 + 2 * kind + int(gq) + int(theta > 0))
+    dm = O.dims(B, T, d, HQ, HKV, HD, F)
+    W = _weights(g)
+    if gq:
+        W["gq"] = 1 + 0.2 * g.standard_normal(HD)
+    if gk:
+        W["gk"] = 1 + 0.2 * g.standard_normal(HD)
+    W["rope_theta"] = theta
+    vs = 1.1
+    x = g.standard_normal((B, T, d))
+    dy = g.standard_normal((B, T, d))
+    bias = 0.1 * g.standard_normal((B, T))
+    r = O.layer_bwd(dm, kind, K, O.GATE_XMOD, O.Layer(W, vs), x, dy, bias=bias, route_coef=0.2)
+    idx = r["idx"]
+    eps = 1e-6
+
+    def J(x_=x, W_=W):
+        return _objective(dm, kind, O.GATE_XMOD, W_, vs, x_, dy, bias, idx, 0.2)
+
+    def check(num, ana, what):
+        assert abs(num - ana) <= 1e-6 * max(1.0, abs(num)), f"{what}: fd {num} vs grad {ana}"
+
+    v = g.standard_normal(x.shape)
+    check((J(x_=x + eps * v) - J(x_=x - eps * v)) / (2 * eps), float((r["dx"] * v).sum()), "x")
+    for name in ("wq", "wk", "wv", "g1", "w_r") + (("gq",) if gq else ()) + (("gk",) if gk else ()):
+        if kind == O.DENSE and name == "w_r":
+            continue
+        v = g.standard_normal(np.shape(W[name]))
+        Wp, Wm = dict(W), dict(W)
+        Wp[name] = W[name] + eps * v
+        Wm[name] = W[name] - eps * v
+        check((J(W_=Wp) - J(W_=Wm)) / (2 * eps), float((r["grads"][name] * v).sum()), name)
+
