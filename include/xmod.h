@@ -285,13 +285,16 @@ XMOD_API int xmod_stack_fwd_sched(const xmod_dims* dims, int K, const int32_t* k
  *             under Eq. 6 and for DENSE); route_loss (one float, NULL allowed)
  *             receives L_route (SPARSE only)
  *   ws        at least xmod_bwd_workspace_bytes(dims, K) bytes
- * The QK-norm / rotary extras and the other layer kinds return XMOD_ERR_UNSUPPORTED.
+ * With the QK-norm / rotary extras the gradient also flows back through them (the
+ * rotation at the tokens' original positions, as in the forward) and q_norm / k_norm
+ * receive the gains' gradients. The other layer kinds return XMOD_ERR_UNSUPPORTED.
  * bf16 runs the projections and their gradients on the tensor cores (bf16 operands,
  * fp32 accumulation, fp32 weight gradients); fp32 runs FFMA kernels throughout. */
 typedef struct {
   float *w_router, *rms1, *wq, *wk, *wv, *wo, *rms2, *w_gate, *w_up, *w_down;
   float* varsigma;
   float* route_loss;
+  float *q_norm, *k_norm;   /* [head_dim] each; required when the layer has that gain */
 } xmod_layer_grads;
 
 XMOD_API size_t xmod_bwd_workspace_bytes(const xmod_dims* dims, int K);

@@ -883,7 +883,9 @@ int xmod_layer_bwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate g
   if (!g->varsigma || (kind == XMOD_LAYER_SPARSE && !aligned16(g->w_router)) ||
       !aligned16_or_null(g->w_router))
     return XMOD_ERR_INVALID_ARG;
-  if (qk_extras(w) || !head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
+  if ((w->q_norm && !aligned16(g->q_norm)) || (w->k_norm && !aligned16(g->k_norm)))
+    return XMOD_ERR_INVALID_ARG;
+  if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
   if (kind == XMOD_LAYER_SPARSE && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
   if (!aligned16(ws) || ws_bytes < bwd_workspace_bytes(dm)) return XMOD_ERR_WORKSPACE;
   return run_layer_bwd((cudaStream_t)stream, dm, kind, K, gate, w, x, bias, dy, route_coef, dx,

@@ -673,7 +673,8 @@ inline int64_t round8(int64_t v) { return (v + 7) / 8 * 8; }
 // Workspace carve-up of the backward; M = B*T rows cover a dense layer.
 struct BwLayout {
   size_t status, s, r, idx, r_sel, dr, dvs, ds, lossp, u, qkv, vt, o, a, h, v2, gu, H, f, df,
-      dae, dH, dGU, dv2, dh, da, dO, lse, Dd, dqkv, du, rstd1, rstd2, tA, tB, tW, part, total;
+      dae, dH, dGU, dv2, dh, da, dO, lse, Dd, dqkv, du, rstd1, rstd2, tA, tB, tW, part, qkpre,
+      dgq, dgk, total;
 };
 
 constexpr int kMaxChunks = 1024;   // row chunks of the column reductions
@@ -724,6 +725,9 @@ BwLayout bw_layout(const xmod_dims* dm) {
   L.tB = take(es * Mp * std::max(std::max(d, F), qw));
   L.tW = take(es * d * std::max(2 * F, qkv_w));
   L.part = take(4 * (size_t)kMaxChunks * std::max(d, (size_t)1));
+  L.qkpre = take(es * M * (qw + kw));   // q | k before the QK-norm / rotation
+  L.dgq = take(4 * M * hd);
+  L.dgk = take(4 * M * hd);
   L.total = off;
   return L;
 }
@@ -869,6 +873,8 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   }
   BW_RUN("gather_rmsnorm",
          launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1, dm->rms_eps, u));
+  const bool extras = w->q_norm || w->k_norm || w->rope_theta > 0.0f;
+  E* qkpre = (E*)bat(ws, L.qkpre);
   const bool tc_attn = tc && attention_tc_supported(hd, n, qkv_w);
   bool v_transposed = false;   // v kept only in its transposed layout (tensor-core path)
   {
@@ -893,7 +899,6 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
       BW_RUN("gemm_qkv", launch_gemm_tc(c, pq, e));
       // the backward also reads v by rows: the v projection once more into the v columns
       BW_RUN("gemm_qkv", bw_gemm(c, dt, M, kw, d, u, d, w->wv, d, qkv + qw + kw, qkv_w, false));
-      BW_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, (int)round8(n), o));
     } else {
       e.vt = nullptr;
       BW_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, qw, d, u, d, w->wq, d, nullptr, e));
@@ -901,10 +906,21 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
       BW_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wk, d, nullptr, e));
       e.out = (char*)qkv + es * (qw + kw);
       BW_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, kw, d, u, d, w->wv, d, nullptr, e));
+    }
+    if (extras) {   // QK-norm and rotation at the original positions, projections kept
+      if (cudaMemcpy2DAsync(qkpre, es * (qw + kw), qkv, es * qkv_w, es * (qw + kw), M,
+                            cudaMemcpyDeviceToDevice, c.stream) != cudaSuccess)
+        return XMOD_ERR_CUDA;
+      BW_RUN("qk_norm_rope", launch_qk_transform(c, dt, M, nullptr, qkv, qkv_w, 0, hq, w->q_norm,
+                                                 qw, hkv, w->k_norm, hd, dm->rms_eps,
+                                                 w->rope_theta, idx, nullptr, n));
+    }
+    if (v_transposed)
+      BW_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, (int)round8(n), o));
+    else
       BW_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w,
                                                 (char*)qkv + es * qw, (char*)qkv + es * (qw + kw),
                                                 qkv_w, o));
-    }
   }
   {
     Epilogue eo;
@@ -1050,6 +1066,24 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     p.ldg = qkv_w;
     p.scale = 1.0f / sqrtf((float)hd);
     BW_RUN("bwd_attention", launch_attn_bwd(c, dt, B, hd, p));
+  }
+
+  if (extras) {   // back through the rotation and the QK-norm to the projections
+    float* dgq = w->q_norm ? (float*)bat(ws, L.dgq) : nullptr;
+    float* dgk = w->k_norm ? (float*)bat(ws, L.dgk) : nullptr;
+    BW_RUN("bwd_rows", launch_qk_transform_bwd(c, dt, M, dqkv, qkv_w, 0, hq, w->q_norm, qw, hkv,
+                                               w->k_norm, qkpre, qw + kw, hd, dm->rms_eps,
+                                               w->rope_theta, idx, n, dgq, dgk));
+    if (dgq) {
+      const int st = bw_coldot<float>(c, M, hd, nullptr, dgq, nullptr, T, n, nullptr, part,
+                                      gr->q_norm);
+      if (st) return st;
+    }
+    if (dgk) {
+      const int st = bw_coldot<float>(c, M, hd, nullptr, dgk, nullptr, T, n, nullptr, part,
+                                      gr->k_norm);
+      if (st) return st;
+    }
   }
 
   // ======== q, k, v = u [Wq | Wk | Wv]^T

@@ -107,6 +107,16 @@ cudaError_t launch_qk_transform(const Ctx& c, xmod_dtype dt, int64_t M, const in
                                 float theta, const int32_t* pos_idx, const int32_t* pos_tok,
                                 int seqT);
 
+// Backward of launch_qk_transform (all M rows): g [M, ld], the gradient at the
+// transformed q (from q_col0) and k (from k_col0) heads, becomes in place the gradient
+// at the projections pre [M, ldp] (q heads from column 0, k heads after them); dgq / dgk
+// [M, hd] fp32 (NULL: no such gain) receive each row's gain gradient over its heads.
+cudaError_t launch_qk_transform_bwd(const Ctx& c, xmod_dtype dt, int64_t M, void* g, int ld,
+                                    int q_col0, int q_heads, const void* q_gain, int k_col0,
+                                    int k_heads, const void* k_gain, const void* pre, int ldp,
+                                    int hd, float eps, float theta, const int32_t* pos_idx,
+                                    int seqT, float* dgq, float* dgk);
+
 // Causal threshold rule over s [B, T] (ranked logit s - bias_step * count >= 0):
 // compact rows tok [<= B*T] (= b * T + t, sequence then position order), r_sel
 // [<= B*T], seq_count [B], seq_off [B] and the total in *M_out (all device).

@@ -1035,6 +1035,128 @@ qk_transform_kernel(int64_t M, const int32_t* __restrict__ M_dev, T* __restrict_
   }
 }
 
+// Backward of qk_transform_kernel (no variable row count): g [M, ld] holds the gradient
+// at the transformed q heads (from q_col0) and k heads (from k_col0); pre [M, ldp] the
+// projections before the transform, the q heads from column 0 and the k heads right
+// after them. g becomes, in place, the gradient at the projections: the rotation is
+// orthogonal, so its gradient rotates back by the same angle; through the QK-norm,
+// rho (dn gain - vhat mean(dn gain vhat)). dgq / dgk [M, HD] (NULL: that gain is absent)
+// receive per row the gain gradient dn * vhat summed over the row's q (k) heads.
+template <typename T, int E>
+__global__ void __launch_bounds__(ROW_WARPS * 32)
+qk_transform_bwd_kernel(int64_t M, T* __restrict__ g, int ld, int q_col0, int q_heads,
+                        const T* __restrict__ q_gain, int k_col0, int k_heads,
+                        const T* __restrict__ k_gain, const T* __restrict__ pre, int ldp,
+                        float eps, double theta, const int32_t* __restrict__ pos_idx, int seqT,
+                        float* __restrict__ dgq, float* __restrict__ dgk) {
+  pdl_trigger();
+  constexpr int HD = 32 * E;
+  __shared__ float2 turns[HD / 2];
+  for (int c = threadIdx.x; c < HD / 2; c += blockDim.x) {
+    const double r = theta > 0.0 ? exp2(-(2.0 * c / HD) * log2(theta)) / 6.283185307179586 : 0.0;
+    const float hi = (float)r;
+    turns[c] = make_float2(hi, (float)(r - (double)hi));
+  }
+  __syncthreads();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
+  if (m >= M) return;
+  const int64_t pos = pos_idx ? pos_idx[m] : m % seqT;
+  const float pf = (float)pos;
+  const bool first = lane < 16;
+  float cs[E], sn[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {   // the forward's angles, computed the same way
+    cs[e] = 1.0f;
+    sn[e] = 0.0f;
+    if (theta > 0.0) {
+      const float2 t = turns[(first ? lane : lane - 16) * E + e];
+      const float a = pf * t.x;
+      const float frac = (a - rintf(a)) + fmaf(pf, t.y, fmaf(pf, t.x, -a));
+      __sincosf(frac * 6.2831853f, &sn[e], &cs[e]);
+    }
+  }
+  float accq[E], acck[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) accq[e] = acck[e] = 0.0f;
+  const int heads = q_heads + k_heads;
+  for (int h = 0; h < heads; ++h) {
+    const bool is_q = h < q_heads;
+    T* gp = g + m * ld + (is_q ? q_col0 + h * HD : k_col0 + (h - q_heads) * HD) + lane * E;
+    const T* vp = pre + m * ldp + h * HD + lane * E;
+    const T* gain = is_q ? q_gain : k_gain;
+    float gv[E], v[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      gv[e] = Elem<T>::to_f(gp[e]);
+      v[e] = Elem<T>::to_f(vp[e]);
+    }
+    if (theta > 0.0) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float other = __shfl_xor_sync(0xffffffffu, gv[e], 16);
+        gv[e] = first ? gv[e] * cs[e] + other * sn[e] : gv[e] * cs[e] - other * sn[e];
+      }
+    }
+    if (gain) {
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
+      const float rho = rsqrtf(warp_sum(ss) / (float)HD + eps);
+      float dot = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) dot += gv[e] * Elem<T>::to_f(gain[lane * E + e]) * v[e] * rho;
+      const float mean = warp_sum(dot) / (float)HD;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float vh = v[e] * rho;
+        if (is_q) accq[e] += gv[e] * vh;
+        else acck[e] += gv[e] * vh;
+        gv[e] = rho * (gv[e] * Elem<T>::to_f(gain[lane * E + e]) - vh * mean);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) gp[e] = Elem<T>::from_f(gv[e]);
+  }
+  if (dgq)
+#pragma unroll
+    for (int e = 0; e < E; ++e) dgq[m * HD + lane * E + e] = accq[e];
+  if (dgk)
+#pragma unroll
+    for (int e = 0; e < E; ++e) dgk[m * HD + lane * E + e] = acck[e];
+}
+
+cudaError_t launch_qk_transform_bwd(const Ctx& c, xmod_dtype dt, int64_t M, void* g, int ld,
+                                    int q_col0, int q_heads, const void* q_gain, int k_col0,
+                                    int k_heads, const void* k_gain, const void* pre, int ldp,
+                                    int hd, float eps, float theta, const int32_t* pos_idx,
+                                    int seqT, float* dgq, float* dgk) {
+  if (M <= 0 || q_heads + k_heads <= 0) return cudaSuccess;
+  if (hd % 32 || hd > 128 || seqT <= 0 || seqT >= (1 << 24)) return cudaErrorInvalidValue;
+  const unsigned blocks = (unsigned)((M + ROW_WARPS - 1) / ROW_WARPS);
+#define XMOD_QKB_CASE(TT, EE)                                                                 \
+  return launch_pdl(qk_transform_bwd_kernel<TT, EE>, dim3(blocks), dim3(ROW_WARPS * 32), 0,    \
+                    c.stream, M, (TT*)g, ld, q_col0, q_heads, (const TT*)q_gain, k_col0,       \
+                    k_heads, (const TT*)k_gain, (const TT*)pre, ldp, eps, (double)theta,       \
+                    pos_idx, seqT, dgq, dgk);
+  if (dt == XMOD_BF16) {
+    switch (hd / 32) {
+      case 1: XMOD_QKB_CASE(__nv_bfloat16, 1)
+      case 2: XMOD_QKB_CASE(__nv_bfloat16, 2)
+      case 4: XMOD_QKB_CASE(__nv_bfloat16, 4)
+    }
+  } else {
+    switch (hd / 32) {
+      case 1: XMOD_QKB_CASE(float, 1)
+      case 2: XMOD_QKB_CASE(float, 2)
+      case 4: XMOD_QKB_CASE(float, 4)
+    }
+  }
+#undef XMOD_QKB_CASE
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_qk_transform(const Ctx& c, xmod_dtype dt, int64_t M, const int32_t* M_dev,
                                 void* x, int ld, int q_col0, int q_heads, const void* q_gain,
                                 int k_col0, int k_heads, const void* k_gain, int hd, float eps,

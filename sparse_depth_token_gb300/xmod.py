@@ -53,7 +53,7 @@ class LayerWeights(ctypes.Structure):
 
 class LayerGrads(ctypes.Structure):
     NAMES = ("w_router", "rms1", "wq", "wk", "wv", "wo", "rms2", "w_gate", "w_up", "w_down",
-             "varsigma", "route_loss")
+             "varsigma", "route_loss", "q_norm", "k_norm")
     _fields_ = [(n, ctypes.c_void_p) for n in NAMES]
 
 

@@ -42,9 +42,17 @@ def _check(got, ref, dtype, what):
             f"{what}: rel-L2 {rl:.2e}, max-abs/max|ref| {mr:.2e}"
 
 
-def _run(X, w: I.Workload, kind, gate, route_coef, seed):
+def _run(X, w: I.Workload, kind, gate, route_coef, seed, extras=None):
     lw = I.layer_weights(w, 0)
     lw["varsigma"] = 0.9
+    theta = 0.0
+    if extras:   # QK-norm gains (non-trivial) and the rotary base
+        ge = np.random.default_rng(seed + 1)
+        for k in ("gq", "gk"):
+            gains = (1 + 0.2 * ge.standard_normal(w.hd)).astype(np.float32)
+            lw[k] = I.f32_to_bf16_bits(gains) if w.dtype == "bf16" else gains
+        theta = extras
+        lw["rope_theta"] = theta
     bias = I.router_bias(w)
     x = I.residual_stream(w)
     if kind == X.LAYER_SPARSE:
@@ -54,13 +62,15 @@ def _run(X, w: I.Workload, kind, gate, route_coef, seed):
     dy = I.f32_to_bf16_bits(dyf) if w.dtype == "bf16" else dyf
     dm = xmod_dims(w)
     ws = torch.zeros(X.bwd_workspace_bytes(dm, w.K), dtype=torch.uint8, device="cuda")
-    abi = X.layer_weights(dev_layer(lw, w.dtype), lw["varsigma"])
+    abi = X.layer_weights(dev_layer(lw, w.dtype), lw["varsigma"], theta)
     xd, dyd = to_dev(x, w.dtype), to_dev(dy, w.dtype)
     dx = torch.empty_like(xd)
     qw, kw = w.hq * w.hd, w.hkv * w.hd
     shapes = {"w_router": (w.d,), "rms1": (w.d,), "wq": (qw, w.d), "wk": (kw, w.d),
               "wv": (kw, w.d), "wo": (w.d, qw), "rms2": (w.d,), "w_gate": (w.F, w.d),
               "w_up": (w.F, w.d), "w_down": (w.d, w.F), "varsigma": (4,), "route_loss": (4,)}
+    if extras:
+        shapes["q_norm"] = shapes["k_norm"] = (w.hd,)
     gd = {k: torch.full(v, float("nan"), dtype=torch.float32, device="cuda")
           for k, v in shapes.items()}
     X.reset_status(ws)
@@ -75,6 +85,9 @@ def _run(X, w: I.Workload, kind, gate, route_coef, seed):
             assert torch.all(gd[an] == 0)
             continue
         _check(gd[an].cpu().numpy(), ref["grads"][on], w.dtype, f"d{on}")
+    if extras:
+        _check(gd["q_norm"].cpu().numpy(), ref["grads"]["gq"], w.dtype, "dq_norm")
+        _check(gd["k_norm"].cpu().numpy(), ref["grads"]["gk"], w.dtype, "dk_norm")
     vs = float(gd["varsigma"][0])
     if kind == X.LAYER_SPARSE and gate == X.GATE_XMOD:
         _check(np.array([vs]), np.array([ref["varsigma"]]), w.dtype, "dvarsigma")
@@ -112,6 +125,19 @@ def test_layer_bwd_bf16_tensor_core(X, T, K, kind, gate, coef):
     w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=T, K=K, d=256, hq=4, hkv=2, F=512, seed=31,
                                          weight_std=0.02 * np.sqrt(1536 / 256))
     _run(X, w, kind, gate, coef, seed=40 + T + K)
+
+
+@pytest.mark.parametrize("dtype,kind,T", [("fp32", 1, 64), ("fp32", 0, 64), ("bf16", 1, 256),
+                                          ("bf16", 0, 160)])
+def test_layer_bwd_qk_norm_rope(X, dtype, kind, T):
+    """With QK-norm gains and the rotary embedding (base 1e4) at the tokens' original
+    positions: dx, every weight gradient and the two gains' gradients."""
+    if dtype == "fp32":
+        w = I.WORKLOADS["tiny_fp32"].replace(T=T)
+    else:
+        w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=T, K=4, d=256, hq=4, hkv=2, F=512, seed=33,
+                                             weight_std=0.02 * np.sqrt(1536 / 256))
+    _run(X, w, kind, X.GATE_XMOD, 0.1, seed=60 + T + kind, extras=1e4)
 
 
 def _grad_set(w, n_layers):
