@@ -259,7 +259,8 @@ def layer_fwd(dm: Dims, kind, K, gate, layer: Layer, x, bias=None, idx_force=Non
 
 def layer_bwd(dm: Dims, kind, K, gate, layer: Layer, x, dy, bias=None, idx_force=None,
               route_coef=0.0):
-    """Backward of one layer (DENSE or SPARSE) for the objective sum(dy * y) + route_coef *
+    """Backward of one layer (DENSE, SPARSE, or the FullAttn / Routed-FFN halves ATTN, RFFN)
+    for the objective sum(dy * y) + route_coef *
     L_route (Eq. 9 on the layer's top-(T/K) decisions), the selection held fixed.
     Returns dict(dx, grads {name: array shaped as the weight}, varsigma, route_loss, idx)."""
     x, xp = _d(x)
@@ -279,14 +280,15 @@ def layer_bwd(dm: Dims, kind, K, gate, layer: Layer, x, dy, bias=None, idx_force
     gs = LayerGrad(*[grads[k].ctypes.data_as(_DP) for k in main], 0.0,
                    *[grads[k].ctypes.data_as(_DP) if k in grads else None for k in ("gq", "gk")])
     dx = np.empty_like(x)
-    n = T // K if kind == SPARSE else 1
+    routed = kind in (SPARSE, RFFN)
+    n = T // K if routed else 1
     idx = np.zeros((B, n), np.int32)
     loss = ctypes.c_double(0.0)
     _check(lib().oracle_layer_bwd(ctypes.byref(dm), kind, K, gate, ctypes.byref(layer.struct),
                                   xp, bp, fp, gp, float(route_coef), dx.ctypes.data_as(_DP),
                                   ctypes.byref(gs), idx.ctypes.data_as(_IP), ctypes.byref(loss)))
     return {"dx": dx, "grads": grads, "varsigma": gs.varsigma, "route_loss": loss.value,
-            "idx": idx if kind == SPARSE else None}
+            "idx": idx if routed else None}
 
 
 TOPK, THRESHOLD = 0, 1

@@ -62,13 +62,15 @@ int oracle_topk(int B, int T, int k, const double* s, int32_t* idx);
 void oracle_linear(int64_t rows, int in, int out, const double* x, const double* W, double* y);
 void oracle_qk_transform(int rows, int heads, int hd, double* x, const double* gain, double eps,
                          double theta, const int32_t* pos);
+void oracle_ffn_rows(const oracle_dims* dm, int nr, const double* xs, const oracle_layer_w* w,
+                     double* f_out);
 
 }  // extern "C"
 
 namespace {
 
 enum { OK = 0, BAD_ARG = -1 };
-enum { DENSE = 0, SPARSE = 1 };
+enum { DENSE = 0, SPARSE = 1, ATTN = 2, RFFN = 3 };
 enum { GATE_XMOD = 0, GATE_MOD = 1 };
 
 double sigmoid(double z) { return 1.0 / (1.0 + std::exp(-z)); }
@@ -163,22 +165,28 @@ void qk_bwd(int rows, int heads, int hd, const double* pre, const double* gain, 
 // The block's backward on one sequence's compact rows xs [n, d], given the gradients
 // reaching its two residuals, da_ext and df [n, d]. Adds to dxs [n, d] and to gw.
 // Compact row j sits at original position pos[j] (NULL: j), which only the rotation sees.
+// attn / ffn select the halves (X-MoD notes, "mechanism controls": a FullAttn layer is the
+// attention half with its residual, a Routed-FFN layer the FFN half on RMSNorm(xs) g2, i.e.
+// a = 0); both: the whole block.
 void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_layer_w* w,
                const double* da_ext, const double* df, double* dxs, oracle_layer_grad* gw,
-               const int32_t* pos) {
+               const int32_t* pos, bool attn = true, bool ffn = true) {
   const int d = dm->d, hq = dm->hq, hkv = dm->hkv, hd = dm->hd, F = dm->F;
   const int G = hq / hkv, qw = hq * hd, kw = hkv * hd;
   const double scale = 1.0 / std::sqrt((double)hd);
   // ---- forward, keeping what the backward reads
   std::vector<double> u((int64_t)n * d), x1((int64_t)n * d), rho1(n);
-  rms_fwd(n, d, xs, w->g1, dm->eps, u.data(), x1.data(), rho1.data());
   std::vector<double> q((int64_t)n * qw), k((int64_t)n * kw), v((int64_t)n * kw);
+  std::vector<double> q_pre, k_pre;
+  std::vector<double> P, o;
+  std::vector<double> a((int64_t)n * d, 0.0), hh((int64_t)n * d);
+  const bool extras = w->gq || w->gk || w->rope_theta > 0.0;
+  if (attn) {
+  rms_fwd(n, d, xs, w->g1, dm->eps, u.data(), x1.data(), rho1.data());
   oracle_linear(n, d, qw, u.data(), w->wq, q.data());
   oracle_linear(n, d, kw, u.data(), w->wk, k.data());
   oracle_linear(n, d, kw, u.data(), w->wv, v.data());
   // QK-norm and rotation at the original positions, the projections kept for the backward
-  const bool extras = w->gq || w->gk || w->rope_theta > 0.0;
-  std::vector<double> q_pre, k_pre;
   if (extras) {
     q_pre = q;
     k_pre = k;
@@ -186,7 +194,8 @@ void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_laye
     oracle_qk_transform(n, hkv, hd, k.data(), w->gk, dm->eps, w->rope_theta, pos);
   }
   // P[h][i][j], causal (j <= i), and o
-  std::vector<double> P((int64_t)hq * n * n, 0.0), o((int64_t)n * qw, 0.0);
+  P.assign((int64_t)hq * n * n, 0.0);
+  o.assign((int64_t)n * qw, 0.0);
   for (int h = 0; h < hq; ++h) {
     const int g = h / G;
     for (int i = 0; i < n; ++i) {
@@ -212,9 +221,11 @@ void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_laye
       }
     }
   }
-  std::vector<double> a((int64_t)n * d), hh((int64_t)n * d);
   oracle_linear(n, qw, d, o.data(), w->wo, a.data());
+  }
   for (int64_t i = 0; i < (int64_t)n * d; ++i) hh[i] = xs[i] + a[i];
+  std::vector<double> dh((int64_t)n * d, 0.0);
+  if (ffn) {
   std::vector<double> v2((int64_t)n * d), x2((int64_t)n * d), rho2(n);
   rms_fwd(n, d, hh.data(), w->g2, dm->eps, v2.data(), x2.data(), rho2.data());
   std::vector<double> Gp((int64_t)n * F), Up((int64_t)n * F), H((int64_t)n * F);
@@ -238,13 +249,12 @@ void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_laye
   linear_dx(n, d, F, dG.data(), w->wg, dv2.data());
   linear_dx(n, d, F, dU.data(), w->wu, dv2.data());
   // ---- v2 = RMSNorm(h) g2, h = xs + a
-  std::vector<double> dh((int64_t)n * d, 0.0);
   rms_bwd(n, d, dv2.data(), w->g2, x2.data(), rho2.data(), dh.data(), gw->g2);
-  std::vector<double> da((int64_t)n * d);
-  for (int64_t i = 0; i < (int64_t)n * d; ++i) {
-    da[i] = dh[i] + da_ext[i];
-    dxs[i] += dh[i];
   }
+  for (int64_t i = 0; i < (int64_t)n * d; ++i) dxs[i] += dh[i];
+  if (!attn) return;
+  std::vector<double> da((int64_t)n * d);
+  for (int64_t i = 0; i < (int64_t)n * d; ++i) da[i] = dh[i] + da_ext[i];
   // ---- a = o Wo^T
   linear_dw(n, qw, d, da.data(), o.data(), gw->wo);
   std::vector<double> dO((int64_t)n * qw, 0.0);
@@ -314,7 +324,7 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
   const int B = dm->B, T = dm->T, d = dm->d, F = dm->F;
   const int qw = dm->hq * dm->hd, kw = dm->hkv * dm->hd;
   if (B <= 0 || T <= 0 || d <= 0 || dm->hq % dm->hkv) return BAD_ARG;
-  if (kind != DENSE && kind != SPARSE) return BAD_ARG;
+  if (kind != DENSE && kind != SPARSE && kind != ATTN && kind != RFFN) return BAD_ARG;
   if ((w->gq && !gw->gq) || (w->gk && !gw->gk)) return BAD_ARG;
   const int64_t BT = (int64_t)B * T;
   std::memset(gw->w_r, 0, sizeof(double) * d);
@@ -334,11 +344,12 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
   // the skip path: y = x + (residual) for every token
   std::memcpy(dx, dy, sizeof(double) * BT * d);
 
-  if (kind == DENSE) {   // y = x + a + f on every token: da_ext = df = dy
+  if (kind == DENSE || kind == ATTN) {   // y = x + a + f (or x + a) on every token
     for (int b = 0; b < B; ++b) {
       const double* xb = x_in + (int64_t)b * T * d;
       const double* gb = dy + (int64_t)b * T * d;
-      block_bwd(dm, T, xb, w, gb, gb, dx + (int64_t)b * T * d, gw, nullptr);
+      block_bwd(dm, T, xb, w, gb, gb, dx + (int64_t)b * T * d, gw, nullptr, true,
+                kind == DENSE);
     }
     return OK;
   }
@@ -374,7 +385,10 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
     std::vector<double> xs((int64_t)n * d), a((int64_t)n * d), f((int64_t)n * d);
     for (int j = 0; j < n; ++j)
       std::memcpy(&xs[(int64_t)j * d], x_in + ((int64_t)b * T + ib[j]) * d, sizeof(double) * d);
-    block_af(dm, n, xs.data(), w, a.data(), f.data(), ib);
+    if (kind == RFFN)   // FFN half only: f = FFN(RMSNorm(xs) g2), a = 0
+      oracle_ffn_rows(dm, n, xs.data(), w, f.data());
+    else
+      block_af(dm, n, xs.data(), w, a.data(), f.data(), ib);
     std::vector<double> da_ext((int64_t)n * d), df((int64_t)n * d), dxs((int64_t)n * d, 0.0);
     for (int j = 0; j < n; ++j) {
       const int64_t t = (int64_t)b * T + ib[j];
@@ -395,7 +409,8 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
       }
       ds[t] += dr * rt * (1.0 - rt);
     }
-    block_bwd(dm, n, xs.data(), w, da_ext.data(), df.data(), dxs.data(), gw, ib);
+    block_bwd(dm, n, xs.data(), w, da_ext.data(), df.data(), dxs.data(), gw, ib, kind != RFFN,
+              true);
     for (int j = 0; j < n; ++j)   // the gather's backward: back to the token's row
       for (int c = 0; c < d; ++c) dx[((int64_t)b * T + ib[j]) * d + c] += dxs[(int64_t)j * d + c];
   }

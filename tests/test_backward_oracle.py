@@ -33,7 +33,7 @@ def _weights(g, scale=0.3):
 def _objective(dm, kind, gate, W, vs, x, dy, bias, idx, coef):
     out = O.layer_fwd(dm, kind, K, gate, O.Layer(W, vs), x, bias=bias, idx_force=idx)
     val = float((dy * out["y"]).sum())
-    if kind == O.SPARSE and coef:
+    if kind in (O.SPARSE, O.RFFN) and coef:
         s = out["s"]
         p = 1.0 / (1.0 + np.exp(-s))
         q = np.zeros_like(s)
@@ -165,4 +165,40 @@ def test_layer_bwd_qk_norm_rope_matches_finite_differences(kind, gq, gk, theta):
         Wp[name] = W[name] + eps * v
         Wm[name] = W[name] - eps * v
         check((J(W_=Wp) - J(W_=Wm)) / (2 * eps), float((r["grads"][name] * v).sum()), name)
+
+
+@pytest.mark.parametrize("kind,gate,coef", [(O.ATTN, O.GATE_XMOD, 0.0), (O.RFFN, O.GATE_XMOD, 0.4),
+                                            (O.RFFN, O.GATE_MOD, 0.0)])
+def test_variant_layer_bwd_matches_finite_differences(kind, gate, coef):
+    """The mechanism controls' halves: FullAttn (attention on every token, y = x + a) and
+    Routed-FFN (the FFN half on the top-(T/K) tokens with a = 0 in the gated residual)."""
+    g = np.random.default_rng(70 + kind + gate)
+    dm = O.dims(B, T, d, HQ, HKV, HD, F)
+    W = _weights(g)
+    vs = 0.9
+    x = g.standard_normal((B, T, d))
+    dy = g.standard_normal((B, T, d))
+    bias = 0.1 * g.standard_normal((B, T))
+    r = O.layer_bwd(dm, kind, K, gate, O.Layer(W, vs), x, dy, bias=bias, route_coef=coef)
+    idx = r["idx"]
+    eps = 1e-6
+
+    def J(x_=x, W_=W, vs_=vs):
+        return _objective(dm, kind, gate, W_, vs_, x_, dy, bias, idx, coef)
+
+    def check(num, ana, what):
+        assert abs(num - ana) <= 1e-6 * max(1.0, abs(num)), f"{what}: fd {num} vs grad {ana}"
+
+    v = g.standard_normal(x.shape)
+    check((J(x_=x + eps * v) - J(x_=x - eps * v)) / (2 * eps), float((r["dx"] * v).sum()), "x")
+    for name in NAMES:
+        v = g.standard_normal(W[name].shape)
+        Wp, Wm = dict(W), dict(W)
+        Wp[name] = W[name] + eps * v
+        Wm[name] = W[name] - eps * v
+        check((J(W_=Wp) - J(W_=Wm)) / (2 * eps), float((r["grads"][name] * v).sum()), name)
+    check((J(vs_=vs + eps) - J(vs_=vs - eps)) / (2 * eps), r["varsigma"], "varsigma")
+    unused = ("g2", "wg", "wu", "wd", "w_r") if kind == O.ATTN else ("g1", "wq", "wk", "wv", "wo")
+    for name in unused:
+        assert np.all(r["grads"][name] == 0.0), name
 
