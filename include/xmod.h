@@ -261,7 +261,7 @@ XMOD_API int xmod_stack_fwd_sched(const xmod_dims* dims, int K, const int32_t* k
                                   void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- backward of one layer
- * The gradient of one DENSE or SPARSE layer (Eq. 7 or Eq. 6 gating) for training: for
+ * The gradient of one layer (Eq. 7 or Eq. 6 gating) for training: for
  * the layer y = layer(x) of xmod_layer_fwd and a caller-given upstream gradient dy,
  * the call returns the gradients of the scalar
  *     J = sum(dy * y) + route_coef * L_route
@@ -287,7 +287,10 @@ XMOD_API int xmod_stack_fwd_sched(const xmod_dims* dims, int K, const int32_t* k
  *   ws        at least xmod_bwd_workspace_bytes(dims, K) bytes
  * With the QK-norm / rotary extras the gradient also flows back through them (the
  * rotation at the tokens' original positions, as in the forward) and q_norm / k_norm
- * receive the gains' gradients. The other layer kinds return XMOD_ERR_UNSUPPORTED.
+ * receive the gains' gradients. The mechanism controls' halves are differentiated too:
+ * ATTN (y = x + a on every token) and ROUTED_FFN (the FFN half on the top-(T/K) tokens
+ * with a = 0 in the gated residual); the gradients of the weights a kind does not use
+ * may be NULL and are zeroed when given. SPARSE_FULLKV returns XMOD_ERR_UNSUPPORTED.
  * bf16 runs the projections and their gradients on the tensor cores (bf16 operands,
  * fp32 accumulation, fp32 weight gradients); fp32 runs FFMA kernels throughout. */
 typedef struct {

@@ -870,23 +870,30 @@ int xmod_layer_bwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate g
                    float route_coef, void* dx, const xmod_layer_grads* g, void* ws,
                    size_t ws_bytes, void* stream) {
   if (!dims_ok(dm) || K <= 0 || K > dm->T) return XMOD_ERR_INVALID_ARG;
-  if (kind != XMOD_LAYER_DENSE && kind != XMOD_LAYER_SPARSE) return XMOD_ERR_UNSUPPORTED;
+  if (kind != XMOD_LAYER_DENSE && kind != XMOD_LAYER_SPARSE && kind != XMOD_LAYER_ATTN &&
+      kind != XMOD_LAYER_ROUTED_FFN)
+    return XMOD_ERR_UNSUPPORTED;
   if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
   if (!weights_ok(w, kind) || !aligned16(x) || !aligned16(dy) || !aligned16(dx) ||
       !aligned16_or_null(bias) || !g || !isfinite(route_coef))
     return XMOD_ERR_INVALID_ARG;
   if (dx == x || dx == dy) return XMOD_ERR_INVALID_ARG;
-  const float* gp[] = {g->rms1, g->wq, g->wk, g->wv, g->wo, g->rms2, g->w_gate, g->w_up,
-                       g->w_down};
-  for (const float* p : gp)
-    if (!aligned16(p)) return XMOD_ERR_INVALID_ARG;
-  if (!g->varsigma || (kind == XMOD_LAYER_SPARSE && !aligned16(g->w_router)) ||
-      !aligned16_or_null(g->w_router))
+  // the gradients of the weights the kind uses are required; the others may be NULL
+  const bool uses_attn = kind != XMOD_LAYER_ROUTED_FFN, uses_ffn = kind != XMOD_LAYER_ATTN;
+  const float* ga[] = {g->rms1, g->wq, g->wk, g->wv, g->wo};
+  const float* gf[] = {g->rms2, g->w_gate, g->w_up, g->w_down};
+  for (const float* p : ga)
+    if (uses_attn ? !aligned16(p) : !aligned16_or_null(p)) return XMOD_ERR_INVALID_ARG;
+  for (const float* p : gf)
+    if (uses_ffn ? !aligned16(p) : !aligned16_or_null(p)) return XMOD_ERR_INVALID_ARG;
+  if (!g->varsigma || (routed(kind) && !aligned16(g->w_router)) ||
+      !aligned16_or_null(g->w_router) || !aligned16_or_null(g->q_norm) ||
+      !aligned16_or_null(g->k_norm))
     return XMOD_ERR_INVALID_ARG;
   if ((w->q_norm && !aligned16(g->q_norm)) || (w->k_norm && !aligned16(g->k_norm)))
     return XMOD_ERR_INVALID_ARG;
   if (!head_dim_supported(dm->head_dim)) return XMOD_ERR_UNSUPPORTED;
-  if (kind == XMOD_LAYER_SPARSE && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
+  if (routed(kind) && dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
   if (!aligned16(ws) || ws_bytes < bwd_workspace_bytes(dm)) return XMOD_ERR_WORKSPACE;
   return run_layer_bwd((cudaStream_t)stream, dm, kind, K, gate, w, x, bias, dy, route_coef, dx,
                        g, ws);

@@ -114,7 +114,9 @@ scatter_bwd_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ dy,
     const Vec16<T> gv = ld_vec(g + c), fv = ld_vec(f + m * d + c);
     Vec16<T> o;
     if (gate == XMOD_GATE_XMOD) {
-      const Vec16<T> av = ld_vec(a + m * d + c);
+      Vec16<T> av;
+      av.raw = make_uint4(0, 0, 0, 0);   // bit pattern 0 is 0 in bf16 and fp32
+      if (a) av = ld_vec(a + m * d + c);
 #pragma unroll
       for (int k = 0; k < V; ++k) {
         dot += gv.get(k) * (av.get(k) + fv.get(k));
@@ -392,7 +394,9 @@ rms_bwd_kernel(int64_t M, int d, const float* __restrict__ dz, const T* __restri
       st4(da_out + m * d + c, make_float4(gr.x + e.x, gr.y + e.y, gr.z + e.z, gr.w + e.w));
     } else {
       T* p = dx_io + row * d + c;
-      const float4 cur = ld4(p), ad = *reinterpret_cast<const float4*>(dadd + m * d + c);
+      const float4 cur = ld4(p);
+      const float4 ad = dadd ? *reinterpret_cast<const float4*>(dadd + m * d + c)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
       st4(p, make_float4(cur.x + (ad.x + gr.x), cur.y + (ad.y + gr.y), cur.z + (ad.z + gr.z),
                          cur.w + (ad.w + gr.w)));
     }
@@ -836,7 +840,12 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   const xmod_dtype dt = dm->dtype;
   const int B = dm->B, T = dm->T, d = dm->d, hq = dm->n_heads, hkv = dm->n_kv_heads,
             hd = dm->head_dim, F = dm->d_ff;
-  const bool sparse = kind == XMOD_LAYER_SPARSE;
+  // routed: the layer selects top-(T/K) tokens; attn / ffn: which halves of the block run
+  // (FullAttn layers: the attention half on every token, y = x + a; Routed-FFN layers:
+  // the FFN half on RMSNorm(x_sel) rms2 with a = 0 in the gated residual)
+  const bool sparse = kind == XMOD_LAYER_SPARSE || kind == XMOD_LAYER_ROUTED_FFN;
+  const bool attn = kind != XMOD_LAYER_ROUTED_FFN;
+  const bool ffn = kind != XMOD_LAYER_ATTN;
   const int n = sparse ? T / K : T;
   const int M = B * n;
   const int Mp = (int)round8(M);
@@ -871,12 +880,13 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     BW_RUN("router", launch_router(c, dt, BT, d, x, w->w_router, bias, s, rr));
     BW_RUN("topk", launch_topk(c, B, T, n, s, idx, r_sel));
   }
-  BW_RUN("gather_rmsnorm",
-         launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1, dm->rms_eps, u));
-  const bool extras = w->q_norm || w->k_norm || w->rope_theta > 0.0f;
+  const bool extras = attn && (w->q_norm || w->k_norm || w->rope_theta > 0.0f);
   E* qkpre = (E*)bat(ws, L.qkpre);
   const bool tc_attn = tc && attention_tc_supported(hd, n, qkv_w);
   bool v_transposed = false;   // v kept only in its transposed layout (tensor-core path)
+  if (attn) {
+  BW_RUN("gather_rmsnorm",
+         launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1, dm->rms_eps, u));
   {
     Epilogue e;
     e.kind = EPI_STORE;
@@ -922,7 +932,8 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
                                                 (char*)qkv + es * qw, (char*)qkv + es * (qw + kw),
                                                 qkv_w, o));
   }
-  {
+  }
+  if (attn && ffn) {
     Epilogue eo;
     eo.kind = EPI_OPROJ;
     eo.out = a;
@@ -941,7 +952,12 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     else
       BW_RUN("gemm_o_residual", launch_gemm_simt(c, dt, M, d, qw, o, qw, w->wo, qw, nullptr, eo));
   }
-  BW_RUN("rmsnorm2", launch_rmsnorm_f32in(c, dt, M, d, h, w->rms2, dm->rms_eps, v2));
+  if (ffn) {
+  if (attn)
+    BW_RUN("rmsnorm2", launch_rmsnorm_f32in(c, dt, M, d, h, w->rms2, dm->rms_eps, v2));
+  else   // Routed-FFN: the FFN input is RMSNorm(x_sel) rms2
+    BW_RUN("gather_rmsnorm",
+           launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms2, dm->rms_eps, v2));
   BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_gate, d, gu, 2 * F, false));
   BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_up, d, gu + F, 2 * F, false));
   {
@@ -951,6 +967,7 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
                                 (int64_t)M, F, (const E*)gu, H));
   }
   BW_RUN("gemm_down", bw_gemm(c, dt, M, d, F, H, F, w->w_down, F, f, d, false));
+  }
 
   // ======== backward: residual rule and router
   E* df;
@@ -964,7 +981,8 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     float* lossp = (float*)bat(ws, L.lossp);
     BW_RUN("bwd_rows", launch_pdl(scatter_bwd_kernel<E>, dim3(rowblk), dim3(BW_WARPS * 32), 0,
                                   c.stream, (int64_t)M, T, n, d, (const E*)dy, (const int32_t*)idx,
-                                  (const float*)r_sel, (const E*)a, (const E*)f, w->varsigma, gate,
+                                  (const float*)r_sel, attn ? (const E*)a : (const E*)nullptr,
+                                  (const E*)f, w->varsigma, gate,
                                   df, dae_buf, dr, dvs));
     dae = gate == XMOD_GATE_XMOD ? df : dae_buf;
     const size_t smr = (size_t)T * (sizeof(float) + 1);
@@ -982,7 +1000,7 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     if (gr->route_loss)
       BW_RUN("bwd_reduce", launch_pdl(sum_kernel, dim3(1), dim3(1024), 0, c.stream, (int64_t)B,
                                       (const float*)lossp, 1.0f / (float)BT, gr->route_loss));
-  } else {   // dense: y = x + a + f, so both residuals receive dy; dx starts as dy
+  } else {   // dense: y = x + a + f (FullAttn: x + a), every residual receives dy; dx = dy
     df = (E*)dy;
     dae = (const E*)dy;
     if (cudaMemcpyAsync(dx, dy, es * (size_t)BT * d, cudaMemcpyDeviceToDevice, c.stream) !=
@@ -997,6 +1015,21 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
       return XMOD_ERR_CUDA;
   }
 
+  // gradients of weights a kind does not use are zero
+  auto zero = [&](float* g, size_t cnt) {
+    return !g || cudaMemsetAsync(g, 0, sizeof(float) * cnt, c.stream) == cudaSuccess;
+  };
+  if (!ffn && !(zero(gr->rms2, d) && zero(gr->w_gate, (size_t)F * d) &&
+                zero(gr->w_up, (size_t)F * d) && zero(gr->w_down, (size_t)d * F)))
+    return XMOD_ERR_CUDA;
+  if (!attn && !(zero(gr->rms1, d) && zero(gr->wq, (size_t)qw * d) && zero(gr->wk, (size_t)kw * d) &&
+                 zero(gr->wv, (size_t)kw * d) && zero(gr->wo, (size_t)d * qw) &&
+                 zero(gr->q_norm, hd) && zero(gr->k_norm, hd)))
+    return XMOD_ERR_CUDA;
+  float* dh = nullptr;   // the gradient reaching h = x_sel + a through the FFN half
+  const E* da = dae;     // the gradient reaching a (FullAttn: dy itself)
+
+  if (ffn) {
   // ======== FFN: f = H Wd^T, H = silu(G) U, [G | U] = v2 [Wg | Wu]^T
   BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, df, d, tA, Mp));      // df^T [d, Mp]
   BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, F, H, F, tB, Mp));       // H^T [F, Mp]
@@ -1020,17 +1053,27 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   BW_RUN("bwd_transpose", transpose(c, dt, F, F, d, w->w_up, d, tW + F, 2 * F));
   float* dv2 = (float*)bat(ws, L.dv2);
   BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, 2 * F, dGU, 2 * F, tW, 2 * F, dv2, d, true));
-  // v2 = RMSNorm(h) g2; h = x_sel + a: dh reaches x_sel and (with dae) a
-  float* dh = (float*)bat(ws, L.dh);
-  E* da = (E*)bat(ws, L.da);
   float* rstd2 = (float*)bat(ws, L.rstd2);
-  BW_RUN("bwd_rows", launch_pdl(rms_bwd_kernel<float, E>, dim3(rowblk), dim3(BW_WARPS * 32), 0,
-                                c.stream, (int64_t)M, d, (const float*)dv2, (const E*)w->rms2,
-                                (const float*)h, (const int32_t*)nullptr, T, n, dm->rms_eps, dae,
-                                dh, da, (const float*)nullptr, (E*)nullptr, rstd2));
-  {
+  if (attn) {
+    // v2 = RMSNorm(h) g2; h = x_sel + a: dh reaches x_sel and (with dae) a
+    dh = (float*)bat(ws, L.dh);
+    E* da_buf = (E*)bat(ws, L.da);
+    BW_RUN("bwd_rows", launch_pdl(rms_bwd_kernel<float, E>, dim3(rowblk), dim3(BW_WARPS * 32), 0,
+                                  c.stream, (int64_t)M, d, (const float*)dv2, (const E*)w->rms2,
+                                  (const float*)h, (const int32_t*)nullptr, T, n, dm->rms_eps, dae,
+                                  dh, da_buf, (const float*)nullptr, (E*)nullptr, rstd2));
+    da = da_buf;
     const int st = bw_coldot<float>(c, M, d, dv2, h, nullptr, T, n, rstd2, part, gr->rms2);
     if (st) return st;
+  } else {
+    // Routed-FFN: v2 = RMSNorm(x_sel) rms2, the gradient goes straight to the token's row
+    BW_RUN("bwd_rows", launch_pdl(rms_bwd_kernel<E, E>, dim3(rowblk), dim3(BW_WARPS * 32), 0,
+                                  c.stream, (int64_t)M, d, (const float*)dv2, (const E*)w->rms2,
+                                  (const E*)x, (const int32_t*)idx, T, n, dm->rms_eps,
+                                  (const E*)nullptr, (float*)nullptr, (E*)nullptr,
+                                  (const float*)nullptr, (E*)dx, rstd2));
+    return bw_coldot<E>(c, M, d, dv2, (const E*)x, idx, T, n, rstd2, part, gr->rms2);
+  }
   }
 
   // ======== a = o Wo^T

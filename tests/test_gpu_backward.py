@@ -1,6 +1,7 @@
 """GPU parity of the layer backward (xmod_layer_bwd) against the oracle's layer_bwd,
 through the C ABI: dx, every weight gradient, dJ/dvarsigma and the Eq. 9 loss, for
-sparse layers under Eq. 7 and Eq. 6 (with and without the Eq. 9 term) and dense layers.
+sparse layers under Eq. 7 and Eq. 6 (with and without the Eq. 9 term), dense layers, the
+QK-norm / RoPE extras and the FullAttn / Routed-FFN halves; and the stack backward.
 
 Tolerances. fp32 (FFMA kernels throughout): relative 1e-5 as for the forward. bf16:
 relative L2 <= 1e-2 (the bound of the bf16 forward); a gradient has no natural unit,
@@ -55,7 +56,8 @@ def _run(X, w: I.Workload, kind, gate, route_coef, seed, extras=None):
         lw["rope_theta"] = theta
     bias = I.router_bias(w)
     x = I.residual_stream(w)
-    if kind == X.LAYER_SPARSE:
+    routed = kind in (X.LAYER_SPARSE, X.LAYER_ROUTED_FFN)
+    if routed:
         x, _ = U.enforce_routing_margin(x, w.dtype, lw["w_r"], bias, w.K)
     g = np.random.default_rng(seed)
     dyf = g.standard_normal((w.B, w.T, w.d)).astype(np.float32)
@@ -80,23 +82,20 @@ def _run(X, w: I.Workload, kind, gate, route_coef, seed, extras=None):
     ref = O.layer_bwd(U_dims(w), kind, w.K, gate, oracle_layer(lw, w.dtype), I.to_f64(x, w.dtype),
                       I.to_f64(dy, w.dtype), bias=bias, route_coef=route_coef)
     _check(from_dev(dx, w.dtype), ref["dx"], w.dtype, "dx")
-    for on, an in GRAD_NAMES.items():
-        if kind == X.LAYER_DENSE and on == "w_r":
-            assert torch.all(gd[an] == 0)
-            continue
+    for on, an in GRAD_NAMES.items():   # unused weights: zero on both sides
         _check(gd[an].cpu().numpy(), ref["grads"][on], w.dtype, f"d{on}")
     if extras:
         _check(gd["q_norm"].cpu().numpy(), ref["grads"]["gq"], w.dtype, "dq_norm")
         _check(gd["k_norm"].cpu().numpy(), ref["grads"]["gk"], w.dtype, "dk_norm")
     vs = float(gd["varsigma"][0])
-    if kind == X.LAYER_SPARSE and gate == X.GATE_XMOD:
+    if routed and gate == X.GATE_XMOD:
         _check(np.array([vs]), np.array([ref["varsigma"]]), w.dtype, "dvarsigma")
     else:
         assert vs == 0.0
-    if kind == X.LAYER_SPARSE:
+    if routed:
         _check(np.array([float(gd["route_loss"][0])]), np.array([ref["route_loss"]]), w.dtype,
                "route loss")
-    if kind == X.LAYER_SPARSE and route_coef == 0.0:
+    if routed and route_coef == 0.0:
         # a skipped token's gradient is the upstream gradient, bit for bit
         sel = np.zeros((w.B, w.T), bool)
         np.put_along_axis(sel, ref["idx"], True, 1)
@@ -138,6 +137,19 @@ def test_layer_bwd_qk_norm_rope(X, dtype, kind, T):
         w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=T, K=4, d=256, hq=4, hkv=2, F=512, seed=33,
                                              weight_std=0.02 * np.sqrt(1536 / 256))
     _run(X, w, kind, X.GATE_XMOD, 0.1, seed=60 + T + kind, extras=1e4)
+
+
+@pytest.mark.parametrize("dtype,kind,gate,coef", [("fp32", 2, 0, 0.0), ("fp32", 3, 0, 0.3),
+                                                 ("fp32", 3, 1, 0.0), ("bf16", 2, 0, 0.0),
+                                                 ("bf16", 3, 0, 0.1), ("bf16", 3, 1, 0.0)])
+def test_layer_bwd_mechanism_controls(X, dtype, kind, gate, coef):
+    """The FullAttn (ATTN) and Routed-FFN (ROUTED_FFN) halves of the block."""
+    if dtype == "fp32":
+        w = I.WORKLOADS["tiny_fp32"]
+    else:
+        w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=256, K=4, d=256, hq=4, hkv=2, F=512, seed=35,
+                                             weight_std=0.02 * np.sqrt(1536 / 256))
+    _run(X, w, kind, gate, coef, seed=80 + 5 * kind + gate)
 
 
 def _grad_set(w, n_layers):
