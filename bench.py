@@ -1,12 +1,16 @@
-"""Benchmark of the sparse-depth layer forward on GB300.
+"""Benchmark of the sparse-depth layer stack on GB300.
 
-One step = one pass of the whole X-MoD A4K8 block (32 Sparse(K=8) layers with
+Default (the headline): one step = one pass of the whole X-MoD A4K8 block (32 Sparse(K=8) layers with
 Eq. 7 gating + 1 Dense anchor; d=1536, 12 q / 4 kv heads, head_dim 128, SwiGLU
 d_ff=4096, B=8 sequences of T=4096 tokens, per-token router bias) through the
 library's stack entry point. Metric: selected tokens processed by sparse layers
 per second (B * T/K * 32 per step), whole job over all ranks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl xmod|reference]
+
+Other workloads: --workload mod_bf16 | a3k16_bf16 | tiny_fp32 (the same stack step),
+--workload routing_bf16 (the routing-only microbench: router + top-(T/K) + gather +
+Eq. 7 scatter of a given block output), --pass bwd (the backward of every layer).
 
 Under torchrun every rank runs its own B sequences (sequences are independent;
 no data-path collective), the timing is the max over ranks.
@@ -995,10 +999,61 @@ def run_routing(args):
         e1.record(stream)
         torch.cuda.synchronize()
         ems = max_over_ranks(e0.elapsed_time(e1) / e_steps)
-        e2e = {"value": world * M / (ems / 1e3), "unit": UNIT, "ms_per_step": ems,
+        e2e_serial = {"value": world * M / (ems / 1e3), "unit": UNIT, "ms_per_step": ems,
+                      "transfers": "serial: copies in, routing, copy out on one stream"}
+
+        # double-buffered: step i's routing runs on one pair of device buffers while one
+        # copy stream brings in step i+1's x and a+f and another takes out step i's x
+        x2, af2 = [x, torch.empty_like(x)], [af, torch.empty_like(af)]
+        outs = [out_h, torch.empty_like(xh).pin_memory()]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+
+        def h2d(k):
+            s_in.wait_event(ev_out[k])
+            with torch.cuda.stream(s_in):
+                x2[k].copy_(xh, non_blocking=True)
+                af2[k].copy_(afh, non_blocking=True)
+            ev_in[k].record(s_in)
+
+        def pipelined(nsteps, t0=None, t1=None):
+            if t0 is not None:
+                t0.record(stream)
+                s_in.wait_event(t0)
+            h2d(0)
+            for i in range(nsteps):
+                k = i & 1
+                stream.wait_event(ev_in[k])
+                X.router_topk(dm, K, x2[k], w_r, None, logits, None, idx, r_sel, ws, stream)
+                X.gather(dm, K, x2[k], idx, xs, stream)
+                X.gated_scatter(dm, K, x2[k], idx, r_sel, af2[k], None, 1.0, X.GATE_XMOD, stream)
+                ev_done[k].record(stream)
+                if i + 1 < nsteps:
+                    h2d(1 - k)
+                s_out.wait_event(ev_done[k])
+                with torch.cuda.stream(s_out):
+                    outs[k].copy_(x2[k], non_blocking=True)
+                ev_out[k].record(s_out)
+            stream.wait_event(ev_out[(nsteps - 1) & 1])
+            if t1 is not None:
+                t1.record(stream)
+
+        pipelined(2)
+        barrier()
+        torch.cuda.synchronize()
+        pipelined(e_steps, e0, e1)
+        torch.cuda.synchronize()
+        pms = max_over_ranks(e0.elapsed_time(e1) / e_steps)
+        e2e = {"value": world * M / (pms / 1e3), "unit": UNIT, "ms_per_step": pms,
                "steps": e_steps,
                "h2d_bytes_per_step": int(xh.numel() * 2 + afh.numel() * 2),
-               "d2h_bytes_per_step": int(out_h.numel() * 2)}
+               "d2h_bytes_per_step": int(out_h.numel() * 2),
+               "transfers": "double-buffered: step i+1's copies in and step i's copy out run "
+                            "on their own streams while step i's routing runs",
+               "serial": e2e_serial}
+        del x2, af2
         st = X.sync_status(ws)
         if st != X.OK:
             raise RuntimeError(f"device status after the e2e run: {X.status_string(st)}")
