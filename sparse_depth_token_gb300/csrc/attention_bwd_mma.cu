@@ -427,16 +427,18 @@ attn_bwd_kv_mma(const AmArgs p) {
 }
 
 template <int HD>
-cudaError_t launch_am(int B, const AmArgs& a, cudaStream_t st) {
+cudaError_t launch_am(int B, const AmArgs& a, cudaStream_t st, bool with_q) {
   constexpr int P = HD + 8;
   const size_t smq = sizeof(__nv_bfloat16) * 6 * AM_T * P;
   const size_t smk = smq + sizeof(float) * 4 * AM_T;
   cudaFuncSetAttribute(attn_bwd_q_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
   cudaFuncSetAttribute(attn_bwd_kv_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
   const int tiles = (a.n + AM_T - 1) / AM_T;
-  cudaError_t e = launch_pdl(attn_bwd_q_mma<HD>, dim3(tiles, a.hq, B), dim3(AM_WARPS * 32), smq,
-                             st, a);
-  if (e != cudaSuccess) return e;
+  if (with_q) {
+    const cudaError_t e = launch_pdl(attn_bwd_q_mma<HD>, dim3(tiles, a.hq, B),
+                                     dim3(AM_WARPS * 32), smq, st, a);
+    if (e != cudaSuccess) return e;
+  }
   return launch_pdl(attn_bwd_kv_mma<HD>, dim3(tiles, a.hkv, B), dim3(AM_WARPS * 32), smk, st, a);
 }
 
@@ -448,7 +450,7 @@ bool attn_bwd_mma_supported(int hd, int ldq, int ldo) {
 
 cudaError_t launch_attn_bwd_mma(const Ctx& c, int B, int n, int hq, int hkv, int hd,
                                 const void* qkv, int ldq, const void* o, const void* dO,
-                                float* lse, float* Dd, void* dqkv, int ldg) {
+                                float* lse, float* Dd, void* dqkv, int ldg, bool with_q) {
   if (!attn_bwd_mma_supported(hd, ldq, hq * hd) || ldg % 2) return cudaErrorInvalidValue;
   AmArgs a;
   a.n = n;
@@ -463,7 +465,7 @@ cudaError_t launch_attn_bwd_mma(const Ctx& c, int B, int n, int hq, int hkv, int
   a.dqkv = (__nv_bfloat16*)dqkv;
   a.ldg = ldg;
   a.scale = 1.0f / sqrtf((float)hd);
-  return hd == 128 ? launch_am<128>(B, a, c.stream) : launch_am<64>(B, a, c.stream);
+  return hd == 128 ? launch_am<128>(B, a, c.stream, with_q) : launch_am<64>(B, a, c.stream, with_q);
 }
 
 }  // namespace xmod

@@ -1,0 +1,376 @@
+// dQ of the causal GQA attention backward on the tcgen05 tensor cores (bf16, head_dim
+// 128): dq = scale * sum_j dS_ij k_j with dS = P * (dP - D), P = exp2(scale_log2 q.k -
+// lse), dP = dO v^T, D_i = <dO_i, o_i>.
+//
+// Source: the block of the X-MoD notes' "backbone configuration" (GQA attention among
+// the selected tokens); the gradient is that of softmax attention.
+//
+// One CTA per (128-query block, query head, sequence), laid out as the forward kernel:
+//   warp 0      TMA: the Q and dO tiles once, then per 64-key block the rows of K and of
+//               V and the transposed keys K^T ([head dim, keys], keys contiguous) into a
+//               three-stage ring
+//   warp 1      TMEM owner; one lane issues S_j = Q K_j^T and dP_j = dO V_j^T into one
+//               of two TMEM buffer pairs, and dQ += dS_j K_j once dS_j is written, with
+//               dS_j read from TMEM as the MMA's A operand
+//   warps 2..5  one query row per thread (a TMEM lane is a row): D and lse of the row,
+//               then per key block P and dS from S and dP in registers; dS goes back to
+//               TMEM as bf16 pairs over the first half of S_j's columns
+// The row statistics lse come from the forward pass (its log2-sum-exp2 output); D is
+// computed here and written for the key/value kernel.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace xmod {
+
+namespace {
+
+using namespace tc;
+
+constexpr int QB = 128;                  // query rows per CTA
+constexpr int HD = 128;                  // head dim
+constexpr int KB = 64;                   // keys per block
+constexpr int NST = 3;                   // stages of the key ring
+constexpr int THREADS = 192;
+constexpr int CHUNK = 128 * 128;         // 128 rows x 64 bf16 columns, 128-byte swizzle
+constexpr int QTILE = 2 * CHUNK;         // 128 x 128
+constexpr int K_CHUNK = KB * 128;        // 64 rows x 64 columns
+constexpr int K_TILE = 2 * K_CHUNK;      // 64 keys x 128 head dims
+constexpr int KT_TILE = CHUNK;           // 128 head dims x 64 keys
+constexpr int STAGE = 2 * K_TILE + KT_TILE;
+constexpr int DATA = 2 * QTILE + NST * STAGE;
+constexpr int SMEM = DATA + 1024;
+constexpr int TMEM_COLS = 512;           // S0, S1, dP0, dP1 (64 each), dQ (128)
+static_assert((1 + 2 * NST + 8) * 8 + 16 <= 256, "barrier block overflows");
+
+struct DqArgs {
+  int n, hq, hkv, nqb;
+  int qw, kw;
+  float scale_log2, scale;
+  const float* lse;           // [B*n, hq], log2 units
+  const __nv_bfloat16* o;     // [B*n, qw]
+  const __nv_bfloat16* dO;    // [B*n, qw]
+  float* Dd;                  // [B*n, hq] out
+  __nv_bfloat16* dq;          // q columns of [B*n, ldg]
+  int ldg;
+  int* status;
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmDO,
+                      const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmKt, const DqArgs a) {
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t sQ = base, sDO = base + QTILE;
+  const uint32_t sSt0 = base + 2 * QTILE;   // stage s: K rows, V rows, K^T
+  const uint32_t sBar = (base - raw >= 256u) ? raw : base + (uint32_t)DATA;
+  const uint32_t QD_FULL = sBar;
+  const uint32_t ST_FULL0 = sBar + 8, ST_EMPTY0 = ST_FULL0 + 8 * NST;
+  const uint32_t S_FULL0 = ST_EMPTY0 + 8 * NST, S_EMPTY0 = S_FULL0 + 16;
+  const uint32_t P_FULL0 = S_EMPTY0 + 16, P_EMPTY0 = P_FULL0 + 16;
+  const uint32_t sTmem = P_EMPTY0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + (sTmem - raw));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + (sTmem - raw) + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qb = a.nqb - 1 - (int)blockIdx.z;   // longest query blocks first
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int g = h / (a.hq / a.hkv);
+  const int q0 = qb * QB;
+
+  if (threadIdx.x == 0) {
+    mbar_init(QD_FULL, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(ST_FULL0 + 8 * s, 1);
+      mbar_init(ST_EMPTY0 + 8 * s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(S_FULL0 + 8 * s, 1);
+      mbar_init(S_EMPTY0 + 8 * s, 128);
+      mbar_init(P_FULL0 + 8 * s, 128);
+      mbar_init(P_EMPTY0 + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmDO);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmKt);
+  }
+  if (warp == 1) tmem_alloc(sTmem, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tDQ = tmem + 256u;
+  pdl_wait();
+  const int last_q = min(q0 + QB, a.n) - 1;
+  const int nkb = q0 < a.n ? last_q / KB + 1 : 0;
+
+  if (warp == 0) {
+    if (lane == 0 && nkb > 0) {
+      mbar_arrive_expect_tx(QD_FULL, 2 * QTILE);
+      tma_load_3d(sQ, &tmQ, QD_FULL, h * HD, q0, b);
+      tma_load_3d(sQ + CHUNK, &tmQ, QD_FULL, h * HD + 64, q0, b);
+      tma_load_3d(sDO, &tmDO, QD_FULL, h * HD, q0, b);
+      tma_load_3d(sDO + CHUNK, &tmDO, QD_FULL, h * HD + 64, q0, b);
+      const int kt_row = (b * a.hkv + g) * HD;
+      for (int j = 0; j < nkb; ++j) {
+        const int s = j % NST;
+        if (!mbar_wait(ST_EMPTY0 + 8 * s, ((uint32_t)(j / NST) & 1u) ^ 1u, abort_flag, a.status))
+          break;
+        const uint32_t st = sSt0 + s * STAGE;
+        mbar_arrive_expect_tx(ST_FULL0 + 8 * s, STAGE);
+        tma_load_3d(st, &tmK, ST_FULL0 + 8 * s, a.qw + g * HD, j * KB, b);
+        tma_load_3d(st + K_CHUNK, &tmK, ST_FULL0 + 8 * s, a.qw + g * HD + 64, j * KB, b);
+        tma_load_3d(st + K_TILE, &tmK, ST_FULL0 + 8 * s, a.qw + a.kw + g * HD, j * KB, b);
+        tma_load_3d(st + K_TILE + K_CHUNK, &tmK, ST_FULL0 + 8 * s, a.qw + a.kw + g * HD + 64,
+                    j * KB, b);
+        tma_load_2d(st + 2 * K_TILE, &tmKt, ST_FULL0 + 8 * s, j * KB, kt_row);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, KB);
+      constexpr uint32_t idesc_q = idesc_bf16_f32(128, HD);
+      bool ok = nkb > 0 && mbar_wait(QD_FULL, 0, abort_flag, a.status);
+      int ns = 0, nd = 0;
+      uint64_t t0 = global_timer_ns();
+      uint32_t spins = 0;
+      while (ok && nd < nkb) {
+        bool progressed = false;
+        // S_{j+2} and dP_{j+2} reuse buffer j & 1, whose first half holds dS_j: issued
+        // after dQ += dS_j K_j (the MMAs of one thread run in order)
+        if (ns < nkb && ns <= nd + 1) {
+          const int s = ns & 1, st = ns % NST;
+          if (mbar_test_wait(ST_FULL0 + 8 * st, (uint32_t)(ns / NST) & 1u) &&
+              mbar_test_wait(S_EMPTY0 + 8 * s, ((uint32_t)(ns >> 1) & 1u) ^ 1u)) {
+            tc_fence_after();
+            const uint32_t stg = sSt0 + st * STAGE;
+            const uint32_t dS = tmem + (uint32_t)(s * KB), dP = tmem + 128u + (uint32_t)(s * KB);
+#pragma unroll
+            for (int kc = 0; kc < 2; ++kc) {
+              const uint64_t aq = smem_desc_sw128(sQ + kc * CHUNK);
+              const uint64_t ao = smem_desc_sw128(sDO + kc * CHUNK);
+              const uint64_t bk = smem_desc_sw128(stg + kc * K_CHUNK);
+              const uint64_t bv = smem_desc_sw128(stg + K_TILE + kc * K_CHUNK);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                mma_bf16(dS, aq + 2ull * k, bk + 2ull * k, idesc_s, (kc | k) != 0 ? 1u : 0u);
+                mma_bf16(dP, ao + 2ull * k, bv + 2ull * k, idesc_s, (kc | k) != 0 ? 1u : 0u);
+              }
+            }
+            mma_commit(S_FULL0 + 8 * s);
+            ++ns;
+            progressed = true;
+          }
+        }
+        if (nd < ns) {
+          const int s = nd & 1, st = nd % NST;
+          if (mbar_test_wait(P_FULL0 + 8 * s, (uint32_t)(nd >> 1) & 1u)) {
+            tc_fence_after();
+            const uint32_t tp = tmem + (uint32_t)(s * KB);
+            const uint64_t bd = smem_desc_sw128(sSt0 + st * STAGE + 2 * K_TILE);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_bf16_tmem_a(tDQ, tp + (uint32_t)(8 * k), bd + 2ull * k, idesc_q,
+                              (nd | k) != 0 ? 1u : 0u);
+            mma_commit(P_EMPTY0 + 8 * s);
+            mma_commit(ST_EMPTY0 + 8 * st);
+            ++nd;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t0 = global_timer_ns();
+          spins = 0;
+          continue;
+        }
+        if ((++spins & 255u) == 0u) {
+          if (*abort_flag) break;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            report_status(a.status, XMOD_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
+    }
+  } else {
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int qi = q0 + row;
+    const bool valid = qi < a.n;
+    const int64_t grow = (int64_t)b * a.n + (valid ? qi : 0);
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    // D_i = <dO_i, o_i> and the row's lse (log2 units)
+    float D = 0.f, lse2 = 0.f;
+    if (valid && nkb > 0) {
+      const uint4* op = reinterpret_cast<const uint4*>(a.o + grow * a.qw + h * HD);
+      const uint4* gp = reinterpret_cast<const uint4*>(a.dO + grow * a.qw + h * HD);
+#pragma unroll 4
+      for (int v = 0; v < HD / 8; ++v) {
+        const uint4 ov = op[v], gv = gp[v];
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __bfloat1622float2(o2[e]), y = __bfloat1622float2(g2[e]);
+          D = fmaf(x.x, y.x, fmaf(x.y, y.y, D));
+        }
+      }
+      lse2 = a.lse[grow * a.hq + h];
+      a.Dd[grow * a.hq + h] = D;
+    }
+    bool ok = true;
+    for (int j = 0; j < nkb; ++j) {
+      const int s = j & 1;
+      if (!mbar_wait(S_FULL0 + 8 * s, (uint32_t)(j >> 1) & 1u, abort_flag, a.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[KB], dp[KB];
+      const uint32_t srow = tmem + lane_off + (uint32_t)(s * KB);
+      const uint32_t prow = tmem + lane_off + 128u + (uint32_t)(s * KB);
+      tmem_ld32(srow, *reinterpret_cast<float(*)[32]>(sv));
+      tmem_ld32(srow + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+      tmem_ld32(prow, *reinterpret_cast<float(*)[32]>(dp));
+      tmem_ld32(prow + 32, *reinterpret_cast<float(*)[32]>(dp + 32));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(S_EMPTY0 + 8 * s);
+      const int key0 = j * KB;
+      float pk[32];
+#pragma unroll
+      for (int i = 0; i < KB; i += 2) {
+        const bool ok0 = valid && key0 + i <= qi, ok1 = valid && key0 + i + 1 <= qi;
+        const float p0 = ok0 ? ex2f(fmaf(sv[i], a.scale_log2, -lse2)) : 0.f;
+        const float p1 = ok1 ? ex2f(fmaf(sv[i + 1], a.scale_log2, -lse2)) : 0.f;
+        pk[i / 2] = __uint_as_float(pack_bf16x2(p0 * (dp[i] - D), p1 * (dp[i + 1] - D)));
+      }
+      // dS_j over the first half of S_j's columns (S_j has been read; dS_{j-2}, which the
+      // buffer held before S_j, was consumed by then)
+      tmem_st32(srow, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(P_FULL0 + 8 * s);
+    }
+    if (nkb == 0) ok = false;
+    if (ok) {
+      const int jl = nkb - 1;
+      ok = mbar_wait(P_EMPTY0 + 8 * (jl & 1), (uint32_t)(jl >> 1) & 1u, abort_flag, a.status);
+    }
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16* dst = a.dq + grow * a.ldg + h * HD;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(tDQ + lane_off + c * 32, v);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 q;
+            q.x = pack_bf16x2(v[e] * a.scale, v[e + 1] * a.scale);
+            q.y = pack_bf16x2(v[e + 2] * a.scale, v[e + 3] * a.scale);
+            q.z = pack_bf16x2(v[e + 4] * a.scale, v[e + 5] * a.scale);
+            q.w = pack_bf16x2(v[e + 6] * a.scale, v[e + 7] * a.scale);
+            *reinterpret_cast<uint4*>(dst + c * 32 + e) = q;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // a wait ran out: let copies and MMAs in flight land before the memory is released
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 20000000ull) {
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+bool attn_bwd_dq_tc_supported(int hd, int ldq, int qw, int kt_ld) {
+  return hd == HD && ldq % 8 == 0 && qw % 8 == 0 && kt_ld % 8 == 0 && tma_available();
+}
+
+cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
+                                  int ldq, const void* kt, int kt_ld, const void* o,
+                                  const void* dO, const float* lse, float* Dd, void* dqkv,
+                                  int ldg) {
+  if (B <= 0 || n <= 0) return cudaSuccess;
+  const int qw = hq * HD, kw = hkv * HD;
+  if (!attn_bwd_dq_tc_supported(HD, ldq, qw, kt_ld) || ldg % 8) return cudaErrorInvalidValue;
+  CUtensorMap mQ, mDO, mK, mKt;
+  {
+    const int64_t dims[3] = {ldq, n, B};
+    const int64_t strides[2] = {(int64_t)ldq * 2, (int64_t)n * ldq * 2};
+    const int qbox[3] = {64, QB, 1};
+    const int kbox[3] = {64, KB, 1};
+    if (!tma_map_bf16(&mQ, qkv, 3, dims, strides, qbox)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(&mK, qkv, 3, dims, strides, kbox)) return cudaErrorInvalidValue;
+  }
+  {
+    const int64_t dims[3] = {qw, n, B};
+    const int64_t strides[2] = {(int64_t)qw * 2, (int64_t)n * qw * 2};
+    const int box[3] = {64, QB, 1};
+    if (!tma_map_bf16(&mDO, dO, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const int64_t dims[2] = {n, (int64_t)B * hkv * HD};
+    const int64_t strides[1] = {(int64_t)kt_ld * 2};
+    const int box[2] = {64, HD};
+    if (!tma_map_bf16(&mKt, kt, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  DqArgs a;
+  a.n = n;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.nqb = (n + QB - 1) / QB;
+  a.qw = qw;
+  a.kw = kw;
+  a.scale = 1.0f / sqrtf((float)HD);
+  a.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  a.lse = lse;
+  a.o = (const __nv_bfloat16*)o;
+  a.dO = (const __nv_bfloat16*)dO;
+  a.Dd = Dd;
+  a.dq = (__nv_bfloat16*)dqkv;
+  a.ldg = ldg;
+  a.status = c.status;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(attn_bwd_dq_tc_kernel, dim3(hq, B, a.nqb), dim3(THREADS), SMEM, c.stream,
+                    mQ, mDO, mK, mKt, a);
+}
+
+}  // namespace xmod

@@ -85,6 +85,9 @@ struct AttnArgs {
   const int32_t* qpos;
   int nkv;
   int k_col0;
+  // optional: each row's log2-sum-exp2 of its scaled logits, [rows, hq] (the backward
+  // recomputes P from it)
+  float* lse;
 };
 
 // 2^x by the PTX ex2.approx instruction: its error is far below the bf16 rounding the
@@ -411,6 +414,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
     if (ok) {
       tc_fence_after();
       const float inv = 1.0f / l;
+      if (a.lse && qi < n_b) a.lse[(row0 + qi) * a.hq + h] = m + log2f(l);
       __nv_bfloat16* dst = a.o + (row0 + qi) * a.ldo + h * HD;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -509,7 +513,7 @@ bool attention_tc_supported(int hd, int n, int ldq) {
 cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
                                 int ldq, const void* vt, int vt_ld, void* o,
                                 const int32_t* seq_count, const int32_t* seq_off,
-                                const AttnKv* kv) {
+                                const AttnKv* kv, float* lse) {
   if (B <= 0 || n <= 0) return cudaSuccess;
   if (kv && (seq_count || !kv->qpos || kv->nkv <= 0 || kv->ldk % 8)) return cudaErrorInvalidValue;
   const int nkv = kv ? kv->nkv : n;
@@ -535,6 +539,7 @@ cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, con
   a.qpos = kv ? kv->qpos : nullptr;
   a.nkv = nkv;
   a.k_col0 = kv ? 0 : a.qw;
+  a.lse = lse;
   if (nkv <= XMOD_ATTN_ONE_BLOCK_MAX_N)
     return launch_attention_cfg<128, 3, 3>(c, B, n, hq, qkv, ldq, mVt, a, kv);
   return launch_attention_cfg<64, XMOD_ATTN_K_STAGES, 5 - XMOD_ATTN_K_STAGES>(c, B, n, hq, qkv,

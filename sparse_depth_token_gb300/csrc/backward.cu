@@ -678,7 +678,7 @@ inline int64_t round8(int64_t v) { return (v + 7) / 8 * 8; }
 struct BwLayout {
   size_t status, s, r, idx, r_sel, dr, dvs, ds, lossp, u, qkv, vt, o, a, h, v2, gu, H, f, df,
       dae, dH, dGU, dv2, dh, da, dO, lse, Dd, dqkv, du, rstd1, rstd2, tA, tB, tW, part, qkpre,
-      dgq, dgk, total;
+      dgq, dgk, kt, total;
 };
 
 constexpr int kMaxChunks = 1024;   // row chunks of the column reductions
@@ -732,6 +732,7 @@ BwLayout bw_layout(const xmod_dims* dm) {
   L.qkpre = take(es * M * (qw + kw));   // q | k before the QK-norm / rotation
   L.dgq = take(4 * M * hd);
   L.dgk = take(4 * M * hd);
+  L.kt = take(es * (size_t)dm->B * dm->n_kv_heads * hd * vtl);   // keys transposed
   L.total = off;
   return L;
 }
@@ -925,8 +926,10 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
                                                  qw, hkv, w->k_norm, hd, dm->rms_eps,
                                                  w->rope_theta, idx, nullptr, n));
     }
-    if (v_transposed)
-      BW_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, (int)round8(n), o));
+    if (v_transposed)   // also the rows' log-sum-exp, which the backward reuses
+      BW_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qkv, qkv_w, vt, (int)round8(n), o,
+                                              nullptr, nullptr, nullptr,
+                                              (float*)bat(ws, L.lse)));
     else
       BW_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qkv, qkv_w,
                                                 (char*)qkv + es * qw, (char*)qkv + es * (qw + kw),
@@ -1087,7 +1090,20 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
 
   // ======== attention
   E* dqkv = (E*)bat(ws, L.dqkv);
-  if (mma_attn) {   // bf16: warp-level tensor-core MMA, v rows and dO in bf16
+  const int kt_ld = (int)round8(n);
+  const bool dq_tc = mma_attn && v_transposed && attn_bwd_dq_tc_supported(hd, qkv_w, qw, kt_ld);
+  if (dq_tc) {   // dq on tcgen05 (lse from the forward), dk and dv on the warp-level MMA
+    E* kt = (E*)bat(ws, L.kt);
+    for (int bb = 0; bb < B; ++bb)   // the keys transposed, per sequence: [hkv * hd, keys]
+      BW_RUN("bwd_transpose", transpose(c, dt, n, n, kw, qkv + ((size_t)bb * n) * qkv_w + qw,
+                                        qkv_w, kt + (size_t)bb * kw * kt_ld, kt_ld));
+    BW_RUN("bwd_attention", launch_attn_bwd_dq_tc(c, B, n, hq, hkv, qkv, qkv_w, kt, kt_ld, o, dO,
+                                                  (const float*)bat(ws, L.lse),
+                                                  (float*)bat(ws, L.Dd), dqkv, qkv_w));
+    BW_RUN("bwd_attention", launch_attn_bwd_mma(c, B, n, hq, hkv, hd, qkv, qkv_w, o, dO,
+                                                (float*)bat(ws, L.lse), (float*)bat(ws, L.Dd),
+                                                dqkv, qkv_w, false));
+  } else if (mma_attn) {   // bf16: warp-level tensor-core MMA, v rows and dO in bf16
     BW_RUN("bwd_attention", launch_attn_bwd_mma(c, B, n, hq, hkv, hd, qkv, qkv_w, o, dO,
                                                 (float*)bat(ws, L.lse), (float*)bat(ws, L.Dd),
                                                 dqkv, qkv_w));

@@ -280,10 +280,12 @@ struct AttnKv {
   const int32_t* qpos = nullptr;
 };
 bool attention_tc_supported(int hd, int n, int ldq);
+// lse (optional, [B*n, hq] fp32): each row's log2-sum-exp2 of its scaled logits.
 cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
                                 int ldq, const void* vt, int vt_ld, void* o,
                                 const int32_t* seq_count = nullptr,
-                                const int32_t* seq_off = nullptr, const AttnKv* kv = nullptr);
+                                const int32_t* seq_off = nullptr, const AttnKv* kv = nullptr,
+                                float* lse = nullptr);
 
 // ---------------------------------------------------------------- backward of one layer
 
@@ -292,9 +294,19 @@ cudaError_t launch_attention_tc(const Ctx& c, int B, int n, int hq, int hkv, con
 // writes lse / Dd [B*n, hq] (log2 units / <dO, o>) and dq, dk, dv into the q, k, v
 // columns of dqkv [B*n, ldg].
 bool attn_bwd_mma_supported(int hd, int ldq, int ldo);
+// with_q false: only dk, dv (lse and Dd already written, e.g. by the tcgen05 dq kernel).
 cudaError_t launch_attn_bwd_mma(const Ctx& c, int B, int n, int hq, int hkv, int hd,
                                 const void* qkv, int ldq, const void* o, const void* dO,
-                                float* lse, float* Dd, void* dqkv, int ldg);
+                                float* lse, float* Dd, void* dqkv, int ldg, bool with_q = true);
+// dq of the attention backward on tcgen05 (bf16, head_dim 128): qkv rows [B*n, ldq] (q, k,
+// v columns), kt [B*hkv*128, kt_ld] the keys transposed (keys contiguous), o and dO
+// [B*n, hq*128] bf16, lse [B*n, hq] from the forward (log2 units); writes Dd [B*n, hq]
+// (<dO, o>) and dq into the q columns of dqkv [B*n, ldg].
+bool attn_bwd_dq_tc_supported(int hd, int ldq, int qw, int kt_ld);
+cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
+                                  int ldq, const void* kt, int kt_ld, const void* o,
+                                  const void* dO, const float* lse, float* Dd, void* dqkv,
+                                  int ldg);
 
 // Workspace bytes of run_layer_bwd for these sizes (covers a dense layer).
 size_t bwd_workspace_bytes(const xmod_dims* dm);
