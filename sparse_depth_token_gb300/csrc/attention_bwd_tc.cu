@@ -55,6 +55,8 @@ struct DqArgs {
   const __nv_bfloat16* o;     // [B*n, qw]
   const __nv_bfloat16* dO;    // [B*n, qw]
   float* Dd;                  // [B*n, hq] out
+  float* DdT;                 // [B*hq, ldS] out (per head, queries contiguous) or NULL
+  int ldS;
   __nv_bfloat16* dq;          // q columns of [B*n, ldg]
   int ldg;
   int* status;
@@ -235,6 +237,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       }
       lse2 = a.lse[grow * a.hq + h];
       a.Dd[grow * a.hq + h] = D;
+      if (a.DdT) a.DdT[(int64_t)(b * a.hq + h) * a.ldS + qi] = D;
     }
     bool ok = true;
     for (int j = 0; j < nkb; ++j) {
@@ -312,6 +315,299 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   }
 }
 
+// ---------------------------------------------------------------- dK, dV
+// One CTA per (128-key block, KV head, sequence), over the group's query heads and the
+// 64-query blocks at or after the key block:
+//   warp 0      TMA: the K and V tiles (rows) once, then per query block the rows of Q
+//               and dO and their transposes Q^T, dO^T ([head dim, queries]) into a
+//               two-stage ring
+//   warp 1      one lane issues S^T = K Q^T and dP^T = V dO^T (keys in the TMEM lanes)
+//               into two buffer pairs, then dV += P^T dO and dK += dS^T Q with P^T and
+//               dS^T read from TMEM
+//   warps 2..5  one key row per thread: P^T = exp2(scale_log2 s - lse[query]) under the
+//               causal mask, dS^T = P^T (dP^T - D[query]), both back to TMEM as bf16
+//               pairs over the first halves of their buffers
+constexpr int KVB = 128;                  // keys per CTA
+constexpr int QBK = 64;                   // queries per block
+constexpr int KV_TILE = 2 * CHUNK;        // 128 keys x 128 head dims
+constexpr int Q_CHUNK = QBK * 128;        // 64 rows x 64 columns
+constexpr int Q_TILE = 2 * Q_CHUNK;       // 64 queries x 128 head dims
+constexpr int QT_TILE = CHUNK;            // 128 head dims x 64 queries
+constexpr int KST2 = 2;                   // stages of the query ring
+constexpr int QSTAGE = 2 * Q_TILE + 2 * QT_TILE;   // Q, dO, Q^T, dO^T
+constexpr int KV_DATA = 2 * KV_TILE + KST2 * QSTAGE;
+constexpr int KV_SMEM = KV_DATA + 1024;
+static_assert((1 + 2 * KST2 + 8) * 8 + 16 <= 256, "barrier block overflows");
+
+struct DkvArgs {
+  int n, hq, hkv;
+  int qw, kw;
+  float scale_log2, scale;
+  const float* lseT;          // [B*hq, ldS]: lse (log2 units), per head, queries contiguous
+  const float* DdT;           // [B*hq, ldS]: D, same layout
+  int ldS;                    // a multiple of 64 at least n
+  __nv_bfloat16* dqkv;        // k and v columns of [B*n, ldg]
+  int ldg;
+  int* status;
+};
+
+__global__ void __launch_bounds__(THREADS, 1)
+attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
+                       const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmQt,
+                       const __grid_constant__ CUtensorMap tmDOt, const DkvArgs a) {
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t sK = base, sV = base + KV_TILE;
+  const uint32_t sSt0 = base + 2 * KV_TILE;   // stage s: Q rows, dO rows, Q^T, dO^T
+  const uint32_t sBar = (base - raw >= 256u) ? raw : base + (uint32_t)KV_DATA;
+  const uint32_t KV_FULL = sBar;
+  const uint32_t ST_FULL0 = sBar + 8, ST_EMPTY0 = ST_FULL0 + 8 * KST2;
+  const uint32_t S_FULL0 = ST_EMPTY0 + 8 * KST2, S_EMPTY0 = S_FULL0 + 16;
+  const uint32_t P_FULL0 = S_EMPTY0 + 16, P_EMPTY0 = P_FULL0 + 16;
+  const uint32_t sTmem = P_EMPTY0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + (sTmem - raw));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + (sTmem - raw) + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x, b = blockIdx.y, kb = blockIdx.z;   // key block 0 has most work
+  const int G = a.hq / a.hkv;
+  const int k0 = kb * KVB;
+  const int qb0 = k0 / QBK;                         // first query block at or after k0
+  const int nqb = (a.n + QBK - 1) / QBK - qb0;      // query blocks per head
+  const int items = k0 < a.n ? G * nqb : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(KV_FULL, 1);
+    for (int s = 0; s < KST2; ++s) {
+      mbar_init(ST_FULL0 + 8 * s, 1);
+      mbar_init(ST_EMPTY0 + 8 * s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(S_FULL0 + 8 * s, 1);
+      mbar_init(S_EMPTY0 + 8 * s, 128);
+      mbar_init(P_FULL0 + 8 * s, 128);
+      mbar_init(P_EMPTY0 + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmKV);
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmDO);
+    prefetch_tensormap(&tmQt);
+    prefetch_tensormap(&tmDOt);
+  }
+  if (warp == 1) tmem_alloc(sTmem, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;   // S^T 0/1: [0, 128); dP^T 0/1: [128, 256); dV, dK
+  const uint32_t tDV = tmem + 256u, tDK = tmem + 384u;
+  pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0 && items > 0) {
+      mbar_arrive_expect_tx(KV_FULL, 2 * KV_TILE);
+      tma_load_3d(sK, &tmKV, KV_FULL, a.qw + g * HD, k0, b);
+      tma_load_3d(sK + CHUNK, &tmKV, KV_FULL, a.qw + g * HD + 64, k0, b);
+      tma_load_3d(sV, &tmKV, KV_FULL, a.qw + a.kw + g * HD, k0, b);
+      tma_load_3d(sV + CHUNK, &tmKV, KV_FULL, a.qw + a.kw + g * HD + 64, k0, b);
+      for (int it = 0; it < items; ++it) {
+        const int s = it % KST2;
+        const int h = g * G + it / nqb, q0 = (qb0 + it % nqb) * QBK;
+        if (!mbar_wait(ST_EMPTY0 + 8 * s, ((uint32_t)(it / KST2) & 1u) ^ 1u, abort_flag,
+                       a.status))
+          break;
+        const uint32_t st = sSt0 + s * QSTAGE;
+        const int trow = (b * a.hq + h) * HD;
+        mbar_arrive_expect_tx(ST_FULL0 + 8 * s, QSTAGE);
+        tma_load_3d(st, &tmQ, ST_FULL0 + 8 * s, h * HD, q0, b);
+        tma_load_3d(st + Q_CHUNK, &tmQ, ST_FULL0 + 8 * s, h * HD + 64, q0, b);
+        tma_load_3d(st + Q_TILE, &tmDO, ST_FULL0 + 8 * s, h * HD, q0, b);
+        tma_load_3d(st + Q_TILE + Q_CHUNK, &tmDO, ST_FULL0 + 8 * s, h * HD + 64, q0, b);
+        tma_load_2d(st + 2 * Q_TILE, &tmQt, ST_FULL0 + 8 * s, q0, trow);
+        tma_load_2d(st + 2 * Q_TILE + QT_TILE, &tmDOt, ST_FULL0 + 8 * s, q0, trow);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, QBK);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD);
+      bool ok = items > 0 && mbar_wait(KV_FULL, 0, abort_flag, a.status);
+      int ns = 0, nd = 0;
+      uint64_t t0 = global_timer_ns();
+      uint32_t spins = 0;
+      while (ok && nd < items) {
+        bool progressed = false;
+        // S^T / dP^T of item i + 2 reuse buffer i & 1, holding P^T_i and dS^T_i: issued
+        // after the dV / dK MMAs of item i (the MMAs of one thread run in order)
+        if (ns < items && ns <= nd + 1) {
+          const int s = ns & 1, st = ns % KST2;
+          if (mbar_test_wait(ST_FULL0 + 8 * st, (uint32_t)(ns / KST2) & 1u) &&
+              mbar_test_wait(S_EMPTY0 + 8 * s, ((uint32_t)(ns >> 1) & 1u) ^ 1u)) {
+            tc_fence_after();
+            const uint32_t stg = sSt0 + st * QSTAGE;
+            const uint32_t dS = tmem + (uint32_t)(s * QBK), dP = tmem + 128u + (uint32_t)(s * QBK);
+#pragma unroll
+            for (int kc = 0; kc < 2; ++kc) {
+              const uint64_t ak = smem_desc_sw128(sK + kc * CHUNK);
+              const uint64_t av = smem_desc_sw128(sV + kc * CHUNK);
+              const uint64_t bq = smem_desc_sw128(stg + kc * Q_CHUNK);
+              const uint64_t bo = smem_desc_sw128(stg + Q_TILE + kc * Q_CHUNK);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                mma_bf16(dS, ak + 2ull * k, bq + 2ull * k, idesc_s, (kc | k) != 0 ? 1u : 0u);
+                mma_bf16(dP, av + 2ull * k, bo + 2ull * k, idesc_s, (kc | k) != 0 ? 1u : 0u);
+              }
+            }
+            mma_commit(S_FULL0 + 8 * s);
+            ++ns;
+            progressed = true;
+          }
+        }
+        if (nd < ns) {
+          const int s = nd & 1, st = nd % KST2;
+          if (mbar_test_wait(P_FULL0 + 8 * s, (uint32_t)(nd >> 1) & 1u)) {
+            tc_fence_after();
+            const uint32_t stg = sSt0 + st * QSTAGE;
+            const uint32_t tp = tmem + (uint32_t)(s * QBK);
+            const uint32_t tds = tmem + 128u + (uint32_t)(s * QBK);
+            const uint64_t bqt = smem_desc_sw128(stg + 2 * Q_TILE);
+            const uint64_t bot = smem_desc_sw128(stg + 2 * Q_TILE + QT_TILE);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              mma_bf16_tmem_a(tDV, tp + (uint32_t)(8 * k), bot + 2ull * k, idesc_o,
+                              (nd | k) != 0 ? 1u : 0u);
+              mma_bf16_tmem_a(tDK, tds + (uint32_t)(8 * k), bqt + 2ull * k, idesc_o,
+                              (nd | k) != 0 ? 1u : 0u);
+            }
+            mma_commit(P_EMPTY0 + 8 * s);
+            mma_commit(ST_EMPTY0 + 8 * st);
+            ++nd;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t0 = global_timer_ns();
+          spins = 0;
+          continue;
+        }
+        if ((++spins & 255u) == 0u) {
+          if (*abort_flag) break;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            report_status(a.status, XMOD_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
+    }
+  } else {
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int key = k0 + row;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    bool ok = true;
+    for (int it = 0; it < items; ++it) {
+      const int s = it & 1;
+      const int h = g * G + it / nqb, q0 = (qb0 + it % nqb) * QBK;
+      // this query block's lse and D (per head, queries contiguous; entries past n are
+      // never used: their probabilities are masked to 0)
+      const float* lrow = a.lseT + (int64_t)(b * a.hq + h) * a.ldS + q0;
+      const float* drow = a.DdT + (int64_t)(b * a.hq + h) * a.ldS + q0;
+      if (!mbar_wait(S_FULL0 + 8 * s, (uint32_t)(it >> 1) & 1u, abort_flag, a.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[QBK], dp[QBK];
+      const uint32_t srow = tmem + lane_off + (uint32_t)(s * QBK);
+      const uint32_t prow = tmem + lane_off + 128u + (uint32_t)(s * QBK);
+      tmem_ld32(srow, *reinterpret_cast<float(*)[32]>(sv));
+      tmem_ld32(srow + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+      tmem_ld32(prow, *reinterpret_cast<float(*)[32]>(dp));
+      tmem_ld32(prow + 32, *reinterpret_cast<float(*)[32]>(dp + 32));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(S_EMPTY0 + 8 * s);
+      float pp[32], pd[32];
+#pragma unroll
+      for (int c4 = 0; c4 < QBK; c4 += 4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(lrow + c4);
+        const float4 d4 = *reinterpret_cast<const float4*>(drow + c4);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pv[4], dsv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int q = q0 + c4 + e;
+          const bool okp = key < a.n && q < a.n && key <= q;
+          const float p = okp ? ex2f(fmaf(sv[c4 + e], a.scale_log2, -lv[e])) : 0.f;
+          pv[e] = p;
+          dsv[e] = okp ? p * (dp[c4 + e] - dv[e]) : 0.f;
+        }
+        pp[c4 / 2] = __uint_as_float(pack_bf16x2(pv[0], pv[1]));
+        pp[c4 / 2 + 1] = __uint_as_float(pack_bf16x2(pv[2], pv[3]));
+        pd[c4 / 2] = __uint_as_float(pack_bf16x2(dsv[0], dsv[1]));
+        pd[c4 / 2 + 1] = __uint_as_float(pack_bf16x2(dsv[2], dsv[3]));
+      }
+      // P^T and dS^T over the first halves of their buffers (read above; what the
+      // buffers held two items ago was consumed by then)
+      tmem_st32(srow, pp);
+      tmem_st32(prow, pd);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(P_FULL0 + 8 * s);
+    }
+    if (items == 0) ok = false;
+    if (ok) {
+      const int il = items - 1;
+      ok = mbar_wait(P_EMPTY0 + 8 * (il & 1), (uint32_t)(il >> 1) & 1u, abort_flag, a.status);
+    }
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16* drow_out = a.dqkv + ((int64_t)b * a.n + key) * a.ldg;
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {   // dK (scaled), then dV
+        const uint32_t src = (part == 0 ? tDK : tDV) + lane_off;
+        const float sc = part == 0 ? a.scale : 1.0f;
+        __nv_bfloat16* dst = drow_out + a.qw + (part == 0 ? 0 : a.kw) + g * HD;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(src + c * 32, v);
+          tmem_ld_wait();
+          if (key < a.n) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              uint4 q;
+              q.x = pack_bf16x2(v[e] * sc, v[e + 1] * sc);
+              q.y = pack_bf16x2(v[e + 2] * sc, v[e + 3] * sc);
+              q.z = pack_bf16x2(v[e + 4] * sc, v[e + 5] * sc);
+              q.w = pack_bf16x2(v[e + 6] * sc, v[e + 7] * sc);
+              *reinterpret_cast<uint4*>(dst + c * 32 + e) = q;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 20000000ull) {
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 }  // namespace
 
 bool attn_bwd_dq_tc_supported(int hd, int ldq, int qw, int kt_ld) {
@@ -321,7 +617,7 @@ bool attn_bwd_dq_tc_supported(int hd, int ldq, int qw, int kt_ld) {
 cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
                                   int ldq, const void* kt, int kt_ld, const void* o,
                                   const void* dO, const float* lse, float* Dd, void* dqkv,
-                                  int ldg) {
+                                  int ldg, float* DdT, int ldS) {
   if (B <= 0 || n <= 0) return cudaSuccess;
   const int qw = hq * HD, kw = hkv * HD;
   if (!attn_bwd_dq_tc_supported(HD, ldq, qw, kt_ld) || ldg % 8) return cudaErrorInvalidValue;
@@ -359,6 +655,8 @@ cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, c
   a.o = (const __nv_bfloat16*)o;
   a.dO = (const __nv_bfloat16*)dO;
   a.Dd = Dd;
+  a.DdT = DdT;
+  a.ldS = ldS;
   a.dq = (__nv_bfloat16*)dqkv;
   a.ldg = ldg;
   a.status = c.status;
@@ -371,6 +669,61 @@ cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, c
   }
   return launch_pdl(attn_bwd_dq_tc_kernel, dim3(hq, B, a.nqb), dim3(THREADS), SMEM, c.stream,
                     mQ, mDO, mK, mKt, a);
+}
+
+cudaError_t launch_attn_bwd_dkv_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
+                                   int ldq, const void* dO, const void* qt, const void* dOt,
+                                   int t_ld, const float* lseT, const float* DdT, int ldS,
+                                   void* dqkv, int ldg) {
+  if (B <= 0 || n <= 0) return cudaSuccess;
+  const int qw = hq * HD, kw = hkv * HD;
+  if (ldq % 8 || t_ld % 8 || ldg % 8 || ldS % QBK || ldS < n || hq % hkv || !tma_available())
+    return cudaErrorInvalidValue;
+  CUtensorMap mKV, mQ, mDO, mQt, mDOt;
+  {
+    const int64_t dims[3] = {ldq, n, B};
+    const int64_t strides[2] = {(int64_t)ldq * 2, (int64_t)n * ldq * 2};
+    const int kvbox[3] = {64, KVB, 1};
+    const int qbox[3] = {64, QBK, 1};
+    if (!tma_map_bf16(&mKV, qkv, 3, dims, strides, kvbox)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(&mQ, qkv, 3, dims, strides, qbox)) return cudaErrorInvalidValue;
+  }
+  {
+    const int64_t dims[3] = {qw, n, B};
+    const int64_t strides[2] = {(int64_t)qw * 2, (int64_t)n * qw * 2};
+    const int box[3] = {64, QBK, 1};
+    if (!tma_map_bf16(&mDO, dO, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const int64_t dims[2] = {n, (int64_t)B * hq * HD};
+    const int64_t strides[1] = {(int64_t)t_ld * 2};
+    const int box[2] = {64, HD};
+    if (!tma_map_bf16(&mQt, qt, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(&mDOt, dOt, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  DkvArgs a;
+  a.n = n;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.qw = qw;
+  a.kw = kw;
+  a.scale = 1.0f / sqrtf((float)HD);
+  a.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  a.lseT = lseT;
+  a.DdT = DdT;
+  a.ldS = ldS;
+  a.dqkv = (__nv_bfloat16*)dqkv;
+  a.ldg = ldg;
+  a.status = c.status;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, KV_SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(attn_bwd_dkv_tc_kernel, dim3(hkv, B, (n + KVB - 1) / KVB), dim3(THREADS),
+                    KV_SMEM, c.stream, mKV, mQ, mDO, mQt, mDOt, a);
 }
 
 }  // namespace xmod

@@ -63,12 +63,15 @@ __device__ __forceinline__ float softplus_f(float z) {
 // 64 x 64 tiles, 256 threads: each thread moves 16 elements, all loads in flight.
 constexpr int TR_T = 64;
 
+// grid.z runs over a batch of such matrices, in_bs / out_bs elements apart.
 template <typename T>
 __global__ void __launch_bounds__(256)
 transpose_kernel(int R, int Rpad, int C, const T* __restrict__ in, int64_t ldi,
-                 T* __restrict__ out, int64_t ldo) {
+                 T* __restrict__ out, int64_t ldo, int64_t in_bs, int64_t out_bs) {
   pdl_trigger();
   pdl_wait();
+  in += blockIdx.z * in_bs;
+  out += blockIdx.z * out_bs;
   __shared__ T tile[TR_T][TR_T + 1];
   const int r0 = blockIdx.y * TR_T, c0 = blockIdx.x * TR_T;
   const int tx = threadIdx.x, ty = threadIdx.y;
@@ -678,7 +681,7 @@ inline int64_t round8(int64_t v) { return (v + 7) / 8 * 8; }
 struct BwLayout {
   size_t status, s, r, idx, r_sel, dr, dvs, ds, lossp, u, qkv, vt, o, a, h, v2, gu, H, f, df,
       dae, dH, dGU, dv2, dh, da, dO, lse, Dd, dqkv, du, rstd1, rstd2, tA, tB, tW, part, qkpre,
-      dgq, dgk, kt, total;
+      dgq, dgk, kt, qt, dOt, lseT, DdT, total;
 };
 
 constexpr int kMaxChunks = 1024;   // row chunks of the column reductions
@@ -733,6 +736,11 @@ BwLayout bw_layout(const xmod_dims* dm) {
   L.dgq = take(4 * M * hd);
   L.dgk = take(4 * M * hd);
   L.kt = take(es * (size_t)dm->B * dm->n_kv_heads * hd * vtl);   // keys transposed
+  L.qt = take(es * (size_t)dm->B * hq * hd * vtl);                 // queries transposed
+  L.dOt = take(es * (size_t)dm->B * hq * hd * vtl);                // dO transposed
+  const size_t lds = ((size_t)dm->T + 63) / 64 * 64;
+  L.lseT = take(4 * (size_t)dm->B * hq * lds);
+  L.DdT = take(4 * (size_t)dm->B * hq * lds);
   L.total = off;
   return L;
 }
@@ -752,18 +760,21 @@ inline char* bat(void* ws, size_t off) { return (char*)ws + off; }
 
 template <typename T>
 cudaError_t transpose_t(const Ctx& c, int R, int Rpad, int C, const void* in, int64_t ldi,
-                        void* out, int64_t ldo) {
-  if (R <= 0 || C <= 0) return cudaSuccess;
-  const dim3 grid((C + TR_T - 1) / TR_T, (Rpad + TR_T - 1) / TR_T);
+                        void* out, int64_t ldo, int batch, int64_t in_bs, int64_t out_bs) {
+  if (R <= 0 || C <= 0 || batch <= 0) return cudaSuccess;
+  const dim3 grid((C + TR_T - 1) / TR_T, (Rpad + TR_T - 1) / TR_T, batch);
   return launch_pdl(transpose_kernel<T>, grid, dim3(32, 8), 0, c.stream, R, Rpad, C,
-                    (const T*)in, ldi, (T*)out, ldo);
+                    (const T*)in, ldi, (T*)out, ldo, in_bs, out_bs);
 }
 
+// out[c, r] = in[r, c] (zero for R <= r < Rpad); with batch > 1, `batch` such matrices,
+// in_bs / out_bs elements apart.
 cudaError_t transpose(const Ctx& c, xmod_dtype dt, int R, int Rpad, int C, const void* in,
-                      int64_t ldi, void* out, int64_t ldo) {
+                      int64_t ldi, void* out, int64_t ldo, int batch = 1, int64_t in_bs = 0,
+                      int64_t out_bs = 0) {
   return dt == XMOD_BF16
-             ? transpose_t<__nv_bfloat16>(c, R, Rpad, C, in, ldi, out, ldo)
-             : transpose_t<float>(c, R, Rpad, C, in, ldi, out, ldo);
+             ? transpose_t<__nv_bfloat16>(c, R, Rpad, C, in, ldi, out, ldo, batch, in_bs, out_bs)
+             : transpose_t<float>(c, R, Rpad, C, in, ldi, out, ldo, batch, in_bs, out_bs);
 }
 
 // C[M, N] = A[M, K] B[N, K]^T, both K-contiguous, stored plain (fp32 if f32out, else
@@ -1092,17 +1103,28 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   E* dqkv = (E*)bat(ws, L.dqkv);
   const int kt_ld = (int)round8(n);
   const bool dq_tc = mma_attn && v_transposed && attn_bwd_dq_tc_supported(hd, qkv_w, qw, kt_ld);
-  if (dq_tc) {   // dq on tcgen05 (lse from the forward), dk and dv on the warp-level MMA
+  if (dq_tc) {   // tcgen05 (lse from the forward): dq, then dk and dv
     E* kt = (E*)bat(ws, L.kt);
-    for (int bb = 0; bb < B; ++bb)   // the keys transposed, per sequence: [hkv * hd, keys]
-      BW_RUN("bwd_transpose", transpose(c, dt, n, n, kw, qkv + ((size_t)bb * n) * qkv_w + qw,
-                                        qkv_w, kt + (size_t)bb * kw * kt_ld, kt_ld));
+    E* qt = (E*)bat(ws, L.qt);
+    E* dOt = (E*)bat(ws, L.dOt);
+    float* lseT = (float*)bat(ws, L.lseT);
+    float* DdT = (float*)bat(ws, L.DdT);
+    const int ldS = (n + 63) / 64 * 64;
+    // per sequence, transposed: keys [hkv * hd, keys], queries and dO [hq * hd, queries],
+    // and the rows' lse per head [hq, queries]
+    BW_RUN("bwd_transpose", transpose(c, dt, n, n, kw, qkv + qw, qkv_w, kt, kt_ld, B,
+                                      (int64_t)n * qkv_w, (int64_t)kw * kt_ld));
+    BW_RUN("bwd_transpose", transpose(c, dt, n, n, qw, qkv, qkv_w, qt, kt_ld, B,
+                                      (int64_t)n * qkv_w, (int64_t)qw * kt_ld));
+    BW_RUN("bwd_transpose", transpose(c, dt, n, n, qw, dO, qw, dOt, kt_ld, B, (int64_t)n * qw,
+                                      (int64_t)qw * kt_ld));
+    BW_RUN("bwd_transpose", transpose_t<float>(c, n, n, hq, bat(ws, L.lse), hq, lseT, ldS, B,
+                                               (int64_t)n * hq, (int64_t)hq * ldS));
     BW_RUN("bwd_attention", launch_attn_bwd_dq_tc(c, B, n, hq, hkv, qkv, qkv_w, kt, kt_ld, o, dO,
                                                   (const float*)bat(ws, L.lse),
-                                                  (float*)bat(ws, L.Dd), dqkv, qkv_w));
-    BW_RUN("bwd_attention", launch_attn_bwd_mma(c, B, n, hq, hkv, hd, qkv, qkv_w, o, dO,
-                                                (float*)bat(ws, L.lse), (float*)bat(ws, L.Dd),
-                                                dqkv, qkv_w, false));
+                                                  (float*)bat(ws, L.Dd), dqkv, qkv_w, DdT, ldS));
+    BW_RUN("bwd_attention", launch_attn_bwd_dkv_tc(c, B, n, hq, hkv, qkv, qkv_w, dO, qt, dOt,
+                                                   kt_ld, lseT, DdT, ldS, dqkv, qkv_w));
   } else if (mma_attn) {   // bf16: warp-level tensor-core MMA, v rows and dO in bf16
     BW_RUN("bwd_attention", launch_attn_bwd_mma(c, B, n, hq, hkv, hd, qkv, qkv_w, o, dO,
                                                 (float*)bat(ws, L.lse), (float*)bat(ws, L.Dd),

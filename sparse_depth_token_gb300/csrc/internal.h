@@ -306,7 +306,14 @@ bool attn_bwd_dq_tc_supported(int hd, int ldq, int qw, int kt_ld);
 cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
                                   int ldq, const void* kt, int kt_ld, const void* o,
                                   const void* dO, const float* lse, float* Dd, void* dqkv,
-                                  int ldg);
+                                  int ldg, float* DdT = nullptr, int ldS = 0);
+// dk and dv on tcgen05: qt and dOt [B*hq*128, t_ld] the queries and dO transposed per
+// sequence (queries contiguous); lseT and DdT [B*hq, ldS] (ldS a multiple of 64, >= n)
+// the rows' lse and D per head; writes the k and v columns of dqkv [B*n, ldg].
+cudaError_t launch_attn_bwd_dkv_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
+                                   int ldq, const void* dO, const void* qt, const void* dOt,
+                                   int t_ld, const float* lseT, const float* DdT, int ldS,
+                                   void* dqkv, int ldg);
 
 // Workspace bytes of run_layer_bwd for these sizes (covers a dense layer).
 size_t bwd_workspace_bytes(const xmod_dims* dm);
