@@ -259,9 +259,9 @@ def layer_fwd(dm: Dims, kind, K, gate, layer: Layer, x, bias=None, idx_force=Non
 
 def layer_bwd(dm: Dims, kind, K, gate, layer: Layer, x, dy, bias=None, idx_force=None,
               route_coef=0.0):
-    """Backward of one layer (DENSE, SPARSE, or the FullAttn / Routed-FFN halves ATTN, RFFN)
-    for the objective sum(dy * y) + route_coef *
-    L_route (Eq. 9 on the layer's top-(T/K) decisions), the selection held fixed.
+    """Backward of one layer (DENSE, SPARSE, the FullAttn / Routed-FFN halves ATTN, RFFN,
+    or the Selected-Q / full-KV control FULLKV) for the objective sum(dy * y) + route_coef
+    * L_route (Eq. 9 on the layer's top-(T/K) decisions), the selection held fixed.
     Returns dict(dx, grads {name: array shaped as the weight}, varsigma, route_loss, idx)."""
     x, xp = _d(x)
     dy, gp = _d(dy)
@@ -280,7 +280,7 @@ def layer_bwd(dm: Dims, kind, K, gate, layer: Layer, x, dy, bias=None, idx_force
     gs = LayerGrad(*[grads[k].ctypes.data_as(_DP) for k in main], 0.0,
                    *[grads[k].ctypes.data_as(_DP) if k in grads else None for k in ("gq", "gk")])
     dx = np.empty_like(x)
-    routed = kind in (SPARSE, RFFN)
+    routed = kind in (SPARSE, RFFN, FULLKV)
     n = T // K if routed else 1
     idx = np.zeros((B, n), np.int32)
     loss = ctypes.c_double(0.0)

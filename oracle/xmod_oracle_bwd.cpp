@@ -64,13 +64,16 @@ void oracle_qk_transform(int rows, int heads, int hd, double* x, const double* g
                          double theta, const int32_t* pos);
 void oracle_ffn_rows(const oracle_dims* dm, int nr, const double* xs, const oracle_layer_w* w,
                      double* f_out);
+void oracle_block_fullkv(const oracle_dims* dm, int T, const double* x_seq,
+                         const oracle_layer_w* w, const int32_t* pos, int n, double* a_out,
+                         double* f_out);
 
 }  // extern "C"
 
 namespace {
 
 enum { OK = 0, BAD_ARG = -1 };
-enum { DENSE = 0, SPARSE = 1, ATTN = 2, RFFN = 3 };
+enum { DENSE = 0, SPARSE = 1, ATTN = 2, RFFN = 3, FULLKV = 4 };
 enum { GATE_XMOD = 0, GATE_MOD = 1 };
 
 double sigmoid(double z) { return 1.0 / (1.0 + std::exp(-z)); }
@@ -162,46 +165,64 @@ void qk_bwd(int rows, int heads, int hd, const double* pre, const double* gain, 
   }
 }
 
-// The block's backward on one sequence's compact rows xs [n, d], given the gradients
-// reaching its two residuals, da_ext and df [n, d]. Adds to dxs [n, d] and to gw.
-// Compact row j sits at original position pos[j] (NULL: j), which only the rotation sees.
-// attn / ffn select the halves (X-MoD notes, "mechanism controls": a FullAttn layer is the
-// attention half with its residual, a Routed-FFN layer the FFN half on RMSNorm(xs) g2, i.e.
-// a = 0); both: the whole block.
-void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_layer_w* w,
-               const double* da_ext, const double* df, double* dxs, oracle_layer_grad* gw,
-               const int32_t* pos, bool attn = true, bool ffn = true) {
+// The block's backward for one sequence. Keys and values come from the nkv rows
+// xkv [nkv, d]; the nq queries are the rows qrow[i] of xkv (NULL: i, nq == nkv), in
+// ascending order, and query i sees the keys j <= qrow[i]. The residual rows of the
+// block are xs_i = xkv[qrow[i]], and the gradients reaching its two residuals are da_ext
+// and df [nq, d]. Adds to dxkv [nkv, d] and to gw. Row j of xkv sits at original
+// position kvpos[j] (NULL: j), which only the rotation sees.
+//   sparse layer: xkv = the compact selected rows, qrow = NULL, kvpos = their positions;
+//   dense layer:  xkv = the whole sequence, qrow = NULL, kvpos = NULL;
+//   Selected-Q / full-KV (X-MoD notes, "mechanism controls"): xkv = the whole sequence,
+//                 qrow = the selected positions, kvpos = NULL.
+// attn / ffn select the halves (same section: a FullAttn layer is the attention half with
+// its residual, a Routed-FFN layer the FFN half on RMSNorm(xs) g2, i.e. a = 0); both: the
+// whole block.
+void block_bwd(const oracle_dims* dm, int nkv, const double* xkv, const oracle_layer_w* w,
+               int nq, const int32_t* qrow, const double* da_ext, const double* df,
+               double* dxkv, oracle_layer_grad* gw, const int32_t* kvpos, bool attn = true,
+               bool ffn = true) {
   const int d = dm->d, hq = dm->hq, hkv = dm->hkv, hd = dm->hd, F = dm->F;
   const int G = hq / hkv, qw = hq * hd, kw = hkv * hd;
   const double scale = 1.0 / std::sqrt((double)hd);
+  std::vector<int32_t> qr(nq), qpos(nq);   // query i: its row of xkv and its position
+  for (int i = 0; i < nq; ++i) {
+    qr[i] = qrow ? qrow[i] : i;
+    qpos[i] = kvpos ? kvpos[qr[i]] : qr[i];
+  }
+  std::vector<double> xs((int64_t)nq * d);
+  for (int i = 0; i < nq; ++i)
+    std::memcpy(&xs[(int64_t)i * d], xkv + (int64_t)qr[i] * d, sizeof(double) * d);
   // ---- forward, keeping what the backward reads
-  std::vector<double> u((int64_t)n * d), x1((int64_t)n * d), rho1(n);
-  std::vector<double> q((int64_t)n * qw), k((int64_t)n * kw), v((int64_t)n * kw);
+  std::vector<double> u((int64_t)nkv * d), x1((int64_t)nkv * d), rho1(nkv), uq((int64_t)nq * d);
+  std::vector<double> q((int64_t)nq * qw), k((int64_t)nkv * kw), v((int64_t)nkv * kw);
   std::vector<double> q_pre, k_pre;
   std::vector<double> P, o;
-  std::vector<double> a((int64_t)n * d, 0.0), hh((int64_t)n * d);
+  std::vector<double> a((int64_t)nq * d, 0.0), hh((int64_t)nq * d);
   const bool extras = w->gq || w->gk || w->rope_theta > 0.0;
   if (attn) {
-  rms_fwd(n, d, xs, w->g1, dm->eps, u.data(), x1.data(), rho1.data());
-  oracle_linear(n, d, qw, u.data(), w->wq, q.data());
-  oracle_linear(n, d, kw, u.data(), w->wk, k.data());
-  oracle_linear(n, d, kw, u.data(), w->wv, v.data());
+  rms_fwd(nkv, d, xkv, w->g1, dm->eps, u.data(), x1.data(), rho1.data());
+  for (int i = 0; i < nq; ++i)
+    std::memcpy(&uq[(int64_t)i * d], &u[(int64_t)qr[i] * d], sizeof(double) * d);
+  oracle_linear(nq, d, qw, uq.data(), w->wq, q.data());
+  oracle_linear(nkv, d, kw, u.data(), w->wk, k.data());
+  oracle_linear(nkv, d, kw, u.data(), w->wv, v.data());
   // QK-norm and rotation at the original positions, the projections kept for the backward
   if (extras) {
     q_pre = q;
     k_pre = k;
-    oracle_qk_transform(n, hq, hd, q.data(), w->gq, dm->eps, w->rope_theta, pos);
-    oracle_qk_transform(n, hkv, hd, k.data(), w->gk, dm->eps, w->rope_theta, pos);
+    oracle_qk_transform(nq, hq, hd, q.data(), w->gq, dm->eps, w->rope_theta, qpos.data());
+    oracle_qk_transform(nkv, hkv, hd, k.data(), w->gk, dm->eps, w->rope_theta, kvpos);
   }
-  // P[h][i][j], causal (j <= i), and o
-  P.assign((int64_t)hq * n * n, 0.0);
-  o.assign((int64_t)n * qw, 0.0);
+  // P[h][i][j] over the keys j <= qr[i], and o
+  P.assign((int64_t)hq * nq * nkv, 0.0);
+  o.assign((int64_t)nq * qw, 0.0);
   for (int h = 0; h < hq; ++h) {
     const int g = h / G;
-    for (int i = 0; i < n; ++i) {
-      double* p = &P[((int64_t)h * n + i) * n];
+    for (int i = 0; i < nq; ++i) {
+      double* p = &P[((int64_t)h * nq + i) * nkv];
       double m = -INFINITY;
-      for (int j = 0; j <= i; ++j) {
+      for (int j = 0; j <= qr[i]; ++j) {
         double acc = 0.0;
         for (int c = 0; c < hd; ++c)
           acc += q[(int64_t)i * qw + h * hd + c] * k[(int64_t)j * kw + g * hd + c];
@@ -209,23 +230,24 @@ void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_laye
         m = std::max(m, p[j]);
       }
       double den = 0.0;
-      for (int j = 0; j <= i; ++j) {
+      for (int j = 0; j <= qr[i]; ++j) {
         p[j] = std::exp(p[j] - m);
         den += p[j];
       }
-      for (int j = 0; j <= i; ++j) p[j] /= den;
+      for (int j = 0; j <= qr[i]; ++j) p[j] /= den;
       for (int c = 0; c < hd; ++c) {
         double acc = 0.0;
-        for (int j = 0; j <= i; ++j) acc += p[j] * v[(int64_t)j * kw + g * hd + c];
+        for (int j = 0; j <= qr[i]; ++j) acc += p[j] * v[(int64_t)j * kw + g * hd + c];
         o[(int64_t)i * qw + h * hd + c] = acc;
       }
     }
   }
-  oracle_linear(n, qw, d, o.data(), w->wo, a.data());
+  oracle_linear(nq, qw, d, o.data(), w->wo, a.data());
   }
-  for (int64_t i = 0; i < (int64_t)n * d; ++i) hh[i] = xs[i] + a[i];
-  std::vector<double> dh((int64_t)n * d, 0.0);
+  for (int64_t i = 0; i < (int64_t)nq * d; ++i) hh[i] = xs[i] + a[i];
+  std::vector<double> dh((int64_t)nq * d, 0.0);
   if (ffn) {
+  const int n = nq;
   std::vector<double> v2((int64_t)n * d), x2((int64_t)n * d), rho2(n);
   rms_fwd(n, d, hh.data(), w->g2, dm->eps, v2.data(), x2.data(), rho2.data());
   std::vector<double> Gp((int64_t)n * F), Up((int64_t)n * F), H((int64_t)n * F);
@@ -251,31 +273,32 @@ void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_laye
   // ---- v2 = RMSNorm(h) g2, h = xs + a
   rms_bwd(n, d, dv2.data(), w->g2, x2.data(), rho2.data(), dh.data(), gw->g2);
   }
-  for (int64_t i = 0; i < (int64_t)n * d; ++i) dxs[i] += dh[i];
+  for (int i = 0; i < nq; ++i)   // h = xs + a: dh reaches the query's own row
+    for (int c = 0; c < d; ++c) dxkv[(int64_t)qr[i] * d + c] += dh[(int64_t)i * d + c];
   if (!attn) return;
-  std::vector<double> da((int64_t)n * d);
-  for (int64_t i = 0; i < (int64_t)n * d; ++i) da[i] = dh[i] + da_ext[i];
+  std::vector<double> da((int64_t)nq * d);
+  for (int64_t i = 0; i < (int64_t)nq * d; ++i) da[i] = dh[i] + da_ext[i];
   // ---- a = o Wo^T
-  linear_dw(n, qw, d, da.data(), o.data(), gw->wo);
-  std::vector<double> dO((int64_t)n * qw, 0.0);
-  linear_dx(n, qw, d, da.data(), w->wo, dO.data());
+  linear_dw(nq, qw, d, da.data(), o.data(), gw->wo);
+  std::vector<double> dO((int64_t)nq * qw, 0.0);
+  linear_dx(nq, qw, d, da.data(), w->wo, dO.data());
   // ---- attention
-  std::vector<double> dq((int64_t)n * qw, 0.0), dk((int64_t)n * kw, 0.0),
-      dv((int64_t)n * kw, 0.0);
+  std::vector<double> dq((int64_t)nq * qw, 0.0), dk((int64_t)nkv * kw, 0.0),
+      dv((int64_t)nkv * kw, 0.0);
   for (int h = 0; h < hq; ++h) {
     const int g = h / G;
-    for (int i = 0; i < n; ++i) {
-      const double* p = &P[((int64_t)h * n + i) * n];
-      std::vector<double> dP(i + 1);
+    for (int i = 0; i < nq; ++i) {
+      const double* p = &P[((int64_t)h * nq + i) * nkv];
+      std::vector<double> dP(qr[i] + 1);
       double Di = 0.0;
-      for (int j = 0; j <= i; ++j) {
+      for (int j = 0; j <= qr[i]; ++j) {
         double acc = 0.0;
         for (int c = 0; c < hd; ++c)
           acc += dO[(int64_t)i * qw + h * hd + c] * v[(int64_t)j * kw + g * hd + c];
         dP[j] = acc;
         Di += p[j] * acc;
       }
-      for (int j = 0; j <= i; ++j) {
+      for (int j = 0; j <= qr[i]; ++j) {
         const double dS = p[j] * (dP[j] - Di);
         for (int c = 0; c < hd; ++c) {
           dv[(int64_t)j * kw + g * hd + c] += p[j] * dO[(int64_t)i * qw + h * hd + c];
@@ -286,19 +309,21 @@ void block_bwd(const oracle_dims* dm, int n, const double* xs, const oracle_laye
     }
   }
   if (extras) {   // back through the rotation and the QK-norm
-    qk_bwd(n, hq, hd, q_pre.data(), w->gq, dm->eps, w->rope_theta, pos, dq.data(), gw->gq);
-    qk_bwd(n, hkv, hd, k_pre.data(), w->gk, dm->eps, w->rope_theta, pos, dk.data(), gw->gk);
+    qk_bwd(nq, hq, hd, q_pre.data(), w->gq, dm->eps, w->rope_theta, qpos.data(), dq.data(), gw->gq);
+    qk_bwd(nkv, hkv, hd, k_pre.data(), w->gk, dm->eps, w->rope_theta, kvpos, dk.data(), gw->gk);
   }
-  // ---- q, k, v = u W^T
-  linear_dw(n, d, qw, dq.data(), u.data(), gw->wq);
-  linear_dw(n, d, kw, dk.data(), u.data(), gw->wk);
-  linear_dw(n, d, kw, dv.data(), u.data(), gw->wv);
-  std::vector<double> du((int64_t)n * d, 0.0);
-  linear_dx(n, d, qw, dq.data(), w->wq, du.data());
-  linear_dx(n, d, kw, dk.data(), w->wk, du.data());
-  linear_dx(n, d, kw, dv.data(), w->wv, du.data());
-  // ---- u = RMSNorm(xs) g1
-  rms_bwd(n, d, du.data(), w->g1, x1.data(), rho1.data(), dxs, gw->g1);
+  // ---- q = u_q Wq^T (the queries' rows of u), k, v = u [Wk | Wv]^T (every row)
+  linear_dw(nq, d, qw, dq.data(), uq.data(), gw->wq);
+  linear_dw(nkv, d, kw, dk.data(), u.data(), gw->wk);
+  linear_dw(nkv, d, kw, dv.data(), u.data(), gw->wv);
+  std::vector<double> du((int64_t)nkv * d, 0.0), duq((int64_t)nq * d, 0.0);
+  linear_dx(nq, d, qw, dq.data(), w->wq, duq.data());
+  for (int i = 0; i < nq; ++i)
+    for (int c = 0; c < d; ++c) du[(int64_t)qr[i] * d + c] += duq[(int64_t)i * d + c];
+  linear_dx(nkv, d, kw, dk.data(), w->wk, du.data());
+  linear_dx(nkv, d, kw, dv.data(), w->wv, du.data());
+  // ---- u = RMSNorm(xkv) g1
+  rms_bwd(nkv, d, du.data(), w->g1, x1.data(), rho1.data(), dxkv, gw->g1);
 }
 
 // a and f of the block on compact rows xs [n, d] (all rows), for the gate derivatives.
@@ -313,8 +338,9 @@ void oracle_block_rows_pos(const oracle_dims* dm, int n, const double* xs,
                            const oracle_layer_w* w, const int32_t* rows, int nrows,
                            double* a_out, double* f_out, const int32_t* pos);
 
-// Backward of one layer (kind DENSE or SPARSE; Eq. 7 or Eq. 6 gating), see the file
-// comment. x_in, dy, dx [B, T, d]; bias [B, T] or NULL; idx_force [B, n] or NULL (the
+// Backward of one layer (any kind: DENSE, SPARSE, the FullAttn / Routed-FFN halves ATTN
+// and RFFN, the Selected-Q / full-KV FULLKV; Eq. 7 or Eq. 6 gating), see the file comment.
+// x_in, dy, dx [B, T, d]; bias [B, T] or NULL; idx_force [B, n] or NULL (the
 // oracle's own top-(T/K) then); idx_out [B, n] or NULL receives the selection used.
 // route_loss (sparse only, NULL allowed) receives L_route of Eq. 9.
 int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const oracle_layer_w* w,
@@ -324,7 +350,7 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
   const int B = dm->B, T = dm->T, d = dm->d, F = dm->F;
   const int qw = dm->hq * dm->hd, kw = dm->hkv * dm->hd;
   if (B <= 0 || T <= 0 || d <= 0 || dm->hq % dm->hkv) return BAD_ARG;
-  if (kind != DENSE && kind != SPARSE && kind != ATTN && kind != RFFN) return BAD_ARG;
+  if (kind < DENSE || kind > FULLKV) return BAD_ARG;
   if ((w->gq && !gw->gq) || (w->gk && !gw->gk)) return BAD_ARG;
   const int64_t BT = (int64_t)B * T;
   std::memset(gw->w_r, 0, sizeof(double) * d);
@@ -348,7 +374,7 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
     for (int b = 0; b < B; ++b) {
       const double* xb = x_in + (int64_t)b * T * d;
       const double* gb = dy + (int64_t)b * T * d;
-      block_bwd(dm, T, xb, w, gb, gb, dx + (int64_t)b * T * d, gw, nullptr, true,
+      block_bwd(dm, T, xb, w, T, nullptr, gb, gb, dx + (int64_t)b * T * d, gw, nullptr, true,
                 kind == DENSE);
     }
     return OK;
@@ -387,6 +413,8 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
       std::memcpy(&xs[(int64_t)j * d], x_in + ((int64_t)b * T + ib[j]) * d, sizeof(double) * d);
     if (kind == RFFN)   // FFN half only: f = FFN(RMSNorm(xs) g2), a = 0
       oracle_ffn_rows(dm, n, xs.data(), w, f.data());
+    else if (kind == FULLKV)
+      oracle_block_fullkv(dm, T, x_in + (int64_t)b * T * d, w, ib, n, a.data(), f.data());
     else
       block_af(dm, n, xs.data(), w, a.data(), f.data(), ib);
     std::vector<double> da_ext((int64_t)n * d), df((int64_t)n * d), dxs((int64_t)n * d, 0.0);
@@ -409,8 +437,13 @@ int oracle_layer_bwd(const oracle_dims* dm, int kind, int K, int gate, const ora
       }
       ds[t] += dr * rt * (1.0 - rt);
     }
-    block_bwd(dm, n, xs.data(), w, da_ext.data(), df.data(), dxs.data(), gw, ib, kind != RFFN,
-              true);
+    if (kind == FULLKV) {   // keys and values from every token: straight into the sequence's dx
+      block_bwd(dm, T, x_in + (int64_t)b * T * d, w, n, ib, da_ext.data(), df.data(),
+                dx + (int64_t)b * T * d, gw, nullptr);
+      continue;
+    }
+    block_bwd(dm, n, xs.data(), w, n, nullptr, da_ext.data(), df.data(), dxs.data(), gw, ib,
+              kind != RFFN, true);
     for (int j = 0; j < n; ++j)   // the gather's backward: back to the token's row
       for (int c = 0; c < d; ++c) dx[((int64_t)b * T + ib[j]) * d + c] += dxs[(int64_t)j * d + c];
   }

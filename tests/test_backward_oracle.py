@@ -7,7 +7,9 @@ difference of J along a random direction of x, of every weight and of varsigma m
 equal the inner product of that direction with the returned gradient. The selection is
 held fixed on both sides (forced indices), as the backward holds it; with the optional
 QK-norm gains and rotary embedding too. Plus closed forms: the skip path of unselected
-rows, the Eq. 9 value at p = 1/2, an FFN with W_down = 0.
+rows, the Eq. 9 value at p = 1/2, an FFN with W_down = 0; for the Selected-Q / full-KV
+control, the K = 1 case (every token selected: the sparse layer) and the rows that no
+query sees.
 """
 import numpy as np
 import pytest
@@ -33,7 +35,7 @@ def _weights(g, scale=0.3):
 def _objective(dm, kind, gate, W, vs, x, dy, bias, idx, coef):
     out = O.layer_fwd(dm, kind, K, gate, O.Layer(W, vs), x, bias=bias, idx_force=idx)
     val = float((dy * out["y"]).sum())
-    if kind in (O.SPARSE, O.RFFN) and coef:
+    if kind in (O.SPARSE, O.RFFN, O.FULLKV) and coef:
         s = out["s"]
         p = 1.0 / (1.0 + np.exp(-s))
         q = np.zeros_like(s)
@@ -202,3 +204,89 @@ def test_variant_layer_bwd_matches_finite_differences(kind, gate, coef):
     for name in unused:
         assert np.all(r["grads"][name] == 0.0), name
 
+
+
+@pytest.mark.parametrize("gate,coef,extras", [(O.GATE_XMOD, 0.0, False), (O.GATE_MOD, 0.5, False),
+                                              (O.GATE_XMOD, 0.3, True)])
+def test_fullkv_layer_bwd_matches_finite_differences(gate, coef, extras):
+    """Selected-Q / full-KV control (X-MoD notes, "mechanism controls"): the selected tokens
+    are the queries, every token provides keys and values, so the gradient reaches the
+    unselected rows through k and v; central differences of the forward oracle along random
+    directions of x, of every weight and of varsigma, the selection held fixed."""
+    g = np.random.default_rng(90 + gate + 2 * int(extras))
+    dm = O.dims(B, T, d, HQ, HKV, HD, F)
+    W = _weights(g)
+    if extras:
+        W["gq"] = 1 + 0.2 * g.standard_normal(HD)
+        W["gk"] = 1 + 0.2 * g.standard_normal(HD)
+        W["rope_theta"] = 1e4
+    vs = 0.9
+    x = g.standard_normal((B, T, d))
+    dy = g.standard_normal((B, T, d))
+    bias = 0.1 * g.standard_normal((B, T))
+    r = O.layer_bwd(dm, O.FULLKV, K, gate, O.Layer(W, vs), x, dy, bias=bias, route_coef=coef)
+    idx = r["idx"]
+    eps = 1e-6
+
+    def J(x_=x, W_=W, vs_=vs):
+        return _objective(dm, O.FULLKV, gate, W_, vs_, x_, dy, bias, idx, coef)
+
+    def check(num, ana, what):
+        assert abs(num - ana) <= 1e-6 * max(1.0, abs(num)), f"{what}: fd {num} vs grad {ana}"
+
+    v = g.standard_normal(x.shape)
+    check((J(x_=x + eps * v) - J(x_=x - eps * v)) / (2 * eps), float((r["dx"] * v).sum()), "x")
+    names = NAMES + (("gq", "gk") if extras else ())
+    for name in names:
+        v = g.standard_normal(np.shape(W[name]))
+        Wp, Wm = dict(W), dict(W)
+        Wp[name] = W[name] + eps * v
+        Wm[name] = W[name] - eps * v
+        check((J(W_=Wp) - J(W_=Wm)) / (2 * eps), float((r["grads"][name] * v).sum()), name)
+    check((J(vs_=vs + eps) - J(vs_=vs - eps)) / (2 * eps), r["varsigma"], "varsigma")
+
+
+@pytest.mark.parametrize("gate", [O.GATE_XMOD, O.GATE_MOD])
+def test_fullkv_with_every_token_selected_is_the_sparse_layer(gate):
+    """K = 1 selects every token: the queries are all rows and the keys are the same rows,
+    so the full-KV layer and the sparse layer are one function, gradients included."""
+    g = np.random.default_rng(95 + gate)
+    dm = O.dims(B, T, d, HQ, HKV, HD, F)
+    W = _weights(g)
+    W["gk"] = 1 + 0.2 * g.standard_normal(HD)
+    W["rope_theta"] = 500.0
+    x = g.standard_normal((B, T, d))
+    dy = g.standard_normal((B, T, d))
+    bias = 0.1 * g.standard_normal((B, T))
+    a = O.layer_bwd(dm, O.FULLKV, 1, gate, O.Layer(W, 1.2), x, dy, bias=bias, route_coef=0.4)
+    b = O.layer_bwd(dm, O.SPARSE, 1, gate, O.Layer(W, 1.2), x, dy, bias=bias, route_coef=0.4)
+    np.testing.assert_allclose(a["dx"], b["dx"], rtol=1e-11, atol=1e-12)
+    for name in a["grads"]:
+        np.testing.assert_allclose(a["grads"][name], b["grads"][name], rtol=1e-11, atol=1e-12,
+                                   err_msg=name)
+    assert a["varsigma"] == pytest.approx(b["varsigma"], rel=1e-11)
+    assert a["route_loss"] == pytest.approx(b["route_loss"], rel=1e-14)
+
+
+def test_fullkv_rows_no_query_sees():
+    """Without Eq. 9, a token after the sequence's last selected position is no query's key
+    and is not selected: its dx is dy exactly. With W_k = W_v = 0 no gradient reaches any
+    unselected row (the keys and values are zero whatever the row holds); with the weights
+    nonzero, unselected rows before the last selected position do receive one."""
+    g = np.random.default_rng(97)
+    dm = O.dims(B, T, d, HQ, HKV, HD, F)
+    W = _weights(g)
+    x = g.standard_normal((B, T, d))
+    dy = g.standard_normal((B, T, d))
+    r = O.layer_bwd(dm, O.FULLKV, K, O.GATE_XMOD, O.Layer(W, 1.1), x, dy)
+    sel = np.zeros((B, T), bool)
+    np.put_along_axis(sel, r["idx"], True, 1)
+    after = np.arange(T)[None, :] > r["idx"].max(axis=1, keepdims=True)
+    before = ~sel & ~after
+    assert after.any()
+    np.testing.assert_array_equal(r["dx"][after], dy[after])
+    assert before.any() and np.all(np.any(r["dx"][before] != dy[before], axis=-1))
+    W["wk"] = np.zeros_like(W["wk"])
+    W["wv"] = np.zeros_like(W["wv"])
+    r0 = O.layer_bwd(dm, O.FULLKV, K, O.GATE_XMOD, O.Layer(W, 1.1), x, dy)
+    np.testing.assert_array_equal(r0["dx"][~sel], dy[~sel])
