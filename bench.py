@@ -598,18 +598,29 @@ def backward_work(w: I.Workload) -> dict:
         out[kind] = out.get(kind, 0.0) + float(v)
 
     qw, kw = w.hq * w.hd, w.hkv * w.hd
-    for kind in schedule(w, "xmod"):
-        n = w.T // w.K if kind == SPARSE else w.T
+    BT = w.B * w.T
+    for kind in schedule(w):
+        n = w.T // w.K if routed(kind) else w.T
         M = w.B * n
-        add("gemm_qkv", 2 * M * w.d * (qw + 2 * kw))
-        add("attention", 2 * w.B * n * n * w.hd * w.hq)
-        add("gemm_o_residual", 2 * M * qw * w.d)
-        add("gemm_gate_up", 4 * M * w.d * w.F)
-        add("gemm_down", 2 * M * w.F * w.d)
-        proj = 2 * M * w.d * (qw + 2 * kw) + 2 * M * qw * w.d + 6 * M * w.d * w.F
+        proj = 0
+        if kind != RFFN:   # the attention half
+            if kind == FULLKV:   # k, v of every token; a query at position p sees p + 1 keys
+                qkv = 2 * BT * w.d * 2 * kw + 2 * M * w.d * qw
+                att = 2 * M * (w.T / 2) * w.hd * w.hq    # one product, T / 2 keys on average
+            else:
+                qkv = 2 * M * w.d * (qw + 2 * kw)
+                att = w.B * n * n * w.hd * w.hq          # one causal n x n x hd product
+            add("gemm_qkv", qkv)
+            add("attention", 2 * att)
+            add("gemm_o_residual", 2 * M * qw * w.d)
+            add("bwd_attention", 5 * att)
+            proj += qkv + 2 * M * qw * w.d
+        if kind != ATTN:   # the FFN half
+            add("gemm_gate_up", 4 * M * w.d * w.F)
+            add("gemm_down", 2 * M * w.F * w.d)
+            proj += 6 * M * w.d * w.F
         add("bwd_gemm_dw", proj)
         add("bwd_gemm_dx", proj)
-        add("bwd_attention", 5 * w.B * n * n * w.hd * w.hq)
     return out
 
 
@@ -630,9 +641,9 @@ def run_backward(args):
     dev = torch.device("cuda", 0)
     X.load()
     w = I.WORKLOADS[args.workload]
-    kinds = schedule(w, "xmod")
-    n_sparse = sum(1 for k in kinds if k == SPARSE)
-    sel_per_step = n_sparse * w.B * (w.T // w.K)
+    kinds = schedule(w)
+    n_routed = sum(1 for k in kinds if routed(k))
+    sel_per_step = n_routed * w.B * (w.T // w.K)
     layers = I.all_layer_weights(w, len(kinds))
 
     def to_dev(a):
@@ -648,7 +659,7 @@ def run_backward(args):
     xs = [to_dev(I.residual_stream(w))]
     for l, kind in enumerate(kinds):
         x = xs[-1].clone()
-        X.layer_fwd(dm, kind, w.K, w.gate, abi[l], x, bias if kind == SPARSE else None, None,
+        X.layer_fwd(dm, kind, w.K, w.gate, abi[l], x, bias if routed(kind) else None, None,
                     None, ws_f)
         xs.append(x)
     del ws_f
@@ -671,7 +682,7 @@ def run_backward(args):
         for l in range(len(kinds) - 1, -1, -1):
             dx = dbuf[l & 1]
             X.layer_bwd(dm, kinds[l], w.K, w.gate, abi[l], xs[l],
-                        bias if kinds[l] == SPARSE else None, dy, coef, dx, grads, ws, stream)
+                        bias if routed(kinds[l]) else None, dy, coef, dx, grads, ws, stream)
             dy = dx
 
     X.reset_status(ws)

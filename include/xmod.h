@@ -283,14 +283,18 @@ XMOD_API int xmod_stack_fwd_sched(const xmod_dims* dims, int K, const int32_t* k
  *   grads     fp32 device arrays shaped as the weights (overwritten); w_router is
  *             ignored for DENSE layers; varsigma (one float) receives dJ/dvarsigma (0
  *             under Eq. 6 and for DENSE); route_loss (one float, NULL allowed)
- *             receives L_route (SPARSE only)
+ *             receives L_route (the routed kinds; 0 for DENSE and ATTN)
  *   ws        at least xmod_bwd_workspace_bytes(dims, K) bytes
  * With the QK-norm / rotary extras the gradient also flows back through them (the
  * rotation at the tokens' original positions, as in the forward) and q_norm / k_norm
  * receive the gains' gradients. The mechanism controls' halves are differentiated too:
  * ATTN (y = x + a on every token) and ROUTED_FFN (the FFN half on the top-(T/K) tokens
  * with a = 0 in the gated residual); the gradients of the weights a kind does not use
- * may be NULL and are zeroed when given. SPARSE_FULLKV returns XMOD_ERR_UNSUPPORTED.
+ * may be NULL and are zeroed when given. SPARSE_FULLKV (the Selected-Q / full-KV
+ * control) sends the gradient through every token's key and value as well: rows the
+ * layer did not select receive more than dy when a selected query sees them. Its
+ * attention backward runs on FFMA kernels in both dtypes (the projections still use the
+ * tensor cores in bf16). An unknown kind returns XMOD_ERR_INVALID_ARG.
  * bf16 runs the projections and their gradients on the tensor cores (bf16 operands,
  * fp32 accumulation, fp32 weight gradients); fp32 runs FFMA kernels throughout. */
 typedef struct {

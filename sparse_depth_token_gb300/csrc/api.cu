@@ -870,9 +870,7 @@ int xmod_layer_bwd(const xmod_dims* dm, xmod_layer_kind kind, int K, xmod_gate g
                    float route_coef, void* dx, const xmod_layer_grads* g, void* ws,
                    size_t ws_bytes, void* stream) {
   if (!dims_ok(dm) || K <= 0 || K > dm->T) return XMOD_ERR_INVALID_ARG;
-  if (kind != XMOD_LAYER_DENSE && kind != XMOD_LAYER_SPARSE && kind != XMOD_LAYER_ATTN &&
-      kind != XMOD_LAYER_ROUTED_FFN)
-    return XMOD_ERR_UNSUPPORTED;
+  if (!kind_ok(kind)) return XMOD_ERR_INVALID_ARG;
   if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
   if (!weights_ok(w, kind) || !aligned16(x) || !aligned16(dy) || !aligned16(dx) ||
       !aligned16_or_null(bias) || !g || !isfinite(route_coef))

@@ -7,12 +7,18 @@
 // over the keys at or before each query: with D_i = <dO_i, o_i>,
 //   dP = dO v^T,   dS = P * (dP - D),   dq = scale dS k,   dk = scale dS^T q,   dv = P^T dO.
 //
+// The Selected-Q / full-KV control (same section) is the general form: n queries per
+// sequence at ascending positions qpos among nk keys, query i seeing the keys j <=
+// qpos[i]; the compact case is qpos[i] = i, nk = n.
+//
 // Two kernels, each a CTA of four warps and 64-row tiles (16 rows per warp):
 //   attn_bwd_q_mma: per (64-query tile, query head, sequence). Pass 1 recomputes the row
-//     statistics lse = m + log(l) over the key tiles at or before the query tile; pass 2
+//     statistics lse = m + log(l) over the key tiles up to the tile's last query position;
+//     pass 2
 //     forms P, dP, dS and accumulates dq. Writes lse and D for the second kernel.
 //   attn_bwd_kv_mma: per (64-key tile, KV head, sequence), over the group's query heads
-//     and the query tiles at or after the key tile: S^T = k q^T and dP^T = v dO^T, then
+//     and the queries from the first one positioned at or after the tile's first key:
+//     S^T = k q^T and dP^T = v dO^T, then
 //     dv += P^T dO and dk += dS^T q. Every key row belongs to one CTA: no atomics.
 // Operands are staged in shared memory with rows padded by 8 elements (16 bytes), so the
 // eight rows an ldmatrix reads fall in distinct 16-byte bank groups.
@@ -173,17 +179,29 @@ __device__ __forceinline__ void am_pv(const float (&pa)[8][4], const __nv_bfloat
 }
 
 struct AmArgs {
-  int n, hq, hkv;
-  const __nv_bfloat16* qkv;   // q, k, v rows [B*n, ldq]
+  int n, hq, hkv;             // n queries per sequence
+  int nk;                     // keys per sequence
+  const int32_t* qpos;        // [B*n] ascending query positions (NULL: i, nk == n)
+  const __nv_bfloat16* q;     // q of head h at column h*HD of [B*n, ldq]
   int ldq;
+  const __nv_bfloat16* k;     // k, v of KV head g at column g*HD of [B*nk, ldk], [B*nk, ldv]
+  const __nv_bfloat16* v;
+  int ldk, ldv;
   const __nv_bfloat16* o;     // [B*n, hq*HD]
   const __nv_bfloat16* dO;    // [B*n, hq*HD]
   float* lse;                 // [B*n, hq]
   float* Dd;                  // [B*n, hq]
-  __nv_bfloat16* dqkv;        // dq, dk, dv at the q, k, v columns of [B*n, ldg]
-  int ldg;
+  __nv_bfloat16* dq;          // dq of head h at column h*HD of [B*n, ldgq]
+  int ldgq;
+  __nv_bfloat16* dk;          // dk, dv of KV head g at column g*HD of [B*nk, ldgk]
+  __nv_bfloat16* dv;
+  int ldgk;
   float scale;
 };
+
+__device__ __forceinline__ int am_qpos(const AmArgs& p, int b, int i) {
+  return p.qpos ? p.qpos[(int64_t)b * p.n + i] : i;
+}
 
 template <int HD>
 __global__ void __launch_bounds__(AM_WARPS * 32)
@@ -198,29 +216,34 @@ attn_bwd_q_mma(const AmArgs p) {
   __nv_bfloat16* Vb = Kb + 2 * AM_T * P;   // two value tiles
   const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int g = h / (p.hq / p.hkv);
-  const int qw = p.hq * HD, kw = p.hkv * HD;
+  const int qw = p.hq * HD;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q0 = qt * AM_T;
-  const __nv_bfloat16* base = p.qkv + (int64_t)b * p.n * p.ldq;
-  // Key tiles 0..qt (pass 1: keys only), then again with values (pass 2): item i loads
-  // into buffer i % 2 while item i - 1 is computed.
-  const int items = 2 * (qt + 1);
+  const __nv_bfloat16* kbase = p.k + (int64_t)b * p.nk * p.ldk;
+  const __nv_bfloat16* vbase = p.v + (int64_t)b * p.nk * p.ldv;
+  // Key tiles up to the tile's last query position (positions ascend): nkt of them in
+  // pass 1 (keys only), then again with values (pass 2); item i loads into buffer i % 2
+  // while item i - 1 is computed.
+  const int nkt = am_qpos(p, b, min(q0 + AM_T, p.n) - 1) / AM_T + 1;
+  const int items = 2 * nkt;
   auto issue = [&](int it) {
-    const int kt = it <= qt ? it : it - qt - 1, buf = it & 1;
-    am_load_tile_async<HD>(Kb + buf * AM_T * P, base, p.ldq, kt * AM_T, p.n, qw + g * HD);
-    if (it > qt)
-      am_load_tile_async<HD>(Vb + buf * AM_T * P, base, p.ldq, kt * AM_T, p.n, qw + kw + g * HD);
+    const int kt = it < nkt ? it : it - nkt, buf = it & 1;
+    am_load_tile_async<HD>(Kb + buf * AM_T * P, kbase, p.ldk, kt * AM_T, p.nk, g * HD);
+    if (it >= nkt)
+      am_load_tile_async<HD>(Vb + buf * AM_T * P, vbase, p.ldv, kt * AM_T, p.nk, g * HD);
     cp_commit();
   };
-  am_load_tile_async<HD>(Qs, base, p.ldq, q0, p.n, h * HD);
+  am_load_tile_async<HD>(Qs, p.q + (int64_t)b * p.n * p.ldq, p.ldq, q0, p.n, h * HD);
   am_load_tile_async<HD>(dOs, p.dO + (int64_t)b * p.n * qw, qw, q0, p.n, h * HD);
   issue(0);
   // D_i = <dO_i, o_i>: four lanes per row of this warp's 16 (rows lane/4 and lane/4 + 8
   // are this lane's rows in the MMA fragments)
   float Dr[2];
+  int qp[2];   // the rows' positions (-1 past the sequence: no key)
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
     const int i = warp * 16 + (lane >> 2) + 8 * hr, qi = q0 + i;
+    qp[hr] = qi < p.n ? am_qpos(p, b, qi) : -1;
     float acc = 0.0f;
     if (qi < p.n) {
       const __nv_bfloat16* orow = p.o + ((int64_t)b * p.n + qi) * qw + h * HD;
@@ -238,7 +261,7 @@ attn_bwd_q_mma(const AmArgs p) {
   const float sl2 = p.scale * 1.4426950408889634f;   // scale in log2 units
   // pass 1: row max and sum in log2 units
   float mr[2] = {-INFINITY, -INFINITY}, lr[2] = {0.0f, 0.0f};
-  for (int kt = 0; kt <= qt; ++kt) {
+  for (int kt = 0; kt < nkt; ++kt) {
     const int k0 = kt * AM_T;
     const __nv_bfloat16* Ks = Kb + (kt & 1) * AM_T * P;
     issue(kt + 1);   // the next item exists: pass 2 follows
@@ -248,14 +271,13 @@ attn_bwd_q_mma(const AmArgs p) {
     am_qk<HD>(Qs, warp * 16, Ks, s);
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
-      const int qi = q0 + warp * 16 + (lane >> 2) + 8 * hr;
       float mx = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 8; ++j)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int kj = k0 + j * 8 + (lane & 3) * 2 + e;
-          const bool ok = qi < p.n && kj <= qi;
+          const bool ok = kj <= qp[hr];   // qp < nk
           const float v = ok ? s[j][2 * hr + e] * sl2 : -INFINITY;
           s[j][2 * hr + e] = v;
           mx = fmaxf(mx, v);
@@ -292,8 +314,8 @@ attn_bwd_q_mma(const AmArgs p) {
   float dq[HD / 8][4];
 #pragma unroll
   for (int j = 0; j < HD / 8; ++j) dq[j][0] = dq[j][1] = dq[j][2] = dq[j][3] = 0.0f;
-  for (int kt = 0; kt <= qt; ++kt) {
-    const int k0 = kt * AM_T, it = qt + 1 + kt;
+  for (int kt = 0; kt < nkt; ++kt) {
+    const int k0 = kt * AM_T, it = nkt + kt;
     const __nv_bfloat16* Ks = Kb + (it & 1) * AM_T * P;
     const __nv_bfloat16* Vs = Vb + (it & 1) * AM_T * P;
     if (it + 1 < items) {
@@ -311,9 +333,8 @@ attn_bwd_q_mma(const AmArgs p) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int hr = e >> 1;
-        const int qi = q0 + warp * 16 + (lane >> 2) + 8 * hr;
         const int kj = k0 + j * 8 + (lane & 3) * 2 + (e & 1);
-        const bool ok = qi < p.n && kj <= qi;
+        const bool ok = kj <= qp[hr];
         const float pr = ok ? exp2f(s[j][e] * sl2 - lse2[hr]) : 0.0f;
         s[j][e] = pr * (dp[j][e] - Dr[hr]);   // dS
       }
@@ -324,7 +345,7 @@ attn_bwd_q_mma(const AmArgs p) {
   for (int hr = 0; hr < 2; ++hr) {
     const int qi = q0 + warp * 16 + (lane >> 2) + 8 * hr;
     if (qi >= p.n) continue;
-    __nv_bfloat16* out = p.dqkv + ((int64_t)b * p.n + qi) * p.ldg + h * HD;
+    __nv_bfloat16* out = p.dq + ((int64_t)b * p.n + qi) * p.ldgq + h * HD;
 #pragma unroll
     for (int j = 0; j < HD / 8; ++j)
       *reinterpret_cast<uint32_t*>(out + j * 8 + (lane & 3) * 2) =
@@ -345,19 +366,31 @@ attn_bwd_kv_mma(const AmArgs p) {
   __nv_bfloat16* dOb = Qb + 2 * AM_T * P;   // two dO tiles
   float* lse_b = reinterpret_cast<float*>(dOb + 2 * AM_T * P);   // [2][AM_T]
   float* D_b = lse_b + 2 * AM_T;                                   // [2][AM_T]
+  int* qp_b = reinterpret_cast<int*>(D_b + 2 * AM_T);              // [2][AM_T]
   const int kt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = p.hq / p.hkv;
-  const int qw = p.hq * HD, kw = p.hkv * HD;
+  const int qw = p.hq * HD;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int k0 = kt * AM_T;
-  const __nv_bfloat16* base = p.qkv + (int64_t)b * p.n * p.ldq;
-  // items: (query head of the group, query tile at or after the key tile); item i loads
-  // into buffer i % 2 while item i - 1 is computed
-  const int nq = (p.n - k0 + AM_T - 1) / AM_T;
+  const __nv_bfloat16* qbase = p.q + (int64_t)b * p.n * p.ldq;
+  // the first query positioned at or after the tile's first key: a binary search over the
+  // ascending positions, the same in every thread
+  int qstart;
+  {
+    int lo = 0, hi = p.n;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (am_qpos(p, b, mid) >= k0) hi = mid; else lo = mid + 1;
+    }
+    qstart = lo;
+  }
+  // items: (query head of the group, query tile from qstart); item i loads into buffer
+  // i % 2 while item i - 1 is computed
+  const int nq = (p.n - qstart + AM_T - 1) / AM_T;
   const int items = G * nq;
   auto issue = [&](int it) {
-    const int h = g * G + it / nq, q0 = k0 + (it % nq) * AM_T, buf = it & 1;
-    am_load_tile_async<HD>(Qb + buf * AM_T * P, base, p.ldq, q0, p.n, h * HD);
+    const int h = g * G + it / nq, q0 = qstart + (it % nq) * AM_T, buf = it & 1;
+    am_load_tile_async<HD>(Qb + buf * AM_T * P, qbase, p.ldq, q0, p.n, h * HD);
     am_load_tile_async<HD>(dOb + buf * AM_T * P, p.dO + (int64_t)b * p.n * qw, qw, q0, p.n,
                            h * HD);
     for (int i = threadIdx.x; i < AM_T; i += AM_WARPS * 32) {
@@ -366,12 +399,18 @@ attn_bwd_kv_mma(const AmArgs p) {
       const int64_t o = ok ? ((int64_t)b * p.n + qi) * p.hq + h : 0;
       cp4(lse_b + buf * AM_T + i, p.lse + o, ok);
       cp4(D_b + buf * AM_T + i, p.Dd + o, ok);
+      if (p.qpos)
+        cp4(qp_b + buf * AM_T + i, p.qpos + (ok ? (int64_t)b * p.n + qi : 0), ok);
+      else
+        qp_b[buf * AM_T + i] = qi;   // read after the barrier that follows the wait
     }
     cp_commit();
   };
-  am_load_tile_async<HD>(Ks, base, p.ldq, k0, p.n, qw + g * HD);
-  am_load_tile_async<HD>(Vs, base, p.ldq, k0, p.n, qw + kw + g * HD);
-  issue(0);
+  if (items > 0) {   // no query sees this key tile: its dk, dv stay zero (written below)
+    am_load_tile_async<HD>(Ks, p.k + (int64_t)b * p.nk * p.ldk, p.ldk, k0, p.nk, g * HD);
+    am_load_tile_async<HD>(Vs, p.v + (int64_t)b * p.nk * p.ldv, p.ldv, k0, p.nk, g * HD);
+    issue(0);
+  }
   const float sl2 = p.scale * 1.4426950408889634f;
   float dk[HD / 8][4], dv[HD / 8][4];
 #pragma unroll
@@ -379,11 +418,12 @@ attn_bwd_kv_mma(const AmArgs p) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) dk[j][e] = dv[j][e] = 0.0f;
   for (int it = 0; it < items; ++it) {
-    const int q0 = k0 + (it % nq) * AM_T, buf = it & 1;
+    const int q0 = qstart + (it % nq) * AM_T, buf = it & 1;
     const __nv_bfloat16* Qs = Qb + buf * AM_T * P;
     const __nv_bfloat16* dOs = dOb + buf * AM_T * P;
     const float* lse_s = lse_b + buf * AM_T;
     const float* D_s = D_b + buf * AM_T;
+    const int* qp_s = qp_b + buf * AM_T;
     if (it + 1 < items) {
       issue(it + 1);
       cp_wait<1>();
@@ -401,7 +441,7 @@ attn_bwd_kv_mma(const AmArgs p) {
         const int kj = k0 + warp * 16 + (lane >> 2) + 8 * (e >> 1);
         const int ci = j * 8 + (lane & 3) * 2 + (e & 1);   // query within the tile
         const int qi = q0 + ci;
-        const bool ok = qi < p.n && kj < p.n && kj <= qi;
+        const bool ok = qi < p.n && kj < p.nk && kj <= qp_s[ci];
         const float pr = ok ? exp2f(s[j][e] * sl2 - lse_s[ci]) : 0.0f;
         s[j][e] = pr;
         dp[j][e] = pr * (dp[j][e] - D_s[ci]);   // dS^T
@@ -413,15 +453,14 @@ attn_bwd_kv_mma(const AmArgs p) {
 #pragma unroll
   for (int hr = 0; hr < 2; ++hr) {
     const int kj = k0 + warp * 16 + (lane >> 2) + 8 * hr;
-    if (kj >= p.n) continue;
-    __nv_bfloat16* row = p.dqkv + ((int64_t)b * p.n + kj) * p.ldg;
+    if (kj >= p.nk) continue;
+    const int64_t row = ((int64_t)b * p.nk + kj) * p.ldgk + g * HD;
 #pragma unroll
     for (int j = 0; j < HD / 8; ++j) {
       const int c = j * 8 + (lane & 3) * 2;
-      *reinterpret_cast<uint32_t*>(row + qw + g * HD + c) =
+      *reinterpret_cast<uint32_t*>(p.dk + row + c) =
           am_pack(dk[j][2 * hr] * p.scale, dk[j][2 * hr + 1] * p.scale);
-      *reinterpret_cast<uint32_t*>(row + qw + kw + g * HD + c) =
-          am_pack(dv[j][2 * hr], dv[j][2 * hr + 1]);
+      *reinterpret_cast<uint32_t*>(p.dv + row + c) = am_pack(dv[j][2 * hr], dv[j][2 * hr + 1]);
     }
   }
 }
@@ -430,16 +469,17 @@ template <int HD>
 cudaError_t launch_am(int B, const AmArgs& a, cudaStream_t st, bool with_q) {
   constexpr int P = HD + 8;
   const size_t smq = sizeof(__nv_bfloat16) * 6 * AM_T * P;
-  const size_t smk = smq + sizeof(float) * 4 * AM_T;
+  const size_t smk = smq + sizeof(float) * 6 * AM_T;
   cudaFuncSetAttribute(attn_bwd_q_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
   cudaFuncSetAttribute(attn_bwd_kv_mma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
-  const int tiles = (a.n + AM_T - 1) / AM_T;
+  const int qtiles = (a.n + AM_T - 1) / AM_T, ktiles = (a.nk + AM_T - 1) / AM_T;
   if (with_q) {
-    const cudaError_t e = launch_pdl(attn_bwd_q_mma<HD>, dim3(tiles, a.hq, B),
+    const cudaError_t e = launch_pdl(attn_bwd_q_mma<HD>, dim3(qtiles, a.hq, B),
                                      dim3(AM_WARPS * 32), smq, st, a);
     if (e != cudaSuccess) return e;
   }
-  return launch_pdl(attn_bwd_kv_mma<HD>, dim3(tiles, a.hkv, B), dim3(AM_WARPS * 32), smk, st, a);
+  return launch_pdl(attn_bwd_kv_mma<HD>, dim3(ktiles, a.hkv, B), dim3(AM_WARPS * 32), smk, st,
+                    a);
 }
 
 }  // namespace
@@ -448,24 +488,47 @@ bool attn_bwd_mma_supported(int hd, int ldq, int ldo) {
   return (hd == 64 || hd == 128) && ldq % 8 == 0 && ldo % 8 == 0;
 }
 
-cudaError_t launch_attn_bwd_mma(const Ctx& c, int B, int n, int hq, int hkv, int hd,
-                                const void* qkv, int ldq, const void* o, const void* dO,
-                                float* lse, float* Dd, void* dqkv, int ldg, bool with_q) {
-  if (!attn_bwd_mma_supported(hd, ldq, hq * hd) || ldg % 2) return cudaErrorInvalidValue;
+cudaError_t launch_attn_bwd_mma_kv(const Ctx& c, int B, int n, int nk, const int32_t* qpos,
+                                   int hq, int hkv, int hd, const void* q, int ldq,
+                                   const void* k, int ldk, const void* v, int ldv, const void* o,
+                                   const void* dO, float* lse, float* Dd, void* dq, int ldgq,
+                                   void* dk, void* dv, int ldgk, bool with_q) {
+  if (!attn_bwd_mma_supported(hd, ldq, hq * hd) || ldk % 8 || ldv % 8 || ldgq % 2 || ldgk % 2)
+    return cudaErrorInvalidValue;
   AmArgs a;
   a.n = n;
+  a.nk = nk;
+  a.qpos = qpos;
   a.hq = hq;
   a.hkv = hkv;
-  a.qkv = (const __nv_bfloat16*)qkv;
+  a.q = (const __nv_bfloat16*)q;
   a.ldq = ldq;
+  a.k = (const __nv_bfloat16*)k;
+  a.v = (const __nv_bfloat16*)v;
+  a.ldk = ldk;
+  a.ldv = ldv;
   a.o = (const __nv_bfloat16*)o;
   a.dO = (const __nv_bfloat16*)dO;
   a.lse = lse;
   a.Dd = Dd;
-  a.dqkv = (__nv_bfloat16*)dqkv;
-  a.ldg = ldg;
+  a.dq = (__nv_bfloat16*)dq;
+  a.ldgq = ldgq;
+  a.dk = (__nv_bfloat16*)dk;
+  a.dv = (__nv_bfloat16*)dv;
+  a.ldgk = ldgk;
   a.scale = 1.0f / sqrtf((float)hd);
   return hd == 128 ? launch_am<128>(B, a, c.stream, with_q) : launch_am<64>(B, a, c.stream, with_q);
+}
+
+cudaError_t launch_attn_bwd_mma(const Ctx& c, int B, int n, int hq, int hkv, int hd,
+                                const void* qkv, int ldq, const void* o, const void* dO,
+                                float* lse, float* Dd, void* dqkv, int ldg, bool with_q) {
+  const int qw = hq * hd, kw = hkv * hd;
+  const __nv_bfloat16* x = (const __nv_bfloat16*)qkv;
+  __nv_bfloat16* g = (__nv_bfloat16*)dqkv;
+  return launch_attn_bwd_mma_kv(c, B, n, n, nullptr, hq, hkv, hd, x, ldq, x + qw, ldq,
+                                x + qw + kw, ldq, o, dO, lse, Dd, g, ldg, g + qw, g + qw + kw,
+                                ldg, with_q);
 }
 
 }  // namespace xmod

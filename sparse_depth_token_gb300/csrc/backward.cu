@@ -408,28 +408,63 @@ rms_bwd_kernel(int64_t M, int d, const float* __restrict__ dz, const T* __restri
 }
 
 
+// Selected-Q / full-KV: the RMSNorm1 output u of a selected token feeds its query and its
+// key / value. Selected compact row m (stream row t) adds its query-side gradient
+// du_sel[m] into du[t] (the keys' and values' part, every token) and puts dh[m] (the
+// gradient through h = x + a) in dadd[t], which the caller zeroed.
+__global__ void __launch_bounds__(BW_WARPS * 32)
+fullkv_merge_kernel(int64_t M, int seqT, int n, int d, const int32_t* __restrict__ idx,
+                    const float* __restrict__ du_sel, const float* __restrict__ dh,
+                    float* __restrict__ du, float* __restrict__ dadd) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * BW_WARPS + warp;
+  if (m >= M) return;
+  const int64_t t = bw_stream_row(m, seqT, n, idx);
+  for (int c = lane * 4; c < d; c += 128) {
+    const float4 q = *reinterpret_cast<const float4*>(du_sel + m * d + c);
+    float4* pu = reinterpret_cast<float4*>(du + t * d + c);
+    const float4 u = *pu;
+    *pu = make_float4(u.x + q.x, u.y + q.y, u.z + q.z, u.w + q.w);
+    *reinterpret_cast<float4*>(dadd + t * d + c) =
+        *reinterpret_cast<const float4*>(dh + m * d + c);
+  }
+}
+
 // ---------------------------------------------------------------- attention backward
 // Causal GQA attention on each sequence's n compact rows (query head h reads KV head
-// h / (hq / hkv)); FFMA tiles of 32 queries x 32 keys in shared memory (fp32).
+// h / (hq / hkv)), or on n queries at ascending positions over nk keys, each query seeing
+// the keys at or before its position (Selected-Q / full-KV); FFMA tiles of 32 queries x
+// 32 keys in shared memory (fp32).
 // bwd_q: per (32-query tile, head, sequence): the row statistics lse = m + log l, D =
 //        <dO, O>, then dQ = scale * sum_j P (dP - D) K_j with P = exp(scale q.k - lse),
 //        dP = dO . v_j.
 // bwd_kv: per (32-key tile, KV head, sequence), over the group's query heads and the
-//        query tiles at or after the key tile: dV = sum_i P dO_i, dK = scale * sum_i
+//        queries from the first one positioned at or after the tile's first key: dV =
+//        sum_i P dO_i, dK = scale * sum_i
 //        P (dP - D) q_i. Every key row is owned by one CTA: no atomics.
 struct AttnBwd {
-  int n, hq, hkv;
-  const void* qkv;   // q of head h at column h*HD, k of KV head g at column qw + g*HD
+  int n, hq, hkv;      // n queries per sequence
+  int nk;              // keys per sequence
+  const int32_t* qpos; // [B*n] ascending positions of the queries among the nk keys; query
+                       // i sees keys j <= qpos[i] (NULL: j <= i, nk == n)
+  const void* q;       // q of head h at column h*HD of [B*n, ldq]
   int ldq;
-  const void* v;     // vt_mode 0: the qkv buffer (v at column qw + kw + g*HD, stride ldq);
-  int vt_mode;       // 1: v transposed, [B, hkv, HD, vt_ld] (keys contiguous)
-  int vt_ld;
-  const void* o;     // [B*n, hq*HD]
-  const float* dO;   // [B*n, hq*HD]
-  float* lse;        // [B*n, hq]
-  float* Dd;         // [B*n, hq]
-  void* dqkv;        // dq, dk, dv at the q, k, v columns of [B*n, ldg]
-  int ldg;
+  const void* k;       // k of KV head g at column g*HD of [B*nk, ldk]
+  int ldk;
+  const void* v;       // vt_mode 0: v of KV head g at column g*HD of [B*nk, ldv];
+  int vt_mode;         // 1: v transposed, [B, hkv, HD, vt_ld] (keys contiguous)
+  int ldv, vt_ld;
+  const void* o;       // [B*n, hq*HD]
+  const float* dO;     // [B*n, hq*HD]
+  float* lse;          // [B*n, hq]
+  float* Dd;           // [B*n, hq]
+  void* dq;            // dq of head h at column h*HD of [B*n, ldgq]
+  int ldgq;
+  void* dk;            // dk, dv of KV head g at column g*HD of [B*nk, ldgk]
+  void* dv;
+  int ldgk;
   float scale;
 };
 
@@ -437,10 +472,14 @@ constexpr int AB_T = 32;   // queries and keys per tile
 
 template <typename T, int HD>
 __device__ __forceinline__ float ab_v(const AttnBwd& p, int b, int g, int j, int c) {
-  const int qw = p.hq * HD, kw = p.hkv * HD;
   if (p.vt_mode)
     return Elem<T>::to_f(((const T*)p.v)[(((int64_t)b * p.hkv + g) * HD + c) * p.vt_ld + j]);
-  return Elem<T>::to_f(((const T*)p.qkv)[((int64_t)b * p.n + j) * p.ldq + qw + kw + g * HD + c]);
+  return Elem<T>::to_f(((const T*)p.v)[((int64_t)b * p.nk + j) * p.ldv + g * HD + c]);
+}
+
+// position of query i of sequence b among its keys
+__device__ __forceinline__ int ab_qpos(const AttnBwd& p, int b, int i) {
+  return p.qpos ? p.qpos[(int64_t)b * p.n + i] : i;
 }
 
 template <typename T, int HD>
@@ -460,15 +499,17 @@ attn_bwd_q_kernel(const AttnBwd p) {
   const int qw = p.hq * HD;
   const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
   const int q0 = qt * AB_T;
-  const T* qkv = (const T*)p.qkv;
+  const T* Q = (const T*)p.q;
+  const T* Kp = (const T*)p.k;
   for (int e = tid; e < AB_T * HD; e += 256) {
     const int i = e / HD, c = e - i * HD, qi = q0 + i;
     const int64_t row = (int64_t)b * p.n + qi;
-    Qs[i * P + c] = qi < p.n ? Elem<T>::to_f(qkv[row * p.ldq + h * HD + c]) : 0.0f;
+    Qs[i * P + c] = qi < p.n ? Elem<T>::to_f(Q[row * p.ldq + h * HD + c]) : 0.0f;
     dOs[i * P + c] = qi < p.n ? p.dO[row * qw + h * HD + c] : 0.0f;
   }
   __syncthreads();
   float Dr[4], mr[4], lr[4];
+  int qp[4];   // the rows' positions (-1 past the sequence: no key)
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int i = ty + 8 * r, qi = q0 + i;
@@ -480,26 +521,30 @@ attn_bwd_q_kernel(const AttnBwd p) {
     Dr[r] = warp_sum(acc);
     mr[r] = -INFINITY;
     lr[r] = 0.0f;
+    qp[r] = qi < p.n ? ab_qpos(p, b, qi) : -1;
   }
+  // the key tiles up to the tile's last query position (positions ascend)
+  const int kmax = ab_qpos(p, b, min(q0 + AB_T, p.n) - 1);
+  const int nkt = kmax / AB_T + 1;
   // pass 1: row max and sum over the keys at or before each query
-  for (int kt = 0; kt <= qt; ++kt) {
+  for (int kt = 0; kt < nkt; ++kt) {
     const int k0 = kt * AB_T;
     for (int e = tid; e < AB_T * HD; e += 256) {
       const int j = e / HD, c = e - j * HD, kj = k0 + j;
-      Ks[j * P + c] = kj < p.n
-          ? Elem<T>::to_f(qkv[((int64_t)b * p.n + kj) * p.ldq + qw + g * HD + c]) : 0.0f;
+      Ks[j * P + c] = kj < p.nk
+          ? Elem<T>::to_f(Kp[((int64_t)b * p.nk + kj) * p.ldk + g * HD + c]) : 0.0f;
     }
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int i = ty + 8 * r, qi = q0 + i, kj = k0 + tx;
+      const int i = ty + 8 * r, kj = k0 + tx;
       float s = 0.0f;
 #pragma unroll 8
       for (int c = 0; c < HD; ++c) s += Qs[i * P + c] * Ks[tx * P + c];
       s *= p.scale;
-      const bool ok = qi < p.n && kj < p.n && kj <= qi;
+      const bool ok = kj < p.nk && kj <= qp[r];
       const float mx = warp_max(ok ? s : -INFINITY);
-      if (mx > -INFINITY) {
+      if (mx > -INFINITY) {   // uniform over the warp (one row per warp)
         const float mn = fmaxf(mr[r], mx);
         const float add = warp_sum(ok ? expf(s - mn) : 0.0f);
         lr[r] = lr[r] * expf(mr[r] - mn) + add;
@@ -524,26 +569,26 @@ attn_bwd_q_kernel(const AttnBwd p) {
   for (int r = 0; r < 4; ++r)
 #pragma unroll
     for (int k = 0; k < KC; ++k) dq[r][k] = 0.0f;
-  for (int kt = 0; kt <= qt; ++kt) {
+  for (int kt = 0; kt < nkt; ++kt) {
     const int k0 = kt * AB_T;
     for (int e = tid; e < AB_T * HD; e += 256) {
       const int j = e / HD, c = e - j * HD, kj = k0 + j;
-      const bool ok = kj < p.n;
+      const bool ok = kj < p.nk;
       Ks[j * P + c] = ok
-          ? Elem<T>::to_f(qkv[((int64_t)b * p.n + kj) * p.ldq + qw + g * HD + c]) : 0.0f;
+          ? Elem<T>::to_f(Kp[((int64_t)b * p.nk + kj) * p.ldk + g * HD + c]) : 0.0f;
       Vs[j * P + c] = ok ? ab_v<T, HD>(p, b, g, kj, c) : 0.0f;
     }
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int i = ty + 8 * r, qi = q0 + i, kj = k0 + tx;
+      const int i = ty + 8 * r, kj = k0 + tx;
       float s = 0.0f, dp = 0.0f;
 #pragma unroll 8
       for (int c = 0; c < HD; ++c) {
         s += Qs[i * P + c] * Ks[tx * P + c];
         dp += dOs[i * P + c] * Vs[tx * P + c];
       }
-      const bool ok = qi < p.n && kj < p.n && kj <= qi;
+      const bool ok = kj < p.nk && kj <= qp[r];
       const float pr = ok ? expf(s * p.scale - lse[r]) : 0.0f;
       dSs[i * (AB_T + 1) + tx] = pr * (dp - Dr[r]);
     }
@@ -562,14 +607,14 @@ attn_bwd_q_kernel(const AttnBwd p) {
     }
     __syncthreads();
   }
-  T* out = (T*)p.dqkv;
+  T* out = (T*)p.dq;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int qi = q0 + ty + 8 * r;
     if (qi >= p.n) continue;
 #pragma unroll
     for (int k = 0; k < KC; ++k)
-      out[((int64_t)b * p.n + qi) * p.ldg + h * HD + tx + 32 * k] =
+      out[((int64_t)b * p.n + qi) * p.ldgq + h * HD + tx + 32 * k] =
           Elem<T>::from_f(dq[r][k] * p.scale);
   }
 }
@@ -589,18 +634,31 @@ attn_bwd_kv_kernel(const AttnBwd p) {
   float* dSs = Ps + AB_T * (AB_T + 1);
   float* lse_s = dSs + AB_T * (AB_T + 1);
   float* D_s = lse_s + AB_T;
+  int* qp_s = (int*)(D_s + AB_T);
   const int kt = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int G = p.hq / p.hkv;
-  const int qw = p.hq * HD, kw = p.hkv * HD;
+  const int qw = p.hq * HD;
   const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
   const int k0 = kt * AB_T;
-  const T* qkv = (const T*)p.qkv;
+  const T* Q = (const T*)p.q;
+  const T* Kp = (const T*)p.k;
   for (int e = tid; e < AB_T * HD; e += 256) {
     const int j = e / HD, c = e - j * HD, kj = k0 + j;
-    const bool ok = kj < p.n;
+    const bool ok = kj < p.nk;
     Ks[j * P + c] = ok
-        ? Elem<T>::to_f(qkv[((int64_t)b * p.n + kj) * p.ldq + qw + g * HD + c]) : 0.0f;
+        ? Elem<T>::to_f(Kp[((int64_t)b * p.nk + kj) * p.ldk + g * HD + c]) : 0.0f;
     Vs[j * P + c] = ok ? ab_v<T, HD>(p, b, g, kj, c) : 0.0f;
+  }
+  // the first query at or after the tile's first key: positions ascend, so a binary search
+  // (the same in every thread)
+  int qstart = p.n;
+  {
+    int lo = 0, hi = p.n;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (ab_qpos(p, b, mid) >= k0) hi = mid; else lo = mid + 1;
+    }
+    qstart = lo;
   }
   float dk[4][KC], dv[4][KC];
 #pragma unroll
@@ -609,30 +667,31 @@ attn_bwd_kv_kernel(const AttnBwd p) {
     for (int k = 0; k < KC; ++k) dk[r][k] = dv[r][k] = 0.0f;
   for (int hh = 0; hh < G; ++hh) {
     const int h = g * G + hh;
-    for (int q0 = k0; q0 < p.n; q0 += AB_T) {
+    for (int q0 = qstart; q0 < p.n; q0 += AB_T) {
       __syncthreads();   // the previous tile's readers are done
       for (int e = tid; e < AB_T * HD; e += 256) {
         const int i = e / HD, c = e - i * HD, qi = q0 + i;
         const int64_t row = (int64_t)b * p.n + qi;
-        Qs[i * P + c] = qi < p.n ? Elem<T>::to_f(qkv[row * p.ldq + h * HD + c]) : 0.0f;
+        Qs[i * P + c] = qi < p.n ? Elem<T>::to_f(Q[row * p.ldq + h * HD + c]) : 0.0f;
         dOs[i * P + c] = qi < p.n ? p.dO[row * qw + h * HD + c] : 0.0f;
       }
       if (tid < AB_T) {
         const int qi = q0 + tid;
         lse_s[tid] = qi < p.n ? p.lse[((int64_t)b * p.n + qi) * p.hq + h] : 0.0f;
         D_s[tid] = qi < p.n ? p.Dd[((int64_t)b * p.n + qi) * p.hq + h] : 0.0f;
+        qp_s[tid] = qi < p.n ? ab_qpos(p, b, qi) : -1;
       }
       __syncthreads();
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int j = ty + 8 * r, kj = k0 + j, qi = q0 + tx;
+        const int j = ty + 8 * r, kj = k0 + j;
         float s = 0.0f, dp = 0.0f;
 #pragma unroll 8
         for (int c = 0; c < HD; ++c) {
           s += Ks[j * P + c] * Qs[tx * P + c];
           dp += Vs[j * P + c] * dOs[tx * P + c];
         }
-        const bool ok = qi < p.n && kj < p.n && kj <= qi;
+        const bool ok = kj < p.nk && kj <= qp_s[tx];
         const float pr = ok ? expf(s * p.scale - lse_s[tx]) : 0.0f;
         Ps[j * (AB_T + 1) + tx] = pr;
         dSs[j * (AB_T + 1) + tx] = pr * (dp - D_s[tx]);
@@ -656,17 +715,18 @@ attn_bwd_kv_kernel(const AttnBwd p) {
       }
     }
   }
-  T* out = (T*)p.dqkv;
+  T* odk = (T*)p.dk;
+  T* odv = (T*)p.dv;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int kj = k0 + ty + 8 * r;
-    if (kj >= p.n) continue;
-    const int64_t row = ((int64_t)b * p.n + kj) * p.ldg;
+    if (kj >= p.nk) continue;
+    const int64_t row = ((int64_t)b * p.nk + kj) * p.ldgk;
 #pragma unroll
     for (int k = 0; k < KC; ++k) {
       const int c = tx + 32 * k;
-      out[row + qw + g * HD + c] = Elem<T>::from_f(dk[r][k] * p.scale);
-      out[row + qw + kw + g * HD + c] = Elem<T>::from_f(dv[r][k]);
+      odk[row + g * HD + c] = Elem<T>::from_f(dk[r][k] * p.scale);
+      odv[row + g * HD + c] = Elem<T>::from_f(dv[r][k]);
     }
   }
 }
@@ -814,16 +874,16 @@ template <typename T, int HD>
 cudaError_t launch_attn_bwd_t(const Ctx& c, int B, const AttnBwd& p) {
   constexpr int P = HD + 1;
   const size_t smq = sizeof(float) * (4 * AB_T * P + AB_T * (AB_T + 1));
-  const size_t smk = sizeof(float) * (4 * AB_T * P + 2 * AB_T * (AB_T + 1) + 2 * AB_T);
+  const size_t smk = sizeof(float) * (4 * AB_T * P + 2 * AB_T * (AB_T + 1) + 3 * AB_T);
   cudaFuncSetAttribute(attn_bwd_q_kernel<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smq);
   cudaFuncSetAttribute(attn_bwd_kv_kernel<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smk);
-  const int tiles = (p.n + AB_T - 1) / AB_T;
-  cudaError_t e = launch_pdl(attn_bwd_q_kernel<T, HD>, dim3(tiles, p.hq, B), dim3(256), smq,
+  const int qtiles = (p.n + AB_T - 1) / AB_T, ktiles = (p.nk + AB_T - 1) / AB_T;
+  cudaError_t e = launch_pdl(attn_bwd_q_kernel<T, HD>, dim3(qtiles, p.hq, B), dim3(256), smq,
                              c.stream, p);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_bwd_kv_kernel<T, HD>, dim3(tiles, p.hkv, B), dim3(256), smk, c.stream,
+  return launch_pdl(attn_bwd_kv_kernel<T, HD>, dim3(ktiles, p.hkv, B), dim3(256), smk, c.stream,
                     p);
 }
 
@@ -844,6 +904,131 @@ cudaError_t launch_attn_bwd(const Ctx& c, xmod_dtype dt, int B, int hd, const At
   return cudaErrorInvalidValue;
 }
 
+// The Selected-Q / full-KV layer's backward from the attention down (X-MoD notes,
+// "mechanism controls"): the selected tokens' queries qb [M, qw] (M = B * T/K rows, at
+// positions idx) over the keys and values kvb [B*T, 2kw] of every token (v only
+// transposed, in vt, when v_transposed); dO [M, qw] (bf16 with mma, else fp32) and dh
+// [M, d] (the gradient through h = x_sel + a) come from the block's backward above. The
+// attention backward runs on the warp-level tensor-core MMA with mma (bf16, head_dim 64 or
+// 128), on FFMA tiles otherwise. Every token's row of dx receives the gradient through its
+// key and value; the selected ones, through their query too.
+template <typename E>
+int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weights* w,
+                const void* x, const int32_t* idx, void* dx, const xmod_layer_grads* gr,
+                void* ws, const BwLayout& L, const E* kvb, const E* qb, const E* kpre,
+                const E* qpre, const E* vt, bool v_transposed, const E* o, const void* dO,
+                bool mma, const float* dh) {
+  const xmod_dtype dt = dm->dtype;
+  const int B = dm->B, T = dm->T, d = dm->d, hq = dm->n_heads, hkv = dm->n_kv_heads,
+            hd = dm->head_dim;
+  const int qw = hq * hd, kw = hkv * hd;
+  const int M = B * n, Mp = (int)round8(M);
+  const int BT = B * T, BTp = (int)round8(BT);
+  E* dqkv = (E*)bat(ws, L.dqkv);
+  E* dkv = dqkv;                               // [BT, 2kw]: dk | dv of every token
+  E* dqb = dqkv + (size_t)BT * 2 * kw;         // [M, qw]: dq of the selected tokens
+  E* tA = (E*)bat(ws, L.tA);
+  E* tB = (E*)bat(ws, L.tB);
+  E* tW = (E*)bat(ws, L.tW);
+  float* part = (float*)bat(ws, L.part);
+
+  // ======== attention: n queries per sequence over its T keys
+  if (mma) {
+    E* kvw = const_cast<E*>(kvb);
+    if (v_transposed)   // the MMA kernels read v by rows: the v projection once more
+      BW_RUN("gemm_qkv", bw_gemm(c, dt, BT, kw, d, bat(ws, L.u), d, w->wv, d, kvw + kw, 2 * kw,
+                                 false));
+    BW_RUN("bwd_attention",
+           launch_attn_bwd_mma_kv(c, B, n, T, idx, hq, hkv, hd, qb, qw, kvb, 2 * kw, kvb + kw,
+                                  2 * kw, o, dO, (float*)bat(ws, L.lse), (float*)bat(ws, L.Dd),
+                                  dqb, qw, dkv, dkv + kw, 2 * kw));
+  } else {
+  AttnBwd p;
+  p.n = n;
+  p.nk = T;
+  p.qpos = idx;
+  p.hq = hq;
+  p.hkv = hkv;
+  p.q = qb;
+  p.ldq = qw;
+  p.k = kvb;
+  p.ldk = 2 * kw;
+  p.v = v_transposed ? (const void*)vt : (const void*)(kvb + kw);
+  p.vt_mode = v_transposed ? 1 : 0;
+  p.ldv = 2 * kw;
+  p.vt_ld = (int)round8(T);
+  p.o = o;
+  p.dO = (const float*)dO;
+  p.lse = (float*)bat(ws, L.lse);
+  p.Dd = (float*)bat(ws, L.Dd);
+  p.dq = dqb;
+  p.ldgq = qw;
+  p.dk = dkv;
+  p.dv = dkv + kw;
+  p.ldgk = 2 * kw;
+  p.scale = 1.0f / sqrtf((float)hd);
+  BW_RUN("bwd_attention", launch_attn_bwd(c, dt, B, hd, p));
+  }
+
+  if (w->q_norm || w->k_norm || w->rope_theta > 0.0f) {   // back through the QK-norm, rotation
+    float* dgq = w->q_norm ? (float*)bat(ws, L.dgq) : nullptr;
+    float* dgk = w->k_norm ? (float*)bat(ws, L.dgk) : nullptr;
+    BW_RUN("bwd_rows", launch_qk_transform_bwd(c, dt, M, dqb, qw, 0, hq, w->q_norm, 0, 0, nullptr,
+                                               qpre, qw, hd, dm->rms_eps, w->rope_theta, idx, T,
+                                               dgq, nullptr));
+    BW_RUN("bwd_rows", launch_qk_transform_bwd(c, dt, BT, dkv, 2 * kw, 0, 0, nullptr, 0, hkv,
+                                               w->k_norm, kpre, kw, hd, dm->rms_eps,
+                                               w->rope_theta, nullptr, T, nullptr, dgk));
+    if (dgq) {
+      const int st = bw_coldot<float>(c, M, hd, nullptr, dgq, nullptr, T, n, nullptr, part,
+                                      gr->q_norm);
+      if (st) return st;
+    }
+    if (dgk) {
+      const int st = bw_coldot<float>(c, BT, hd, nullptr, dgk, nullptr, T, T, nullptr, part,
+                                      gr->k_norm);
+      if (st) return st;
+    }
+  }
+
+  // ======== q = u_sel Wq^T (u_sel again in the RMSNorm2 buffer, which the FFN is done with)
+  E* u = (E*)bat(ws, L.u);
+  E* usel = (E*)bat(ws, L.v2);
+  BW_RUN("gather_rmsnorm",
+         launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1, dm->rms_eps, usel));
+  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, qw, dqb, qw, tA, Mp));     // dq^T [qw, Mp]
+  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, usel, d, tB, Mp));      // u_sel^T [d, Mp]
+  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, qw, d, Mp, tA, Mp, tB, Mp, gr->wq, d, true));
+  BW_RUN("bwd_transpose", transpose(c, dt, qw, qw, d, w->wq, d, tW, qw));   // Wq^T [d, qw]
+  float* du_sel = (float*)bat(ws, L.dv2);
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qw, dqb, qw, tW, qw, du_sel, d, true));
+  // ======== k, v = u [Wk | Wv]^T on every token
+  BW_RUN("bwd_transpose", transpose(c, dt, BT, BTp, 2 * kw, dkv, 2 * kw, tA, BTp));  // [2kw, BTp]
+  BW_RUN("bwd_transpose", transpose(c, dt, BT, BTp, d, u, d, tB, BTp));              // [d, BTp]
+  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, kw, d, BTp, tA, BTp, tB, BTp, gr->wk, d, true));
+  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, kw, d, BTp, tA + (size_t)kw * BTp, BTp, tB, BTp, gr->wv,
+                                d, true));
+  BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wk, d, tW, 2 * kw));   // [d, 2kw]
+  BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wv, d, tW + kw, 2 * kw));
+  float* du = (float*)bat(ws, L.du);
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, BT, d, 2 * kw, dkv, 2 * kw, tW, 2 * kw, du, d, true));
+  // ======== u = RMSNorm(x) g1 on every token; the selected rows add their query's part
+  // and the gradient through h
+  float* dadd = (float*)bat(ws, L.h);
+  if (cudaMemsetAsync(dadd, 0, sizeof(float) * (size_t)BT * d, c.stream) != cudaSuccess)
+    return XMOD_ERR_CUDA;
+  BW_RUN("bwd_rows", launch_pdl(fullkv_merge_kernel, dim3((unsigned)((M + BW_WARPS - 1) / BW_WARPS)),
+                                dim3(BW_WARPS * 32), 0, c.stream, (int64_t)M, T, n, d, idx,
+                                (const float*)du_sel, dh, du, dadd));
+  float* rstd1 = (float*)bat(ws, L.rstd1);
+  BW_RUN("bwd_rows", launch_pdl(rms_bwd_kernel<E, E>, dim3((unsigned)((BT + BW_WARPS - 1) / BW_WARPS)),
+                                dim3(BW_WARPS * 32), 0, c.stream, (int64_t)BT, d, (const float*)du,
+                                (const E*)w->rms1, (const E*)x, (const int32_t*)nullptr, T, T,
+                                dm->rms_eps, (const E*)nullptr, (float*)nullptr, (E*)nullptr,
+                                (const float*)dadd, (E*)dx, rstd1));
+  return bw_coldot<E>(c, BT, d, du, (const E*)x, nullptr, T, T, rstd1, part, gr->rms1);
+}
+
 template <typename E>
 int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
                 const xmod_layer_weights* w, const void* x, const float* bias, const void* dy,
@@ -854,8 +1039,10 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
             hd = dm->head_dim, F = dm->d_ff;
   // routed: the layer selects top-(T/K) tokens; attn / ffn: which halves of the block run
   // (FullAttn layers: the attention half on every token, y = x + a; Routed-FFN layers:
-  // the FFN half on RMSNorm(x_sel) rms2 with a = 0 in the gated residual)
-  const bool sparse = kind == XMOD_LAYER_SPARSE || kind == XMOD_LAYER_ROUTED_FFN;
+  // the FFN half on RMSNorm(x_sel) rms2 with a = 0 in the gated residual); fullkv: the
+  // Selected-Q / full-KV control, whose selected queries see every token's keys and values
+  const bool fullkv = kind == XMOD_LAYER_SPARSE_FULLKV;
+  const bool sparse = kind == XMOD_LAYER_SPARSE || kind == XMOD_LAYER_ROUTED_FFN || fullkv;
   const bool attn = kind != XMOD_LAYER_ROUTED_FFN;
   const bool ffn = kind != XMOD_LAYER_ATTN;
   const int n = sparse ? T / K : T;
@@ -896,7 +1083,71 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   E* qkpre = (E*)bat(ws, L.qkpre);
   const bool tc_attn = tc && attention_tc_supported(hd, n, qkv_w);
   bool v_transposed = false;   // v kept only in its transposed layout (tensor-core path)
-  if (attn) {
+  // Selected-Q / full-KV buffers: k | v of every token [BT, 2kw] and the selected tokens'
+  // q [M, qw] in the qkv buffer, their gradients alike in dqkv; the projections before
+  // the QK-norm / rotation (k [BT, kw], then q [M, qw]) in qkpre
+  E* kvb = qkv;
+  E* qb = qkv + (size_t)BT * 2 * kw;
+  E* kpre = qkpre;
+  E* qpre = qkpre + (size_t)BT * kw;
+  if (fullkv) {
+    // RMSNorm1 of every token (keys, values) and of the selected ones (queries; the
+    // RMSNorm2 buffer holds them until the o-projection)
+    BW_RUN("gather_rmsnorm",
+           launch_gather_rmsnorm(c, dt, B, T, T, d, x, nullptr, w->rms1, dm->rms_eps, u));
+    BW_RUN("gather_rmsnorm",
+           launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1, dm->rms_eps, v2));
+    Epilogue ek;
+    ek.kind = EPI_STORE;
+    ek.out = kvb;
+    ek.ldo = 2 * kw;
+    GemmTcProblem pk;
+    pk.M = (int)BT; pk.N = 2 * kw; pk.K = d; pk.A = u; pk.lda = d; pk.ldb = d;
+    pk.B[0] = w->wk; pk.B[1] = w->wv; pk.nB = 2; pk.split[0] = kw;
+    const bool tc_kv = tc && attention_tc_supported(hd, n, qw) &&
+                       attention_tc_supported(hd, T, 2 * kw);
+    if (tc_kv) {   // v straight to its transposed layout for the tensor-core attention
+      ek.vt = vt;
+      ek.vt_col0 = kw;
+      ek.vt_hd = hd;
+      ek.vt_hkv = hkv;
+      ek.vt_ld = (int)round8(T);
+      ek.n_per_seq = T;
+      v_transposed = gemm_tc_supported(pk, ek);
+    }
+    if (v_transposed) {
+      BW_RUN("gemm_qkv", launch_gemm_tc(c, pk, ek));
+    } else {
+      BW_RUN("gemm_qkv", bw_gemm(c, dt, (int)BT, kw, d, u, d, w->wk, d, kvb, 2 * kw, false));
+      BW_RUN("gemm_qkv", bw_gemm(c, dt, (int)BT, kw, d, u, d, w->wv, d, kvb + kw, 2 * kw, false));
+    }
+    BW_RUN("gemm_qkv", bw_gemm(c, dt, M, qw, d, v2, d, w->wq, d, qb, qw, false));
+    if (extras) {   // keys at every position, queries at the selected ones; projections kept
+      if (cudaMemcpy2DAsync(kpre, es * kw, kvb, es * 2 * kw, es * kw, (size_t)BT,
+                            cudaMemcpyDeviceToDevice, c.stream) != cudaSuccess ||
+          cudaMemcpyAsync(qpre, qb, es * (size_t)M * qw, cudaMemcpyDeviceToDevice, c.stream) !=
+              cudaSuccess)
+        return XMOD_ERR_CUDA;
+      BW_RUN("qk_norm_rope", launch_qk_transform(c, dt, BT, nullptr, kvb, 2 * kw, 0, 0, nullptr,
+                                                 0, hkv, w->k_norm, hd, dm->rms_eps,
+                                                 w->rope_theta, nullptr, nullptr, T));
+      BW_RUN("qk_norm_rope", launch_qk_transform(c, dt, M, nullptr, qb, qw, 0, hq, w->q_norm, 0,
+                                                 0, nullptr, hd, dm->rms_eps, w->rope_theta, idx,
+                                                 nullptr, T));
+    }
+    if (v_transposed) {
+      AttnKv akv;
+      akv.k = kvb;
+      akv.ldk = 2 * kw;
+      akv.nkv = T;
+      akv.qpos = idx;
+      BW_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qb, qw, vt, (int)round8(T), o,
+                                              nullptr, nullptr, &akv));
+    } else {
+      BW_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qb, qw, kvb, kvb + kw,
+                                                2 * kw, o, idx, T));
+    }
+  } else if (attn) {
   BW_RUN("gather_rmsnorm",
          launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1, dm->rms_eps, u));
   {
@@ -1096,13 +1347,16 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, d, qw, Mp, tA, Mp, tB, Mp, gr->wo, qw, true));
   BW_RUN("bwd_transpose", transpose(c, dt, d, d, qw, w->wo, qw, tW, d));  // Wo^T [qw, d]
   float* dO = (float*)bat(ws, L.dO);
-  const bool mma_attn = tc && attn_bwd_mma_supported(hd, qkv_w, qw);
+  const bool mma_attn = tc && attn_bwd_mma_supported(hd, fullkv ? qw : qkv_w, qw);
   BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, qw, d, da, d, tW, d, dO, qw, !mma_attn));
 
   // ======== attention
   E* dqkv = (E*)bat(ws, L.dqkv);
   const int kt_ld = (int)round8(n);
   const bool dq_tc = mma_attn && v_transposed && attn_bwd_dq_tc_supported(hd, qkv_w, qw, kt_ld);
+  if (fullkv)
+    return fullkv_tail<E>(c, dm, n, w, x, idx, dx, gr, ws, L, kvb, qb, kpre, qpre, vt,
+                          v_transposed, o, dO, mma_attn, dh);
   if (dq_tc) {   // tcgen05 (lse from the forward): dq, then dk and dv
     E* kt = (E*)bat(ws, L.kt);
     E* qt = (E*)bat(ws, L.qt);
@@ -1132,19 +1386,27 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   } else {
     AttnBwd p;
     p.n = n;
+    p.nk = n;
+    p.qpos = nullptr;
     p.hq = hq;
     p.hkv = hkv;
-    p.qkv = qkv;
+    p.q = qkv;
     p.ldq = qkv_w;
-    p.v = v_transposed ? (const void*)vt : (const void*)qkv;
+    p.k = qkv + qw;
+    p.ldk = qkv_w;
+    p.v = v_transposed ? (const void*)vt : (const void*)(qkv + qw + kw);
     p.vt_mode = v_transposed ? 1 : 0;
+    p.ldv = qkv_w;
     p.vt_ld = (int)round8(n);
     p.o = o;
     p.dO = dO;
     p.lse = (float*)bat(ws, L.lse);
     p.Dd = (float*)bat(ws, L.Dd);
-    p.dqkv = dqkv;
-    p.ldg = qkv_w;
+    p.dq = dqkv;
+    p.ldgq = qkv_w;
+    p.dk = dqkv + qw;
+    p.dv = dqkv + qw + kw;
+    p.ldgk = qkv_w;
     p.scale = 1.0f / sqrtf((float)hd);
     BW_RUN("bwd_attention", launch_attn_bwd(c, dt, B, hd, p));
   }

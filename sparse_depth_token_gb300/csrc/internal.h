@@ -298,6 +298,15 @@ bool attn_bwd_mma_supported(int hd, int ldq, int ldo);
 cudaError_t launch_attn_bwd_mma(const Ctx& c, int B, int n, int hq, int hkv, int hd,
                                 const void* qkv, int ldq, const void* o, const void* dO,
                                 float* lse, float* Dd, void* dqkv, int ldg, bool with_q = true);
+// The general form (Selected-Q / full-KV): n queries per sequence at ascending positions
+// qpos [B*n] (NULL: i, nk == n) over nk keys, query i seeing the keys j <= qpos[i];
+// q [B*n, ldq], k [B*nk, ldk], v [B*nk, ldv] (head h / KV head g at column h*hd / g*hd);
+// dq [B*n, ldgq], dk and dv [B*nk, ldgk] likewise.
+cudaError_t launch_attn_bwd_mma_kv(const Ctx& c, int B, int n, int nk, const int32_t* qpos,
+                                   int hq, int hkv, int hd, const void* q, int ldq,
+                                   const void* k, int ldk, const void* v, int ldv, const void* o,
+                                   const void* dO, float* lse, float* Dd, void* dq, int ldgq,
+                                   void* dk, void* dv, int ldgk, bool with_q = true);
 // dq of the attention backward on tcgen05 (bf16, head_dim 128): qkv rows [B*n, ldq] (q, k,
 // v columns), kt [B*hkv*128, kt_ld] the keys transposed (keys contiguous), o and dO
 // [B*n, hq*128] bf16, lse [B*n, hq] from the forward (log2 units); writes Dd [B*n, hq]

@@ -1,11 +1,14 @@
 """GPU parity of the layer backward (xmod_layer_bwd) against the oracle's layer_bwd,
 through the C ABI: dx, every weight gradient, dJ/dvarsigma and the Eq. 9 loss, for
 sparse layers under Eq. 7 and Eq. 6 (with and without the Eq. 9 term), dense layers, the
-QK-norm / RoPE extras and the FullAttn / Routed-FFN halves; and the stack backward.
+QK-norm / RoPE extras, the FullAttn / Routed-FFN halves and the Selected-Q / full-KV
+control; and the stack backward.
 
 Tolerances. fp32 (FFMA kernels throughout): relative 1e-5 as for the forward. bf16:
 relative L2 <= 1e-2 (the bound of the bf16 forward); a gradient has no natural unit,
 so the max-abs bound 2e-2 is taken relative to the gradient's largest reference entry.
+The scalar dJ/dvarsigma, a sum of terms of both signs, is bounded by the same relative
+figure times the L2 norm of its terms.
 """
 import numpy as np
 import pytest
@@ -56,7 +59,7 @@ def _run(X, w: I.Workload, kind, gate, route_coef, seed, extras=None):
         lw["rope_theta"] = theta
     bias = I.router_bias(w)
     x = I.residual_stream(w)
-    routed = kind in (X.LAYER_SPARSE, X.LAYER_ROUTED_FFN)
+    routed = kind in (X.LAYER_SPARSE, X.LAYER_ROUTED_FFN, X.LAYER_SPARSE_FULLKV)
     if routed:
         x, _ = U.enforce_routing_margin(x, w.dtype, lw["w_r"], bias, w.K)
     g = np.random.default_rng(seed)
@@ -89,16 +92,28 @@ def _run(X, w: I.Workload, kind, gate, route_coef, seed, extras=None):
         _check(gd["k_norm"].cpu().numpy(), ref["grads"]["gk"], w.dtype, "dk_norm")
     vs = float(gd["varsigma"][0])
     if routed and gate == X.GATE_XMOD:
-        _check(np.array([vs]), np.array([ref["varsigma"]]), w.dtype, "dvarsigma")
+        # dJ/dvarsigma = sum over the selected rows of r <dy, a + f> (Eq. 7): a sum whose
+        # terms cancel, so its error is bounded on the scale of the terms, r dy (a + f) =
+        # dy (y - x) / varsigma elementwise, as every other gradient is bounded on its own
+        x64 = I.to_f64(x, w.dtype)
+        fw = O.layer_fwd(U_dims(w), kind, w.K, gate, oracle_layer(lw, w.dtype), x64, bias=bias,
+                         idx_force=ref["idx"])
+        terms = I.to_f64(dy, w.dtype) * (fw["y"] - x64) / lw["varsigma"]
+        tol = (U.FP32_REL if w.dtype == "fp32" else U.BF16_REL_L2) * float(np.linalg.norm(terms))
+        assert np.isfinite(vs) and abs(vs - ref["varsigma"]) <= tol, \
+            f"dvarsigma: {vs} vs {ref['varsigma']} (bound {tol:.2e})"
     else:
         assert vs == 0.0
     if routed:
         _check(np.array([float(gd["route_loss"][0])]), np.array([ref["route_loss"]]), w.dtype,
                "route loss")
     if routed and route_coef == 0.0:
-        # a skipped token's gradient is the upstream gradient, bit for bit
+        # a skipped token's gradient is the upstream gradient, bit for bit (full-KV: a
+        # token that is also no selected query's key, i.e. after the last selected one)
         sel = np.zeros((w.B, w.T), bool)
         np.put_along_axis(sel, ref["idx"], True, 1)
+        if kind == X.LAYER_SPARSE_FULLKV:
+            sel |= np.arange(w.T)[None, :] <= ref["idx"].max(axis=1, keepdims=True)
         got = from_dev(dx, w.dtype)
         np.testing.assert_array_equal(got[~sel], I.to_f64(dy, w.dtype)[~sel])
 
@@ -150,6 +165,32 @@ def test_layer_bwd_mechanism_controls(X, dtype, kind, gate, coef):
         w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=256, K=4, d=256, hq=4, hkv=2, F=512, seed=35,
                                              weight_std=0.02 * np.sqrt(1536 / 256))
     _run(X, w, kind, gate, coef, seed=80 + 5 * kind + gate)
+
+
+@pytest.mark.parametrize("dtype,T,K,gate,coef,extras", [
+    ("fp32", 64, 4, 0, 0.0, None), ("fp32", 64, 4, 1, 0.3, None), ("fp32", 64, 4, 0, 0.1, 1e4),
+    ("bf16", 256, 4, 0, 0.1, None), ("bf16", 303, 3, 1, 0.0, None), ("bf16", 256, 8, 0, 0.0, 1e4)])
+def test_layer_bwd_fullkv(X, dtype, T, K, gate, coef, extras):
+    """The Selected-Q / full-KV control (SPARSE_FULLKV): the selected tokens' queries over
+    every token's keys and values, so the gradient also reaches unselected rows; both
+    gates, the Eq. 9 term, the QK-norm / RoPE extras, a ragged count (n = 101 of 303)."""
+    if dtype == "fp32":
+        w = I.WORKLOADS["tiny_fp32"].replace(T=T, K=K)
+    else:
+        w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=T, K=K, d=256, hq=4, hkv=2, F=512, seed=37,
+                                             weight_std=0.02 * np.sqrt(1536 / 256))
+    _run(X, w, X.LAYER_SPARSE_FULLKV, gate, coef, seed=120 + T + K + gate, extras=extras)
+
+
+@pytest.mark.parametrize("kind,T,K", [(1, 256, 4), (1, 303, 3), (0, 160, 1), (4, 256, 4),
+                                      (4, 303, 3)])
+def test_layer_bwd_bf16_head_dim_64(X, kind, T, K):
+    """bf16 at head_dim 64: the attention backward on the warp-level tensor-core MMA kernels
+    (the tcgen05 pair takes head_dim 128), for sparse, dense and Selected-Q / full-KV
+    layers, ragged counts included."""
+    w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=T, K=K, d=256, hq=4, hkv=2, hd=64, F=512,
+                                         seed=39, weight_std=0.02 * np.sqrt(1536 / 256))
+    _run(X, w, kind, X.GATE_XMOD, 0.1 if kind else 0.0, seed=140 + T + K + kind)
 
 
 def _grad_set(w, n_layers):
