@@ -250,6 +250,19 @@ def oracle_sample(w: I.Workload, budget_s: float = 15.0, max_reps: int = 50):
         f"{reps} repetition(s) in {el:.1f} s")
 
 
+def single_thread_variant(sample_fn, budget_s: float) -> dict:
+    """The same oracle sample on one host thread (OpenMP limited to 1), then the thread
+    count restored: the single-thread variant of the oracle timing."""
+    import oracle as O
+    cores = O.num_threads()
+    O.set_num_threads(1)
+    try:
+        v, _, sample = sample_fn(budget_s)
+    finally:
+        O.set_num_threads(cores)
+    return {"value": v, "cores": 1, "sample": sample}
+
+
 def run_reference(args):
     """--impl reference: the oracle as it stands, timed on the host cores (rank 0 only)."""
     rank = int(os.environ.get("RANK", "0"))
@@ -553,7 +566,9 @@ def run_xmod(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = oracle_sample(w, budget_s=args.cpu_budget)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+               "single_thread": single_thread_variant(
+                   lambda bs: oracle_sample(w, budget_s=bs, max_reps=1), args.cpu_budget / 3)}
 
     if rank == 0:
         cfg = workload_config(w)
@@ -1072,7 +1087,9 @@ def run_routing(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = oracle_routing_sample(w, K, budget_s=args.cpu_budget)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+               "single_thread": single_thread_variant(
+                   lambda bs: oracle_routing_sample(w, K, budget_s=bs), args.cpu_budget / 3)}
 
     if rank == 0:
         h = results[K]

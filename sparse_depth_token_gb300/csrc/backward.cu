@@ -21,6 +21,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -60,37 +61,58 @@ __device__ __forceinline__ float softplus_f(float z) {
 
 // ---------------------------------------------------------------- transpose
 // out[c, r] = in[r, c] for r < R, c < C; out[c, r] = 0 for R <= r < Rpad (zero tokens).
-// 64 x 64 tiles, 256 threads: each thread moves 16 elements, all loads in flight.
+// The kernel moves bits (U = a 2- or 4-byte word; 0 bits are +0.0 in bf16 and fp32).
+// 64 x 64 tiles, 256 threads. Both phases move 16-byte chunks (V words) where the
+// pointers, strides and bounds allow it (vec_in / vec_out), word by word otherwise. In
+// shared memory chunk ch of tile row r sits at chunk ch ^ ((r / V) % (64 / V)): the
+// read phase gathers one word from each of V consecutive rows, and across a warp those
+// rows fall in distinct chunks, so neither phase has bank conflicts.
 constexpr int TR_T = 64;
 
 // grid.z runs over a batch of such matrices, in_bs / out_bs elements apart.
-template <typename T>
+template <typename U>
 __global__ void __launch_bounds__(256)
-transpose_kernel(int R, int Rpad, int C, const T* __restrict__ in, int64_t ldi,
-                 T* __restrict__ out, int64_t ldo, int64_t in_bs, int64_t out_bs) {
+transpose_kernel(int R, int Rpad, int C, const U* __restrict__ in, int64_t ldi,
+                 U* __restrict__ out, int64_t ldo, int64_t in_bs, int64_t out_bs, int vec_in,
+                 int vec_out) {
   pdl_trigger();
   pdl_wait();
+  constexpr int V = 16 / sizeof(U), CH = TR_T / V;
   in += blockIdx.z * in_bs;
   out += blockIdx.z * out_bs;
-  __shared__ T tile[TR_T][TR_T + 1];
+  __shared__ __align__(16) U tile[TR_T * TR_T];
   const int r0 = blockIdx.y * TR_T, c0 = blockIdx.x * TR_T;
-  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (int e = threadIdx.x; e < TR_T * CH; e += 256) {
+    const int r = e / CH, ch = e - r * CH, gr = r0 + r, gc = c0 + ch * V;
+    U* dst = tile + r * TR_T + ((ch ^ ((r / V) & (CH - 1))) * V);
+    if (vec_in && gr < R && gc + V <= C) {
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(in + (int64_t)gr * ldi + gc);
+    } else {
 #pragma unroll
-  for (int k = 0; k < TR_T / 8; ++k)
-#pragma unroll
-    for (int h = 0; h < TR_T; h += 32) {
-      const int r = r0 + ty + 8 * k, c = c0 + tx + h;
-      tile[ty + 8 * k][tx + h] =
-          (r < R && c < C) ? in[(int64_t)r * ldi + c] : Elem<T>::from_f(0.0f);
+      for (int k = 0; k < V; ++k) dst[k] = (gr < R && gc + k < C) ? in[(int64_t)gr * ldi + gc + k] : U(0);
     }
+  }
   __syncthreads();
+  for (int e = threadIdx.x; e < TR_T * CH; e += 256) {
+    const int c = e / CH, ch = e - c * CH, gc = c0 + c, gr = r0 + ch * V;
+    if (gc >= C) continue;
+    // rows ch * V + k all have r / V == ch: their chunk c / V sits at (c / V) ^ ch
+    const U* src = tile + ((c / V) ^ ch) * V + (c % V);
+    union {
+      uint4 q;
+      U w[V];
+    } v;
 #pragma unroll
-  for (int k = 0; k < TR_T / 8; ++k)
+    for (int k = 0; k < V; ++k) v.w[k] = src[(ch * V + k) * TR_T];
+    U* dst = out + (int64_t)gc * ldo + gr;
+    if (vec_out && gr + V <= Rpad) {
+      *reinterpret_cast<uint4*>(dst) = v.q;
+    } else {
 #pragma unroll
-    for (int h = 0; h < TR_T; h += 32) {
-      const int c = c0 + ty + 8 * k, r = r0 + tx + h;
-      if (c < C && r < Rpad) out[(int64_t)c * ldo + r] = tile[tx + h][ty + 8 * k];
+      for (int k = 0; k < V; ++k)
+        if (gr + k < Rpad) dst[k] = v.w[k];
     }
+  }
 }
 
 // ---------------------------------------------------------------- gated residual backward
@@ -818,13 +840,18 @@ inline char* bat(void* ws, size_t off) { return (char*)ws + off; }
     if (_e != cudaSuccess) return XMOD_ERR_CUDA;  \
   } while (0)
 
+// out[c, r] = in[r, c] (zero for R <= r < Rpad) of T-typed matrices (2- or 4-byte).
 template <typename T>
 cudaError_t transpose_t(const Ctx& c, int R, int Rpad, int C, const void* in, int64_t ldi,
                         void* out, int64_t ldo, int batch, int64_t in_bs, int64_t out_bs) {
   if (R <= 0 || C <= 0 || batch <= 0) return cudaSuccess;
+  using U = typename std::conditional<sizeof(T) == 2, uint16_t, uint32_t>::type;
+  constexpr int V = 16 / sizeof(U);
+  const int vec_in = ((uintptr_t)in % 16 == 0 && ldi % V == 0 && in_bs % V == 0) ? 1 : 0;
+  const int vec_out = ((uintptr_t)out % 16 == 0 && ldo % V == 0 && out_bs % V == 0) ? 1 : 0;
   const dim3 grid((C + TR_T - 1) / TR_T, (Rpad + TR_T - 1) / TR_T, batch);
-  return launch_pdl(transpose_kernel<T>, grid, dim3(32, 8), 0, c.stream, R, Rpad, C,
-                    (const T*)in, ldi, (T*)out, ldo, in_bs, out_bs);
+  return launch_pdl(transpose_kernel<U>, grid, dim3(256), 0, c.stream, R, Rpad, C,
+                    (const U*)in, ldi, (U*)out, ldo, in_bs, out_bs, vec_in, vec_out);
 }
 
 // out[c, r] = in[r, c] (zero for R <= r < Rpad); with batch > 1, `batch` such matrices,
