@@ -17,6 +17,11 @@
 //               TMEM as bf16 pairs over the first half of S_j's columns
 // The row statistics lse come from the forward pass (its log2-sum-exp2 output); D is
 // computed here and written for the key/value kernel.
+//
+// Both kernels also take the Selected-Q / full-KV control of the same notes ("mechanism
+// controls"): n queries per sequence at ascending positions qpos among nk keys, query i
+// seeing the keys j <= qpos[i], keys and values read from their own rows; the compact
+// case is qpos[i] = i, nk = n.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -49,7 +54,10 @@ static_assert((1 + 2 * NST + 8) * 8 + 16 <= 256, "barrier block overflows");
 
 struct DqArgs {
   int n, hq, hkv, nqb;
-  int qw, kw;
+  int nk;                     // keys per sequence
+  const int32_t* qpos;        // [B*n] query positions (NULL: i)
+  int k_col0, v_col0;         // columns of KV head 0's k and v in the key map's rows
+  int qw;
   float scale_log2, scale;
   const float* lse;           // [B*n, hq], log2 units
   const __nv_bfloat16* o;     // [B*n, qw]
@@ -121,7 +129,9 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   const uint32_t tDQ = tmem + 256u;
   pdl_wait();
   const int last_q = min(q0 + QB, a.n) - 1;
-  const int nkb = q0 < a.n ? last_q / KB + 1 : 0;
+  // key blocks up to the block's last query position (positions ascend)
+  const int last_key = a.qpos && q0 < a.n ? a.qpos[(int64_t)b * a.n + last_q] : last_q;
+  const int nkb = q0 < a.n ? last_key / KB + 1 : 0;
 
   if (warp == 0) {
     if (lane == 0 && nkb > 0) {
@@ -137,10 +147,10 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           break;
         const uint32_t st = sSt0 + s * STAGE;
         mbar_arrive_expect_tx(ST_FULL0 + 8 * s, STAGE);
-        tma_load_3d(st, &tmK, ST_FULL0 + 8 * s, a.qw + g * HD, j * KB, b);
-        tma_load_3d(st + K_CHUNK, &tmK, ST_FULL0 + 8 * s, a.qw + g * HD + 64, j * KB, b);
-        tma_load_3d(st + K_TILE, &tmK, ST_FULL0 + 8 * s, a.qw + a.kw + g * HD, j * KB, b);
-        tma_load_3d(st + K_TILE + K_CHUNK, &tmK, ST_FULL0 + 8 * s, a.qw + a.kw + g * HD + 64,
+        tma_load_3d(st, &tmK, ST_FULL0 + 8 * s, a.k_col0 + g * HD, j * KB, b);
+        tma_load_3d(st + K_CHUNK, &tmK, ST_FULL0 + 8 * s, a.k_col0 + g * HD + 64, j * KB, b);
+        tma_load_3d(st + K_TILE, &tmK, ST_FULL0 + 8 * s, a.v_col0 + g * HD, j * KB, b);
+        tma_load_3d(st + K_TILE + K_CHUNK, &tmK, ST_FULL0 + 8 * s, a.v_col0 + g * HD + 64,
                     j * KB, b);
         tma_load_2d(st + 2 * K_TILE, &tmKt, ST_FULL0 + 8 * s, j * KB, kt_row);
       }
@@ -218,6 +228,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int qi = q0 + row;
     const bool valid = qi < a.n;
     const int64_t grow = (int64_t)b * a.n + (valid ? qi : 0);
+    const int qp = valid ? (a.qpos ? a.qpos[grow] : qi) : -1;   // the row's last key
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     // D_i = <dO_i, o_i> and the row's lse (log2 units)
     float D = 0.f, lse2 = 0.f;
@@ -261,7 +272,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       float pk[32];
 #pragma unroll
       for (int i = 0; i < KB; i += 2) {
-        const bool ok0 = valid && key0 + i <= qi, ok1 = valid && key0 + i + 1 <= qi;
+        const bool ok0 = key0 + i <= qp, ok1 = key0 + i + 1 <= qp;
         const float p0 = ok0 ? ex2f(fmaf(sv[i], a.scale_log2, -lse2)) : 0.f;
         const float p1 = ok1 ? ex2f(fmaf(sv[i + 1], a.scale_log2, -lse2)) : 0.f;
         pk[i / 2] = __uint_as_float(pack_bf16x2(p0 * (dp[i] - D), p1 * (dp[i + 1] - D)));
@@ -317,7 +328,8 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 
 // ---------------------------------------------------------------- dK, dV
 // One CTA per (128-key block, KV head, sequence), over the group's query heads and the
-// 64-query blocks at or after the key block:
+// 64-query blocks from the one holding the first query positioned at or after the key
+// block's first key:
 //   warp 0      TMA: the K and V tiles (rows) once, then per query block the rows of Q
 //               and dO and their transposes Q^T, dO^T ([head dim, queries]) into a
 //               two-stage ring
@@ -327,7 +339,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 //   warps 2..5  one key row per thread: P^T = exp2(scale_log2 s - lse[query]) under the
 //               causal mask, dS^T = P^T (dP^T - D[query]), both back to TMEM as bf16
 //               pairs over the first halves of their buffers
-constexpr int KVB = 128;                  // keys per CTA
+constexpr int KVB = kAttnBwdKvBlock;      // keys per CTA (128)
 constexpr int QBK = 64;                   // queries per block
 constexpr int KV_TILE = 2 * CHUNK;        // 128 keys x 128 head dims
 constexpr int Q_CHUNK = QBK * 128;        // 64 rows x 64 columns
@@ -341,13 +353,20 @@ static_assert((1 + 2 * KST2 + 8) * 8 + 16 <= 256, "barrier block overflows");
 
 struct DkvArgs {
   int n, hq, hkv;
-  int qw, kw;
+  int nk;                     // keys per sequence
+  int k_col0, v_col0;         // columns of KV head 0's k and v in the key map's rows
+  // Selected-Q / full-KV (NULL both for the compact case): qposS [B, ldS] the query
+  // positions, -1 past n; qstart [B, key blocks] the first query positioned at or after
+  // each key block's first key
+  const int32_t* qposS;
+  const int32_t* qstart;
   float scale_log2, scale;
   const float* lseT;          // [B*hq, ldS]: lse (log2 units), per head, queries contiguous
   const float* DdT;           // [B*hq, ldS]: D, same layout
   int ldS;                    // a multiple of 64 at least n
-  __nv_bfloat16* dqkv;        // k and v columns of [B*n, ldg]
-  int ldg;
+  __nv_bfloat16* dk;          // dk, dv of KV head g at column g*HD of [B*nk, ldgk]
+  __nv_bfloat16* dv;
+  int ldgk;
   int* status;
 };
 
@@ -376,9 +395,11 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
   const int g = blockIdx.x, b = blockIdx.y, kb = blockIdx.z;   // key block 0 has most work
   const int G = a.hq / a.hkv;
   const int k0 = kb * KVB;
-  const int qb0 = k0 / QBK;                         // first query block at or after k0
+  // the first query that can see key k0 (compact case: query k0), its 64-query block
+  const int qs = a.qstart ? a.qstart[(int64_t)b * gridDim.z + kb] : min(k0, a.n);
+  const int qb0 = qs / QBK;
   const int nqb = (a.n + QBK - 1) / QBK - qb0;      // query blocks per head
-  const int items = k0 < a.n ? G * nqb : 0;
+  const int items = k0 < a.nk && qs < a.n ? G * nqb : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(KV_FULL, 1);
@@ -411,10 +432,10 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
   if (warp == 0) {
     if (lane == 0 && items > 0) {
       mbar_arrive_expect_tx(KV_FULL, 2 * KV_TILE);
-      tma_load_3d(sK, &tmKV, KV_FULL, a.qw + g * HD, k0, b);
-      tma_load_3d(sK + CHUNK, &tmKV, KV_FULL, a.qw + g * HD + 64, k0, b);
-      tma_load_3d(sV, &tmKV, KV_FULL, a.qw + a.kw + g * HD, k0, b);
-      tma_load_3d(sV + CHUNK, &tmKV, KV_FULL, a.qw + a.kw + g * HD + 64, k0, b);
+      tma_load_3d(sK, &tmKV, KV_FULL, a.k_col0 + g * HD, k0, b);
+      tma_load_3d(sK + CHUNK, &tmKV, KV_FULL, a.k_col0 + g * HD + 64, k0, b);
+      tma_load_3d(sV, &tmKV, KV_FULL, a.v_col0 + g * HD, k0, b);
+      tma_load_3d(sV + CHUNK, &tmKV, KV_FULL, a.v_col0 + g * HD + 64, k0, b);
       for (int it = 0; it < items; ++it) {
         const int s = it % KST2;
         const int h = g * G + it / nqb, q0 = (qb0 + it % nqb) * QBK;
@@ -518,6 +539,7 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
       // never used: their probabilities are masked to 0)
       const float* lrow = a.lseT + (int64_t)(b * a.hq + h) * a.ldS + q0;
       const float* drow = a.DdT + (int64_t)(b * a.hq + h) * a.ldS + q0;
+      const int32_t* prow_q = a.qposS ? a.qposS + (int64_t)b * a.ldS + q0 : nullptr;
       if (!mbar_wait(S_FULL0 + 8 * s, (uint32_t)(it >> 1) & 1u, abort_flag, a.status)) {
         ok = false;
         break;
@@ -539,11 +561,18 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
         const float4 l4 = *reinterpret_cast<const float4*>(lrow + c4);
         const float4 d4 = *reinterpret_cast<const float4*>(drow + c4);
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+        int qpv[4];   // the queries' positions, -1 past n
+        if (prow_q) {
+          const int4 p4 = *reinterpret_cast<const int4*>(prow_q + c4);
+          qpv[0] = p4.x; qpv[1] = p4.y; qpv[2] = p4.z; qpv[3] = p4.w;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) qpv[e] = q0 + c4 + e < a.n ? q0 + c4 + e : -1;
+        }
         float pv[4], dsv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int q = q0 + c4 + e;
-          const bool okp = key < a.n && q < a.n && key <= q;
+          const bool okp = key < a.nk && key <= qpv[e];
           const float p = okp ? ex2f(fmaf(sv[c4 + e], a.scale_log2, -lv[e])) : 0.f;
           pv[e] = p;
           dsv[e] = okp ? p * (dp[c4 + e] - dv[e]) : 0.f;
@@ -561,25 +590,36 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
       tc_fence_before();
       mbar_arrive(P_FULL0 + 8 * s);
     }
-    if (items == 0) ok = false;
+    if (items == 0) {   // no query sees these keys: their gradients are zero
+      ok = false;
+      if (key < a.nk) {
+        const int64_t orow = ((int64_t)b * a.nk + key) * a.ldgk + g * HD;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 4
+        for (int e = 0; e < HD; e += 8) {
+          *reinterpret_cast<uint4*>(a.dk + orow + e) = z;
+          *reinterpret_cast<uint4*>(a.dv + orow + e) = z;
+        }
+      }
+    }
     if (ok) {
       const int il = items - 1;
       ok = mbar_wait(P_EMPTY0 + 8 * (il & 1), (uint32_t)(il >> 1) & 1u, abort_flag, a.status);
     }
     if (ok) {
       tc_fence_after();
-      __nv_bfloat16* drow_out = a.dqkv + ((int64_t)b * a.n + key) * a.ldg;
+      const int64_t orow = ((int64_t)b * a.nk + key) * a.ldgk + g * HD;
 #pragma unroll 1
       for (int part = 0; part < 2; ++part) {   // dK (scaled), then dV
         const uint32_t src = (part == 0 ? tDK : tDV) + lane_off;
         const float sc = part == 0 ? a.scale : 1.0f;
-        __nv_bfloat16* dst = drow_out + a.qw + (part == 0 ? 0 : a.kw) + g * HD;
+        __nv_bfloat16* dst = (part == 0 ? a.dk : a.dv) + orow;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float v[32];
           tmem_ld32(src + c * 32, v);
           tmem_ld_wait();
-          if (key < a.n) {
+          if (key < a.nk) {
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
               uint4 q;
@@ -614,21 +654,28 @@ bool attn_bwd_dq_tc_supported(int hd, int ldq, int qw, int kt_ld) {
   return hd == HD && ldq % 8 == 0 && qw % 8 == 0 && kt_ld % 8 == 0 && tma_available();
 }
 
-cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
-                                  int ldq, const void* kt, int kt_ld, const void* o,
-                                  const void* dO, const float* lse, float* Dd, void* dqkv,
-                                  int ldg, float* DdT, int ldS) {
+cudaError_t launch_attn_bwd_dq_tc_kv(const Ctx& c, int B, int n, int nk, const int32_t* qpos,
+                                     int hq, int hkv, const void* q, int ldq, const void* kv,
+                                     int ldk, int k_col0, int v_col0, const void* kt, int kt_ld,
+                                     const void* o, const void* dO, const float* lse, float* Dd,
+                                     void* dq, int ldg, float* DdT, int ldS) {
   if (B <= 0 || n <= 0) return cudaSuccess;
-  const int qw = hq * HD, kw = hkv * HD;
-  if (!attn_bwd_dq_tc_supported(HD, ldq, qw, kt_ld) || ldg % 8) return cudaErrorInvalidValue;
+  const int qw = hq * HD;
+  if (!attn_bwd_dq_tc_supported(HD, ldq, qw, kt_ld) || ldk % 8 || ldg % 8 || nk <= 0 ||
+      (!qpos && nk != n))
+    return cudaErrorInvalidValue;
   CUtensorMap mQ, mDO, mK, mKt;
   {
     const int64_t dims[3] = {ldq, n, B};
     const int64_t strides[2] = {(int64_t)ldq * 2, (int64_t)n * ldq * 2};
     const int qbox[3] = {64, QB, 1};
+    if (!tma_map_bf16(&mQ, q, 3, dims, strides, qbox)) return cudaErrorInvalidValue;
+  }
+  {
+    const int64_t dims[3] = {ldk, nk, B};
+    const int64_t strides[2] = {(int64_t)ldk * 2, (int64_t)nk * ldk * 2};
     const int kbox[3] = {64, KB, 1};
-    if (!tma_map_bf16(&mQ, qkv, 3, dims, strides, qbox)) return cudaErrorInvalidValue;
-    if (!tma_map_bf16(&mK, qkv, 3, dims, strides, kbox)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(&mK, kv, 3, dims, strides, kbox)) return cudaErrorInvalidValue;
   }
   {
     const int64_t dims[3] = {qw, n, B};
@@ -637,7 +684,7 @@ cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, c
     if (!tma_map_bf16(&mDO, dO, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
-    const int64_t dims[2] = {n, (int64_t)B * hkv * HD};
+    const int64_t dims[2] = {nk, (int64_t)B * hkv * HD};
     const int64_t strides[1] = {(int64_t)kt_ld * 2};
     const int box[2] = {64, HD};
     if (!tma_map_bf16(&mKt, kt, 2, dims, strides, box)) return cudaErrorInvalidValue;
@@ -647,8 +694,11 @@ cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, c
   a.hq = hq;
   a.hkv = hkv;
   a.nqb = (n + QB - 1) / QB;
+  a.nk = nk;
+  a.qpos = qpos;
+  a.k_col0 = k_col0;
+  a.v_col0 = v_col0;
   a.qw = qw;
-  a.kw = kw;
   a.scale = 1.0f / sqrtf((float)HD);
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   a.lse = lse;
@@ -657,7 +707,7 @@ cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, c
   a.Dd = Dd;
   a.DdT = DdT;
   a.ldS = ldS;
-  a.dq = (__nv_bfloat16*)dqkv;
+  a.dq = (__nv_bfloat16*)dq;
   a.ldg = ldg;
   a.status = c.status;
   static bool attr = false;
@@ -671,22 +721,38 @@ cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, c
                     mQ, mDO, mK, mKt, a);
 }
 
-cudaError_t launch_attn_bwd_dkv_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
-                                   int ldq, const void* dO, const void* qt, const void* dOt,
-                                   int t_ld, const float* lseT, const float* DdT, int ldS,
-                                   void* dqkv, int ldg) {
-  if (B <= 0 || n <= 0) return cudaSuccess;
+cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
+                                  int ldq, const void* kt, int kt_ld, const void* o,
+                                  const void* dO, const float* lse, float* Dd, void* dqkv,
+                                  int ldg, float* DdT, int ldS) {
   const int qw = hq * HD, kw = hkv * HD;
-  if (ldq % 8 || t_ld % 8 || ldg % 8 || ldS % QBK || ldS < n || hq % hkv || !tma_available())
+  return launch_attn_bwd_dq_tc_kv(c, B, n, n, nullptr, hq, hkv, qkv, ldq, qkv, ldq, qw, qw + kw,
+                                  kt, kt_ld, o, dO, lse, Dd, dqkv, ldg, DdT, ldS);
+}
+
+cudaError_t launch_attn_bwd_dkv_tc_kv(const Ctx& c, int B, int n, int nk, const int32_t* qposS,
+                                      const int32_t* qstart, int hq, int hkv, const void* q,
+                                      int ldq, const void* kv, int ldk, int k_col0, int v_col0,
+                                      const void* dO, const void* qt, const void* dOt, int t_ld,
+                                      const float* lseT, const float* DdT, int ldS, void* dk,
+                                      void* dv, int ldgk) {
+  if (B <= 0 || n <= 0 || nk <= 0) return cudaSuccess;
+  const int qw = hq * HD;
+  if (ldq % 8 || ldk % 8 || t_ld % 8 || ldgk % 8 || ldS % QBK || ldS < n || hq % hkv ||
+      !tma_available() || (!qposS) != (!qstart) || (!qposS && nk != n))
     return cudaErrorInvalidValue;
   CUtensorMap mKV, mQ, mDO, mQt, mDOt;
   {
+    const int64_t dims[3] = {ldk, nk, B};
+    const int64_t strides[2] = {(int64_t)ldk * 2, (int64_t)nk * ldk * 2};
+    const int kvbox[3] = {64, KVB, 1};
+    if (!tma_map_bf16(&mKV, kv, 3, dims, strides, kvbox)) return cudaErrorInvalidValue;
+  }
+  {
     const int64_t dims[3] = {ldq, n, B};
     const int64_t strides[2] = {(int64_t)ldq * 2, (int64_t)n * ldq * 2};
-    const int kvbox[3] = {64, KVB, 1};
     const int qbox[3] = {64, QBK, 1};
-    if (!tma_map_bf16(&mKV, qkv, 3, dims, strides, kvbox)) return cudaErrorInvalidValue;
-    if (!tma_map_bf16(&mQ, qkv, 3, dims, strides, qbox)) return cudaErrorInvalidValue;
+    if (!tma_map_bf16(&mQ, q, 3, dims, strides, qbox)) return cudaErrorInvalidValue;
   }
   {
     const int64_t dims[3] = {qw, n, B};
@@ -705,15 +771,19 @@ cudaError_t launch_attn_bwd_dkv_tc(const Ctx& c, int B, int n, int hq, int hkv, 
   a.n = n;
   a.hq = hq;
   a.hkv = hkv;
-  a.qw = qw;
-  a.kw = kw;
+  a.nk = nk;
+  a.k_col0 = k_col0;
+  a.v_col0 = v_col0;
+  a.qposS = qposS;
+  a.qstart = qstart;
   a.scale = 1.0f / sqrtf((float)HD);
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   a.lseT = lseT;
   a.DdT = DdT;
   a.ldS = ldS;
-  a.dqkv = (__nv_bfloat16*)dqkv;
-  a.ldg = ldg;
+  a.dk = (__nv_bfloat16*)dk;
+  a.dv = (__nv_bfloat16*)dv;
+  a.ldgk = ldgk;
   a.status = c.status;
   static bool attr = false;
   if (!attr) {
@@ -722,8 +792,19 @@ cudaError_t launch_attn_bwd_dkv_tc(const Ctx& c, int B, int n, int hq, int hkv, 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(attn_bwd_dkv_tc_kernel, dim3(hkv, B, (n + KVB - 1) / KVB), dim3(THREADS),
+  return launch_pdl(attn_bwd_dkv_tc_kernel, dim3(hkv, B, (nk + KVB - 1) / KVB), dim3(THREADS),
                     KV_SMEM, c.stream, mKV, mQ, mDO, mQt, mDOt, a);
+}
+
+cudaError_t launch_attn_bwd_dkv_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
+                                   int ldq, const void* dO, const void* qt, const void* dOt,
+                                   int t_ld, const float* lseT, const float* DdT, int ldS,
+                                   void* dqkv, int ldg) {
+  const int qw = hq * HD, kw = hkv * HD;
+  __nv_bfloat16* g = (__nv_bfloat16*)dqkv;
+  return launch_attn_bwd_dkv_tc_kv(c, B, n, n, nullptr, nullptr, hq, hkv, qkv, ldq, qkv, ldq, qw,
+                                   qw + kw, dO, qt, dOt, t_ld, lseT, DdT, ldS, g + qw, g + qw + kw,
+                                   ldg);
 }
 
 }  // namespace xmod

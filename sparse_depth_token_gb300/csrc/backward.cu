@@ -454,6 +454,28 @@ fullkv_merge_kernel(int64_t M, int seqT, int n, int d, const int32_t* __restrict
   }
 }
 
+// Selected-Q / full-KV, for the tcgen05 dk / dv kernel: qposS [B, ldS] = the query
+// positions qpos [B, n] padded with -1, and qstart [B, nkb] = the first query positioned
+// at or after key block kb's first key kb * kvb (n if none). One CTA per sequence.
+__global__ void __launch_bounds__(256)
+fullkv_qindex_kernel(int n, int ldS, int nkb, int kvb, const int32_t* __restrict__ qpos,
+                     int32_t* __restrict__ qposS, int32_t* __restrict__ qstart) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x;
+  const int32_t* p = qpos + (int64_t)b * n;
+  for (int i = threadIdx.x; i < ldS; i += blockDim.x) qposS[(int64_t)b * ldS + i] = i < n ? p[i] : -1;
+  for (int kb = threadIdx.x; kb < nkb; kb += blockDim.x) {
+    const int k0 = kb * kvb;
+    int lo = 0, hi = n;   // positions ascend: binary search for the first >= k0
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (p[mid] >= k0) hi = mid; else lo = mid + 1;
+    }
+    qstart[(int64_t)b * nkb + kb] = lo;
+  }
+}
+
 // ---------------------------------------------------------------- attention backward
 // Causal GQA attention on each sequence's n compact rows (query head h reads KV head
 // h / (hq / hkv)), or on n queries at ascending positions over nk keys, each query seeing
@@ -763,7 +785,7 @@ inline int64_t round8(int64_t v) { return (v + 7) / 8 * 8; }
 struct BwLayout {
   size_t status, s, r, idx, r_sel, dr, dvs, ds, lossp, u, qkv, vt, o, a, h, v2, gu, H, f, df,
       dae, dH, dGU, dv2, dh, da, dO, lse, Dd, dqkv, du, rstd1, rstd2, tA, tB, tW, part, qkpre,
-      dgq, dgk, kt, qt, dOt, lseT, DdT, total;
+      dgq, dgk, kt, qt, dOt, lseT, DdT, qposS, qstart, total;
 };
 
 constexpr int kMaxChunks = 1024;   // row chunks of the column reductions
@@ -823,6 +845,8 @@ BwLayout bw_layout(const xmod_dims* dm) {
   const size_t lds = ((size_t)dm->T + 63) / 64 * 64;
   L.lseT = take(4 * (size_t)dm->B * hq * lds);
   L.DdT = take(4 * (size_t)dm->B * hq * lds);
+  L.qposS = take(4 * (size_t)dm->B * lds);   // full-KV: query positions, padded
+  L.qstart = take(4 * (size_t)dm->B * (((size_t)dm->T + kAttnBwdKvBlock - 1) / kAttnBwdKvBlock));
   L.total = off;
   return L;
 }
@@ -960,11 +984,42 @@ int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weigh
   float* part = (float*)bat(ws, L.part);
 
   // ======== attention: n queries per sequence over its T keys
-  if (mma) {
+  const int kt_ld = (int)round8(T), qt_ld = (int)round8(n), ldS = (n + 63) / 64 * 64;
+  const bool tc_bwd = mma && v_transposed && attn_bwd_dq_tc_supported(hd, qw, qw, kt_ld);
+  if (mma && v_transposed) {   // the backward reads v by rows: the v projection once more
     E* kvw = const_cast<E*>(kvb);
-    if (v_transposed)   // the MMA kernels read v by rows: the v projection once more
-      BW_RUN("gemm_qkv", bw_gemm(c, dt, BT, kw, d, bat(ws, L.u), d, w->wv, d, kvw + kw, 2 * kw,
-                                 false));
+    BW_RUN("gemm_qkv", bw_gemm(c, dt, BT, kw, d, bat(ws, L.u), d, w->wv, d, kvw + kw, 2 * kw,
+                               false));
+  }
+  if (tc_bwd) {   // tcgen05 (the forward wrote lse): dq, then dk and dv over every key
+    E* kt = (E*)bat(ws, L.kt);
+    E* qt = (E*)bat(ws, L.qt);
+    E* dOt = (E*)bat(ws, L.dOt);
+    float* lseT = (float*)bat(ws, L.lseT);
+    float* DdT = (float*)bat(ws, L.DdT);
+    int32_t* qposS = (int32_t*)bat(ws, L.qposS);
+    int32_t* qstart = (int32_t*)bat(ws, L.qstart);
+    const int nkb = (T + kAttnBwdKvBlock - 1) / kAttnBwdKvBlock;
+    // per sequence, transposed: keys [hkv * hd, T], queries and dO [hq * hd, n], lse [hq, n]
+    BW_RUN("bwd_transpose", transpose(c, dt, T, T, kw, kvb, 2 * kw, kt, kt_ld, B,
+                                      (int64_t)T * 2 * kw, (int64_t)kw * kt_ld));
+    BW_RUN("bwd_transpose", transpose(c, dt, n, n, qw, qb, qw, qt, qt_ld, B, (int64_t)n * qw,
+                                      (int64_t)qw * qt_ld));
+    BW_RUN("bwd_transpose", transpose(c, dt, n, n, qw, dO, qw, dOt, qt_ld, B, (int64_t)n * qw,
+                                      (int64_t)qw * qt_ld));
+    BW_RUN("bwd_transpose", transpose_t<float>(c, n, n, hq, bat(ws, L.lse), hq, lseT, ldS, B,
+                                               (int64_t)n * hq, (int64_t)hq * ldS));
+    BW_RUN("bwd_rows", launch_pdl(fullkv_qindex_kernel, dim3(B), dim3(256), 0, c.stream, n, ldS,
+                                  nkb, kAttnBwdKvBlock, idx, qposS, qstart));
+    BW_RUN("bwd_attention",
+           launch_attn_bwd_dq_tc_kv(c, B, n, T, idx, hq, hkv, qb, qw, kvb, 2 * kw, 0, kw, kt,
+                                    kt_ld, o, dO, (const float*)bat(ws, L.lse),
+                                    (float*)bat(ws, L.Dd), dqb, qw, DdT, ldS));
+    BW_RUN("bwd_attention",
+           launch_attn_bwd_dkv_tc_kv(c, B, n, T, qposS, qstart, hq, hkv, qb, qw, kvb, 2 * kw, 0,
+                                     kw, dO, qt, dOt, qt_ld, lseT, DdT, ldS, dkv, dkv + kw,
+                                     2 * kw));
+  } else if (mma) {
     BW_RUN("bwd_attention",
            launch_attn_bwd_mma_kv(c, B, n, T, idx, hq, hkv, hd, qb, qw, kvb, 2 * kw, kvb + kw,
                                   2 * kw, o, dO, (float*)bat(ws, L.lse), (float*)bat(ws, L.Dd),
@@ -1169,7 +1224,7 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
       akv.nkv = T;
       akv.qpos = idx;
       BW_RUN("attention", launch_attention_tc(c, B, n, hq, hkv, qb, qw, vt, (int)round8(T), o,
-                                              nullptr, nullptr, &akv));
+                                              nullptr, nullptr, &akv, (float*)bat(ws, L.lse)));
     } else {
       BW_RUN("attention", launch_attention_simt(c, dt, B, n, hq, hkv, hd, qb, qw, kvb, kvb + kw,
                                                 2 * kw, o, idx, T));

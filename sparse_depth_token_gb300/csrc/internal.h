@@ -323,6 +323,25 @@ cudaError_t launch_attn_bwd_dkv_tc(const Ctx& c, int B, int n, int hq, int hkv, 
                                    int ldq, const void* dO, const void* qt, const void* dOt,
                                    int t_ld, const float* lseT, const float* DdT, int ldS,
                                    void* dqkv, int ldg);
+// The general forms (Selected-Q / full-KV): n queries per sequence at ascending
+// positions over nk keys, query i seeing the keys j <= its position. q [B*n, ldq]; the
+// keys' and values' rows kv [B*nk, ldk] (KV head g's k at column k_col0 + g*128, v at
+// v_col0 + g*128); kt [B*hkv*128, kt_ld] over the nk keys. dq_tc_kv: qpos [B*n] (NULL:
+// i, nk == n), dq [B*n, ldg]. dkv_tc_kv: qposS [B, ldS] the positions padded with -1 and
+// qstart [B, ceil(nk / kAttnBwdKvBlock)] the first query positioned at or after each key
+// block's first key (both NULL: the compact case), dk and dv [B*nk, ldgk].
+constexpr int kAttnBwdKvBlock = 128;   // keys per CTA of the tcgen05 dk / dv kernel
+cudaError_t launch_attn_bwd_dq_tc_kv(const Ctx& c, int B, int n, int nk, const int32_t* qpos,
+                                     int hq, int hkv, const void* q, int ldq, const void* kv,
+                                     int ldk, int k_col0, int v_col0, const void* kt, int kt_ld,
+                                     const void* o, const void* dO, const float* lse, float* Dd,
+                                     void* dq, int ldg, float* DdT, int ldS);
+cudaError_t launch_attn_bwd_dkv_tc_kv(const Ctx& c, int B, int n, int nk, const int32_t* qposS,
+                                      const int32_t* qstart, int hq, int hkv, const void* q,
+                                      int ldq, const void* kv, int ldk, int k_col0, int v_col0,
+                                      const void* dO, const void* qt, const void* dOt, int t_ld,
+                                      const float* lseT, const float* DdT, int ldS, void* dk,
+                                      void* dv, int ldgk);
 
 // Workspace bytes of run_layer_bwd for these sizes (covers a dense layer).
 size_t bwd_workspace_bytes(const xmod_dims* dm);
