@@ -367,6 +367,22 @@ XMOD_API int xmod_router_topk_noalloc(const xmod_dims* dims, int K, const void* 
                                       const void* w_r, const float* bias, int32_t* idx,
                                       float* r_sel, int* status_out, void* stream);
 
+/* ---------------------------------------------------------------- failure detection
+ * Not part of the method. Every wait inside the library's tcgen05 kernels (on an
+ * mbarrier, or on a flag another CTA sets) gives up after 2 s without progress: the
+ * waiting thread records XMOD_ERR_TIMEOUT in the status word, the CTA lets its copies in
+ * flight land, frees its tensor memory and returns, so the CUDA context stays usable and
+ * xmod_sync_status reports the error.
+ *
+ * Self-test of that path (no fault, no trap): one CTA waits, through the kernels' own
+ * bounded wait, on an mbarrier phase that nothing completes, for the 2 s limit, then
+ * returns. Afterwards the status word of `ws` (reset it first) holds XMOD_ERR_TIMEOUT,
+ * and the ints at ws + 4 and ws + 8 hold the wait's result (0: it gave up) and the
+ * CTA's abort flag (1: raised).
+ *   ws        device buffer of at least 256 bytes, 16-byte aligned
+ * Returns XMOD_OK once launched, XMOD_ERR_INVALID_ARG for a bad buffer. */
+XMOD_API int xmod_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------- measurement
  * Not part of the method: support for benchmarking the calls above. */
 

@@ -25,7 +25,7 @@ EXPORTS = ("xmod_version", "xmod_status_string", "xmod_workspace_bytes", "xmod_r
            "xmod_profile_enable", "xmod_profile_read", "xmod_router_topk_noalloc",
            "xmod_stack_fwd_ex", "xmod_layer_fwd_threshold", "xmod_stack_fwd_sched",
            "xmod_bwd_workspace_bytes", "xmod_layer_bwd", "xmod_stack_bwd_workspace_bytes",
-           "xmod_stack_bwd")
+           "xmod_stack_bwd", "xmod_selftest_wait_timeout")
 
 # Largest B*T the allocation-free router entry point accepts (its fixed scratch).
 NOALLOC_MAX_TOKENS = 2 * 1024 * 1024
@@ -128,6 +128,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                     ctypes.POINTER(ctypes.c_int)]
     L.xmod_router_topk_noalloc.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _VP, _VP, _VP, _VP,
                                            _VP, _VP, _VP]
+    L.xmod_selftest_wait_timeout.argtypes = [_VP, ctypes.c_size_t, _VP]
     L.xmod_bwd_workspace_bytes.restype = ctypes.c_size_t
     L.xmod_bwd_workspace_bytes.argtypes = [ctypes.POINTER(Dims), ctypes.c_int]
     L.xmod_layer_bwd.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -340,3 +341,11 @@ def stack_bwd(dm, K, A, N0, N1, gate, layers, x, bias, dy, route_coef, dx, grads
         ctypes.byref(dm), int(K), float(A), int(N0), int(N1), int(gate), arr, len(layers), _p(x),
         _p(bias), _p(dy), float(route_coef), _p(dx), garr, _p(checkpoints), _p(ws), _wsb(ws),
         _stream(stream)))
+
+
+def selftest_wait_timeout(ws, stream=None):
+    """xmod_selftest_wait_timeout: one CTA runs the kernels' bounded wait on a barrier
+    that nothing completes until it gives up (about 2 s); the status word of ws then holds
+    ERR_TIMEOUT."""
+    _check("xmod_selftest_wait_timeout",
+           load().xmod_selftest_wait_timeout(_p(ws), _wsb(ws), _stream(stream)))
