@@ -153,6 +153,24 @@ TENSOR_KINDS = {"gemm_qkv", "attention", "gemm_o_residual", "gemm_gate_up_swiglu
                 "gemm_down_scatter"}
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a bench
+# line's dominant kernel, from one ncu capture of that kernel in that configuration, with
+# the summary that records it; used only while the kernel is unchanged and the run is
+# the captured configuration. Key: (workload, B, variant / routing tag, kernel kind).
+RECORDED_TRAFFIC = {
+    # the 33 gate/up launches of one A4K8 step (32 sparse layers + the dense one), mean
+    ("a4k8_bf16", 8, "xmod", "gemm_gate_up_swiglu"):
+        (53.42e6, "profiles/gemm_gate_up_dram_a4k8.md"),
+    # the router's x read + logits write at B = 8, scaled by 8 to B = 64 (x is read once)
+    ("routing_bf16", 64, "routing", "router"):
+        (8 * 540.3e6, "profiles/routing_kernels_c2_microbench.md"),
+}
+
+
+def recorded_traffic(w: I.Workload, tag: str, kernel: str):
+    return RECORDED_TRAFFIC.get((w.name, w.B, tag, kernel), (None, None))
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -453,11 +471,15 @@ def run_xmod(args):
         if top in TENSOR_KINDS:
             ach = work[top] / (kms / prof_steps / 1e3) / 1e12
             peak = peaks["bf16_tflops_sustained"]
+            tag = "xmod" if (VARIANT == "xmod" and plain and not args.qwen3) else "other"
+            traffic, tsrc = recorded_traffic(w, tag, top)
             roofline = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": peak,
-                        "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                        "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
                         "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside "
                                        f"a long step)",
                         "algorithmic_per_launch": work[top] / (cnt / prof_steps)}
+            if tsrc:
+                roofline["traffic_source"] = tsrc
         else:
             ach = work[top] / (kms / prof_steps / 1e3) / 1e9
             peak = peaks["hbm_gbs"]
@@ -973,10 +995,13 @@ def run_routing(args):
         top = max(prof.items(), key=lambda kv: kv[1][1])[0]
         cnt, kms = prof[top]
         ach = work[top] / (kms / prof_steps / 1e3) / 1e9
+        traffic, tsrc = recorded_traffic(w, "routing", top)
         roofline = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                    "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": traffic,
                     "peak_source": f"{peaks['source']} HBM copy",
                     "algorithmic_per_launch": work[top] / (cnt / prof_steps)}
+        if tsrc:
+            roofline["traffic_source"] = tsrc
         total = sum(work.values())
         results[K] = {"value": world * M / (ms / 1e3), "ms_per_step": ms,
                       "pipeline_gbs": total / (ms / 1e3) / 1e9,
