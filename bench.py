@@ -636,10 +636,35 @@ def backward_work(w: I.Workload) -> dict:
 
     qw, kw = w.hq * w.hd, w.hkv * w.hd
     BT = w.B * w.T
+    es = 2 if w.dtype == "bf16" else 4
+
+    def r8(v):
+        return (v + 7) // 8 * 8
+
+    def tr(R, Rpad, C, e=es):   # one transpose: R x C read, C x Rpad written (zero padding)
+        return e * (R * C + C * Rpad)
+
     for kind in schedule(w):
         n = w.T // w.K if routed(kind) else w.T
         M = w.B * n
+        Mp = r8(M)
         proj = 0
+        # the transposes that feed the gradient GEMMs token-contiguous operands (bytes)
+        tb = 0
+        if kind != ATTN:   # df, H, W_down, [dG | dU], v2, W_gate, W_up
+            tb += tr(M, Mp, w.d) + tr(M, Mp, w.F) + tr(w.d, w.d, w.F) + tr(M, Mp, 2 * w.F)
+            tb += tr(M, Mp, w.d) + 2 * tr(w.F, w.F, w.d)
+        if kind != RFFN:   # da, o, W_o; the attention backward's per-sequence transposes
+            tb += tr(M, Mp, w.d) + tr(M, Mp, qw) + tr(w.d, w.d, qw)
+            nk = w.T if kind == FULLKV else n
+            tb += w.B * (tr(nk, nk, kw) + 2 * tr(n, n, qw) + tr(n, n, w.hq, 4))
+            if kind == FULLKV:   # dq, u_sel, W_q; [dk | dv], u of every token, W_k, W_v
+                tb += tr(M, Mp, qw) + tr(M, Mp, w.d) + tr(qw, qw, w.d)
+                tb += tr(BT, r8(BT), 2 * kw) + tr(BT, r8(BT), w.d) + 2 * tr(kw, kw, w.d)
+            else:                # [dq | dk | dv], u, W_q, W_k, W_v
+                tb += tr(M, Mp, qw + 2 * kw) + tr(M, Mp, w.d) + tr(qw, qw, w.d)
+                tb += 2 * tr(kw, kw, w.d)
+        add("bwd_transpose", tb)
         if kind != RFFN:   # the attention half
             if kind == FULLKV:   # k, v of every token; a query at position p sees p + 1 keys
                 qkv = 2 * BT * w.d * 2 * kw + 2 * M * w.d * qw
@@ -763,18 +788,29 @@ def run_backward(args):
         e = {"launches_per_step": cnt // prof_steps, "ms_per_step": pms,
              "share": kms / total_ms if total_ms else None}
         if kind in work and pms > 0:
-            e["tflops"] = work[kind] / (pms / 1e3) / 1e12
+            if kind in BWD_TENSOR_KINDS:
+                e["tflops"] = work[kind] / (pms / 1e3) / 1e12
+            else:
+                e["gbs"] = work[kind] / (pms / 1e3) / 1e9
         kernels[kind] = e
     top = max(prof.items(), key=lambda kv: kv[1][1])[0]
     roofline = None
     if top in work:
         cnt, kms = prof[top]
-        ach = work[top] / (kms / prof_steps / 1e3) / 1e12
-        peak = peaks["bf16_tflops_sustained"]
-        roofline = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": peak,
-                    "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
-                    "peak_source": f"{peaks['source']} bf16 sustained",
-                    "algorithmic_per_launch": work[top] / (cnt / prof_steps)}
+        if top in BWD_TENSOR_KINDS:
+            ach = work[top] / (kms / prof_steps / 1e3) / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            roofline = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": peak,
+                        "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                        "peak_source": f"{peaks['source']} bf16 sustained",
+                        "algorithmic_per_launch": work[top] / (cnt / prof_steps)}
+        else:   # data movement (the transposes): compulsory bytes over the HBM copy rate
+            ach = work[top] / (kms / prof_steps / 1e3) / 1e9
+            peak = peaks["hbm_gbs"]
+            roofline = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": peak,
+                        "unit": "GB/s", "frac": ach / peak, "traffic": None,
+                        "peak_source": f"{peaks['source']} HBM copy",
+                        "algorithmic_per_launch": work[top] / (cnt / prof_steps)}
     cfg = workload_config(w)
     cfg["pass"] = "backward of every layer (xmod_layer_bwd, forward recomputed inside), " \
                   "Eq. 9 coefficient 1e-4, synthetic upstream gradient dy~N(0,1)"
@@ -785,7 +821,8 @@ def run_backward(args):
         "data": "synthetic (seeded; random-init weights)", "config": cfg,
         "roofline": roofline, "gpu_launches": int(launches) * args.steps,
         "gpu_launches_per_step": int(launches), "clocks": clock_info,
-        "step_tflops": sum(work.values()) / (ms / 1e3) / 1e12, "kernels": kernels}), flush=True)
+        "step_tflops": sum(v for k, v in work.items() if k in BWD_TENSOR_KINDS) / (ms / 1e3) / 1e12,
+        "kernels": kernels}), flush=True)
 
 
 # ---------------------------------------------------------------------- routing microbench

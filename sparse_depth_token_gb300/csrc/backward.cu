@@ -905,6 +905,44 @@ cudaError_t bw_gemm(const Ctx& c, xmod_dtype dt, int M, int N, int K, const void
   return launch_gemm_simt(c, dt, M, N, K, A, lda, Bm, ldb, nullptr, e);
 }
 
+// The fp32 weight gradients of weights stacked along M in one GEMM: C = A B^T with rows
+// [0, s0) to o0, [s0, s1) to o1 and [s1, M) to o2 (s1 = 0: rows [s0, M) to o1), each
+// [rows, N] with row stride ldo. tcgen05 when the shape allows (one launch), else one
+// GEMM per part.
+cudaError_t bw_gemm_dw_split(const Ctx& c, xmod_dtype dt, int M, int N, int K, const void* A,
+                             int lda, const void* Bm, int ldb, float* o0, float* o1, float* o2,
+                             int s0, int s1, int ldo) {
+  if (dt == XMOD_BF16) {
+    Epilogue e;
+    e.kind = EPI_STORE;
+    e.out = o0;
+    e.ldo = ldo;
+    e.out_f32 = true;
+    e.row_split[0] = s0;
+    e.out_rows[0] = o1;
+    if (s1 > 0) {
+      e.row_split[1] = s1;
+      e.out_rows[1] = o2;
+    }
+    GemmTcProblem p;
+    p.M = M; p.N = N; p.K = K; p.A = A; p.lda = lda; p.B[0] = Bm; p.ldb = ldb;
+    if (gemm_tc_supported(p, e)) return launch_gemm_tc(c, p, e);
+  }
+  const size_t es = dt == XMOD_BF16 ? 2 : 4;
+  const int parts = s1 > 0 ? 3 : 2;
+  const int ends[3] = {s0, s1 > 0 ? s1 : M, M};
+  float* outs[3] = {o0, o1, o2};
+  int r0 = 0;
+  for (int i = 0; i < parts; ++i) {
+    if (i > 0) count_launch();   // the caller counts one launch
+    const cudaError_t err = bw_gemm(c, dt, ends[i] - r0, N, K, (const char*)A + es * (size_t)r0 * lda,
+                                    lda, Bm, ldb, outs[i], ldo, true);
+    if (err != cudaSuccess) return err;
+    r0 = ends[i];
+  }
+  return cudaSuccess;
+}
+
 // Column sums out[c] = sum_m (A ? A[m, c] : 1) * Bv[row(m), c] * (w ? w[m] : 1).
 template <typename TB>
 int bw_coldot(const Ctx& c, int64_t M, int d, const float* A, const TB* Bv, const int32_t* idx,
@@ -1087,9 +1125,8 @@ int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weigh
   // ======== k, v = u [Wk | Wv]^T on every token
   BW_RUN("bwd_transpose", transpose(c, dt, BT, BTp, 2 * kw, dkv, 2 * kw, tA, BTp));  // [2kw, BTp]
   BW_RUN("bwd_transpose", transpose(c, dt, BT, BTp, d, u, d, tB, BTp));              // [d, BTp]
-  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, kw, d, BTp, tA, BTp, tB, BTp, gr->wk, d, true));
-  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, kw, d, BTp, tA + (size_t)kw * BTp, BTp, tB, BTp, gr->wv,
-                                d, true));
+  BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, 2 * kw, d, BTp, tA, BTp, tB, BTp, gr->wk, gr->wv,
+                                         nullptr, kw, 0, d));
   BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wk, d, tW, 2 * kw));   // [d, 2kw]
   BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wv, d, tW + kw, 2 * kw));
   float* du = (float*)bat(ws, L.du);
@@ -1393,9 +1430,8 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   }
   BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, 2 * F, dGU, 2 * F, tA, Mp));  // [2F, Mp]
   BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, v2, d, tB, Mp));           // v2^T [d, Mp]
-  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, F, d, Mp, tA, Mp, tB, Mp, gr->w_gate, d, true));
-  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, F, d, Mp, tA + (size_t)F * Mp, Mp, tB, Mp, gr->w_up, d,
-                                true));
+  BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, 2 * F, d, Mp, tA, Mp, tB, Mp, gr->w_gate,
+                                         gr->w_up, nullptr, F, 0, d));
   BW_RUN("bwd_transpose", transpose(c, dt, F, F, d, w->w_gate, d, tW, 2 * F));  // [d, 2F]
   BW_RUN("bwd_transpose", transpose(c, dt, F, F, d, w->w_up, d, tW + F, 2 * F));
   float* dv2 = (float*)bat(ws, L.dv2);
@@ -1514,11 +1550,8 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   // ======== q, k, v = u [Wq | Wk | Wv]^T
   BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, qkv_w, dqkv, qkv_w, tA, Mp));  // [qkv_w, Mp]
   BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, u, d, tB, Mp));              // u^T [d, Mp]
-  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, qw, d, Mp, tA, Mp, tB, Mp, gr->wq, d, true));
-  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, kw, d, Mp, tA + (size_t)qw * Mp, Mp, tB, Mp, gr->wk, d,
-                                true));
-  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, kw, d, Mp, tA + (size_t)(qw + kw) * Mp, Mp, tB, Mp, gr->wv,
-                                d, true));
+  BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, qkv_w, d, Mp, tA, Mp, tB, Mp, gr->wq, gr->wk,
+                                         gr->wv, qw, qw + kw, d));
   BW_RUN("bwd_transpose", transpose(c, dt, qw, qw, d, w->wq, d, tW, qkv_w));      // [d, qkv_w]
   BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wk, d, tW + qw, qkv_w));
   BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wv, d, tW + qw + kw, qkv_w));

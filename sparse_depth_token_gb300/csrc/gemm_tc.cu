@@ -443,7 +443,16 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, in
 #pragma unroll
     for (int g = 0; g < 8; ++g)
       fv[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-    st_seg_f32((float*)e.out + (int64_t)m * e.ldo + col0, fv, rem, a.v8);
+    float* base = (float*)e.out;
+    int row = m;
+    if (e.row_split[1] > 0 && m >= e.row_split[1]) {
+      base = (float*)e.out_rows[1];
+      row = m - e.row_split[1];
+    } else if (e.row_split[0] > 0 && m >= e.row_split[0]) {
+      base = (float*)e.out_rows[0];
+      row = m - e.row_split[0];
+    }
+    st_seg_f32(base + (int64_t)row * e.ldo + col0, fv, rem, a.v8);
   } else if (MODE == EPI_STORE || MODE == EPI_SWIGLU) {
     store32_bf16((__nv_bfloat16*)e.out + (int64_t)m * e.ldo + col0, v, rem, a.v8);
   } else if (MODE == EPI_OPROJ) {
@@ -1007,6 +1016,8 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
   bool v8 = true;
   if (e.out && e.kind != EPI_ROUTER)
     v8 = v8 && seg_ok(e.out, (int64_t)e.ldo * (e.out_f32 ? 4 : 2));
+  for (int i = 0; i < 2; ++i)
+    if (e.row_split[i] > 0) v8 = v8 && seg_ok(e.out_rows[i], (int64_t)e.ldo * 4);
   if (e.out2) v8 = v8 && seg_ok(e.out2, (int64_t)e.ldo2 * 4);
   if (e.x) v8 = v8 && seg_ok(e.x, (int64_t)e.d * 2);
   if (e.a) v8 = v8 && seg_ok(e.a, (int64_t)e.d * 2);

@@ -222,6 +222,11 @@ struct Epilogue {
   // STORE: write the fp32 accumulator itself (out is float [M, ldo]) instead of
   // rounding it to the layer's element type
   bool out_f32 = false;
+  // STORE with out_f32: rows from row_split[0] (when > 0) go to out_rows[0] and rows from
+  // row_split[1] (when > 0) to out_rows[1], renumbered from 0 there (same ldo): one
+  // GEMM writes the gradients of weights stacked along M, e.g. [W_q; W_k; W_v]
+  int row_split[2] = {0, 0};
+  void* out_rows[2] = {nullptr, nullptr};
 };
 
 // C[M, N] = A[M, K] . B[N, K]^T (fp32 accumulate), then the epilogue. For
