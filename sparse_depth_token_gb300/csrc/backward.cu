@@ -21,6 +21,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <initializer_list>
 #include <type_traits>
 
 #include "common.cuh"
@@ -69,19 +70,12 @@ __device__ __forceinline__ float softplus_f(float z) {
 // rows fall in distinct chunks, so neither phase has bank conflicts.
 constexpr int TR_T = 64;
 
-// grid.z runs over a batch of such matrices, in_bs / out_bs elements apart.
+// One 64 x 64 tile at (r0, c0) of out = in^T, through the shared tile `tile`.
 template <typename U>
-__global__ void __launch_bounds__(256)
-transpose_kernel(int R, int Rpad, int C, const U* __restrict__ in, int64_t ldi,
-                 U* __restrict__ out, int64_t ldo, int64_t in_bs, int64_t out_bs, int vec_in,
-                 int vec_out) {
-  pdl_trigger();
-  pdl_wait();
+__device__ __forceinline__ void transpose_tile(int R, int Rpad, int C, const U* __restrict__ in,
+                                               int64_t ldi, U* __restrict__ out, int64_t ldo,
+                                               int r0, int c0, int vec_in, int vec_out, U* tile) {
   constexpr int V = 16 / sizeof(U), CH = TR_T / V;
-  in += blockIdx.z * in_bs;
-  out += blockIdx.z * out_bs;
-  __shared__ __align__(16) U tile[TR_T * TR_T];
-  const int r0 = blockIdx.y * TR_T, c0 = blockIdx.x * TR_T;
   for (int e = threadIdx.x; e < TR_T * CH; e += 256) {
     const int r = e / CH, ch = e - r * CH, gr = r0 + r, gc = c0 + ch * V;
     U* dst = tile + r * TR_T + ((ch ^ ((r / V) & (CH - 1))) * V);
@@ -113,6 +107,50 @@ transpose_kernel(int R, int Rpad, int C, const U* __restrict__ in, int64_t ldi,
         if (gr + k < Rpad) dst[k] = v.w[k];
     }
   }
+}
+
+// grid.z runs over a batch of such matrices, in_bs / out_bs elements apart.
+template <typename U>
+__global__ void __launch_bounds__(256)
+transpose_kernel(int R, int Rpad, int C, const U* __restrict__ in, int64_t ldi,
+                 U* __restrict__ out, int64_t ldo, int64_t in_bs, int64_t out_bs, int vec_in,
+                 int vec_out) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ __align__(16) U tile[TR_T * TR_T];
+  transpose_tile<U>(R, Rpad, C, in + blockIdx.z * in_bs, ldi, out + blockIdx.z * out_bs, ldo,
+                    blockIdx.y * TR_T, blockIdx.x * TR_T, vec_in, vec_out, tile);
+}
+
+// Several independent transposes in one launch: job k owns the tiles [start, start +
+// tiles_x * tiles_y) of grid.x (tile (bx, by) of its own matrix); grid.y runs over a
+// batch common to the jobs (in_bs / out_bs elements apart per job).
+struct TrJob {
+  const void* in;
+  void* out;
+  int64_t ldi, ldo, in_bs, out_bs;
+  int R, Rpad, C, tiles_x, start, vec_in, vec_out;
+};
+constexpr int kTrMaxJobs = 8;
+struct TrJobs {
+  TrJob j[kTrMaxJobs];
+  int n;
+};
+
+template <typename U>
+__global__ void __launch_bounds__(256)
+transpose_multi_kernel(const __grid_constant__ TrJobs jobs) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ __align__(16) U tile[TR_T * TR_T];
+  int k = 0;
+  while (k + 1 < jobs.n && (int)blockIdx.x >= jobs.j[k + 1].start) ++k;
+  const TrJob& J = jobs.j[k];
+  const int t = (int)blockIdx.x - J.start;
+  const int by = t / J.tiles_x, bx = t - by * J.tiles_x;
+  transpose_tile<U>(J.R, J.Rpad, J.C, (const U*)J.in + blockIdx.y * J.in_bs, J.ldi,
+                    (U*)J.out + blockIdx.y * J.out_bs, J.ldo, by * TR_T, bx * TR_T, J.vec_in,
+                    J.vec_out, tile);
 }
 
 // ---------------------------------------------------------------- gated residual backward
@@ -834,7 +872,7 @@ BwLayout bw_layout(const xmod_dims* dm) {
   L.rstd2 = take(4 * M);
   L.tA = take(es * Mp * std::max(std::max(d, 2 * F), qkv_w));
   L.tB = take(es * Mp * std::max(std::max(d, F), qw));
-  L.tW = take(es * d * std::max(2 * F, qkv_w));
+  L.tW = take(es * d * (3 * F + qw + qkv_w));   // every transposed weight of a layer
   L.part = take(4 * (size_t)kMaxChunks * std::max(d, (size_t)1));
   L.qkpre = take(es * M * (qw + kw));   // q | k before the QK-norm / rotation
   L.dgq = take(4 * M * hd);
@@ -878,14 +916,69 @@ cudaError_t transpose_t(const Ctx& c, int R, int Rpad, int C, const void* in, in
                     (const U*)in, ldi, (U*)out, ldo, in_bs, out_bs, vec_in, vec_out);
 }
 
-// out[c, r] = in[r, c] (zero for R <= r < Rpad); with batch > 1, `batch` such matrices,
-// in_bs / out_bs elements apart.
-cudaError_t transpose(const Ctx& c, xmod_dtype dt, int R, int Rpad, int C, const void* in,
-                      int64_t ldi, void* out, int64_t ldo, int batch = 1, int64_t in_bs = 0,
-                      int64_t out_bs = 0) {
-  return dt == XMOD_BF16
-             ? transpose_t<__nv_bfloat16>(c, R, Rpad, C, in, ldi, out, ldo, batch, in_bs, out_bs)
-             : transpose_t<float>(c, R, Rpad, C, in, ldi, out, ldo, batch, in_bs, out_bs);
+// One transpose of a multi-transpose launch: out[c, r] = in[r, c] (zero for R <= r < Rpad),
+// per batch entry in_bs / out_bs elements further.
+struct TrSpec {
+  const void* in;
+  int64_t ldi;
+  void* out;
+  int64_t ldo;
+  int R, Rpad, C;
+  int64_t in_bs, out_bs;
+};
+
+// Up to kTrMaxJobs independent transposes of T-typed matrices in one launch.
+template <typename T>
+cudaError_t transpose_multi_t(const Ctx& c, const TrSpec* specs, int nspecs, int batch) {
+  using U = typename std::conditional<sizeof(T) == 2, uint16_t, uint32_t>::type;
+  constexpr int V = 16 / sizeof(U);
+  if (nspecs > kTrMaxJobs || batch <= 0) return cudaErrorInvalidValue;
+  TrJobs jobs{};
+  int total = 0;
+  for (int i = 0; i < nspecs; ++i) {
+    const TrSpec& s = specs[i];
+    if (s.R <= 0 || s.C <= 0) continue;
+    TrJob& J = jobs.j[jobs.n++];
+    J.in = s.in;
+    J.out = s.out;
+    J.ldi = s.ldi;
+    J.ldo = s.ldo;
+    J.in_bs = s.in_bs;
+    J.out_bs = s.out_bs;
+    J.R = s.R;
+    J.Rpad = s.Rpad;
+    J.C = s.C;
+    J.tiles_x = (s.C + TR_T - 1) / TR_T;
+    J.start = total;
+    J.vec_in = ((uintptr_t)s.in % 16 == 0 && s.ldi % V == 0 && s.in_bs % V == 0) ? 1 : 0;
+    J.vec_out = ((uintptr_t)s.out % 16 == 0 && s.ldo % V == 0 && s.out_bs % V == 0) ? 1 : 0;
+    total += J.tiles_x * ((s.Rpad + TR_T - 1) / TR_T);
+  }
+  if (jobs.n == 0) return cudaSuccess;
+  return launch_pdl(transpose_multi_kernel<U>, dim3(total, batch), dim3(256), 0, c.stream, jobs);
+}
+
+cudaError_t transpose_multi(const Ctx& c, xmod_dtype dt, const TrSpec* specs, int nspecs,
+                            int batch = 1) {
+  return dt == XMOD_BF16 ? transpose_multi_t<__nv_bfloat16>(c, specs, nspecs, batch)
+                         : transpose_multi_t<float>(c, specs, nspecs, batch);
+}
+cudaError_t transpose_multi(const Ctx& c, xmod_dtype dt, std::initializer_list<TrSpec> specs,
+                            int batch = 1) {
+  return transpose_multi(c, dt, specs.begin(), (int)specs.size(), batch);
+}
+
+// The transposed weights of a layer's backward, each in its own part of the tW scratch:
+// W_down^T [F, d]; [W_gate | W_up]^T [d, 2F]; W_o^T [qw, d]; [W_q | W_k | W_v]^T
+// [d, qkv_w] (Selected-Q / full-KV: W_q^T [d, qw], then [W_k | W_v]^T [d, 2 kw]).
+template <typename E>
+struct TwParts {
+  E *d, *gu, *o, *qkv;
+};
+template <typename E>
+TwParts<E> tw_parts(const xmod_dims* dm, E* tW) {
+  const size_t d = dm->d, F = dm->d_ff, qw = (size_t)dm->n_heads * dm->head_dim;
+  return {tW, tW + F * d, tW + 3 * F * d, tW + (3 * F + qw) * d};
 }
 
 // C[M, N] = A[M, K] B[N, K]^T, both K-contiguous, stored plain (fp32 if f32out, else
@@ -1018,7 +1111,7 @@ int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weigh
   E* dqb = dqkv + (size_t)BT * 2 * kw;         // [M, qw]: dq of the selected tokens
   E* tA = (E*)bat(ws, L.tA);
   E* tB = (E*)bat(ws, L.tB);
-  E* tW = (E*)bat(ws, L.tW);
+  const TwParts<E> tw = tw_parts<E>(dm, (E*)bat(ws, L.tW));   // transposed by the caller
   float* part = (float*)bat(ws, L.part);
 
   // ======== attention: n queries per sequence over its T keys
@@ -1039,12 +1132,14 @@ int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weigh
     int32_t* qstart = (int32_t*)bat(ws, L.qstart);
     const int nkb = (T + kAttnBwdKvBlock - 1) / kAttnBwdKvBlock;
     // per sequence, transposed: keys [hkv * hd, T], queries and dO [hq * hd, n], lse [hq, n]
-    BW_RUN("bwd_transpose", transpose(c, dt, T, T, kw, kvb, 2 * kw, kt, kt_ld, B,
-                                      (int64_t)T * 2 * kw, (int64_t)kw * kt_ld));
-    BW_RUN("bwd_transpose", transpose(c, dt, n, n, qw, qb, qw, qt, qt_ld, B, (int64_t)n * qw,
-                                      (int64_t)qw * qt_ld));
-    BW_RUN("bwd_transpose", transpose(c, dt, n, n, qw, dO, qw, dOt, qt_ld, B, (int64_t)n * qw,
-                                      (int64_t)qw * qt_ld));
+    BW_RUN("bwd_transpose",
+           transpose_multi(c, dt, {{kvb, 2 * kw, kt, kt_ld, T, T, kw, (int64_t)T * 2 * kw,
+                                    (int64_t)kw * kt_ld},
+                                   {qb, qw, qt, qt_ld, n, n, qw, (int64_t)n * qw,
+                                    (int64_t)qw * qt_ld},
+                                   {dO, qw, dOt, qt_ld, n, n, qw, (int64_t)n * qw,
+                                    (int64_t)qw * qt_ld}},
+                           B));
     BW_RUN("bwd_transpose", transpose_t<float>(c, n, n, hq, bat(ws, L.lse), hq, lseT, ldS, B,
                                                (int64_t)n * hq, (int64_t)hq * ldS));
     BW_RUN("bwd_rows", launch_pdl(fullkv_qindex_kernel, dim3(B), dim3(256), 0, c.stream, n, ldS,
@@ -1116,21 +1211,21 @@ int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weigh
   E* usel = (E*)bat(ws, L.v2);
   BW_RUN("gather_rmsnorm",
          launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1, dm->rms_eps, usel));
-  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, qw, dqb, qw, tA, Mp));     // dq^T [qw, Mp]
-  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, usel, d, tB, Mp));      // u_sel^T [d, Mp]
+  // dq^T [qw, Mp], u_sel^T [d, Mp]
+  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{dqb, qw, tA, Mp, M, Mp, qw, 0, 0},
+                                                  {usel, d, tB, Mp, M, Mp, d, 0, 0}}));
   BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, qw, d, Mp, tA, Mp, tB, Mp, gr->wq, d, true));
-  BW_RUN("bwd_transpose", transpose(c, dt, qw, qw, d, w->wq, d, tW, qw));   // Wq^T [d, qw]
   float* du_sel = (float*)bat(ws, L.dv2);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qw, dqb, qw, tW, qw, du_sel, d, true));
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qw, dqb, qw, tw.qkv, qw, du_sel, d, true));
   // ======== k, v = u [Wk | Wv]^T on every token
-  BW_RUN("bwd_transpose", transpose(c, dt, BT, BTp, 2 * kw, dkv, 2 * kw, tA, BTp));  // [2kw, BTp]
-  BW_RUN("bwd_transpose", transpose(c, dt, BT, BTp, d, u, d, tB, BTp));              // [d, BTp]
+  // [dk | dv]^T [2kw, BTp], u^T [d, BTp]
+  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{dkv, 2 * kw, tA, BTp, BT, BTp, 2 * kw, 0, 0},
+                                                  {u, d, tB, BTp, BT, BTp, d, 0, 0}}));
   BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, 2 * kw, d, BTp, tA, BTp, tB, BTp, gr->wk, gr->wv,
                                          nullptr, kw, 0, d));
-  BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wk, d, tW, 2 * kw));   // [d, 2kw]
-  BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wv, d, tW + kw, 2 * kw));
   float* du = (float*)bat(ws, L.du);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, BT, d, 2 * kw, dkv, 2 * kw, tW, 2 * kw, du, d, true));
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, BT, d, 2 * kw, dkv, 2 * kw, tw.qkv + (size_t)d * qw,
+                                2 * kw, du, d, true));
   // ======== u = RMSNorm(x) g1 on every token; the selected rows add their query's part
   // and the gradient through h
   float* dadd = (float*)bat(ws, L.h);
@@ -1413,14 +1508,39 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   float* dh = nullptr;   // the gradient reaching h = x_sel + a through the FFN half
   const E* da = dae;     // the gradient reaching a (FullAttn: dy itself)
 
+  // ======== every weight the activation gradients multiply by, transposed in one launch
+  const TwParts<E> tw = tw_parts<E>(dm, tW);
+  {
+    TrSpec sp[7];
+    int ns = 0;
+    if (ffn) {
+      sp[ns++] = {w->w_down, F, tw.d, d, d, d, F, 0, 0};          // [F, d]
+      sp[ns++] = {w->w_gate, d, tw.gu, 2 * F, F, F, d, 0, 0};     // [d, 2F]
+      sp[ns++] = {w->w_up, d, tw.gu + F, 2 * F, F, F, d, 0, 0};
+    }
+    if (attn) {
+      sp[ns++] = {w->wo, qw, tw.o, d, d, d, qw, 0, 0};            // [qw, d]
+      if (fullkv) {   // [d, qw] and [d, 2kw]
+        sp[ns++] = {w->wq, d, tw.qkv, qw, qw, qw, d, 0, 0};
+        sp[ns++] = {w->wk, d, tw.qkv + (size_t)d * qw, 2 * kw, kw, kw, d, 0, 0};
+        sp[ns++] = {w->wv, d, tw.qkv + (size_t)d * qw + kw, 2 * kw, kw, kw, d, 0, 0};
+      } else {        // [d, qkv_w]
+        sp[ns++] = {w->wq, d, tw.qkv, qkv_w, qw, qw, d, 0, 0};
+        sp[ns++] = {w->wk, d, tw.qkv + qw, qkv_w, kw, kw, d, 0, 0};
+        sp[ns++] = {w->wv, d, tw.qkv + qw + kw, qkv_w, kw, kw, d, 0, 0};
+      }
+    }
+    BW_RUN("bwd_transpose", transpose_multi(c, dt, sp, ns));
+  }
+
   if (ffn) {
   // ======== FFN: f = H Wd^T, H = silu(G) U, [G | U] = v2 [Wg | Wu]^T
-  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, df, d, tA, Mp));      // df^T [d, Mp]
-  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, F, H, F, tB, Mp));       // H^T [F, Mp]
+  // df^T [d, Mp], H^T [F, Mp]
+  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{df, d, tA, Mp, M, Mp, d, 0, 0},
+                                                  {H, F, tB, Mp, M, Mp, F, 0, 0}}));
   BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, d, F, Mp, tA, Mp, tB, Mp, gr->w_down, F, true));
-  BW_RUN("bwd_transpose", transpose(c, dt, d, d, F, w->w_down, F, tW, d));  // Wd^T [F, d]
   float* dH = (float*)bat(ws, L.dH);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, F, d, df, d, tW, d, dH, F, true));
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, F, d, df, d, tw.d, d, dH, F, true));
   E* dGU = (E*)bat(ws, L.dGU);
   {
     const int64_t tot = (int64_t)M * F / (16 / sizeof(E));
@@ -1428,14 +1548,13 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     BW_RUN("swiglu", launch_pdl(swiglu_bwd_kernel<E>, dim3(blk), dim3(256), 0, c.stream,
                                 (int64_t)M, F, (const E*)gu, (const float*)dH, dGU));
   }
-  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, 2 * F, dGU, 2 * F, tA, Mp));  // [2F, Mp]
-  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, v2, d, tB, Mp));           // v2^T [d, Mp]
+  // [dG | dU]^T [2F, Mp], v2^T [d, Mp]
+  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{dGU, 2 * F, tA, Mp, M, Mp, 2 * F, 0, 0},
+                                                  {v2, d, tB, Mp, M, Mp, d, 0, 0}}));
   BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, 2 * F, d, Mp, tA, Mp, tB, Mp, gr->w_gate,
                                          gr->w_up, nullptr, F, 0, d));
-  BW_RUN("bwd_transpose", transpose(c, dt, F, F, d, w->w_gate, d, tW, 2 * F));  // [d, 2F]
-  BW_RUN("bwd_transpose", transpose(c, dt, F, F, d, w->w_up, d, tW + F, 2 * F));
   float* dv2 = (float*)bat(ws, L.dv2);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, 2 * F, dGU, 2 * F, tW, 2 * F, dv2, d, true));
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, 2 * F, dGU, 2 * F, tw.gu, 2 * F, dv2, d, true));
   float* rstd2 = (float*)bat(ws, L.rstd2);
   if (attn) {
     // v2 = RMSNorm(h) g2; h = x_sel + a: dh reaches x_sel and (with dae) a
@@ -1460,13 +1579,13 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   }
 
   // ======== a = o Wo^T
-  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, da, d, tA, Mp));     // da^T [d, Mp]
-  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, qw, o, qw, tB, Mp));    // o^T [qw, Mp]
+  // da^T [d, Mp], o^T [qw, Mp]
+  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{da, d, tA, Mp, M, Mp, d, 0, 0},
+                                                  {o, qw, tB, Mp, M, Mp, qw, 0, 0}}));
   BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, d, qw, Mp, tA, Mp, tB, Mp, gr->wo, qw, true));
-  BW_RUN("bwd_transpose", transpose(c, dt, d, d, qw, w->wo, qw, tW, d));  // Wo^T [qw, d]
   float* dO = (float*)bat(ws, L.dO);
   const bool mma_attn = tc && attn_bwd_mma_supported(hd, fullkv ? qw : qkv_w, qw);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, qw, d, da, d, tW, d, dO, qw, !mma_attn));
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, qw, d, da, d, tw.o, d, dO, qw, !mma_attn));
 
   // ======== attention
   E* dqkv = (E*)bat(ws, L.dqkv);
@@ -1484,12 +1603,14 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     const int ldS = (n + 63) / 64 * 64;
     // per sequence, transposed: keys [hkv * hd, keys], queries and dO [hq * hd, queries],
     // and the rows' lse per head [hq, queries]
-    BW_RUN("bwd_transpose", transpose(c, dt, n, n, kw, qkv + qw, qkv_w, kt, kt_ld, B,
-                                      (int64_t)n * qkv_w, (int64_t)kw * kt_ld));
-    BW_RUN("bwd_transpose", transpose(c, dt, n, n, qw, qkv, qkv_w, qt, kt_ld, B,
-                                      (int64_t)n * qkv_w, (int64_t)qw * kt_ld));
-    BW_RUN("bwd_transpose", transpose(c, dt, n, n, qw, dO, qw, dOt, kt_ld, B, (int64_t)n * qw,
-                                      (int64_t)qw * kt_ld));
+    BW_RUN("bwd_transpose",
+           transpose_multi(c, dt, {{qkv + qw, qkv_w, kt, kt_ld, n, n, kw, (int64_t)n * qkv_w,
+                                    (int64_t)kw * kt_ld},
+                                   {qkv, qkv_w, qt, kt_ld, n, n, qw, (int64_t)n * qkv_w,
+                                    (int64_t)qw * kt_ld},
+                                   {dO, qw, dOt, kt_ld, n, n, qw, (int64_t)n * qw,
+                                    (int64_t)qw * kt_ld}},
+                           B));
     BW_RUN("bwd_transpose", transpose_t<float>(c, n, n, hq, bat(ws, L.lse), hq, lseT, ldS, B,
                                                (int64_t)n * hq, (int64_t)hq * ldS));
     BW_RUN("bwd_attention", launch_attn_bwd_dq_tc(c, B, n, hq, hkv, qkv, qkv_w, kt, kt_ld, o, dO,
@@ -1548,15 +1669,13 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   }
 
   // ======== q, k, v = u [Wq | Wk | Wv]^T
-  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, qkv_w, dqkv, qkv_w, tA, Mp));  // [qkv_w, Mp]
-  BW_RUN("bwd_transpose", transpose(c, dt, M, Mp, d, u, d, tB, Mp));              // u^T [d, Mp]
+  // [dq | dk | dv]^T [qkv_w, Mp], u^T [d, Mp]
+  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{dqkv, qkv_w, tA, Mp, M, Mp, qkv_w, 0, 0},
+                                                  {u, d, tB, Mp, M, Mp, d, 0, 0}}));
   BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, qkv_w, d, Mp, tA, Mp, tB, Mp, gr->wq, gr->wk,
                                          gr->wv, qw, qw + kw, d));
-  BW_RUN("bwd_transpose", transpose(c, dt, qw, qw, d, w->wq, d, tW, qkv_w));      // [d, qkv_w]
-  BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wk, d, tW + qw, qkv_w));
-  BW_RUN("bwd_transpose", transpose(c, dt, kw, kw, d, w->wv, d, tW + qw + kw, qkv_w));
   float* du = (float*)bat(ws, L.du);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qkv_w, dqkv, qkv_w, tW, qkv_w, du, d, true));
+  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qkv_w, dqkv, qkv_w, tw.qkv, qkv_w, du, d, true));
   // u = RMSNorm(x_sel) g1; the gather's backward adds into the token's row of dx
   float* rstd1 = (float*)bat(ws, L.rstd1);
   BW_RUN("bwd_rows", launch_pdl(rms_bwd_kernel<E, E>, dim3(rowblk), dim3(BW_WARPS * 32), 0,
