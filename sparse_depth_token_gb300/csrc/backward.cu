@@ -1088,7 +1088,7 @@ cudaError_t launch_attn_bwd(const Ctx& c, xmod_dtype dt, int B, int hd, const At
 
 // The Selected-Q / full-KV layer's backward from the attention down (X-MoD notes,
 // "mechanism controls"): the selected tokens' queries qb [M, qw] (M = B * T/K rows, at
-// positions idx) over the keys and values kvb [B*T, 2kw] of every token (v only
+// positions idx) over the keys and values kvb [B*T, 2kw] of every token (v also
 // transposed, in vt, when v_transposed); dO [M, qw] (bf16 with mma, else fp32) and dh
 // [M, d] (the gradient through h = x_sel + a) come from the block's backward above. The
 // attention backward runs on the warp-level tensor-core MMA with mma (bf16, head_dim 64 or
@@ -1117,11 +1117,6 @@ int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weigh
   // ======== attention: n queries per sequence over its T keys
   const int kt_ld = (int)round8(T), qt_ld = (int)round8(n), ldS = (n + 63) / 64 * 64;
   const bool tc_bwd = mma && v_transposed && attn_bwd_dq_tc_supported(hd, qw, qw, kt_ld);
-  if (mma && v_transposed) {   // the backward reads v by rows: the v projection once more
-    E* kvw = const_cast<E*>(kvb);
-    BW_RUN("gemm_qkv", bw_gemm(c, dt, BT, kw, d, bat(ws, L.u), d, w->wv, d, kvw + kw, 2 * kw,
-                               false));
-  }
   if (tc_bwd) {   // tcgen05 (the forward wrote lse): dq, then dk and dv over every key
     E* kt = (E*)bat(ws, L.kt);
     E* qt = (E*)bat(ws, L.qt);
@@ -1320,13 +1315,14 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     pk.B[0] = w->wk; pk.B[1] = w->wv; pk.nB = 2; pk.split[0] = kw;
     const bool tc_kv = tc && attention_tc_supported(hd, n, qw) &&
                        attention_tc_supported(hd, T, 2 * kw);
-    if (tc_kv) {   // v straight to its transposed layout for the tensor-core attention
+    if (tc_kv) {   // v transposed for the tensor-core attention, and by rows as well
       ek.vt = vt;
       ek.vt_col0 = kw;
       ek.vt_hd = hd;
       ek.vt_hkv = hkv;
       ek.vt_ld = (int)round8(T);
       ek.n_per_seq = T;
+      ek.vt_rows = true;
       v_transposed = gemm_tc_supported(pk, ek);
     }
     if (v_transposed) {
@@ -1369,13 +1365,14 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     e.kind = EPI_STORE;
     e.out = qkv;
     e.ldo = qkv_w;
-    if (tc_attn) {
+    if (tc_attn) {   // v transposed for the forward attention, and by rows for the backward
       e.vt = vt;
       e.vt_col0 = qw + kw;
       e.vt_hd = hd;
       e.vt_hkv = hkv;
       e.vt_ld = (int)round8(n);
       e.n_per_seq = n;
+      e.vt_rows = true;
     }
     GemmTcProblem pq;
     pq.M = M; pq.N = qkv_w; pq.K = d; pq.A = u; pq.lda = d; pq.ldb = d;
@@ -1384,8 +1381,6 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     v_transposed = tc_attn && gemm_tc_supported(pq, e);
     if (v_transposed) {
       BW_RUN("gemm_qkv", launch_gemm_tc(c, pq, e));
-      // the backward also reads v by rows: the v projection once more into the v columns
-      BW_RUN("gemm_qkv", bw_gemm(c, dt, M, kw, d, u, d, w->wv, d, qkv + qw + kw, qkv_w, false));
     } else {
       e.vt = nullptr;
       BW_RUN("gemm_qkv", launch_gemm_simt(c, dt, M, qw, d, u, d, w->wq, d, nullptr, e));
@@ -1437,8 +1432,21 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   else   // Routed-FFN: the FFN input is RMSNorm(x_sel) rms2
     BW_RUN("gather_rmsnorm",
            launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms2, dm->rms_eps, v2));
-  BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_gate, d, gu, 2 * F, false));
-  BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_up, d, gu + F, 2 * F, false));
+  {   // [G | U] = v2 [W_gate | W_up]^T, one GEMM on the tensor cores
+    Epilogue e;
+    e.kind = EPI_STORE;
+    e.out = gu;
+    e.ldo = 2 * F;
+    GemmTcProblem p;
+    p.M = M; p.N = 2 * F; p.K = d; p.A = v2; p.lda = d; p.ldb = d;
+    p.B[0] = w->w_gate; p.B[1] = w->w_up; p.nB = 2; p.split[0] = F;
+    if (tc && gemm_tc_supported(p, e)) {
+      BW_RUN("gemm_gate_up", launch_gemm_tc(c, p, e));
+    } else {
+      BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_gate, d, gu, 2 * F, false));
+      BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_up, d, gu + F, 2 * F, false));
+    }
+  }
   {
     const int64_t tot = (int64_t)M * F / (16 / sizeof(E));
     const unsigned blk = (unsigned)std::min<int64_t>((tot + 255) / 256, 8192);

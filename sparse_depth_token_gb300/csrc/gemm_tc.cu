@@ -602,7 +602,7 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0,
 #pragma unroll
         for (int i = 0; i < 32; ++i) p[(int64_t)i * e.vt_ld] = __float2bfloat16_rn(v[i]);
       }
-      continue;
+      if (!e.vt_rows) continue;
     }
     epilogue_chunk_direct<MODE>(a, M, m_own, col0, xrow_own, r_own, v, cur, ks);
     cur = nxt;

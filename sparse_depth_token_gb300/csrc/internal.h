@@ -219,6 +219,7 @@ struct Epilogue {
   // transposed to vt [B, hkv, hd, vt_ld] (keys contiguous) instead of to `out`.
   void* vt = nullptr;
   int vt_col0 = 0, vt_hd = 0, vt_hkv = 0, vt_ld = 0;
+  bool vt_rows = false;         // with vt: write the values' columns to `out` as well
   // STORE: write the fp32 accumulator itself (out is float [M, ldo]) instead of
   // rounding it to the layer's element type
   bool out_f32 = false;
