@@ -300,3 +300,53 @@ def test_stack_bwd_bf16_equals_layer_chain(X):
             if k == "varsigma":
                 a, b = a[:1], b[:1]
             assert torch.equal(a, b), f"layer {l} {k}"
+
+
+def _bwd_once(X, w, kind, lw, x, dy, bias, pairs):
+    import os
+    dm = xmod_dims(w)
+    ws = torch.zeros(X.bwd_workspace_bytes(dm, w.K), dtype=torch.uint8, device="cuda")
+    abi = X.layer_weights(dev_layer(lw, w.dtype), lw["varsigma"], 0.0)
+    xd, dyd = to_dev(x, w.dtype), to_dev(dy, w.dtype)
+    dx = torch.empty_like(xd)
+    gd = _grad_set(w, 1)[0]
+    old = {k: os.environ.get(k) for k in ("XMOD_PAIR_MIN_WAVES", "XMOD_STREAM_K")}
+    os.environ["XMOD_PAIR_MIN_WAVES"] = "0" if pairs else "999999"
+    os.environ["XMOD_STREAM_K"] = "0"
+    try:
+        X.reset_status(ws)
+        X.layer_bwd(dm, kind, w.K, X.GATE_XMOD, abi, xd,
+                    torch.from_numpy(bias).cuda() if bias is not None else None, dyd, 0.1, dx,
+                    X.layer_grads(gd), ws)
+        assert X.sync_status(ws) == X.OK
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return dx, gd
+
+
+@pytest.mark.parametrize("kind", [0, 1, 4])
+def test_layer_bwd_on_cta_pairs_equals_single_ctas(X, kind):
+    """Every GEMM of the backward on CTA pairs (XMOD_PAIR_MIN_WAVES=0) against the same
+    call on single CTAs: the pair and single kernels form each output element as the same
+    dot product in the same k order, so dx and every gradient agree bit for bit -- this
+    covers the pair kernel's q|k|v epilogue writing v both transposed and by rows, and its
+    fp32 store splitting the stacked weight gradients by rows. Dense, sparse and full-KV."""
+    w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=512, K=4, d=256, hq=4, hkv=2, F=384, seed=43,
+                                         weight_std=0.049)
+    lw = I.layer_weights(w, 0)
+    lw["varsigma"] = 0.9
+    bias = I.router_bias(w)
+    x = I.residual_stream(w)
+    if kind:
+        x, _ = U.enforce_routing_margin(x, w.dtype, lw["w_r"], bias, w.K)
+    dyf = np.random.default_rng(44).standard_normal((w.B, w.T, w.d)).astype(np.float32)
+    dy = I.f32_to_bf16_bits(dyf)
+    dx1, g1 = _bwd_once(X, w, kind, lw, x, dy, bias, pairs=True)
+    dx0, g0 = _bwd_once(X, w, kind, lw, x, dy, bias, pairs=False)
+    assert torch.equal(dx1.view(torch.int16), dx0.view(torch.int16))
+    for k in ("rms1", "wq", "wk", "wv", "wo", "rms2", "w_gate", "w_up", "w_down", "varsigma"):
+        assert torch.equal(g1[k].view(torch.int32), g0[k].view(torch.int32)), k
