@@ -97,3 +97,39 @@ def test_invalid_arguments_rejected_before_launch():
     _expect(lambda: X.gather(dm, 0, FAKE, FAKE, FAKE, stream=0), X.ERR_INVALID_ARG)
     big = _dims(T=64 * 1024, B=1)
     assert L.xmod_topk(ctypes.byref(big), 4, FAKE, FAKE, None, ws, 1 << 40, None) == X.ERR_UNSUPPORTED
+
+
+def test_backward_arguments_rejected_before_launch():
+    """xmod_layer_bwd / xmod_stack_bwd / the wait self-test check their arguments on the
+    host: an unknown kind, aliasing outputs, a missing gradient of a weight the kind uses,
+    a bad layer count or a short workspace return before anything reaches the device --
+    and every layer kind, the Selected-Q / full-KV control included, passes the kind
+    check (it reaches the workspace check)."""
+    L = X.load()
+    dm = _dims()
+    dmp = ctypes.byref(dm)
+    w = X.LayerWeights(*([FAKE] * 10), 1.0)
+    grads = X.LayerGrads(*([FAKE] * 12), None, None)
+    A, B, C = FAKE, FAKE + 0x1000, FAKE + 0x2000   # x, dy, dx
+
+    def bwd(kind, x=A, dy=B, dx=C, g=grads, ws_bytes=16):
+        return L.xmod_layer_bwd(dmp, kind, 4, X.GATE_XMOD, ctypes.byref(w), x, None, dy,
+                                ctypes.c_float(0.0), dx, ctypes.byref(g), FAKE, ws_bytes, None)
+
+    assert bwd(9) == X.ERR_INVALID_ARG
+    assert bwd(X.LAYER_SPARSE, dx=A) == X.ERR_INVALID_ARG          # dx aliases x
+    assert bwd(X.LAYER_SPARSE, dx=B) == X.ERR_INVALID_ARG          # dx aliases dy
+    for kind in (X.LAYER_DENSE, X.LAYER_SPARSE, X.LAYER_ATTN, X.LAYER_ROUTED_FFN,
+                 X.LAYER_SPARSE_FULLKV):
+        assert bwd(kind) == X.ERR_WORKSPACE, kind
+    no_wk = X.LayerGrads(*([FAKE] * 3 + [None] + [FAKE] * 8), None, None)
+    assert bwd(X.LAYER_SPARSE_FULLKV, g=no_wk) == X.ERR_INVALID_ARG   # W_k's gradient needed
+    assert bwd(X.LAYER_ROUTED_FFN, g=no_wk) == X.ERR_WORKSPACE        # not used: may be NULL
+    arr = (X.LayerWeights * 6)(*([w] * 6))
+    garr = (X.LayerGrads * 6)(*([grads] * 6))
+    assert L.xmod_stack_bwd(dmp, 4, ctypes.c_double(1.0), 1, 1, X.GATE_XMOD, arr, 5, A, None, B,
+                            ctypes.c_float(0.0), C, garr, FAKE + 0x10000, FAKE, 1 << 30,
+                            None) == X.ERR_INVALID_ARG   # Eq. 3: 1 + 1 * 5 = 6 layers
+    assert L.xmod_selftest_wait_timeout(None, 256, None) == X.ERR_INVALID_ARG
+    assert L.xmod_selftest_wait_timeout(FAKE, 128, None) == X.ERR_INVALID_ARG
+    assert L.xmod_selftest_wait_timeout(FAKE + 4, 256, None) == X.ERR_INVALID_ARG
