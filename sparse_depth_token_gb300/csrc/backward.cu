@@ -1432,26 +1432,27 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   else   // Routed-FFN: the FFN input is RMSNorm(x_sel) rms2
     BW_RUN("gather_rmsnorm",
            launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms2, dm->rms_eps, v2));
-  {   // [G | U] = v2 [W_gate | W_up]^T, one GEMM on the tensor cores
+  {   // H = silu(G) U with G | U = v2 [W_gate | W_up]^T: one tensor-core GEMM whose
+      // SwiGLU epilogue also stores the pre-activations [G | U] for the SwiGLU backward
     Epilogue e;
-    e.kind = EPI_STORE;
-    e.out = gu;
-    e.ldo = 2 * F;
+    e.kind = EPI_SWIGLU;
+    e.out = H;
+    e.ldo = F;
+    e.out2 = gu;
+    e.ldo2 = 2 * F;
     GemmTcProblem p;
-    p.M = M; p.N = 2 * F; p.K = d; p.A = v2; p.lda = d; p.ldb = d;
-    p.B[0] = w->w_gate; p.B[1] = w->w_up; p.nB = 2; p.split[0] = F;
+    p.M = M; p.N = F; p.K = d; p.A = v2; p.lda = d; p.ldb = d;
+    p.B[0] = w->w_gate; p.B[1] = w->w_up; p.nB = 2;
     if (tc && gemm_tc_supported(p, e)) {
       BW_RUN("gemm_gate_up", launch_gemm_tc(c, p, e));
-    } else {
+    } else {   // [G | U] stored, then H from them
       BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_gate, d, gu, 2 * F, false));
       BW_RUN("gemm_gate_up", bw_gemm(c, dt, M, F, d, v2, d, w->w_up, d, gu + F, 2 * F, false));
+      const int64_t tot = (int64_t)M * F / (16 / sizeof(E));
+      const unsigned blk = (unsigned)std::min<int64_t>((tot + 255) / 256, 8192);
+      BW_RUN("swiglu", launch_pdl(swiglu_fwd_kernel<E>, dim3(blk), dim3(256), 0, c.stream,
+                                  (int64_t)M, F, (const E*)gu, H));
     }
-  }
-  {
-    const int64_t tot = (int64_t)M * F / (16 / sizeof(E));
-    const unsigned blk = (unsigned)std::min<int64_t>((tot + 255) / 256, 8192);
-    BW_RUN("swiglu", launch_pdl(swiglu_fwd_kernel<E>, dim3(blk), dim3(256), 0, c.stream,
-                                (int64_t)M, F, (const E*)gu, H));
   }
   BW_RUN("gemm_down", bw_gemm(c, dt, M, d, F, H, F, w->w_down, F, f, d, false));
   }

@@ -577,7 +577,18 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0,
       tmem_ld32(t_row + BN / 2 + c * 32, u);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i] * rstd_own) * (u[i] * rstd_own);
+      for (int i = 0; i < 32; ++i) {
+        v[i] *= rstd_own;
+        u[i] *= rstd_own;
+      }
+      const int colh = col_tile0 + c * 32;
+      if (e.out2 && m_own < M && colh < a.N) {   // the pre-activations G | U as well
+        __nv_bfloat16* pg = (__nv_bfloat16*)e.out2 + (int64_t)m_own * e.ldo2 + colh;
+        store32_bf16(pg, v, a.N - colh, a.v8);
+        store32_bf16(pg + a.N, u, a.N - colh, a.v8);
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]) * u[i];
     } else {
       tmem_ld32(t_row + c * 32, v);
       tmem_ld_wait();
@@ -1018,7 +1029,11 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
     v8 = v8 && seg_ok(e.out, (int64_t)e.ldo * (e.out_f32 ? 4 : 2));
   for (int i = 0; i < 2; ++i)
     if (e.row_split[i] > 0) v8 = v8 && seg_ok(e.out_rows[i], (int64_t)e.ldo * 4);
-  if (e.out2) v8 = v8 && seg_ok(e.out2, (int64_t)e.ldo2 * 4);
+  if (e.out2 && e.kind == EPI_SWIGLU)   // bf16 [G | U] rows, the U half N columns on
+    v8 = v8 && seg_ok(e.out2, (int64_t)e.ldo2 * 2) &&
+         seg_ok((const __nv_bfloat16*)e.out2 + p.N, (int64_t)e.ldo2 * 2);
+  else if (e.out2)
+    v8 = v8 && seg_ok(e.out2, (int64_t)e.ldo2 * 4);
   if (e.x) v8 = v8 && seg_ok(e.x, (int64_t)e.d * 2);
   if (e.a) v8 = v8 && seg_ok(e.a, (int64_t)e.d * 2);
   a.v8 = v8 ? 1 : 0;

@@ -189,8 +189,8 @@ struct Epilogue {
   int kind = EPI_STORE;
   void* out = nullptr;
   int ldo = 0;
-  void* out2 = nullptr;
-  int ldo2 = 0;
+  void* out2 = nullptr;          // OPROJ: h (fp32); SWIGLU: the pre-activations [G | U]
+  int ldo2 = 0;                  //   (bf16 [M, 2N]) when not NULL
   void* x = nullptr;            // residual stream [B, T, d] (read for OPROJ, updated for DOWN)
   const int32_t* idx = nullptr;
   int T = 0, n_per_seq = 0, d = 0;
