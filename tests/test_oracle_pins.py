@@ -279,6 +279,45 @@ def test_block_zero_up_gives_zero_ffn_and_zero_wo_gives_zero_attn():
     np.testing.assert_array_equal(f1, f2)
 
 
+def test_block_ffn_reads_the_in_block_residual_x_plus_a():
+    """The FFN's input is RMSNorm(h)·γ2 with h = x_sel + a, a the attention residual
+    (X-MoD notes, Eq. 6 / Eq. 7: a and f are the block's two residual branches; pre-norm
+    SwiGLU block). Built so that every value is fixed by hand:
+      rows x_i = 4·e_i, eps = 0        -> u_i = RMSNorm(x_i) = 2√2·e_i, Σ_j u_i[j] = 2√2;
+      every Wv row constant c_j / (2√2) -> v = c = e_0 on every row, so each head's
+                                          softmax average is c whatever the weights;
+      Wo[:, 0] = Wo[:, hd] = 1          -> a = 2 on every element;
+      h_i = x_i + a = 6 at i, 2 elsewhere -> mean(h²) = 8, v2 = h / (2√2);
+      Wg = 1/√2 everywhere              -> Wg·v2 = (6 + 7·2) / 4 = 5 (row independent);
+      Wu = √2 on column 0 only          -> Wu·v2 = 3 on row 0, 1 on rows 1, 2;
+      f_i = Wd[:, 0]·silu(5)·(Wu·v2).
+    An FFN fed RMSNorm(x_sel) gives Wg·v2 = 2, one fed RMSNorm(a) gives 4√2."""
+    d, hq, hkv, hd, F, n = 8, 2, 1, 4, 1, 3
+    g = _rng(21)
+    s2 = math.sqrt(2.0)
+    arr = {"w_r": np.zeros(d), "g1": np.ones(d), "g2": np.ones(d),
+           "wq": g.standard_normal((hq * hd, d)), "wk": g.standard_normal((hkv * hd, d))}
+    c = np.array([1.0, 0.0, 0.0, 0.0])
+    arr["wv"] = np.repeat(c[:, None] / (2 * s2), d, axis=1)
+    wo = np.zeros((d, hq * hd))
+    wo[:, 0] = 1.0
+    wo[:, hd] = 1.0
+    arr["wo"] = wo
+    arr["wg"] = np.full((F, d), 1.0 / s2)
+    wu = np.zeros((F, d))
+    wu[0, 0] = s2
+    arr["wu"] = wu
+    arr["wd"] = np.arange(1.0, d + 1)[:, None]
+    xs = 4.0 * np.eye(d)[:n]
+    dm = O.dims(1, n, d, hq, hkv, hd, F, eps=0.0)
+    a, f = O.block(dm, xs, O.Layer(arr))
+    np.testing.assert_allclose(a, 2.0, rtol=1e-14)
+    silu5 = 5.0 / (1.0 + math.exp(-5.0))
+    up = np.array([3.0, 1.0, 1.0])
+    want = up[:, None] * silu5 * np.arange(1.0, d + 1)[None, :]
+    np.testing.assert_allclose(f, want, rtol=1e-13)
+
+
 def test_block_row_subset_matches_full():
     d, hq, hkv, hd, F = 16, 4, 2, 4, 24
     g = _rng(14)

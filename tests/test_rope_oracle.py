@@ -9,6 +9,8 @@ pinned to properties the transforms have by construction:
   * a sparse layer rotates at the tokens' original positions: selecting every other
     token differs from selecting a prefix of the same tokens (which compact positions
     could not tell apart)."""
+import math
+
 import numpy as np
 
 import oracle as O
@@ -37,6 +39,23 @@ def test_rotated_dot_product_depends_on_the_offset_only():
         a = O.qk_transform(q, 1, hd, theta=THETA, pos=[p1]) @ O.qk_transform(k, 1, hd, theta=THETA, pos=[p2]).T
         b = O.qk_transform(q, 1, hd, theta=THETA, pos=[p1 + c]) @ O.qk_transform(k, 1, hd, theta=THETA, pos=[p2 + c]).T
         np.testing.assert_allclose(a, b, rtol=1e-9)
+
+
+def test_rotation_angles_and_pairing_closed_form():
+    """The rotary embedding's definition evaluated by hand (rotate-half convention of the
+    Qwen / LLaMA family): dimension c pairs with c + hd/2 and turns by t·θ^(−2c/hd).
+    hd = 4, θ = 16, t = 3: pair (0, 2) turns by 3 rad, pair (1, 3) by 3·16^(−1/2) = 0.75
+    rad. Basis vectors come out as the columns of the two plane rotations. An exponent of
+    −c/hd (1.5 rad on the second pair) or interleaved pairs (0, 1), (2, 3) fail."""
+    hd, theta, t = 4, 16.0, 3
+    y = O.qk_transform(np.eye(hd), 1, hd, theta=theta, pos=[t] * hd)
+    c0, s0 = math.cos(3.0), math.sin(3.0)
+    c1, s1 = math.cos(0.75), math.sin(0.75)
+    want = np.array([[c0, 0.0, s0, 0.0],      # e_0 -> (cos, sin) in the plane (0, 2)
+                     [0.0, c1, 0.0, s1],      # e_1 -> (cos, sin) in the plane (1, 3)
+                     [-s0, 0.0, c0, 0.0],     # e_2 -> (-sin, cos) in the plane (0, 2)
+                     [0.0, -s1, 0.0, c1]])    # e_3 -> (-sin, cos) in the plane (1, 3)
+    np.testing.assert_allclose(y, want, rtol=0, atol=1e-15)
 
 
 def _layer(w, g_scale=1.0, wqk_scale=1.0, theta=THETA):
