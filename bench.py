@@ -1,14 +1,15 @@
 """Benchmark of the sparse-depth layer stack on GB300.
 
-Default (the headline): one step = one pass of the whole X-MoD A4K8 block (32 Sparse(K=8) layers with
-Eq. 7 gating + 1 Dense anchor; d=1536, 12 q / 4 kv heads, head_dim 128, SwiGLU
-d_ff=4096, B=8 sequences of T=4096 tokens, per-token router bias) through the
-library's stack entry point. Metric: selected tokens processed by sparse layers
-per second (B * T/K * 32 per step), whole job over all ranks.
+Default (the headline): one step = one pass of the whole X-MoD A3K16 stack, the largest
+single-GPU configuration (Eq. 3 with N0=2, N1=2, 48 Sparse(K=16) layers per block with
+Eq. 7 gating: 2 Dense + (48 Sparse + 1 Dense) x 2 = 100 layers; d=2048, 16 q / 4 kv
+heads, head_dim 128, SwiGLU d_ff=5632, B=4 sequences of T=16384 tokens) through the
+library's stack entry point. Metric: selected tokens processed by sparse layers per
+second (B * T/K * 96 per step), whole job over all ranks.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl xmod|reference]
 
-Other workloads: --workload mod_bf16 | a3k16_bf16 | tiny_fp32 (the same stack step),
+Other workloads: --workload a4k8_bf16 | mod_bf16 | tiny_fp32 (the same stack step),
 --workload routing_bf16 (the routing-only microbench: router + top-(T/K) + gather +
 Eq. 7 scatter of a given block output), --pass bwd (the backward of every layer).
 
@@ -36,7 +37,7 @@ from sparse_depth_token_gb300 import inputs as I  # noqa: E402
 
 METRIC = "selected tokens/s per X-MoD sparse-layer fwd (bf16, 1xGB300); % HBM / tensor roofline"
 UNIT = "selected tokens/s"
-WORKLOAD = "a4k8_bf16"
+WORKLOAD = "a3k16_bf16"
 ABI_NAMES = {"w_r": "w_router", "g1": "rms1", "wq": "wq", "wk": "wk", "wv": "wv", "wo": "wo",
              "g2": "rms2", "wg": "w_gate", "wu": "w_up", "wd": "w_down"}
 
@@ -79,11 +80,46 @@ def workload_config(w: I.Workload) -> dict:
                     f"head_dim {w.hd}, SwiGLU d_ff={w.F}",
         "B_per_gpu": w.B, "T": w.T, "K": w.K,
         "selected_tokens_per_step_per_gpu": n_routed * w.B * (w.T // w.K),
-        "l2": "no flush: one step streams 1.7 GB of distinct layer weights and a 100 MB "
-              "stream, both larger than the 129 MB L2",
+        "l2": l2_note(w),
         "inputs": "seeded synthetic: x~N(0,1), matrices~N(0,0.02^2), w_r~N(0,1/d), "
-                  "bias~N(0,0.1^2), varsigma~U(0.5,1.5), RMSNorm gains 1",
+                  + (f"bias~N(0,{w.bias_std}^2), " if w.bias_std else "no router bias, ")
+                  + ("varsigma~U(0.5,1.5), " if w.gate == 0 else "")
+                  + "RMSNorm gains 1",
     }
+
+
+def l2_note(w: I.Workload) -> str:
+    """Why the timed steps need no L2 flush: the distinct bytes one step streams."""
+    es = 2 if w.dtype == "bf16" else 4
+    per_layer = es * (w.d * (w.hq + 2 * w.hkv) * w.hd + w.hq * w.hd * w.d + 3 * w.d * w.F + w.d)
+    weights = per_layer * len(schedule(w))
+    stream = es * w.B * w.T * w.d
+    if weights + stream > 2 * 129e6:
+        return (f"no flush: one step streams {weights / 1e9:.1f} GB of distinct layer weights "
+                f"and a {stream / 1e6:.0f} MB stream, both larger than the 129 MB L2"
+                if stream > 129e6 else
+                f"no flush: one step streams {weights / 1e9:.1f} GB of distinct layer weights "
+                f"(the 129 MB L2 holds under a tenth of a step's bytes)")
+    return "no flush: a latency-bound tiny step (its bytes fit in L2)"
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() == "Model name":
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
 
 
 def algorithmic_work(w: I.Workload, sel_counts=None) -> dict:
@@ -242,9 +278,13 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------- CPU oracle baseline
 
-def oracle_sample(w: I.Workload, budget_s: float = 15.0, max_reps: int = 50):
+def oracle_sample(w: I.Workload, budget_s: float = 15.0, max_reps: int = 50,
+                  row_frac: float = 1.0):
     """The CPU oracle on a bounded sample of the workload: one sparse layer of the stack
     (layer 0 weights) on sequence 0 of the batch, repeated until `budget_s` elapses.
+    row_frac < 1: only the selected tokens in the first row_frac of the positions are
+    computed (the router and top-k still cover the whole sequence; keys and values up
+    to the last wanted row); the tokens counted are those rows.
     Returns (selected tokens/s, threads, description)."""
     import oracle as O
     lw = I.layer_weights(w, 0)
@@ -255,16 +295,23 @@ def oracle_sample(w: I.Workload, budget_s: float = 15.0, max_reps: int = 50):
     bias = I.router_bias(w1)
     dm = O.dims(1, w.T, w.d, w.hq, w.hkv, w.hd, w.F, w.eps)
     n = w.T // w.K
+    kind = {"routed_ffn": O.RFFN, "fullkv": O.FULLKV}.get(VARIANT, O.SPARSE)
+    mask, counted, what = None, n, f"n={n} selected"
+    if row_frac < 1.0 and kind != O.FULLKV:
+        cut = int(w.T * row_frac)
+        mask = (np.arange(w.T) < cut).astype(np.int32)[None, :]
+        idx = O.topk(O.router(x, L.arrays["w_r"], bias)[0], n)   # the layer's own selection
+        counted = int((idx[0] < cut).sum())
+        what = f"the {counted} of its n={n} selected tokens before position {cut}"
     reps, t0 = 0, time.perf_counter()
     while True:
-        O.layer_fwd(dm, {"routed_ffn": O.RFFN, "fullkv": O.FULLKV}.get(VARIANT, O.SPARSE), w.K,
-                    w.gate, L, x, bias=bias)
+        O.layer_fwd(dm, kind, w.K, w.gate, L, x, bias=bias, row_mask=mask)
         reps += 1
         el = time.perf_counter() - t0
         if el >= budget_s or reps >= max_reps:
             break
-    return reps * n / el, O.num_threads(), (
-        f"one Sparse(K={w.K}) layer on 1 of the {w.B} sequences (T={w.T}, n={n} selected), "
+    return reps * counted / el, O.num_threads(), (
+        f"one Sparse(K={w.K}) layer on 1 of the {w.B} sequences (T={w.T}, {what}), "
         f"{reps} repetition(s) in {el:.1f} s")
 
 
@@ -316,7 +363,7 @@ def run_reference(args):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.num_threads(),
-                             "kind": "oracle", "sample": sample},
+                             "cpu_model": cpu_model(), "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -444,9 +491,12 @@ def run_xmod(args):
     X.profile_read()
     X.profile_enable(True)
     prof_steps = max(1, min(args.steps, 3))
+    e0.record(stream)
     for _ in range(prof_steps):
         step()
+    e1.record(stream)
     torch.cuda.synchronize()
+    prof_ms = e0.elapsed_time(e1)
     X.profile_enable(False)
     prof = X.profile_read()
     work = algorithmic_work(w, sel_counts)
@@ -470,13 +520,15 @@ def run_xmod(args):
         cnt, kms = prof[top]
         if top in TENSOR_KINDS:
             ach = work[top] / (kms / prof_steps / 1e3) / 1e12
-            peak = peaks["bf16_tflops_sustained"]
+            peak = peaks["bf16_tflops"]
             tag = "xmod" if (VARIANT == "xmod" and plain and not args.qwen3) else "other"
             traffic, tsrc = recorded_traffic(w, tag, top)
             roofline = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": peak,
                         "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
-                        "peak_source": f"{peaks['source']} bf16 sustained (kernel timed inside "
-                                       f"a long step)",
+                        "peak_source": f"{peaks['source']} bf16 burst (the kernel is timed "
+                                       f"in a profiled pass of {prof_steps} step(s), "
+                                       f"{prof_ms:.0f} ms: not a seconds-long run)",
+                        "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
                         "algorithmic_per_launch": work[top] / (cnt / prof_steps)}
             if tsrc:
                 roofline["traffic_source"] = tsrc
@@ -588,9 +640,12 @@ def run_xmod(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = oracle_sample(w, budget_s=args.cpu_budget)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "cpu_model": cpu_model(),
+               "kind": "oracle", "sample": sample,
                "single_thread": single_thread_variant(
-                   lambda bs: oracle_sample(w, budget_s=bs, max_reps=1), args.cpu_budget / 3)}
+                   lambda bs: oracle_sample(w, budget_s=bs, max_reps=1,
+                                            row_frac=min(1.0, 256 / (w.T // w.K))),
+                   args.cpu_budget / 3)}
 
     if rank == 0:
         cfg = workload_config(w)
@@ -799,10 +854,12 @@ def run_backward(args):
         cnt, kms = prof[top]
         if top in BWD_TENSOR_KINDS:
             ach = work[top] / (kms / prof_steps / 1e3) / 1e12
-            peak = peaks["bf16_tflops_sustained"]
+            peak = peaks["bf16_tflops"]
             roofline = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": peak,
                         "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
-                        "peak_source": f"{peaks['source']} bf16 sustained",
+                        "peak_source": f"{peaks['source']} bf16 burst (profiled pass of "
+                                       f"{prof_steps} step(s))",
+                        "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
                         "algorithmic_per_launch": work[top] / (cnt / prof_steps)}
         else:   # data movement (the transposes): compulsory bytes over the HBM copy rate
             ach = work[top] / (kms / prof_steps / 1e3) / 1e9
@@ -916,7 +973,7 @@ def run_routing_reference(args):
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": routing_config(w, K),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.num_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "cpu_model": cpu_model(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0}}), flush=True)
 
@@ -1149,7 +1206,8 @@ def run_routing(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = oracle_routing_sample(w, K, budget_s=args.cpu_budget)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "cpu_model": cpu_model(),
+               "kind": "oracle", "sample": sample,
                "single_thread": single_thread_variant(
                    lambda bs: oracle_routing_sample(w, K, budget_s=bs), args.cpu_budget / 3)}
 

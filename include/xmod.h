@@ -29,6 +29,13 @@
  *     by xmod_sync_status; kernels never trap.
  *   - Pointers must be 16-byte aligned; d, hq*hd, hkv*hd and F must be
  *     multiples of 8.
+ *   - Which kernels run. bf16: every projection on the tcgen05 tensor cores (bf16
+ *     operands, fp32 accumulation); the attention on the tcgen05 attention kernel when
+ *     head_dim is 128, and on an FFMA kernel (bf16 operands, fp32 accumulation, much
+ *     slower) for any other head_dim. fp32: FFMA kernels throughout (no TF32). The
+ *     routing, gather and scatter kernels are the same in both. There is no other
+ *     fallback: a bf16 call on a system without the TMA tensor-map entry point returns
+ *     XMOD_ERR_UNSUPPORTED instead of running its projections on FFMA kernels.
  *   - Entry points are stateless and may run concurrently on different streams
  *     with different workspaces.
  */
@@ -293,8 +300,9 @@ XMOD_API int xmod_stack_fwd_sched(const xmod_dims* dims, int K, const int32_t* k
  * may be NULL and are zeroed when given. SPARSE_FULLKV (the Selected-Q / full-KV
  * control) sends the gradient through every token's key and value as well: rows the
  * layer did not select receive more than dy when a selected query sees them. Its
- * attention backward runs on FFMA kernels in both dtypes (the projections still use the
- * tensor cores in bf16). An unknown kind returns XMOD_ERR_INVALID_ARG.
+ * attention backward runs on the tcgen05 kernels in bf16 with head_dim 128 (query
+ * positions over a separate key set), on warp-level MMA kernels in bf16 with head_dim
+ * 64 and on FFMA kernels in fp32. An unknown kind returns XMOD_ERR_INVALID_ARG.
  * bf16 runs the projections and their gradients on the tensor cores (bf16 operands,
  * fp32 accumulation, fp32 weight gradients); fp32 runs FFMA kernels throughout. */
 typedef struct {
@@ -354,8 +362,11 @@ XMOD_API int xmod_stack_bwd(const xmod_dims* dims, int K, double A, int N0, int 
  * each call clears the status word first and rewrites every logit it reads, so
  * back-to-back calls on one stream are independent. Calls that overlap on the GPU
  * (different streams with no ordering between them) race on the array.
- * The first call on a device looks up the array's device address with that device
- * current; make that first call before any stream capture.
+ * A call looks up the array's device address with its device current whenever its
+ * stream is not being captured, and remembers it per device; a call made during
+ * stream capture uses the remembered address. So make one call on a device before
+ * any capture, and again after a device reset (which moves the array); a captured
+ * call on a device never called outside capture returns XMOD_ERR_INVALID_ARG.
  *
  *   x, w_r, bias, idx, r_sel: as for xmod_router_topk (device pointers, bias and
  *   r_sel may be NULL). status_out: NULL or a device int that receives the device

@@ -310,6 +310,9 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
   char* h = at(ws, L.h);
   char* hidden = at(ws, L.hidden);
   const bool tc = dt == XMOD_BF16;
+  // bf16 projections run on the tensor cores only (no FFMA route for them): without the
+  // TMA tensor-map entry point the call is refused rather than run on FFMA kernels
+  if (tc && !tma_available()) return XMOD_ERR_UNSUPPORTED;
   char* v2 = u;   // RMSNorm2 output, in the buffer of u (consumed by the q/k/v projection)
   // a, the attention residual, for the down projection's scatter (the caller's a_out
   // when given); NULL for an FFN-only block (a = 0)

@@ -1261,6 +1261,7 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   const int qw = hq * hd, kw = hkv * hd, qkv_w = qw + 2 * kw;
   const size_t es = sizeof(E);
   const bool tc = dt == XMOD_BF16;
+  if (tc && !tma_available()) return XMOD_ERR_UNSUPPORTED;   // no FFMA route for bf16 GEMMs
   // route_bwd_kernel keeps a float and a flag per token of a sequence in shared memory
   if (sparse && (size_t)T * (sizeof(float) + 1) > 200 * 1024) return XMOD_ERR_UNSUPPORTED;
   float* s = (float*)bat(ws, L.s);

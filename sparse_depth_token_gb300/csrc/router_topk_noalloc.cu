@@ -13,8 +13,11 @@
 // the last call's contents; the status word is cleared at the start of each call
 // and the logits are fully rewritten, so nothing stale is read. Calls that
 // overlap on the GPU (different streams, no ordering between them) race on the
-// array. The first call on a device looks up the array's device address once,
-// with that device current; make that first call before any stream capture.
+// array. Every call that is not being captured into a CUDA graph looks up the
+// array's device address afresh (a host-side query, with the call's device current)
+// and remembers it per device; a call made during stream capture uses the remembered
+// address, so make one call on the device before any capture -- and again after a
+// device reset, which reloads the library's device image at a new address.
 
 #include <cuda_runtime.h>
 #include <math.h>
@@ -38,17 +41,25 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once per
-// device). In host code the array's name is only a host-side stand-in, so the
-// address must come from the runtime.
-void* scratch_on_current_device(int* err) {
+// Device address of the scratch array on the current device. In host code the
+// array's name is only a host-side stand-in, so the address must come from the
+// runtime. Outside stream capture it is looked up on every call (so a device reset,
+// which moves the array, is picked up by the next call); during capture, where the
+// lookup could load the module, the address remembered by the last uncaptured call on
+// this device is used, and a device never called outside capture is an error.
+void* scratch_on_current_device(cudaStream_t s, int* err) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     *err = XMOD_ERR_CUDA;
     return nullptr;
   }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    *err = XMOD_ERR_CUDA;
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_addr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
       *err = XMOD_ERR_CUDA;
@@ -56,6 +67,7 @@ void* scratch_on_current_device(int* err) {
     }
     g_addr[dev] = p;
   }
+  if (!g_addr[dev]) *err = XMOD_ERR_INVALID_ARG;   // first call on this device is captured
   return g_addr[dev];
 }
 
@@ -78,12 +90,12 @@ extern "C" int xmod_router_topk_noalloc(const xmod_dims* dm, int K, const void* 
     return XMOD_ERR_INVALID_ARG;
   if ((int64_t)dm->B * dm->T > (int64_t)XMOD_NOALLOC_MAX_TOKENS) return XMOD_ERR_UNSUPPORTED;
   if (dm->T > topk_max_T()) return XMOD_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
   int err = XMOD_OK;
-  void* base = scratch_on_current_device(&err);
+  void* base = scratch_on_current_device(s, &err);
   if (!base) return err;
   int* status = reinterpret_cast<int*>(base);
   float* logits = reinterpret_cast<float*>(reinterpret_cast<char*>(base) + kStatusBytes);
-  cudaStream_t s = (cudaStream_t)stream;
   Ctx c{s, status};
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return XMOD_ERR_CUDA;
   cudaError_t e;

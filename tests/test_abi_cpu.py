@@ -32,6 +32,13 @@ def test_library_exports_every_declared_symbol():
     assert all(s.startswith("xmod_") for s in exported), "internal symbols leak from the library"
 
 
+def test_noalloc_limit_matches_the_header():
+    """The binding's pre-check of the allocation-free entry point uses the header's limit."""
+    m = re.search(r"#define\s+XMOD_NOALLOC_MAX_TOKENS\s+\(([^)]*)\)", open(HEADER).read())
+    assert m, "XMOD_NOALLOC_MAX_TOKENS not found in the header"
+    assert eval(m.group(1), {"__builtins__": {}}) == X.NOALLOC_MAX_TOKENS
+
+
 def test_version_and_status_strings():
     assert "sm_103a" in X.version()
     for st in (0, -1, -2, -3, -4, -5, -6):

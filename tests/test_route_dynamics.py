@@ -147,3 +147,52 @@ def test_oracle_dynamics_overwhelming_growth_rotates_tokens():
             penalised = sb[l] < -big / 2
             assert np.all(penalised.sum(axis=1) == l * n)     # earlier picks carry -big
             assert np.array_equal(penalised, blk[:l].any(axis=0))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_host_averaging_matches_plain_mask_diagnostics(seed):
+    """The library's host-side averaging (sparse_depth_token_gb300.diagnostics, fed the
+    per-layer and per-block counters the device gathers) against the plain mask
+    diagnostics (oracle.diagnostics) on random selections and logits: coverage,
+    adjacent Jaccard, agreement and the update distribution. Layers select random
+    subsets of varying size (some empty, so Jaccard is undefined for some pairs), so
+    the averages are not degenerate."""
+    g = np.random.default_rng(seed)
+    n_blocks, AK, B, T = 3, 5, 4, 40
+    L = n_blocks * AK
+    masks = np.zeros((L, B, T), bool)
+    for l in range(L):
+        for b in range(B):
+            k = int(g.integers(0, 9)) if (l + b) % 7 else 0
+            masks[l, b, g.choice(T, k, replace=False)] = True
+    masks[AK:2 * AK, 1] = False   # one (block, sequence) with nothing selected: Jaccard undefined
+    logits = g.standard_normal((L, B, T))
+    # the counters of xmod_stack_fwd_ex: selected, threshold-selected, agreeing,
+    # selected again after the previous sparse layer of the block
+    thr = logits >= 0.0
+    st = np.zeros((L, B, 4), np.int64)
+    st[:, :, 0] = masks.sum(2)
+    st[:, :, 1] = thr.sum(2)
+    st[:, :, 2] = (masks == thr).sum(2)
+    for l in range(L):
+        if l % AK:
+            st[l, :, 3] = np.logical_and(masks[l], masks[l - 1]).sum(1)
+    uh = np.zeros((n_blocks, B, AK + 1), np.int64)
+    for k in range(n_blocks):
+        c = D.update_counts(masks[k * AK:(k + 1) * AK])
+        for b in range(B):
+            uh[k, b] = np.bincount(c[b], minlength=AK + 1)
+    got = PD.route_diagnostics(st, uh, T, AK)
+
+    cov = [D.coverage(masks[k * AK:(k + 1) * AK]) for k in range(n_blocks)]
+    jac = np.concatenate([D.adjacent_jaccard(masks[k * AK:(k + 1) * AK])
+                          for k in range(n_blocks)])
+    assert np.isnan(jac).any() and np.isfinite(jac).sum() > 3
+    np.testing.assert_allclose(got.coverage, np.mean(cov), rtol=1e-12)
+    np.testing.assert_allclose(got.jaccard, np.nanmean(jac), rtol=1e-12)
+    np.testing.assert_allclose(got.agreement, D.agreement(masks, logits), rtol=1e-12)
+    np.testing.assert_allclose(got.threshold_rate, thr.mean(), rtol=1e-12)
+    counts = np.concatenate([D.update_counts(masks[k * AK:(k + 1) * AK]).ravel()
+                             for k in range(n_blocks)])
+    np.testing.assert_allclose(got.update_dist, np.bincount(counts, minlength=AK + 1) / counts.size,
+                               rtol=1e-12)

@@ -65,3 +65,37 @@ def test_router_topk_noalloc_rejects_oversized_problem():
     fake = 0x10000   # never dereferenced: the size check comes first
     assert L.xmod_router_topk_noalloc(ctypes.byref(dm), 8, fake, fake, None, fake, None, None,
                                       None) == X.ERR_UNSUPPORTED
+
+
+def test_router_topk_noalloc_status_word():
+    """The status word of the shared scratch: a non-finite logit (a NaN placed in the
+    input on the host) is reported as XMOD_ERR_DEVICE_CHECK through status_out; the next
+    clean call clears it and reports XMOD_OK; a call without status_out runs too."""
+    need_gpu()
+    from sparse_depth_token_gb300 import xmod as X
+    X.load()
+    B, T, d, K = 2, 512, 128, 4
+    n = T // K
+    dm, xd, wr, bd = _case(X, B, T, d, K, 44, "bf16", 0.0)
+    x_nan = xd.clone()
+    x_nan[1, 77, 5] = float("nan")
+    ws = workspace(dm, K)
+    idx_ref = torch.empty((B, n), dtype=torch.int32, device="cuda")
+    rs_ref = torch.empty((B, n), dtype=torch.float32, device="cuda")
+    X.reset_status(ws)
+    X.router_topk(dm, K, xd, wr, bd, None, None, idx_ref, rs_ref, ws)
+    assert X.sync_status(ws) == X.OK
+    idx = torch.empty((B, n), dtype=torch.int32, device="cuda")
+    rs = torch.empty((B, n), dtype=torch.float32, device="cuda")
+    st = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    X.router_topk_noalloc(dm, K, x_nan, wr, bd, idx, rs, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == X.ERR_DEVICE_CHECK
+    X.router_topk_noalloc(dm, K, xd, wr, bd, idx, rs, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == X.OK
+    np.testing.assert_array_equal(idx.cpu().numpy(), idx_ref.cpu().numpy())
+    idx.fill_(-1)
+    X.router_topk_noalloc(dm, K, xd, wr, bd, idx, None, None)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), idx_ref.cpu().numpy())
