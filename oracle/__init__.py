@@ -52,6 +52,7 @@ def lib():
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_round_bf16.restype = ctypes.c_double
         L.oracle_round_bf16.argtypes = [ctypes.c_double]
+        L.oracle_round_bf16_n.argtypes = [ctypes.c_int64, _DP]
         L.oracle_router.argtypes = [ctypes.c_int64, ctypes.c_int, _DP, _DP, _DP, _DP, _DP]
         L.oracle_topk.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _DP, _IP]
         L.oracle_rmsnorm.argtypes = [ctypes.c_int64, ctypes.c_int, _DP, _DP, ctypes.c_double, _DP]
@@ -116,6 +117,13 @@ def _check(st):
 
 def round_bf16(v: float) -> float:
     return lib().oracle_round_bf16(float(v))
+
+
+def round_bf16_array(v):
+    """round_bf16 of every element; returns a new float64 array of v's shape."""
+    out = np.array(v, dtype=np.float64, copy=True, order="C")
+    lib().oracle_round_bf16_n(out.size, out.ctypes.data_as(_DP))
+    return out
 
 
 def router(x, w_r, bias=None):

@@ -98,6 +98,12 @@ double oracle_round_bf16(double v) {
   return std::nearbyint(v / ulp) * ulp;   // default rounding mode: nearest-even
 }
 
+// The same rounding applied to n values in place.
+void oracle_round_bf16_n(int64_t n, double* v) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) v[i] = oracle_round_bf16(v[i]);
+}
+
 // Eq. 8: s_i = w_r . x_i + b_i, r_i = sigmoid(s_i).
 void oracle_router(int64_t rows, int d, const double* x, const double* w_r,
                    const double* bias, double* s, double* r) {

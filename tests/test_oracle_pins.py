@@ -472,6 +472,22 @@ def test_round_bf16_agrees_with_float32_path():
     np.testing.assert_array_equal(got, ref)
 
 
+def test_round_bf16_array_matches_scalar_and_stack_mirroring():
+    g = _rng(23)
+    v = g.standard_normal((3, 5, 7)) * 10.0 ** g.integers(-3, 4, (3, 5, 7))
+    got = O.round_bf16_array(v)
+    assert got.shape == v.shape
+    np.testing.assert_array_equal(got.ravel(), [O.round_bf16(float(t)) for t in v.ravel()])
+    # one dense layer in storage-mirroring mode = the layer, then the rounding
+    d, hq, hkv, hd, F = 16, 4, 2, 4, 24
+    arr = _layer_arrays(_rng(24), d, hq, hkv, hd, F)
+    x = g.standard_normal((2, 6, d))
+    dm = O.dims(2, 6, d, hq, hkv, hd, F)
+    y = O.layer_fwd(dm, O.DENSE, 1, 0, O.Layer(arr), x)["y"]
+    mirrored = O.stack_fwd(dm, 1, 0, [O.DENSE], [O.Layer(arr)], x, mirror_bf16=True)
+    np.testing.assert_array_equal(O.round_bf16_array(y), mirrored)
+
+
 def test_gated_scatter_matches_layer_residual():
     """The standalone scatter step reproduces the layer's own residual on its selected rows."""
     dm = _small_dims()
