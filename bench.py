@@ -44,6 +44,8 @@ ABI_NAMES = {"w_r": "w_router", "g1": "rms1", "wq": "wq", "wk": "wk", "wv": "wv"
 
 DENSE, SPARSE, ATTN, RFFN, FULLKV = 0, 1, 2, 3, 4   # the library's layer kinds
 VARIANT = "xmod"   # set from --variant before any schedule is built
+ONLY = None        # --only: a stack of one layer kind (profiling), set before any schedule
+ONLY_LAYERS = {"sparse": 16, "dense": 2}
 
 
 def schedule(w: I.Workload, variant=None):
@@ -51,6 +53,8 @@ def schedule(w: I.Workload, variant=None):
     control (([FullAttn] + [Routed-FFN] x K) x A between the anchors); fullkv: the
     Selected-Q / full-KV control (the Eq. 3 stack with full-sequence keys and values)."""
     variant = variant or VARIANT
+    if ONLY is not None:   # one kind only, at the workload's shapes
+        return [SPARSE if ONLY == "sparse" else DENSE] * ONLY_LAYERS[ONLY]
     ak = int(round(w.A * w.K))
     if variant == "routed_ffn":
         A = ak // w.K
@@ -66,7 +70,9 @@ def routed(k) -> bool:
 def workload_config(w: I.Workload) -> dict:
     kinds = schedule(w)
     n_routed = sum(1 for k in kinds if routed(k))
-    if VARIANT == "routed_ffn":
+    if ONLY is not None:
+        what = f"{len(kinds)} {ONLY} layers only (profiling stack)"
+    elif VARIANT == "routed_ffn":
         what = (f"Routed-FFN control {n_routed} Routed-FFN(K={w.K}) + {kinds.count(ATTN)} "
                 f"FullAttn + {kinds.count(DENSE)} Dense")
     elif VARIANT == "fullkv":
@@ -75,7 +81,8 @@ def workload_config(w: I.Workload) -> dict:
         what = f"X-MoD stack {n_routed} Sparse(K={w.K}) + {kinds.count(DENSE)} Dense"
     return {
         "workload": f"{w.name}: {what} "
-                    f"(Eq. 3, N0={w.N0}, N1={w.N1}, A={w.A}), Eq. "
+                    + ("" if ONLY is not None else f"(Eq. 3, N0={w.N0}, N1={w.N1}, A={w.A}), ")
+                    + f"Eq. "
                     f"{'7' if w.gate == 0 else '6'} gating, d={w.d}, {w.hq}/{w.hkv} heads, "
                     f"head_dim {w.hd}, SwiGLU d_ff={w.F}",
         "B_per_gpu": w.B, "T": w.T, "K": w.K,
@@ -425,7 +432,7 @@ def run_xmod(args):
     def run_stack(stats=None, xb=None, bb=None):
         xb = x if xb is None else xb
         bb = bias if bb is None else bb
-        if VARIANT != "xmod":
+        if VARIANT != "xmod" or ONLY is not None:
             X.stack_fwd_sched(dm, w.K, kinds, w.gate, abi, xb, bb, ws,
                               bias_step=args.bias_step, layer_stats=stats,
                               routing=X.ROUTE_THRESHOLD if args.routing == "threshold"
@@ -1257,12 +1264,16 @@ def main():
                     help="QK-norm and RoPE (base 1e6) in every attending layer")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="bwd: time the backward of every layer of the stack (xmod_layer_bwd)")
+    ap.add_argument("--only", choices=["sparse", "dense"], default=None,
+                    help="profiling: a stack of 16 sparse or 2 dense layers of the workload "
+                         "instead of its Eq. 3 schedule (not a headline configuration)")
     ap.add_argument("--K", type=int, default=None,
                     help="routing_bf16 only: one sparsity K (default: 8 as the headline, with "
                          "2 and 16 under \"sweep\")")
     args = ap.parse_args()
-    global VARIANT
+    global VARIANT, ONLY
     VARIANT = args.variant
+    ONLY = args.only
     if args.B is not None or args.A is not None:
         w = I.WORKLOADS[args.workload]
         A = w.A if args.A is None else args.A

@@ -155,9 +155,13 @@ XMOD_API int xmod_router_topk(const xmod_dims* dims, int K, const void* x, const
 XMOD_API int xmod_topk(const xmod_dims* dims, int K, const float* logits, int32_t* idx, float* r_sel,
               void* ws, size_t ws_bytes, void* stream);
 
-/* Position-ordered gather: xs[b*n + j, :] = x[b, idx[b, j], :], n = floor(T/K). */
+/* Position-ordered gather: xs[b*n + j, :] = x[b, idx[b, j], :], n = floor(T/K).
+ * The positions are checked on the device: a row whose position is outside [0, T) or
+ * not above the previous row's in its sequence is skipped (its xs row is not written)
+ * and, when status_out (a device int, or NULL) is given, XMOD_ERR_DEVICE_CHECK is
+ * stored there if it still holds 0 (the caller zeroes it; the first error stays). */
 XMOD_API int xmod_gather(const xmod_dims* dims, int K, const void* x, const int32_t* idx, void* xs,
-                void* stream);
+                int* status_out, void* stream);
 
 /* The transformer block on n_per_seq tokens of every sequence (X-MoD notes,
  * backbone configuration: GQA attention, SwiGLU FFN; pre-norm RMSNorm):
@@ -166,7 +170,11 @@ XMOD_API int xmod_gather(const xmod_dims* dims, int K, const void* x, const int3
  *       scale 1/sqrt(head_dim), query head h reads KV head h / (n_heads/n_kv_heads)
  *   a = o Wo^T; h = xs + a; f = (silu(v2 Wg^T) * (v2 Wu^T)) Wd^T, v2 = RMSNorm(h) * rms2
  * With idx == NULL, `xs` is the compact buffer [B * n_per_seq, d]; otherwise `xs`
- * is the full stream x [B, T, d] and row j of sequence b is x[b, idx[b, j]].
+ * is the full stream x [B, T, d] and row j of sequence b is x[b, idx[b, j]]; the
+ * positions are checked on the device first (in [0, T), ascending within a sequence):
+ * a bad row records XMOD_ERR_DEVICE_CHECK in the status word and is read at its
+ * position clamped into [0, T), so nothing outside the stream is touched (its a_out,
+ * f_out rows and those of the rows attending to it are then meaningless).
  * a_out, f_out: [B * n_per_seq, d] (dtype). Workspace: xmod_workspace_bytes with
  * K = T / n_per_seq rounded down. */
 XMOD_API int xmod_block_fwd(const xmod_dims* dims, int n_per_seq, const void* xs, const int32_t* idx,
@@ -177,10 +185,12 @@ XMOD_API int xmod_block_fwd(const xmod_dims* dims, int n_per_seq, const void* xs
  *   gate XMOD: x[b, idx[b,j]] += varsigma * r_sel[b,j] * (a + f)
  *   gate MOD:  x[b, idx[b,j]] += a + r_sel[b,j] * f
  * a, f: [B * n, d] (dtype). f may be NULL under XMOD, in which case `a` holds a + f.
- * Rows not in idx are not touched. */
+ * Rows not in idx are not touched. The positions are checked as for xmod_gather: a
+ * bad row is skipped (no stream row is written for it) and reported through
+ * status_out (a device int, or NULL) as XMOD_ERR_DEVICE_CHECK. */
 XMOD_API int xmod_gated_scatter(const xmod_dims* dims, int K, void* x_inout, const int32_t* idx,
                        const float* r_sel, const void* a, const void* f, float varsigma,
-                       xmod_gate gate, void* stream);
+                       xmod_gate gate, int* status_out, void* stream);
 
 /* One layer in place on x [B, T, d]. Sparse: router + top-(T/K) + block on the
  * selected tokens + gated residual; unselected rows untouched. Dense: the block on

@@ -293,6 +293,16 @@ int fullkv_attention(const Ctx& c, const xmod_dims* dm, const Layout& L, void* w
   return XMOD_OK;
 }
 
+// The standalone gather + RMSNorm1 kernel and a GEMM on its compact output (default),
+// or the gathered RMSNorm inside the q|k|v GEMM's operand load: the environment variable
+// XMOD_GATHER_FUSED=1, read at every call, selects the latter (both compute the block;
+// they differ only in rounding order). The fused form measured slower on GB300 (see the
+// gathered-RMSNorm GEMM in gemm_tc.cu), so it is not the default.
+bool gather_fused_enabled() {
+  const char* v = getenv("XMOD_GATHER_FUSED");
+  return v && v[0] == '1' && v[1] == '\0';
+}
+
 int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int n,
               const void* x_src, const int32_t* idx, const xmod_layer_weights* w, void* a_out,
               void* f_out, bool scatter, void* x_inout, const float* r_sel, int gate,
@@ -344,9 +354,6 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
       const int st = fullkv_attention(c, dm, L, ws, n, x_src, idx, w);
       if (st) return st;
     } else {
-      // 1. gather + RMSNorm1
-      XMOD_RUN("gather_rmsnorm",
-               launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms1, dm->rms_eps, u, rm));
       // 2. q, k, v projections into one [M, qkv_w] buffer
       char* vt = at(ws, L.vt);
       const bool tc_attn = tc && attention_tc_supported(hd, n, qkv_w);
@@ -366,6 +373,26 @@ int run_block(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int 
       pq.M = M; pq.N = qkv_w; pq.K = d; pq.A = u; pq.lda = d; pq.ldb = d;
       pq.B[0] = w->wq; pq.B[1] = w->wk; pq.B[2] = w->wv; pq.nB = 3;
       pq.split[0] = qw; pq.split[1] = qw + kw;
+      // 1. gather + RMSNorm1: for the routed rows of a stream (idx given, a fixed count per
+      // sequence) inside the q|k|v GEMM's operand load, else a gathered copy u
+      bool fused_gather = false;
+      if (tc && idx && !rg && gather_fused_enabled()) {
+        GemmTcProblem pg = pq;
+        pg.A = x_src;
+        pg.gather_idx = idx;
+        pg.gather_T = T;
+        pg.gather_n = n;
+        pg.gather_rows = (int64_t)B * T;
+        pg.gather_gamma = w->rms1;
+        pg.gather_eps = dm->rms_eps;
+        if (gemm_tc_supported(pg, e)) {
+          pq = pg;
+          fused_gather = true;
+        }
+      }
+      if (!fused_gather)
+        XMOD_RUN("gather_rmsnorm", launch_gather_rmsnorm(c, dt, B, T, n, d, x_src, idx, w->rms1,
+                                                         dm->rms_eps, u, rm));
       const bool tc_qkv = tc && gemm_tc_supported(pq, e);
       if (rg) {
         if (!tc_qkv || !tc_attn) return XMOD_ERR_UNSUPPORTED;
@@ -817,10 +844,11 @@ int xmod_topk(const xmod_dims* dm, int K, const float* logits, int32_t* idx, flo
 }
 
 int xmod_gather(const xmod_dims* dm, int K, const void* x, const int32_t* idx, void* xs,
-                void* stream) {
+                int* status_out, void* stream) {
   if (!dims_ok(dm) || K <= 0 || K > dm->T) return XMOD_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(idx) || !aligned16(xs)) return XMOD_ERR_INVALID_ARG;
-  Ctx c{(cudaStream_t)stream, nullptr};
+  if (!aligned16(x) || !aligned16(idx) || !aligned16(xs) || ((uintptr_t)status_out & 3u))
+    return XMOD_ERR_INVALID_ARG;
+  Ctx c{(cudaStream_t)stream, status_out};
   XMOD_RUN("gather", launch_gather(c, dm->dtype, dm->B, dm->T, dm->T / K, dm->d, x, idx, xs));
   return XMOD_OK;
 }
@@ -841,23 +869,32 @@ int xmod_block_fwd(const xmod_dims* dm, int n_per_seq, const void* xs, const int
   st = make_ctx(dm, ws, L, stream, c);
   if (st) return st;
   // Without idx the rows come from the compact buffer: view it as B sequences of
-  // n_per_seq tokens.
+  // n_per_seq tokens. With idx, the caller's positions are checked on the device first
+  // and a copy with every bad row clamped into range is used, so no access leaves the
+  // stream; the status word records the bad rows.
   xmod_dims local = *dm;
   if (!idx) local.T = n_per_seq;
-  return run_block(c, &local, L, ws, n_per_seq, xs, idx, w, a_out, f_out, false, nullptr,
+  const int32_t* use_idx = idx;
+  if (idx) {
+    int32_t* safe = (int32_t*)at(ws, L.idx);
+    XMOD_RUN("idx_check", launch_idx_sanitize(c, dm->B, dm->T, n_per_seq, idx, safe));
+    use_idx = safe;
+  }
+  return run_block(c, &local, L, ws, n_per_seq, xs, use_idx, w, a_out, f_out, false, nullptr,
                    nullptr, -1);
 }
 
 int xmod_gated_scatter(const xmod_dims* dm, int K, void* x_inout, const int32_t* idx,
                        const float* r_sel, const void* a, const void* f, float varsigma,
-                       xmod_gate gate, void* stream) {
+                       xmod_gate gate, int* status_out, void* stream) {
   if (!dims_ok(dm) || K <= 0 || K > dm->T) return XMOD_ERR_INVALID_ARG;
   if (gate != XMOD_GATE_XMOD && gate != XMOD_GATE_MOD) return XMOD_ERR_INVALID_ARG;
   if (!aligned16(x_inout) || !aligned16(idx) || !aligned16(r_sel) || !aligned16(a) ||
       !aligned16_or_null(f) || !isfinite(varsigma))
     return XMOD_ERR_INVALID_ARG;
   if (!f && gate != XMOD_GATE_XMOD) return XMOD_ERR_INVALID_ARG;
-  Ctx c{(cudaStream_t)stream, nullptr};
+  if ((uintptr_t)status_out & 3u) return XMOD_ERR_INVALID_ARG;
+  Ctx c{(cudaStream_t)stream, status_out};
   XMOD_RUN("gated_scatter", launch_gated_scatter(c, dm->dtype, dm->B, dm->T, dm->T / K, dm->d,
                                                  x_inout, idx, r_sel, a, f, varsigma, (int)gate));
   return XMOD_OK;

@@ -13,6 +13,12 @@
 //               row, 32 columns at a time), the fused epilogue math, and 16-byte global
 //               loads and stores of that row segment. The other accumulator meanwhile
 //               receives the next tile's MMAs.
+// Gathered-RMSNorm variant (q | k | v of a sparse layer): the A tile rows are the
+// selected tokens' rows of the residual stream itself, brought in by TMA gather4 (four
+// rows per copy), and four more warps apply RMSNorm1 on the way: each thread owns one
+// row of the A tile, multiplies it by the gain in shared memory before the MMA reads it
+// and sums its squares over the k-blocks; the epilogue scales the row's outputs by
+// 1 / rms (RMSNorm(x) g . W^T = (1 / rms) (x g) . W^T), so no gathered copy is written.
 // Fused epilogues: plain store (optionally q | k | v from three weight tensors, with
 // v written transposed for the attention kernel), O-projection (a in bf16; h = x_sel
 // + a in fp32 when a separate RMSNorm needs it, or h * rms2 and h's sums of squares
@@ -43,6 +49,10 @@ constexpr int BM = 128, BK = 64;
 #endif
 constexpr int EPI_WARPS = XMOD_EPI_WARPS;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+// RMSNorm warps of the gathered-A variant (one thread per A tile row), and the shared
+// memory they add: 1 / rms of both accumulators' rows, then their barriers.
+constexpr int XF_WARPS = 4;
+constexpr int XF_SMEM = 2 * 128 * 4 + 256;
 
 template <int BN>
 struct Cfg {
@@ -64,6 +74,11 @@ struct TcArgs {
   int ksplit;              // k slices per output tile (ROUTER only; else 1)
   const int32_t* M_dev;    // if set, the rows are min(*M_dev, M), read on the device
   int v8;                  // epilogue row segments may use 32-byte accesses
+  // gathered-A variant: row m of A is row (m / g_n) * g_T + g_idx[m] of the stream
+  const int32_t* g_idx;
+  int g_T, g_n;
+  const __nv_bfloat16* g_gamma;
+  float g_eps;
   // Stream-K (see Work): the tiles' k-blocks split evenly over the CTAs
   int sk;
   int64_t units;           // tiles x k-blocks
@@ -315,6 +330,15 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* p, const float (&v)[
 #ifndef XMOD_PAIR_MIN_WAVES
 #define XMOD_PAIR_MIN_WAVES 6
 #endif
+// Cost per column of a 256 x 256 pair tile (per SM, the single-CTA tiles' units), and
+// the margin by which the pair estimate must beat the best single-CTA one below
+// XMOD_PAIR_MIN_WAVES.
+#ifndef XMOD_COST_PAIR
+#define XMOD_COST_PAIR 0.82
+#endif
+#ifndef XMOD_PAIR_MARGIN
+#define XMOD_PAIR_MARGIN 0.10
+#endif
 // 0 disables the CTA-pair kernels.
 #ifndef XMOD_GEMM_PAIRS
 #define XMOD_GEMM_PAIRS 1
@@ -529,11 +553,12 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, in
   }
 }
 
-// Epilogue of one tile for this warp's 32-row slab [wrow0, wrow0 + 32).
-template <int BN, int MODE>
+// Epilogue of one tile for this warp's 32-row slab [wrow0, wrow0 + 32). RS: every
+// accumulator value of this lane's row is scaled by rscale first (gathered RMSNorm).
+template <int BN, int MODE, bool RS = false>
 __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0, int lane,
                                               int n_blk, uint32_t t_row, int part, int nparts,
-                                              int ks = 0) {
+                                              int ks = 0, float rscale = 1.0f) {
   const Epilogue& e = a.e;
   constexpr bool swiglu = MODE == EPI_SWIGLU;
   // the row this lane owns in TMEM: its stream row and gate
@@ -592,6 +617,10 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0,
     } else {
       tmem_ld32(t_row + c * 32, v);
       tmem_ld_wait();
+      if (RS) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= rscale;
+      }
     }
     const int col0 = col_tile0 + c * 32;
     if (MODE == EPI_STORE && e.vt && col0 >= e.vt_col0) {
@@ -620,12 +649,13 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0,
   }
 }
 
-template <int BN, int MODE>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int BN, int MODE, bool GATHER = false>
+__global__ void __launch_bounds__(NUM_THREADS + (GATHER ? 32 * XF_WARPS : 0), 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
                const TcArgs args) {
   using C = Cfg<BN>;
+  static_assert(!GATHER || MODE == EPI_STORE, "the gathered RMSNorm feeds a plain store");
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -642,6 +672,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #define ACC_FULL(a) (sBar + 8u * (2 * C::STAGES + (a)))
 #define ACC_EMPTY(a) (sBar + 8u * (2 * C::STAGES + 2 + (a)))
 #define EPI_MEET (sBar + 8u * (2 * C::STAGES + 4))
+  // gathered-A variant only: 1 / rms of the rows of accumulator a at sXf + 512 a, then
+  // XFORM(s) (stage s holds RMSNorm-gained rows) and RSTD_FULL(a) (1 / rms of a's rows
+  // written)
+  const uint32_t sXf = sBar + 256;
+  float* rstd_buf = reinterpret_cast<float*>(gbase + (sXf - base));
+#define XFORM(s) (sXf + 1024u + 8u * (s))
+#define RSTD_FULL(a) (sXf + 1024u + 8u * (C::STAGES + (a)))
+  static_assert(!GATHER || 8 * (C::STAGES + 2) <= XF_SMEM - 1024, "RMSNorm barriers overflow");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = (args.K + BK - 1) / BK;
@@ -650,10 +688,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(FULL(s), 1);
       mbar_init(EMPTY(s), 1);
+      if (GATHER) mbar_init(XFORM(s), XF_WARPS);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(ACC_FULL(a), 1);
       mbar_init(ACC_EMPTY(a), 32 * EPI_WARPS);
+      if (GATHER) mbar_init(RSTD_FULL(a), XF_WARPS);
     }
     mbar_init(EPI_MEET, EPI_WARPS);
     *abort_flag = 0;
@@ -671,7 +711,49 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   pdl_wait();  // everything above overlapped the previous kernel's tail
   const Extent ext = launch_extent(args, BM);
 
-  if (warp == 0) {
+  if (warp == 0 && GATHER) {
+    // The whole warp loads: lane l gathers rows 4l .. 4l+3 of each A tile, lane 0 also
+    // the B tile.
+    int it = 0;
+    Work w;
+    bool run = true;
+    for (int i = 0; run && work_at(args, ext, nk, i, w); ++i) {
+      int m_blk, n_blk;
+      tile_coords(args, ext.tiles_m, w.tile, m_blk, n_blk);
+      const int m0 = m_blk * BM;
+      int r[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {   // rows past M repeat a valid row; never stored
+        const int m = m0 + 4 * lane + q;
+        r[q] = m < ext.M ? (m / args.g_n) * args.g_T + args.g_idx[m] : 0;
+      }
+      const CUtensorMap* mp = &tmB0;
+      int brow = n_blk * BN;
+      if (brow >= args.n_split2) {
+        mp = &tmB2;
+        brow -= args.n_split2;
+      } else if (brow >= args.n_split1) {
+        mp = &tmB1;
+        brow -= args.n_split1;
+      }
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+        const int s = it % C::STAGES;
+        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+        int ok = 1;
+        if (lane == 0) {
+          ok = !*abort_flag && mbar_wait(EMPTY(s), ph ^ 1u, abort_flag, args.status);
+          if (ok) mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          run = false;
+          break;
+        }
+        tma_gather4(sA + s * C::A_BYTES + lane * 512, &tmA, FULL(s), kb * BK, r[0], r[1], r[2],
+                    r[3]);
+        if (lane == 0) tma_load_2d(sB + s * C::B_BYTES, mp, FULL(s), kb * BK, brow);
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       int it = 0;
       Work w;
@@ -723,7 +805,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const int s = it % C::STAGES;
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
-          if (!mbar_wait(FULL(s), ph, abort_flag, args.status)) {
+          if (!mbar_wait(GATHER ? XFORM(s) : FULL(s), ph, abort_flag, args.status)) {
             ok = false;
             break;
           }
@@ -738,6 +820,73 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!ok) break;
         mma_commit(ACC_FULL(acc));
       }
+    }
+  } else if (GATHER && warp >= 2 + EPI_WARPS) {
+    // RMSNorm1 on the gathered rows: this thread owns row xr of every A tile. Each stage:
+    // the row's 64 columns times the gain, back in place (the 128-byte swizzle puts
+    // 16-byte chunk c of row r at chunk c ^ (r & 7)), and their squares summed in column
+    // order. After a tile's last k-block: 1 / rms for the epilogue.
+    const int xr = (warp - 2 - EPI_WARPS) * 32 + lane;
+    const float inv_d = 1.0f / (float)args.K;
+    int it = 0;
+    Work w;
+    for (int lt = 0; work_at(args, ext, nk, lt, w); ++lt) {
+      const int acc = lt & 1;
+      const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+      float ss = 0.0f;
+      bool ok = true;
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+        const int s = it % C::STAGES;
+        const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
+        if (!mbar_wait(FULL(s), ph, abort_flag, args.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* row = gbase + (sA - base) + s * C::A_BYTES + xr * 128;
+        // columns past K are the map's zero fill: nothing to add or scale there
+        const int nc = min(8, (args.K - kb * BK) / 8);
+        // two halves of four 16-byte chunks, every load of a half issued before its math
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint4 v[4], g[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int cc = 4 * h + c;
+            if (cc < nc) {
+              v[c] = *reinterpret_cast<const uint4*>(row + ((cc ^ (xr & 7)) << 4));
+              g[c] = __ldg(reinterpret_cast<const uint4*>(args.g_gamma + kb * BK + 8 * cc));
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int cc = 4 * h + c;
+            if (cc < nc) {
+              uint32_t* vw = reinterpret_cast<uint32_t*>(&v[c]);
+              const uint32_t* gw = reinterpret_cast<const uint32_t*>(&g[c]);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float2 xf =
+                    __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vw[q]));
+                const float2 gf =
+                    __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[q]));
+                ss = fmaf(xf.x, xf.x, ss);
+                ss = fmaf(xf.y, xf.y, ss);
+                vw[q] = pack_bf16x2(xf.x * gf.x, xf.y * gf.y);
+              }
+              *reinterpret_cast<uint4*>(row + ((cc ^ (xr & 7)) << 4)) = v[c];
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(XFORM(s));
+      }
+      if (!ok) break;
+      // the buffer of accumulator acc is free once the epilogue of tile lt - 2 is done
+      if (!mbar_wait(ACC_EMPTY(acc), aph ^ 1u, abort_flag, args.status)) break;
+      rstd_buf[acc * 128 + xr] = 1.0f / sqrtf(ss * inv_d + args.g_eps);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(RSTD_FULL(acc));
     }
   } else {
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 belong to this warp
@@ -768,8 +917,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           ok = epi_meet(EPI_MEET, meets, lane, abort_flag, args.status) && !*abort_flag;
           if (ok) sk_add_partial<BN>(args, quad * 32 + lane, t_row, part, nparts);
         }
-        if (ok)
+        if (GATHER) {
+          ok = ok && mbar_wait(RSTD_FULL(acc), aph, abort_flag, args.status);
+          if (ok)
+            epilogue_tile<BN, MODE, true>(args, ext.M, wrow0, lane, n_blk, t_row, part, nparts,
+                                          w.ks, rstd_buf[acc * 128 + quad * 32 + lane]);
+        } else if (ok) {
           epilogue_tile<BN, MODE>(args, ext.M, wrow0, lane, n_blk, t_row, part, nparts, w.ks);
+        }
       }
       tc_fence_before();
       mbar_arrive(ACC_EMPTY(acc));
@@ -795,6 +950,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #undef ACC_FULL
 #undef ACC_EMPTY
 #undef EPI_MEET
+#undef XFORM
+#undef RSTD_FULL
 }
 
 // ---------------------------------------------------------------- CTA-pair variant
@@ -1005,7 +1162,16 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
            CUtensorMap& mA, CUtensorMap& mB0, CUtensorMap& mB1, CUtensorMap& mB2, TcArgs& a) {
   memset(&mB1, 0, sizeof(mB1));
   memset(&mB2, 0, sizeof(mB2));
-  if (!make_map(&mA, p.A, p.K, p.M, p.lda, BM)) return false;
+  a.g_idx = p.gather_idx;
+  a.g_T = p.gather_T;
+  a.g_n = p.gather_n;
+  a.g_gamma = (const __nv_bfloat16*)p.gather_gamma;
+  a.g_eps = p.gather_eps;
+  if (p.gather_idx) {   // the stream's rows, one-row boxes for gather4
+    if (!make_map(&mA, p.A, p.K, p.gather_rows, p.lda, 1)) return false;
+  } else if (!make_map(&mA, p.A, p.K, p.M, p.lda, BM)) {
+    return false;
+  }
   a.M = p.M;
   a.M_dev = p.M_dev;
   a.ksplit = p.ksplit > 1 ? p.ksplit : 1;
@@ -1102,6 +1268,21 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, b
   }
   void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
             const TcArgs) = nullptr;
+  if constexpr (BN != 32) {
+    if (p.gather_idx) {   // RMSNorm of gathered rows in the A operand (STORE only)
+      if (e.kind != EPI_STORE || sk) return cudaErrorInvalidValue;
+      k = gemm_tc_kernel<BN, EPI_STORE, true>;
+      static bool gattr = false;
+      if (!gattr) {
+        cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               Cf::SMEM + XF_SMEM);
+        if (err != cudaSuccess) return err;
+        gattr = true;
+      }
+      return launch_pdl(k, dim3(grid), dim3(NUM_THREADS + 32 * XF_WARPS), Cf::SMEM + XF_SMEM,
+                        c.stream, mA, mB0, mB1, mB2, a);
+    }
+  }
   if constexpr (BN == 32) {
     k = gemm_tc_kernel<BN, EPI_ROUTER>;
   } else {
@@ -1189,6 +1370,11 @@ bool bn_ok(const GemmTcProblem& p, const Epilogue& e, int bn) {
 bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e) {
   if (!tma_available()) return false;
   if (p.M <= 0 || p.N <= 0 || p.K <= 0) return false;
+  if (p.gather_idx &&
+      (e.kind != EPI_STORE || p.M_dev || p.gather_n <= 0 || p.gather_T < p.gather_n ||
+       p.gather_rows <= 0 || p.lda != p.K || !p.gather_gamma ||
+       ((uintptr_t)p.gather_gamma & 15)))
+    return false;
   if (p.K % 8 || p.lda % 8 || p.ldb % 8) return false;
   if (p.N % 8 && e.kind != EPI_ROUTER) return false;   // the others store 8-column groups
   if (p.b_rows && (p.b_rows < p.N || p.nB != 1)) return false;
@@ -1223,20 +1409,8 @@ int stream_k_mode() {
 
 cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
   if (e.kind == EPI_ROUTER) return launch_bn<32>(c, p, e);
-  // CTA pairs on 256 x 256 tiles when there are enough of them. Measured on GB300
-  // against the best single-CTA tiling (A4K8 block, d = 1536): 256 x 256 pair tiles cost
-  // 18% less time per tile but about 5 us more per launch, so they win from six waves
-  // up (gate/up at M = 4096: 58.7 -> 53.9 us; every dense-layer GEMM at M = 32768:
-  // 7-17%) and lose below three (q|k|v, o-proj, down at M = 4096: 3-12%). Narrower
-  // pair tiles were slower than single-CTA tiles of the same width.
-  if (XMOD_GEMM_PAIRS && p.M > BM && !p.M_dev && bn_ok(p, e, 256)) {
-    const long tiles_m = (p.M + 2 * BM - 1) / (2 * BM);
-    const int cols = e.kind == EPI_SWIGLU ? 128 : 256;
-    const long tiles = tiles_m * ((p.N + cols - 1) / cols);
-    if (tiles >= (long)pair_min_waves() * max_pairs<256>()) return launch_bn2<256>(c, p, e);
-  }
   const int sms = sm_count();
-  // Otherwise the tile width with the shortest estimated time: waves x tile width,
+  // The single-CTA tile width with the shortest estimated time: waves x tile width,
   // with narrower tiles charged for their higher shared-memory traffic per FLOP.
   const int tiles_m = (p.M + BM - 1) / BM;
   const int widths[3] = {256, 192, 128};
@@ -1253,6 +1427,31 @@ cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue&
       best = bn;
       best_cost = cost;
     }
+  }
+  // CTA pairs on 256 x 256 tiles: each SM of a pair streams half of the B tile, so a
+  // pair tile costs about 18% less time per SM than a 128 x 256 single-CTA tile (cost
+  // XMOD_COST_PAIR per column in the units above), for about 5 us more per launch.
+  // They run from six waves up (gate/up at M = 4096, every dense-layer GEMM), and below
+  // that when the same waves-times-width estimate puts them at least XMOD_PAIR_MARGIN
+  // ahead of the best single-CTA tiling. Measured on GB300 at M = 4096: with d = 2048,
+  // d_ff = 5632 (2 pair waves against 2 single waves of 256) down 83.6 -> 70.2 us,
+  // q|k|v 43.8 -> 40.2, o-proj 41.6 -> 39.4; with d = 1536, d_ff = 4096 (a second pair
+  // wave on a quarter of the pairs against 192-wide single tiles) pairs lost 2-4 us on
+  // the o-proj and down GEMMs, which the margin keeps single.
+  if (p.gather_idx) {   // the gathered-RMSNorm variant exists for single-CTA tiles only
+    if (best == 256) return launch_bn<256>(c, p, e);
+    if (best == 192) return launch_bn<192>(c, p, e);
+    return launch_bn<128>(c, p, e);
+  }
+  if (XMOD_GEMM_PAIRS && p.M > BM && !p.M_dev && bn_ok(p, e, 256)) {
+    const long ptiles_m = (p.M + 2 * BM - 1) / (2 * BM);
+    const int cols = e.kind == EPI_SWIGLU ? 128 : 256;
+    const long tiles = ptiles_m * ((p.N + cols - 1) / cols);
+    const long pairs = max_pairs<256>();
+    const double pair_cost = (double)((tiles + pairs - 1) / pairs) * 256 * XMOD_COST_PAIR;
+    if (tiles >= (long)pair_min_waves() * pairs ||
+        (best > 0 && pair_cost * (1.0 + XMOD_PAIR_MARGIN) <= best_cost))
+      return launch_bn2<256>(c, p, e);
   }
   // Stream-K at 256-wide tiles, on request only: on the A4K8 block's sparse-layer GEMMs
   // (1.3-2.1 waves) it measured 10-50% slower than the tiling above -- storing and

@@ -157,6 +157,11 @@ cudaError_t launch_rmsnorm_f32in(const Ctx& c, xmod_dtype dt, int64_t M, int d, 
                                  const int32_t* M_dev = nullptr);
 
 // Gated residual in place, see xmod_gated_scatter. gate < 0: dense update x + a + f.
+// Copy of the caller's positions idx [B * n] with every row that is out of [0, T) or
+// not above the previous row of its sequence clamped into range, recorded as
+// XMOD_ERR_DEVICE_CHECK in the status word.
+cudaError_t launch_idx_sanitize(const Ctx& c, int B, int T, int n, const int32_t* idx,
+                                int32_t* out);
 cudaError_t launch_gated_scatter(const Ctx& c, xmod_dtype dt, int B, int T, int n, int d,
                                  void* x, const int32_t* idx, const float* r_sel, const void* a,
                                  const void* f, float varsigma, int gate);
@@ -255,6 +260,16 @@ struct GemmTcProblem {
   // ROUTER only: the K range split in ksplit slices (at most the number of 64-deep
   // k-blocks); slice k's partial sums go to the output plane k (Epilogue::plane apart).
   int ksplit = 1;
+  // RMSNorm of gathered rows fused into the A operand (STORE epilogue only): row m of A
+  // is row (m / gather_n) * gather_T + gather_idx[m] of the [gather_rows, K] matrix A
+  // (the residual stream, lda = K), and the GEMM computes
+  //   C[m, :] = rstd_m * (x_m * gather_gamma) . B^T,  rstd_m = (mean(x_m^2) + eps)^-1/2,
+  // i.e. RMSNorm(x_m) * gamma times B^T, without a gathered copy of the rows.
+  const int32_t* gather_idx = nullptr;
+  int gather_T = 0, gather_n = 0;
+  int64_t gather_rows = 0;
+  const void* gather_gamma = nullptr;
+  float gather_eps = 0.f;
 };
 bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e);
 cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e);

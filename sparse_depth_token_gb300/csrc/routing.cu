@@ -207,14 +207,23 @@ cudaError_t launch_router(const Ctx& c, xmod_dtype dt, int64_t rows, int d, cons
 // ================================================================ top-(T/K)
 //
 // One CTA per sequence. Logits become order-preserving 32-bit keys in shared
-// memory (-0 folded onto +0, so equal values compare equal). A 4-pass, 8-bit
-// radix select finds the n-th largest key K* and how many of the keys equal to
-// K* are taken; since ties go to the lower position, those are the first
-// `remaining` equal keys in position order. A warp-ballot compaction then emits
-// the selected positions in ascending order.
+// memory (-0 folded onto +0, so equal values compare equal). A radix select over
+// three digits (12, 12 and 8 bits from the top) finds the n-th largest key K* and
+// how many of the keys equal to K* are taken; since ties go to the lower position,
+// those are the first `remaining` equal keys in position order. Each lane then
+// owns a run of consecutive positions: one warp scan and one block scan of the
+// per-lane counts of keys above and equal to K* give every selected key its output
+// slot, and the selected positions come out in ascending order.
+//
+// The first digit's histogram is counted while the logits are loaded (16-byte loads
+// of every plane); the later digits count only the keys that share the digits found
+// so far. A 12-bit first digit (sign, exponent and three mantissa bits) spreads router
+// logits over tens of bins, where an 8-bit one puts most of them in two or three and
+// the shared-memory atomics on those bins serialise.
 
 constexpr int TOPK_THREADS = 1024;
 constexpr int TOPK_MAX_T = 48 * 1024;  // 192 KB of keys in shared memory
+constexpr int TOPK_BINS = 4096;        // 12-bit digits
 
 int topk_max_T() { return TOPK_MAX_T; }
 
@@ -228,6 +237,84 @@ __device__ __forceinline__ uint32_t order_key(float v) {
 // the selected tokens); longer sequences read them again from global memory.
 constexpr int TOPK_CACHE_MAX_T = 24 * 1024;
 
+// Adds to hist[d] the number of keys of src[0, len) whose bits under `mask` equal
+// `prefix`, d = (key >> shift) & dmask.
+__device__ __forceinline__ void radix_count(const uint32_t* src, int len, uint32_t mask,
+                                            uint32_t prefix, int shift, uint32_t dmask,
+                                            uint32_t* hist) {
+  for (int t = threadIdx.x; t < len; t += TOPK_THREADS) {
+    const uint32_t k = src[t];
+    if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & dmask], 1u);
+  }
+}
+
+// Scans hist[0, NB) from the largest digit down and finds the digit D at which the
+// running count reaches `remaining`; every thread returns D and the count still to
+// take among the keys with digit D. Thread i owns digits NB-1-i*P .. NB-P-i*P.
+template <int NB>
+__device__ __forceinline__ void radix_find(const uint32_t* hist, uint32_t remaining,
+                                           uint32_t* warp_sums, uint32_t* result,
+                                           uint32_t* digit, uint32_t* rem_out) {
+  constexpr int P = NB >= TOPK_THREADS ? NB / TOPK_THREADS : 1;
+  constexpr int ACTIVE = NB / P;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t c[P], tot = 0;
+#pragma unroll
+  for (int e = 0; e < P; ++e) {
+    c[e] = threadIdx.x < ACTIVE ? hist[NB - 1 - (threadIdx.x * P + e)] : 0u;
+    tot += c[e];
+  }
+  uint32_t inc = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_sums[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t v = warp_sums[lane];
+    uint32_t wi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    warp_sums[lane] = wi - v;   // exclusive prefix of the warps above
+  }
+  __syncthreads();
+  const uint32_t excl = warp_sums[warp] + inc - tot;
+  if (threadIdx.x < ACTIVE && excl < remaining && remaining <= excl + tot) {
+    uint32_t run = excl;
+#pragma unroll
+    for (int e = 0; e < P; ++e) {
+      if (run + c[e] >= remaining) {
+        result[0] = (uint32_t)(NB - 1 - (threadIdx.x * P + e));
+        result[1] = remaining - run;
+        break;
+      }
+      run += c[e];
+    }
+  }
+  __syncthreads();
+  *digit = result[0];
+  *rem_out = result[1];
+}
+
+// The ranked logit of position t from its planes' sum v: minus the block's
+// accumulated token-choice bias; its key goes to shared memory and into the first
+// digit's histogram.
+__device__ __forceinline__ void topk_take(int t, float v, const int32_t* cnt, float bias_step,
+                                          uint32_t* keys, float* lsh, uint32_t* hist,
+                                          int* bad) {
+  const float x = cnt ? v - bias_step * (float)cnt[t] : v;
+  if (!isfinite(x)) *bad = 1;
+  const uint32_t k = order_key(x);
+  keys[t] = k;
+  if (lsh) lsh[t] = x;
+  atomicAdd(&hist[k >> 20], 1u);
+}
+
 // TRACK: the token-choice bias state / statistics of tr are used (else tr is ignored
 // and the kernel is the plain top-(T/K)).
 template <bool TRACK>
@@ -239,9 +326,9 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
   pdl_wait();
   extern __shared__ uint32_t keys[];
   float* lsh = T <= TOPK_CACHE_MAX_T ? reinterpret_cast<float*>(keys + T) : nullptr;
-  __shared__ uint32_t hist[2][256];
+  __shared__ uint32_t hist[TOPK_BINS];
   __shared__ uint32_t scan_sh[2][32];
-  __shared__ uint32_t sh_prefix[2], sh_remaining[2];
+  __shared__ uint32_t sh_result[2];
   __shared__ int sh_bad;
   __shared__ uint32_t sh_stat[3];   // threshold-selected, agreeing, also selected before
   const int b = blockIdx.x;
@@ -251,106 +338,142 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
   int32_t* last = tr.last ? tr.last + (int64_t)b * T : nullptr;
   if (threadIdx.x == 0) sh_bad = 0;
   if (threadIdx.x < 3) sh_stat[threadIdx.x] = 0u;
-  for (int i = threadIdx.x; i < 256; i += TOPK_THREADS) hist[0][i] = 0u;
+  for (int i = threadIdx.x; i < TOPK_BINS; i += TOPK_THREADS) hist[i] = 0u;
   __syncthreads();
   // The logit this layer ranks: s (the sum of its planes, in order) minus the block's
-  // accumulated token-choice bias. Four positions per thread at a time, every plane's
-  // load issued before any is used.
-  for (int t0 = threadIdx.x; t0 < T; t0 += 4 * TOPK_THREADS) {
-    float v[4];
+  // accumulated token-choice bias. With T a multiple of 4 every plane of the sequence
+  // starts on a 16-byte boundary: four positions per load, four loads per plane in
+  // flight, every plane's loads issued before any is used.
+  if ((T & 3) == 0) {
+    const int T4 = T >> 2;
+    const float4* s4 = reinterpret_cast<const float4*>(sb);
+    const int64_t plane4 = plane >> 2;
+    for (int q0 = threadIdx.x; q0 < T4; q0 += 4 * TOPK_THREADS) {
+      float4 v[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = t0 + i * TOPK_THREADS;
-      v[i] = t < T ? sb[t] : 0.0f;
+      for (int i = 0; i < 4; ++i) {
+        const int q = q0 + i * TOPK_THREADS;
+        v[i] = q < T4 ? s4[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      for (int k = 1; k < nplanes; ++k) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int q = q0 + i * TOPK_THREADS;
+          if (q < T4) {
+            const float4 u = s4[k * plane4 + q];
+            v[i].x += u.x;
+            v[i].y += u.y;
+            v[i].z += u.z;
+            v[i].w += u.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int q = q0 + i * TOPK_THREADS;
+        if (q < T4) {
+          float4 x = v[i];
+          if (cnt) {
+            x.x -= tr.bias_step * (float)cnt[4 * q];
+            x.y -= tr.bias_step * (float)cnt[4 * q + 1];
+            x.z -= tr.bias_step * (float)cnt[4 * q + 2];
+            x.w -= tr.bias_step * (float)cnt[4 * q + 3];
+          }
+          if (!isfinite(x.x) || !isfinite(x.y) || !isfinite(x.z) || !isfinite(x.w)) sh_bad = 1;
+          const uint4 k = make_uint4(order_key(x.x), order_key(x.y), order_key(x.z), order_key(x.w));
+          reinterpret_cast<uint4*>(keys)[q] = k;
+          if (lsh) reinterpret_cast<float4*>(lsh)[q] = x;
+          atomicAdd(&hist[k.x >> 20], 1u);
+          atomicAdd(&hist[k.y >> 20], 1u);
+          atomicAdd(&hist[k.z >> 20], 1u);
+          atomicAdd(&hist[k.w >> 20], 1u);
+        }
+      }
     }
-    for (int k = 1; k < nplanes; ++k) {
+  } else {
+    for (int t0 = threadIdx.x; t0 < T; t0 += 4 * TOPK_THREADS) {
+      float v[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int t = t0 + i * TOPK_THREADS;
-        if (t < T) v[i] += sb[k * plane + t];
+        v[i] = t < T ? sb[t] : 0.0f;
       }
-    }
+      for (int k = 1; k < nplanes; ++k) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = t0 + i * TOPK_THREADS;
-      if (t < T) {
-        const float x = cnt ? v[i] - tr.bias_step * (float)cnt[t] : v[i];
-        if (!isfinite(x)) sh_bad = 1;
-        keys[t] = order_key(x);
-        if (lsh) lsh[t] = x;
+        for (int i = 0; i < 4; ++i) {
+          const int t = t0 + i * TOPK_THREADS;
+          if (t < T) v[i] += sb[k * plane + t];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int t = t0 + i * TOPK_THREADS;
+        if (t < T) topk_take(t, v[i], cnt, tr.bias_step, keys, lsh, hist, &sh_bad);
       }
     }
   }
   __syncthreads();
   if (sh_bad && threadIdx.x == 0) report_status(status, XMOD_ERR_DEVICE_CHECK);
 
-  // Radix select, 8 bits per pass from the top. Histograms and results alternate
-  // between two buffers, so one pass needs two barriers: the next pass's histogram
-  // is cleared while this one is counted.
-  uint32_t prefix = 0u, mask = 0u, remaining = (uint32_t)n;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass, cur = pass & 1;
-    for (int t = threadIdx.x; t < T; t += TOPK_THREADS) {
-      const uint32_t k = keys[t];
-      if ((k & mask) == prefix) atomicAdd(&hist[cur][(k >> shift) & 0xffu], 1u);
-    }
-    if (pass < 3)
-      for (int i = threadIdx.x; i < 256; i += TOPK_THREADS) hist[cur ^ 1][i] = 0u;
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns digits 255-8l .. 248-8l (descending)
-      uint32_t c8[8], tot = 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        c8[e] = hist[cur][255 - (lane * 8 + e)];
-        tot += c8[e];
-      }
-      uint32_t inc = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
-      }
-      const uint32_t excl = inc - tot;
-      if (excl < remaining && remaining <= inc) {
-        uint32_t run = excl;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (run + c8[e] >= remaining) {
-            const uint32_t D = 255u - (uint32_t)(lane * 8 + e);
-            sh_prefix[cur] = prefix | (D << shift);
-            sh_remaining[cur] = remaining - run;
-            break;
-          }
-          run += c8[e];
-        }
-      }
-    }
-    __syncthreads();
-    prefix = sh_prefix[cur];
-    remaining = sh_remaining[cur];
-    mask |= 0xffu << shift;
-  }
-  const uint32_t kth = prefix;
+  // Digit 1 (bits 31..20) was counted during the load.
+  uint32_t d1, remaining;
+  radix_find<TOPK_BINS>(hist, (uint32_t)n, scan_sh[0], sh_result, &d1, &remaining);
+  uint32_t prefix = d1 << 20, mask = 0xfff00000u;
+  for (int i = threadIdx.x; i < TOPK_BINS; i += TOPK_THREADS) hist[i] = 0u;
+  __syncthreads();
+  // Digit 2: bits 19..8 among the keys that match digit 1.
+  radix_count(keys, T, mask, prefix, 8, 0xfffu, hist);
+  __syncthreads();
+  uint32_t d2;
+  radix_find<TOPK_BINS>(hist, remaining, scan_sh[1], sh_result, &d2, &remaining);
+  prefix |= d2 << 8;
+  mask |= 0x000fff00u;
+  for (int i = threadIdx.x; i < 256; i += TOPK_THREADS) hist[i] = 0u;
+  __syncthreads();
+  // Digit 3: bits 7..0.
+  radix_count(keys, T, mask, prefix, 0, 0xffu, hist);
+  __syncthreads();
+  uint32_t d3;
+  radix_find<256>(hist, remaining, scan_sh[0], sh_result, &d3, &remaining);
+  const uint32_t kth = prefix | d3;
 
-  // Warp w owns positions [w*W, (w+1)*W), visited 32 at a time in order. One sweep
-  // counts the keys above K* and equal to it per warp; one scan of both counts gives
-  // each warp its first output slot: the keys above K* before it, plus the equal keys
-  // before it up to `remaining` (ties go to the lower position).
-  const int W = ((T + TOPK_THREADS - 1) / TOPK_THREADS) * 32;
-  const int lo = warp * W;
-  const int hi = min(T, lo + W);
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  uint32_t my_gt = 0, my_eq = 0;
-  for (int base = lo; base < hi; base += 32) {
-    const int t = base + lane;
-    const uint32_t k = t < hi ? keys[t] : 0u;
-    my_gt += __popc(__ballot_sync(0xffffffffu, t < hi && k > kth));
-    my_eq += __popc(__ballot_sync(0xffffffffu, t < hi && k == kth));
+  // Lane l of warp w owns positions [lo, hi): PL consecutive positions starting at
+  // (32 w + l) PL, recorded as bit masks (bit j = position lo + j) of the keys above,
+  // equal to and (for the statistics) at or above 0 in logit. The lanes visit their
+  // positions rotated by (l PL) / 32 so that a warp's shared-memory reads fall in
+  // distinct banks. A key's output slot is the number of keys above K* before it plus
+  // the number of keys equal to K* before it, capped at `remaining` (ties go to the
+  // lower position).
+  const int PL = (T + TOPK_THREADS - 1) / TOPK_THREADS;   // <= 48: fits a 64-bit mask
+  const int lo = (warp * 32 + lane) * PL;
+  const int cnt_here = max(0, min(T, lo + PL) - lo);
+  const int rot = (lane * PL) >> 5;
+  uint64_t gt_m = 0ull, eq_m = 0ull, thr_m = 0ull;
+  for (int jj = 0; jj < PL; ++jj) {
+    int j = jj + rot;
+    if (j >= PL) j -= PL;
+    if (j < cnt_here) {
+      const uint32_t k = keys[lo + j];
+      const uint64_t bit = 1ull << j;
+      if (k > kth) gt_m |= bit;
+      if (k == kth) eq_m |= bit;
+      if (k >= 0x80000000u) thr_m |= bit;   // logit >= 0, i.e. r >= 1/2
+    }
   }
-  if (lane == 0) {
-    scan_sh[0][warp] = my_gt;
-    scan_sh[1][warp] = my_eq;
+  const uint32_t my_gt = (uint32_t)__popcll(gt_m), my_eq = (uint32_t)__popcll(eq_m);
+  uint32_t gi = my_gt, ei = my_eq;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t yg = __shfl_up_sync(0xffffffffu, gi, o);
+    const uint32_t ye = __shfl_up_sync(0xffffffffu, ei, o);
+    if (lane >= o) {
+      gi += yg;
+      ei += ye;
+    }
+  }
+  if (lane == 31) {
+    scan_sh[0][warp] = gi;
+    scan_sh[1][warp] = ei;
   }
   __syncthreads();
   if (warp < 2) {
@@ -364,47 +487,54 @@ topk_kernel(int T, int n, const float* __restrict__ s, int32_t* __restrict__ idx
     scan_sh[warp][lane] = inc - v;
   }
   __syncthreads();
-  uint32_t eq_run = scan_sh[1][warp];
-  uint32_t out = scan_sh[0][warp] + min(eq_run, remaining);
+  const uint32_t gt_before = scan_sh[0][warp] + gi - my_gt;
+  const uint32_t eq_before = scan_sh[1][warp] + ei - my_eq;
+  // the equal keys this lane takes: its first min(my_eq, remaining - eq_before)
+  uint64_t sel_m = gt_m;
+  {
+    const uint32_t take = eq_before < remaining ? min(my_eq, remaining - eq_before) : 0u;
+    uint64_t e = eq_m;
+    for (uint32_t i = 0; i < take; ++i) {
+      sel_m |= e & (~e + 1ull);   // lowest remaining equal key
+      e &= e - 1ull;
+    }
+  }
   uint32_t n_thr = 0, n_agree = 0, n_again = 0;
-  for (int base = lo; base < hi; base += 32) {
-    const int t = base + lane;
-    const uint32_t k = t < hi ? keys[t] : 0u;
-    const bool eq = t < hi && k == kth;
-    const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
-    const bool sel = t < hi && (k > kth || (eq && eq_run + __popc(eqm & lt_mask) < remaining));
-    const uint32_t selm = __ballot_sync(0xffffffffu, sel);
-    if (tr.stats) {
-      const bool thr = t < hi && k >= 0x80000000u;   // logit >= 0, i.e. r >= 1/2
-      n_thr += __popc(__ballot_sync(0xffffffffu, thr));
-      n_agree += __popc(__ballot_sync(0xffffffffu, t < hi && thr == sel));
-      n_again += __popc(__ballot_sync(0xffffffffu, sel && last && last[t] == tr.layer - 1));
-    }
-    if (sel) {
-      const uint32_t o = out + __popc(selm & lt_mask);
-      if (o < (uint32_t)n) {
-        idx[(int64_t)b * n + o] = t;
-        if (r_sel) {
-          float x;
-          if (lsh) {
-            x = lsh[t];
-          } else {
-            x = sb[t];
-            for (int k2 = 1; k2 < nplanes; ++k2) x += sb[k2 * plane + t];
-            if (cnt) x -= tr.bias_step * (float)cnt[t];
-          }
-          r_sel[(int64_t)b * n + o] = sigmoidf_acc(x);
+  if (tr.stats) {
+    const uint64_t valid = cnt_here >= 64 ? ~0ull : ((1ull << cnt_here) - 1ull);
+    n_thr = (uint32_t)__popcll(thr_m);
+    n_agree = (uint32_t)(cnt_here - __popcll((thr_m ^ sel_m) & valid));
+  }
+  for (uint64_t m = sel_m; m; m &= m - 1ull) {
+    const int j = __ffsll((long long)m) - 1;
+    const int t = lo + j;
+    const uint64_t below = (1ull << j) - 1ull;
+    const uint32_t o = gt_before + (uint32_t)__popcll(gt_m & below) +
+                       min(eq_before + (uint32_t)__popcll(eq_m & below), remaining);
+    if (tr.stats && last && last[t] == tr.layer - 1) ++n_again;
+    if (o < (uint32_t)n) {
+      idx[(int64_t)b * n + o] = t;
+      if (r_sel) {
+        float x;
+        if (lsh) {
+          x = lsh[t];
+        } else {
+          x = sb[t];
+          for (int k2 = 1; k2 < nplanes; ++k2) x += sb[k2 * plane + t];
+          if (cnt) x -= tr.bias_step * (float)cnt[t];
         }
+        r_sel[(int64_t)b * n + o] = sigmoidf_acc(x);
       }
-      // this thread alone owns position t: record the selection for the block's later
-      // layers after its last read of cnt[t] and last[t] above
-      if (cnt) cnt[t] += 1;
-      if (last) last[t] = tr.layer;
     }
-    out += __popc(selm);
-    eq_run += __popc(eqm);
+    // this thread alone owns position t: record the selection for the block's later
+    // layers after its last read of cnt[t] and last[t] above
+    if (cnt) cnt[t] += 1;
+    if (last) last[t] = tr.layer;
   }
   if (tr.stats) {
+    n_thr = __reduce_add_sync(0xffffffffu, n_thr);
+    n_agree = __reduce_add_sync(0xffffffffu, n_agree);
+    n_again = __reduce_add_sync(0xffffffffu, n_again);
     if (lane == 0) {
       atomicAdd(&sh_stat[0], n_thr);
       atomicAdd(&sh_stat[1], n_agree);
@@ -427,10 +557,10 @@ cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32
   if (B <= 0) return cudaSuccess;
   // keys, and the logits too up to TOPK_CACHE_MAX_T
   const size_t smem = sizeof(uint32_t) * (size_t)T * (T <= TOPK_CACHE_MAX_T ? 2 : 1);
-  cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)(sizeof(uint32_t) * TOPK_MAX_T));
-  cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)(sizeof(uint32_t) * TOPK_MAX_T));
+  const int smem_max = (int)(sizeof(uint32_t) * (size_t)TOPK_MAX_T);
+  static_assert(2 * TOPK_CACHE_MAX_T <= TOPK_MAX_T, "cached logits fit the key budget");
+  cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+  cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
   if (tr)
     launch_pdl(topk_kernel<true>, dim3(B), dim3(TOPK_THREADS), smem, c.stream, T, n, s, idx,
                r_sel, c.status, *tr, nplanes, plane);
@@ -582,16 +712,29 @@ __device__ __forceinline__ int64_t stream_row(int64_t m, int T, int n, const int
   return b * T + t;
 }
 
+// Positions from the caller (or top-k): row m, the (m % n)-th row of its sequence, must
+// name a position in [0, seqT) above the one of the row before it in the sequence. A row
+// that does not is skipped -- nothing is read or written for it -- and the status word
+// records XMOD_ERR_DEVICE_CHECK.
+__device__ __forceinline__ bool row_idx_ok(int64_t m, int seqT, int n, const int32_t* idx,
+                                           int* status) {
+  if (!idx) return true;
+  const int32_t t = idx[m];
+  const bool ok = t >= 0 && t < seqT && (m % n == 0 || t > idx[m - 1]);
+  if (!ok) report_status(status, XMOD_ERR_DEVICE_CHECK);
+  return ok;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 gather_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
-              const int32_t* __restrict__ idx, T* __restrict__ xs) {
+              const int32_t* __restrict__ idx, T* __restrict__ xs, int* status) {
   pdl_trigger();
   pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
-  if (m >= M) return;
+  if (m >= M || !row_idx_ok(m, seqT, n, idx, status)) return;
   const T* src = x + stream_row(m, seqT, n, idx) * d;
   T* dst = xs + m * d;
   for (int c = lane * V; c < d; c += 32 * V) st_vec(dst + c, ld_vec(src + c));
@@ -601,13 +744,13 @@ template <typename T>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 gather_rmsnorm_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
                       const int32_t* __restrict__ idx, const T* __restrict__ gamma, float eps,
-                      T* __restrict__ u) {
+                      T* __restrict__ u, int* status) {
   pdl_trigger();
   pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
-  if (m >= M) return;
+  if (m >= M || !row_idx_ok(m, seqT, n, idx, status)) return;
   const T* src = x + stream_row(m, seqT, n, idx) * d;
   float ss = 0.f;
   for (int c = lane * V; c < d; c += 32 * V) {
@@ -634,13 +777,14 @@ template <typename T, int VPL>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 gather_rmsnorm_rows_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
                            const int32_t* __restrict__ idx, const T* __restrict__ gamma,
-                           float eps, T* __restrict__ u, RowMap rm) {
+                           float eps, T* __restrict__ u, RowMap rm, int* status) {
   pdl_trigger();
   pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
   if (m >= rm.rows(M)) return;
+  if (!rm.tok && !row_idx_ok(m, seqT, n, idx, status)) return;
   const T* src = x + (rm.tok ? (int64_t)rm.tok[m] : stream_row(m, seqT, n, idx)) * d;
   Vec16<T> v[VPL];
 #pragma unroll
@@ -680,8 +824,8 @@ static cudaError_t launch_gather_rmsnorm_rows(const Ctx& c, int vpl, unsigned bl
                                               T* u, RowMap rm) {
 #define XMOD_GR_CASE(N)                                                                     \
   case N:                                                                                   \
-    launch_pdl(gather_rmsnorm_rows_kernel<T, N>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream,               \
-        M, seqT, n, d, x, idx, gamma, eps, u, rm);                                          \
+    launch_pdl(gather_rmsnorm_rows_kernel<T, N>, dim3(blocks), dim3(ROW_WARPS * 32), 0,     \
+               c.stream, M, seqT, n, d, x, idx, gamma, eps, u, rm, c.status);               \
     break;
   switch (vpl) {
     XMOD_GR_CASE(1)
@@ -729,13 +873,13 @@ cudaError_t launch_stack_rows(const Ctx& c, const RowPtrs& rows, int count, int 
 template <typename T, int VPL>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 gather_rows_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
-                   const int32_t* __restrict__ idx, T* __restrict__ xs) {
+                   const int32_t* __restrict__ idx, T* __restrict__ xs, int* status) {
   pdl_trigger();
   pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
-  if (m >= M) return;
+  if (m >= M || !row_idx_ok(m, seqT, n, idx, status)) return;
   const T* src = x + stream_row(m, seqT, n, idx) * d;
   T* dst = xs + m * d;
   Vec16<T> v[VPL];
@@ -761,7 +905,7 @@ cudaError_t launch_gather(const Ctx& c, xmod_dtype dt, int B, int T, int n, int 
 #define XMOD_GA_CASE(TT, N)                                                                  \
   case N:                                                                                    \
     return launch_pdl(gather_rows_kernel<TT, N>, dim3(blocks), dim3(ROW_WARPS * 32), 0,      \
-                      c.stream, M, T, n, d, (const TT*)x, idx, (TT*)xs);
+                      c.stream, M, T, n, d, (const TT*)x, idx, (TT*)xs, c.status);
     if (dt == XMOD_BF16) {
       switch (vpl) {
         XMOD_GA_CASE(__nv_bfloat16, 1) XMOD_GA_CASE(__nv_bfloat16, 2)
@@ -780,11 +924,11 @@ cudaError_t launch_gather(const Ctx& c, xmod_dtype dt, int B, int T, int n, int 
     return cudaErrorInvalidValue;
   }
   if (dt == XMOD_BF16)
-    launch_pdl(gather_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
-        M, T, n, d, (const __nv_bfloat16*)x, idx, (__nv_bfloat16*)xs);
+    launch_pdl(gather_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream,
+               M, T, n, d, (const __nv_bfloat16*)x, idx, (__nv_bfloat16*)xs, c.status);
   else
-    launch_pdl(gather_kernel<float>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, M, T, n, d, (const float*)x, idx,
-                                                          (float*)xs);
+    launch_pdl(gather_kernel<float>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, M, T, n,
+               d, (const float*)x, idx, (float*)xs, c.status);
   return cudaGetLastError();
 }
 
@@ -805,12 +949,12 @@ cudaError_t launch_gather_rmsnorm(const Ctx& c, xmod_dtype dt, int B, int T, int
   }
   if (rm.tok || rm.M_dev) return cudaErrorInvalidValue;   // rows beyond the cached widths
   if (dt == XMOD_BF16)
-    launch_pdl(gather_rmsnorm_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
-        M, T, n, d, (const __nv_bfloat16*)x, idx, (const __nv_bfloat16*)gamma, eps,
-        (__nv_bfloat16*)u);
+    launch_pdl(gather_rmsnorm_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0,
+               c.stream, M, T, n, d, (const __nv_bfloat16*)x, idx, (const __nv_bfloat16*)gamma,
+               eps, (__nv_bfloat16*)u, c.status);
   else
-    launch_pdl(gather_rmsnorm_kernel<float>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
-        M, T, n, d, (const float*)x, idx, (const float*)gamma, eps, (float*)u);
+    launch_pdl(gather_rmsnorm_kernel<float>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream,
+               M, T, n, d, (const float*)x, idx, (const float*)gamma, eps, (float*)u, c.status);
   return cudaGetLastError();
 }
 
@@ -1187,6 +1331,29 @@ cudaError_t launch_qk_transform(const Ctx& c, xmod_dtype dt, int64_t M, const in
   return cudaErrorInvalidValue;
 }
 
+// ================================================================ caller positions
+
+// out[m] = idx[m] where row m passes row_idx_ok; a row that does not gets its position
+// clamped into [0, seqT) (so every later access stays inside the stream) and the status
+// word records XMOD_ERR_DEVICE_CHECK.
+__global__ void idx_sanitize_kernel(int64_t M, int seqT, int n, const int32_t* __restrict__ idx,
+                                    int32_t* __restrict__ out, int* status) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t m = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= M) return;
+  const int32_t t = idx[m];
+  out[m] = row_idx_ok(m, seqT, n, idx, status) ? t : min(max(t, 0), seqT - 1);
+}
+
+cudaError_t launch_idx_sanitize(const Ctx& c, int B, int T, int n, const int32_t* idx,
+                                int32_t* out) {
+  const int64_t M = (int64_t)B * n;
+  if (M <= 0) return cudaSuccess;
+  return launch_pdl(idx_sanitize_kernel, dim3((unsigned)((M + 255) / 256)), dim3(256), 0,
+                    c.stream, M, T, n, idx, out, c.status);
+}
+
 // ================================================================ gated scatter
 
 // One warp per selected row, the row taken in chunks of SCATTER_CHUNK 16-byte vectors
@@ -1197,13 +1364,14 @@ template <typename T>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
 gated_scatter_kernel(int64_t M, int seqT, int n, int d, T* __restrict__ x,
                      const int32_t* __restrict__ idx, const float* __restrict__ r_sel,
-                     const T* __restrict__ a, const T* __restrict__ f, float varsigma, int gate) {
+                     const T* __restrict__ a, const T* __restrict__ f, float varsigma, int gate,
+                     int* status) {
   pdl_trigger();
   pdl_wait();
   constexpr int V = Vec16<T>::N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * ROW_WARPS + warp;
-  if (m >= M) return;
+  if (m >= M || !row_idx_ok(m, seqT, n, idx, status)) return;
   T* row = x + stream_row(m, seqT, n, idx) * d;
   const T* arow = a + m * d;
   const T* frow = f ? f + m * d : nullptr;
@@ -1253,10 +1421,11 @@ cudaError_t launch_gated_scatter(const Ctx& c, xmod_dtype dt, int B, int T, int 
   if (dt == XMOD_BF16)
     launch_pdl(gated_scatter_kernel<__nv_bfloat16>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
         M, T, n, d, (__nv_bfloat16*)x, idx, r_sel, (const __nv_bfloat16*)a,
-        (const __nv_bfloat16*)f, varsigma, gate);
+        (const __nv_bfloat16*)f, varsigma, gate, c.status);
   else
     launch_pdl(gated_scatter_kernel<float>, dim3(blocks), dim3(ROW_WARPS * 32), 0, c.stream, 
-        M, T, n, d, (float*)x, idx, r_sel, (const float*)a, (const float*)f, varsigma, gate);
+        M, T, n, d, (float*)x, idx, r_sel, (const float*)a, (const float*)f, varsigma, gate,
+        c.status);
   return cudaGetLastError();
 }
 

@@ -100,11 +100,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                    _VP, _VP, _VP, ctypes.c_size_t, _VP]
     L.xmod_topk.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _VP, _VP, _VP, _VP,
                             ctypes.c_size_t, _VP]
-    L.xmod_gather.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _VP, _VP, _VP, _VP]
+    L.xmod_gather.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _VP, _VP, _VP, _VP, _VP]
     L.xmod_block_fwd.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _VP, _VP,
                                  ctypes.POINTER(LayerWeights), _VP, _VP, _VP, ctypes.c_size_t, _VP]
     L.xmod_gated_scatter.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, _VP, _VP, _VP, _VP, _VP,
-                                     ctypes.c_float, ctypes.c_int, _VP]
+                                     ctypes.c_float, ctypes.c_int, _VP, _VP]
     L.xmod_layer_fwd.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                  ctypes.POINTER(LayerWeights), _VP, _VP, _VP, _VP, _VP,
                                  ctypes.c_size_t, _VP]
@@ -219,9 +219,11 @@ def topk(dm, K, logits, idx, r_sel, ws, stream=None):
                                          _p(ws), _wsb(ws), _stream(stream)))
 
 
-def gather(dm, K, x, idx, xs, stream=None):
+def gather(dm, K, x, idx, xs, stream=None, status=None):
+    """status: None, or a device int32 tensor that receives XMOD_ERR_DEVICE_CHECK when a
+    position is out of range or not ascending (that row is skipped)."""
     _check("xmod_gather", load().xmod_gather(ctypes.byref(dm), int(K), _p(x), _p(idx), _p(xs),
-                                             _stream(stream)))
+                                             _p(status), _stream(stream)))
 
 
 def block_fwd(dm, n_per_seq, xs, idx, w: LayerWeights, a_out, f_out, ws, stream=None):
@@ -230,10 +232,11 @@ def block_fwd(dm, n_per_seq, xs, idx, w: LayerWeights, a_out, f_out, ws, stream=
         _p(ws), _wsb(ws), _stream(stream)))
 
 
-def gated_scatter(dm, K, x, idx, r_sel, a, f, varsigma, gate, stream=None):
+def gated_scatter(dm, K, x, idx, r_sel, a, f, varsigma, gate, stream=None, status=None):
+    """status: as for gather (a bad position's row is not written)."""
     _check("xmod_gated_scatter", load().xmod_gated_scatter(
         ctypes.byref(dm), int(K), _p(x), _p(idx), _p(r_sel), _p(a), _p(f), float(varsigma),
-        int(gate), _stream(stream)))
+        int(gate), _p(status), _stream(stream)))
 
 
 def layer_fwd(dm, kind, K, gate, w: LayerWeights, x, bias, idx_out, r_sel_out, ws, stream=None):

@@ -86,9 +86,10 @@ def test_invalid_arguments_rejected_before_launch():
     assert L.xmod_router_topk(dmp, 4, None, FAKE, None, None, None, FAKE, None, ws, 1 << 30, None) == X.ERR_INVALID_ARG
     assert L.xmod_router_topk(dmp, 4, FAKE, FAKE, None, None, None, FAKE, None, ws, 16, None) == X.ERR_WORKSPACE
     assert L.xmod_topk(dmp, 4, FAKE, None, None, ws, 1 << 30, None) == X.ERR_INVALID_ARG
-    assert L.xmod_gather(dmp, 4, FAKE, FAKE, FAKE + 8, None) == X.ERR_INVALID_ARG
-    assert L.xmod_gated_scatter(dmp, 4, FAKE, FAKE, FAKE, FAKE, None, ctypes.c_float(1.0), X.GATE_MOD, None) == X.ERR_INVALID_ARG
-    assert L.xmod_gated_scatter(dmp, 4, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), 5, None) == X.ERR_INVALID_ARG
+    assert L.xmod_gather(dmp, 4, FAKE, FAKE, FAKE + 8, None, None) == X.ERR_INVALID_ARG
+    assert L.xmod_gather(dmp, 4, FAKE, FAKE, FAKE, FAKE + 2, None) == X.ERR_INVALID_ARG   # misaligned status
+    assert L.xmod_gated_scatter(dmp, 4, FAKE, FAKE, FAKE, FAKE, None, ctypes.c_float(1.0), X.GATE_MOD, None, None) == X.ERR_INVALID_ARG
+    assert L.xmod_gated_scatter(dmp, 4, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(1.0), 5, None, None) == X.ERR_INVALID_ARG
     w = X.LayerWeights(*([FAKE] * 10), 1.0)
     w_bad = X.LayerWeights(*([FAKE] * 9 + [None]), 1.0)
     assert L.xmod_layer_fwd(dmp, X.LAYER_SPARSE, 4, X.GATE_XMOD, ctypes.byref(w_bad), FAKE, None, None, None, ws, 1 << 30, None) == X.ERR_INVALID_ARG

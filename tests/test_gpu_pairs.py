@@ -1,8 +1,9 @@
 """The CTA-pair GEMM kernels (tcgen05 cta_group::2, 256 x 256 tiles) against the
 single-CTA kernels and the oracle.
 
-The library puts a GEMM on CTA pairs only from six waves of pair tiles up (about 450
-tiles), so at test sizes they run only when XMOD_PAIR_MIN_WAVES=0 asks for them.
+The library puts a GEMM on CTA pairs from six waves of pair tiles up (about 450 tiles),
+or below that when its waves-times-width estimate favours them clearly; at test sizes
+this test forces them (XMOD_PAIR_MIN_WAVES=0) or keeps them off (a huge threshold).
 Single layers (dense and sparse) run once each way: the q|k|v, o-projection, gate/up
 and down-projection epilogues all run on pairs, with ragged row and column tiles."""
 import os
