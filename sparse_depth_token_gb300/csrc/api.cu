@@ -66,8 +66,8 @@ inline int router_split(const xmod_dims* dm) {
 
 // Workspace carve-up. M rows of block scratch cover a dense layer (M = B*T).
 struct Layout {
-  size_t status, s, idx, r_sel, u, qkv, vt, o, h, a, hidden, wr, count, last, seq, rowss, skflag,
-      skpart, total;
+  size_t status, s, idx, r_sel, u, qkv, vt, o, h, a, hidden, wr, count, last, seq, thr, rowss,
+      skflag, skpart, total;
 };
 
 // Stream-K scratch of the tensor-core GEMMs (bf16 layouts): one 128 x 256 fp32 partial
@@ -101,6 +101,7 @@ Layout layout(const xmod_dims* dm, int K) {
   L.count = off;  off = align_up(off + 4 * BT);   // token-choice bias state of a block
   L.last = off;   off = align_up(off + 4 * BT);
   L.seq = off;    off = align_up(off + 4 * (2 * (size_t)dm->B + 1));   // threshold rows
+  L.thr = off;    off = align_up(off + 8 * BT);   // threshold picks per sequence (pos, gate)
   L.rowss = off;  off = align_up(off + 4 * M * (size_t)(dm->d / 32));   // h^2 sums per chunk
   const size_t slots = dm->dtype == XMOD_BF16 ? kSkSlots : 0;
   L.skflag = off; off = align_up(off + 4 * slots);
@@ -608,9 +609,10 @@ int sparse_run(const Ctx& c, const xmod_dims* dm, const Layout& L, void* ws, int
     const int planes = router_split(dm);
     const int64_t plane = (int64_t)kRouterRun * BT;
     if (threshold)
-      XMOD_RUN("threshold", launch_threshold_select(c, B, T, S + j * BT, idx, r_sel, seq, seq + B,
-                                                    seq + 2 * B, track ? &tj : nullptr, planes,
-                                                    plane));
+      XMOD_RUN("threshold",
+               launch_threshold_select(c, B, T, S + j * BT, idx, r_sel, seq, seq + B, seq + 2 * B,
+                                       track ? &tj : nullptr, planes, plane,
+                                       (int32_t*)at(ws, L.thr), (float*)at(ws, L.thr) + BT));
     else
       XMOD_RUN("topk", launch_topk(c, B, T, n, S + j * BT, idx, r_sel, track ? &tj : nullptr,
                                    planes, plane));

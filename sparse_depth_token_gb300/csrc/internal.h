@@ -120,10 +120,12 @@ cudaError_t launch_qk_transform_bwd(const Ctx& c, xmod_dtype dt, int64_t M, void
 // Causal threshold rule over s [B, T] (ranked logit s - bias_step * count >= 0):
 // compact rows tok [<= B*T] (= b * T + t, sequence then position order), r_sel
 // [<= B*T], seq_count [B], seq_off [B] and the total in *M_out (all device).
+// scratch_pos [B*T] int32 and scratch_gate [B*T] fp32 hold each sequence's picks
+// before the compaction. Two launches (counting, one CTA per sequence; compaction).
 cudaError_t launch_threshold_select(const Ctx& c, int B, int T, const float* s, int32_t* tok,
                                     float* r_sel, int32_t* seq_count, int32_t* seq_off,
-                                    int32_t* M_out, const RouteTrack* tr = nullptr,
-                                    int nplanes = 1, int64_t plane = 0);
+                                    int32_t* M_out, const RouteTrack* tr, int nplanes,
+                                    int64_t plane, int32_t* scratch_pos, float* scratch_gate);
 // update_hist [B, max_count + 1]: histogram of count [B, T] per sequence.
 cudaError_t launch_count_hist(const Ctx& c, int B, int T, int max_count, const int32_t* count,
                               int32_t* update_hist);

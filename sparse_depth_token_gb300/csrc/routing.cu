@@ -574,10 +574,12 @@ cudaError_t launch_topk(const Ctx& c, int B, int T, int n, const float* s, int32
 //
 // X-MoD notes, "top-k in training, causal threshold at evaluation": token t enters the
 // layer when its routing probability is at least 1/2, i.e. its ranked logit
-// s - bias_step * count is >= 0 (-0 included), each token on its own. One CTA walks
-// the sequences in order and each sequence in 1024-token chunks, so the compact rows
-// come out in (sequence, position) order: tok[m] = b * T + t, r_sel[m] = sigmoid of
-// the logit, seq_count[b], seq_off[b] and *M_out = total.
+// s - bias_step * count is >= 0 (-0 included), each token on its own. One CTA per
+// sequence walks it in 1024-token chunks and writes its picks, in position order, to a
+// per-sequence scratch row block; a second kernel gives each sequence its compact row
+// offset (the counts of the sequences before it) and copies the picks there, so the
+// compact rows come out in (sequence, position) order: tok[m] = b * T + t, r_sel[m] =
+// sigmoid of the logit, seq_count[b], seq_off[b] and *M_out = total.
 
 // Sum of one value per thread over the CTA: (exclusive prefix of this thread's warp,
 // CTA total), both uniform within a warp.
@@ -602,79 +604,109 @@ __device__ __forceinline__ uint2 warps_scan_total(uint32_t v, uint32_t* sh) {
   return r;
 }
 
+// Sequence b = blockIdx.x: its picks' positions and gates to pos[b * T + i], gate[b * T
+// + i] for i < seq_count[b].
 __global__ void __launch_bounds__(TOPK_THREADS)
-threshold_select_kernel(int B, int T, const float* __restrict__ s, int32_t* __restrict__ tok,
-                        float* __restrict__ r_sel, int32_t* __restrict__ seq_count,
-                        int32_t* __restrict__ seq_off, int32_t* __restrict__ M_out, int* status,
-                        RouteTrack tr, int nplanes, int64_t plane) {
+threshold_count_kernel(int T, const float* __restrict__ s, int32_t* __restrict__ pos,
+                       float* __restrict__ gate, int32_t* __restrict__ seq_count, int* status,
+                       RouteTrack tr, int nplanes, int64_t plane) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t sh[33];
   __shared__ int sh_bad;
   const int lane = threadIdx.x & 31;
   const uint32_t lt_mask = (1u << lane) - 1u;
+  const int b = blockIdx.x;
   if (threadIdx.x == 0) sh_bad = 0;
   __syncthreads();
-  uint32_t out = 0;   // next compact row (the same in every thread)
-  for (int b = 0; b < B; ++b) {
-    const float* sb = s + (int64_t)b * T;
-    int32_t* cnt = tr.count ? tr.count + (int64_t)b * T : nullptr;
-    int32_t* last = tr.last ? tr.last + (int64_t)b * T : nullptr;
-    const uint32_t first = out;
-    uint32_t again = 0;
-    for (int t0 = 0; t0 < T; t0 += TOPK_THREADS) {
-      const int t = t0 + (int)threadIdx.x;
-      float v = 0.0f;
-      bool take = false;
-      if (t < T) {
-        v = sb[t];
-        for (int k = 1; k < nplanes; ++k) v += sb[k * plane + t];
-        if (cnt) v -= tr.bias_step * (float)cnt[t];
-        if (!isfinite(v)) sh_bad = 1;
-        take = v >= 0.0f;
-      }
-      const uint32_t bal = __ballot_sync(0xffffffffu, take);
-      const uint2 sc = warps_scan_total((uint32_t)__popc(bal), sh);
-      if (take) {
-        const uint32_t m = out + sc.x + (uint32_t)__popc(bal & lt_mask);
-        tok[m] = b * T + t;
-        r_sel[m] = sigmoidf_acc(v);
-        if (last && last[t] == tr.layer - 1) ++again;
-        if (cnt) cnt[t] += 1;
-        if (last) last[t] = tr.layer;
-      }
-      out += sc.y;
+  const float* sb = s + (int64_t)b * T;
+  int32_t* cnt = tr.count ? tr.count + (int64_t)b * T : nullptr;
+  int32_t* last = tr.last ? tr.last + (int64_t)b * T : nullptr;
+  int32_t* pb = pos + (int64_t)b * T;
+  float* gb = gate + (int64_t)b * T;
+  uint32_t out = 0, again = 0;   // out: picks so far (the same in every thread)
+  for (int t0 = 0; t0 < T; t0 += TOPK_THREADS) {
+    const int t = t0 + (int)threadIdx.x;
+    float v = 0.0f;
+    bool take = false;
+    if (t < T) {
+      v = sb[t];
+      for (int k = 1; k < nplanes; ++k) v += sb[k * plane + t];
+      if (cnt) v -= tr.bias_step * (float)cnt[t];
+      if (!isfinite(v)) sh_bad = 1;
+      take = v >= 0.0f;
     }
-    if (tr.stats) {   // reduce `again` over the CTA (only the stats use it)
-      const uint2 sc = warps_scan_total((uint32_t)__reduce_add_sync(0xffffffffu, again), sh);
-      if (threadIdx.x == 0) {
-        int32_t* st = tr.stats + (int64_t)b * 4;
-        st[0] = (int32_t)(out - first);
-        st[1] = (int32_t)(out - first);   // the rule's own picks are its threshold picks
-        st[2] = T;
-        st[3] = (int32_t)sc.y;
-      }
+    const uint32_t bal = __ballot_sync(0xffffffffu, take);
+    const uint2 sc = warps_scan_total((uint32_t)__popc(bal), sh);
+    if (take) {
+      const uint32_t i = out + sc.x + (uint32_t)__popc(bal & lt_mask);
+      pb[i] = t;
+      gb[i] = sigmoidf_acc(v);
+      if (last && last[t] == tr.layer - 1) ++again;
+      if (cnt) cnt[t] += 1;
+      if (last) last[t] = tr.layer;
     }
+    out += sc.y;
+  }
+  if (tr.stats) {   // reduce `again` over the CTA (only the stats use it)
+    const uint2 sc = warps_scan_total((uint32_t)__reduce_add_sync(0xffffffffu, again), sh);
     if (threadIdx.x == 0) {
-      seq_count[b] = (int32_t)(out - first);
-      seq_off[b] = (int32_t)first;
+      int32_t* st = tr.stats + (int64_t)b * 4;
+      st[0] = (int32_t)out;
+      st[1] = (int32_t)out;   // the rule's own picks are its threshold picks
+      st[2] = T;
+      st[3] = (int32_t)sc.y;
     }
   }
   if (threadIdx.x == 0) {
-    *M_out = (int32_t)out;
+    seq_count[b] = (int32_t)out;
     if (sh_bad) report_status(status, XMOD_ERR_DEVICE_CHECK);
+  }
+}
+
+// Sequence b = blockIdx.x: offset = the counts of sequences 0 .. b-1 (added in order),
+// its picks copied to the compact rows from there.
+__global__ void __launch_bounds__(256)
+threshold_compact_kernel(int B, int T, const int32_t* __restrict__ pos,
+                         const float* __restrict__ gate, const int32_t* __restrict__ seq_count,
+                         int32_t* __restrict__ tok, float* __restrict__ r_sel,
+                         int32_t* __restrict__ seq_off, int32_t* __restrict__ M_out) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int32_t sh_off;
+  const int b = blockIdx.x;
+  if (threadIdx.x == 0) {
+    int32_t off = 0;
+    for (int i = 0; i < b; ++i) off += seq_count[i];
+    sh_off = off;
+    seq_off[b] = off;
+    if (b == B - 1) *M_out = off + seq_count[b];
+  }
+  __syncthreads();
+  const int32_t off = sh_off, n = seq_count[b];
+  const int32_t* pb = pos + (int64_t)b * T;
+  const float* gb = gate + (int64_t)b * T;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    tok[off + i] = b * T + pb[i];
+    r_sel[off + i] = gb[i];
   }
 }
 
 cudaError_t launch_threshold_select(const Ctx& c, int B, int T, const float* s, int32_t* tok,
                                     float* r_sel, int32_t* seq_count, int32_t* seq_off,
                                     int32_t* M_out, const RouteTrack* tr, int nplanes,
-                                    int64_t plane) {
-  if (B <= 0 || T <= 0 || nplanes < 1) return cudaErrorInvalidValue;
+                                    int64_t plane, int32_t* scratch_pos, float* scratch_gate) {
+  if (B <= 0 || T <= 0 || nplanes < 1 || !scratch_pos || !scratch_gate)
+    return cudaErrorInvalidValue;
   const RouteTrack none{};
-  return launch_pdl(threshold_select_kernel, dim3(1), dim3(TOPK_THREADS), 0, c.stream, B, T, s,
-                    tok, r_sel, seq_count, seq_off, M_out, c.status, tr ? *tr : none, nplanes,
-                    plane);
+  cudaError_t e = launch_pdl(threshold_count_kernel, dim3(B), dim3(TOPK_THREADS), 0, c.stream,
+                             T, s, scratch_pos, scratch_gate, seq_count, c.status,
+                             tr ? *tr : none, nplanes, plane);
+  if (e != cudaSuccess) return e;
+  count_launch();
+  return launch_pdl(threshold_compact_kernel, dim3(B), dim3(256), 0, c.stream, B, T,
+                    (const int32_t*)scratch_pos, (const float*)scratch_gate,
+                    (const int32_t*)seq_count, tok, r_sel, seq_off, M_out);
 }
 
 // update_hist[b, c] = number of tokens of sequence b whose count is c (0 <= c <= max_count).
@@ -1098,7 +1130,37 @@ cudaError_t launch_rmsnorm_f32in(const Ctx& c, xmod_dtype dt, int64_t M, int d, 
 // The angle pos * theta^(-2c/hd) is taken modulo one turn without losing the position's
 // bits: per pair c the turns per position, theta^(-2c/hd) / (2 pi), are kept as a
 // float hi + lo sum, and pos * hi is split exactly with an fma.
-constexpr int QK_HEADS = 4;
+constexpr int QK_HEADS = 8;
+
+// E consecutive elements of one lane: one 8- or 16-byte access when they fill one
+// (the rows, head offsets and lane offsets are multiples of E elements).
+template <typename T, int E>
+__device__ __forceinline__ void ld_lane(const T* p, float (&v)[E]) {
+  if constexpr (sizeof(T) == 2 && E == 4) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+    v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+  } else if constexpr (sizeof(T) == 4 && E == 4) {
+    const float4 r = *reinterpret_cast<const float4*>(p);
+    v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = Elem<T>::to_f(p[e]);
+  }
+}
+template <typename T, int E>
+__device__ __forceinline__ void st_lane(T* p, const float (&v)[E]) {
+  if constexpr (sizeof(T) == 2 && E == 4) {
+    __nv_bfloat162 r[2] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3])};
+    *reinterpret_cast<uint2*>(p) = *reinterpret_cast<const uint2*>(r);
+  } else if constexpr (sizeof(T) == 4 && E == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < E; ++e) p[e] = Elem<T>::from_f(v[e]);
+  }
+}
 
 template <typename T, int E>
 __global__ void __launch_bounds__(ROW_WARPS * 32)
@@ -1148,8 +1210,7 @@ qk_transform_kernel(int64_t M, const int32_t* __restrict__ M_dev, T* __restrict_
       if (h < h_end) {
         const bool is_q = h < q_heads;
         hp[i] = x + m * ld + (is_q ? q_col0 + h * HD : k_col0 + (h - q_heads) * HD) + lane * E;
-#pragma unroll
-        for (int e = 0; e < E; ++e) v[i][e] = Elem<T>::to_f(hp[i][e]);
+        ld_lane<T, E>(hp[i], v[i]);
       }
     }
 #pragma unroll
@@ -1173,8 +1234,7 @@ qk_transform_kernel(int64_t M, const int32_t* __restrict__ M_dev, T* __restrict_
           v[i][e] = first ? v[i][e] * cs[e] - other * sn[e] : other * sn[e] + v[i][e] * cs[e];
         }
       }
-#pragma unroll
-      for (int e = 0; e < E; ++e) hp[i][e] = Elem<T>::from_f(v[i][e]);
+      st_lane<T, E>(hp[i], v[i]);
     }
   }
 }
