@@ -427,6 +427,52 @@ struct EpiIn {
   uint4 a[4];
 };
 
+// Staged epilogue inputs (CTA-pair kernel, o-projection and down projection): a loader
+// warp brings the tile's x rows (TMA gather4 at their stream rows) and, for the down
+// projection, its a rows (a TMA tile) into shared memory, 64 columns at a time into
+// one of two buffers, while the accumulator is still being computed; the epilogue reads
+// them from there instead of loading one row per lane from global memory. A buffer
+// holds STG_TENSORS 128-row x 64-column bf16 tiles (128-byte swizzle, as TMA writes
+// them: 16-byte chunk k of row r sits at chunk k ^ (r & 7)).
+constexpr int STG_COLS = 64;
+constexpr int STG_TILE = BM * STG_COLS * 2;   // 16 KB
+template <int MODE>
+__host__ __device__ constexpr int stg_tensors() {
+  return MODE == EPI_DOWN_SCATTER ? 2 : (MODE == EPI_OPROJ ? 1 : 0);
+}
+template <int MODE>
+__host__ __device__ constexpr int stg_bytes() {
+  return 2 * stg_tensors<MODE>() * STG_TILE;
+}
+
+// Where the epilogue finds a staged chunk: the buffers' base, their full / empty
+// barriers (two each, 8 bytes apart) and the global index of the tile's first
+// 64-column pair (buffer = index & 1).
+struct EpiStage {
+  uint32_t base, full0, empty0;
+  int gp0;
+  volatile int* abort_flag;
+  int* status;
+};
+
+// This lane's row (row r of the CTA tile) of the 32 columns of chunk c from the staged
+// buffer; false if the wait ran out.
+template <int MODE>
+__device__ __forceinline__ bool epi_load_staged(const EpiStage& st, int c, int r, EpiIn& in) {
+  const int g = st.gp0 + (c >> 1);
+  const uint32_t u = (uint32_t)(g & 1);
+  if (!mbar_wait(st.full0 + 8u * u, (uint32_t)(g >> 1) & 1u, st.abort_flag, st.status))
+    return false;
+  const uint32_t row = st.base + u * (uint32_t)(stg_tensors<MODE>() * STG_TILE) + (uint32_t)r * 128u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t off = (uint32_t)((((c & 1) * 4 + j) ^ (r & 7)) << 4);
+    in.x[j] = lds128(row + off);
+    if (MODE == EPI_DOWN_SCATTER) in.a[j] = lds128(row + STG_TILE + off);
+  }
+  return true;
+}
+
 template <int MODE>
 __device__ __forceinline__ void epi_load_in(const TcArgs& a, int M, int m, int col0, int64_t xrow,
                                             EpiIn& in) {
@@ -555,10 +601,11 @@ __device__ __forceinline__ void epilogue_chunk_direct(const TcArgs& a, int M, in
 
 // Epilogue of one tile for this warp's 32-row slab [wrow0, wrow0 + 32). RS: every
 // accumulator value of this lane's row is scaled by rscale first (gathered RMSNorm).
-template <int BN, int MODE, bool RS = false>
-__device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0, int lane,
+template <int BN, int MODE, bool RS = false, bool STG = false>
+__device__ __forceinline__ bool epilogue_tile(const TcArgs& a, int M, int wrow0, int lane,
                                               int n_blk, uint32_t t_row, int part, int nparts,
-                                              int ks = 0, float rscale = 1.0f) {
+                                              int ks = 0, float rscale = 1.0f,
+                                              const EpiStage* stg = nullptr, int trow0 = 0) {
   const Epilogue& e = a.e;
   constexpr bool swiglu = MODE == EPI_SWIGLU;
   // the row this lane owns in TMEM: its stream row and gate
@@ -588,13 +635,14 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0,
   constexpr int NCH_FULL = BN / 32;
   const int nch = swiglu ? NCH_FULL / 2 : NCH_FULL;
   const int col_tile0 = swiglu ? n_blk * (BN / 2) : n_blk * BN;
-  constexpr bool needs_in = MODE == EPI_OPROJ || MODE == EPI_DOWN_SCATTER;
+  constexpr bool needs_in = (MODE == EPI_OPROJ || MODE == EPI_DOWN_SCATTER) && !STG;
   EpiIn cur, nxt;
   if (needs_in && part < nch) epi_load_in<MODE>(a, M, m_own, col_tile0 + part * 32, xrow_own, cur);
 #pragma unroll 1
   for (int c = part; c < nch; c += nparts) {
     if (needs_in && c + nparts < nch)
       epi_load_in<MODE>(a, M, m_own, col_tile0 + (c + nparts) * 32, xrow_own, nxt);
+    if (STG && !epi_load_staged<MODE>(*stg, c, wrow0 - trow0 + lane, cur)) return false;
     float v[32];
     if (swiglu) {
       float u[32];
@@ -645,8 +693,13 @@ __device__ __forceinline__ void epilogue_tile(const TcArgs& a, int M, int wrow0,
       if (!e.vt_rows) continue;
     }
     epilogue_chunk_direct<MODE>(a, M, m_own, col0, xrow_own, r_own, v, cur, ks);
+    if (STG) {   // this warp is done with the chunk's staged rows
+      __syncwarp();
+      if (lane == 0) mbar_arrive(stg->empty0 + 8u * (uint32_t)((stg->gp0 + (c >> 1)) & 1));
+    }
     cur = nxt;
   }
+  return true;
 }
 
 template <int BN, int MODE, bool GATHER = false>
@@ -972,18 +1025,32 @@ struct Cfg2 {
   static constexpr int TMEM_COLS = 2 * BN <= 256 ? 256 : 512;
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256;
 };
+// The same with STG bytes of staged epilogue inputs, the stage ring filling what is
+// left of the 227 KB a CTA may hold (the staged epilogue needs little L1 cache).
+template <int BN, int STG>
+struct Cfg2S : Cfg2<BN> {
+  static constexpr int STAGES =
+      STG ? (227 * 1024 - 1024 - 256 - STG) / Cfg2<BN>::STAGE_BYTES : Cfg2<BN>::STAGES;
+  static constexpr int SMEM = STAGES * Cfg2<BN>::STAGE_BYTES + STG + 1024 + 256;
+  static_assert(SMEM <= 227 * 1024, "shared memory");
+};
 
 // Row blocks (of 256) per band of the pair kernel's tile order.
 #ifndef XMOD_TILE_BAND2
 #define XMOD_TILE_BAND2 8
 #endif
 
-template <int BN, int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+// STG: the o-projection's / down projection's epilogue inputs are staged in shared
+// memory by one more warp (the loader), see EpiStage.
+template <int BN, int MODE, bool STG = false>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS + (STG ? 32 : 0), 1)
 gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+                const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmAr,
                 const TcArgs args) {
-  using C = Cfg2<BN>;
+  static_assert(!STG || MODE == EPI_OPROJ || MODE == EPI_DOWN_SCATTER, "staged inputs");
+  static_assert(!STG || EPI_WARPS == 8, "a staged buffer is released by eight warps");
+  using C = Cfg2S<BN, STG ? stg_bytes<MODE>() : 0>;
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -991,8 +1058,13 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sA = base;
   const uint32_t sB = sA + C::STAGES * C::A_BYTES;
-  const uint32_t sBar = sB + C::STAGES * C::B_BYTES;
-  const uint32_t sTmem = sBar + 8 * (2 * C::STAGES + 4);
+  const uint32_t sStg = sB + C::STAGES * C::B_BYTES;   // 1024-aligned: stages are
+  const uint32_t sBar = sStg + (STG ? stg_bytes<MODE>() : 0);
+  const uint32_t sTmem = sBar + 8 * (2 * C::STAGES + 8);
+  // staged inputs: IN_FULL(u) (the loader's copies landed), IN_EMPTY(u) (eight epilogue
+  // warps read the buffer)
+  const uint32_t IN_FULL0 = sBar + 8 * (2 * C::STAGES + 4), IN_EMPTY0 = IN_FULL0 + 16;
+  static_assert(8 * (2 * C::STAGES + 8) + 12 <= 256, "barrier block overflows");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + (sTmem - base));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + (sTmem - base) + 8);
 #define FULL(s) (sBar + 8u * (s))
@@ -1013,11 +1085,19 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     for (int a = 0; a < 2; ++a) {
       mbar_init(ACC_FULL(a), 1);
       mbar_init(ACC_EMPTY(a), 2 * EPI_WARPS);   // used in CTA 0: one lane per epilogue warp
+      if (STG) {
+        mbar_init(IN_FULL0 + 8 * a, 1);
+        mbar_init(IN_EMPTY0 + 8 * a, EPI_WARPS);
+      }
     }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB0);
+    if (STG) {
+      prefetch_tensormap(&tmX);
+      if (MODE == EPI_DOWN_SCATTER) prefetch_tensormap(&tmAr);
+    }
     if (MODE == EPI_SWIGLU || args.n_split1 < args.N) prefetch_tensormap(&tmB1);
     if (MODE != EPI_SWIGLU && args.n_split2 < args.N) prefetch_tensormap(&tmB2);
   }
@@ -1091,6 +1171,43 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         mma_commit_pair(ACC_FULL(acc));
       }
     }
+  } else if (STG && warp == 2 + EPI_WARPS) {
+    // The loader: for each tile of this CTA and each 64-column pair of its chunks, the
+    // CTA's 128 x rows by TMA gather4 (lane l: tile rows 4l .. 4l+3, at their stream
+    // rows) and, for the down projection, the 128 a rows as one tile, into buffer
+    // u = pair index & 1 once the epilogue has released it.
+    int gp = 0;
+    bool run = true;
+    for (int tile = pair; run && tile < args.tiles; tile += npairs) {
+      int m_blk, n_blk;
+      tile_coords(args, args.tiles_m, tile, m_blk, n_blk, XMOD_TILE_BAND2);
+      const int m0 = m_blk * (2 * BM) + (int)rank * BM;
+      int r[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {   // rows past M repeat a valid row; never used
+        const int m = m0 + 4 * lane + q;
+        r[q] = m < args.M ? (int)stream_row_of(args.e, m) : 0;
+      }
+      for (int cp = 0; cp < BN / STG_COLS; ++cp, ++gp) {
+        const int u = gp & 1;
+        int ok = 1;
+        if (lane == 0) {
+          ok = !*abort_flag &&
+               mbar_wait(IN_EMPTY0 + 8 * u, ((uint32_t)(gp >> 1) & 1u) ^ 1u, abort_flag,
+                         args.status);
+          if (ok) mbar_arrive_expect_tx(IN_FULL0 + 8 * u, stg_tensors<MODE>() * STG_TILE);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          run = false;
+          break;
+        }
+        const uint32_t buf = sStg + (uint32_t)(u * stg_tensors<MODE>() * STG_TILE);
+        const int col = n_blk * BN + cp * STG_COLS;
+        tma_gather4(buf + lane * 512, &tmX, IN_FULL0 + 8 * u, col, r[0], r[1], r[2], r[3]);
+        if (MODE == EPI_DOWN_SCATTER && lane == 0)
+          tma_load_2d(buf + STG_TILE, &tmAr, IN_FULL0 + 8 * u, col, m0);
+      }
+    }
   } else {
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 belong to this warp
     int lt = 0;
@@ -1099,13 +1216,23 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
       int m_blk, n_blk;
       tile_coords(args, args.tiles_m, tile, m_blk, n_blk, XMOD_TILE_BAND2);
-      const int wrow0 = m_blk * (2 * BM) + (int)rank * BM + quad * 32;
-      epi_prefetch<BN, MODE>(args, args.M, wrow0 + lane, n_blk, (warp - 2) / 4);
+      const int trow0 = m_blk * (2 * BM) + (int)rank * BM;
+      const int wrow0 = trow0 + quad * 32;
+      if (!STG) epi_prefetch<BN, MODE>(args, args.M, wrow0 + lane, n_blk, (warp - 2) / 4);
       if (!mbar_wait_cluster(ACC_FULL(acc), aph, abort_flag, args.status)) break;
       tc_fence_after();
       const uint32_t t_row = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-      epilogue_tile<BN, MODE>(args, args.M, wrow0, lane, n_blk, t_row, (warp - 2) / 4,
-                              EPI_WARPS / 4);
+      if (STG) {
+        const EpiStage st{sStg, IN_FULL0, IN_EMPTY0, lt * (BN / STG_COLS), abort_flag,
+                          args.status};
+        if (!epilogue_tile<BN, MODE, false, true>(args, args.M, wrow0, lane, n_blk, t_row,
+                                                  (warp - 2) / 4, EPI_WARPS / 4, 0, 1.0f, &st,
+                                                  trow0))
+          break;
+      } else {
+        epilogue_tile<BN, MODE>(args, args.M, wrow0, lane, n_blk, t_row, (warp - 2) / 4,
+                                EPI_WARPS / 4);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(ACC_EMPTY(acc), 0));
@@ -1327,31 +1454,68 @@ int max_pairs() {
   return cached;
 }
 
+// Staged epilogue inputs on the CTA-pair kernel (o-projection, down projection); the
+// environment variable XMOD_EPI_STAGE=0, read at every launch, turns them off.
+bool epi_stage_enabled() {
+  const char* v = getenv("XMOD_EPI_STAGE");
+  return !(v && v[0] == '0' && v[1] == '\0');
+}
+
 template <int BN>
 cudaError_t launch_bn2(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) {
-  using Cf = Cfg2<BN>;
   if (e.kind == EPI_ROUTER) return cudaErrorInvalidValue;
-  CUtensorMap mA, mB0, mB1, mB2;
+  CUtensorMap mA, mB0, mB1, mB2, mX, mAr;
+  memset(&mX, 0, sizeof(mX));
+  memset(&mAr, 0, sizeof(mAr));
   TcArgs a;
   if (!setup<BN>(c, p, e, 2 * BM, BN / 2, mA, mB0, mB1, mB2, a)) return cudaErrorInvalidValue;
   if (a.tiles <= 0) return cudaSuccess;
+  // staged inputs: the stream's rows (one-row boxes for gather4) and a's 128-row tiles
+  bool stg = epi_stage_enabled() && !e.tok && e.x && e.n_per_seq > 0 && e.T >= e.n_per_seq &&
+             p.M % e.n_per_seq == 0 && p.N == e.d &&
+             (e.kind == EPI_OPROJ || (e.kind == EPI_DOWN_SCATTER && e.a));
+  if (stg) {
+    const int64_t x_rows = (int64_t)(p.M / e.n_per_seq) * e.T;
+    stg = make_map(&mX, e.x, e.d, x_rows, e.d, 1) &&
+          (e.kind != EPI_DOWN_SCATTER || make_map(&mAr, e.a, e.d, p.M, e.d, BM));
+  }
   void (*k)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
-            const TcArgs) = nullptr;
+            const CUtensorMap, const CUtensorMap, const TcArgs) = nullptr;
+  int smem = 0, threads = NUM_THREADS;
   switch (e.kind) {
-    case EPI_STORE: k = gemm_tc2_kernel<BN, EPI_STORE>; break;
-    case EPI_OPROJ: k = gemm_tc2_kernel<BN, EPI_OPROJ>; break;
-    case EPI_SWIGLU: k = gemm_tc2_kernel<BN, EPI_SWIGLU>; break;
-    case EPI_DOWN_SCATTER: k = gemm_tc2_kernel<BN, EPI_DOWN_SCATTER>; break;
+    case EPI_STORE: k = gemm_tc2_kernel<BN, EPI_STORE>; smem = Cfg2<BN>::SMEM; break;
+    case EPI_SWIGLU: k = gemm_tc2_kernel<BN, EPI_SWIGLU>; smem = Cfg2<BN>::SMEM; break;
+    case EPI_OPROJ:
+      if (stg) {
+        k = gemm_tc2_kernel<BN, EPI_OPROJ, true>;
+        smem = Cfg2S<BN, stg_bytes<EPI_OPROJ>()>::SMEM;
+        threads += 32;
+      } else {
+        k = gemm_tc2_kernel<BN, EPI_OPROJ>;
+        smem = Cfg2<BN>::SMEM;
+      }
+      break;
+    case EPI_DOWN_SCATTER:
+      if (stg) {
+        k = gemm_tc2_kernel<BN, EPI_DOWN_SCATTER, true>;
+        smem = Cfg2S<BN, stg_bytes<EPI_DOWN_SCATTER>()>::SMEM;
+        threads += 32;
+      } else {
+        k = gemm_tc2_kernel<BN, EPI_DOWN_SCATTER>;
+        smem = Cfg2<BN>::SMEM;
+      }
+      break;
     default: return cudaErrorInvalidValue;
   }
-  static bool attr_set[4] = {false, false, false, false};
-  if (!attr_set[e.kind]) {
-    cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+  static bool attr_set[2][4] = {};
+  if (!attr_set[stg][e.kind]) {
+    cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    attr_set[e.kind] = true;
+    attr_set[stg][e.kind] = true;
   }
   const int pairs = a.tiles < max_pairs<BN>() ? a.tiles : max_pairs<BN>();
-  return launch_pdl(k, dim3(2 * pairs), dim3(NUM_THREADS), Cf::SMEM, c.stream, mA, mB0, mB1, mB2, a);
+  return launch_pdl(k, dim3(2 * pairs), dim3(threads), smem, c.stream, mA, mB0, mB1, mB2, mX,
+                    mAr, a);
 }
 
 // Tile widths a problem may use: the q|k|v boundaries must fall on tile edges.

@@ -114,6 +114,15 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 16 bytes from a shared-memory address.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy
 // (TMA, tcgen05) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
