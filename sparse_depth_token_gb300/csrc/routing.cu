@@ -804,9 +804,13 @@ gather_rmsnorm_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x
 }
 
 // Register-cached variant (rows of at most 32 * VPL 16-byte vectors): the row is
-// read once with every load in flight, then normalised from registers.
+// read once with every load in flight, then normalised from registers. Rows of up to
+// eight vectors a lane (2048 bf16, 1024 fp32) run four CTAs per SM (at most 64
+// registers a thread): a sparse layer's 4096 rows are then all in flight in one wave
+// on 152 SMs (three per SM, at 74 registers, left a second partial wave; A3K16 shape
+// 14.6 -> 12.9 us). Longer rows would spill under that bound.
 template <typename T, int VPL>
-__global__ void __launch_bounds__(ROW_WARPS * 32)
+__global__ void __launch_bounds__(ROW_WARPS * 32, VPL <= 8 ? 4 : 1)
 gather_rmsnorm_rows_kernel(int64_t M, int seqT, int n, int d, const T* __restrict__ x,
                            const int32_t* __restrict__ idx, const T* __restrict__ gamma,
                            float eps, T* __restrict__ u, RowMap rm, int* status) {
