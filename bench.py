@@ -201,9 +201,12 @@ TENSOR_KINDS = {"gemm_qkv", "attention", "gemm_o_residual", "gemm_gate_up_swiglu
 # the summary that records it; used only while the kernel is unchanged and the run is
 # the captured configuration. Key: (workload, B, variant / routing tag, kernel kind).
 RECORDED_TRAFFIC = {
-    # the 33 gate/up launches of one A4K8 step (32 sparse layers + the dense one), mean
+    # the gate/up launches of one step, mean: A3K16 (96 sparse layers + 4 dense), A4K8
+    # (32 sparse layers + the dense one)
+    ("a3k16_bf16", 4, "xmod", "gemm_gate_up_swiglu"):
+        (140.60e6, "profiles/gemm_gate_up_dram.md"),
     ("a4k8_bf16", 8, "xmod", "gemm_gate_up_swiglu"):
-        (53.42e6, "profiles/gemm_gate_up_dram_a4k8.md"),
+        (52.56e6, "profiles/gemm_gate_up_dram.md"),
     # the router's x read + logits write at B = 8, scaled by 8 to B = 64 (x is read once)
     ("routing_bf16", 64, "routing", "router"):
         (8 * 540.3e6, "profiles/routing_kernels_c2_microbench.md"),

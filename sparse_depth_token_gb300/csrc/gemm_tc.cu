@@ -1035,9 +1035,15 @@ struct Cfg2S : Cfg2<BN> {
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-// Row blocks (of 256) per band of the pair kernel's tile order.
+// Row blocks (of 256) per band of the pair kernel's tile order. The B operand (the
+// weights) is read from DRAM about once per band: between bands the output stream
+// (738 MB for a dense layer's gate/up at d_ff = 5632, B = 4, T = 16384) evicts it from
+// L2. 8-block bands read that GEMM's 46 MB of weights 32 times (1.35 GB read against
+// 314 MB of operands); 32-block bands 8 times. The step time is the same either way
+// (A3K16 and A4K8 dense layers, same box): the traffic is a third of what the tensor
+// pipe's pace would allow.
 #ifndef XMOD_TILE_BAND2
-#define XMOD_TILE_BAND2 8
+#define XMOD_TILE_BAND2 32
 #endif
 
 // STG: the o-projection's / down projection's epilogue inputs are staged in shared
