@@ -127,6 +127,41 @@ def test_bf16_stack_reduced_teacher_forced(X, name):
     assert torch.equal(xs.view(torch.int16), xd.view(torch.int16))
 
 
+@pytest.mark.parametrize("name", ["a4k8_bf16", "a3k16_bf16"])
+def test_stack_captured_in_a_cuda_graph(X, name):
+    """xmod_stack_fwd is capture-safe: the call recorded once into a CUDA graph on a side
+    stream (its launches, with their programmatic-launch edges, become graph nodes) and
+    replayed twice over a fresh copy of the input gives the eager call's stream bit for
+    bit; the status word stays clear."""
+    w = _reduced(name)
+    layers, kinds, bias, x, dev, abi = _setup(X, w)
+    dm = xmod_dims(w)
+    ws = workspace(dm, w.K)
+    bd = torch.from_numpy(bias).cuda() if bias is not None else None
+    x0 = to_dev(x, w.dtype)
+    eager = x0.clone()
+    X.reset_status(ws)
+    X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, eager, bd, ws)
+    assert X.sync_status(ws) == X.OK
+    xs = torch.empty_like(x0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):   # warm the stream (first-use work stays out of the capture)
+        xs.copy_(x0)
+        X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, xs, bd, ws, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        xs.copy_(x0)
+        X.stack_fwd(dm, w.K, w.A, w.N0, w.N1, w.gate, abi, xs, bd, ws, stream=s)
+    for _ in range(2):
+        xs.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(xs.view(torch.int16), eager.view(torch.int16))
+    assert X.sync_status(ws) == X.OK
+
+
 @pytest.mark.parametrize("name", ["a4k8_bf16", "mod_bf16", "a3k16_bf16"])
 def test_bf16_stack_reduced_end_to_end(X, name):
     """End to end, with no teacher forcing of the stream: xmod_stack_fwd on the shortened
