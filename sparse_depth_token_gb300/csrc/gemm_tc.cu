@@ -84,6 +84,7 @@ struct TcArgs {
   int64_t units;           // tiles x k-blocks
   float* sk_part;          // per-CTA partial accumulator slots, BM x BN fp32 each
   int* sk_flag;            // per-CTA "slot published" flags, 0 between launches
+  int band2;               // CTA-pair kernel: 256-row blocks per band of the tile order
   Epilogue e;
   int* status;
 };
@@ -1035,16 +1036,26 @@ struct Cfg2S : Cfg2<BN> {
   static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
-// Row blocks (of 256) per band of the pair kernel's tile order. The B operand (the
-// weights) is read from DRAM about once per band: between bands the output stream
-// (738 MB for a dense layer's gate/up at d_ff = 5632, B = 4, T = 16384) evicts it from
-// L2. 8-block bands read that GEMM's 46 MB of weights 32 times (1.35 GB read against
-// 314 MB of operands); 32-block bands 8 times. The step time is the same either way
-// (A3K16 and A4K8 dense layers, same box): the traffic is a third of what the tensor
-// pipe's pace would allow.
+// Row blocks (of 256) per band of the pair kernel's tile order: as many as keep the
+// band's A rows within XMOD_BAND_A_BYTES, between 4 and XMOD_TILE_BAND2. Inside a band
+// every column tile reads the band's A rows again, so they must stay in L2 across the
+// band; the B operand (the weights) is read from DRAM about once per band, since between
+// bands the output stream evicts it. A dense layer's gate/up at d_ff = 5632, B = 4, T =
+// 16384 read its 46 MB of weights 32 times with 8-block bands (1.35 GB read against 314
+// MB of operands), 8 times with 32-block bands; the down projection (K = 5632: 2.9 MB of
+// A per row block) read its hidden operand over and over with 32-block bands (919 MB
+// against 342 MB at B = 1), which 11-block bands (32 MB of A) avoid.
 #ifndef XMOD_TILE_BAND2
 #define XMOD_TILE_BAND2 32
 #endif
+#ifndef XMOD_BAND_A_BYTES
+#define XMOD_BAND_A_BYTES (32 << 20)
+#endif
+int band2_rows(int K) {
+  const long per_block = 2L * BM * K * 2;   // bf16 A rows of one 256-row block
+  const long r = (long)XMOD_BAND_A_BYTES / (per_block > 0 ? per_block : 1);
+  return (int)(r < 4 ? 4 : (r > XMOD_TILE_BAND2 ? XMOD_TILE_BAND2 : r));
+}
 
 // STG: the o-projection's / down projection's epilogue inputs are staged in shared
 // memory by one more warp (the loader), see EpiStage.
@@ -1119,7 +1130,7 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       int it = 0;
       for (int tile = pair; tile < args.tiles && !*abort_flag; tile += npairs) {
         int m_blk, n_blk;
-        tile_coords(args, args.tiles_m, tile, m_blk, n_blk, XMOD_TILE_BAND2);
+        tile_coords(args, args.tiles_m, tile, m_blk, n_blk, args.band2);
         const int m0 = m_blk * (2 * BM) + (int)rank * BM;
         const CUtensorMap* mp = &tmB0;
         int brow = n_blk * BN;
@@ -1186,7 +1197,7 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     bool run = true;
     for (int tile = pair; run && tile < args.tiles; tile += npairs) {
       int m_blk, n_blk;
-      tile_coords(args, args.tiles_m, tile, m_blk, n_blk, XMOD_TILE_BAND2);
+      tile_coords(args, args.tiles_m, tile, m_blk, n_blk, args.band2);
       const int m0 = m_blk * (2 * BM) + (int)rank * BM;
       int r[4];
 #pragma unroll
@@ -1221,7 +1232,7 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       const int acc = lt & 1;
       const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
       int m_blk, n_blk;
-      tile_coords(args, args.tiles_m, tile, m_blk, n_blk, XMOD_TILE_BAND2);
+      tile_coords(args, args.tiles_m, tile, m_blk, n_blk, args.band2);
       const int trow0 = m_blk * (2 * BM) + (int)rank * BM;
       const int wrow0 = trow0 + quad * 32;
       if (!STG) epi_prefetch<BN, MODE>(args, args.M, wrow0 + lane, n_blk, (warp - 2) / 4);
@@ -1476,6 +1487,7 @@ cudaError_t launch_bn2(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) 
   TcArgs a;
   if (!setup<BN>(c, p, e, 2 * BM, BN / 2, mA, mB0, mB1, mB2, a)) return cudaErrorInvalidValue;
   if (a.tiles <= 0) return cudaSuccess;
+  a.band2 = band2_rows(p.K);
   // staged inputs: the stream's rows (one-row boxes for gather4) and a's 128-row tiles
   bool stg = epi_stage_enabled() && !e.tok && e.x && e.n_per_seq > 0 && e.T >= e.n_per_seq &&
              p.M % e.n_per_seq == 0 && p.N == e.d &&
