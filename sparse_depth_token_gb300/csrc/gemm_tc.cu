@@ -337,6 +337,12 @@ __device__ __forceinline__ void store32_bf16(__nv_bfloat16* p, const float (&v)[
 #ifndef XMOD_COST_PAIR
 #define XMOD_COST_PAIR 0.82
 #endif
+// The same for 256 x 192 pair tiles (each SM reads 28 KB of operands from shared memory
+// per 64-deep k-block of its 128 x 192 half, against 32 KB per 128 x 256 half of a
+// 256 x 256 pair tile and 40 KB per 128 x 192 single-CTA tile).
+#ifndef XMOD_COST_PAIR192
+#define XMOD_COST_PAIR192 0.88
+#endif
 #ifndef XMOD_PAIR_MARGIN
 #define XMOD_PAIR_MARGIN 0.10
 #endif
@@ -1502,7 +1508,14 @@ cudaError_t launch_bn2(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) 
   int smem = 0, threads = NUM_THREADS;
   switch (e.kind) {
     case EPI_STORE: k = gemm_tc2_kernel<BN, EPI_STORE>; smem = Cfg2<BN>::SMEM; break;
-    case EPI_SWIGLU: k = gemm_tc2_kernel<BN, EPI_SWIGLU>; smem = Cfg2<BN>::SMEM; break;
+    case EPI_SWIGLU:
+      if constexpr (BN == 256) {   // gate / up halves of 128 columns each
+        k = gemm_tc2_kernel<BN, EPI_SWIGLU>;
+        smem = Cfg2<BN>::SMEM;
+        break;
+      } else {
+        return cudaErrorInvalidValue;
+      }
     case EPI_OPROJ:
       if (stg) {
         k = gemm_tc2_kernel<BN, EPI_OPROJ, true>;
@@ -1538,7 +1551,7 @@ cudaError_t launch_bn2(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) 
 
 // Tile widths a problem may use: the q|k|v boundaries must fall on tile edges.
 bool bn_ok(const GemmTcProblem& p, const Epilogue& e, int bn) {
-  if (e.kind == EPI_SWIGLU) return bn == 256;
+  if (e.kind == EPI_SWIGLU) return bn == 256;   // (pair tiles of 192 included)
   // Router logits: 32-wide tiles only, so that a logit's arithmetic never depends on
   // how many router vectors share its launch.
   if (e.kind == EPI_ROUTER) return bn == 32 && p.N <= 32 && p.nB == 1;
@@ -1581,6 +1594,15 @@ int pair_min_waves() {
   return XMOD_PAIR_MIN_WAVES;
 }
 
+// Pair tile width: XMOD_PAIR_BN=256 or 192 (read at every launch) limits the CTA-pair
+// tilings to that width; otherwise the cheaper of the two is taken.
+int pair_bn_forced() {
+  const char* v = getenv("XMOD_PAIR_BN");
+  if (v && strcmp(v, "256") == 0) return 256;
+  if (v && strcmp(v, "192") == 0) return 192;
+  return 0;
+}
+
 // Stream-K choice: XMOD_STREAM_K=1 (read at every launch) runs every GEMM it applies
 // to as stream-K; otherwise none.
 int stream_k_mode() {
@@ -1619,21 +1641,39 @@ cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue&
   // d_ff = 5632 (2 pair waves against 2 single waves of 256) down 83.6 -> 70.2 us,
   // q|k|v 43.8 -> 40.2, o-proj 41.6 -> 39.4; with d = 1536, d_ff = 4096 (a second pair
   // wave on a quarter of the pairs against 192-wide single tiles) pairs lost 2-4 us on
-  // the o-proj and down GEMMs, which the margin keeps single.
+  // the o-proj and down GEMMs, which the margin keeps single. 256 x 192 pair tiles
+  // (cost XMOD_COST_PAIR192) serve those: at d = 1536 they give two waves of 128 pair
+  // tiles, and measured o-proj 30.6 -> 29.0 us, down 53.1 -> 50.8 us against the
+  // 192-wide single-CTA tiles.
   if (p.gather_idx) {   // the gathered-RMSNorm variant exists for single-CTA tiles only
     if (best == 256) return launch_bn<256>(c, p, e);
     if (best == 192) return launch_bn<192>(c, p, e);
     return launch_bn<128>(c, p, e);
   }
-  if (XMOD_GEMM_PAIRS && p.M > BM && !p.M_dev && bn_ok(p, e, 256)) {
+  if (XMOD_GEMM_PAIRS && p.M > BM && !p.M_dev) {
+    // the cheaper of the 256 x 256 and 256 x 192 pair tilings
     const long ptiles_m = (p.M + 2 * BM - 1) / (2 * BM);
-    const int cols = e.kind == EPI_SWIGLU ? 128 : 256;
-    const long tiles = ptiles_m * ((p.N + cols - 1) / cols);
-    const long pairs = max_pairs<256>();
-    const double pair_cost = (double)((tiles + pairs - 1) / pairs) * 256 * XMOD_COST_PAIR;
-    if (tiles >= (long)pair_min_waves() * pairs ||
-        (best > 0 && pair_cost * (1.0 + XMOD_PAIR_MARGIN) <= best_cost))
-      return launch_bn2<256>(c, p, e);
+    int pbn = 0;
+    long ptiles = 0, pairs = 0;
+    double pair_cost = 0.0;
+    const int forced = pair_bn_forced();
+    for (int bn : {256, 192}) {
+      if (!bn_ok(p, e, bn) || (forced && bn != forced)) continue;
+      const int cols = e.kind == EPI_SWIGLU ? bn / 2 : bn;
+      const long tiles = ptiles_m * ((p.N + cols - 1) / cols);
+      const long np = bn == 256 ? max_pairs<256>() : max_pairs<192>();
+      const double cost = (double)((tiles + np - 1) / np) * bn *
+                          (bn == 256 ? XMOD_COST_PAIR : XMOD_COST_PAIR192);
+      if (!pbn || cost < pair_cost) {
+        pbn = bn;
+        ptiles = tiles;
+        pairs = np;
+        pair_cost = cost;
+      }
+    }
+    if (pbn && (ptiles >= (long)pair_min_waves() * pairs ||
+                (best > 0 && pair_cost * (1.0 + XMOD_PAIR_MARGIN) <= best_cost)))
+      return pbn == 256 ? launch_bn2<256>(c, p, e) : launch_bn2<192>(c, p, e);
   }
   // Stream-K at 256-wide tiles, on request only: on the A4K8 block's sparse-layer GEMMs
   // (1.3-2.1 waves) it measured 10-50% slower than the tiling above -- storing and

@@ -37,29 +37,31 @@ CASES = {
 }
 
 
-def _run(X, w, kind, x, lw, bias, pairs):
+def _run(X, w, kind, x, lw, bias, pairs, pair_bn=None):
     dt = w.dtype
     dm = xmod_dims(w)
     ws = workspace(dm, w.K)
     xd = to_dev(x, dt)
-    old = os.environ.get("XMOD_PAIR_MIN_WAVES")
-    old_sk = os.environ.get("XMOD_STREAM_K")
-    os.environ["XMOD_PAIR_MIN_WAVES"] = "0" if pairs else "999999"
-    os.environ["XMOD_STREAM_K"] = "0"   # data-parallel single-CTA tiles: the same k order
+    env = {"XMOD_PAIR_MIN_WAVES": "0" if pairs else "999999",
+           "XMOD_STREAM_K": "0",   # data-parallel single-CTA tiles: the same k order
+           "XMOD_PAIR_BN": str(pair_bn) if pair_bn else None}
+    old = {k: os.environ.get(k) for k in env}
+    for k, v in env.items():
+        if v is None:
+            os.environ.pop(k, None)
+        else:
+            os.environ[k] = v
     try:
         X.reset_status(ws)
         X.layer_fwd(dm, kind, w.K, 0, X.layer_weights(dev_layer(lw, dt), lw["varsigma"]), xd,
                     torch.from_numpy(bias).cuda() if bias is not None else None, None, None, ws)
         assert X.sync_status(ws) == X.OK
     finally:
-        if old is None:
-            del os.environ["XMOD_PAIR_MIN_WAVES"]
-        else:
-            os.environ["XMOD_PAIR_MIN_WAVES"] = old
-        if old_sk is None:
-            del os.environ["XMOD_STREAM_K"]
-        else:
-            os.environ["XMOD_STREAM_K"] = old_sk
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
     return xd
 
 
@@ -80,4 +82,38 @@ def test_pair_gemms_match_single_cta_and_oracle(X, case, kind):
     ref = O.layer_fwd(oracle_dims(w), kind, w.K, 0, oracle_layer(lw, dt), I.to_f64(x, dt),
                       bias=bias)
     got = from_dev(y_pair, dt).reshape(w.B, w.T, w.d)
+    U.assert_close(got, ref["y"], dt, "y", stored_ref=got)
+
+
+CASES_192 = {
+    # d = 384: the o-projection and down GEMMs two 256 x 192 pair tiles wide (q|k|v,
+    # whose q / k / v boundaries fall off the 192 grid, stays on 256-wide pairs)
+    "bf16_d384": I.WORKLOADS["a4k8_bf16"].replace(B=2, T=512, K=4, d=384, hq=3, hkv=1, F=384,
+                                                  seed=43, weight_std=0.049),
+    # d = 320: the second column tile is ragged (128 of its 192 columns exist)
+    "bf16_d320": I.WORKLOADS["a4k8_bf16"].replace(B=2, T=512, K=4, d=320, hq=2, hkv=1, F=264,
+                                                  seed=44, weight_std=0.049),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES_192))
+@pytest.mark.parametrize("kind", [0, 1])
+def test_pair_tiles_192_wide(X, case, kind):
+    """CTA pairs on 256 x 192 tiles (XMOD_PAIR_BN=192) for the o-projection (staged x
+    rows) and the down projection's gated scatter (staged x and a rows): the same dot
+    products in the same k order as the single-CTA tiles, so the stream agrees bit for
+    bit, and the oracle within the bf16 tolerance."""
+    w = CASES_192[case]
+    dt = w.dtype
+    lw = I.layer_weights(w, 4)
+    bias = I.router_bias(w)
+    x = I.residual_stream(w)
+    if kind == 1:
+        x, _ = U.enforce_routing_margin(x, dt, lw["w_r"], bias, w.K)
+    y192 = _run(X, w, kind, x, lw, bias, pairs=True, pair_bn=192)
+    y_single = _run(X, w, kind, x, lw, bias, pairs=False)
+    assert torch.equal(y192.view(torch.int16), y_single.view(torch.int16))
+    ref = O.layer_fwd(oracle_dims(w), kind, w.K, 0, oracle_layer(lw, dt), I.to_f64(x, dt),
+                      bias=bias)
+    got = from_dev(y192, dt).reshape(w.B, w.T, w.d)
     U.assert_close(got, ref["y"], dt, "y", stored_ref=got)
