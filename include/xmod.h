@@ -37,7 +37,18 @@
  *     fallback: a bf16 call on a system without the TMA tensor-map entry point returns
  *     XMOD_ERR_UNSUPPORTED instead of running its projections on FFMA kernels.
  *   - Entry points are stateless and may run concurrently on different streams
- *     with different workspaces.
+ *     with different workspaces. They are capture-safe: a call recorded into a CUDA
+ *     graph and replayed computes the same results as the eager call.
+ *   - Tuning overrides, read from the environment at every launch (the defaults are
+ *     the measured choices; the results do not depend on them beyond the order of
+ *     fp32 additions in stream-K): XMOD_PAIR_MIN_WAVES (waves of 256 x 256 tiles
+ *     from which GEMMs always run on CTA pairs; 0 puts every eligible GEMM on
+ *     pairs), XMOD_PAIR_BN (256 or 192: the only CTA-pair tile width tried),
+ *     XMOD_STREAM_K=1 (stream-K single-CTA GEMMs where they apply) and
+ *     XMOD_STREAM_K_CTAS (their grid cap), XMOD_EPI_STAGE=0 (the pair GEMMs' epilogue
+ *     inputs read from global memory instead of staged in shared memory),
+ *     XMOD_GATHER_FUSED=1 (a sparse layer's gather + RMSNorm1 folded into the q|k|v
+ *     GEMM's operand load).
  */
 #ifndef XMOD_H
 #define XMOD_H
