@@ -40,8 +40,10 @@
  *     with different workspaces. They are capture-safe: a call recorded into a CUDA
  *     graph and replayed computes the same results as the eager call.
  *   - Tuning overrides, read from the environment at every launch (the defaults are
- *     the measured choices; the results do not depend on them beyond the order of
- *     fp32 additions in stream-K): XMOD_PAIR_MIN_WAVES (waves of 256 x 256 tiles
+ *     the measured choices; the results are the same bit for bit except under
+ *     stream-K, which changes the order of fp32 additions, and the fused gather, which
+ *     scales the GEMM's output rows by 1 / rms instead of rounding normalised rows to
+ *     bf16 first): XMOD_PAIR_MIN_WAVES (waves of 256 x 256 tiles
  *     from which GEMMs always run on CTA pairs; 0 puts every eligible GEMM on
  *     pairs), XMOD_PAIR_BN (256 or 192: the only CTA-pair tile width tried),
  *     XMOD_STREAM_K=1 (stream-K single-CTA GEMMs where they apply) and
