@@ -105,6 +105,34 @@ __device__ __forceinline__ float exp2_p(float x) {
 #endif
 }
 
+// Blackwell's paired fp32 arithmetic (two lanes per instruction, each rounded as the
+// scalar instruction would) and three-input max: the softmax warps share their
+// schedulers with the warps that issue the MMAs and the TMA loads, so fewer softmax
+// instructions leave those more issue slots.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 template <int KB, int KST, int VST>
 __global__ void __launch_bounds__(THREADS, (AttnCfg<KB, KST, VST>::MIN_BLOCKS))
 attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -348,17 +376,25 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
       mbar_arrive(S_EMPTY0 + 8 * s);
       const int key0 = j * KB;
       const bool diag = key0 + KB - 1 > qp_min;   // only blocks reaching past a row need the mask
-      float mx = -INFINITY;
       if (diag) {
 #pragma unroll
-        for (int i = 0; i < KB; ++i) {
+        for (int i = 0; i < KB; ++i)
           if (key0 + i > qp) v[i] = -INFINITY;
-          mx = fmaxf(mx, v[i]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < KB; ++i) mx = fmaxf(mx, v[i]);
       }
+      // row max (exact in any order): KB / 16 chains of three-input max over 16 scores
+      float mc[KB / 16];
+#pragma unroll
+      for (int r = 0; r < KB / 16; ++r) {
+        const float* w = v + 16 * r;
+        float t = max3(w[0], w[1], w[2]);
+#pragma unroll
+        for (int i = 3; i < 15; i += 2) t = max3(t, w[i], w[i + 1]);
+        mc[r] = fmaxf(t, w[15]);
+      }
+      float mx = mc[0];
+#pragma unroll
+      for (int r = 1; r + 1 < KB / 16; r += 2) mx = max3(mx, mc[r], mc[r + 1]);
+      if ((KB / 16) % 2 == 0) mx = fmaxf(mx, mc[KB / 16 - 1]);
       const float m_cand = mx * a.scale_log2;
       const bool grow = m_cand > m + kRescaleThreshold;
       const float m_new = grow ? m_cand : m;
@@ -386,22 +422,31 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
       m = m_new;
       // P_j as bf16 pairs over the first KB / 2 columns of S_j's buffer (S_j has been
       // read; P_{j-2}, which the buffer held before S_j, was consumed by then)
-      float sum = 0.f;
+      // p = 2^(s * scale - m), two keys per paired instruction; the row sum in two
+      // paired accumulators (four interleaved partial sums)
+      const uint64_t scale2 = f2_pack(a.scale_log2, a.scale_log2);
+      const uint64_t negm2 = f2_pack(-m, -m);
+      uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
       const uint32_t prow = tmem + lane_off + (uint32_t)(s * KB);
 #pragma unroll
       for (int c = 0; c < KB / 64; ++c) {
         float pk[32];
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
-          const float p0 = exp2_p(fmaf(v[c * 64 + i], a.scale_log2, -m));
-          const float p1 = exp2_p(fmaf(v[c * 64 + i + 1], a.scale_log2, -m));
-          sum += p0 + p1;
+          float x0, x1;
+          f2_unpack(fma_f2(f2_pack(v[c * 64 + i], v[c * 64 + i + 1]), scale2, negm2), x0, x1);
+          const float p0 = exp2_p(x0);
+          const float p1 = exp2_p(x1);
+          acc2[(i >> 1) & 1] = add_f2(acc2[(i >> 1) & 1], f2_pack(p0, p1));
           pk[i / 2] = __uint_as_float(pack_bf16x2(p0, p1));
         }
         tmem_st32(prow + (uint32_t)(32 * c), pk);
       }
       tmem_st_wait();
-      l = l * alpha + sum;
+      float s0, s1, s2, s3;
+      f2_unpack(acc2[0], s0, s1);
+      f2_unpack(acc2[1], s2, s3);
+      l = l * alpha + ((s0 + s2) + (s1 + s3));
       tc_fence_before();
       mbar_arrive(P_FULL0 + 8 * s);
     }
