@@ -1036,6 +1036,45 @@ cudaError_t bw_gemm_dw_split(const Ctx& c, xmod_dtype dt, int M, int N, int K, c
   return cudaSuccess;
 }
 
+// A weight gradient dW = Y^T X in fp32 straight from the token-major Y [rows, Mo] (row
+// stride ldy) and X [rows, N] (row stride ldx): the tensor-core GEMM reads both as stored
+// (MN-major operands, the contraction over the token rows; rows past `rows` read as 0),
+// so no token-contiguous copies are made. Rows [0, s0) of dW go to o0, [s0, s1) (or
+// [s0, Mo) when s1 = 0) to o1, [s1, Mo) to o2; s0 = 0: all of dW to o0; row stride ldo.
+// ok is false where that GEMM does not take the type or shape (the caller transposes).
+struct DwDirect {
+  GemmTcProblem p;
+  Epilogue e;
+  bool ok = false;
+};
+DwDirect dw_direct(xmod_dtype dt, int Mo, int N, int rows, const void* Y, int ldy, const void* X,
+                   int ldx, float* o0, float* o1, float* o2, int s0, int s1, int ldo) {
+  DwDirect w;
+  w.e.kind = EPI_STORE;
+  w.e.out = o0;
+  w.e.ldo = ldo;
+  w.e.out_f32 = true;
+  if (s0 > 0) {
+    w.e.row_split[0] = s0;
+    w.e.out_rows[0] = o1;
+    if (s1 > 0) {
+      w.e.row_split[1] = s1;
+      w.e.out_rows[1] = o2;
+    }
+  }
+  w.p.M = Mo;
+  w.p.N = N;
+  w.p.K = rows;
+  w.p.A = Y;
+  w.p.lda = ldy;
+  w.p.B[0] = X;
+  w.p.ldb = ldx;
+  w.p.a_mn = 1;
+  w.p.b_mn = 1;
+  w.ok = dt == XMOD_BF16 && rows > 0 && gemm_tc_supported(w.p, w.e);
+  return w;
+}
+
 // Column sums out[c] = sum_m (A ? A[m, c] : 1) * Bv[row(m), c] * (w ? w[m] : 1).
 template <typename TB>
 int bw_coldot(const Ctx& c, int64_t M, int d, const float* A, const TB* Bv, const int32_t* idx,
@@ -1206,18 +1245,28 @@ int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weigh
   E* usel = (E*)bat(ws, L.v2);
   BW_RUN("gather_rmsnorm",
          launch_gather_rmsnorm(c, dt, B, T, n, d, x, idx, w->rms1, dm->rms_eps, usel));
-  // dq^T [qw, Mp], u_sel^T [d, Mp]
-  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{dqb, qw, tA, Mp, M, Mp, qw, 0, 0},
-                                                  {usel, d, tB, Mp, M, Mp, d, 0, 0}}));
-  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, qw, d, Mp, tA, Mp, tB, Mp, gr->wq, d, true));
+  const DwDirect dwq = dw_direct(dt, qw, d, M, dqb, qw, usel, d, gr->wq, nullptr, nullptr, 0, 0, d);
+  if (dwq.ok) {
+    BW_RUN("bwd_gemm_dw", launch_gemm_tc(c, dwq.p, dwq.e));
+  } else {   // dq^T [qw, Mp], u_sel^T [d, Mp]
+    BW_RUN("bwd_transpose", transpose_multi(c, dt, {{dqb, qw, tA, Mp, M, Mp, qw, 0, 0},
+                                                    {usel, d, tB, Mp, M, Mp, d, 0, 0}}));
+    BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, qw, d, Mp, tA, Mp, tB, Mp, gr->wq, d, true));
+  }
   float* du_sel = (float*)bat(ws, L.dv2);
   BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qw, dqb, qw, tw.qkv, qw, du_sel, d, true));
   // ======== k, v = u [Wk | Wv]^T on every token
-  // [dk | dv]^T [2kw, BTp], u^T [d, BTp]
-  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{dkv, 2 * kw, tA, BTp, BT, BTp, 2 * kw, 0, 0},
-                                                  {u, d, tB, BTp, BT, BTp, d, 0, 0}}));
-  BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, 2 * kw, d, BTp, tA, BTp, tB, BTp, gr->wk, gr->wv,
-                                         nullptr, kw, 0, d));
+  const DwDirect dwkv = dw_direct(dt, 2 * kw, d, (int)BT, dkv, 2 * kw, u, d, gr->wk, gr->wv,
+                                  nullptr, kw, 0, d);
+  if (dwkv.ok) {
+    BW_RUN("bwd_gemm_dw", launch_gemm_tc(c, dwkv.p, dwkv.e));
+  } else {   // [dk | dv]^T [2kw, BTp], u^T [d, BTp]
+    BW_RUN("bwd_transpose",
+           transpose_multi(c, dt, {{dkv, 2 * kw, tA, BTp, BT, BTp, 2 * kw, 0, 0},
+                                   {u, d, tB, BTp, BT, BTp, d, 0, 0}}));
+    BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, 2 * kw, d, BTp, tA, BTp, tB, BTp, gr->wk,
+                                           gr->wv, nullptr, kw, 0, d));
+  }
   float* du = (float*)bat(ws, L.du);
   BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, BT, d, 2 * kw, dkv, 2 * kw, tw.qkv + (size_t)d * qw,
                                 2 * kw, du, d, true));
@@ -1545,10 +1594,14 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
 
   if (ffn) {
   // ======== FFN: f = H Wd^T, H = silu(G) U, [G | U] = v2 [Wg | Wu]^T
-  // df^T [d, Mp], H^T [F, Mp]
-  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{df, d, tA, Mp, M, Mp, d, 0, 0},
-                                                  {H, F, tB, Mp, M, Mp, F, 0, 0}}));
-  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, d, F, Mp, tA, Mp, tB, Mp, gr->w_down, F, true));
+  const DwDirect dwd = dw_direct(dt, d, F, M, df, d, H, F, gr->w_down, nullptr, nullptr, 0, 0, F);
+  if (dwd.ok) {
+    BW_RUN("bwd_gemm_dw", launch_gemm_tc(c, dwd.p, dwd.e));
+  } else {   // df^T [d, Mp], H^T [F, Mp]
+    BW_RUN("bwd_transpose", transpose_multi(c, dt, {{df, d, tA, Mp, M, Mp, d, 0, 0},
+                                                    {H, F, tB, Mp, M, Mp, F, 0, 0}}));
+    BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, d, F, Mp, tA, Mp, tB, Mp, gr->w_down, F, true));
+  }
   float* dH = (float*)bat(ws, L.dH);
   BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, F, d, df, d, tw.d, d, dH, F, true));
   E* dGU = (E*)bat(ws, L.dGU);
@@ -1558,11 +1611,16 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     BW_RUN("swiglu", launch_pdl(swiglu_bwd_kernel<E>, dim3(blk), dim3(256), 0, c.stream,
                                 (int64_t)M, F, (const E*)gu, (const float*)dH, dGU));
   }
-  // [dG | dU]^T [2F, Mp], v2^T [d, Mp]
-  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{dGU, 2 * F, tA, Mp, M, Mp, 2 * F, 0, 0},
-                                                  {v2, d, tB, Mp, M, Mp, d, 0, 0}}));
-  BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, 2 * F, d, Mp, tA, Mp, tB, Mp, gr->w_gate,
-                                         gr->w_up, nullptr, F, 0, d));
+  const DwDirect dwgu = dw_direct(dt, 2 * F, d, M, dGU, 2 * F, v2, d, gr->w_gate, gr->w_up,
+                                  nullptr, F, 0, d);
+  if (dwgu.ok) {
+    BW_RUN("bwd_gemm_dw", launch_gemm_tc(c, dwgu.p, dwgu.e));
+  } else {   // [dG | dU]^T [2F, Mp], v2^T [d, Mp]
+    BW_RUN("bwd_transpose", transpose_multi(c, dt, {{dGU, 2 * F, tA, Mp, M, Mp, 2 * F, 0, 0},
+                                                    {v2, d, tB, Mp, M, Mp, d, 0, 0}}));
+    BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, 2 * F, d, Mp, tA, Mp, tB, Mp, gr->w_gate,
+                                           gr->w_up, nullptr, F, 0, d));
+  }
   float* dv2 = (float*)bat(ws, L.dv2);
   BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, 2 * F, dGU, 2 * F, tw.gu, 2 * F, dv2, d, true));
   float* rstd2 = (float*)bat(ws, L.rstd2);
@@ -1589,10 +1647,14 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   }
 
   // ======== a = o Wo^T
-  // da^T [d, Mp], o^T [qw, Mp]
-  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{da, d, tA, Mp, M, Mp, d, 0, 0},
-                                                  {o, qw, tB, Mp, M, Mp, qw, 0, 0}}));
-  BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, d, qw, Mp, tA, Mp, tB, Mp, gr->wo, qw, true));
+  const DwDirect dwo = dw_direct(dt, d, qw, M, da, d, o, qw, gr->wo, nullptr, nullptr, 0, 0, qw);
+  if (dwo.ok) {
+    BW_RUN("bwd_gemm_dw", launch_gemm_tc(c, dwo.p, dwo.e));
+  } else {   // da^T [d, Mp], o^T [qw, Mp]
+    BW_RUN("bwd_transpose", transpose_multi(c, dt, {{da, d, tA, Mp, M, Mp, d, 0, 0},
+                                                    {o, qw, tB, Mp, M, Mp, qw, 0, 0}}));
+    BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, d, qw, Mp, tA, Mp, tB, Mp, gr->wo, qw, true));
+  }
   float* dO = (float*)bat(ws, L.dO);
   const bool mma_attn = tc && attn_bwd_mma_supported(hd, fullkv ? qw : qkv_w, qw);
   BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, qw, d, da, d, tw.o, d, dO, qw, !mma_attn));
@@ -1679,11 +1741,17 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   }
 
   // ======== q, k, v = u [Wq | Wk | Wv]^T
-  // [dq | dk | dv]^T [qkv_w, Mp], u^T [d, Mp]
-  BW_RUN("bwd_transpose", transpose_multi(c, dt, {{dqkv, qkv_w, tA, Mp, M, Mp, qkv_w, 0, 0},
-                                                  {u, d, tB, Mp, M, Mp, d, 0, 0}}));
-  BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, qkv_w, d, Mp, tA, Mp, tB, Mp, gr->wq, gr->wk,
-                                         gr->wv, qw, qw + kw, d));
+  const DwDirect dwqkv = dw_direct(dt, qkv_w, d, M, dqkv, qkv_w, u, d, gr->wq, gr->wk, gr->wv,
+                                   qw, qw + kw, d);
+  if (dwqkv.ok) {
+    BW_RUN("bwd_gemm_dw", launch_gemm_tc(c, dwqkv.p, dwqkv.e));
+  } else {   // [dq | dk | dv]^T [qkv_w, Mp], u^T [d, Mp]
+    BW_RUN("bwd_transpose",
+           transpose_multi(c, dt, {{dqkv, qkv_w, tA, Mp, M, Mp, qkv_w, 0, 0},
+                                   {u, d, tB, Mp, M, Mp, d, 0, 0}}));
+    BW_RUN("bwd_gemm_dw", bw_gemm_dw_split(c, dt, qkv_w, d, Mp, tA, Mp, tB, Mp, gr->wq, gr->wk,
+                                           gr->wv, qw, qw + kw, d));
+  }
   float* du = (float*)bat(ws, L.du);
   BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qkv_w, dqkv, qkv_w, tw.qkv, qkv_w, du, d, true));
   // u = RMSNorm(x_sel) g1; the gather's backward adds into the token's row of dx

@@ -98,6 +98,57 @@ struct TcArgs {
 #define XMOD_TILE_BAND 16
 #endif
 
+// An operand stored [K, rows] (its rows contiguous) reaches shared memory as 64 x 64 TMA
+// boxes, one per 64 of the tile's rows: box j holds rows 64j .. 64j + 63 for the 64 k of
+// the block, one 128-byte line (64 rows) per k under the 128-byte swizzle, 8 KB a box.
+// The MMA reads it as an MN-major operand: 64-row swizzle atoms one box apart (leading
+// byte offset) and groups of 8 k 1 KB apart (stride byte offset); a 16-deep MMA step
+// moves 2 KB along k. The instruction descriptor marks the operand MN-major.
+constexpr int MN_BOX_BYTES = 64 * BK * 2;
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);            // start address
+  d |= (uint64_t)(MN_BOX_BYTES >> 4) << 16;          // leading byte offset: next 64 rows
+  d |= (uint64_t)(1024u >> 4) << 32;                 // stride byte offset: next 8 k
+  d |= (uint64_t)1 << 46;                            // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                            // layout: 128-byte swizzle
+  return d;
+}
+// The kernels take the layout as a template parameter MN (both operands MN-major, or both
+// K-major), so the K-major kernels' MMA-issuing loop keeps compile-time descriptors.
+constexpr uint32_t kIdescMajorMN = (1u << 15) | (1u << 16);   // A and B MN-major
+// Descriptor of an operand tile and its advance per 16-deep MMA step (in 16-byte units):
+// K-major 32 bytes along each row, MN-major 2 KB (two groups of 8 k).
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t addr) {
+  if constexpr (MN) return smem_desc_sw128_mn(addr);
+  else return smem_desc_sw128(addr);
+}
+template <bool MN>
+constexpr uint64_t kOperandStep = MN ? 128ull : 2ull;
+// The loads of `rows` rows of an operand tile from row r0, k-block kb.
+template <bool MN>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                             int kb, int r0, int rows) {
+  if constexpr (!MN) {
+    tma_load_2d(dst, map, bar, kb * BK, r0);
+  } else {
+    for (int j = 0; j < rows / 64; ++j)
+      tma_load_2d(dst + j * MN_BOX_BYTES, map, bar, r0 + 64 * j, kb * BK);
+  }
+}
+// The same for a CTA of a pair, the bytes counted on a barrier of either CTA.
+template <bool MN>
+__device__ __forceinline__ void load_operand_pair(uint32_t dst, const CUtensorMap* map,
+                                                  uint32_t bar, int kb, int r0, int rows) {
+  if constexpr (!MN) {
+    tma_load_2d_pair(dst, map, bar, kb * BK, r0);
+  } else {
+    for (int j = 0; j < rows / 64; ++j)
+      tma_load_2d_pair(dst + j * MN_BOX_BYTES, map, bar, r0 + 64 * j, kb * BK);
+  }
+}
+
 __device__ __forceinline__ void tile_coords(const TcArgs& a, int tiles_m, int tile, int& m_blk,
                                             int& n_blk, int band_rows = XMOD_TILE_BAND) {
   const int per_band = band_rows * a.tiles_n;
@@ -709,7 +760,7 @@ __device__ __forceinline__ bool epilogue_tile(const TcArgs& a, int M, int wrow0,
   return true;
 }
 
-template <int BN, int MODE, bool GATHER = false>
+template <int BN, int MODE, bool GATHER = false, bool MN = false>
 __global__ void __launch_bounds__(NUM_THREADS + (GATHER ? 32 * XF_WARPS : 0), 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
@@ -838,20 +889,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
           if (!mbar_wait(EMPTY(s), ph ^ 1u, abort_flag, args.status)) break;
           mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
-          tma_load_2d(sA + s * C::A_BYTES, &tmA, FULL(s), kb * BK, m0);
+          load_operand<MN>(sA + s * C::A_BYTES, &tmA, FULL(s), kb, m0, BM);
           if (MODE == EPI_SWIGLU) {
             const int h0 = n_blk * (BN / 2);
             tma_load_2d(sB + s * C::B_BYTES, &tmB0, FULL(s), kb * BK, h0);
             tma_load_2d(sB + s * C::B_BYTES + (BN / 2) * 128, &tmB1, FULL(s), kb * BK, h0);
           } else {
-            tma_load_2d(sB + s * C::B_BYTES, mp, FULL(s), kb * BK, brow);
+            load_operand<MN>(sB + s * C::B_BYTES, mp, FULL(s), kb, brow, BN);
           }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN) | (MN ? kIdescMajorMN : 0u);
+      constexpr uint64_t step = kOperandStep<MN>;
       int it = 0;
       Work w;
       for (int lt = 0; work_at(args, ext, nk, lt, w) && !*abort_flag; ++lt) {
@@ -870,11 +922,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             break;
           }
           tc_fence_after();
-          const uint64_t ad = smem_desc_sw128(sA + s * C::A_BYTES);
-          const uint64_t bd = smem_desc_sw128(sB + s * C::B_BYTES);
+          const uint64_t ad = operand_desc<MN>(sA + s * C::A_BYTES);
+          const uint64_t bd = operand_desc<MN>(sB + s * C::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb != kb0 || k) ? 1u : 0u);
+            mma_bf16(d_tmem, ad + step * k, bd + step * k, idesc, (kb != kb0 || k) ? 1u : 0u);
           mma_commit(EMPTY(s));
         }
         if (!ok) break;
@@ -1065,7 +1117,7 @@ int band2_rows(int K) {
 
 // STG: the o-projection's / down projection's epilogue inputs are staged in shared
 // memory by one more warp (the loader), see EpiStage.
-template <int BN, int MODE, bool STG = false>
+template <int BN, int MODE, bool STG = false, bool MN = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS + (STG ? 32 : 0), 1)
 gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
@@ -1159,14 +1211,15 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           if (!mbar_wait_cluster(EMPTY(s), ph ^ 1u, abort_flag, args.status)) break;
           const uint32_t full0 = mapa_shared(FULL(s), 0);
           if (rank == 0) mbar_arrive_expect_tx(FULL(s), 2 * C::STAGE_BYTES);
-          tma_load_2d_pair(sA + s * C::A_BYTES, &tmA, full0, kb * BK, m0);
-          tma_load_2d_pair(sB + s * C::B_BYTES, mp, full0, kb * BK, brow);
+          load_operand_pair<MN>(sA + s * C::A_BYTES, &tmA, full0, kb, m0, BM);
+          load_operand_pair<MN>(sB + s * C::B_BYTES, mp, full0, kb, brow, BN / 2);
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN);
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN) | (MN ? kIdescMajorMN : 0u);
+      constexpr uint64_t step = kOperandStep<MN>;
       int it = 0, lt = 0;
       for (int tile = pair; tile < args.tiles && !*abort_flag; tile += npairs, ++lt) {
         const int acc = lt & 1;
@@ -1183,11 +1236,11 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             break;
           }
           tc_fence_after();
-          const uint64_t ad = smem_desc_sw128(sA + s * C::A_BYTES);
-          const uint64_t bd = smem_desc_sw128(sB + s * C::B_BYTES);
+          const uint64_t ad = operand_desc<MN>(sA + s * C::A_BYTES);
+          const uint64_t bd = operand_desc<MN>(sB + s * C::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16_pair(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            mma_bf16_pair(d_tmem, ad + step * k, bd + step * k, idesc, (kb | k) != 0 ? 1u : 0u);
           mma_commit_pair(EMPTY(s));
         }
         if (!ok) break;
@@ -1319,6 +1372,8 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
   a.g_eps = p.gather_eps;
   if (p.gather_idx) {   // the stream's rows, one-row boxes for gather4
     if (!make_map(&mA, p.A, p.K, p.gather_rows, p.lda, 1)) return false;
+  } else if (p.a_mn) {  // [K, M]: 64 x 64 boxes
+    if (!make_map(&mA, p.A, p.M, p.K, p.lda, BK)) return false;
   } else if (!make_map(&mA, p.A, p.K, p.M, p.lda, BM)) {
     return false;
   }
@@ -1362,7 +1417,11 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
     tiles_n = (p.N + BN / 2 - 1) / (BN / 2);
   } else {
     const int rows0 = p.nB > 1 ? p.split[0] : (p.b_rows > 0 ? p.b_rows : p.N);
-    if (!make_map(&mB0, p.B[0], p.K, rows0, p.ldb, b_box)) return false;
+    if (p.b_mn) {   // [K, N]: 64 x 64 boxes
+      if (!make_map(&mB0, p.B[0], rows0, p.K, p.ldb, BK)) return false;
+    } else if (!make_map(&mB0, p.B[0], p.K, rows0, p.ldb, b_box)) {
+      return false;
+    }
     if (p.nB > 1) {
       a.n_split1 = p.split[0];
       const int rows1 = (p.nB > 2 ? p.split[1] : p.N) - p.split[0];
@@ -1437,7 +1496,9 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, b
     k = gemm_tc_kernel<BN, EPI_ROUTER>;
   } else {
     switch (e.kind) {
-      case EPI_STORE: k = gemm_tc_kernel<BN, EPI_STORE>; break;
+      case EPI_STORE:
+        k = p.a_mn ? gemm_tc_kernel<BN, EPI_STORE, false, true> : gemm_tc_kernel<BN, EPI_STORE>;
+        break;
       case EPI_OPROJ: k = gemm_tc_kernel<BN, EPI_OPROJ>; break;
       case EPI_SWIGLU: k = gemm_tc_kernel<BN, EPI_SWIGLU>; break;
       case EPI_DOWN_SCATTER: k = gemm_tc_kernel<BN, EPI_DOWN_SCATTER>; break;
@@ -1445,11 +1506,12 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, b
     }
   }
   if (!k) return cudaErrorInvalidValue;
-  static bool attr_set[5] = {false, false, false, false, false};
-  if (!attr_set[e.kind]) {
+  static bool attr_set[2][5] = {};   // [MN-major][epilogue]: one entry per kernel
+  const int mn = p.a_mn ? 1 : 0;
+  if (!attr_set[mn][e.kind]) {
     cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     if (err != cudaSuccess) return err;
-    attr_set[e.kind] = true;
+    attr_set[mn][e.kind] = true;
   }
   return launch_pdl(k, dim3(grid), dim3(NUM_THREADS), Cf::SMEM, c.stream, mA, mB0, mB1, mB2, a);
 }
@@ -1507,7 +1569,15 @@ cudaError_t launch_bn2(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) 
             const CUtensorMap, const CUtensorMap, const TcArgs) = nullptr;
   int smem = 0, threads = NUM_THREADS;
   switch (e.kind) {
-    case EPI_STORE: k = gemm_tc2_kernel<BN, EPI_STORE>; smem = Cfg2<BN>::SMEM; break;
+    case EPI_STORE:
+      if constexpr (BN == 256) {   // MN-major B halves need whole 64-row boxes
+        k = p.a_mn ? gemm_tc2_kernel<BN, EPI_STORE, false, true> : gemm_tc2_kernel<BN, EPI_STORE>;
+      } else {
+        if (p.a_mn) return cudaErrorInvalidValue;
+        k = gemm_tc2_kernel<BN, EPI_STORE>;
+      }
+      smem = Cfg2<BN>::SMEM;
+      break;
     case EPI_SWIGLU:
       if constexpr (BN == 256) {   // gate / up halves of 128 columns each
         k = gemm_tc2_kernel<BN, EPI_SWIGLU>;
@@ -1538,11 +1608,12 @@ cudaError_t launch_bn2(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) 
       break;
     default: return cudaErrorInvalidValue;
   }
-  static bool attr_set[2][4] = {};
-  if (!attr_set[stg][e.kind]) {
+  static bool attr_set[2][2][4] = {};   // [MN-major][staged inputs][epilogue]: per kernel
+  const int mn = p.a_mn ? 1 : 0;
+  if (!attr_set[mn][stg][e.kind]) {
     cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
-    attr_set[stg][e.kind] = true;
+    attr_set[mn][stg][e.kind] = true;
   }
   const int pairs = a.tiles < max_pairs<BN>() ? a.tiles : max_pairs<BN>();
   return launch_pdl(k, dim3(2 * pairs), dim3(threads), smem, c.stream, mA, mB0, mB1, mB2, mX,
@@ -1570,7 +1641,12 @@ bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e) {
        p.gather_rows <= 0 || p.lda != p.K || !p.gather_gamma ||
        ((uintptr_t)p.gather_gamma & 15)))
     return false;
-  if (p.K % 8 || p.lda % 8 || p.ldb % 8) return false;
+  if (p.a_mn || p.b_mn) {   // both MN-major, plain stores of one B
+    if (!p.a_mn || !p.b_mn || e.kind != EPI_STORE || p.gather_idx || p.nB != 1 ||
+        p.ksplit > 1 || p.b_rows)
+      return false;
+  }
+  if ((p.K % 8 && !(p.a_mn && p.b_mn)) || p.lda % 8 || p.ldb % 8) return false;
   if (p.N % 8 && e.kind != EPI_ROUTER) return false;   // the others store 8-column groups
   if (p.b_rows && (p.b_rows < p.N || p.nB != 1)) return false;
   if (p.ksplit > 1 && (e.kind != EPI_ROUTER || p.ksplit > (p.K + BK - 1) / BK)) return false;
@@ -1659,6 +1735,7 @@ cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue&
     const int forced = pair_bn_forced();
     for (int bn : {256, 192}) {
       if (!bn_ok(p, e, bn) || (forced && bn != forced)) continue;
+      if (p.b_mn && bn != 256) continue;   // a CTA's B half must be whole 64-row boxes
       const int cols = e.kind == EPI_SWIGLU ? bn / 2 : bn;
       const long tiles = ptiles_m * ((p.N + cols - 1) / cols);
       const long np = bn == 256 ? max_pairs<256>() : max_pairs<192>();
@@ -1679,7 +1756,8 @@ cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue&
   // (1.3-2.1 waves) it measured 10-50% slower than the tiling above -- storing and
   // re-reading the fp32 partial tiles (128 KB per CTA, all CTAs at once) costs more
   // than the partial last wave it removes.
-  if (stream_k_mode() == 1 && bn_ok(p, e, 256) && !p.M_dev && p.ksplit <= 1) {
+  if (stream_k_mode() == 1 && bn_ok(p, e, 256) && !p.M_dev && p.ksplit <= 1 && !p.a_mn &&
+      !p.b_mn) {
     const int cols = e.kind == EPI_SWIGLU ? 128 : 256;
     const long tiles = (long)tiles_m * ((p.N + cols - 1) / cols);
     if (stream_k_grid(c, tiles, (p.K + BK - 1) / BK) > 0) return launch_bn<256>(c, p, e, true);

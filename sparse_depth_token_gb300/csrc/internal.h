@@ -272,6 +272,11 @@ struct GemmTcProblem {
   int64_t gather_rows = 0;
   const void* gather_gamma = nullptr;
   float gather_eps = 0.f;
+  // Operands stored with the contraction index as the row (STORE epilogue, one B):
+  // a_mn: A is [K, M] (M contiguous, lda elements per row k); b_mn: B is [K, N]. With
+  // both set K is free (rows past K read as zero), e.g. weight gradients dW = dY^T X
+  // straight from token-major dY and X.
+  int a_mn = 0, b_mn = 0;
 };
 bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e);
 cudaError_t launch_gemm_tc(const Ctx& c, const GemmTcProblem& p, const Epilogue& e);
