@@ -1075,6 +1075,42 @@ DwDirect dw_direct(xmod_dtype dt, int Mo, int N, int rows, const void* Y, int ld
   return w;
 }
 
+// An activation gradient dX [rows, N] = dY [rows, K] W (row strides ldy, ldo; fp32 out if
+// f32out), W a projection's weights stacked along K -- w0 for k < k1, w1 for k1 <= k < k2
+// (or < K when w2 is null), w2 for k >= k2, each [part rows, N] with row stride ldw:
+// the tensor-core GEMM reads the weights as stored (an MN-major B operand, one tensor
+// map per part), so they are not transposed. ok is false where that GEMM does not take
+// the type or shape.
+struct DxDirect {
+  GemmTcProblem p;
+  Epilogue e;
+  bool ok = false;
+};
+DxDirect dx_direct(xmod_dtype dt, int rows, int N, int K, const void* dY, int ldy, const void* w0,
+                   const void* w1, const void* w2, int k1, int k2, int ldw, void* out, int ldo,
+                   bool f32out) {
+  DxDirect x;
+  x.e.kind = EPI_STORE;
+  x.e.out = out;
+  x.e.ldo = ldo;
+  x.e.out_f32 = f32out;
+  x.p.M = rows;
+  x.p.N = N;
+  x.p.K = K;
+  x.p.A = dY;
+  x.p.lda = ldy;
+  x.p.B[0] = w0;
+  x.p.B[1] = w1;
+  x.p.B[2] = w2;
+  x.p.nB = w2 ? 3 : w1 ? 2 : 1;
+  x.p.split[0] = k1;
+  x.p.split[1] = k2;
+  x.p.ldb = ldw;
+  x.p.b_mn = 1;
+  x.ok = dt == XMOD_BF16 && rows > 0 && gemm_tc_supported(x.p, x.e);
+  return x;
+}
+
 // Column sums out[c] = sum_m (A ? A[m, c] : 1) * Bv[row(m), c] * (w ? w[m] : 1).
 template <typename TB>
 int bw_coldot(const Ctx& c, int64_t M, int d, const float* A, const TB* Bv, const int32_t* idx,
@@ -1138,7 +1174,7 @@ int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weigh
                 const void* x, const int32_t* idx, void* dx, const xmod_layer_grads* gr,
                 void* ws, const BwLayout& L, const E* kvb, const E* qb, const E* kpre,
                 const E* qpre, const E* vt, bool v_transposed, const E* o, const void* dO,
-                bool mma, const float* dh) {
+                bool mma, const float* dh, bool dx_mn) {
   const xmod_dtype dt = dm->dtype;
   const int B = dm->B, T = dm->T, d = dm->d, hq = dm->n_heads, hkv = dm->n_kv_heads,
             hd = dm->head_dim;
@@ -1254,7 +1290,14 @@ int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weigh
     BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, qw, d, Mp, tA, Mp, tB, Mp, gr->wq, d, true));
   }
   float* du_sel = (float*)bat(ws, L.dv2);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qw, dqb, qw, tw.qkv, qw, du_sel, d, true));
+  if (dx_mn) {
+    const DxDirect x = dx_direct(dt, M, d, qw, dqb, qw, w->wq, nullptr, nullptr, 0, 0, d, du_sel,
+                                 d, true);
+    if (!x.ok) return XMOD_ERR_UNSUPPORTED;
+    BW_RUN("bwd_gemm_dx", launch_gemm_tc(c, x.p, x.e));
+  } else {
+    BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qw, dqb, qw, tw.qkv, qw, du_sel, d, true));
+  }
   // ======== k, v = u [Wk | Wv]^T on every token
   const DwDirect dwkv = dw_direct(dt, 2 * kw, d, (int)BT, dkv, 2 * kw, u, d, gr->wk, gr->wv,
                                   nullptr, kw, 0, d);
@@ -1268,8 +1311,15 @@ int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weigh
                                            gr->wv, nullptr, kw, 0, d));
   }
   float* du = (float*)bat(ws, L.du);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, BT, d, 2 * kw, dkv, 2 * kw, tw.qkv + (size_t)d * qw,
-                                2 * kw, du, d, true));
+  if (dx_mn) {
+    const DxDirect x = dx_direct(dt, BT, d, 2 * kw, dkv, 2 * kw, w->wk, w->wv, nullptr, kw, 0, d,
+                                 du, d, true);
+    if (!x.ok) return XMOD_ERR_UNSUPPORTED;
+    BW_RUN("bwd_gemm_dx", launch_gemm_tc(c, x.p, x.e));
+  } else {
+    BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, BT, d, 2 * kw, dkv, 2 * kw, tw.qkv + (size_t)d * qw,
+                                  2 * kw, du, d, true));
+  }
   // ======== u = RMSNorm(x) g1 on every token; the selected rows add their query's part
   // and the gradient through h
   float* dadd = (float*)bat(ws, L.h);
@@ -1567,9 +1617,27 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   float* dh = nullptr;   // the gradient reaching h = x_sel + a through the FFN half
   const E* da = dae;     // the gradient reaching a (FullAttn: dy itself)
 
-  // ======== every weight the activation gradients multiply by, transposed in one launch
+  // ======== the weights the activation gradients multiply by: read as stored when the
+  // tensor-core GEMM takes every such product of this layer (dx_mn), else all transposed
+  // in one launch. (The checks use the aligned scratch for the gradients' addresses.)
   const TwParts<E> tw = tw_parts<E>(dm, tW);
-  {
+  bool dx_mn = dt == XMOD_BF16;
+  if (dx_mn && ffn)
+    dx_mn = dx_direct(dt, M, F, d, tW, d, w->w_down, nullptr, nullptr, 0, 0, F, tW, F, true).ok &&
+            dx_direct(dt, M, d, 2 * F, tW, 2 * F, w->w_gate, w->w_up, nullptr, F, 0, d, tW, d,
+                      true).ok;
+  if (dx_mn && attn) {
+    dx_mn = dx_direct(dt, M, qw, d, tW, d, w->wo, nullptr, nullptr, 0, 0, qw, tW, qw, true).ok;
+    if (fullkv)
+      dx_mn = dx_mn &&
+              dx_direct(dt, M, d, qw, tW, qw, w->wq, nullptr, nullptr, 0, 0, d, tW, d, true).ok &&
+              dx_direct(dt, B * T, d, 2 * kw, tW, 2 * kw, w->wk, w->wv, nullptr, kw, 0, d, tW, d,
+                        true).ok;
+    else
+      dx_mn = dx_mn && dx_direct(dt, M, d, qkv_w, tW, qkv_w, w->wq, w->wk, w->wv, qw, qw + kw, d,
+                                 tW, d, true).ok;
+  }
+  if (!dx_mn) {
     TrSpec sp[7];
     int ns = 0;
     if (ffn) {
@@ -1603,7 +1671,14 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
     BW_RUN("bwd_gemm_dw", bw_gemm(c, dt, d, F, Mp, tA, Mp, tB, Mp, gr->w_down, F, true));
   }
   float* dH = (float*)bat(ws, L.dH);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, F, d, df, d, tw.d, d, dH, F, true));
+  if (dx_mn) {
+    const DxDirect x = dx_direct(dt, M, F, d, df, d, w->w_down, nullptr, nullptr, 0, 0, F, dH, F,
+                                 true);
+    if (!x.ok) return XMOD_ERR_UNSUPPORTED;
+    BW_RUN("bwd_gemm_dx", launch_gemm_tc(c, x.p, x.e));
+  } else {
+    BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, F, d, df, d, tw.d, d, dH, F, true));
+  }
   E* dGU = (E*)bat(ws, L.dGU);
   {
     const int64_t tot = (int64_t)M * F / (16 / sizeof(E));
@@ -1622,7 +1697,14 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
                                            gr->w_up, nullptr, F, 0, d));
   }
   float* dv2 = (float*)bat(ws, L.dv2);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, 2 * F, dGU, 2 * F, tw.gu, 2 * F, dv2, d, true));
+  if (dx_mn) {
+    const DxDirect x = dx_direct(dt, M, d, 2 * F, dGU, 2 * F, w->w_gate, w->w_up, nullptr, F, 0,
+                                 d, dv2, d, true);
+    if (!x.ok) return XMOD_ERR_UNSUPPORTED;
+    BW_RUN("bwd_gemm_dx", launch_gemm_tc(c, x.p, x.e));
+  } else {
+    BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, 2 * F, dGU, 2 * F, tw.gu, 2 * F, dv2, d, true));
+  }
   float* rstd2 = (float*)bat(ws, L.rstd2);
   if (attn) {
     // v2 = RMSNorm(h) g2; h = x_sel + a: dh reaches x_sel and (with dae) a
@@ -1657,7 +1739,14 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   }
   float* dO = (float*)bat(ws, L.dO);
   const bool mma_attn = tc && attn_bwd_mma_supported(hd, fullkv ? qw : qkv_w, qw);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, qw, d, da, d, tw.o, d, dO, qw, !mma_attn));
+  if (dx_mn) {
+    const DxDirect x = dx_direct(dt, M, qw, d, da, d, w->wo, nullptr, nullptr, 0, 0, qw, dO, qw,
+                                 !mma_attn);
+    if (!x.ok) return XMOD_ERR_UNSUPPORTED;
+    BW_RUN("bwd_gemm_dx", launch_gemm_tc(c, x.p, x.e));
+  } else {
+    BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, qw, d, da, d, tw.o, d, dO, qw, !mma_attn));
+  }
 
   // ======== attention
   E* dqkv = (E*)bat(ws, L.dqkv);
@@ -1665,7 +1754,7 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
   const bool dq_tc = mma_attn && v_transposed && attn_bwd_dq_tc_supported(hd, qkv_w, qw, kt_ld);
   if (fullkv)
     return fullkv_tail<E>(c, dm, n, w, x, idx, dx, gr, ws, L, kvb, qb, kpre, qpre, vt,
-                          v_transposed, o, dO, mma_attn, dh);
+                          v_transposed, o, dO, mma_attn, dh, dx_mn);
   if (dq_tc) {   // tcgen05 (lse from the forward): dq, then dk and dv
     E* kt = (E*)bat(ws, L.kt);
     E* qt = (E*)bat(ws, L.qt);
@@ -1753,7 +1842,14 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
                                            gr->wv, qw, qw + kw, d));
   }
   float* du = (float*)bat(ws, L.du);
-  BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qkv_w, dqkv, qkv_w, tw.qkv, qkv_w, du, d, true));
+  if (dx_mn) {
+    const DxDirect x = dx_direct(dt, M, d, qkv_w, dqkv, qkv_w, w->wq, w->wk, w->wv, qw, qw + kw,
+                                 d, du, d, true);
+    if (!x.ok) return XMOD_ERR_UNSUPPORTED;
+    BW_RUN("bwd_gemm_dx", launch_gemm_tc(c, x.p, x.e));
+  } else {
+    BW_RUN("bwd_gemm_dx", bw_gemm(c, dt, M, d, qkv_w, dqkv, qkv_w, tw.qkv, qkv_w, du, d, true));
+  }
   // u = RMSNorm(x_sel) g1; the gather's backward adds into the token's row of dx
   float* rstd1 = (float*)bat(ws, L.rstd1);
   BW_RUN("bwd_rows", launch_pdl(rms_bwd_kernel<E, E>, dim3(rowblk), dim3(BW_WARPS * 32), 0,

@@ -85,6 +85,7 @@ struct TcArgs {
   float* sk_part;          // per-CTA partial accumulator slots, BM x BN fp32 each
   int* sk_flag;            // per-CTA "slot published" flags, 0 between launches
   int band2;               // CTA-pair kernel: 256-row blocks per band of the tile order
+  int k_split1, k_split2;  // MN-major B stacked along K: first k of B map 1 / map 2
   Epilogue e;
   int* status;
 };
@@ -98,9 +99,10 @@ struct TcArgs {
 #define XMOD_TILE_BAND 16
 #endif
 
-// An operand stored [K, rows] (its rows contiguous) reaches shared memory as 64 x 64 TMA
-// boxes, one per 64 of the tile's rows: box j holds rows 64j .. 64j + 63 for the 64 k of
-// the block, one 128-byte line (64 rows) per k under the 128-byte swizzle, 8 KB a box.
+// An operand stored [K, rows] (its rows contiguous) reaches shared memory in one TMA
+// load through a 3-D tensor map (64 rows, k, 64-row chunk): chunk j holds rows 64j ..
+// 64j + 63 for the 64 k of the block, one 128-byte line (64 rows) per k under the
+// 128-byte swizzle, 8 KB a chunk.
 // The MMA reads it as an MN-major operand: 64-row swizzle atoms one box apart (leading
 // byte offset) and groups of 8 k 1 KB apart (stride byte offset); a 16-deep MMA step
 // moves 2 KB along k. The instruction descriptor marks the operand MN-major.
@@ -114,9 +116,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr) {
   d |= (uint64_t)2 << 61;                            // layout: 128-byte swizzle
   return d;
 }
-// The kernels take the layout as a template parameter MN (both operands MN-major, or both
-// K-major), so the K-major kernels' MMA-issuing loop keeps compile-time descriptors.
-constexpr uint32_t kIdescMajorMN = (1u << 15) | (1u << 16);   // A and B MN-major
+// The kernels take the operand layout as a template parameter LAY, so the K-major
+// kernels' MMA-issuing loop keeps compile-time descriptors: LAY_KK both operands K-major,
+// LAY_MM both MN-major (weight gradients dY^T X from token-major dY and X), LAY_KM A
+// K-major and B MN-major (activation gradients dY W from W as stored).
+enum { LAY_KK = 0, LAY_MM = 1, LAY_KM = 2 };
+template <int LAY> constexpr bool kAMn = LAY == LAY_MM;
+template <int LAY> constexpr bool kBMn = LAY != LAY_KK;
+template <int LAY>
+constexpr uint32_t kIdescMajor = (kAMn<LAY> ? 1u << 15 : 0u) | (kBMn<LAY> ? 1u << 16 : 0u);
 // Descriptor of an operand tile and its advance per 16-deep MMA step (in 16-byte units):
 // K-major 32 bytes along each row, MN-major 2 KB (two groups of 8 k).
 template <bool MN>
@@ -126,27 +134,41 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t addr) {
 }
 template <bool MN>
 constexpr uint64_t kOperandStep = MN ? 128ull : 2ull;
-// The loads of `rows` rows of an operand tile from row r0, k-block kb.
+// The loads of `rows` rows of an operand tile from row r0, k from k0.
 template <bool MN>
 __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                             int kb, int r0, int rows) {
+                                             int k0, int r0, int rows) {
   if constexpr (!MN) {
-    tma_load_2d(dst, map, bar, kb * BK, r0);
+    tma_load_2d(dst, map, bar, k0, r0);
   } else {
-    for (int j = 0; j < rows / 64; ++j)
-      tma_load_2d(dst + j * MN_BOX_BYTES, map, bar, r0 + 64 * j, kb * BK);
+    tma_load_3d(dst, map, bar, 0, k0, r0 / 64);
   }
 }
 // The same for a CTA of a pair, the bytes counted on a barrier of either CTA.
 template <bool MN>
 __device__ __forceinline__ void load_operand_pair(uint32_t dst, const CUtensorMap* map,
-                                                  uint32_t bar, int kb, int r0, int rows) {
+                                                  uint32_t bar, int k0, int r0, int rows) {
   if constexpr (!MN) {
-    tma_load_2d_pair(dst, map, bar, kb * BK, r0);
+    tma_load_2d_pair(dst, map, bar, k0, r0);
   } else {
-    for (int j = 0; j < rows / 64; ++j)
-      tma_load_2d_pair(dst + j * MN_BOX_BYTES, map, bar, r0 + 64 * j, kb * BK);
+    tma_load_3d_pair(dst, map, bar, 0, k0, r0 / 64);
   }
+}
+// An MN-major B stacked along K from up to three maps: the map holding k-block kb and
+// the block's first k inside it.
+__device__ __forceinline__ const CUtensorMap* b_map_at_k(const TcArgs& a, const CUtensorMap* m0,
+                                                         const CUtensorMap* m1,
+                                                         const CUtensorMap* m2, int kb, int& k0) {
+  k0 = kb * BK;
+  if (k0 >= a.k_split2) {
+    k0 -= a.k_split2;
+    return m2;
+  }
+  if (k0 >= a.k_split1) {
+    k0 -= a.k_split1;
+    return m1;
+  }
+  return m0;
 }
 
 __device__ __forceinline__ void tile_coords(const TcArgs& a, int tiles_m, int tile, int& m_blk,
@@ -760,7 +782,7 @@ __device__ __forceinline__ bool epilogue_tile(const TcArgs& a, int M, int wrow0,
   return true;
 }
 
-template <int BN, int MODE, bool GATHER = false, bool MN = false>
+template <int BN, int MODE, bool GATHER = false, int LAY = LAY_KK>
 __global__ void __launch_bounds__(NUM_THREADS + (GATHER ? 32 * XF_WARPS : 0), 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
@@ -889,21 +911,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint32_t ph = (uint32_t)(it / C::STAGES) & 1u;
           if (!mbar_wait(EMPTY(s), ph ^ 1u, abort_flag, args.status)) break;
           mbar_arrive_expect_tx(FULL(s), C::STAGE_BYTES);
-          load_operand<MN>(sA + s * C::A_BYTES, &tmA, FULL(s), kb, m0, BM);
+          load_operand<kAMn<LAY>>(sA + s * C::A_BYTES, &tmA, FULL(s), kb * BK, m0, BM);
           if (MODE == EPI_SWIGLU) {
             const int h0 = n_blk * (BN / 2);
             tma_load_2d(sB + s * C::B_BYTES, &tmB0, FULL(s), kb * BK, h0);
             tma_load_2d(sB + s * C::B_BYTES + (BN / 2) * 128, &tmB1, FULL(s), kb * BK, h0);
           } else {
-            load_operand<MN>(sB + s * C::B_BYTES, mp, FULL(s), kb, brow, BN);
+            int k0 = kb * BK;
+            const CUtensorMap* bm = mp;
+            if constexpr (kBMn<LAY>) bm = b_map_at_k(args, &tmB0, &tmB1, &tmB2, kb, k0);
+            load_operand<kBMn<LAY>>(sB + s * C::B_BYTES, bm, FULL(s), k0, brow, BN);
           }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN) | (MN ? kIdescMajorMN : 0u);
-      constexpr uint64_t step = kOperandStep<MN>;
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN) | kIdescMajor<LAY>;
+      constexpr uint64_t astep = kOperandStep<kAMn<LAY>>, bstep = kOperandStep<kBMn<LAY>>;
       int it = 0;
       Work w;
       for (int lt = 0; work_at(args, ext, nk, lt, w) && !*abort_flag; ++lt) {
@@ -922,11 +947,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             break;
           }
           tc_fence_after();
-          const uint64_t ad = operand_desc<MN>(sA + s * C::A_BYTES);
-          const uint64_t bd = operand_desc<MN>(sB + s * C::B_BYTES);
+          const uint64_t ad = operand_desc<kAMn<LAY>>(sA + s * C::A_BYTES);
+          const uint64_t bd = operand_desc<kBMn<LAY>>(sB + s * C::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16(d_tmem, ad + step * k, bd + step * k, idesc, (kb != kb0 || k) ? 1u : 0u);
+            mma_bf16(d_tmem, ad + astep * k, bd + bstep * k, idesc, (kb != kb0 || k) ? 1u : 0u);
           mma_commit(EMPTY(s));
         }
         if (!ok) break;
@@ -1117,7 +1142,7 @@ int band2_rows(int K) {
 
 // STG: the o-projection's / down projection's epilogue inputs are staged in shared
 // memory by one more warp (the loader), see EpiStage.
-template <int BN, int MODE, bool STG = false, bool MN = false>
+template <int BN, int MODE, bool STG = false, int LAY = LAY_KK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS + (STG ? 32 : 0), 1)
 gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                 const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
@@ -1211,15 +1236,18 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
           if (!mbar_wait_cluster(EMPTY(s), ph ^ 1u, abort_flag, args.status)) break;
           const uint32_t full0 = mapa_shared(FULL(s), 0);
           if (rank == 0) mbar_arrive_expect_tx(FULL(s), 2 * C::STAGE_BYTES);
-          load_operand_pair<MN>(sA + s * C::A_BYTES, &tmA, full0, kb, m0, BM);
-          load_operand_pair<MN>(sB + s * C::B_BYTES, mp, full0, kb, brow, BN / 2);
+          load_operand_pair<kAMn<LAY>>(sA + s * C::A_BYTES, &tmA, full0, kb * BK, m0, BM);
+          int k0 = kb * BK;
+          const CUtensorMap* bm = mp;
+          if constexpr (kBMn<LAY>) bm = b_map_at_k(args, &tmB0, &tmB1, &tmB2, kb, k0);
+          load_operand_pair<kBMn<LAY>>(sB + s * C::B_BYTES, bm, full0, k0, brow, BN / 2);
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN) | (MN ? kIdescMajorMN : 0u);
-      constexpr uint64_t step = kOperandStep<MN>;
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, BN) | kIdescMajor<LAY>;
+      constexpr uint64_t astep = kOperandStep<kAMn<LAY>>, bstep = kOperandStep<kBMn<LAY>>;
       int it = 0, lt = 0;
       for (int tile = pair; tile < args.tiles && !*abort_flag; tile += npairs, ++lt) {
         const int acc = lt & 1;
@@ -1236,11 +1264,11 @@ gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             break;
           }
           tc_fence_after();
-          const uint64_t ad = operand_desc<MN>(sA + s * C::A_BYTES);
-          const uint64_t bd = operand_desc<MN>(sB + s * C::B_BYTES);
+          const uint64_t ad = operand_desc<kAMn<LAY>>(sA + s * C::A_BYTES);
+          const uint64_t bd = operand_desc<kBMn<LAY>>(sB + s * C::B_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16_pair(d_tmem, ad + step * k, bd + step * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            mma_bf16_pair(d_tmem, ad + astep * k, bd + bstep * k, idesc, (kb | k) != 0 ? 1u : 0u);
           mma_commit_pair(EMPTY(s));
         }
         if (!ok) break;
@@ -1347,6 +1375,17 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int
   return tma_map_bf16(m, base, 2, dims, strides, box);
 }
 
+// 3-D bf16 tensor map over a row-major [rows, mn] matrix (mn a multiple of 64) read as
+// (64 columns, row, 64-column chunk): a box of 64 rows x `chunks` chunks lands as
+// `chunks` consecutive 64 x 64 swizzled tiles, the MN-major operand layout.
+bool make_map_mn(CUtensorMap* m, const void* base, int64_t mn, int64_t rows, int64_t ld,
+                 int chunks) {
+  const int64_t dims[3] = {64, rows, mn / 64};
+  const int64_t strides[2] = {ld * 2, 128};
+  const int box[3] = {64, BK, chunks};
+  return tma_map_bf16(m, base, 3, dims, strides, box);
+}
+
 int g_sms = 0;
 int sm_count() {
   if (!g_sms) {
@@ -1372,8 +1411,8 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
   a.g_eps = p.gather_eps;
   if (p.gather_idx) {   // the stream's rows, one-row boxes for gather4
     if (!make_map(&mA, p.A, p.K, p.gather_rows, p.lda, 1)) return false;
-  } else if (p.a_mn) {  // [K, M]: 64 x 64 boxes
-    if (!make_map(&mA, p.A, p.M, p.K, p.lda, BK)) return false;
+  } else if (p.a_mn) {  // [K, M]: a CTA's BM rows, 64 x 64 tiles, in one load
+    if (!make_map_mn(&mA, p.A, p.M, p.K, p.lda, BM / 64)) return false;
   } else if (!make_map(&mA, p.A, p.K, p.M, p.lda, BM)) {
     return false;
   }
@@ -1391,6 +1430,8 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
   a.sk_flag = nullptr;
   a.n_split1 = INT_MAX;
   a.n_split2 = INT_MAX;
+  a.k_split1 = INT_MAX;
+  a.k_split2 = INT_MAX;
   // 32-byte epilogue accesses need every row segment the epilogue touches aligned
   auto seg_ok = [](const void* base, int64_t row_bytes) {
     return ((uintptr_t)base & 31) == 0 && row_bytes % 32 == 0;
@@ -1417,17 +1458,27 @@ bool setup(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, int tile_m, 
     tiles_n = (p.N + BN / 2 - 1) / (BN / 2);
   } else {
     const int rows0 = p.nB > 1 ? p.split[0] : (p.b_rows > 0 ? p.b_rows : p.N);
-    if (p.b_mn) {   // [K, N]: 64 x 64 boxes
-      if (!make_map(&mB0, p.B[0], rows0, p.K, p.ldb, BK)) return false;
+    if (p.b_mn) {   // [K, N] in up to three parts stacked along K: b_box / 64 tiles a load
+      const int k1 = p.nB > 1 ? p.split[0] : p.K;
+      const int k2 = p.nB > 2 ? p.split[1] : p.K;
+      if (!make_map_mn(&mB0, p.B[0], p.N, k1, p.ldb, b_box / 64)) return false;
+      if (p.nB > 1) {
+        a.k_split1 = k1;
+        if (!make_map_mn(&mB1, p.B[1], p.N, k2 - k1, p.ldb, b_box / 64)) return false;
+      }
+      if (p.nB > 2) {
+        a.k_split2 = k2;
+        if (!make_map_mn(&mB2, p.B[2], p.N, p.K - k2, p.ldb, b_box / 64)) return false;
+      }
     } else if (!make_map(&mB0, p.B[0], p.K, rows0, p.ldb, b_box)) {
       return false;
     }
-    if (p.nB > 1) {
+    if (p.nB > 1 && !p.b_mn) {
       a.n_split1 = p.split[0];
       const int rows1 = (p.nB > 2 ? p.split[1] : p.N) - p.split[0];
       if (!make_map(&mB1, p.B[1], p.K, rows1, p.ldb, b_box)) return false;
     }
-    if (p.nB > 2) {
+    if (p.nB > 2 && !p.b_mn) {
       a.n_split2 = p.split[1];
       if (!make_map(&mB2, p.B[2], p.K, p.N - p.split[1], p.ldb, b_box)) return false;
     }
@@ -1497,7 +1548,9 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, b
   } else {
     switch (e.kind) {
       case EPI_STORE:
-        k = p.a_mn ? gemm_tc_kernel<BN, EPI_STORE, false, true> : gemm_tc_kernel<BN, EPI_STORE>;
+        k = p.a_mn   ? gemm_tc_kernel<BN, EPI_STORE, false, LAY_MM>
+            : p.b_mn ? gemm_tc_kernel<BN, EPI_STORE, false, LAY_KM>
+                     : gemm_tc_kernel<BN, EPI_STORE>;
         break;
       case EPI_OPROJ: k = gemm_tc_kernel<BN, EPI_OPROJ>; break;
       case EPI_SWIGLU: k = gemm_tc_kernel<BN, EPI_SWIGLU>; break;
@@ -1506,8 +1559,8 @@ cudaError_t launch_bn(const Ctx& c, const GemmTcProblem& p, const Epilogue& e, b
     }
   }
   if (!k) return cudaErrorInvalidValue;
-  static bool attr_set[2][5] = {};   // [MN-major][epilogue]: one entry per kernel
-  const int mn = p.a_mn ? 1 : 0;
+  static bool attr_set[3][5] = {};   // [layout][epilogue]: one entry per kernel
+  const int mn = p.a_mn ? LAY_MM : p.b_mn ? LAY_KM : LAY_KK;
   if (!attr_set[mn][e.kind]) {
     cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
     if (err != cudaSuccess) return err;
@@ -1571,9 +1624,11 @@ cudaError_t launch_bn2(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) 
   switch (e.kind) {
     case EPI_STORE:
       if constexpr (BN == 256) {   // MN-major B halves need whole 64-row boxes
-        k = p.a_mn ? gemm_tc2_kernel<BN, EPI_STORE, false, true> : gemm_tc2_kernel<BN, EPI_STORE>;
+        k = p.a_mn   ? gemm_tc2_kernel<BN, EPI_STORE, false, LAY_MM>
+            : p.b_mn ? gemm_tc2_kernel<BN, EPI_STORE, false, LAY_KM>
+                     : gemm_tc2_kernel<BN, EPI_STORE>;
       } else {
-        if (p.a_mn) return cudaErrorInvalidValue;
+        if (p.b_mn) return cudaErrorInvalidValue;
         k = gemm_tc2_kernel<BN, EPI_STORE>;
       }
       smem = Cfg2<BN>::SMEM;
@@ -1608,8 +1663,8 @@ cudaError_t launch_bn2(const Ctx& c, const GemmTcProblem& p, const Epilogue& e) 
       break;
     default: return cudaErrorInvalidValue;
   }
-  static bool attr_set[2][2][4] = {};   // [MN-major][staged inputs][epilogue]: per kernel
-  const int mn = p.a_mn ? 1 : 0;
+  static bool attr_set[3][2][4] = {};   // [layout][staged inputs][epilogue]: per kernel
+  const int mn = p.a_mn ? LAY_MM : p.b_mn ? LAY_KM : LAY_KK;
   if (!attr_set[mn][stg][e.kind]) {
     cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess) return err;
@@ -1626,6 +1681,7 @@ bool bn_ok(const GemmTcProblem& p, const Epilogue& e, int bn) {
   // Router logits: 32-wide tiles only, so that a logit's arithmetic never depends on
   // how many router vectors share its launch.
   if (e.kind == EPI_ROUTER) return bn == 32 && p.N <= 32 && p.nB == 1;
+  if (p.b_mn) return true;   // its B parts are stacked along K, not N
   for (int i = 1; i < p.nB; ++i)
     if (p.split[i - 1] % bn) return false;
   return true;
@@ -1641,9 +1697,15 @@ bool gemm_tc_supported(const GemmTcProblem& p, const Epilogue& e) {
        p.gather_rows <= 0 || p.lda != p.K || !p.gather_gamma ||
        ((uintptr_t)p.gather_gamma & 15)))
     return false;
-  if (p.a_mn || p.b_mn) {   // both MN-major, plain stores of one B
-    if (!p.a_mn || !p.b_mn || e.kind != EPI_STORE || p.gather_idx || p.nB != 1 ||
-        p.ksplit > 1 || p.b_rows)
+  if (p.a_mn || p.b_mn) {   // plain stores; MN-major A only with MN-major B of one part
+    if (!p.b_mn || e.kind != EPI_STORE || p.gather_idx || p.ksplit > 1 || p.b_rows ||
+        (p.a_mn && p.nB != 1))
+      return false;
+    // MN-major operands are read in 64-row chunks of whole rows
+    if (p.N % 64 || (p.a_mn && p.M % 64)) return false;
+    // parts of B stacked along K: whole 64-deep k-blocks each
+    if (p.nB > 1 && (p.split[0] % BK || p.split[0] <= 0 || p.split[0] >= p.K)) return false;
+    if (p.nB > 2 && (p.split[1] % BK || p.split[1] <= p.split[0] || p.split[1] >= p.K))
       return false;
   }
   if ((p.K % 8 && !(p.a_mn && p.b_mn)) || p.lda % 8 || p.ldb % 8) return false;
