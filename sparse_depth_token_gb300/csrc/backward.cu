@@ -11,9 +11,12 @@
 // The layer's forward is recomputed from x with the forward kernels (router, top-k,
 // gather + RMSNorm1, projections, attention), keeping the intermediates the backward
 // reads; then every step is differentiated in reverse order. Weight gradients are
-// GEMMs over the token dimension: their operands are transposed into token-contiguous
-// buffers (padded with zero tokens to a multiple of 8) so that the same K-major GEMM
-// kernels (tcgen05 for bf16, FFMA for fp32) compute them. Column sums (RMSNorm gains,
+// GEMMs over the token dimension and activation gradients GEMMs with the weights: for
+// bf16 the tcgen05 GEMM reads dY, X and W as stored (MN-major operands); otherwise (fp32
+// on the FFMA GEMM, or bf16 dimensions that are not multiples of 64 on the K-major
+// tcgen05 GEMM) they are transposed into K-contiguous buffers, the token dimension padded
+// with zero tokens to a multiple of 8.
+// Column sums (RMSNorm gains,
 // router vector) are taken in a fixed order: partial sums per row chunk, then the
 // chunks in order, so every result is deterministic.
 
