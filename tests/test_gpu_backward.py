@@ -46,7 +46,11 @@ def _check(got, ref, dtype, what):
             f"{what}: rel-L2 {rl:.2e}, max-abs/max|ref| {mr:.2e}"
 
 
-def _run(X, w: I.Workload, kind, gate, route_coef, seed, extras=None):
+def _run(X, w: I.Workload, kind, gate, route_coef, seed, extras=None, path=None):
+    """path: "as stored" -- the gradient GEMMs read dY, X and W as stored, so the only
+    transposes left are the attention backward's (at most two launches); "transposed" --
+    the weights and the activations are transposed for them (a weight launch and one
+    per weight gradient)."""
     lw = I.layer_weights(w, 0)
     lw["varsigma"] = 0.9
     theta = 0.0
@@ -79,9 +83,19 @@ def _run(X, w: I.Workload, kind, gate, route_coef, seed, extras=None):
     gd = {k: torch.full(v, float("nan"), dtype=torch.float32, device="cuda")
           for k, v in shapes.items()}
     X.reset_status(ws)
+    if path:
+        X.profile_enable(True)
+        X.profile_read()
     X.layer_bwd(dm, kind, w.K, gate, abi, xd, torch.from_numpy(bias).cuda()
                 if bias is not None else None, dyd, route_coef, dx, X.layer_grads(gd), ws)
     assert X.sync_status(ws) == X.OK
+    if path:
+        n_tr = X.profile_read().get("bwd_transpose", (0, 0.0))[0]
+        X.profile_enable(False)
+        if path == "as stored":
+            assert n_tr <= 2, f"{n_tr} transpose launches on the as-stored path"
+        else:
+            assert n_tr >= 5, f"only {n_tr} transpose launches on the transposed path"
     ref = O.layer_bwd(U_dims(w), kind, w.K, gate, oracle_layer(lw, w.dtype), I.to_f64(x, w.dtype),
                       I.to_f64(dy, w.dtype), bias=bias, route_coef=route_coef)
     _check(from_dev(dx, w.dtype), ref["dx"], w.dtype, "dx")
@@ -133,12 +147,23 @@ def test_layer_bwd_fp32_tiny(X, kind, gate, coef):
 @pytest.mark.parametrize("T,K,kind,gate,coef", [(256, 4, 1, 0, 0.0), (303, 3, 1, 1, 0.0),
                                                 (256, 8, 1, 0, 1e-1), (160, 1, 0, 0, 0.0)])
 def test_layer_bwd_bf16_tensor_core(X, T, K, kind, gate, coef):
-    """bf16, head_dim 128 (tensor-core projections and gradients): A4K8-shaped heads at a
-    reduced width, ragged row counts (n = 101: the zero-token padding of the transposed
-    operands), both gates, the Eq. 9 term, a dense layer."""
+    """bf16, head_dim 128 (tensor-core projections and gradients, the gradient GEMMs on
+    operands as stored): A4K8-shaped heads at a reduced width, ragged row counts (n = 101:
+    token rows past the count read as zero), both gates, the Eq. 9 term, a dense layer."""
     w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=T, K=K, d=256, hq=4, hkv=2, F=512, seed=31,
                                          weight_std=0.02 * np.sqrt(1536 / 256))
-    _run(X, w, kind, gate, coef, seed=40 + T + K)
+    _run(X, w, kind, gate, coef, seed=40 + T + K, path="as stored")
+
+
+@pytest.mark.parametrize("T,K,kind", [(256, 4, 1), (303, 3, 1), (160, 1, 0)])
+def test_layer_bwd_bf16_transposed_operands(X, T, K, kind):
+    """bf16 whose model and FFN widths are not multiples of 64 (d = 288, F = 480): the
+    gradient GEMMs cannot read their operands as stored (whole 64-column chunks) and get
+    them transposed, on the K-major tensor-core GEMM; ragged row counts included."""
+    w = I.WORKLOADS["a4k8_bf16"].replace(B=2, T=T, K=K, d=288, hq=2, hkv=1, F=480, seed=43,
+                                         weight_std=0.02 * np.sqrt(1536 / 288))
+    _run(X, w, kind, X.GATE_XMOD, 0.1 if kind else 0.0, seed=170 + T + K,
+         path="transposed")
 
 
 @pytest.mark.parametrize("dtype,kind,T", [("fp32", 1, 64), ("fp32", 0, 64), ("bf16", 1, 256),
