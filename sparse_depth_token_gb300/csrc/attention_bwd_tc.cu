@@ -7,8 +7,8 @@
 //
 // One CTA per (128-query block, query head, sequence), laid out as the forward kernel:
 //   warp 0      TMA: the Q and dO tiles once, then per 64-key block the rows of K and of
-//               V and the transposed keys K^T ([head dim, keys], keys contiguous) into a
-//               three-stage ring
+//               V into a three-stage ring (the K rows serve S = Q K^T as a K-major
+//               operand and dQ += dS K as an MN-major one, so no transposed copy)
 //   warp 1      TMEM owner; one lane issues S_j = Q K_j^T and dP_j = dO V_j^T into one
 //               of two TMEM buffer pairs, and dQ += dS_j K_j once dS_j is written, with
 //               dS_j read from TMEM as the MMA's A operand
@@ -45,8 +45,7 @@ constexpr int CHUNK = 128 * 128;         // 128 rows x 64 bf16 columns, 128-byte
 constexpr int QTILE = 2 * CHUNK;         // 128 x 128
 constexpr int K_CHUNK = KB * 128;        // 64 rows x 64 columns
 constexpr int K_TILE = 2 * K_CHUNK;      // 64 keys x 128 head dims
-constexpr int KT_TILE = CHUNK;           // 128 head dims x 64 keys
-constexpr int STAGE = 2 * K_TILE + KT_TILE;
+constexpr int STAGE = 2 * K_TILE;        // K and V rows
 constexpr int DATA = 2 * QTILE + NST * STAGE;
 constexpr int SMEM = DATA + 1024;
 constexpr int TMEM_COLS = 512;           // S0, S1, dP0, dP1 (64 each), dQ (128)
@@ -80,7 +79,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmDO,
                       const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmKt, const DqArgs a) {
+                      const DqArgs a) {
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -119,7 +118,6 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmDO);
     prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmKt);
   }
   if (warp == 1) tmem_alloc(sTmem, TMEM_COLS);
   tc_fence_before();
@@ -140,7 +138,6 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       tma_load_3d(sQ + CHUNK, &tmQ, QD_FULL, h * HD + 64, q0, b);
       tma_load_3d(sDO, &tmDO, QD_FULL, h * HD, q0, b);
       tma_load_3d(sDO + CHUNK, &tmDO, QD_FULL, h * HD + 64, q0, b);
-      const int kt_row = (b * a.hkv + g) * HD;
       for (int j = 0; j < nkb; ++j) {
         const int s = j % NST;
         if (!mbar_wait(ST_EMPTY0 + 8 * s, ((uint32_t)(j / NST) & 1u) ^ 1u, abort_flag, a.status))
@@ -152,13 +149,12 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         tma_load_3d(st + K_TILE, &tmK, ST_FULL0 + 8 * s, a.v_col0 + g * HD, j * KB, b);
         tma_load_3d(st + K_TILE + K_CHUNK, &tmK, ST_FULL0 + 8 * s, a.v_col0 + g * HD + 64,
                     j * KB, b);
-        tma_load_2d(st + 2 * K_TILE, &tmKt, ST_FULL0 + 8 * s, j * KB, kt_row);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, KB);
-      constexpr uint32_t idesc_q = idesc_bf16_f32(128, HD);
+      constexpr uint32_t idesc_q = idesc_bf16_f32(128, HD) | kIdescBMajorMN;   // B = K rows
       bool ok = nkb > 0 && mbar_wait(QD_FULL, 0, abort_flag, a.status);
       int ns = 0, nd = 0;
       uint64_t t0 = global_timer_ns();
@@ -196,10 +192,12 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           if (mbar_test_wait(P_FULL0 + 8 * s, (uint32_t)(nd >> 1) & 1u)) {
             tc_fence_after();
             const uint32_t tp = tmem + (uint32_t)(s * KB);
-            const uint64_t bd = smem_desc_sw128(sSt0 + st * STAGE + 2 * K_TILE);
+            // B = K_j [64 keys, 128 head dims] as stored: MN-major, 64-dim atoms one
+            // chunk apart, 16 keys (2 KB) per MMA
+            const uint64_t bd = smem_desc_sw128_mn(sSt0 + st * STAGE, K_CHUNK);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_bf16_tmem_a(tDQ, tp + (uint32_t)(8 * k), bd + 2ull * k, idesc_q,
+              mma_bf16_tmem_a(tDQ, tp + (uint32_t)(8 * k), bd + 128ull * k, idesc_q,
                               (nd | k) != 0 ? 1u : 0u);
             mma_commit(P_EMPTY0 + 8 * s);
             mma_commit(ST_EMPTY0 + 8 * st);
@@ -331,8 +329,8 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 // 64-query blocks from the one holding the first query positioned at or after the key
 // block's first key:
 //   warp 0      TMA: the K and V tiles (rows) once, then per query block the rows of Q
-//               and dO and their transposes Q^T, dO^T ([head dim, queries]) into a
-//               two-stage ring
+//               and dO into a two-stage ring (K-major operands of S^T and dP^T, MN-major
+//               ones of dK and dV, so no transposed copies)
 //   warp 1      one lane issues S^T = K Q^T and dP^T = V dO^T (keys in the TMEM lanes)
 //               into two buffer pairs, then dV += P^T dO and dK += dS^T Q with P^T and
 //               dS^T read from TMEM
@@ -344,9 +342,8 @@ constexpr int QBK = 64;                   // queries per block
 constexpr int KV_TILE = 2 * CHUNK;        // 128 keys x 128 head dims
 constexpr int Q_CHUNK = QBK * 128;        // 64 rows x 64 columns
 constexpr int Q_TILE = 2 * Q_CHUNK;       // 64 queries x 128 head dims
-constexpr int QT_TILE = CHUNK;            // 128 head dims x 64 queries
 constexpr int KST2 = 2;                   // stages of the query ring
-constexpr int QSTAGE = 2 * Q_TILE + 2 * QT_TILE;   // Q, dO, Q^T, dO^T
+constexpr int QSTAGE = 2 * Q_TILE;        // Q, dO
 constexpr int KV_DATA = 2 * KV_TILE + KST2 * QSTAGE;
 constexpr int KV_SMEM = KV_DATA + 1024;
 static_assert((1 + 2 * KST2 + 8) * 8 + 16 <= 256, "barrier block overflows");
@@ -373,9 +370,7 @@ struct DkvArgs {
 __global__ void __launch_bounds__(THREADS, 1)
 attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
                        const __grid_constant__ CUtensorMap tmQ,
-                       const __grid_constant__ CUtensorMap tmDO,
-                       const __grid_constant__ CUtensorMap tmQt,
-                       const __grid_constant__ CUtensorMap tmDOt, const DkvArgs a) {
+                       const __grid_constant__ CUtensorMap tmDO, const DkvArgs a) {
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -418,8 +413,6 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
     prefetch_tensormap(&tmKV);
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmDO);
-    prefetch_tensormap(&tmQt);
-    prefetch_tensormap(&tmDOt);
   }
   if (warp == 1) tmem_alloc(sTmem, TMEM_COLS);
   tc_fence_before();
@@ -443,20 +436,18 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
                        a.status))
           break;
         const uint32_t st = sSt0 + s * QSTAGE;
-        const int trow = (b * a.hq + h) * HD;
         mbar_arrive_expect_tx(ST_FULL0 + 8 * s, QSTAGE);
         tma_load_3d(st, &tmQ, ST_FULL0 + 8 * s, h * HD, q0, b);
         tma_load_3d(st + Q_CHUNK, &tmQ, ST_FULL0 + 8 * s, h * HD + 64, q0, b);
         tma_load_3d(st + Q_TILE, &tmDO, ST_FULL0 + 8 * s, h * HD, q0, b);
         tma_load_3d(st + Q_TILE + Q_CHUNK, &tmDO, ST_FULL0 + 8 * s, h * HD + 64, q0, b);
-        tma_load_2d(st + 2 * Q_TILE, &tmQt, ST_FULL0 + 8 * s, q0, trow);
-        tma_load_2d(st + 2 * Q_TILE + QT_TILE, &tmDOt, ST_FULL0 + 8 * s, q0, trow);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, QBK);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD);
+      // dV += P^T dO and dK += dS^T Q: B = the dO / Q rows as stored, MN-major
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, HD) | kIdescBMajorMN;
       bool ok = items > 0 && mbar_wait(KV_FULL, 0, abort_flag, a.status);
       int ns = 0, nd = 0;
       uint64_t t0 = global_timer_ns();
@@ -496,13 +487,15 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
             const uint32_t stg = sSt0 + st * QSTAGE;
             const uint32_t tp = tmem + (uint32_t)(s * QBK);
             const uint32_t tds = tmem + 128u + (uint32_t)(s * QBK);
-            const uint64_t bqt = smem_desc_sw128(stg + 2 * Q_TILE);
-            const uint64_t bot = smem_desc_sw128(stg + 2 * Q_TILE + QT_TILE);
+            // Q and dO [64 queries, 128 head dims]: 64-dim atoms one chunk apart, 16
+            // queries (2 KB) per MMA
+            const uint64_t bq = smem_desc_sw128_mn(stg, Q_CHUNK);
+            const uint64_t bo = smem_desc_sw128_mn(stg + Q_TILE, Q_CHUNK);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              mma_bf16_tmem_a(tDV, tp + (uint32_t)(8 * k), bot + 2ull * k, idesc_o,
+              mma_bf16_tmem_a(tDV, tp + (uint32_t)(8 * k), bo + 128ull * k, idesc_o,
                               (nd | k) != 0 ? 1u : 0u);
-              mma_bf16_tmem_a(tDK, tds + (uint32_t)(8 * k), bqt + 2ull * k, idesc_o,
+              mma_bf16_tmem_a(tDK, tds + (uint32_t)(8 * k), bq + 128ull * k, idesc_o,
                               (nd | k) != 0 ? 1u : 0u);
             }
             mma_commit(P_EMPTY0 + 8 * s);
@@ -650,21 +643,21 @@ attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tmKV,
 
 }  // namespace
 
-bool attn_bwd_dq_tc_supported(int hd, int ldq, int qw, int kt_ld) {
-  return hd == HD && ldq % 8 == 0 && qw % 8 == 0 && kt_ld % 8 == 0 && tma_available();
+bool attn_bwd_dq_tc_supported(int hd, int ldq, int qw) {
+  return hd == HD && ldq % 8 == 0 && qw % 8 == 0 && tma_available();
 }
 
 cudaError_t launch_attn_bwd_dq_tc_kv(const Ctx& c, int B, int n, int nk, const int32_t* qpos,
                                      int hq, int hkv, const void* q, int ldq, const void* kv,
-                                     int ldk, int k_col0, int v_col0, const void* kt, int kt_ld,
-                                     const void* o, const void* dO, const float* lse, float* Dd,
-                                     void* dq, int ldg, float* DdT, int ldS) {
+                                     int ldk, int k_col0, int v_col0, const void* o,
+                                     const void* dO, const float* lse, float* Dd, void* dq,
+                                     int ldg, float* DdT, int ldS) {
   if (B <= 0 || n <= 0) return cudaSuccess;
   const int qw = hq * HD;
-  if (!attn_bwd_dq_tc_supported(HD, ldq, qw, kt_ld) || ldk % 8 || ldg % 8 || nk <= 0 ||
+  if (!attn_bwd_dq_tc_supported(HD, ldq, qw) || ldk % 8 || ldg % 8 || nk <= 0 ||
       (!qpos && nk != n))
     return cudaErrorInvalidValue;
-  CUtensorMap mQ, mDO, mK, mKt;
+  CUtensorMap mQ, mDO, mK;
   {
     const int64_t dims[3] = {ldq, n, B};
     const int64_t strides[2] = {(int64_t)ldq * 2, (int64_t)n * ldq * 2};
@@ -682,12 +675,6 @@ cudaError_t launch_attn_bwd_dq_tc_kv(const Ctx& c, int B, int n, int nk, const i
     const int64_t strides[2] = {(int64_t)qw * 2, (int64_t)n * qw * 2};
     const int box[3] = {64, QB, 1};
     if (!tma_map_bf16(&mDO, dO, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  {
-    const int64_t dims[2] = {nk, (int64_t)B * hkv * HD};
-    const int64_t strides[1] = {(int64_t)kt_ld * 2};
-    const int box[2] = {64, HD};
-    if (!tma_map_bf16(&mKt, kt, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   DqArgs a;
   a.n = n;
@@ -718,30 +705,28 @@ cudaError_t launch_attn_bwd_dq_tc_kv(const Ctx& c, int B, int n, int nk, const i
     attr = true;
   }
   return launch_pdl(attn_bwd_dq_tc_kernel, dim3(hq, B, a.nqb), dim3(THREADS), SMEM, c.stream,
-                    mQ, mDO, mK, mKt, a);
+                    mQ, mDO, mK, a);
 }
 
 cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
-                                  int ldq, const void* kt, int kt_ld, const void* o,
-                                  const void* dO, const float* lse, float* Dd, void* dqkv,
-                                  int ldg, float* DdT, int ldS) {
+                                  int ldq, const void* o, const void* dO, const float* lse,
+                                  float* Dd, void* dqkv, int ldg, float* DdT, int ldS) {
   const int qw = hq * HD, kw = hkv * HD;
   return launch_attn_bwd_dq_tc_kv(c, B, n, n, nullptr, hq, hkv, qkv, ldq, qkv, ldq, qw, qw + kw,
-                                  kt, kt_ld, o, dO, lse, Dd, dqkv, ldg, DdT, ldS);
+                                  o, dO, lse, Dd, dqkv, ldg, DdT, ldS);
 }
 
 cudaError_t launch_attn_bwd_dkv_tc_kv(const Ctx& c, int B, int n, int nk, const int32_t* qposS,
                                       const int32_t* qstart, int hq, int hkv, const void* q,
                                       int ldq, const void* kv, int ldk, int k_col0, int v_col0,
-                                      const void* dO, const void* qt, const void* dOt, int t_ld,
-                                      const float* lseT, const float* DdT, int ldS, void* dk,
-                                      void* dv, int ldgk) {
+                                      const void* dO, const float* lseT, const float* DdT,
+                                      int ldS, void* dk, void* dv, int ldgk) {
   if (B <= 0 || n <= 0 || nk <= 0) return cudaSuccess;
   const int qw = hq * HD;
-  if (ldq % 8 || ldk % 8 || t_ld % 8 || ldgk % 8 || ldS % QBK || ldS < n || hq % hkv ||
+  if (ldq % 8 || ldk % 8 || ldgk % 8 || ldS % QBK || ldS < n || hq % hkv ||
       !tma_available() || (!qposS) != (!qstart) || (!qposS && nk != n))
     return cudaErrorInvalidValue;
-  CUtensorMap mKV, mQ, mDO, mQt, mDOt;
+  CUtensorMap mKV, mQ, mDO;
   {
     const int64_t dims[3] = {ldk, nk, B};
     const int64_t strides[2] = {(int64_t)ldk * 2, (int64_t)nk * ldk * 2};
@@ -759,13 +744,6 @@ cudaError_t launch_attn_bwd_dkv_tc_kv(const Ctx& c, int B, int n, int nk, const 
     const int64_t strides[2] = {(int64_t)qw * 2, (int64_t)n * qw * 2};
     const int box[3] = {64, QBK, 1};
     if (!tma_map_bf16(&mDO, dO, 3, dims, strides, box)) return cudaErrorInvalidValue;
-  }
-  {
-    const int64_t dims[2] = {n, (int64_t)B * hq * HD};
-    const int64_t strides[1] = {(int64_t)t_ld * 2};
-    const int box[2] = {64, HD};
-    if (!tma_map_bf16(&mQt, qt, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    if (!tma_map_bf16(&mDOt, dOt, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   DkvArgs a;
   a.n = n;
@@ -793,18 +771,16 @@ cudaError_t launch_attn_bwd_dkv_tc_kv(const Ctx& c, int B, int n, int nk, const 
     attr = true;
   }
   return launch_pdl(attn_bwd_dkv_tc_kernel, dim3(hkv, B, (nk + KVB - 1) / KVB), dim3(THREADS),
-                    KV_SMEM, c.stream, mKV, mQ, mDO, mQt, mDOt, a);
+                    KV_SMEM, c.stream, mKV, mQ, mDO, a);
 }
 
 cudaError_t launch_attn_bwd_dkv_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
-                                   int ldq, const void* dO, const void* qt, const void* dOt,
-                                   int t_ld, const float* lseT, const float* DdT, int ldS,
-                                   void* dqkv, int ldg) {
+                                   int ldq, const void* dO, const float* lseT, const float* DdT,
+                                   int ldS, void* dqkv, int ldg) {
   const int qw = hq * HD, kw = hkv * HD;
   __nv_bfloat16* g = (__nv_bfloat16*)dqkv;
   return launch_attn_bwd_dkv_tc_kv(c, B, n, n, nullptr, nullptr, hq, hkv, qkv, ldq, qkv, ldq, qw,
-                                   qw + kw, dO, qt, dOt, t_ld, lseT, DdT, ldS, g + qw, g + qw + kw,
-                                   ldg);
+                                   qw + kw, dO, lseT, DdT, ldS, g + qw, g + qw + kw, ldg);
 }
 
 }  // namespace xmod

@@ -826,7 +826,7 @@ inline int64_t round8(int64_t v) { return (v + 7) / 8 * 8; }
 struct BwLayout {
   size_t status, s, r, idx, r_sel, dr, dvs, ds, lossp, u, qkv, vt, o, a, h, v2, gu, H, f, df,
       dae, dH, dGU, dv2, dh, da, dO, lse, Dd, dqkv, du, rstd1, rstd2, tA, tB, tW, part, qkpre,
-      dgq, dgk, kt, qt, dOt, lseT, DdT, qposS, qstart, total;
+      dgq, dgk, lseT, DdT, qposS, qstart, total;
 };
 
 constexpr int kMaxChunks = 1024;   // row chunks of the column reductions
@@ -880,9 +880,6 @@ BwLayout bw_layout(const xmod_dims* dm) {
   L.qkpre = take(es * M * (qw + kw));   // q | k before the QK-norm / rotation
   L.dgq = take(4 * M * hd);
   L.dgk = take(4 * M * hd);
-  L.kt = take(es * (size_t)dm->B * dm->n_kv_heads * hd * vtl);   // keys transposed
-  L.qt = take(es * (size_t)dm->B * hq * hd * vtl);                 // queries transposed
-  L.dOt = take(es * (size_t)dm->B * hq * hd * vtl);                // dO transposed
   const size_t lds = ((size_t)dm->T + 63) / 64 * 64;
   L.lseT = take(4 * (size_t)dm->B * hq * lds);
   L.DdT = take(4 * (size_t)dm->B * hq * lds);
@@ -1193,38 +1190,26 @@ int fullkv_tail(const Ctx& c, const xmod_dims* dm, int n, const xmod_layer_weigh
   float* part = (float*)bat(ws, L.part);
 
   // ======== attention: n queries per sequence over its T keys
-  const int kt_ld = (int)round8(T), qt_ld = (int)round8(n), ldS = (n + 63) / 64 * 64;
-  const bool tc_bwd = mma && v_transposed && attn_bwd_dq_tc_supported(hd, qw, qw, kt_ld);
+  const int ldS = (n + 63) / 64 * 64;
+  const bool tc_bwd = mma && v_transposed && attn_bwd_dq_tc_supported(hd, qw, qw);
   if (tc_bwd) {   // tcgen05 (the forward wrote lse): dq, then dk and dv over every key
-    E* kt = (E*)bat(ws, L.kt);
-    E* qt = (E*)bat(ws, L.qt);
-    E* dOt = (E*)bat(ws, L.dOt);
     float* lseT = (float*)bat(ws, L.lseT);
     float* DdT = (float*)bat(ws, L.DdT);
     int32_t* qposS = (int32_t*)bat(ws, L.qposS);
     int32_t* qstart = (int32_t*)bat(ws, L.qstart);
     const int nkb = (T + kAttnBwdKvBlock - 1) / kAttnBwdKvBlock;
-    // per sequence, transposed: keys [hkv * hd, T], queries and dO [hq * hd, n], lse [hq, n]
-    BW_RUN("bwd_transpose",
-           transpose_multi(c, dt, {{kvb, 2 * kw, kt, kt_ld, T, T, kw, (int64_t)T * 2 * kw,
-                                    (int64_t)kw * kt_ld},
-                                   {qb, qw, qt, qt_ld, n, n, qw, (int64_t)n * qw,
-                                    (int64_t)qw * qt_ld},
-                                   {dO, qw, dOt, qt_ld, n, n, qw, (int64_t)n * qw,
-                                    (int64_t)qw * qt_ld}},
-                           B));
+    // the rows' lse per sequence and head, queries contiguous [hq, n]
     BW_RUN("bwd_transpose", transpose_t<float>(c, n, n, hq, bat(ws, L.lse), hq, lseT, ldS, B,
                                                (int64_t)n * hq, (int64_t)hq * ldS));
     BW_RUN("bwd_rows", launch_pdl(fullkv_qindex_kernel, dim3(B), dim3(256), 0, c.stream, n, ldS,
                                   nkb, kAttnBwdKvBlock, idx, qposS, qstart));
     BW_RUN("bwd_attention",
-           launch_attn_bwd_dq_tc_kv(c, B, n, T, idx, hq, hkv, qb, qw, kvb, 2 * kw, 0, kw, kt,
-                                    kt_ld, o, dO, (const float*)bat(ws, L.lse),
-                                    (float*)bat(ws, L.Dd), dqb, qw, DdT, ldS));
+           launch_attn_bwd_dq_tc_kv(c, B, n, T, idx, hq, hkv, qb, qw, kvb, 2 * kw, 0, kw, o, dO,
+                                    (const float*)bat(ws, L.lse), (float*)bat(ws, L.Dd), dqb, qw,
+                                    DdT, ldS));
     BW_RUN("bwd_attention",
            launch_attn_bwd_dkv_tc_kv(c, B, n, T, qposS, qstart, hq, hkv, qb, qw, kvb, 2 * kw, 0,
-                                     kw, dO, qt, dOt, qt_ld, lseT, DdT, ldS, dkv, dkv + kw,
-                                     2 * kw));
+                                     kw, dO, lseT, DdT, ldS, dkv, dkv + kw, 2 * kw));
   } else if (mma) {
     BW_RUN("bwd_attention",
            launch_attn_bwd_mma_kv(c, B, n, T, idx, hq, hkv, hd, qb, qw, kvb, 2 * kw, kvb + kw,
@@ -1753,35 +1738,22 @@ int layer_bwd_t(const Ctx& c, const xmod_dims* dm, int kind, int K, int gate,
 
   // ======== attention
   E* dqkv = (E*)bat(ws, L.dqkv);
-  const int kt_ld = (int)round8(n);
-  const bool dq_tc = mma_attn && v_transposed && attn_bwd_dq_tc_supported(hd, qkv_w, qw, kt_ld);
+  const bool dq_tc = mma_attn && v_transposed && attn_bwd_dq_tc_supported(hd, qkv_w, qw);
   if (fullkv)
     return fullkv_tail<E>(c, dm, n, w, x, idx, dx, gr, ws, L, kvb, qb, kpre, qpre, vt,
                           v_transposed, o, dO, mma_attn, dh, dx_mn);
   if (dq_tc) {   // tcgen05 (lse from the forward): dq, then dk and dv
-    E* kt = (E*)bat(ws, L.kt);
-    E* qt = (E*)bat(ws, L.qt);
-    E* dOt = (E*)bat(ws, L.dOt);
     float* lseT = (float*)bat(ws, L.lseT);
     float* DdT = (float*)bat(ws, L.DdT);
     const int ldS = (n + 63) / 64 * 64;
-    // per sequence, transposed: keys [hkv * hd, keys], queries and dO [hq * hd, queries],
-    // and the rows' lse per head [hq, queries]
-    BW_RUN("bwd_transpose",
-           transpose_multi(c, dt, {{qkv + qw, qkv_w, kt, kt_ld, n, n, kw, (int64_t)n * qkv_w,
-                                    (int64_t)kw * kt_ld},
-                                   {qkv, qkv_w, qt, kt_ld, n, n, qw, (int64_t)n * qkv_w,
-                                    (int64_t)qw * kt_ld},
-                                   {dO, qw, dOt, kt_ld, n, n, qw, (int64_t)n * qw,
-                                    (int64_t)qw * kt_ld}},
-                           B));
+    // the rows' lse per sequence and head, queries contiguous [hq, queries]
     BW_RUN("bwd_transpose", transpose_t<float>(c, n, n, hq, bat(ws, L.lse), hq, lseT, ldS, B,
                                                (int64_t)n * hq, (int64_t)hq * ldS));
-    BW_RUN("bwd_attention", launch_attn_bwd_dq_tc(c, B, n, hq, hkv, qkv, qkv_w, kt, kt_ld, o, dO,
+    BW_RUN("bwd_attention", launch_attn_bwd_dq_tc(c, B, n, hq, hkv, qkv, qkv_w, o, dO,
                                                   (const float*)bat(ws, L.lse),
                                                   (float*)bat(ws, L.Dd), dqkv, qkv_w, DdT, ldS));
-    BW_RUN("bwd_attention", launch_attn_bwd_dkv_tc(c, B, n, hq, hkv, qkv, qkv_w, dO, qt, dOt,
-                                                   kt_ld, lseT, DdT, ldS, dqkv, qkv_w));
+    BW_RUN("bwd_attention", launch_attn_bwd_dkv_tc(c, B, n, hq, hkv, qkv, qkv_w, dO, lseT, DdT,
+                                                   ldS, dqkv, qkv_w));
   } else if (mma_attn) {   // bf16: warp-level tensor-core MMA, v rows and dO in bf16
     BW_RUN("bwd_attention", launch_attn_bwd_mma(c, B, n, hq, hkv, hd, qkv, qkv_w, o, dO,
                                                 (float*)bat(ws, L.lse), (float*)bat(ws, L.Dd),

@@ -103,19 +103,10 @@ struct TcArgs {
 // load through a 3-D tensor map (64 rows, k, 64-row chunk): chunk j holds rows 64j ..
 // 64j + 63 for the 64 k of the block, one 128-byte line (64 rows) per k under the
 // 128-byte swizzle, 8 KB a chunk.
-// The MMA reads it as an MN-major operand: 64-row swizzle atoms one box apart (leading
-// byte offset) and groups of 8 k 1 KB apart (stride byte offset); a 16-deep MMA step
-// moves 2 KB along k. The instruction descriptor marks the operand MN-major.
+// The MMA reads it as an MN-major operand (smem_desc_sw128_mn: 64-row atoms one chunk
+// apart, groups of 8 k 1 KB apart), the instruction descriptor marking it MN-major.
 constexpr int MN_BOX_BYTES = 64 * BK * 2;
-__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr >> 4) & 0x3FFFu);            // start address
-  d |= (uint64_t)(MN_BOX_BYTES >> 4) << 16;          // leading byte offset: next 64 rows
-  d |= (uint64_t)(1024u >> 4) << 32;                 // stride byte offset: next 8 k
-  d |= (uint64_t)1 << 46;                            // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;                            // layout: 128-byte swizzle
-  return d;
-}
+
 // The kernels take the operand layout as a template parameter LAY, so the K-major
 // kernels' MMA-issuing loop keeps compile-time descriptors: LAY_KK both operands K-major,
 // LAY_MM both MN-major (weight gradients dY^T X from token-major dY and X), LAY_KM A
@@ -124,12 +115,13 @@ enum { LAY_KK = 0, LAY_MM = 1, LAY_KM = 2 };
 template <int LAY> constexpr bool kAMn = LAY == LAY_MM;
 template <int LAY> constexpr bool kBMn = LAY != LAY_KK;
 template <int LAY>
-constexpr uint32_t kIdescMajor = (kAMn<LAY> ? 1u << 15 : 0u) | (kBMn<LAY> ? 1u << 16 : 0u);
+constexpr uint32_t kIdescMajor =
+    (kAMn<LAY> ? kIdescAMajorMN : 0u) | (kBMn<LAY> ? kIdescBMajorMN : 0u);
 // Descriptor of an operand tile and its advance per 16-deep MMA step (in 16-byte units):
 // K-major 32 bytes along each row, MN-major 2 KB (two groups of 8 k).
 template <bool MN>
 __device__ __forceinline__ uint64_t operand_desc(uint32_t addr) {
-  if constexpr (MN) return smem_desc_sw128_mn(addr);
+  if constexpr (MN) return smem_desc_sw128_mn(addr, MN_BOX_BYTES);
   else return smem_desc_sw128(addr);
 }
 template <bool MN>

@@ -336,40 +336,38 @@ cudaError_t launch_attn_bwd_mma_kv(const Ctx& c, int B, int n, int nk, const int
                                    const void* dO, float* lse, float* Dd, void* dq, int ldgq,
                                    void* dk, void* dv, int ldgk, bool with_q = true);
 // dq of the attention backward on tcgen05 (bf16, head_dim 128): qkv rows [B*n, ldq] (q, k,
-// v columns), kt [B*hkv*128, kt_ld] the keys transposed (keys contiguous), o and dO
-// [B*n, hq*128] bf16, lse [B*n, hq] from the forward (log2 units); writes Dd [B*n, hq]
-// (<dO, o>) and dq into the q columns of dqkv [B*n, ldg].
-bool attn_bwd_dq_tc_supported(int hd, int ldq, int qw, int kt_ld);
+// v columns; the key rows serve both S = Q K^T and dQ += dS K, the latter as an MN-major
+// operand), o and dO [B*n, hq*128] bf16, lse [B*n, hq] from the forward (log2 units);
+// writes Dd [B*n, hq] (<dO, o>) and dq into the q columns of dqkv [B*n, ldg].
+bool attn_bwd_dq_tc_supported(int hd, int ldq, int qw);
 cudaError_t launch_attn_bwd_dq_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
-                                  int ldq, const void* kt, int kt_ld, const void* o,
-                                  const void* dO, const float* lse, float* Dd, void* dqkv,
-                                  int ldg, float* DdT = nullptr, int ldS = 0);
-// dk and dv on tcgen05: qt and dOt [B*hq*128, t_ld] the queries and dO transposed per
-// sequence (queries contiguous); lseT and DdT [B*hq, ldS] (ldS a multiple of 64, >= n)
-// the rows' lse and D per head; writes the k and v columns of dqkv [B*n, ldg].
+                                  int ldq, const void* o, const void* dO, const float* lse,
+                                  float* Dd, void* dqkv, int ldg, float* DdT = nullptr,
+                                  int ldS = 0);
+// dk and dv on tcgen05 (the query and dO rows read as stored); lseT and DdT [B*hq, ldS]
+// (ldS a multiple of 64, >= n) the rows' lse and D per head; writes the k and v columns
+// of dqkv [B*n, ldg].
 cudaError_t launch_attn_bwd_dkv_tc(const Ctx& c, int B, int n, int hq, int hkv, const void* qkv,
-                                   int ldq, const void* dO, const void* qt, const void* dOt,
-                                   int t_ld, const float* lseT, const float* DdT, int ldS,
-                                   void* dqkv, int ldg);
+                                   int ldq, const void* dO, const float* lseT, const float* DdT,
+                                   int ldS, void* dqkv, int ldg);
 // The general forms (Selected-Q / full-KV): n queries per sequence at ascending
 // positions over nk keys, query i seeing the keys j <= its position. q [B*n, ldq]; the
 // keys' and values' rows kv [B*nk, ldk] (KV head g's k at column k_col0 + g*128, v at
-// v_col0 + g*128); kt [B*hkv*128, kt_ld] over the nk keys. dq_tc_kv: qpos [B*n] (NULL:
+// v_col0 + g*128). dq_tc_kv: qpos [B*n] (NULL:
 // i, nk == n), dq [B*n, ldg]. dkv_tc_kv: qposS [B, ldS] the positions padded with -1 and
 // qstart [B, ceil(nk / kAttnBwdKvBlock)] the first query positioned at or after each key
 // block's first key (both NULL: the compact case), dk and dv [B*nk, ldgk].
 constexpr int kAttnBwdKvBlock = 128;   // keys per CTA of the tcgen05 dk / dv kernel
 cudaError_t launch_attn_bwd_dq_tc_kv(const Ctx& c, int B, int n, int nk, const int32_t* qpos,
                                      int hq, int hkv, const void* q, int ldq, const void* kv,
-                                     int ldk, int k_col0, int v_col0, const void* kt, int kt_ld,
-                                     const void* o, const void* dO, const float* lse, float* Dd,
-                                     void* dq, int ldg, float* DdT, int ldS);
+                                     int ldk, int k_col0, int v_col0, const void* o,
+                                     const void* dO, const float* lse, float* Dd, void* dq,
+                                     int ldg, float* DdT, int ldS);
 cudaError_t launch_attn_bwd_dkv_tc_kv(const Ctx& c, int B, int n, int nk, const int32_t* qposS,
                                       const int32_t* qstart, int hq, int hkv, const void* q,
                                       int ldq, const void* kv, int ldk, int k_col0, int v_col0,
-                                      const void* dO, const void* qt, const void* dOt, int t_ld,
-                                      const float* lseT, const float* DdT, int ldS, void* dk,
-                                      void* dv, int ldgk);
+                                      const void* dO, const float* lseT, const float* DdT,
+                                      int ldS, void* dk, void* dv, int ldgk);
 
 // Workspace bytes of run_layer_bwd for these sizes (covers a dense layer).
 size_t bwd_workspace_bytes(const xmod_dims* dm);

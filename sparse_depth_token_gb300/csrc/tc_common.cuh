@@ -177,6 +177,22 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
+// Shared-memory descriptor for an MN-major operand under the 128-byte swizzle: 64-wide
+// (MN) atoms of 8 k-rows x 128 bytes, consecutive 8-row groups along k 1 KB apart
+// (stride byte offset), consecutive 64-wide atoms along MN `atom_stride` bytes apart
+// (leading byte offset). A 16-deep MMA step along k moves 2 KB (+128 in the descriptor).
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr, uint32_t atom_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
+  d |= (uint64_t)((atom_stride >> 4) & 0x3FFFu) << 16;   // leading byte offset
+  d |= (uint64_t)(1024u >> 4) << 32;               // stride byte offset: next 8 k
+  d |= (uint64_t)1 << 46;                          // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                          // layout: 128-byte swizzle
+  return d;
+}
+// Instruction-descriptor flags marking A / B as MN-major (transposed) operands.
+constexpr uint32_t kIdescAMajorMN = 1u << 15, kIdescBMajorMN = 1u << 16;
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator, both
 // operands K-major, shape M x N (M = 128, N multiple of 16 up to 256).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {

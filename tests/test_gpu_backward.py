@@ -47,10 +47,10 @@ def _check(got, ref, dtype, what):
 
 
 def _run(X, w: I.Workload, kind, gate, route_coef, seed, extras=None, path=None):
-    """path: "as stored" -- the gradient GEMMs read dY, X and W as stored, so the only
-    transposes left are the attention backward's (at most two launches); "transposed" --
-    the weights and the activations are transposed for them (a weight launch and one
-    per weight gradient)."""
+    """path: "as stored" -- the gradient GEMMs and the attention backward read their
+    operands as stored, so the only transpose left is the rows' lse per head (at most two
+    launches); "transposed" -- the weights and the activations are transposed for the
+    gradient GEMMs (a weight launch and one per weight gradient)."""
     lw = I.layer_weights(w, 0)
     lw["varsigma"] = 0.9
     theta = 0.0
