@@ -7,7 +7,7 @@
 //
 // One CTA per (128-query block, query head, sequence), laid out as the forward kernel:
 //   warp 0      TMA: the Q and dO tiles once, then per 64-key block the rows of K and of
-//               V into a three-stage ring (the K rows serve S = Q K^T as a K-major
+//               V into a four-stage ring (the K rows serve S = Q K^T as a K-major
 //               operand and dQ += dS K as an MN-major one, so no transposed copy)
 //   warp 1      TMEM owner; one lane issues S_j = Q K_j^T and dP_j = dO V_j^T into one
 //               of two TMEM buffer pairs, and dQ += dS_j K_j once dS_j is written, with
@@ -39,7 +39,7 @@ using namespace tc;
 constexpr int QB = 128;                  // query rows per CTA
 constexpr int HD = 128;                  // head dim
 constexpr int KB = 64;                   // keys per block
-constexpr int NST = 3;                   // stages of the key ring
+constexpr int NST = 4;                   // stages of the key ring
 constexpr int THREADS = 192;
 constexpr int CHUNK = 128 * 128;         // 128 rows x 64 bf16 columns, 128-byte swizzle
 constexpr int QTILE = 2 * CHUNK;         // 128 x 128
@@ -329,7 +329,7 @@ attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 // 64-query blocks from the one holding the first query positioned at or after the key
 // block's first key:
 //   warp 0      TMA: the K and V tiles (rows) once, then per query block the rows of Q
-//               and dO into a two-stage ring (K-major operands of S^T and dP^T, MN-major
+//               and dO into a four-stage ring (K-major operands of S^T and dP^T, MN-major
 //               ones of dK and dV, so no transposed copies)
 //   warp 1      one lane issues S^T = K Q^T and dP^T = V dO^T (keys in the TMEM lanes)
 //               into two buffer pairs, then dV += P^T dO and dK += dS^T Q with P^T and
@@ -342,7 +342,7 @@ constexpr int QBK = 64;                   // queries per block
 constexpr int KV_TILE = 2 * CHUNK;        // 128 keys x 128 head dims
 constexpr int Q_CHUNK = QBK * 128;        // 64 rows x 64 columns
 constexpr int Q_TILE = 2 * Q_CHUNK;       // 64 queries x 128 head dims
-constexpr int KST2 = 2;                   // stages of the query ring
+constexpr int KST2 = 4;                   // stages of the query ring
 constexpr int QSTAGE = 2 * Q_TILE;        // Q, dO
 constexpr int KV_DATA = 2 * KV_TILE + KST2 * QSTAGE;
 constexpr int KV_SMEM = KV_DATA + 1024;
