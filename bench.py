@@ -204,9 +204,9 @@ RECORDED_TRAFFIC = {
     # the gate/up launches of one step, mean: A3K16 (96 sparse layers + 4 dense), A4K8
     # (32 sparse layers + the dense one)
     ("a3k16_bf16", 4, "xmod", "gemm_gate_up_swiglu"):
-        (140.60e6, "profiles/gemm_gate_up_dram.md"),
+        (137.35e6, "profiles/gemm_gate_up_dram.md"),
     ("a4k8_bf16", 8, "xmod", "gemm_gate_up_swiglu"):
-        (52.56e6, "profiles/gemm_gate_up_dram.md"),
+        (52.54e6, "profiles/gemm_gate_up_dram.md"),
     # the router's x read + logits write at B = 8, scaled by 8 to B = 64 (x is read once)
     ("routing_bf16", 64, "routing", "router"):
         (8 * 540.3e6, "profiles/routing_kernels_c2_microbench.md"),
